@@ -1,0 +1,391 @@
+"""ctypes front end of the fp64 oracle (``lowram_oracle.c``) -- TEST INFRASTRUCTURE ONLY.
+
+Every array is converted to fp64 exactly (bf16, fp16 and fp32 values are all representable in
+double) before it reaches the C code.  Stored quantised formats are decoded by the oracle's own
+dequantisers.  The functions below follow the method's steps in order; the docstrings name the web
+page (by title and section) each step comes from.
+
+Pages cited:
+  [ABS] "LowRAM: Low-Rank Keys and Amortised Values for Composable KV Cache Compression at
+        Test-Time" (arXiv listing), Abstract.
+  [EX]  "LowRAM Paper: Amortised Values and Low-Rank Keys for KV Compression", sections "Value
+        cache amortisation in plain language", "Asymmetric key compression with xKV",
+        "Step-by-step mental model for one decoding session".
+  [CB]  "LowRAM: predict values from keys, store only the misses", flowchart and Key points.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lowram_oracle.c")
+_SO = os.path.join(_HERE, "liblowram_oracle.so")
+
+__all__ = [
+    "build", "lib", "Dims", "f64", "round_bf16", "round_f16", "round_f32", "quant_int4_g32",
+    "dequant_int4_g32", "quant_int8_vec", "dequant_int8_vec", "rope", "rope_angles", "mlp",
+    "rebuild_keys", "predict_values", "decode", "project", "residuals", "compress_group",
+    "dense_decode", "top_n", "n_res_for", "max_threads", "store",
+]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP, no fast-math) into ``liblowram_oracle.so``."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-Wall",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("B", "T", "H_q", "H_kv", "d", "r", "m", "S", "n_res")] + [
+        ("rope_theta", ctypes.c_double), ("sm_scale", ctypes.c_double)]
+
+
+_lib = None
+_D = ctypes.POINTER(ctypes.c_double)
+_I32 = ctypes.POINTER(ctypes.c_int32)
+_U8 = ctypes.POINTER(ctypes.c_uint8)
+_I8 = ctypes.POINTER(ctypes.c_int8)
+
+
+def lib():
+    """The compiled oracle.  LOWRAM_ORACLE_LIB may name another build of the same source (the mutation
+    test points it at copies with planted mistakes)."""
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(os.environ.get("LOWRAM_ORACLE_LIB") or build())
+        i64, ci, cd = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        sig = {
+            "lro_round_bf16": (None, [i64, _D, _D]),
+            "lro_round_f32": (None, [i64, _D, _D]),
+            "lro_round_f16_scalar": (cd, [cd]),
+            "lro_quant_int4_g32": (None, [i64, ci, _D, _U8, _D]),
+            "lro_dequant_int4_g32": (None, [i64, ci, _U8, _D, _D]),
+            "lro_quant_int8_vec": (None, [i64, ci, _D, _I8, _D]),
+            "lro_dequant_int8_vec": (None, [i64, ci, _I8, _D, _D]),
+            "lro_rope_angles": (None, [ci, cd, cd, _D, _D]),
+            "lro_rope": (None, [ci, cd, cd, _D, _D, ci]),
+            "lro_mlp": (None, [ci, ci, _D, _D, _D, _D, _D, _D, _D]),
+            "lro_top_n": (None, [ci, _D, ci, _I32]),
+            "lro_decode": (ci, [ctypes.POINTER(Dims), _D, _D, _I32, _D, _D, _D, _D, _D, _I32, _D,
+                                _D, _D, _D, _I32, ci]),
+            "lro_project": (ci, [ci, ci, ci, ci, ci, ci, _D, _I32, ci, cd, _D, _D, ci]),
+            "lro_residuals": (ci, [ctypes.POINTER(Dims), _D, _D, _D, _D, _D, _D, _D, _I32, _D, _D, ci]),
+            "lro_dense_decode": (ci, [ci, ci, ci, ci, ci, cd, _D, _D, _D, _D, _D, ci]),
+            "lro_rebuild_keys": (ci, [ctypes.POINTER(Dims), _D, _D, _D, ci]),
+            "lro_predict_values": (ci, [ci, ci, ci, ci, ci, _D, _D, _D, _D, _D, _D, ci]),
+            "lro_max_threads": (ci, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------------------------
+# array plumbing
+# ---------------------------------------------------------------------------------------------
+def f64(x) -> np.ndarray:
+    """Exact conversion of a torch tensor or array-like to a contiguous float64 numpy array."""
+    if x is None:
+        return None
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu", torch.float64).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _i32(x) -> np.ndarray:
+    if x is None:
+        return None
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu", torch.int32).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _p(a, ty=_D):
+    return None if a is None else a.ctypes.data_as(ty)
+
+
+def _chk(status: int, what: str):
+    if status != 0:
+        raise RuntimeError(f"oracle {what} failed with status {status}")
+
+
+def max_threads() -> int:
+    return int(lib().lro_max_threads())
+
+
+# ---------------------------------------------------------------------------------------------
+# storage formats
+# ---------------------------------------------------------------------------------------------
+def round_bf16(x) -> np.ndarray:
+    """Round to bfloat16 (nearest, ties to even), returned as exactly representable fp64 values."""
+    a = f64(x)
+    y = np.empty_like(a)
+    lib().lro_round_bf16(a.size, _p(a), _p(y))
+    return y
+
+
+def round_f32(x) -> np.ndarray:
+    a = f64(x)
+    y = np.empty_like(a)
+    lib().lro_round_f32(a.size, _p(a), _p(y))
+    return y
+
+
+def round_f16(x) -> np.ndarray:
+    a = f64(x)
+    return np.vectorize(lib().lro_round_f16_scalar, otypes=[np.float64])(a) if a.size else a.copy()
+
+
+def quant_int4_g32(x):
+    """int4 codes in groups of 32 with an fp16 scale -> (packed uint8 [..., r/2], scales fp64 [..., r/32])."""
+    a = f64(x)
+    r = a.shape[-1]
+    rows = a.size // r
+    packed = np.empty(a.shape[:-1] + (r // 2,), dtype=np.uint8)
+    scales = np.empty(a.shape[:-1] + (r // 32,), dtype=np.float64)
+    lib().lro_quant_int4_g32(rows, r, _p(a), _p(packed, _U8), _p(scales))
+    return packed, scales
+
+
+def dequant_int4_g32(packed, scales) -> np.ndarray:
+    pk = np.ascontiguousarray(np.asarray(packed, dtype=np.uint8))
+    sc = f64(scales)
+    r = pk.shape[-1] * 2
+    x = np.empty(pk.shape[:-1] + (r,), dtype=np.float64)
+    lib().lro_dequant_int4_g32(pk.size // (r // 2), r, _p(pk, _U8), _p(sc), _p(x))
+    return x
+
+
+def quant_int8_vec(x):
+    """int8 codes with one fp16 scale per last-axis vector -> (codes int8, scales fp64)."""
+    a = f64(x)
+    d = a.shape[-1]
+    codes = np.empty(a.shape, dtype=np.int8)
+    scales = np.empty(a.shape[:-1], dtype=np.float64)
+    lib().lro_quant_int8_vec(a.size // d, d, _p(a), _p(codes, _I8), _p(scales))
+    return codes, scales
+
+
+def dequant_int8_vec(codes, scales) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.int8))
+    sc = f64(scales)
+    d = c.shape[-1]
+    x = np.empty(c.shape, dtype=np.float64)
+    lib().lro_dequant_int8_vec(c.size // d, d, _p(c, _I8), _p(sc), _p(x))
+    return x
+
+
+def store(x, fmt: str):
+    """Round a fp64 tensor to a storage format: 'f64' (kept) | 'f32' | 'bf16' (values) or 'int4' | 'int8'
+    (codes, scales)."""
+    if fmt == "f64":
+        return f64(x).copy()
+    if fmt == "f32":
+        return round_f32(x)
+    if fmt == "bf16":
+        return round_bf16(x)
+    if fmt == "int4":
+        return quant_int4_g32(x)
+    if fmt == "int8":
+        return quant_int8_vec(x)
+    raise ValueError(fmt)
+
+
+# ---------------------------------------------------------------------------------------------
+# single steps
+# ---------------------------------------------------------------------------------------------
+def rope_angles(d: int, theta: float, pos: float):
+    c = np.empty(d // 2)
+    s = np.empty(d // 2)
+    lib().lro_rope_angles(d, float(theta), float(pos), _p(c), _p(s))
+    return c, s
+
+
+def rope(x, pos: float, theta: float, inverse: bool = False) -> np.ndarray:
+    """Rotate one d-vector at a position (rotate-half RoPE) [EX "Asymmetric key compression with xKV"]."""
+    a = f64(x)
+    y = np.empty_like(a)
+    lib().lro_rope(a.shape[-1], float(theta), float(pos), _p(a), _p(y), int(bool(inverse)))
+    return y
+
+
+def mlp(k_pre, w1, b1, w2, b2) -> np.ndarray:
+    """One head's predictor on one pre-RoPE key: w2 . silu(w1 . k + b1) + b2 [ABS; EX "Value cache amortisation"]."""
+    k, W1, W2 = f64(k_pre), f64(w1), f64(w2)
+    B1, B2 = f64(b1), f64(b2)
+    m, d = W1.shape
+    hid = np.empty(m)
+    v = np.empty(d)
+    lib().lro_mlp(d, m, _p(W1), _p(B1), _p(W2), _p(B2), _p(k), _p(hid), _p(v))
+    return v
+
+
+def top_n(values, n: int) -> np.ndarray:
+    """The n largest values (ties to the lower index), returned as ascending indices."""
+    v = f64(values)
+    out = np.empty(n, dtype=np.int32)
+    lib().lro_top_n(v.size, _p(v), int(n), _p(out, _I32))
+    return out
+
+
+def _dims(B, T, H_q, H_kv, d, r, m, S, n_res, theta, sm_scale):
+    return Dims(int(B), int(T), int(H_q), int(H_kv), int(d), int(r), int(m), int(S), int(n_res),
+                float(theta), float(sm_scale))
+
+
+def rebuild_keys(coef, basis, H_kv: int, d: int, threads: int = 0) -> np.ndarray:
+    """Pre-RoPE keys [B, T, H_kv, d] of every token from coefficients [B, T, r] and basis [H_kv*d, r]."""
+    C, W = f64(coef), f64(basis)
+    B, T, r = C.shape
+    out = np.empty((B, T, H_kv, d))
+    D = _dims(B, T, H_kv, H_kv, d, r, 1, 0, 0, 1.0, 0.0)
+    _chk(lib().lro_rebuild_keys(ctypes.byref(D), _p(C), _p(W), _p(out), threads), "rebuild_keys")
+    return out
+
+
+def predict_values(k_pre, w1, w2, b1=None, b2=None, threads: int = 0) -> np.ndarray:
+    """Predicted values [B, T, H_kv, d] of every token from pre-RoPE keys [B, T, H_kv, d]."""
+    K, W1, W2, B1, B2 = f64(k_pre), f64(w1), f64(w2), f64(b1), f64(b2)
+    B, T, H_kv, d = K.shape
+    m = W1.shape[1]
+    out = np.empty_like(K)
+    _chk(lib().lro_predict_values(B, T, H_kv, d, m, _p(K), _p(W1), _p(B1), _p(W2), _p(B2), _p(out), threads),
+         "predict_values")
+    return out
+
+
+# ---------------------------------------------------------------------------------------------
+# the two calls
+# ---------------------------------------------------------------------------------------------
+def n_res_for(rho: float, T: int) -> int:
+    """Residual budget per (sequence, kv-head): the smallest count that keeps at least a fraction rho."""
+    return max(0, min(T, int(math.ceil(rho * T - 1e-9))))
+
+
+@dataclass
+class DecodeResult:
+    out: np.ndarray
+    lse: np.ndarray
+    key: np.ndarray
+    sel: np.ndarray
+
+
+def decode(q, coef, basis, w1, w2, *, S: int, theta: float, pos=None, b1=None, b2=None, res_idx=None,
+           res_val=None, sm_scale: float = 0.0, threads: int = 0) -> DecodeResult:
+    """One decode-step attention of one layer from the compressed cache (see ``lro_decode``).
+
+    coef must already be decoded to values (``dequant_int4_g32`` for the int4 format); res_val likewise
+    (``dequant_int8_vec``).  Shapes: q [B,H_q,d], coef [B,T,r], basis [H_kv*d,r], w1 [H_kv,m,d],
+    w2 [H_kv,d,m], res_idx [B,H_kv,n_res], res_val [B,H_kv,n_res,d], pos [B,T] or None.
+    """
+    Q, C, W, W1, W2 = f64(q), f64(coef), f64(basis), f64(w1), f64(w2)
+    B1, B2, RV = f64(b1), f64(b2), f64(res_val)
+    RI, P = _i32(res_idx), _i32(pos)
+    B, H_q, d = Q.shape
+    T, r = C.shape[1], C.shape[2]
+    H_kv, m = W1.shape[0], W1.shape[1]
+    n_res = 0 if RI is None else RI.shape[-1]
+    S_eff = min(S, T)
+    out = np.empty((B, H_q, d))
+    lse = np.empty((B, H_q))
+    key = np.empty((B, H_kv, T))
+    sel = np.empty((B, H_kv, S_eff), dtype=np.int32)
+    D = _dims(B, T, H_q, H_kv, d, r, m, S, n_res, theta, sm_scale)
+    _chk(lib().lro_decode(ctypes.byref(D), _p(Q), _p(C), _p(P, _I32), _p(W), _p(W1), _p(B1), _p(W2), _p(B2),
+                          _p(RI, _I32), _p(RV), _p(out), _p(lse), _p(key), _p(sel, _I32), threads), "decode")
+    return DecodeResult(out, lse, key, sel)
+
+
+def project(k_cat, proj, G: int, H_kv: int, d: int, *, pos=None, keys_post_rope: bool = False,
+            theta: float = 1e4, threads: int = 0) -> np.ndarray:
+    """Latent coefficients [B, T, r] = proj . (RoPE-inverted) keys, unrounded [EX "Step-by-step", step 1]."""
+    K, Pj, PS = f64(k_cat), f64(proj), _i32(pos)
+    B, T = K.shape[0], K.shape[1]
+    r = Pj.shape[0]
+    K = K.reshape(B, T, G * H_kv * d)
+    coef = np.empty((B, T, r))
+    _chk(lib().lro_project(B, T, G, H_kv, d, r, _p(K), _p(PS, _I32), int(bool(keys_post_rope)), float(theta),
+                           _p(Pj), _p(coef), threads), "project")
+    return coef
+
+
+def residuals(coef_stored, v, basis, w1, w2, n_res: int, *, b1=None, b2=None, threads: int = 0):
+    """Worst-token residuals of one layer: (res_idx [B,H_kv,n_res], res_raw [B,H_kv,n_res,d], err [B,H_kv,T])."""
+    C, V, W, W1, W2, B1, B2 = f64(coef_stored), f64(v), f64(basis), f64(w1), f64(w2), f64(b1), f64(b2)
+    B, T, r = C.shape
+    H_kv, d = V.shape[2], V.shape[3]
+    m = W1.shape[1]
+    ridx = np.empty((B, H_kv, n_res), dtype=np.int32)
+    rraw = np.empty((B, H_kv, n_res, d))
+    err = np.empty((B, H_kv, T))
+    D = _dims(B, T, H_kv, H_kv, d, r, m, 0, n_res, 1.0, 0.0)
+    _chk(lib().lro_residuals(ctypes.byref(D), _p(C), _p(V), _p(W), _p(W1), _p(B1), _p(W2), _p(B2),
+                             _p(ridx, _I32), _p(rraw), _p(err), threads), "residuals")
+    return ridx, rraw, err
+
+
+def compress_group(k_cat, vs, proj, bases, w1s, w2s, *, G: int, H_kv: int, d: int, n_res: int,
+                   coef_fmt: str = "bf16", res_fmt: str = "bf16", pos=None, keys_post_rope: bool = False,
+                   theta: float = 1e4, b1s=None, b2s=None, threads: int = 0) -> dict:
+    """The write side for one layer group, in the method's order [EX "Step-by-step mental model", step 1]:
+    project the keys onto the latent coefficients and store them (rounded or quantised); then per layer
+    rebuild the keys from the *stored* coefficients, predict values, rank tokens by error and keep the
+    worst n_res as stored residuals [ABS; CB flowchart "Residual store: worst tokens only"].
+    """
+    coef_raw = project(k_cat, proj, G, H_kv, d, pos=pos, keys_post_rope=keys_post_rope, theta=theta,
+                       threads=threads)
+    res = {"coef_raw": coef_raw}
+    if coef_fmt == "int4":
+        packed, scales = quant_int4_g32(coef_raw)
+        coef_vals = dequant_int4_g32(packed, scales)
+        res.update(coef_q=packed, coef_scale=scales)
+    else:
+        coef_vals = store(coef_raw, coef_fmt)
+    res["coef"] = coef_vals
+    layers = []
+    for li in range(G):
+        ridx, rraw, err = residuals(coef_vals, vs[li], bases[li], w1s[li], w2s[li], n_res,
+                                    b1=None if b1s is None else b1s[li], b2=None if b2s is None else b2s[li],
+                                    threads=threads)
+        entry = {"res_idx": ridx, "res_raw": rraw, "err": err}
+        if res_fmt == "int8":
+            codes, sc = quant_int8_vec(rraw)
+            entry.update(res_q=codes, res_scale=sc, res_val=dequant_int8_vec(codes, sc))
+        else:
+            entry["res_val"] = store(rraw, res_fmt)
+        layers.append(entry)
+    res["layers"] = layers
+    return res
+
+
+def dense_decode(q, k, v, *, sm_scale: float = 0.0, threads: int = 0):
+    """Plain softmax attention over explicit rotated keys and values [B, T, H_kv, d] -> (out, lse)."""
+    Q, K, V = f64(q), f64(k), f64(v)
+    B, H_q, d = Q.shape
+    T, H_kv = K.shape[1], K.shape[2]
+    out = np.empty((B, H_q, d))
+    lse = np.empty((B, H_q))
+    _chk(lib().lro_dense_decode(B, T, H_q, H_kv, d, float(sm_scale), _p(Q), _p(K), _p(V), _p(out), _p(lse),
+                                threads), "dense_decode")
+    return out, lse
