@@ -1,0 +1,510 @@
+#!/usr/bin/env python
+"""Decode-step throughput of LowRAM compressed decode attention on B300.
+
+A step is one model decode step: L sequential ``lowram_decode_attn`` calls, one per layer, each over all B
+sequences of the workload (selection keys for every stored token, exact top-S, value regeneration for the
+selected tokens, split softmax and merge).  The compressed cache (latent coefficients, bases, predictor
+weights, residual lists) is written once by ``lowram_compress`` before timing and stays resident in HBM.
+Inputs are seeded synthetic tensors shaped like the workload; nothing is read from disk.
+
+Timing: W warm-up steps, then K steps.  L2 is flushed (a 256 MB buffer is zeroed) before every layer call,
+outside the CUDA events that bracket the call, so each call reads its cache cold from HBM (consecutive
+layers of a group share the latent coefficients, which would otherwise stay in L2).  Five events per call
+on the launching stream split it into its kernels.  ``value`` = 1000 / (mean over steps of the summed call
+times).  Multi-GPU (torchrun): every rank runs its own replica of the workload (no data-path collective);
+the slowest rank's time and the sum of work give the job's throughput.
+
+    python bench.py [--steps K] [--warmup W] [--workload llama8b] [--impl lowram|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from decode_attention_19_b300 import synth  # noqa: E402
+
+METRIC = "compressed decode-attn steps/s"
+UNIT = "steps/s"
+L2_BYTES = 126 * 1024 * 1024
+NOMINAL_SM = 148
+FP32_LANES_PER_SM = 128
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["lowram", "reference"], default="lowram")
+    ap.add_argument("--workload", default="llama8b", choices=list(synth.WORKLOADS))
+    ap.add_argument("--B", type=int, default=0)
+    ap.add_argument("--T", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0, help="layers per step (default: the workload's L)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dense", action="store_true", help="also time the uncompressed-cache comparator")
+    return ap.parse_args()
+
+
+def workload(args) -> synth.Workload:
+    w = synth.WORKLOADS[args.workload]
+    kw = {}
+    if args.B:
+        kw["B"] = args.B
+    if args.T:
+        kw["T"] = args.T
+    if args.layers:
+        kw["L"] = args.layers
+    return w.with_(**kw) if kw else w
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "sm_max_mhz": 2032.0}, \
+        "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic work per call (bytes, flops) -- the roofline's numerators
+# ------------------------------------------------------------------------------------------------
+def coef_bytes_per_token(w):
+    if w.coef_fmt == "int4":
+        return w.r // 2 + 2 * (w.r // 32)
+    return w.r * (4 if w.coef_fmt == "f32" else 2)
+
+
+def algorithmic(w):
+    """Per decode call: bytes that must move (cache read once, keys written/read, outputs) and FLOPs."""
+    act = 4 if w.act == "f32" else 2
+    res_row = w.d * (4 if w.res_fmt == "f32" else 2 if w.res_fmt == "bf16" else 1) + (2 if w.res_fmt == "int8" else 0)
+    S = w.S_eff
+    bytes_ = (w.B * w.T * coef_bytes_per_token(w)                       # latent coefficients
+              + w.H_kv * w.d * w.r * act + 2 * w.H_kv * w.d * w.m * act   # basis + predictor
+              + w.B * w.H_kv * w.n_res * 4                                # residual indices
+              + w.B * w.H_kv * math.ceil(w.rho * S) * res_row             # residual rows touched (~rho of S)
+              + 2 * w.B * w.H_kv * w.T * 4                                # selection keys written + read
+              + w.B * w.H_q * w.d * (act + 4))                            # q in, out
+    f_keys = 2.0 * w.B * w.T * w.H_kv * w.d * w.r
+    f_sel = 2.0 * w.B * w.H_kv * S * w.r * w.d
+    f_mlp = 4.0 * w.B * w.H_kv * S * w.d * w.m
+    return bytes_, f_keys, f_sel, f_mlp
+
+
+def kernel_digest(paths):
+    h = hashlib.sha256()
+    for p in sorted(paths):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name, src_files):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_digest") != kernel_digest(src_files):
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.proc = None
+        self.f = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(dev).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, RuntimeError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# the compressed cache of the whole model (all layer groups), written by lowram_compress
+# ------------------------------------------------------------------------------------------------
+def build_cache(w, dev):
+    import torch.nn.functional as F
+
+    import decode_attention_19_b300 as L
+    act = torch.bfloat16 if w.act == "bf16" else torch.float32
+    fmt = {"f32": L.LOWRAM_F32, "bf16": L.LOWRAM_BF16, "int4": L.LOWRAM_INT4_G32, "int8": L.LOWRAM_INT8_VEC}
+    pos = synth.eviction_positions(w).to(dev) if w.T_nominal else None
+    groups, compress_ms = [], []
+    for gi in range(w.groups):
+        raw = synth.draw_group(w, gi, with_noise=False)
+        C = raw["coef"].to(dev)
+        gen = torch.Generator(device=dev).manual_seed(synth.sub_seed(w.seed, w.name, gi, "noise-device"))
+        keys, vals = [], []
+        for l in range(w.G):
+            K = (C.view(-1, w.r) @ raw["basis"][l].to(dev).float().T).view(w.B, w.T, w.H_kv, w.d)
+            Hh = F.silu(torch.einsum("bthd,hmd->bthm", K, raw["w1"][l].to(dev).float()))
+            V = torch.einsum("bthm,hdm->bthd", Hh, raw["w2"][l].to(dev).float())
+            V += 0.3 * torch.randn(V.shape, device=dev, generator=gen)
+            keys.append(K.to(act))
+            vals.append(V.to(act))
+            del K, Hh, V
+        kg = torch.stack(keys, dim=2).contiguous()
+        del keys
+        Wst = torch.cat([b.double() for b in raw["basis"]]).to(dev)
+        proj = torch.linalg.pinv(Wst).float().contiguous()
+        bases = [b.to(dev) for b in raw["basis"]]
+        w1s = [x.to(dev) for x in raw["w1"]]
+        w2s = [x.to(dev) for x in raw["w2"]]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        r = L.lowram_compress(kg, vals, proj, bases, w1s, w2s, n_res=w.n_res, coef_dtype=fmt[w.coef_fmt],
+                              res_dtype=fmt[w.res_fmt], pos=pos)
+        e1.record()
+        torch.cuda.synchronize()
+        compress_ms.append(e0.elapsed_time(e1))
+        del kg, vals, C
+        groups.append(dict(coef=r["coef"], coef_scale=r["coef_scale"], bases=bases, w1s=w1s, w2s=w2s,
+                           res_idx=r["res_idx"], res_val=r["res_val"],
+                           res_scale=r["res_scale"] if r["res_scale"] is not None else [None] * w.G))
+        torch.cuda.empty_cache()
+    return groups, pos, compress_ms
+
+
+def layer_args(w, groups, layer):
+    g = groups[layer // w.G]
+    l = layer % w.G
+    return dict(coef=g["coef"], coef_scale=g["coef_scale"], basis=g["bases"][l], w1=g["w1s"][l], w2=g["w2s"][l],
+                res_idx=g["res_idx"][l] if w.n_res else None, res_val=g["res_val"][l] if w.n_res else None,
+                res_scale=g["res_scale"][l] if w.n_res else None)
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle sample (cpu_baseline and the reference arm)
+# ------------------------------------------------------------------------------------------------
+def oracle_sample_inputs(w, n_seq=1):
+    """One layer call restricted to n_seq sequences, built on the CPU from the seeded draws."""
+    import oracle as O
+    ws = w.with_(B=n_seq)
+    raw = synth.draw_group(ws, 0, with_noise=False)
+    coef = raw["coef"].to(torch.bfloat16 if w.coef_fmt == "bf16" else torch.float32)
+    coef_vals = O.f64(coef)
+    if w.coef_fmt == "int4":
+        packed, sc = O.quant_int4_g32(raw["coef"])
+        coef_vals = O.dequant_int4_g32(packed, sc)
+    ridx, rval = synth.placeholder_residuals(ws, 0)
+    res_vals = O.f64(rval.to(torch.bfloat16)) if w.res_fmt != "int8" else O.dequant_int8_vec(*O.quant_int8_vec(rval))
+    pos = synth.eviction_positions(ws) if w.T_nominal else None
+    return dict(q=synth.draw_query(ws, 0), coef=coef_vals, basis=raw["basis"][0], w1=raw["w1"][0], w2=raw["w2"][0],
+                res_idx=ridx if w.n_res else None, res_val=res_vals if w.n_res else None, pos=pos)
+
+
+def time_oracle_sample(w, inp, reps):
+    import oracle as O
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        O.decode(inp["q"], inp["coef"], inp["basis"], inp["w1"], inp["w2"], S=w.S, theta=w.theta, pos=inp["pos"],
+                 res_idx=inp["res_idx"], res_val=inp["res_val"])
+        ts.append(time.perf_counter() - t0)
+    return ts
+
+
+def run_reference(args, rank):
+    """The oracle as it stands, timed on the host cores: each step is one layer call for one sequence,
+    scaled to the workload's steps/s (B sequences x L layers per step)."""
+    if rank != 0:
+        return
+    import oracle as O
+    w = workload(args)
+    inp = oracle_sample_inputs(w)
+    time_oracle_sample(w, inp, args.warmup)
+    ts = time_oracle_sample(w, inp, args.steps)
+    t_step = statistics.mean(ts) * w.B * w.L
+    v = 1.0 / t_step
+    cores = O.max_threads()
+    sample = f"one layer call of 1 of {w.B} sequences (all {w.H_kv} kv-heads, T={w.T}); x{w.B * w.L} per step"
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "layers": w.L, "S": w.S, "n_res": w.n_res},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
+# main arm
+# ------------------------------------------------------------------------------------------------
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    import decode_attention_19_b300 as L
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = workload(args)
+    pk, pk_kind = peaks()
+    groups, pos, compress_ms = build_cache(w, dev)
+    cos, sin = L.lowram_rope_table(w.d, w.theta, w.T_nominal or w.T)
+    qs = [synth.draw_query(w, l).to(dev) for l in range(w.L)]
+    shape_probe = L.decode_shape(qs[0], groups[0]["coef"], groups[0]["w1s"][0], S=w.S, n_res=w.n_res,
+                                 max_pos=cos.shape[1], res_dtype=1, coef_int4=w.coef_fmt == "int4")
+    ws = torch.zeros(L.lowram_decode_workspace_size(shape_probe), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.B, w.H_q, w.d), dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    args_l = [layer_args(w, groups, l) for l in range(w.L)]
+
+    def call(l, q=None, events=None):
+        a = args_l[l]
+        return L.lowram_decode_attn(qs[l] if q is None else q, a["coef"], a["basis"], a["w1"], a["w2"], rope_cos=cos,
+                                    rope_sin=sin, S=w.S, coef_scale=a["coef_scale"], pos=pos, res_idx=a["res_idx"],
+                                    res_val=a["res_val"], res_scale=a["res_scale"], out=out, workspace=ws,
+                                    want_lse=False, events=events)
+
+    # warm-up
+    for _ in range(args.warmup):
+        for l in range(w.L):
+            flush.zero_()
+            call(l)
+    torch.cuda.synchronize()
+    if L.lowram_get_error(ws):
+        raise RuntimeError("device check word set during warm-up")
+
+    # timed region: K steps x L calls, 5 events per call
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(w.L)] for _ in range(args.steps)]
+    for step in evs:
+        for e5 in step:
+            for e in e5:
+                e.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(dev)
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        for l in range(w.L):
+            flush.zero_()
+            call(l, events=evs[s][l])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    stage = np.zeros((args.steps, w.L, 4))
+    for s in range(args.steps):
+        for l in range(w.L):
+            e = evs[s][l]
+            for k in range(4):
+                stage[s, l, k] = e[k].elapsed_time(e[k + 1])
+    step_ms = stage.sum(axis=(1, 2))
+    ms_per_step = float(step_ms.mean())
+    if dist:
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = world * 1000.0 / ms_per_step
+    per_kernel_ms = stage.mean(axis=(0, 1))          # K1 keys, K2 select, K3 values, K4 merge
+    names = ["score", "select", "vregen", "merge"]
+    dom = int(np.argmax(per_kernel_ms))
+
+    # back-to-back (no flush) for context
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for l in range(w.L):
+        call(l)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_b2b = e0.elapsed_time(e1)
+
+    # end to end through the public API: q from pinned host memory in, out back to pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        q_host = [q.cpu().pin_memory() for q in qs]
+        out_host = [torch.empty((w.B, w.H_q, w.d), dtype=torch.float32).pin_memory() for _ in range(w.L)]
+        q_dev = torch.empty_like(qs[0])
+        st = torch.cuda.current_stream()
+        e2e_ms = []
+        for s in range(args.warmup + args.steps):
+            pairs = []
+            for l in range(w.L):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                q_dev.copy_(q_host[l], non_blocking=True)
+                call(l, q=q_dev)
+                out_host[l].copy_(out, non_blocking=True)
+                b.record()
+                pairs.append((a, b))
+            st.synchronize()
+            if s >= args.warmup:
+                e2e_ms.append(sum(a.elapsed_time(b) for a, b in pairs))
+        m = float(np.mean(e2e_ms))
+        if dist:
+            t = torch.tensor([m], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            m = float(t.item())
+        e2e = {"value": world * 1000.0 / m, "unit": UNIT,
+               "h2d_bytes_per_step": w.L * qs[0].numel() * qs[0].element_size(),
+               "d2h_bytes_per_step": w.L * out.numel() * out.element_size(), "ms_per_step": m}
+
+    # roofline of the dominant kernel
+    bytes_call, f_keys, f_sel, f_mlp = algorithmic(w)
+    src = [os.path.join(ROOT, "decode_attention_19_b300", "csrc", f) for f in
+           ("simt_decode.cu", "tc_decode.cu", "select.cu", "predict.cuh", "simt_tile.cuh", "common.cuh", "tc_common.cuh")
+           if os.path.exists(os.path.join(ROOT, "decode_attention_19_b300", "csrc", f))]
+    tc_path = L.lowram_decode_uses_tensor_cores(shape_probe)
+    k1_ms = per_kernel_ms[0]
+    if tc_path:
+        peak_tf = pk["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": f_keys / (k1_ms * 1e-3) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+                "peak_kind": f"{pk_kind} bf16 sustained"}
+    else:
+        peak_tf = NOMINAL_SM * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": f_keys / (k1_ms * 1e-3) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+                "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = "score (selection keys of every token)"
+    traffic = profiled_traffic("score_llama8b.txt", src) if w.name == "llama8b" else None
+    roof["traffic"] = traffic
+    t_bytes_us = bytes_call / (pk["hbm_gbs"] * 1e9) * 1e6
+    t_alg_us = max(t_bytes_us, (f_keys + f_sel + f_mlp) / (pk["bf16_tflops_sustained"] * 1e12) * 1e6)
+    t_lit_us = max(t_bytes_us, f_mlp / (pk["bf16_tflops_sustained"] * 1e12) * 1e6)
+    call_us = ms_per_step * 1e3 / w.L
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.act == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "T_nominal": w.T_nominal or w.T, "layers": w.L,
+                       "G": w.G, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d, "r": w.r, "m": w.m, "S": w.S,
+                       "n_res": w.n_res, "coef": w.coef_fmt, "res": w.res_fmt,
+                       "l2": "flushed before every layer call (256 MB zero fill, outside the timed events)",
+                       "parallelism": f"replicas x{world}"},
+            "tokens_heads_per_s": w.B * w.T * w.H_q / (call_us * 1e-6) * world,
+            "hbm_gbs_algorithmic": bytes_call / (call_us * 1e-6) / 1e9,
+            "roofline_call": {"t_call_us": call_us, "bytes_per_call": bytes_call,
+                              "t_bytes_us": t_bytes_us, "literal_roof_us": t_lit_us, "algorithmic_roof_us": t_alg_us,
+                              "frac_literal": t_lit_us / call_us, "frac_algorithmic": t_alg_us / call_us},
+            "per_kernel_us": {n: float(v) * 1e3 for n, v in zip(names, per_kernel_ms)},
+            "dominant_kernel": names[dom],
+            "roofline": roof,
+            "ms_per_step_no_flush": ms_b2b, "wall_ms_per_step": t_wall * 1e3 / args.steps,
+            "compress_ms_per_group": float(np.mean(compress_ms)),
+            "gpu_launches": args.steps * w.L * (4 if w.S_eff > 0 else 2),
+            "clocks": clk, "peaks": pk_kind}
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle as O
+        inp = oracle_sample_inputs(w)
+        ts = time_oracle_sample(w, inp, 3)
+        t_step = statistics.median(ts) * w.B * w.L
+        line["cpu_baseline"] = {"value": 1.0 / t_step, "unit": UNIT, "cores": O.max_threads(), "kind": "oracle",
+                                "sample": f"one layer call of 1 of {w.B} sequences (all kv-heads, T={w.T}), "
+                                          f"median of 3, x{w.B * w.L} per step"}
+    if args.dense and w.act == "bf16":
+        line["dense_comparator"] = dense_bench(w, dev, qs, flush, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def dense_bench(w, dev, qs, flush, args):
+    """Same kernel family on an uncompressed bf16 cache at the same shape (explicit rotated K and V)."""
+    import decode_attention_19_b300 as L
+    Tn = w.T_nominal or w.T
+    n_layers = min(w.L, 4)
+    g = torch.Generator(device=dev).manual_seed(7)
+    ks = [torch.randn((w.B, Tn, w.H_kv, w.d), device=dev, generator=g).to(torch.bfloat16) for _ in range(n_layers)]
+    vs = [torch.randn((w.B, Tn, w.H_kv, w.d), device=dev, generator=g).to(torch.bfloat16) for _ in range(n_layers)]
+    out = torch.empty((w.B, w.H_q, w.d), dtype=torch.float32, device=dev)
+    ws = torch.zeros(L.lowram_dense_workspace_size(w.B, Tn, w.H_q, w.H_kv, w.d), dtype=torch.uint8, device=dev)
+    ts = []
+    for it in range(args.warmup + args.steps):
+        for l in range(n_layers):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            L.lowram_dense_decode_attn(qs[l], ks[l], vs[l], out=out, workspace=ws, want_lse=False)
+            b.record()
+            if it >= args.warmup:
+                ts.append((a, b))
+    torch.cuda.synchronize()
+    t_call = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+    kv_bytes = 2 * w.B * Tn * w.H_kv * w.d * 2
+    return {"t_call_us": t_call * 1e3, "T": Tn, "kv_bytes_per_call": kv_bytes,
+            "hbm_gbs": kv_bytes / (t_call * 1e-3) / 1e9, "steps_per_s_equiv": 1000.0 / (t_call * w.L)}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,305 @@
+"""Thin ctypes binding of liblowram.so.  Argument marshalling only: every step of the path runs in the
+library's CUDA kernels; this module reads shapes and dtypes off torch tensors, allocates outputs and
+workspaces with torch, and passes raw device pointers and the current CUDA stream.
+
+The functions carry the names of the C entry points in include/lowram.h.  If the library is not
+built the first call raises (there is no other implementation to fall back to).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblowram.so")
+
+LOWRAM_F32, LOWRAM_BF16, LOWRAM_INT4_G32, LOWRAM_INT8_VEC = 0, 1, 2, 3
+CHECK_POS_RANGE, CHECK_RES_INDEX = 1, 2
+STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported", 4: "workspace", 5: "cuda",
+          6: "device check"}
+
+
+class lowram_decode_shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "T", "H_q", "H_kv", "d", "r", "m", "S", "n_res", "act_dtype",
+                                              "coef_dtype", "res_dtype", "max_pos")] + [("sm_scale", ctypes.c_float)]
+
+
+class lowram_compress_shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "T", "G", "H_kv", "d", "r", "m", "n_res", "act_dtype", "coef_dtype",
+                                              "res_dtype", "keys_post_rope", "max_pos")]
+
+
+class LowramError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"liblowram: {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -m decode_attention_19_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, sz, dbl, flt = ctypes.c_int32, ctypes.c_size_t, ctypes.c_double, ctypes.c_float
+        psz = ctypes.POINTER(ctypes.c_size_t)
+        sigs = {
+            "lowram_decode_workspace_size": [ctypes.POINTER(lowram_decode_shape), psz],
+            "lowram_decode_attn": [ctypes.POINTER(lowram_decode_shape)] + [_vp] * 18 + [_vp, sz, _vp],
+            "lowram_decode_attn_events": [ctypes.POINTER(lowram_decode_shape)] + [_vp] * 18 + [_vp, sz, _vp, _vp],
+            "lowram_rope_table": [i32, dbl, i32, _vp, _vp, _vp],
+            "lowram_compress_workspace_size": [ctypes.POINTER(lowram_compress_shape), psz],
+            "lowram_compress": [ctypes.POINTER(lowram_compress_shape)] + [_vp] * 18 + [sz, _vp],
+            "lowram_dense_workspace_size": [i32, i32, i32, i32, i32, psz],
+            "lowram_dense_decode_attn": [i32, i32, i32, i32, i32, i32, flt, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp],
+            "lowram_get_error": [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)],
+            "lowram_decode_uses_tensor_cores": [ctypes.POINTER(lowram_decode_shape), ctypes.POINTER(ctypes.c_int32)],
+            "lowram_clear_error": [_vp, _vp],
+        }
+        for name, args in sigs.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.lowram_status_string.restype = ctypes.c_char_p
+        L.lowram_status_string.argtypes = [ctypes.c_int]
+        L.lowram_last_error.restype = ctypes.c_char_p
+        L.lowram_last_error.argtypes = []
+        L.lowram_version.restype = ctypes.c_int32
+        _lib = L
+    return _lib
+
+
+def lib():
+    return _load()
+
+
+def _check(st: int):
+    if st != 0:
+        raise LowramError(st, _load().lowram_last_error().decode())
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _stream():
+    return _vp(torch.cuda.current_stream().cuda_stream)
+
+
+def _act(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LOWRAM_F32
+    if t.dtype == torch.bfloat16:
+        return LOWRAM_BF16
+    raise TypeError(f"activation dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _workspace(nbytes: int, workspace: Optional[torch.Tensor], device) -> torch.Tensor:
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace too small: {nbytes} bytes needed")
+        return workspace
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------------------------------------
+# RoPE tables
+# ------------------------------------------------------------------------------------------------
+def lowram_rope_table(d: int, theta: float, max_pos: int, device="cuda"):
+    """cos/sin tables [d/2, max_pos] float32 (frequency-major) built on the device in fp64."""
+    cos = torch.empty((d // 2, max_pos), dtype=torch.float32, device=device)
+    sin = torch.empty_like(cos)
+    _check(_load().lowram_rope_table(int(d), float(theta), int(max_pos), _p(cos), _p(sin), _stream()))
+    return cos, sin
+
+
+# ------------------------------------------------------------------------------------------------
+# decode
+# ------------------------------------------------------------------------------------------------
+def decode_shape(q, coef, w1, *, S: int, n_res: int, max_pos: int, res_dtype: int, sm_scale: float = 0.0,
+                 coef_int4: bool = False) -> lowram_decode_shape:
+    B, H_q, d = q.shape
+    T = coef.shape[1]
+    r = coef.shape[2] * 2 if coef_int4 else coef.shape[2]
+    H_kv, m = w1.shape[0], w1.shape[1]
+    act = _act(q)
+    return lowram_decode_shape(B, T, H_q, H_kv, d, r, m, int(S), int(n_res), act,
+                               LOWRAM_INT4_G32 if coef_int4 else _act(coef), int(res_dtype), int(max_pos),
+                               float(sm_scale))
+
+
+def lowram_decode_uses_tensor_cores(shape: lowram_decode_shape) -> bool:
+    y = ctypes.c_int32(0)
+    _check(_load().lowram_decode_uses_tensor_cores(ctypes.byref(shape), ctypes.byref(y)))
+    return bool(y.value)
+
+
+def lowram_decode_workspace_size(shape: lowram_decode_shape) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_load().lowram_decode_workspace_size(ctypes.byref(shape), ctypes.byref(n)))
+    return int(n.value)
+
+
+def lowram_decode_attn(q: torch.Tensor, coef: torch.Tensor, basis: torch.Tensor, w1: torch.Tensor, w2: torch.Tensor,
+                       *, rope_cos: torch.Tensor, rope_sin: torch.Tensor, S: int,
+                       coef_scale: Optional[torch.Tensor] = None, pos: Optional[torch.Tensor] = None,
+                       b1: Optional[torch.Tensor] = None, b2: Optional[torch.Tensor] = None,
+                       res_idx: Optional[torch.Tensor] = None, res_val: Optional[torch.Tensor] = None,
+                       res_scale: Optional[torch.Tensor] = None, sm_scale: float = 0.0,
+                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                       sel_out: Optional[torch.Tensor] = None, key_out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, want_lse: bool = True, events=None):
+    """Decode-step attention of one layer read from the compressed cache.  Returns (out, lse).
+
+    events: optional sequence of five recorded torch.cuda.Event objects (timing marks between the kernels,
+    see lowram_decode_attn_events).
+
+    Layouts as in include/lowram.h: q [B,H_q,d]; coef [B,T,r] (uint8 [B,T,r/2] + coef_scale fp16 [B,T,r/32] for
+    int4); basis [H_kv*d, r]; w1 [H_kv,m,d]; w2 [H_kv,d,m]; res_idx int32 [B,H_kv,n_res]; res_val [B,H_kv,n_res,d]
+    (int8 + res_scale fp16 [B,H_kv,n_res] for the int8 format); rope tables [d/2, max_pos].
+    """
+    coef_int4 = coef.dtype == torch.uint8
+    n_res = 0 if res_idx is None else int(res_idx.shape[-1])
+    if res_val is None:
+        res_dtype = _act(q)
+    elif res_val.dtype == torch.int8:
+        res_dtype = LOWRAM_INT8_VEC
+    else:
+        res_dtype = _act(res_val)
+    shape = decode_shape(q, coef, w1, S=S, n_res=n_res, max_pos=rope_cos.shape[1], res_dtype=res_dtype,
+                         sm_scale=sm_scale, coef_int4=coef_int4)
+    _dev(q, coef, basis, w1, w2, rope_cos, rope_sin, coef_scale, pos, b1, b2, res_idx, res_val, res_scale)
+    B, H_q, d = q.shape
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=dev)
+    ws = _workspace(lowram_decode_workspace_size(shape), workspace, dev)
+    args = (ctypes.byref(shape), _p(q), _p(coef), _p(coef_scale), _p(pos), _p(rope_cos), _p(rope_sin), _p(basis),
+            _p(w1), _p(w2), _p(b1), _p(b2), _p(res_idx), _p(res_val), _p(res_scale), _p(out), _p(lse), _p(sel_out),
+            _p(key_out), _p(ws), ws.numel() * ws.element_size(), _stream())
+    if events is None:
+        _check(_load().lowram_decode_attn(*args))
+    else:
+        arr = (ctypes.c_void_p * 5)(*[None if e is None else e.cuda_event for e in events])
+        _check(_load().lowram_decode_attn_events(*args, ctypes.cast(arr, _vp)))
+    return out, lse
+
+
+# ------------------------------------------------------------------------------------------------
+# compress
+# ------------------------------------------------------------------------------------------------
+def _ptr_array(ts: Optional[Sequence[Optional[torch.Tensor]]]):
+    if ts is None:
+        return None
+    arr = (ctypes.c_void_p * len(ts))(*[None if t is None else t.data_ptr() for t in ts])
+    return arr
+
+
+def lowram_compress_workspace_size(shape: lowram_compress_shape) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_load().lowram_compress_workspace_size(ctypes.byref(shape), ctypes.byref(n)))
+    return int(n.value)
+
+
+def lowram_compress(keys: torch.Tensor, values: Sequence[torch.Tensor], proj: torch.Tensor,
+                    bases: Sequence[torch.Tensor], w1s: Sequence[torch.Tensor], w2s: Sequence[torch.Tensor], *,
+                    n_res: int, coef_dtype: int, res_dtype: int, pos: Optional[torch.Tensor] = None,
+                    rope_cos: Optional[torch.Tensor] = None, rope_sin: Optional[torch.Tensor] = None,
+                    keys_post_rope: bool = False, b1s=None, b2s=None, want_err: bool = False,
+                    workspace: Optional[torch.Tensor] = None) -> dict:
+    """Write side of one layer group.  keys [B,T,G,H_kv,d]; values G x [B,T,H_kv,d]; proj [r, G*H_kv*d] float32."""
+    B, T, G, H_kv, d = keys.shape
+    r = proj.shape[0]
+    m = w1s[0].shape[1]
+    dev = keys.device
+    shape = lowram_compress_shape(B, T, G, H_kv, d, r, m, int(n_res), _act(keys), int(coef_dtype), int(res_dtype),
+                                  int(bool(keys_post_rope)), 0 if rope_cos is None else rope_cos.shape[1])
+    _dev(keys, proj, pos, rope_cos, rope_sin, *values, *bases, *w1s, *w2s)
+    if coef_dtype == LOWRAM_INT4_G32:
+        coef = torch.empty((B, T, r // 2), dtype=torch.uint8, device=dev)
+        coef_scale = torch.empty((B, T, r // 32), dtype=torch.float16, device=dev)
+    else:
+        coef = torch.empty((B, T, r), dtype=torch.float32 if coef_dtype == LOWRAM_F32 else torch.bfloat16, device=dev)
+        coef_scale = None
+    res_idx = [torch.empty((B, H_kv, n_res), dtype=torch.int32, device=dev) for _ in range(G)]
+    if res_dtype == LOWRAM_INT8_VEC:
+        res_val = [torch.empty((B, H_kv, n_res, d), dtype=torch.int8, device=dev) for _ in range(G)]
+        res_scale = [torch.empty((B, H_kv, n_res), dtype=torch.float16, device=dev) for _ in range(G)]
+    else:
+        vdt = torch.float32 if res_dtype == LOWRAM_F32 else torch.bfloat16
+        res_val = [torch.empty((B, H_kv, n_res, d), dtype=vdt, device=dev) for _ in range(G)]
+        res_scale = None
+    err = [torch.empty((B, H_kv, T), dtype=torch.float32, device=dev) for _ in range(G)] if want_err else None
+    ws = _workspace(lowram_compress_workspace_size(shape), workspace, dev)
+    arrays = {name: _ptr_array(ts) for name, ts in (("values", values), ("basis", bases), ("w1", w1s), ("w2", w2s),
+                                                   ("b1", b1s), ("b2", b2s), ("res_idx", res_idx),
+                                                   ("res_val", res_val), ("res_scale", res_scale), ("err", err))}
+    ap = {k: (None if v is None else ctypes.cast(v, _vp)) for k, v in arrays.items()}
+    _check(_load().lowram_compress(ctypes.byref(shape), _p(keys), ap["values"], _p(proj), _p(pos), _p(rope_cos),
+                                   _p(rope_sin), ap["basis"], ap["w1"], ap["w2"], ap["b1"], ap["b2"], _p(coef),
+                                   _p(coef_scale), ap["res_idx"], ap["res_val"], ap["res_scale"], ap["err"], _p(ws),
+                                   ws.numel() * ws.element_size(), _stream()))
+    return {"coef": coef, "coef_scale": coef_scale, "res_idx": res_idx, "res_val": res_val, "res_scale": res_scale,
+            "err": err, "workspace": ws}
+
+
+# ------------------------------------------------------------------------------------------------
+# dense comparator
+# ------------------------------------------------------------------------------------------------
+def lowram_dense_workspace_size(B: int, T: int, H_q: int, H_kv: int, d: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_load().lowram_dense_workspace_size(B, T, H_q, H_kv, d, ctypes.byref(n)))
+    return int(n.value)
+
+
+def lowram_dense_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, sm_scale: float = 0.0,
+                             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                             workspace: Optional[torch.Tensor] = None, want_lse: bool = True):
+    """Plain decode attention over explicit rotated K and V [B,T,H_kv,d]; q [B,H_q,d].  Returns (out, lse)."""
+    B, H_q, d = q.shape
+    T, H_kv = k.shape[1], k.shape[2]
+    _dev(q, k, v)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=dev)
+    ws = _workspace(lowram_dense_workspace_size(B, T, H_q, H_kv, d), workspace, dev)
+    _check(_load().lowram_dense_decode_attn(B, T, H_q, H_kv, d, _act(q), float(sm_scale), _p(q), _p(k), _p(v),
+                                            _p(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream()))
+    return out, lse
+
+
+# ------------------------------------------------------------------------------------------------
+# status
+# ------------------------------------------------------------------------------------------------
+def lowram_get_error(workspace: torch.Tensor) -> int:
+    """Device check word of a workspace (LOWRAM_CHECK_* bits), cleared afterwards.  Synchronises the stream."""
+    w = ctypes.c_uint32(0)
+    st = _load().lowram_get_error(_p(workspace), _stream(), ctypes.byref(w))
+    if st not in (0, 6):
+        _check(st)
+    return int(w.value)
+
+
+def lowram_clear_error(workspace: torch.Tensor):
+    _check(_load().lowram_clear_error(_p(workspace), _stream()))
+
+
+def lowram_version() -> int:
+    return int(_load().lowram_version())

@@ -1,0 +1,97 @@
+// kernels.h -- host launchers of liblowram.so's kernels (internal; the public ABI is include/lowram.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/lowram.h"
+
+namespace lowram {
+
+// Everything a decode call needs, already validated by the ABI layer.
+struct DecodeArgs {
+    lowram_decode_shape s;
+    int g, S_eff;
+    float scale;
+    const void* q;
+    const void* coef;
+    const void* coef_scale;
+    const int32_t* pos;
+    const float* rope_cos;
+    const float* rope_sin;
+    const void* basis;
+    const void* w1;
+    const void* w2;
+    const float* b1;
+    const float* b2;
+    const int32_t* res_idx;
+    const void* res_val;
+    const void* res_scale;
+    float* out;
+    float* lse;
+    // scratch (carved from the workspace, or the caller's test hooks)
+    float* key;
+    int32_t* sel;
+    float* partial;
+    int n_chunks;        // partial chunks per (b, q-head)
+    uint32_t* check;
+    void* scratch;       // extra scratch for the tensor-core kernels
+    size_t scratch_bytes;
+};
+
+// Chunk (selected tokens per vregen CTA) used by each path.
+constexpr int kSimtChunk = 32;
+
+cudaError_t launch_rope_table(int d, double theta, int max_pos, float* cos_out, float* sin_out, cudaStream_t st);
+
+// K1: selection keys of every token (CUDA-core path; any dtype)
+cudaError_t launch_score_simt(const DecodeArgs& a, cudaStream_t st);
+// K2: exact top-n per problem row (values [P][T] -> ascending indices [P][n])
+cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, int32_t* out, cudaStream_t st);
+size_t select_scratch_bytes(int P, int T, int n_keep);
+// K3: value regeneration + softmax partials for selected chunks of 32 (CUDA-core path)
+cudaError_t launch_vregen_simt(const DecodeArgs& a, cudaStream_t st);
+// K4: merge partials -> out, lse
+cudaError_t launch_merge(int B, int H_q, int n_chunks, int d, const float* partial, float* out, float* lse,
+                         cudaStream_t st);
+
+// Tensor-core path (bf16 / int4 caches).  Returns cudaErrorNotSupported when the shape is not covered.
+bool tc_supported(const DecodeArgs& a);
+size_t tc_scratch_bytes(const lowram_decode_shape& s);
+cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st);
+
+// Write side
+struct CompressArgs {
+    lowram_compress_shape s;
+    const void* keys;
+    const void* values[16];
+    const float* proj;
+    const int32_t* pos;
+    const float* rope_cos;
+    const float* rope_sin;
+    const void* basis[16];
+    const void* w1[16];
+    const void* w2[16];
+    const float* b1[16];
+    const float* b2[16];
+    void* coef_out;
+    void* coef_scale_out;
+    int32_t* res_idx_out[16];
+    void* res_val_out[16];
+    void* res_scale_out[16];
+    float* err_out[16];
+    float* err_scratch;
+    uint32_t* check;
+};
+cudaError_t launch_project(const CompressArgs& a, cudaStream_t st);
+cudaError_t launch_predict_err(const CompressArgs& a, int layer, float* err, cudaStream_t st);
+cudaError_t launch_residual_rows(const CompressArgs& a, int layer, cudaStream_t st);
+
+// Comparator
+int dense_splits(int B, int T, int H_kv);
+cudaError_t launch_dense(int B, int T, int H_q, int H_kv, int d, int dtype, float scale, const void* q, const void* k,
+                         const void* v, float* partial, int n_split, cudaStream_t st);
+
+}  // namespace lowram

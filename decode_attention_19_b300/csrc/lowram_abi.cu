@@ -1,0 +1,382 @@
+// lowram_abi.cu -- the C ABI of liblowram.so: argument and alignment checks, workspace carving,
+// and the launch sequence of each call.  See include/lowram.h for the contract of every entry point.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace lowram;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+lowram_status fail(lowram_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+lowram_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(LOWRAM_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+constexpr size_t kHeader = 256;
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool is_act(int dt) { return dt == LOWRAM_F32 || dt == LOWRAM_BF16; }
+
+// ------------------------------------------------------------------------------------------------
+// decode
+// ------------------------------------------------------------------------------------------------
+lowram_status check_decode_shape(const lowram_decode_shape* s) {
+    if (!s) return fail(LOWRAM_ERR_INVALID_ARG, "shape is NULL");
+    if (s->B < 0 || s->T < 0 || s->S < 0 || s->n_res < 0)
+        return fail(LOWRAM_ERR_INVALID_ARG, "negative size (B=%d T=%d S=%d n_res=%d)", s->B, s->T, s->S, s->n_res);
+    if (s->H_kv < 1 || s->H_q < 1 || s->H_q % s->H_kv != 0)
+        return fail(LOWRAM_ERR_INVALID_ARG, "H_q=%d must be a positive multiple of H_kv=%d", s->H_q, s->H_kv);
+    if (s->H_q / s->H_kv > 8) return fail(LOWRAM_ERR_UNSUPPORTED, "H_q/H_kv=%d > 8", s->H_q / s->H_kv);
+    if (s->d != 64 && s->d != 128) return fail(LOWRAM_ERR_UNSUPPORTED, "d=%d (64 or 128 supported)", s->d);
+    if (s->r < 32 || s->r % 32 != 0 || s->r > 1024)
+        return fail(LOWRAM_ERR_UNSUPPORTED, "r=%d (multiple of 32, <= 1024)", s->r);
+    if (s->m < 32 || s->m % 32 != 0 || s->m > 256)
+        return fail(LOWRAM_ERR_UNSUPPORTED, "m=%d (multiple of 32, <= 256)", s->m);
+    if (s->n_res > s->T) return fail(LOWRAM_ERR_INVALID_ARG, "n_res=%d > T=%d", s->n_res, s->T);
+    if (!is_act(s->act_dtype)) return fail(LOWRAM_ERR_INVALID_ARG, "act_dtype=%d", s->act_dtype);
+    if (s->coef_dtype == LOWRAM_F32 || s->coef_dtype == LOWRAM_BF16) {
+        if (s->coef_dtype != s->act_dtype)
+            return fail(LOWRAM_ERR_UNSUPPORTED, "coef_dtype %d must equal act_dtype %d", s->coef_dtype, s->act_dtype);
+    } else if (s->coef_dtype != LOWRAM_INT4_G32) {
+        return fail(LOWRAM_ERR_INVALID_ARG, "coef_dtype=%d", s->coef_dtype);
+    }
+    if (s->res_dtype != LOWRAM_F32 && s->res_dtype != LOWRAM_BF16 && s->res_dtype != LOWRAM_INT8_VEC)
+        return fail(LOWRAM_ERR_INVALID_ARG, "res_dtype=%d", s->res_dtype);
+    if (s->T > 0 && s->max_pos < 1) return fail(LOWRAM_ERR_INVALID_ARG, "max_pos=%d", s->max_pos);
+    if ((int64_t)s->B * s->T * s->r > ((int64_t)1 << 40)) return fail(LOWRAM_ERR_UNSUPPORTED, "cache too large");
+    return LOWRAM_OK;
+}
+
+struct DecodeLayout {
+    bool tc;
+    int chunk, n_chunks, S_eff;
+    size_t off_key, off_sel, off_partial, off_tc, total;
+};
+
+DecodeLayout decode_layout(const lowram_decode_shape& s) {
+    DecodeLayout L{};
+    L.S_eff = s.S < s.T ? s.S : s.T;
+    DecodeArgs probe{};
+    probe.s = s;
+    probe.g = s.H_q / s.H_kv;
+    probe.S_eff = L.S_eff;
+    L.tc = tc_supported(probe);
+    L.chunk = L.tc ? 128 : kSimtChunk;
+    L.n_chunks = (int)cdiv(L.S_eff, L.chunk);
+    size_t off = kHeader;
+    L.off_key = off;
+    off += align256(sizeof(float) * (size_t)s.B * s.H_kv * s.T);
+    L.off_sel = off;
+    off += align256(sizeof(int32_t) * (size_t)s.B * s.H_kv * L.S_eff);
+    L.off_partial = off;
+    off += align256(sizeof(float) * (size_t)s.B * s.H_q * L.n_chunks * (s.d + 2));
+    L.off_tc = off;
+    off += L.tc ? align256(tc_scratch_bytes(s)) : 0;
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t lowram_version(void) { return 100; }
+
+const char* lowram_last_error(void) { return g_msg; }
+
+const char* lowram_status_string(lowram_status st) {
+    switch (st) {
+        case LOWRAM_OK: return "ok";
+        case LOWRAM_ERR_INVALID_ARG: return "invalid argument";
+        case LOWRAM_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case LOWRAM_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case LOWRAM_ERR_WORKSPACE: return "workspace missing or too small";
+        case LOWRAM_ERR_CUDA: return "CUDA error";
+        case LOWRAM_ERR_DEVICE_CHECK: return "device check failed";
+    }
+    return "unknown status";
+}
+
+lowram_status lowram_decode_workspace_size(const lowram_decode_shape* shape, size_t* bytes) {
+    lowram_status st = check_decode_shape(shape);
+    if (st != LOWRAM_OK) return st;
+    if (!bytes) return fail(LOWRAM_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = decode_layout(*shape).total;
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_decode_uses_tensor_cores(const lowram_decode_shape* shape, int32_t* yes) {
+    lowram_status st = check_decode_shape(shape);
+    if (st != LOWRAM_OK) return st;
+    if (!yes) return fail(LOWRAM_ERR_INVALID_ARG, "yes is NULL");
+    *yes = decode_layout(*shape).tc ? 1 : 0;
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_rope_table(int32_t d, double theta, int32_t max_pos, float* cos_out, float* sin_out,
+                                void* stream) {
+    if (d <= 0 || d % 2 || max_pos < 0 || !(theta > 0.0)) return fail(LOWRAM_ERR_INVALID_ARG, "d=%d max_pos=%d theta=%g", d, max_pos, theta);
+    if (max_pos == 0) return LOWRAM_OK;
+    if (!cos_out || !sin_out) return fail(LOWRAM_ERR_INVALID_ARG, "NULL table pointer");
+    cudaError_t e = launch_rope_table(d, theta, max_pos, cos_out, sin_out, (cudaStream_t)stream);
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "rope_table");
+}
+
+static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q, const void* coef,
+                                 const void* coef_scale, const int32_t* pos, const float* rope_cos,
+                                 const float* rope_sin, const void* basis, const void* w1, const void* w2,
+                                 const float* b1, const float* b2, const int32_t* res_idx, const void* res_val,
+                                 const void* res_scale, float* out, float* lse, int32_t* sel_out, float* key_out,
+                                 void* workspace, size_t workspace_bytes, void* stream, void* const* events) {
+    lowram_status st = check_decode_shape(shape);
+    if (st != LOWRAM_OK) return st;
+    const lowram_decode_shape& s = *shape;
+    const cudaStream_t cs = (cudaStream_t)stream;
+    const bool any = (int64_t)s.B * s.H_q > 0;
+    if (any && !out) return fail(LOWRAM_ERR_INVALID_ARG, "out is NULL");
+    if ((int64_t)s.B * s.T > 0) {
+        if (!q || !coef || !rope_cos || !rope_sin || !basis || !w1 || !w2)
+            return fail(LOWRAM_ERR_INVALID_ARG, "a required tensor pointer is NULL");
+        if (s.coef_dtype == LOWRAM_INT4_G32 && !coef_scale) return fail(LOWRAM_ERR_INVALID_ARG, "coef_scale is NULL");
+        if (s.n_res > 0 && (!res_idx || !res_val)) return fail(LOWRAM_ERR_INVALID_ARG, "residual list is NULL");
+        if (s.n_res > 0 && s.res_dtype == LOWRAM_INT8_VEC && !res_scale)
+            return fail(LOWRAM_ERR_INVALID_ARG, "res_scale is NULL");
+    }
+    const void* ptrs[] = {q, coef, coef_scale, pos, rope_cos, rope_sin, basis, w1, w2, b1, b2, res_idx, res_val,
+                          res_scale, out, lse, sel_out, key_out, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
+    const DecodeLayout L = decode_layout(s);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(LOWRAM_ERR_WORKSPACE, "workspace %zu bytes, %zu needed", workspace ? workspace_bytes : 0, L.total);
+
+    char* ws = (char*)workspace;
+    DecodeArgs a{};
+    a.s = s;
+    a.g = s.H_q / s.H_kv;
+    a.S_eff = L.S_eff;
+    a.scale = s.sm_scale > 0.0f ? s.sm_scale : 1.0f / sqrtf((float)s.d);
+    a.q = q; a.coef = coef; a.coef_scale = coef_scale; a.pos = pos;
+    a.rope_cos = rope_cos; a.rope_sin = rope_sin; a.basis = basis; a.w1 = w1; a.w2 = w2; a.b1 = b1; a.b2 = b2;
+    a.res_idx = res_idx; a.res_val = res_val; a.res_scale = res_scale; a.out = out; a.lse = lse;
+    a.key = key_out ? key_out : (float*)(ws + L.off_key);
+    a.sel = sel_out ? sel_out : (int32_t*)(ws + L.off_sel);
+    a.partial = (float*)(ws + L.off_partial);
+    a.n_chunks = L.n_chunks;
+    a.check = (uint32_t*)ws;
+    a.scratch = L.tc ? ws + L.off_tc : nullptr;
+    a.scratch_bytes = L.tc ? tc_scratch_bytes(s) : 0;
+
+    // optional timing marks: before K1, after K1, after K2, after K3, after K4
+    auto mark = [&](int i) -> cudaError_t {
+        return (events && events[i]) ? cudaEventRecord((cudaEvent_t)events[i], cs) : cudaSuccess;
+    };
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess && (int64_t)s.B * s.T > 0 && (L.S_eff > 0 || key_out))
+        e = L.tc ? launch_score_tc(a, cs) : launch_score_simt(a, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "score");
+    if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event");
+    if ((int64_t)s.B * L.S_eff > 0) e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "select");
+    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event");
+    if ((int64_t)s.B * L.S_eff > 0) e = L.tc ? launch_vregen_tc(a, cs) : launch_vregen_simt(a, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "vregen");
+    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event");
+    if (any) e = launch_merge(s.B, s.H_q, (int64_t)s.B * L.S_eff > 0 ? L.n_chunks : 0, s.d, a.partial, out, lse, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "merge");
+    if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "event");
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_decode_attn(const lowram_decode_shape* shape, const void* q, const void* coef,
+                                 const void* coef_scale, const int32_t* pos, const float* rope_cos,
+                                 const float* rope_sin, const void* basis, const void* w1, const void* w2,
+                                 const float* b1, const float* b2, const int32_t* res_idx, const void* res_val,
+                                 const void* res_scale, float* out, float* lse, int32_t* sel_out, float* key_out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl(shape, q, coef, coef_scale, pos, rope_cos, rope_sin, basis, w1, w2, b1, b2, res_idx, res_val,
+                       res_scale, out, lse, sel_out, key_out, workspace, workspace_bytes, stream, nullptr);
+}
+
+lowram_status lowram_decode_attn_events(const lowram_decode_shape* shape, const void* q, const void* coef,
+                                        const void* coef_scale, const int32_t* pos, const float* rope_cos,
+                                        const float* rope_sin, const void* basis, const void* w1, const void* w2,
+                                        const float* b1, const float* b2, const int32_t* res_idx,
+                                        const void* res_val, const void* res_scale, float* out, float* lse,
+                                        int32_t* sel_out, float* key_out, void* workspace, size_t workspace_bytes,
+                                        void* stream, void* const* events) {
+    return decode_impl(shape, q, coef, coef_scale, pos, rope_cos, rope_sin, basis, w1, w2, b1, b2, res_idx, res_val,
+                       res_scale, out, lse, sel_out, key_out, workspace, workspace_bytes, stream, events);
+}
+
+// ------------------------------------------------------------------------------------------------
+// compress
+// ------------------------------------------------------------------------------------------------
+static lowram_status check_compress_shape(const lowram_compress_shape* s) {
+    if (!s) return fail(LOWRAM_ERR_INVALID_ARG, "shape is NULL");
+    if (s->B < 0 || s->T < 0 || s->n_res < 0 || s->n_res > s->T)
+        return fail(LOWRAM_ERR_INVALID_ARG, "bad sizes (B=%d T=%d n_res=%d)", s->B, s->T, s->n_res);
+    if (s->G < 1 || s->G > 16) return fail(LOWRAM_ERR_UNSUPPORTED, "G=%d (1..16)", s->G);
+    if (s->H_kv < 1) return fail(LOWRAM_ERR_INVALID_ARG, "H_kv=%d", s->H_kv);
+    if (s->d != 64 && s->d != 128) return fail(LOWRAM_ERR_UNSUPPORTED, "d=%d (64 or 128 supported)", s->d);
+    if (s->r < 32 || s->r % 32 != 0 || s->r > 1024) return fail(LOWRAM_ERR_UNSUPPORTED, "r=%d", s->r);
+    if (s->m < 32 || s->m % 32 != 0 || s->m > 256) return fail(LOWRAM_ERR_UNSUPPORTED, "m=%d", s->m);
+    if (!is_act(s->act_dtype)) return fail(LOWRAM_ERR_INVALID_ARG, "act_dtype=%d", s->act_dtype);
+    if (s->coef_dtype != LOWRAM_F32 && s->coef_dtype != LOWRAM_BF16 && s->coef_dtype != LOWRAM_INT4_G32)
+        return fail(LOWRAM_ERR_INVALID_ARG, "coef_dtype=%d", s->coef_dtype);
+    if (s->res_dtype != LOWRAM_F32 && s->res_dtype != LOWRAM_BF16 && s->res_dtype != LOWRAM_INT8_VEC)
+        return fail(LOWRAM_ERR_INVALID_ARG, "res_dtype=%d", s->res_dtype);
+    if (s->keys_post_rope && s->T > 0 && s->max_pos < 1) return fail(LOWRAM_ERR_INVALID_ARG, "max_pos=%d", s->max_pos);
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_compress_workspace_size(const lowram_compress_shape* shape, size_t* bytes) {
+    lowram_status st = check_compress_shape(shape);
+    if (st != LOWRAM_OK) return st;
+    if (!bytes) return fail(LOWRAM_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = kHeader + align256(sizeof(float) * (size_t)shape->B * shape->H_kv * shape->T);
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_compress(const lowram_compress_shape* shape, const void* keys, const void* const* values,
+                              const float* proj, const int32_t* pos, const float* rope_cos, const float* rope_sin,
+                              const void* const* basis, const void* const* w1, const void* const* w2,
+                              const float* const* b1, const float* const* b2, void* coef_out, void* coef_scale_out,
+                              int32_t* const* res_idx_out, void* const* res_val_out, void* const* res_scale_out,
+                              float* const* err_out, void* workspace, size_t workspace_bytes, void* stream) {
+    lowram_status st = check_compress_shape(shape);
+    if (st != LOWRAM_OK) return st;
+    const lowram_compress_shape& s = *shape;
+    const cudaStream_t cs = (cudaStream_t)stream;
+    size_t need = 0;
+    lowram_compress_workspace_size(shape, &need);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return fail(LOWRAM_ERR_WORKSPACE, "workspace %zu bytes, %zu needed", workspace ? workspace_bytes : 0, need);
+    if ((int64_t)s.B * s.T == 0) return LOWRAM_OK;
+    if (!keys || !values || !proj || !basis || !w1 || !w2 || !coef_out)
+        return fail(LOWRAM_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (s.coef_dtype == LOWRAM_INT4_G32 && !coef_scale_out) return fail(LOWRAM_ERR_INVALID_ARG, "coef_scale_out is NULL");
+    if (s.keys_post_rope && (!rope_cos || !rope_sin)) return fail(LOWRAM_ERR_INVALID_ARG, "RoPE tables are NULL");
+    if (s.n_res > 0 && (!res_idx_out || !res_val_out)) return fail(LOWRAM_ERR_INVALID_ARG, "residual outputs are NULL");
+    if (s.n_res > 0 && s.res_dtype == LOWRAM_INT8_VEC && !res_scale_out)
+        return fail(LOWRAM_ERR_INVALID_ARG, "res_scale_out is NULL");
+
+    CompressArgs a{};
+    a.s = s;
+    a.keys = keys; a.proj = proj; a.pos = pos; a.rope_cos = rope_cos; a.rope_sin = rope_sin;
+    a.coef_out = coef_out; a.coef_scale_out = coef_scale_out;
+    a.check = (uint32_t*)workspace;
+    a.err_scratch = (float*)((char*)workspace + kHeader);
+    const void* top[] = {keys, proj, pos, rope_cos, rope_sin, coef_out, coef_scale_out};
+    for (const void* p : top)
+        if (p && !aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
+    for (int l = 0; l < s.G; ++l) {
+        a.values[l] = values[l]; a.basis[l] = basis[l]; a.w1[l] = w1[l]; a.w2[l] = w2[l];
+        a.b1[l] = b1 ? b1[l] : nullptr; a.b2[l] = b2 ? b2[l] : nullptr;
+        a.res_idx_out[l] = s.n_res > 0 ? res_idx_out[l] : nullptr;
+        a.res_val_out[l] = s.n_res > 0 ? res_val_out[l] : nullptr;
+        a.res_scale_out[l] = (s.n_res > 0 && res_scale_out) ? res_scale_out[l] : nullptr;
+        a.err_out[l] = err_out ? err_out[l] : nullptr;
+        if (!a.values[l] || !a.basis[l] || !a.w1[l] || !a.w2[l])
+            return fail(LOWRAM_ERR_INVALID_ARG, "layer %d: a required pointer is NULL", l);
+        if (s.n_res > 0 && (!a.res_idx_out[l] || !a.res_val_out[l]))
+            return fail(LOWRAM_ERR_INVALID_ARG, "layer %d: residual output is NULL", l);
+        if (s.n_res > 0 && s.res_dtype == LOWRAM_INT8_VEC && !a.res_scale_out[l])
+            return fail(LOWRAM_ERR_INVALID_ARG, "layer %d: res_scale_out is NULL", l);
+        const void* lp[] = {a.values[l], a.basis[l], a.w1[l], a.w2[l], a.b1[l], a.b2[l], a.res_idx_out[l],
+                            a.res_val_out[l], a.res_scale_out[l], a.err_out[l]};
+        for (const void* p : lp)
+            if (p && !aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "layer %d: pointer %p is not 16-byte aligned", l, p);
+    }
+    cudaError_t e = launch_project(a, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "project");
+    for (int l = 0; l < s.G; ++l) {
+        float* err = a.err_out[l] ? a.err_out[l] : a.err_scratch;
+        e = launch_predict_err(a, l, err, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "predict_err");
+        if (s.n_res > 0) {
+            e = launch_select_topn(s.B * s.H_kv, s.T, s.n_res, err, a.res_idx_out[l], cs);
+            if (e != cudaSuccess) return cuda_fail(e, "select residuals");
+            e = launch_residual_rows(a, l, cs);
+            if (e != cudaSuccess) return cuda_fail(e, "residual rows");
+        }
+    }
+    return LOWRAM_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+// dense comparator
+// ------------------------------------------------------------------------------------------------
+lowram_status lowram_dense_workspace_size(int32_t B, int32_t T, int32_t H_q, int32_t H_kv, int32_t d, size_t* bytes) {
+    if (B < 0 || T < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv || (d != 64 && d != 128) || !bytes)
+        return fail(LOWRAM_ERR_INVALID_ARG, "bad dense shape");
+    const int ns = dense_splits(B, T, H_kv);
+    *bytes = kHeader + align256(sizeof(float) * (size_t)B * H_q * ns * (d + 2));
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_dense_decode_attn(int32_t B, int32_t T, int32_t H_q, int32_t H_kv, int32_t d, int32_t dtype,
+                                       float sm_scale, const void* q, const void* k, const void* v, float* out,
+                                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    size_t need = 0;
+    lowram_status st = lowram_dense_workspace_size(B, T, H_q, H_kv, d, &need);
+    if (st != LOWRAM_OK) return st;
+    if (!is_act(dtype)) return fail(LOWRAM_ERR_INVALID_ARG, "dtype=%d", dtype);
+    const int g = H_q / H_kv;
+    if (g != 1 && g != 2 && g != 4 && g != 7 && g != 8) return fail(LOWRAM_ERR_UNSUPPORTED, "H_q/H_kv=%d", g);
+    if (!workspace || workspace_bytes < need) return fail(LOWRAM_ERR_WORKSPACE, "workspace too small (%zu needed)", need);
+    if ((int64_t)B * H_q == 0) return LOWRAM_OK;
+    if (!out || (T > 0 && (!q || !k || !v))) return fail(LOWRAM_ERR_INVALID_ARG, "a required pointer is NULL");
+    const void* ptrs[] = {q, k, v, out, lse, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
+    const cudaStream_t cs = (cudaStream_t)stream;
+    const int ns = dense_splits(B, T, H_kv);
+    float* partial = (float*)((char*)workspace + kHeader);
+    const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf((float)d);
+    cudaError_t e = cudaSuccess;
+    if (T > 0) {
+        e = launch_dense(B, T, H_q, H_kv, d, dtype, scale, q, k, v, partial, ns, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "dense");
+    }
+    e = launch_merge(B, H_q, T > 0 ? ns : 0, d, partial, out, lse, cs);
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "merge");
+}
+
+// ------------------------------------------------------------------------------------------------
+// status
+// ------------------------------------------------------------------------------------------------
+lowram_status lowram_get_error(void* workspace, void* stream, uint32_t* check_word) {
+    if (!workspace || !check_word) return fail(LOWRAM_ERR_INVALID_ARG, "NULL argument");
+    const cudaStream_t cs = (cudaStream_t)stream;
+    uint32_t w = 0;
+    cudaError_t e = cudaMemcpyAsync(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e, "get_error");
+    *check_word = w;
+    return w ? fail(LOWRAM_ERR_DEVICE_CHECK, "device check word 0x%x", w) : LOWRAM_OK;
+}
+
+lowram_status lowram_clear_error(void* workspace, void* stream) {
+    if (!workspace) return fail(LOWRAM_ERR_INVALID_ARG, "workspace is NULL");
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kHeader, (cudaStream_t)stream);
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "clear_error");
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+// select.cu -- K2: exact top-n of each row of a float matrix, ties to the lower index, output
+// ascending.  Used for the per-(sequence, kv-head) token selection of decode (LowRAM abstract:
+// "reconstructing only a selected subset of KV pairs at each decoding step"; the rule -- exact
+// largest scores -- is this library's reading) and for the worst-n_res residual tokens of the write
+// side ("stores residuals only for the tokens it reconstructs worst").
+//
+// Radix select on order-preserving uint32 keys: four 8-bit digit passes narrow the candidates to
+// the exact value of the n-th largest element (the threshold) and how many elements equal to it must
+// be kept; a final pass in index order keeps every element above the threshold and the
+// lowest-indexed equal ones, writing their indices ascending through a block-wide prefix sum.
+// One CTA per row; the row streams from global memory (L2) on every pass.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lowram {
+
+constexpr int kSelThreads = 1024;
+
+// Exclusive block-wide prefix sum of a 0/1 flag (one per thread), plus the block total.
+__device__ __forceinline__ int block_excl_scan(bool f, int* warp_tot, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    unsigned bal = __ballot_sync(0xffffffffu, f);
+    int in_warp = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_tot[warp] = __popc(bal);
+    __syncthreads();
+    if (warp == 0) {
+        int v = lane < nw ? warp_tot[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        if (lane < nw) warp_tot[lane] = incl - v;  // exclusive
+        if (lane == 31) warp_tot[32] = incl;        // total
+    }
+    __syncthreads();
+    int r = warp_tot[warp] + in_warp;
+    total = warp_tot[32];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_keep, const float* __restrict__ values,
+                                                                  int32_t* __restrict__ out) {
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* v = values + (int64_t)row * T;
+    int32_t* o = out + (int64_t)row * n_keep;
+    if (n_keep <= 0) return;
+    if (n_keep >= T) {
+        for (int t = tid; t < T; t += kSelThreads) o[t] = t;
+        return;
+    }
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_need;
+    __shared__ int warp_tot[33];
+
+    uint32_t prefix = 0, mask = 0;
+    int need = n_keep;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+        __syncthreads();
+        for (int t = tid; t < T; t += kSelThreads) {
+            uint32_t u = order_key(v[t]);
+            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane L owns bins [8L, 8L+8); suffix sums over lanes from the top bin down
+            uint32_t mine = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mine += hist[lane * 8 + j];
+            uint32_t suf = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                uint32_t x = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += x;
+            }
+            bool hit = suf >= (uint32_t)need && suf - mine < (uint32_t)need;
+            unsigned bal = __ballot_sync(0xffffffffu, hit);
+            int L = __ffs(bal) - 1;
+            if (lane == L) {
+                uint32_t above = suf - mine;
+                for (int j = 7; j >= 0; --j) {
+                    uint32_t c = hist[L * 8 + j];
+                    if (above + c >= (uint32_t)need) {
+                        s_prefix = prefix | ((uint32_t)(L * 8 + j) << shift);
+                        s_need = need - (int)above;
+                        break;
+                    }
+                    above += c;
+                }
+            }
+        }
+        __syncthreads();
+        prefix = s_prefix;
+        need = s_need;
+        mask |= 0xFFu << shift;
+        __syncthreads();
+    }
+    // prefix is now the threshold key; keep all keys above it and the first `need` equal ones.
+    int taken = 0, eq_seen = 0;
+    for (int base = 0; base < T; base += kSelThreads) {
+        const int t = base + tid;
+        const uint32_t u = t < T ? order_key(v[t]) : 0u;
+        const bool eq = t < T && u == prefix;
+        int eq_total;
+        const int eq_rank = eq_seen + block_excl_scan(eq, warp_tot, eq_total);
+        const bool take = (t < T && u > prefix) || (eq && eq_rank < need);
+        int take_total;
+        const int at = taken + block_excl_scan(take, warp_tot, take_total);
+        if (take && at < n_keep) o[at] = t;
+        taken += take_total;
+        eq_seen += eq_total;
+    }
+}
+
+size_t select_scratch_bytes(int, int, int) { return 0; }
+
+cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, int32_t* out, cudaStream_t st) {
+    if (P == 0 || n_keep <= 0) return cudaSuccess;
+    select_topn_kernel<<<(unsigned)P, kSelThreads, 0, st>>>(T, n_keep, values, out);
+    return cudaGetLastError();
+}
+
+}  // namespace lowram

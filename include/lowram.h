@@ -1,0 +1,249 @@
+/*
+ * lowram.h -- C ABI of liblowram.so: LowRAM compressed-cache decode attention on B300 (sm_103a).
+ *
+ * The method (web pages about arXiv:2611.07025, cited by page title and section):
+ *   - "LowRAM: Low-Rank Keys and Amortised Values for Composable KV Cache Compression at Test-Time"
+ *     (arXiv listing), Abstract: values are predicted from keys by a lightweight per-head predictor
+ *     fitted at test time, residuals are stored only for the worst-reconstructed tokens, keys get
+ *     cross-layer low-rank compression, and each decode step reconstructs only a selected subset of
+ *     KV pairs.  It composes with quantisation and eviction.
+ *   - "LowRAM Paper: Amortised Values and Low-Rank Keys for KV Compression", sections "Value cache
+ *     amortisation in plain language" (per-head MLP, per-token error, sparse residuals for the
+ *     worst), "Asymmetric key compression with xKV" (a layer group shares the token-side factor;
+ *     RoPE is inverted before compression and re-applied during attention), "Step-by-step mental
+ *     model for one decoding session" (prefill compresses; decode rebuilds on demand).
+ *   - "LowRAM: predict values from keys, store only the misses", flowchart "Values are mostly a
+ *     function of keys" (keys -> predictor -> predicted values + residual store -> attention on a
+ *     subset rebuilt per step).
+ * The pages fix neither the selection rule nor the predictor's shape.  This library fixes them:
+ * exact-score top-S per (sequence, kv-head), where a token's score is the largest scaled logit over
+ * the q-heads sharing the kv-head (ties to the lower token index; unselected tokens are left out of
+ * the softmax), and a 2-layer MLP with SiLU on the rebuilt pre-RoPE key.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller, row-major and contiguous, 16-byte
+ *     aligned (LOWRAM_ERR_ALIGNMENT otherwise).  Arrays of pointers (one per layer of a group) are
+ *     HOST arrays holding device pointers.  The library allocates no device memory: scratch comes
+ *     from the caller's workspace, sized by the matching *_workspace_size query.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Calls enqueue
+ *     work on it and return without synchronising, after checking their arguments on the host.
+ *   - Errors are return codes; no C++ exception crosses the ABI.  lowram_last_error() gives a
+ *     message for the calling thread's last failing call.  Kernels that find bad data (positions or
+ *     residual indices out of range or unordered) clamp, keep going, and set a sticky word in the
+ *     workspace that lowram_get_error() reads and clears.  No kernel waits on another CTA.
+ *   - q-head hq reads kv-head hq / (H_q / H_kv).
+ */
+#ifndef LOWRAM_H
+#define LOWRAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LOWRAM_API __attribute__((visibility("default")))
+#else
+#define LOWRAM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LOWRAM_OK = 0,
+    LOWRAM_ERR_INVALID_ARG = 1,   /* a size, a dtype or a required pointer is wrong */
+    LOWRAM_ERR_ALIGNMENT = 2,     /* a pointer is not 16-byte aligned */
+    LOWRAM_ERR_UNSUPPORTED = 3,   /* valid, but not built for this shape or dtype combination */
+    LOWRAM_ERR_WORKSPACE = 4,     /* workspace NULL, misaligned or smaller than the query's answer */
+    LOWRAM_ERR_CUDA = 5,          /* a CUDA runtime call or a launch failed */
+    LOWRAM_ERR_DEVICE_CHECK = 6   /* lowram_get_error: a kernel found out-of-range or unordered data */
+} lowram_status;
+
+typedef enum {
+    LOWRAM_F32 = 0,        /* float32 */
+    LOWRAM_BF16 = 1,       /* bfloat16 */
+    LOWRAM_INT4_G32 = 2,   /* coefficients: int4 codes, two per byte (even entry in the low nibble,
+                              two's complement, -7..7), plus one fp16 scale per 32 consecutive
+                              entries of a row: value = code * scale */
+    LOWRAM_INT8_VEC = 3    /* residuals: int8 codes (-127..127) plus one fp16 scale per d-vector */
+} lowram_dtype;
+
+/* Bits of the device check word returned by lowram_get_error(). */
+#define LOWRAM_CHECK_POS_RANGE 1u      /* a position was < 0 or >= max_pos (clamped) */
+#define LOWRAM_CHECK_RES_INDEX 2u      /* a residual index was out of range or not strictly ascending */
+
+/* ---------------------------------------------------------------------------------------------
+ * Decode: one layer, all B sequences.
+ * ------------------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t B;          /* sequences */
+    int32_t T;          /* stored tokens per sequence (after eviction, if any) */
+    int32_t H_q, H_kv;  /* query heads, kv-heads; H_q % H_kv == 0, H_q / H_kv <= 8 */
+    int32_t d;          /* head dim: 64 or 128 */
+    int32_t r;          /* latent rank of the layer group: multiple of 32, <= 1024 */
+    int32_t m;          /* predictor hidden width: multiple of 32, <= 256 */
+    int32_t S;          /* tokens selected per (sequence, kv-head); min(S, T) are used */
+    int32_t n_res;      /* stored residuals per (sequence, kv-head), 0 <= n_res <= T */
+    int32_t act_dtype;  /* q, basis, w1, w2: LOWRAM_F32 or LOWRAM_BF16 */
+    int32_t coef_dtype; /* LOWRAM_F32, LOWRAM_BF16 (both need act_dtype equal) or LOWRAM_INT4_G32 */
+    int32_t res_dtype;  /* LOWRAM_F32, LOWRAM_BF16 or LOWRAM_INT8_VEC */
+    int32_t max_pos;    /* rows of the RoPE tables: positions are in [0, max_pos) */
+    float sm_scale;     /* softmax scale; <= 0 selects 1/sqrt(d) */
+} lowram_decode_shape;
+
+/* Workspace bytes lowram_decode_attn needs for this shape (a multiple of 256). */
+LOWRAM_API lowram_status lowram_decode_workspace_size(const lowram_decode_shape* shape, size_t* bytes);
+
+/* *yes = 1 if calls of this shape run the key pass and the value regeneration on the tensor cores
+ * (tcgen05; bf16 or int4 caches), 0 if they run on the CUDA cores (float32 caches and shapes the
+ * tensor-core kernels do not cover). */
+LOWRAM_API lowram_status lowram_decode_uses_tensor_cores(const lowram_decode_shape* shape, int32_t* yes);
+
+/*
+ * lowram_decode_attn -- decode-step attention read directly from the compressed cache.
+ * Steps (LowRAM abstract; "Step-by-step mental model", step 2; "Asymmetric key compression with
+ * xKV"; flowchart "Values are mostly a function of keys"):
+ *   1. every token's pre-RoPE key k_pre[t, h, :] = basis[h*d : h*d+d, :] . coef[b, t, :];
+ *   2. k = RoPE(k_pre) at the token's position (rotate-half: pair (i, i+d/2) rotated by
+ *      pos * theta^(-2i/d), read from the cos/sin tables);
+ *   3. s[hq, t] = sm_scale * q[b, hq] . k; selection key[h, t] = max over the q-heads of kv-head h;
+ *   4. keep the min(S, T) tokens with the largest key (ties to the lower index);
+ *   5. for kept tokens only: v = w2[h] . SiLU(w1[h] . k_pre + b1[h]) + b2[h], plus res_val[b, h, j]
+ *      when t == res_idx[b, h, j];
+ *   6. out[b, hq] = softmax over the kept tokens of s[hq, .] applied to their values.
+ * Arguments (device pointers; shapes use the fields of *shape):
+ *   q          [B, H_q, d] act_dtype, already rotated at the query's own position
+ *   coef       [B, T, r] coef_dtype; LOWRAM_INT4_G32: [B, T, r/2] bytes
+ *   coef_scale LOWRAM_INT4_G32 only: [B, T, r/32] fp16 scales; else NULL
+ *   pos        [B, T] int32 original positions (eviction); NULL means position t
+ *   rope_cos, rope_sin  [d/2, max_pos] float32 each (frequency-major), see lowram_rope_table
+ *   basis      [H_kv*d, r] act_dtype (row h*d+i: latent coefficients of key feature (h, i))
+ *   w1         [H_kv, m, d] act_dtype;  b1 [H_kv, m] float32 or NULL
+ *   w2         [H_kv, d, m] act_dtype;  b2 [H_kv, d] float32 or NULL
+ *   res_idx    [B, H_kv, n_res] int32, strictly ascending per (b, h), in [0, T)
+ *   res_val    [B, H_kv, n_res, d] res_dtype
+ *   res_scale  LOWRAM_INT8_VEC only: [B, H_kv, n_res] fp16; else NULL
+ *   out        [B, H_q, d] float32 (written)
+ *   lse        [B, H_q] float32 log-sum-exp of the kept scaled logits, or NULL
+ *   sel_out    [B, H_kv, min(S,T)] int32 kept token indices, ascending, or NULL
+ *   key_out    [B, H_kv, T] float32 selection keys, or NULL
+ * With T == 0 or S == 0, out is zero and lse is -inf.
+ */
+LOWRAM_API lowram_status lowram_decode_attn(const lowram_decode_shape* shape, const void* q, const void* coef,
+                                 const void* coef_scale, const int32_t* pos, const float* rope_cos,
+                                 const float* rope_sin, const void* basis, const void* w1, const void* w2,
+                                 const float* b1, const float* b2, const int32_t* res_idx, const void* res_val,
+                                 const void* res_scale, float* out, float* lse, int32_t* sel_out, float* key_out,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * lowram_decode_attn_events -- lowram_decode_attn, plus timing marks: when `events` (a host array of five
+ * cudaEvent_t, any of them NULL) is given, events[0] is recorded on `stream` before the key pass,
+ * events[1] after it, events[2] after the top-S selection, events[3] after value regeneration and
+ * events[4] after the softmax merge.  Same kernels, same results.
+ */
+LOWRAM_API lowram_status lowram_decode_attn_events(const lowram_decode_shape* shape, const void* q, const void* coef,
+                                                   const void* coef_scale, const int32_t* pos, const float* rope_cos,
+                                                   const float* rope_sin, const void* basis, const void* w1,
+                                                   const void* w2, const float* b1, const float* b2,
+                                                   const int32_t* res_idx, const void* res_val, const void* res_scale,
+                                                   float* out, float* lse, int32_t* sel_out, float* key_out,
+                                                   void* workspace, size_t workspace_bytes, void* stream,
+                                                   void* const* events);
+
+/*
+ * lowram_rope_table -- cos/sin tables of the rotary embedding re-applied at decode ("Asymmetric key
+ * compression with xKV": RoPE is inverted before compression and re-applied during attention).
+ * cos_out[i * max_pos + p] = cos(p * theta^(-2i/d)), sin_out likewise, i < d/2, p < max_pos.
+ * Angles are formed and evaluated in fp64 on the device, then rounded to float32.
+ */
+LOWRAM_API lowram_status lowram_rope_table(int32_t d, double theta, int32_t max_pos, float* cos_out, float* sin_out,
+                                void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Compress: the write side for one layer group (prefill).
+ * ------------------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t B, T;          /* sequences; stored tokens per sequence */
+    int32_t G;             /* layers in the group, 1..16 */
+    int32_t H_kv, d, r, m; /* kv-heads, head dim (64/128), latent rank (multiple of 32), hidden width */
+    int32_t n_res;         /* residuals kept per (sequence, layer, kv-head) */
+    int32_t act_dtype;     /* keys, values, basis, w1, w2: LOWRAM_F32 or LOWRAM_BF16 */
+    int32_t coef_dtype;    /* output coefficients: LOWRAM_F32, LOWRAM_BF16 or LOWRAM_INT4_G32 */
+    int32_t res_dtype;     /* output residuals: LOWRAM_F32, LOWRAM_BF16 or LOWRAM_INT8_VEC */
+    int32_t keys_post_rope;/* 1: keys are given rotated at their positions and are rotated back first */
+    int32_t max_pos;       /* rows of the RoPE tables (used when keys_post_rope == 1) */
+} lowram_compress_shape;
+
+LOWRAM_API lowram_status lowram_compress_workspace_size(const lowram_compress_shape* shape, size_t* bytes);
+
+/*
+ * lowram_compress -- latent coefficients and worst-token residual lists of one layer group.
+ * Steps (LowRAM abstract: "stores residuals only for the tokens it reconstructs worst"; "Value
+ * cache amortisation in plain language": scores the per-token reconstruction error and keeps sparse
+ * residuals for the worst predictions; "Step-by-step mental model", step 1; "Asymmetric key
+ * compression with xKV"):
+ *   1. (keys_post_rope) rotate each key back by its position; concatenate the G layers' keys of a
+ *      token: k_cat[b, t, :] of length G*H_kv*d (layer, then head, then feature);
+ *   2. coef[b, t, k] = sum_n proj[k, n] * k_cat[b, t, n], stored as coef_dtype (round to nearest
+ *      even; int4: per-32 fp16 scale = amax/7, codes round(x/scale) clamped to +-7);
+ *   3. per layer l: rebuild keys from the STORED coefficients, predict values with the layer's
+ *      MLP in float32, err[b, h, t] = || values[l][b, t, h, :] - prediction ||_2;
+ *   4. keep the n_res largest errors per (b, h) (ties to the lower index), ascending by index, with
+ *      residual values - prediction stored as res_dtype (int8: per-vector fp16 scale = amax/127).
+ * Arguments:
+ *   keys       [B, T, G, H_kv, d] act_dtype (pre-RoPE unless keys_post_rope)
+ *   values     host array of G device pointers, each [B, T, H_kv, d] act_dtype
+ *   proj       [r, G*H_kv*d] float32: a left inverse of the group's stacked bases (proj . W = I)
+ *   pos        [B, T] int32 or NULL (position t); rope_cos/rope_sin as for decode, NULL unless
+ *              keys_post_rope
+ *   basis, w1, w2   host arrays of G device pointers, layouts as for decode; b1, b2 host arrays of G
+ *              float32 device pointers, or NULL
+ *   coef_out   [B, T, r] coef_dtype (int4: [B, T, r/2] bytes); coef_scale_out [B, T, r/32] fp16 for
+ *              int4, else NULL
+ *   res_idx_out, res_val_out, res_scale_out   host arrays of G device pointers: [B, H_kv, n_res]
+ *              int32; [B, H_kv, n_res, d] res_dtype; [B, H_kv, n_res] fp16 (int8 only, else NULL)
+ *   err_out    host array of G device pointers to [B, H_kv, T] float32, or NULL
+ */
+LOWRAM_API lowram_status lowram_compress(const lowram_compress_shape* shape, const void* keys, const void* const* values,
+                              const float* proj, const int32_t* pos, const float* rope_cos, const float* rope_sin,
+                              const void* const* basis, const void* const* w1, const void* const* w2,
+                              const float* const* b1, const float* const* b2, void* coef_out, void* coef_scale_out,
+                              int32_t* const* res_idx_out, void* const* res_val_out, void* const* res_scale_out,
+                              float* const* err_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Comparator: the same kernel family on an uncompressed cache.
+ * ------------------------------------------------------------------------------------------- */
+LOWRAM_API lowram_status lowram_dense_workspace_size(int32_t B, int32_t T, int32_t H_q, int32_t H_kv, int32_t d, size_t* bytes);
+
+/*
+ * lowram_dense_decode_attn -- softmax attention of one decode query per q-head over an explicit,
+ * already rotated key cache and a value cache, both [B, T, H_kv, d] in dtype (LOWRAM_BF16 or
+ * LOWRAM_F32); q [B, H_q, d] in dtype; out [B, H_q, d] float32; lse [B, H_q] float32 or NULL.
+ * This is the baseline the compressed cache replaces (LowRAM abstract: the KV cache's footprint
+ * caps batch size and throughput).
+ */
+LOWRAM_API lowram_status lowram_dense_decode_attn(int32_t B, int32_t T, int32_t H_q, int32_t H_kv, int32_t d, int32_t dtype,
+                                       float sm_scale, const void* q, const void* k, const void* v, float* out,
+                                       float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Status
+ * ------------------------------------------------------------------------------------------- */
+/* Synchronises `stream`, returns the device check word accumulated in `workspace` since it was last
+ * cleared (LOWRAM_CHECK_* bits; 0 = no bad data), and clears it.  A fresh workspace must have its first
+ * 256 bytes zeroed once (lowram_clear_error) before its first use. */
+LOWRAM_API lowram_status lowram_get_error(void* workspace, void* stream, uint32_t* check_word);
+/* Enqueues a clear of the device check word in `workspace`. */
+LOWRAM_API lowram_status lowram_clear_error(void* workspace, void* stream);
+LOWRAM_API const char* lowram_status_string(lowram_status status);
+/* Message for the calling thread's most recent failing call ("" if none). */
+LOWRAM_API const char* lowram_last_error(void);
+/* Library version: major * 10000 + minor * 100 + patch. */
+LOWRAM_API int32_t lowram_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LOWRAM_H */

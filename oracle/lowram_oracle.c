@@ -161,6 +161,11 @@ void lro_rope(int d, double theta, double pos, const double* x, double* y, int i
     }
 }
 
+/* Rotate n d-vectors, row i at position pos[i] (a batch of lro_rope calls). */
+void lro_rope_rows(int64_t n, int d, double theta, const int32_t* pos, const double* x, double* y, int inverse) {
+    for (int64_t i = 0; i < n; ++i) lro_rope(d, theta, (double)pos[i], x + i * d, y + i * d, inverse);
+}
+
 /* ---------------------------------------------------------------------------------------------
  * Key rebuild from the cross-layer low-rank factors ([EX] "Asymmetric key compression with xKV";
  * [ABS] "cross-layer low-rank key compression"): the pre-RoPE key of feature (h, i) of token t is

@@ -29,7 +29,7 @@ _SO = os.path.join(_HERE, "liblowram_oracle.so")
 
 __all__ = [
     "build", "lib", "Dims", "f64", "round_bf16", "round_f16", "round_f32", "quant_int4_g32",
-    "dequant_int4_g32", "quant_int8_vec", "dequant_int8_vec", "rope", "rope_angles", "mlp",
+    "dequant_int4_g32", "quant_int8_vec", "dequant_int8_vec", "rope", "rope_rows", "rope_angles", "mlp",
     "rebuild_keys", "predict_values", "decode", "project", "residuals", "compress_group",
     "dense_decode", "top_n", "n_res_for", "max_threads", "store",
 ]
@@ -74,6 +74,7 @@ def lib():
             "lro_dequant_int8_vec": (None, [i64, ci, _I8, _D, _D]),
             "lro_rope_angles": (None, [ci, cd, cd, _D, _D]),
             "lro_rope": (None, [ci, cd, cd, _D, _D, ci]),
+            "lro_rope_rows": (None, [i64, ci, cd, _I32, _D, _D, ci]),
             "lro_mlp": (None, [ci, ci, _D, _D, _D, _D, _D, _D, _D]),
             "lro_top_n": (None, [ci, _D, ci, _I32]),
             "lro_decode": (ci, [ctypes.POINTER(Dims), _D, _D, _I32, _D, _D, _D, _D, _D, _I32, _D,
@@ -227,6 +228,16 @@ def rope(x, pos: float, theta: float, inverse: bool = False) -> np.ndarray:
     a = f64(x)
     y = np.empty_like(a)
     lib().lro_rope(a.shape[-1], float(theta), float(pos), _p(a), _p(y), int(bool(inverse)))
+    return y
+
+
+def rope_rows(x, pos, theta: float, inverse: bool = False) -> np.ndarray:
+    """Rotate every d-vector of x [..., d]; pos has x's shape without the last axis (one position per vector)."""
+    a = f64(x)
+    d = a.shape[-1]
+    P = np.ascontiguousarray(np.broadcast_to(_i32(pos), a.shape[:-1]), dtype=np.int32)
+    y = np.empty_like(a)
+    lib().lro_rope_rows(a.size // d, d, float(theta), _p(P, _I32), _p(a), _p(y), int(bool(inverse)))
     return y
 
 

@@ -1,0 +1,155 @@
+"""GPU parity of lowram_decode_attn against the fp64 oracle, through the C ABI.
+
+Small cases (the oracle runs the whole problem) span several tiles with ragged tails for every workload
+shape; full-size cases run the GPU at the benchmark's sizes and compare sampled (sequence, kv-head) pairs
+that the oracle recomputes independently.  Edge cases: empty inputs, S >= T (selection is a no-op), S = 1,
+no residuals, every token a residual, exact ties, and the device check word on bad indices.
+"""
+import numpy as np
+import pytest
+import torch
+
+import lowram_cases as C
+import oracle as O
+from decode_attention_19_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+SMALL = {
+    "tiny": W["tiny"],
+    "tiny_ragged_S": W["tiny"].with_(T=250, S=100),
+    "llama8b_small": W["llama8b"].with_(B=2, T=1000, S=300),
+    "long_small": W["long"].with_(B=1, T=1500, S=400),
+    "peak_small": W["peak"].with_(B=3, T=777, S=200),
+    "evict_quant_small": W["evict_quant"].with_(B=2, T=3000, T_nominal=12000, S=500),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def test_rope_table_matches_fp64_angles():
+    import decode_attention_19_b300 as L
+    for d, theta, n in [(64, 1e4, 300), (128, 5e5, 65536)]:
+        cos, sin = L.lowram_rope_table(d, theta, n)
+        cos, sin = cos.cpu().double().numpy(), sin.cpu().double().numpy()
+        for p in [0, 1, 17, n // 2, n - 1]:
+            c, s = O.rope_angles(d, theta, p)
+            np.testing.assert_allclose(cos[:, p], c, atol=1e-7, rtol=0)
+            np.testing.assert_allclose(sin[:, p], s, atol=1e-7, rtol=0)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("biases", [False, True])
+def test_decode_small_matches_oracle(name, biases):
+    w = SMALL[name]
+    c = C.decode_case(w, biases=biases)
+    gpu = C.run_gpu_decode(c)
+    orc = C.run_oracle_decode(c)
+    C.check_decode(gpu, orc, w.S_eff)
+
+
+@pytest.mark.parametrize("S", [0, 1, 7, 129, 999, 1000, 5000])
+def test_decode_selection_sizes(S):
+    w = SMALL["llama8b_small"].with_(S=S)
+    c = C.decode_case(w)
+    gpu = C.run_gpu_decode(c, S=S)
+    orc = C.run_oracle_decode(c, S=S)
+    S_eff = min(S, w.T)
+    C.check_decode(gpu, orc, S_eff)
+    if S_eff == 0:
+        assert np.all(gpu["out"] == 0) and np.all(np.isneginf(gpu["lse"]))
+
+
+@pytest.mark.parametrize("rho", [0.0, 1.0])
+def test_decode_residual_extremes(rho):
+    w = SMALL["llama8b_small"].with_(rho=rho)
+    c = C.decode_case(w)
+    if rho == 0.0:
+        assert c["res_idx"].shape[-1] == 0
+    C.check_decode(C.run_gpu_decode(c), C.run_oracle_decode(c), w.S_eff)
+
+
+@pytest.mark.parametrize("T", [1, 31, 33, 127, 129])
+def test_decode_tiny_token_counts(T):
+    w = SMALL["llama8b_small"].with_(T=T, S=min(T, 17))
+    c = C.decode_case(w)
+    C.check_decode(C.run_gpu_decode(c), C.run_oracle_decode(c), w.S_eff)
+
+
+def test_decode_exact_ties_take_the_lower_index():
+    w = SMALL["llama8b_small"].with_(B=1, T=300, S=100)
+    c = C.decode_case(w)
+    # copy token 10's latents and position onto tokens 11..40: identical keys in every head
+    coef = c["coef"].clone()
+    coef[0, 11:41] = coef[0, 10]
+    c["coef"] = coef
+    c["coef_vals"] = O.f64(coef)
+    pos = torch.arange(w.T, dtype=torch.int32)[None].clone()
+    pos[0, 11:41] = 10
+    c["pos"] = pos
+    gpu = C.run_gpu_decode(c)
+    orc = C.run_oracle_decode(c)
+    assert np.array_equal(gpu["key"][0, :, 10:41], np.repeat(gpu["key"][0, :, 10:11], 31, axis=1))
+    C.check_decode(gpu, orc, w.S_eff)
+    # where the cut falls inside the tie block the lower indices are kept: the kept members of the block
+    # form a prefix of it
+    for h in range(w.H_kv):
+        kept = [t for t in gpu["sel"][0, h] if 10 <= t <= 40]
+        assert kept == list(range(10, 10 + len(kept)))
+
+
+def test_decode_empty_batch_and_empty_cache():
+    import decode_attention_19_b300 as L
+    w = SMALL["llama8b_small"].with_(T=0, S=10, rho=0.0)
+    c = C.decode_case(w)
+    gpu = C.run_gpu_decode(c, hooks=False)
+    assert np.all(gpu["out"] == 0) and np.all(np.isneginf(gpu["lse"]))
+    w0 = SMALL["llama8b_small"].with_(B=0)
+    c0 = C.decode_case(w0)
+    gpu0 = C.run_gpu_decode(c0, hooks=False)
+    assert gpu0["out"].shape == (0, w.H_q, w.d)
+
+
+def test_device_check_word_flags_bad_residual_list_and_positions():
+    import decode_attention_19_b300 as L
+    w = SMALL["llama8b_small"]
+    c = C.decode_case(w)
+    ws = torch.zeros(1 << 24, dtype=torch.uint8, device="cuda")
+    C.run_gpu_decode(c, workspace=ws)
+    assert L.lowram_get_error(ws) == 0
+    bad = c["res_idx"].clone()
+    bad[0, 0, 5] = bad[0, 0, 4]          # not strictly ascending (still in range)
+    c2 = dict(c, res_idx=bad)
+    C.run_gpu_decode(c2, workspace=ws)
+    assert L.lowram_get_error(ws) & L.CHECK_RES_INDEX
+    assert L.lowram_get_error(ws) == 0   # cleared by the read
+    pos = torch.arange(w.T, dtype=torch.int32)[None].repeat(w.B, 1)
+    pos[1, 7] = 5000                     # beyond the tables (max_pos = T): clamped and flagged
+    c3 = dict(c, pos=pos)
+    C.run_gpu_decode(c3, workspace=ws)
+    assert L.lowram_get_error(ws) & L.CHECK_POS_RANGE
+
+
+FULL = ["tiny", "llama8b", "long", "peak", "evict_quant"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_decode_full_size_sampled(name):
+    """The benchmark's sizes on the GPU; the oracle recomputes sampled (sequence, kv-head) sub-problems."""
+    w = W[name]
+    c = C.decode_case(w)
+    gpu = C.run_gpu_decode(c)
+    g = w.H_q // w.H_kv
+    samples = [(0, 0), (w.B - 1, w.H_kv - 1)] if w.B * w.H_kv > 1 else [(0, 0)]
+    for b, h in samples:
+        sub = C.slice_case(c, [b], [h])
+        orc = C.run_oracle_decode(sub)
+        part = {"out": gpu["out"][b:b + 1, h * g:(h + 1) * g], "lse": gpu["lse"][b:b + 1, h * g:(h + 1) * g],
+                "key": gpu["key"][b:b + 1, h:h + 1], "sel": gpu["sel"][b:b + 1, h:h + 1]}
+        C.check_decode(part, orc, w.S_eff)
