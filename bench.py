@@ -205,7 +205,7 @@ def build_cache(w, dev):
             V = torch.einsum("bthm,hdm->bthd", Hh, raw["w2"][l].to(dev).float())
             V += 0.3 * torch.randn(V.shape, device=dev, generator=gen)
             keys.append(K.to(act))
-            vals.append(V.to(act))
+            vals.append(V.to(act).contiguous())
             del K, Hh, V
         kg = torch.stack(keys, dim=2).contiguous()
         del keys

@@ -56,9 +56,11 @@ cudaError_t launch_vregen_simt(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_merge(int B, int H_q, int n_chunks, int d, const float* partial, float* out, float* lse,
                          cudaStream_t st);
 
-// Tensor-core path (bf16 / int4 caches).  Returns cudaErrorNotSupported when the shape is not covered.
-bool tc_supported(const DecodeArgs& a);
+// Tensor-core path (bf16 caches): which of K1 / K3 cover a shape, and the scratch they need.
+bool tc_score_supported(const lowram_decode_shape& s);
+bool tc_vregen_supported(const lowram_decode_shape& s);
 size_t tc_scratch_bytes(const lowram_decode_shape& s);
+constexpr int kTcChunk = 128;
 cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st);
 

@@ -63,7 +63,7 @@ lowram_status check_decode_shape(const lowram_decode_shape* s) {
 }
 
 struct DecodeLayout {
-    bool tc;
+    bool tc_score, tc_vregen;
     int chunk, n_chunks, S_eff;
     size_t off_key, off_sel, off_partial, off_tc, total;
 };
@@ -71,12 +71,9 @@ struct DecodeLayout {
 DecodeLayout decode_layout(const lowram_decode_shape& s) {
     DecodeLayout L{};
     L.S_eff = s.S < s.T ? s.S : s.T;
-    DecodeArgs probe{};
-    probe.s = s;
-    probe.g = s.H_q / s.H_kv;
-    probe.S_eff = L.S_eff;
-    L.tc = tc_supported(probe);
-    L.chunk = L.tc ? 128 : kSimtChunk;
+    L.tc_score = tc_score_supported(s);
+    L.tc_vregen = tc_vregen_supported(s);
+    L.chunk = L.tc_vregen ? kTcChunk : kSimtChunk;
     L.n_chunks = (int)cdiv(L.S_eff, L.chunk);
     size_t off = kHeader;
     L.off_key = off;
@@ -86,7 +83,7 @@ DecodeLayout decode_layout(const lowram_decode_shape& s) {
     L.off_partial = off;
     off += align256(sizeof(float) * (size_t)s.B * s.H_q * L.n_chunks * (s.d + 2));
     L.off_tc = off;
-    off += L.tc ? align256(tc_scratch_bytes(s)) : 0;
+    off += L.tc_vregen ? align256(tc_scratch_bytes(s)) : 0;
     L.total = off;
     return L;
 }
@@ -124,7 +121,7 @@ lowram_status lowram_decode_uses_tensor_cores(const lowram_decode_shape* shape, 
     lowram_status st = check_decode_shape(shape);
     if (st != LOWRAM_OK) return st;
     if (!yes) return fail(LOWRAM_ERR_INVALID_ARG, "yes is NULL");
-    *yes = decode_layout(*shape).tc ? 1 : 0;
+    *yes = decode_layout(*shape).tc_score ? 1 : 0;
     return LOWRAM_OK;
 }
 
@@ -179,8 +176,8 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     a.partial = (float*)(ws + L.off_partial);
     a.n_chunks = L.n_chunks;
     a.check = (uint32_t*)ws;
-    a.scratch = L.tc ? ws + L.off_tc : nullptr;
-    a.scratch_bytes = L.tc ? tc_scratch_bytes(s) : 0;
+    a.scratch = L.tc_vregen ? ws + L.off_tc : nullptr;
+    a.scratch_bytes = L.tc_vregen ? tc_scratch_bytes(s) : 0;
 
     // optional timing marks: before K1, after K1, after K2, after K3, after K4
     auto mark = [&](int i) -> cudaError_t {
@@ -188,13 +185,13 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     };
     cudaError_t e = mark(0);
     if (e == cudaSuccess && (int64_t)s.B * s.T > 0 && (L.S_eff > 0 || key_out))
-        e = L.tc ? launch_score_tc(a, cs) : launch_score_simt(a, cs);
+        e = L.tc_score ? launch_score_tc(a, cs) : launch_score_simt(a, cs);
     if (e != cudaSuccess) return cuda_fail(e, "score");
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event");
     if ((int64_t)s.B * L.S_eff > 0) e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs);
     if (e != cudaSuccess) return cuda_fail(e, "select");
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event");
-    if ((int64_t)s.B * L.S_eff > 0) e = L.tc ? launch_vregen_tc(a, cs) : launch_vregen_simt(a, cs);
+    if ((int64_t)s.B * L.S_eff > 0) e = L.tc_vregen ? launch_vregen_tc(a, cs) : launch_vregen_simt(a, cs);
     if (e != cudaSuccess) return cuda_fail(e, "vregen");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event");
     if (any) e = launch_merge(s.B, s.H_q, (int64_t)s.B * L.S_eff > 0 ? L.n_chunks : 0, s.d, a.partial, out, lse, cs);

@@ -71,6 +71,7 @@ typedef enum {
 /* Bits of the device check word returned by lowram_get_error(). */
 #define LOWRAM_CHECK_POS_RANGE 1u      /* a position was < 0 or >= max_pos (clamped) */
 #define LOWRAM_CHECK_RES_INDEX 2u      /* a residual index was out of range or not strictly ascending */
+#define LOWRAM_CHECK_TIMEOUT 4u        /* a tensor-core pipeline wait gave up (internal error; results invalid) */
 
 /* ---------------------------------------------------------------------------------------------
  * Decode: one layer, all B sequences.

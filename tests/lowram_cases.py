@@ -69,6 +69,9 @@ def run_gpu_decode(c: dict, *, S=None, hooks=True, workspace=None):
     key = torch.empty((B, w.H_kv, T), dtype=torch.float32, device=dev) if hooks else None
     sel = torch.empty((B, w.H_kv, S_eff), dtype=torch.int32, device=dev) if hooks else None
     n_res = c["res_idx"].shape[-1]
+    own_ws = workspace is None
+    if own_ws:
+        workspace = torch.zeros(1 << 26, dtype=torch.uint8, device=dev)
     out, lse = L.lowram_decode_attn(cu(c["q"]), cu(c["coef"]), cu(c["basis"]), cu(c["w1"]), cu(c["w2"]),
                                     rope_cos=cos, rope_sin=sin, S=S, coef_scale=cu(c["coef_scale"]), pos=cu(c["pos"]),
                                     b1=cu(c["b1"]), b2=cu(c["b2"]),
@@ -77,6 +80,8 @@ def run_gpu_decode(c: dict, *, S=None, hooks=True, workspace=None):
                                     res_scale=cu(c["res_scale"]) if n_res else None, sel_out=sel, key_out=key,
                                     workspace=workspace)
     torch.cuda.synchronize()
+    if own_ws:
+        assert L.lowram_get_error(workspace) == 0, "device check word set"
     r = {"out": out.cpu().double().numpy(), "lse": lse.cpu().double().numpy()}
     if hooks:
         r["key"] = key.cpu().double().numpy()
@@ -206,54 +211,85 @@ def run_oracle_compress(c: dict, bs=None) -> dict:
                             keys_post_rope=c["keys_post_rope"], theta=w.theta)
 
 
-def check_compress(gpu: dict, orc: dict, w: synth.Workload, bs=None):
-    """Stored coefficients are valid roundings of the oracle's unrounded projection; errors, residual index
-    sets and residual rows match, except on tokens whose stored coefficients came out differently (a
-    rounding decision flipped by the fp32 vs fp64 projection) or that lie within the band of the cut."""
+def _proj_abs_bound(c, sl):
+    """Worst-case fp32 accumulation error of the projection per coefficient: N * 2^-24 * sum_n |k_n p_n|."""
+    K = np.abs(O.f64(c["keys"])[sl]).reshape(-1, c["proj"].shape[1])
+    P = np.abs(O.f64(c["proj"]))
+    N = P.shape[1]
+    return (K @ P.T).reshape(O.f64(c["keys"])[sl].shape[:2] + (P.shape[0],)) * N * 2.0 ** -24
+
+
+def check_compress(gpu: dict, orc: dict, w: synth.Workload, c: dict, bs=None):
+    """Stored coefficients are valid roundings of the oracle's unrounded projection (within the fp32
+    accumulation bound); errors, residual index sets and residual rows match.  A token whose stored
+    coefficients came out differently on the two sides (a rounding decision flipped by the fp32 vs fp64
+    projection) gets a different error, so it may enter or leave the residual set on either side; what is
+    unique is the ranking of the other tokens: the GPU's residual tokens outside that flipped set must be the
+    oracle's top ones among the unflipped tokens, up to the 1e-3 band at that cut-off."""
     sl = slice(None) if bs is None else bs
     raw = orc["coef_raw"]
+    acc = _proj_abs_bound(c, sl)
+    stats = {}
     if w.coef_fmt == "int4":
         g_codes = gpu["coef"].cpu()[sl].numpy()
         g_scale = gpu["coef_scale"].cpu()[sl].double().numpy()
         g_vals = O.dequant_int4_g32(g_codes, g_scale)
         s_full = np.repeat(g_scale, 32, axis=-1)
-        assert np.all(np.abs(g_vals - raw) <= s_full / 2 * (1 + 1e-3) + 1e-5), "int4 codes are not a valid rounding"
+        assert np.all(np.abs(g_vals - raw) <= s_full / 2 * (1 + 1e-3) + acc + 1e-7), "int4 codes are not a valid rounding"
         o_scale = orc["coef_scale"]
         assert np.all(np.abs(g_scale - o_scale) <= np.abs(o_scale) * 2.0 ** -10 + 1e-12)
         flipped_rows = np.any(g_codes != orc["coef_q"], axis=-1) | np.any(g_scale != o_scale, axis=-1)   # [B, T]
     else:
         g_vals = gpu["coef"].cpu()[sl].double().numpy()
         if w.coef_fmt == "bf16":
-            assert np.all(np.abs(g_vals - raw) <= np.abs(raw) * 2.0 ** -8 + 1e-6), "bf16 coefficients misrounded"
+            assert np.all(np.abs(g_vals - raw) <= np.abs(raw) * 2.0 ** -8 + acc * (1 + 2.0 ** -8) + 1e-12), \
+                "bf16 coefficients misrounded"
         else:
-            assert np.all(np.abs(g_vals - raw) <= np.abs(raw) * 1e-5 + 1e-5)
-        flipped_rows = np.any(g_vals != orc["coef"], axis=-1)
-    assert flipped_rows.mean() < 0.05 if w.coef_fmt == "int4" else flipped_rows.mean() < 0.5
+            assert np.all(np.abs(g_vals - raw) <= np.abs(raw) * 2.0 ** -24 + acc + 1e-12)
+        # float32 storage has no rounding decision to flip; 16-bit storage flips where the fp32 and fp64
+        # projections straddle a rounding boundary
+        flipped_rows = np.any(g_vals != orc["coef"], axis=-1) if w.coef_fmt == "bf16" else np.zeros(g_vals.shape[:2], bool)
+    stats["flipped_row_frac"] = float(flipped_rows.mean())
     B, T = flipped_rows.shape
     for l in range(w.G):
         lay = orc["layers"][l]
         g_err = gpu["err"][l].cpu()[sl].double().numpy()             # [B, H_kv, T]
         same = ~flipped_rows[:, None, :].repeat(w.H_kv, 1)
         ed = np.abs(g_err - lay["err"])[same]
-        assert ed.size == 0 or float(ed.max()) <= 1e-3, f"layer {l}: err differs by {float(ed.max()):.3g}"
+        stats[f"err_maxdiff_l{l}"] = float(ed.max()) if ed.size else 0.0
+        assert ed.size == 0 or float(ed.max()) <= 1e-4, f"layer {l}: err differs by {float(ed.max()):.3g}"
         if w.n_res == 0:
             continue
         g_idx = gpu["res_idx"][l].cpu()[sl].numpy()
-        P = B * w.H_kv
-        extra = [set(np.nonzero(flipped_rows[p // w.H_kv])[0].tolist()) for p in range(P)]
-        check_index_sets(g_idx.reshape(P, -1), lay["res_idx"].reshape(P, -1), lay["err"].reshape(P, -1), w.n_res,
-                         allowed_extra=extra, what=f"layer {l} residuals")
+        for b in range(B):
+            F = set(np.nonzero(flipped_rows[b])[0].tolist())
+            for h in range(w.H_kv):
+                gs = g_idx[b, h].tolist()
+                assert gs == sorted(set(gs)), f"layer {l} (b={b}, h={h}): residual list not strictly ascending"
+                g_rest = set(gs) - F
+                n_rest = len(g_rest)
+                e = lay["err"][b, h]
+                order = sorted((t for t in range(T) if t not in F), key=lambda t: (-e[t], t))
+                want = set(order[:n_rest])
+                if n_rest == 0 or g_rest == want:
+                    continue
+                cut = e[order[n_rest - 1]]
+                for t in g_rest ^ want:
+                    assert abs(e[t] - cut) <= BAND, \
+                        f"layer {l} (b={b}, h={h}): token {t} differs, {abs(e[t] - cut):.3g} from the cut-off"
         # residual rows of tokens kept by both sides, with unflipped coefficients
         if w.res_fmt == "int8":
             g_rv = O.dequant_int8_vec(gpu["res_val"][l].cpu()[sl].numpy(), gpu["res_scale"][l].cpu()[sl].double().numpy())
         else:
             g_rv = gpu["res_val"][l].cpu()[sl].double().numpy()
         o_rv = lay["res_val"]
-        for p in range(P):
-            b, h = divmod(p, w.H_kv)
-            gi = {t: j for j, t in enumerate(g_idx[b, h].tolist())}
-            for j, t in enumerate(lay["res_idx"][b, h].tolist()):
-                if t in gi and not flipped_rows[b, t]:
-                    gv, ov = g_rv[b, h, gi[t]], o_rv[b, h, j]
-                    tol = (np.abs(ov).max() / 127.0 + 1e-4) if w.res_fmt == "int8" else (np.abs(ov) * 2.0 ** -7 + 1e-4)
-                    assert np.all(np.abs(gv - ov) <= tol), f"layer {l} (b={b}, h={h}) residual row of token {t}"
+        for b in range(B):
+            for h in range(w.H_kv):
+                gi = {t: j for j, t in enumerate(g_idx[b, h].tolist())}
+                for j, t in enumerate(lay["res_idx"][b, h].tolist()):
+                    if t in gi and not flipped_rows[b, t]:
+                        gv, ov = g_rv[b, h, gi[t]], o_rv[b, h, j]
+                        tol = (np.abs(ov).max() / 127.0 + 1e-4) if w.res_fmt == "int8" else (np.abs(ov) * 2.0 ** -7 + 1e-4)
+                        assert np.all(np.abs(gv - ov) <= tol), f"layer {l} (b={b}, h={h}) residual row of token {t}"
+    print("compress parity:", stats)
+    return stats

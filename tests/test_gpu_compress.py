@@ -28,14 +28,14 @@ def _cuda():
 def test_compress_small_matches_oracle(name):
     w = SMALL[name]
     c = C.compress_case(w)
-    C.check_compress(C.run_gpu_compress(c), C.run_oracle_compress(c), w)
+    C.check_compress(C.run_gpu_compress(c), C.run_oracle_compress(c), w, c)
 
 
 @pytest.mark.parametrize("name", ["llama8b_small", "evict_quant_small"])
 def test_compress_keys_given_after_rope(name):
     w = SMALL[name]
     c = C.compress_case(w, keys_post_rope=True)
-    C.check_compress(C.run_gpu_compress(c), C.run_oracle_compress(c), w)
+    C.check_compress(C.run_gpu_compress(c), C.run_oracle_compress(c), w, c)
 
 
 @pytest.mark.parametrize("rho", [0.0, 1.0])
@@ -43,7 +43,7 @@ def test_compress_residual_extremes(rho):
     w = SMALL["llama8b_small"].with_(rho=rho)
     c = C.compress_case(w)
     gpu = C.run_gpu_compress(c)
-    C.check_compress(gpu, C.run_oracle_compress(c), w)
+    C.check_compress(gpu, C.run_oracle_compress(c), w, c)
     if rho == 1.0:
         assert all(np.array_equal(gpu["res_idx"][l].cpu().numpy()[b, h], np.arange(w.T))
                    for l in range(w.G) for b in range(w.B) for h in range(w.H_kv))
@@ -56,7 +56,7 @@ def test_compress_full_size_sampled(name):
     c = C.compress_case(w)
     gpu = C.run_gpu_compress(c)
     b = [w.B - 1]
-    C.check_compress(gpu, C.run_oracle_compress(c, bs=b), w, bs=b)
+    C.check_compress(gpu, C.run_oracle_compress(c, bs=b), w, c, bs=b)
 
 
 def test_compress_then_decode_round_trip():

@@ -33,6 +33,17 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
+def test_bf16_workloads_take_the_tensor_core_key_pass():
+    import decode_attention_19_b300 as L
+    for name in ["llama8b", "long", "peak"]:
+        w = W[name]
+        sh = L.lowram_decode_shape(w.B, w.T, w.H_q, w.H_kv, w.d, w.r, w.m, w.S, w.n_res, 1, 1, 1, w.T, 0.0)
+        assert L.lowram_decode_uses_tensor_cores(sh), name
+    tiny = W["tiny"]
+    sh = L.lowram_decode_shape(1, 256, 4, 2, 64, 32, 64, 256, 64, 0, 0, 0, 256, 0.0)
+    assert not L.lowram_decode_uses_tensor_cores(sh)
+
+
 def test_rope_table_matches_fp64_angles():
     import decode_attention_19_b300 as L
     for d, theta, n in [(64, 1e4, 300), (128, 5e5, 65536)]:
