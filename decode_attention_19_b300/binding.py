@@ -54,6 +54,7 @@ def _load():
             "lowram_decode_workspace_size": [ctypes.POINTER(lowram_decode_shape), psz],
             "lowram_decode_attn": [ctypes.POINTER(lowram_decode_shape)] + [_vp] * 18 + [_vp, sz, _vp],
             "lowram_decode_attn_events": [ctypes.POINTER(lowram_decode_shape)] + [_vp] * 18 + [_vp, sz, _vp, _vp],
+            "lowram_decode_attn_static": [ctypes.POINTER(lowram_decode_shape)] + [_vp] * 18 + [_vp],
             "lowram_rope_table": [i32, dbl, i32, _vp, _vp, _vp],
             "lowram_compress_workspace_size": [ctypes.POINTER(lowram_compress_shape), psz],
             "lowram_compress": [ctypes.POINTER(lowram_compress_shape)] + [_vp] * 18 + [sz, _vp],
@@ -197,6 +198,34 @@ def lowram_decode_attn(q: torch.Tensor, coef: torch.Tensor, basis: torch.Tensor,
     else:
         arr = (ctypes.c_void_p * 5)(*[None if e is None else e.cuda_event for e in events])
         _check(_load().lowram_decode_attn_events(*args, ctypes.cast(arr, _vp)))
+    return out, lse
+
+
+def lowram_decode_attn_static(q: torch.Tensor, coef: torch.Tensor, basis: torch.Tensor, w1: torch.Tensor,
+                              w2: torch.Tensor, *, rope_cos: torch.Tensor, rope_sin: torch.Tensor, S: int,
+                              out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                              coef_scale: Optional[torch.Tensor] = None, pos: Optional[torch.Tensor] = None,
+                              b1: Optional[torch.Tensor] = None, b2: Optional[torch.Tensor] = None,
+                              res_idx: Optional[torch.Tensor] = None, res_val: Optional[torch.Tensor] = None,
+                              res_scale: Optional[torch.Tensor] = None, sm_scale: float = 0.0):
+    """lowram_decode_attn for callers that cannot allocate: the library's static device scratch replaces the
+    workspace (see include/lowram.h).  The caller passes every input and preallocated outputs; this wrapper
+    allocates nothing."""
+    coef_int4 = coef.dtype == torch.uint8
+    n_res = 0 if res_idx is None else int(res_idx.shape[-1])
+    if res_val is None:
+        res_dtype = _act(q)
+    elif res_val.dtype == torch.int8:
+        res_dtype = LOWRAM_INT8_VEC
+    else:
+        res_dtype = _act(res_val)
+    shape = decode_shape(q, coef, w1, S=S, n_res=n_res, max_pos=rope_cos.shape[1], res_dtype=res_dtype,
+                         sm_scale=sm_scale, coef_int4=coef_int4)
+    _dev(q, coef, basis, w1, w2, rope_cos, rope_sin, coef_scale, pos, b1, b2, res_idx, res_val, res_scale, out, lse)
+    _check(_load().lowram_decode_attn_static(ctypes.byref(shape), _p(q), _p(coef), _p(coef_scale), _p(pos),
+                                             _p(rope_cos), _p(rope_sin), _p(basis), _p(w1), _p(w2), _p(b1), _p(b2),
+                                             _p(res_idx), _p(res_val), _p(res_scale), _p(out), _p(lse), None, None,
+                                             _stream()))
     return out, lse
 
 

@@ -9,6 +9,8 @@
 
 namespace lowram {
 
+void set_error_message(const char* fmt, ...);
+
 // Everything a decode call needs, already validated by the ABI layer.
 struct DecodeArgs {
     lowram_decode_shape s;

@@ -90,6 +90,16 @@ DecodeLayout decode_layout(const lowram_decode_shape& s) {
 
 }  // namespace
 
+namespace lowram {
+// Set the calling thread's lowram_last_error() message (for entry points defined in other files).
+void set_error_message(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+}
+}  // namespace lowram
+
 extern "C" {
 
 int32_t lowram_version(void) { return 100; }

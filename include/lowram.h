@@ -153,6 +153,32 @@ LOWRAM_API lowram_status lowram_decode_attn_events(const lowram_decode_shape* sh
                                                    void* const* events);
 
 /*
+ * lowram_decode_attn_static -- lowram_decode_attn for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for integration.  Some callers cannot
+ * call cudaMalloc or pass a workspace: code running inside another runtime's memory pool or arena that
+ * owns every allocation, plug-ins loaded by a host that gives them no allocator, and code paths that
+ * must not allocate after setup.  This call takes the same inputs and outputs as lowram_decode_attn
+ * (same meaning, layouts and results) but allocates nothing: its scratch lives in one file-scope device
+ * array of 32 MiB that every GPU which loads the library holds until the process exits.
+ *   - Shapes whose lowram_decode_workspace_size() exceeds 32 MiB are rejected with
+ *     LOWRAM_ERR_WORKSPACE (lowram_last_error() says how much they need).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, once per
+ *     device, with that device current).  Make that first call before any stream capture.
+ *   - Every call shares the one array per device, which keeps the last call's contents: calls that
+ *     overlap on the GPU (different streams, or threads without ordering) race and corrupt each other's
+ *     results.  Order them on one stream.
+ *   - Each call clears the device check word at its start; that word cannot be read through this call,
+ *     so data checks (LOWRAM_CHECK_*) are not reported here.
+ */
+LOWRAM_API lowram_status lowram_decode_attn_static(const lowram_decode_shape* shape, const void* q, const void* coef,
+                                                   const void* coef_scale, const int32_t* pos, const float* rope_cos,
+                                                   const float* rope_sin, const void* basis, const void* w1,
+                                                   const void* w2, const float* b1, const float* b2,
+                                                   const int32_t* res_idx, const void* res_val, const void* res_scale,
+                                                   float* out, float* lse, int32_t* sel_out, float* key_out,
+                                                   void* stream);
+
+/*
  * lowram_rope_table -- cos/sin tables of the rotary embedding re-applied at decode ("Asymmetric key
  * compression with xKV": RoPE is inverted before compression and re-applied during attention).
  * cos_out[i * max_pos + p] = cos(p * theta^(-2i/d)), sin_out likewise, i < d/2, p < max_pos.
