@@ -37,9 +37,9 @@ struct DecodeArgs {
     int32_t* sel;
     float* partial;
     int n_chunks;        // partial chunks per (b, q-head)
+    int PW;              // floats per partial record
+    float* sall;         // [B, H_q, T] scaled logits of every q-head (tensor-core path), or null
     uint32_t* check;
-    void* scratch;       // extra scratch for the tensor-core kernels
-    size_t scratch_bytes;
 };
 
 // Chunk (selected tokens per vregen CTA) used by each path.
@@ -58,13 +58,17 @@ cudaError_t launch_vregen_simt(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_merge(int B, int H_q, int n_chunks, int d, const float* partial, float* out, float* lse,
                          cudaStream_t st);
 
-// Tensor-core path (bf16 caches): which of K1 / K3 cover a shape, and the scratch they need.
+// Tensor-core path (bf16 caches): which of K1 / K3 cover a shape.  K3 on the tensor cores needs K1 on them
+// too (it reads the scaled logits K1 stores) and writes partial records of tc_partial_width floats: the
+// weighted hidden-unit sums [m], the weighted residual sums [d], the chunk's max logit and weight sum.
 bool tc_score_supported(const lowram_decode_shape& s);
 bool tc_vregen_supported(const lowram_decode_shape& s);
-size_t tc_scratch_bytes(const lowram_decode_shape& s);
+int tc_partial_width(const lowram_decode_shape& s);
 constexpr int kTcChunk = 128;
 cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st);
+// K4 for the tensor-core path: merge, then the predictor's second layer on the merged sums
+cudaError_t launch_merge_w2(const DecodeArgs& a, int n_chunks, cudaStream_t st);
 
 // Write side
 struct CompressArgs {

@@ -64,8 +64,8 @@ lowram_status check_decode_shape(const lowram_decode_shape* s) {
 
 struct DecodeLayout {
     bool tc_score, tc_vregen;
-    int chunk, n_chunks, S_eff;
-    size_t off_key, off_sel, off_partial, off_tc, total;
+    int chunk, n_chunks, S_eff, PW;
+    size_t off_key, off_sel, off_partial, off_sall, total;
 };
 
 DecodeLayout decode_layout(const lowram_decode_shape& s) {
@@ -75,15 +75,16 @@ DecodeLayout decode_layout(const lowram_decode_shape& s) {
     L.tc_vregen = tc_vregen_supported(s);
     L.chunk = L.tc_vregen ? kTcChunk : kSimtChunk;
     L.n_chunks = (int)cdiv(L.S_eff, L.chunk);
+    L.PW = L.tc_vregen ? tc_partial_width(s) : s.d + 2;
     size_t off = kHeader;
     L.off_key = off;
     off += align256(sizeof(float) * (size_t)s.B * s.H_kv * s.T);
     L.off_sel = off;
     off += align256(sizeof(int32_t) * (size_t)s.B * s.H_kv * L.S_eff);
     L.off_partial = off;
-    off += align256(sizeof(float) * (size_t)s.B * s.H_q * L.n_chunks * (s.d + 2));
-    L.off_tc = off;
-    off += L.tc_vregen ? align256(tc_scratch_bytes(s)) : 0;
+    off += align256(sizeof(float) * (size_t)s.B * s.H_q * L.n_chunks * L.PW);
+    L.off_sall = off;
+    off += L.tc_vregen ? align256(sizeof(float) * (size_t)s.B * s.H_q * s.T) : 0;
     L.total = off;
     return L;
 }
@@ -185,9 +186,9 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     a.sel = sel_out ? sel_out : (int32_t*)(ws + L.off_sel);
     a.partial = (float*)(ws + L.off_partial);
     a.n_chunks = L.n_chunks;
+    a.PW = L.PW;
+    a.sall = L.tc_vregen ? (float*)(ws + L.off_sall) : nullptr;
     a.check = (uint32_t*)ws;
-    a.scratch = L.tc_vregen ? ws + L.off_tc : nullptr;
-    a.scratch_bytes = L.tc_vregen ? tc_scratch_bytes(s) : 0;
 
     // optional timing marks: before K1, after K1, after K2, after K3, after K4
     auto mark = [&](int i) -> cudaError_t {
@@ -204,7 +205,10 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     if ((int64_t)s.B * L.S_eff > 0) e = L.tc_vregen ? launch_vregen_tc(a, cs) : launch_vregen_simt(a, cs);
     if (e != cudaSuccess) return cuda_fail(e, "vregen");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event");
-    if (any) e = launch_merge(s.B, s.H_q, (int64_t)s.B * L.S_eff > 0 ? L.n_chunks : 0, s.d, a.partial, out, lse, cs);
+    if (any) {
+        const int nc = (int64_t)s.B * L.S_eff > 0 ? L.n_chunks : 0;
+        e = L.tc_vregen ? launch_merge_w2(a, nc, cs) : launch_merge(s.B, s.H_q, nc, s.d, a.partial, out, lse, cs);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "merge");
     if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "event");
     return LOWRAM_OK;

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 
@@ -66,6 +67,22 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+
+// ------------------------------------------------------------------------------------------------
+// cp.async (gathers of scattered rows into the swizzled operand layout) and the proxy fence
+// ------------------------------------------------------------------------------------------------
+// 16-byte copy global -> shared through L2 only; src_bytes == 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Shared-memory writes of the generic proxy (st.shared, cp.async) made visible to the async proxy, which
+// tcgen05.mma reads operands through.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // ------------------------------------------------------------------------------------------------
 // TMA
@@ -163,6 +180,48 @@ __device__ __forceinline__ void tmem_ld_2x32(uint32_t ta, uint32_t tb, float (&x
         x[i] = __uint_as_float(a[i]);
         y[i] = __uint_as_float(b[i]);
     }
+}
+
+// ------------------------------------------------------------------------------------------------
+// host side: tensor maps and the SM count
+// ------------------------------------------------------------------------------------------------
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    }();
+    return fn;
+}
+
+inline int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
+// bf16 tensor [dims[rank-1]] ... [dims[0]] (dims[0] innermost), box of box[i] elements, 128B swizzle.
+inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[3], gstride[2];
+    cuuint32_t bdim[3], estr[3] = {1, 1, 1};
+    uint64_t stride = 2;
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        if (i > 0) gstride[i - 1] = stride;
+        stride *= dims[i];
+    }
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gdim, gstride, bdim,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 }  // namespace tc

@@ -43,6 +43,7 @@ struct ScoreTcParams {
     const float* rcos;
     const float* rsin;
     float* key;
+    float* sall;        // [B, H_q, T] scaled logits of every q-head, or null
     uint32_t* check;
 };
 
@@ -218,7 +219,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 float best = -INFINITY;
 #pragma unroll
                 for (int jq = 0; jq < G; ++jq) best = fmaxf(best, acc[jq] * p.scale);
-                if (t < p.T) p.key[((int64_t)b * p.H_kv + h) * p.T + t] = best;
+                if (t < p.T) {
+                    p.key[((int64_t)b * p.H_kv + h) * p.T + t] = best;
+                    if (p.sall)
+#pragma unroll
+                        for (int jq = 0; jq < G; ++jq)
+                            p.sall[((int64_t)b * p.H_q + h * G + jq) * p.T + t] = acc[jq] * p.scale;
+                }
             }
         }
     }
@@ -236,44 +243,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // ------------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            ptr = nullptr;
-        return (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-    }();
-    return fn;
-}
-
-int sm_count() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 148;
-}
-
-// bf16 tensor [dims[rank-1]] ... [dims[0]] (dims[0] innermost), box of box[i] elements, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t gdim[3], gstride[2];
-    cuuint32_t bdim[3], estr[3] = {1, 1, 1};
-    uint64_t stride = 2;
-    for (int i = 0; i < rank; ++i) {
-        gdim[i] = dims[i];
-        bdim[i] = box[i];
-        if (i > 0) gstride[i - 1] = stride;
-        stride *= dims[i];
-    }
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gdim, gstride, bdim,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
+using tc::encode_fn;
+using tc::make_map;
+using tc::sm_count;
 
 int stages_for(int KC) {
     for (int ns = 4; ns >= 2; --ns)
@@ -292,8 +264,6 @@ bool tc_score_supported(const lowram_decode_shape& s) {
            encode_fn() != nullptr;
 }
 
-bool tc_vregen_supported(const lowram_decode_shape&) { return false; }
-size_t tc_scratch_bytes(const lowram_decode_shape&) { return 0; }
 
 cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     const auto& s = a.s;
@@ -315,6 +285,7 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     p.rcos = a.rope_cos;
     p.rsin = a.rope_sin;
     p.key = a.key;
+    p.sall = a.sall;
     p.check = a.check;
     if (p.n_tiles == 0) return cudaSuccess;
     CUtensorMap mA, mB;
@@ -343,7 +314,5 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     }
     return e;
 }
-
-cudaError_t launch_vregen_tc(const DecodeArgs&, cudaStream_t) { return cudaErrorNotSupported; }
 
 }  // namespace lowram
