@@ -86,6 +86,9 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+// SiLU with the fast reciprocal-based division (a few ulp; the tensor-core path's operands are bf16).  For
+// x < -88 the denominator is +inf and the result is -0.
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 __host__ __device__ constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

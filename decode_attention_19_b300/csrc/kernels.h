@@ -39,6 +39,8 @@ struct DecodeArgs {
     int n_chunks;        // partial chunks per (b, q-head)
     int PW;              // floats per partial record
     float* sall;         // [B, H_q, T] scaled logits of every q-head (tensor-core path), or null
+    int32_t* cnt;        // [B, H_kv] finished-chunk counters for the merge fused into K3, or null
+    int32_t* hit;        // [B, H_kv, S_eff] residual row of each selected token or -1 (tensor-core path), or null
     uint32_t* check;
 };
 
@@ -49,8 +51,12 @@ cudaError_t launch_rope_table(int d, double theta, int max_pos, float* cos_out, 
 
 // K1: selection keys of every token (CUDA-core path; any dtype)
 cudaError_t launch_score_simt(const DecodeArgs& a, cudaStream_t st);
-// K2: exact top-n per problem row (values [P][T] -> ascending indices [P][n])
-cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, int32_t* out, cudaStream_t st);
+// K2: exact top-n per problem row (values [P][T] -> ascending indices [P][n]).  For the value pass it can also
+// zero zero_cnt[row] (merge counters) and write hit[row][j] = position of token out[row][j] in the row's
+// ascending residual list res_idx[row][0..n_res) or -1, checking the list (LOWRAM_CHECK_RES_INDEX into check).
+cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, int32_t* out, cudaStream_t st,
+                               int32_t* zero_cnt = nullptr, int32_t* hit = nullptr, const int32_t* res_idx = nullptr,
+                               int n_res = 0, uint32_t* check = nullptr);
 size_t select_scratch_bytes(int P, int T, int n_keep);
 // K3: value regeneration + softmax partials for selected chunks of 32 (CUDA-core path)
 cudaError_t launch_vregen_simt(const DecodeArgs& a, cudaStream_t st);
@@ -64,6 +70,7 @@ cudaError_t launch_merge(int B, int H_q, int n_chunks, int d, const float* parti
 bool tc_score_supported(const lowram_decode_shape& s);
 bool tc_vregen_supported(const lowram_decode_shape& s);
 int tc_partial_width(const lowram_decode_shape& s);
+bool tc_fused_merge(const lowram_decode_shape& s, int n_chunks);
 constexpr int kTcChunk = 128;
 cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st);

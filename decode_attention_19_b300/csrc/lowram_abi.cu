@@ -65,7 +65,8 @@ lowram_status check_decode_shape(const lowram_decode_shape* s) {
 struct DecodeLayout {
     bool tc_score, tc_vregen;
     int chunk, n_chunks, S_eff, PW;
-    size_t off_key, off_sel, off_partial, off_sall, total;
+    bool fused_merge;
+    size_t off_key, off_sel, off_partial, off_sall, off_cnt, off_hit, total;
 };
 
 DecodeLayout decode_layout(const lowram_decode_shape& s) {
@@ -85,6 +86,11 @@ DecodeLayout decode_layout(const lowram_decode_shape& s) {
     off += align256(sizeof(float) * (size_t)s.B * s.H_q * L.n_chunks * L.PW);
     L.off_sall = off;
     off += L.tc_vregen ? align256(sizeof(float) * (size_t)s.B * s.H_q * s.T) : 0;
+    L.fused_merge = L.tc_vregen && L.n_chunks > 0 && tc_fused_merge(s, L.n_chunks);
+    L.off_cnt = off;
+    off += L.fused_merge ? align256(sizeof(int32_t) * (size_t)s.B * s.H_kv) : 0;
+    L.off_hit = off;
+    off += L.tc_vregen ? align256(sizeof(int32_t) * (size_t)s.B * s.H_kv * L.S_eff) : 0;
     L.total = off;
     return L;
 }
@@ -188,6 +194,8 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     a.n_chunks = L.n_chunks;
     a.PW = L.PW;
     a.sall = L.tc_vregen ? (float*)(ws + L.off_sall) : nullptr;
+    a.cnt = L.fused_merge ? (int32_t*)(ws + L.off_cnt) : nullptr;
+    a.hit = (L.tc_vregen && s.n_res > 0) ? (int32_t*)(ws + L.off_hit) : nullptr;
     a.check = (uint32_t*)ws;
 
     // optional timing marks: before K1, after K1, after K2, after K3, after K4
@@ -199,13 +207,15 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
         e = L.tc_score ? launch_score_tc(a, cs) : launch_score_simt(a, cs);
     if (e != cudaSuccess) return cuda_fail(e, "score");
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event");
-    if ((int64_t)s.B * L.S_eff > 0) e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs);
+    if ((int64_t)s.B * L.S_eff > 0)
+        e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs, a.cnt, a.hit, res_idx, s.n_res, a.check);
     if (e != cudaSuccess) return cuda_fail(e, "select");
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event");
     if ((int64_t)s.B * L.S_eff > 0) e = L.tc_vregen ? launch_vregen_tc(a, cs) : launch_vregen_simt(a, cs);
     if (e != cudaSuccess) return cuda_fail(e, "vregen");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event");
-    if (any) {
+    const bool merged = L.fused_merge && (int64_t)s.B * L.S_eff > 0;   // K3 merged as it finished
+    if (any && !merged) {
         const int nc = (int64_t)s.B * L.S_eff > 0 ? L.n_chunks : 0;
         e = L.tc_vregen ? launch_merge_w2(a, nc, cs) : launch_merge(s.B, s.H_q, nc, s.d, a.partial, out, lse, cs);
     }

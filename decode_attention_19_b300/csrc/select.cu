@@ -8,13 +8,14 @@
 // the exact value of the n-th largest element (the threshold) and how many elements equal to it must
 // be kept; a final pass in index order keeps every element above the threshold and the
 // lowest-indexed equal ones, writing their indices ascending through a block-wide prefix sum.
-// One CTA per row; the row streams from global memory (L2) on every pass.
+// One CTA per row; rows up to 48K elements are read once into shared memory.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace lowram {
 
 constexpr int kSelThreads = 1024;
+constexpr int kSelMaxStaged = 48 * 1024;   // row elements staged in shared memory (192 KB)
 
 // Exclusive block-wide prefix sum of a 0/1 flag (one per thread), plus the block total.
 __device__ __forceinline__ int block_excl_scan(bool f, int* warp_tot, int& total) {
@@ -41,30 +42,94 @@ __device__ __forceinline__ int block_excl_scan(bool f, int* warp_tot, int& total
     return r;
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_keep, const float* __restrict__ values,
-                                                                  int32_t* __restrict__ out) {
-    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float* v = values + (int64_t)row * T;
-    int32_t* o = out + (int64_t)row * n_keep;
-    if (n_keep <= 0) return;
-    if (n_keep >= T) {
-        for (int t = tid; t < T; t += kSelThreads) o[t] = t;
-        return;
+// Residual lookup for the value pass: hit[row][j] = the position of token o[j] in the row's ascending
+// residual list, or -1.  The list is checked (in range, strictly ascending; LOWRAM_CHECK_RES_INDEX on
+// failure) and, when staged, copied into shared memory (free once the selection is written) for the
+// binary searches.
+struct SelectExtras {
+    int32_t* zero_cnt;        // [rows] set to 0, or null
+    int32_t* hit;             // [rows][n_keep] residual row of each kept token, or null
+    const int32_t* res_idx;   // [rows][n_res] ascending residual token indices
+    int n_res;
+    uint32_t* check;
+};
+
+template <bool Staged>
+__device__ void match_residuals(int T, int n_keep, const int32_t* o, const SelectExtras& x, int row, uint32_t* staged) {
+    const int tid = threadIdx.x;
+    const int32_t* ri = x.res_idx + (int64_t)row * x.n_res;
+    const bool in_smem = Staged && x.n_res <= kSelMaxStaged;
+    __syncthreads();   // the kept indices o[] (global) and the staged keys are complete
+    bool bad = false;
+    for (int j = tid; j < x.n_res; j += kSelThreads) {
+        const int v = ri[j];
+        bad |= v < 0 || v >= T || (j > 0 && v <= ri[j - 1]);
+        if (in_smem) staged[j] = (uint32_t)v;
     }
+    if (bad) flag(x.check, LOWRAM_CHECK_RES_INDEX);
+    __syncthreads();
+    int32_t* hit = x.hit + (int64_t)row * n_keep;
+    for (int j = tid; j < n_keep; j += kSelThreads) {
+        const int tok = o[j];
+        int lo = 0, hi = x.n_res - 1, found = -1;
+        while (lo <= hi) {
+            const int mid = (lo + hi) >> 1;
+            const int v = in_smem ? (int)staged[mid] : ri[mid];
+            if (v == tok) {
+                found = mid;
+                break;
+            }
+            if (v < tok) lo = mid + 1;
+            else hi = mid - 1;
+        }
+        hit[j] = found;
+    }
+}
+
+// Staged: the row's order keys are copied into shared memory once and every pass reads them there (rows of
+// up to kSelMaxStaged elements); otherwise each pass streams the row from global memory (L2).  Histograms
+// are kept per warp, which spreads the atomics of the first digit (few distinct exponents) over 32 copies.
+template <bool Staged>
+__global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_keep, const float* __restrict__ values,
+                                                                  int32_t* __restrict__ out, SelectExtras x) {
+    extern __shared__ uint32_t staged[];
+    __shared__ uint32_t whist[kSelThreads / 32][256];
     __shared__ uint32_t hist[256];
     __shared__ uint32_t s_prefix;
     __shared__ int s_need;
     __shared__ int warp_tot[33];
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* v = values + (int64_t)row * T;
+    int32_t* o = out + (int64_t)row * n_keep;
+    if (x.zero_cnt && tid == 0) x.zero_cnt[row] = 0;
+    if (n_keep <= 0) return;
+    if (n_keep >= T) {
+        for (int t = tid; t < T; t += kSelThreads) o[t] = t;
+        if (x.hit) match_residuals<Staged>(T, n_keep, o, x, row, staged);
+        return;
+    }
+    if (Staged) {
+        for (int t = tid; t < T; t += kSelThreads) staged[t] = order_key(v[t]);
+        __syncthreads();
+    }
+    auto key_at = [&](int t) -> uint32_t { return Staged ? staged[t] : order_key(v[t]); };
 
     uint32_t prefix = 0, mask = 0;
     int need = n_keep;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+        for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&whist[0][0])[i] = 0;
         __syncthreads();
         for (int t = tid; t < T; t += kSelThreads) {
-            uint32_t u = order_key(v[t]);
-            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+            const uint32_t u = key_at(t);
+            if ((u & mask) == prefix) atomicAdd(&whist[warp][(u >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid < 256) {
+            uint32_t c = 0;
+#pragma unroll 8
+            for (int w = 0; w < kSelThreads / 32; ++w) c += whist[w][tid];
+            hist[tid] = c;
         }
         __syncthreads();
         if (warp == 0) {
@@ -74,9 +139,9 @@ __global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_k
             for (int j = 0; j < 8; ++j) mine += hist[lane * 8 + j];
             uint32_t suf = mine;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t x = __shfl_down_sync(0xffffffffu, suf, o);
-                if (lane + o < 32) suf += x;
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                uint32_t x = __shfl_down_sync(0xffffffffu, suf, o2);
+                if (lane + o2 < 32) suf += x;
             }
             bool hit = suf >= (uint32_t)need && suf - mine < (uint32_t)need;
             unsigned bal = __ballot_sync(0xffffffffu, hit);
@@ -104,7 +169,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_k
     int taken = 0, eq_seen = 0;
     for (int base = 0; base < T; base += kSelThreads) {
         const int t = base + tid;
-        const uint32_t u = t < T ? order_key(v[t]) : 0u;
+        const uint32_t u = t < T ? key_at(t) : 0u;
         const bool eq = t < T && u == prefix;
         int eq_total;
         const int eq_rank = eq_seen + block_excl_scan(eq, warp_tot, eq_total);
@@ -115,13 +180,24 @@ __global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_k
         taken += take_total;
         eq_seen += eq_total;
     }
+    if (x.hit) match_residuals<Staged>(T, n_keep, o, x, row, staged);
 }
 
 size_t select_scratch_bytes(int, int, int) { return 0; }
 
-cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, int32_t* out, cudaStream_t st) {
-    if (P == 0 || n_keep <= 0) return cudaSuccess;
-    select_topn_kernel<<<(unsigned)P, kSelThreads, 0, st>>>(T, n_keep, values, out);
+cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, int32_t* out, cudaStream_t st,
+                               int32_t* zero_cnt, int32_t* hit, const int32_t* res_idx, int n_res, uint32_t* check) {
+    if (P == 0) return cudaSuccess;
+    const SelectExtras x{zero_cnt, (hit && n_res > 0) ? hit : nullptr, res_idx, n_res, check};
+    if (n_keep > 0 && T <= kSelMaxStaged) {
+        const size_t smem = sizeof(uint32_t) * (size_t)T;   // also holds the residual list (n_res <= T)
+        cudaError_t e = cudaFuncSetAttribute(select_topn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(sizeof(uint32_t) * kSelMaxStaged));
+        if (e != cudaSuccess) return e;
+        select_topn_kernel<true><<<(unsigned)P, kSelThreads, smem, st>>>(T, n_keep, values, out, x);
+    } else {
+        select_topn_kernel<false><<<(unsigned)P, kSelThreads, 0, st>>>(T, n_keep, values, out, x);
+    }
     return cudaGetLastError();
 }
 

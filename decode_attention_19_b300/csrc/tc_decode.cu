@@ -1,23 +1,30 @@
-// tc_decode.cu -- tensor-core (tcgen05) kernels of the decode path for bf16 caches.
+// tc_decode.cu -- tensor-core (tcgen05) key pass of the decode path for bf16 caches (K1).
 //
-// K1 score_tc: selection keys of every stored token.  Rebuilding the pre-RoPE keys from the low-rank
-// factors ("Asymmetric key compression with xKV", LowRAM Paper: Amortised Values and Low-Rank Keys for
-// KV Compression) is a dense [tokens x r] . [r x H_kv*d] product, the dominant cost of a decode call, so
-// it runs on the tensor cores; RoPE ("re-applied during attention", same section), the q.k scores of the
-// q-heads sharing each kv-head and their maximum (this library's exact-score selection key) are fused
-// into the epilogue that reads the accumulators out of TMEM.
+// Selection keys of every stored token.  Rebuilding the pre-RoPE keys from the low-rank factors
+// ("Asymmetric key compression with xKV", LowRAM Paper: Amortised Values and Low-Rank Keys for KV
+// Compression) is a dense [tokens x r] . [r x H_kv*d] product, the dominant cost of a decode call, so it
+// runs on the tensor cores; RoPE ("re-applied during attention", same section), the q.k scores of the
+// q-heads sharing each kv-head and their maximum (this library's exact-score selection key) are fused into
+// the epilogue that reads the accumulators out of TMEM.  Every q-head's scaled logit is stored too: the
+// value pass takes the softmax of the selected tokens from exactly the scores the selection saw.
 //
-// Shape of the kernel (persistent, one CTA per SM, 320 threads):
-//   warp 0      TMA producer: the 128-token latent tile [128 x r] (r/64 chunks of 16 KB, 128B swizzle,
-//               resident for the whole tile) and a ring of basis chunks [256 features x 64] (32 KB each).
-//   warp 1      TMEM owner (512 columns) and MMA issuer (one thread): per pair of kv-heads, M=128, N=256,
-//               K=r in r/16 tcgen05.mma steps into one of two 256-column accumulators.
-//   warps 2-9   epilogue: warp w reads TMEM lane quarter w%4 (32 tokens), head (w-2)/4 of the pair; one
-//               thread holds one token's 128 features, applies RoPE from the cos/sin tables, forms the g
-//               dot products with q and writes their maximum.  The accumulator is released as soon as it
-//               has been read, so the next pair's MMAs overlap the arithmetic.
+// Shape of the kernel (persistent, one CTA per SM, 320 threads; each CTA takes a contiguous range of
+// 128-token tiles, so the sequence -- and the query -- rarely changes inside a CTA):
+//   warp 0      TMA producer: a ring of NS stages, each one 64-wide k-chunk of the 128-token latent tile and
+//               of the unit's basis rows [UN x 64].  The latent tile is re-read from L2 for every unit rather
+//               than kept resident: the freed shared memory holds a deeper ring, and the basis stream, not the
+//               latent tile, is what the pass waits on (L2 latency x bytes in flight).
+//   warp 1      TMEM owner and MMA issuer (one thread): per unit of UN/128 kv-heads, M=128, N=UN, K=r in
+//               r/16 tcgen05.mma steps into one of two UN-column accumulators.
+//   warps 2-9   epilogue, two groups of four warps taking alternate units (so one group's arithmetic overlaps
+//               the other's and the next unit's MMAs).  Warp w reads TMEM lane quarter w%4: one thread holds
+//               one token and, per 8 rotary frequencies, rotates the unit's heads and accumulates the dot
+//               products with the queries.  Per tile the token's cos/sin are fetched once (64 independent
+//               loads per thread) into shared memory and reused by every unit; the queries sit pre-scaled in
+//               float32 in shared memory.  Table fetches inside the unit loop would each be an L2 round trip
+//               on the critical path.
 // Every wait is bounded (see tc_common.cuh); on a timeout the kernel flags LOWRAM_CHECK_TIMEOUT, drains
-// the copies and MMAs it issued and returns.
+// the copies and MMAs it issued and returns.  The epilogue's named barriers are reached on every path.
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -30,13 +37,11 @@ namespace {
 constexpr int kTokTile = 128;
 constexpr int kChunkK = 64;                    // bf16 per 128-byte row
 constexpr int kAChunkBytes = kTokTile * 128;   // 16 KB
-constexpr int kPairN = 256;                    // basis rows per MMA (two heads of 128)
-constexpr int kBStageBytes = kPairN * 128;     // 32 KB
 constexpr int kScoreThreads = 320;
 constexpr int kSmemLimit = 232448;
 
 struct ScoreTcParams {
-    int B, T, H_q, H_kv, r, max_pos, tiles_per_seq, n_tiles, KC, NP, NS;
+    int B, T, H_q, H_kv, r, max_pos, tiles_per_seq, n_tiles, KC, NU, NS;
     float scale;
     const __nv_bfloat16* q;
     const int32_t* pos;
@@ -47,21 +52,27 @@ struct ScoreTcParams {
     uint32_t* check;
 };
 
-size_t score_smem_bytes(int KC, int NS) {
-    return 1024 + (size_t)KC * kAChunkBytes + (size_t)NS * kBStageBytes + 8 * (2 * KC + 2 * NS + 5) + 16;
+// Stage s of the ring: one 64-wide k-chunk of the latent tile [128 x 64] and of the unit's basis rows
+// [UN x 64], both 128B-swizzled as TMA writes them.
+// Beside the ring: the queries of the current sequence (fp32, pre-scaled) and the cos/sin of the current
+// tile's 128 tokens for the 64 rotary frequencies (fp32, [2][64][128]).
+size_t score_smem_bytes(int NS, int UN, int H_q) {
+    return 1024 + (size_t)NS * (kAChunkBytes + UN * 128) + (size_t)H_q * 128 * 4 + 2 * 64 * 128 * 4 +
+           8 * (2 * NS + 5) + 16;
 }
 
-template <int G>
+template <int G, int HPU>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ScoreTcParams p) {
     using namespace tc;
+    constexpr int UN = HPU * 128;              // accumulator columns per unit
+    constexpr int kStage = kAChunkBytes + UN * 128;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* A = smem;
-    uint8_t* Bst = A + p.KC * kAChunkBytes;
-    uint64_t* a_full = (uint64_t*)(Bst + p.NS * kBStageBytes);
-    uint64_t* a_empty = a_full + p.KC;
-    uint64_t* b_full = a_empty + p.KC;
+    uint8_t* St = smem;
+    float* Qs = (float*)(St + p.NS * kStage);     // [H_q][128] query of the current sequence x scale
+    float* CS = Qs + p.H_q * 128;                  // [2][64][128] cos, sin of the tile's tokens
+    uint64_t* b_full = (uint64_t*)(CS + 2 * 64 * 128);
     uint64_t* b_empty = b_full + p.NS;
     uint64_t* t_full = b_empty + p.NS;
     uint64_t* t_empty = t_full + 2;
@@ -70,18 +81,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t_begin = (int)((int64_t)blockIdx.x * p.n_tiles / gridDim.x);
+    const int t_end = (int)((int64_t)(blockIdx.x + 1) * p.n_tiles / gridDim.x);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < p.KC; ++i) {
-            mbar_init(&a_full[i], 1);
-            mbar_init(&a_empty[i], 1);
-        }
         for (int i = 0; i < p.NS; ++i) {
             mbar_init(&b_full[i], 1);
             mbar_init(&b_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&t_full[i], 1);
-            mbar_init(&t_empty[i], 8 * 32);
+            mbar_init(&t_empty[i], 4 * 32);
         }
         mbar_init(m_drain, 1);
         *abort_flag = 0;
@@ -92,7 +101,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 512);
+        tmem_alloc(tmem_slot, 2 * UN);
         tmem_relinquish();
     }
     fence_before();
@@ -104,61 +113,45 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t ib = 0;
-            int it = 0, a_last = -1;     // iteration of the most recent latent-tile load
-            for (int tile = blockIdx.x; tile < p.n_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+            for (int tile = t_begin; tile < t_end && !*abort_flag; ++tile) {
                 const int b = tile / p.tiles_per_seq, t0 = (tile % p.tiles_per_seq) * kTokTile;
-                for (int pp = 0; pp < p.NP; ++pp) {
-                    for (int kc = 0; kc < p.KC; ++kc) {
-                        if (pp == 0) {
-                            if (!mbar_wait(&a_empty[kc], (it & 1) ^ 1, abort_flag)) goto produced;
-                            mbar_expect_tx(&a_full[kc], kAChunkBytes);
-                            tma_load_3d(A + kc * kAChunkBytes, &tmA, &a_full[kc], kc * kChunkK, t0, b);
-                            a_last = it;
-                        }
+                for (int u = 0; u < p.NU; ++u) {
+                    for (int kc = 0; kc < p.KC; ++kc, ++ib) {
                         const uint32_t s = ib % p.NS, ph = (ib / p.NS) & 1;
                         if (!mbar_wait(&b_empty[s], ph ^ 1, abort_flag)) goto produced;
-                        mbar_expect_tx(&b_full[s], kBStageBytes);
-                        tma_load_2d(Bst + s * kBStageBytes, &tmB, &b_full[s], kc * kChunkK, pp * kPairN);
-                        ++ib;
+                        mbar_expect_tx(&b_full[s], kStage);
+                        tma_load_3d(St + s * kStage, &tmA, &b_full[s], kc * kChunkK, t0, b);
+                        tma_load_2d(St + s * kStage + kAChunkBytes, &tmB, &b_full[s], kc * kChunkK, u * UN);
                     }
                 }
             }
         produced:
-            if (*abort_flag) {
-                // drain: every copy issued lands before the CTA exits (chunks of the latest tile were loaded
-                // in that tile's iteration, or not at all if the producer stopped before them)
+            if (*abort_flag)   // stages older than the last NS were consumed by MMAs, so they have landed
                 for (uint32_t k = (ib > (uint32_t)p.NS ? ib - p.NS : 0); k < ib; ++k)
                     mbar_wait_drain(&b_full[k % p.NS], (k / p.NS) & 1);
-                if (a_last >= 0)
-                    for (int kc = 0; kc < p.KC; ++kc) mbar_wait_drain(&a_full[kc], a_last & 1);
-            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(kTokTile, kPairN);
+            const uint32_t idesc = idesc_bf16(kTokTile, UN);
             uint32_t ib = 0, j = 0;
-            int it = 0;
-            for (int tile = blockIdx.x; tile < p.n_tiles && !*abort_flag; tile += gridDim.x, ++it) {
-                for (int pp = 0; pp < p.NP; ++pp, ++j) {
+            for (int tile = t_begin; tile < t_end && !*abort_flag; ++tile) {
+                for (int u = 0; u < p.NU; ++u, ++j) {
                     const uint32_t buf = j & 1;
                     if (!mbar_wait(&t_empty[buf], ((j >> 1) & 1) ^ 1, abort_flag)) goto issued;
                     fence_after();
-                    const uint32_t d_tmem = tmem + buf * kPairN;
-                    for (int kc = 0; kc < p.KC; ++kc) {
-                        if (pp == 0 && !mbar_wait(&a_full[kc], it & 1, abort_flag)) goto issued;
+                    const uint32_t d_tmem = tmem + buf * UN;
+                    for (int kc = 0; kc < p.KC; ++kc, ++ib) {
                         const uint32_t s = ib % p.NS, ph = (ib / p.NS) & 1;
                         if (!mbar_wait(&b_full[s], ph, abort_flag)) goto issued;
                         fence_after();
-                        const uint32_t a_addr = smem_u32(A + kc * kAChunkBytes);
-                        const uint32_t b_addr = smem_u32(Bst + s * kBStageBytes);
+                        const uint32_t a_addr = smem_u32(St + s * kStage);
+                        const uint32_t b_addr = a_addr + kAChunkBytes;
 #pragma unroll
                         for (int k = 0; k < kChunkK / 16; ++k)
                             mma_bf16(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), idesc,
                                      (kc | k) != 0);
                         mma_commit(&b_empty[s]);
-                        if (pp == p.NP - 1) mma_commit(&a_empty[kc]);
-                        ++ib;
                     }
                     mma_commit(&t_full[buf]);
                 }
@@ -170,61 +163,125 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue
-        const int e = warp - 2;
+        const int et = threadIdx.x - 64;
+        const int grp = (warp - 2) >> 2;
         const int quarter = warp & 3;
-        const int half = e >> 2;
         const int row = quarter * 32 + lane;
+        const int64_t mp = p.max_pos;
         uint32_t j = 0;
-        for (int tile = blockIdx.x; tile < p.n_tiles && !*abort_flag; tile += gridDim.x) {
+        int cur_b = -1;
+        // no abort test in the loop conditions: every epilogue thread walks the same tiles and reaches the
+        // same named barriers; after an abort the waits fail at once and the work is skipped
+        for (int tile = t_begin; tile < t_end; ++tile) {
             const int b = tile / p.tiles_per_seq, t0 = (tile % p.tiles_per_seq) * kTokTile;
             const int t = t0 + row;
             int ps = 0;
             if (t < p.T) {
                 ps = p.pos ? p.pos[(int64_t)b * p.T + t] : t;
                 if (ps < 0 || ps >= p.max_pos) {
-                    flag(p.check, LOWRAM_CHECK_POS_RANGE);
+                    if (grp == 0) flag(p.check, LOWRAM_CHECK_POS_RANGE);
                     ps = ps < 0 ? 0 : p.max_pos - 1;
                 }
             }
-            for (int pp = 0; pp < p.NP; ++pp, ++j) {
+            named_bar_sync(1, 256);          // every epilogue thread is done with the previous tile
+            if (!*abort_flag) {
+                if (b != cur_b) {
+                    const __nv_bfloat16* qb = p.q + (int64_t)b * p.H_q * 128;
+                    for (int e = et; e < p.H_q * 128; e += 256) Qs[e] = __bfloat162float(qb[e]) * p.scale;
+                }
+                // this row's cos/sin, half of the frequencies per group: 64 independent loads in flight
+                float cv[32], sv[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    cv[k] = __ldg(p.rcos + (int64_t)(grp * 32 + k) * mp + ps);
+                    sv[k] = __ldg(p.rsin + (int64_t)(grp * 32 + k) * mp + ps);
+                }
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    CS[(grp * 32 + k) * 128 + row] = cv[k];
+                    CS[(64 + grp * 32 + k) * 128 + row] = sv[k];
+                }
+            }
+            cur_b = b;
+            named_bar_sync(1, 256);
+            for (int u = 0; u < p.NU; ++u, ++j) {
+                if ((int)(j & 1) != grp) continue;
                 const uint32_t buf = j & 1;
-                if (!mbar_wait(&t_full[buf], (j >> 1) & 1, abort_flag)) break;
+                if (!mbar_wait(&t_full[buf], (j >> 1) & 1, abort_flag)) continue;
                 fence_after();
-                const int h = pp * 2 + half;
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * kPairN + half * 128;
-                const __nv_bfloat16* qh = p.q + ((int64_t)b * p.H_q + h * G) * 128;   // same for all lanes
-                float acc[G];
+                const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + buf * UN;
+                float acc[HPU][G];
 #pragma unroll
-                for (int jq = 0; jq < G; ++jq) acc[jq] = 0.0f;
+                for (int hx = 0; hx < HPU; ++hx)
+#pragma unroll
+                    for (int jq = 0; jq < G; ++jq) acc[hx][jq] = 0.0f;
 #pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    float x[32], y[32];
-                    tmem_ld_2x32(taddr + c * 32, taddr + 64 + c * 32, x, y);
+                for (int c = 0; c < 8; ++c) {       // rotary frequencies c*8 .. c*8+7
+                    float cc[8], ss[8];
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int i = c * 32 + jj;
-                        const float cs = __ldg(p.rcos + (int64_t)i * p.max_pos + ps);
-                        const float sn = __ldg(p.rsin + (int64_t)i * p.max_pos + ps);
-                        const float kx = x[jj] * cs - y[jj] * sn;
-                        const float ky = y[jj] * cs + x[jj] * sn;
+                    for (int k = 0; k < 8; ++k) {
+                        cc[k] = CS[(c * 8 + k) * 128 + row];
+                        ss[k] = CS[(64 + c * 8 + k) * 128 + row];
+                    }
+                    float x[HPU][8], y[HPU][8];
+                    if (HPU == 2)
+                        tmem_ld_4x8(tb + c * 8, tb + 64 + c * 8, tb + 128 + c * 8, tb + 192 + c * 8, x[0], y[0],
+                                    x[HPU - 1], y[HPU - 1]);
+                    else
+                        tmem_ld_2x8(tb + c * 8, tb + 64 + c * 8, x[0], y[0]);
+#pragma unroll
+                    for (int hx = 0; hx < HPU; ++hx)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float kx = x[hx][k] * cc[k] - y[hx][k] * ss[k];
+                            const float ky = y[hx][k] * cc[k] + x[hx][k] * ss[k];
+                            x[hx][k] = kx;
+                            y[hx][k] = ky;
+                        }
+#pragma unroll
+                    for (int hx = 0; hx < HPU; ++hx)
 #pragma unroll
                         for (int jq = 0; jq < G; ++jq) {
-                            acc[jq] = fmaf(__bfloat162float(__ldg(qh + jq * 128 + i)), kx, acc[jq]);
-                            acc[jq] = fmaf(__bfloat162float(__ldg(qh + jq * 128 + i + 64)), ky, acc[jq]);
+                            const float* qv = Qs + ((u * HPU + hx) * G + jq) * 128 + c * 8;
+                            const float4 q0 = *reinterpret_cast<const float4*>(qv);
+                            const float4 q1 = *reinterpret_cast<const float4*>(qv + 4);
+                            const float4 q2 = *reinterpret_cast<const float4*>(qv + 64);
+                            const float4 q3 = *reinterpret_cast<const float4*>(qv + 68);
+                            float a = acc[hx][jq];
+                            a = fmaf(q0.x, x[hx][0], a);
+                            a = fmaf(q0.y, x[hx][1], a);
+                            a = fmaf(q0.z, x[hx][2], a);
+                            a = fmaf(q0.w, x[hx][3], a);
+                            a = fmaf(q1.x, x[hx][4], a);
+                            a = fmaf(q1.y, x[hx][5], a);
+                            a = fmaf(q1.z, x[hx][6], a);
+                            a = fmaf(q1.w, x[hx][7], a);
+                            a = fmaf(q2.x, y[hx][0], a);
+                            a = fmaf(q2.y, y[hx][1], a);
+                            a = fmaf(q2.z, y[hx][2], a);
+                            a = fmaf(q2.w, y[hx][3], a);
+                            a = fmaf(q3.x, y[hx][4], a);
+                            a = fmaf(q3.y, y[hx][5], a);
+                            a = fmaf(q3.z, y[hx][6], a);
+                            a = fmaf(q3.w, y[hx][7], a);
+                            acc[hx][jq] = a;
                         }
-                    }
                 }
                 fence_before();
                 mbar_arrive(&t_empty[buf]);
-                float best = -INFINITY;
-#pragma unroll
-                for (int jq = 0; jq < G; ++jq) best = fmaxf(best, acc[jq] * p.scale);
                 if (t < p.T) {
-                    p.key[((int64_t)b * p.H_kv + h) * p.T + t] = best;
-                    if (p.sall)
 #pragma unroll
-                        for (int jq = 0; jq < G; ++jq)
-                            p.sall[((int64_t)b * p.H_q + h * G + jq) * p.T + t] = acc[jq] * p.scale;
+                    for (int hx = 0; hx < HPU; ++hx) {
+                        const int h = u * HPU + hx;
+                        float best = -INFINITY;
+#pragma unroll
+                        for (int jq = 0; jq < G; ++jq) best = fmaxf(best, acc[hx][jq]);
+                        p.key[((int64_t)b * p.H_kv + h) * p.T + t] = best;
+                        if (p.sall)
+#pragma unroll
+                            for (int jq = 0; jq < G; ++jq)
+                                p.sall[((int64_t)b * p.H_q + h * G + jq) * p.T + t] = acc[hx][jq];
+                    }
                 }
             }
         }
@@ -236,7 +293,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (*abort_flag && threadIdx.x == 0) flag(p.check, LOWRAM_CHECK_TIMEOUT);
     if (warp == 1) {
         fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, 2 * UN);
     }
 }
 
@@ -247,10 +304,17 @@ using tc::encode_fn;
 using tc::make_map;
 using tc::sm_count;
 
-int stages_for(int KC) {
-    for (int ns = 4; ns >= 2; --ns)
-        if (score_smem_bytes(KC, ns) <= (size_t)kSmemLimit) return ns;
-    return 0;
+// Unit width (basis rows per MMA) and ring depth: two heads per unit when the kv-heads pair up, else one;
+// as many stages as fit beside the queries.
+struct ScoreConfig {
+    int UN, NS;
+};
+
+ScoreConfig score_config(int H_q, int H_kv) {
+    const int UN = (H_kv % 2 == 0 && H_q / H_kv != 8) ? 256 : 128;   // two heads of eight queries: registers
+    for (int ns = 8; ns >= 2; --ns)
+        if (score_smem_bytes(ns, UN, H_q) <= (size_t)kSmemLimit) return {UN, ns};
+    return {0, 0};
 }
 
 bool g_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 7 || g == 8; }
@@ -259,11 +323,10 @@ bool g_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 7 || g == 8; }
 
 bool tc_score_supported(const lowram_decode_shape& s) {
     const int g = s.H_q / s.H_kv;
-    return s.act_dtype == LOWRAM_BF16 && s.coef_dtype == LOWRAM_BF16 && s.d == 128 && (s.H_kv * s.d) % kPairN == 0 &&
-           s.r % kChunkK == 0 && s.r <= 640 && g_ok(g) && s.T > 0 && stages_for(s.r / kChunkK) >= 2 &&
+    return s.act_dtype == LOWRAM_BF16 && s.coef_dtype == LOWRAM_BF16 && s.d == 128 && s.r % kChunkK == 0 &&
+           s.r <= 1024 && g_ok(g) && s.T > 0 && score_config(s.H_q, s.H_kv).NS >= 2 &&
            encode_fn() != nullptr;
 }
-
 
 cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     const auto& s = a.s;
@@ -277,8 +340,9 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     p.tiles_per_seq = (int)cdiv(s.T, kTokTile);
     p.n_tiles = p.tiles_per_seq * s.B;
     p.KC = s.r / kChunkK;
-    p.NP = s.H_kv * s.d / kPairN;
-    p.NS = stages_for(p.KC);
+    const ScoreConfig cfg = score_config(s.H_q, s.H_kv);
+    p.NU = s.H_kv * s.d / cfg.UN;
+    p.NS = cfg.NS;
     p.scale = a.scale;
     p.q = (const __nv_bfloat16*)a.q;
     p.pos = a.pos;
@@ -288,13 +352,14 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     p.sall = a.sall;
     p.check = a.check;
     if (p.n_tiles == 0) return cudaSuccess;
+    if (cfg.NS < 2) return cudaErrorNotSupported;
     CUtensorMap mA, mB;
     const uint64_t dA[3] = {(uint64_t)s.r, (uint64_t)s.T, (uint64_t)s.B};
     const uint32_t bA[3] = {kChunkK, kTokTile, 1};
     const uint64_t dB[2] = {(uint64_t)s.r, (uint64_t)s.H_kv * s.d};
-    const uint32_t bB[2] = {kChunkK, kPairN};
+    const uint32_t bB[2] = {kChunkK, (uint32_t)cfg.UN};
     if (!make_map(&mA, a.coef, 3, dA, bA) || !make_map(&mB, a.basis, 2, dB, bB)) return cudaErrorInvalidValue;
-    const size_t smem = score_smem_bytes(p.KC, p.NS);
+    const size_t smem = score_smem_bytes(p.NS, cfg.UN, s.H_q);
     const int grid = std::min(p.n_tiles, sm_count());
     cudaError_t e = cudaSuccess;
     auto go = [&](auto kern) {
@@ -304,12 +369,13 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
             e = cudaGetLastError();
         }
     };
+    const bool two = cfg.UN == 256;
     switch (s.H_q / s.H_kv) {
-        case 1: go(score_tc_kernel<1>); break;
-        case 2: go(score_tc_kernel<2>); break;
-        case 4: go(score_tc_kernel<4>); break;
-        case 7: go(score_tc_kernel<7>); break;
-        case 8: go(score_tc_kernel<8>); break;
+        case 1: two ? go(score_tc_kernel<1, 2>) : go(score_tc_kernel<1, 1>); break;
+        case 2: two ? go(score_tc_kernel<2, 2>) : go(score_tc_kernel<2, 1>); break;
+        case 4: two ? go(score_tc_kernel<4, 2>) : go(score_tc_kernel<4, 1>); break;
+        case 7: two ? go(score_tc_kernel<7, 2>) : go(score_tc_kernel<7, 1>); break;
+        case 8: two ? go(score_tc_kernel<8, 2>) : go(score_tc_kernel<8, 1>); break;
         default: return cudaErrorNotSupported;
     }
     return e;

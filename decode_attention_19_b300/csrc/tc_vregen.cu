@@ -38,23 +38,27 @@ constexpr int kVThreads = 192;
 constexpr int kRows = 128;              // selected tokens per CTA
 constexpr int kStageBytes = 32768;      // latent chunk [128 x 64] + basis chunk [128 x 64], bf16
 constexpr int kHalf = 16384;
-constexpr int kSmemLimit = 232448;
+constexpr int kNS = 3;                  // ring stages; after MMA1 the ring holds the keys and w1[h]
 
 struct VregenTcParams {
-    int T, H_q, H_kv, r, m, S_eff, n_chunks, n_res, KC, NS, PW;
+    int T, H_q, H_kv, r, m, S_eff, n_chunks, n_res, KC, PW;
     const __nv_bfloat16* coef;
     const float* sall;        // [B, H_q, T] scaled logits written by the key pass
     const float* b1;          // [H_kv, m] or null
+    const float* b2;          // [H_kv, d] or null
+    const __nv_bfloat16* w2;  // [H_kv, d, m]
     const int32_t* sel;       // [B, H_kv, S_eff]
-    const int32_t* res_idx;   // [B, H_kv, n_res]
+    const int32_t* hit;       // [B, H_kv, S_eff] residual row of each selected token, or -1
     ResView res;
     float* partial;           // [B, H_q, n_chunks, PW]
+    int32_t* cnt;             // [B, H_kv] chunks finished per (b, h); zeroed by the selection kernel
+    float* out;               // [B, H_q, d]
+    float* lse;               // [B, H_q] or null
     uint32_t* check;
 };
 
-size_t vregen_smem_bytes(int NS, int m) {
-    return 1024 + (size_t)NS * kStageBytes + (size_t)m * 256 + 8 * 128 * 4 + 2 * 128 * 4 + 64 * 4 +
-           8 * (3 * NS + 5) + 16;
+size_t vregen_smem_bytes() {
+    return 1024 + (size_t)kNS * kStageBytes + 8 * 128 * 4 + 3 * 128 * 4 + 72 * 4 + 8 * (3 * kNS + 5) + 16;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -67,6 +71,100 @@ __device__ __forceinline__ void st_shared_16(uint8_t* p, uint32_t a, uint32_t b,
                  : "memory");
 }
 
+// The last CTA of a (sequence, kv-head) to finish merges the chunks' partials of its G q-heads (threads =
+// the 128 epilogue threads, et = 0..127): W = max_c M_c, w_c = exp(M_c - W), L = sum_c w_c l_c,
+// out = w2[h] (sum_c w_c z_c / L) + b2[h] + sum_c w_c rz_c / L,  lse = W + log L.
+// The G q-heads' records are contiguous; they are copied into shared memory with batches of independent
+// 16-byte loads, all G at once when they fit, else one q-head at a time.
+template <int G>
+__device__ __forceinline__ void merge_last(const VregenTcParams& p, int b, int h, int et, float* scratch) {
+    const int64_t qstride = (int64_t)p.n_chunks * p.PW;
+    const float* P0 = p.partial + ((int64_t)b * p.H_q + h * G) * qstride;
+    const int ZW = p.m + 128;
+    float* Z = scratch;                          // [G][m + 128] merged hidden sums, then residual sums
+    float* Pb = scratch + G * ZW;                // [G][n_chunks][PW] staged records
+    // all G q-heads' records at once when they fit beside Z, else one q-head at a time (tc_fused_merge
+    // guarantees one fits)
+    const int per = (G * (qstride + ZW) * sizeof(float) <= (size_t)kNS * kStageBytes) ? G : 1;
+    float M[G], L[G];
+    for (int q0 = 0; q0 < G; q0 += per) {
+        {   // copy records of q-heads q0 .. q0+per-1: batches of 8 independent 16-byte loads per thread
+            const float4* src = reinterpret_cast<const float4*>(P0 + q0 * qstride);
+            float4* d4 = reinterpret_cast<float4*>(Pb);
+            const int n4 = (int)(per * qstride / 4);
+            for (int i0 = 0; i0 < n4; i0 += 8 * kRows) {
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * kRows + et;
+                    if (i < n4) v[u] = __ldcg(src + i);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * kRows + et;
+                    if (i < n4) d4[i] = v[u];
+                }
+            }
+            tc::named_bar_sync(1, kRows);
+        }
+#pragma unroll
+        for (int jq = 0; jq < G; ++jq) {
+            if (jq < q0 || jq >= q0 + per) continue;
+            const float* Pq = Pb + (jq - q0) * qstride;
+            float mx = -INFINITY;
+            for (int c = 0; c < p.n_chunks; ++c) mx = fmaxf(mx, Pq[(int64_t)c * p.PW + p.m + 128]);
+            float l = 0.0f;
+            for (int c = 0; c < p.n_chunks; ++c) {
+                const float mc = Pq[(int64_t)c * p.PW + p.m + 128];
+                l = fmaf(mc == -INFINITY ? 0.0f : __expf(mc - mx), Pq[(int64_t)c * p.PW + p.m + 129], l);
+            }
+            M[jq] = mx;
+            L[jq] = l;
+            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+            for (int j = et; j < ZW; j += kRows) {
+                float acc = 0.0f;
+                for (int c = 0; c < p.n_chunks; ++c) {
+                    const float mc = Pq[(int64_t)c * p.PW + p.m + 128];
+                    if (mc != -INFINITY) acc = fmaf(__expf(mc - mx), Pq[(int64_t)c * p.PW + j], acc);
+                }
+                Z[jq * ZW + j] = acc * inv;
+            }
+        }
+        tc::named_bar_sync(1, kRows);     // Pb is reused by the next group of q-heads
+    }
+    // thread et = output feature i: the second predictor layer on the merged hidden sums
+    const __nv_bfloat16* W2 = p.w2 + ((int64_t)h * 128 + et) * p.m;
+    float acc[G];
+#pragma unroll
+    for (int jq = 0; jq < G; ++jq) acc[jq] = 0.0f;
+    for (int j0 = 0; j0 < p.m; j0 += 64) {
+        uint4 wv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) wv[u] = __ldg(reinterpret_cast<const uint4*>(W2 + j0 + u * 8));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&wv[u]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(pr[e]);
+                const int j = j0 + u * 8 + 2 * e;
+#pragma unroll
+                for (int jq = 0; jq < G; ++jq) {
+                    acc[jq] = fmaf(f.x, Z[jq * ZW + j], acc[jq]);
+                    acc[jq] = fmaf(f.y, Z[jq * ZW + j + 1], acc[jq]);
+                }
+            }
+        }
+    }
+    const float bias = p.b2 ? __ldg(p.b2 + (int64_t)h * 128 + et) : 0.0f;
+#pragma unroll
+    for (int jq = 0; jq < G; ++jq) {
+        const int64_t bhq = (int64_t)b * p.H_q + h * G + jq;
+        p.out[bhq * 128 + et] = L[jq] > 0.0f ? acc[jq] + bias + Z[jq * ZW + p.m + et] : 0.0f;
+        if (p.lse && et == jq) p.lse[bhq] = L[jq] > 0.0f ? M[jq] + logf(L[jq]) : -INFINITY;
+    }
+}
+
 template <int G>
 __global__ void __launch_bounds__(kVThreads, 2)
     vregen_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW1,
@@ -74,22 +172,24 @@ __global__ void __launch_bounds__(kVThreads, 2)
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* ring = smem;
-    uint8_t* W1s = ring + p.NS * kStageBytes;
-    float* Ps = (float*)(W1s + p.m * 256);       // [G][128] softmax weights of the chunk
+    uint8_t* ring = smem;                        // MMA1: stages; then keys [0, 32K) and w1[h] [32K, 32K + m*256)
+    uint8_t* W1s = ring + 2 * kHalf;
+    float* Ps = (float*)(ring + kNS * kStageBytes);   // [G][128] softmax weights of the chunk
     int* Tok = (int*)(Ps + 8 * kRows);           // token of each slot, -1 past the selection
-    int* Hit = Tok + kRows;                      // residual row of each slot, -1 if none
-    float* red = (float*)(Hit + kRows);          // [2][4 warps][8] partial max / sum
-    uint64_t* fullA = (uint64_t*)(red + 64);
-    uint64_t* fullB = fullA + p.NS;
-    uint64_t* empty = fullB + p.NS;
-    uint64_t* w1_full = empty + p.NS;
+    int* Hit = Tok + kRows;                      // compacted: residual rows of the chunk's slots that have one
+    int* HitSlot = Hit + kRows;                  // ... and those slots, ascending
+    float* red = (float*)(HitSlot + kRows);      // [2][4 warps][8] partial max / sum, then 4 hit counts
+    uint64_t* fullA = (uint64_t*)(red + 72);
+    uint64_t* fullB = fullA + kNS;
+    uint64_t* empty = fullB + kNS;
+    uint64_t* w1_full = empty + kNS;
     uint64_t* d1_full = w1_full + 1;
     uint64_t* kbf_full = d1_full + 1;
     uint64_t* d2_full = kbf_full + 1;
     uint64_t* m_drain = d2_full + 1;
     uint32_t* tmem_slot = (uint32_t*)(m_drain + 1);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+    volatile int* last_flag = (volatile int*)(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -97,7 +197,7 @@ __global__ void __launch_bounds__(kVThreads, 2)
     const uint32_t tcols = p.m > 128 ? 256u : 128u;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.NS; ++s) {
+        for (int s = 0; s < kNS; ++s) {
             mbar_init(&fullA[s], kRows);
             mbar_init(&fullB[s], 1);
             mbar_init(&empty[s], 1);
@@ -108,6 +208,7 @@ __global__ void __launch_bounds__(kVThreads, 2)
         mbar_init(d2_full, 1);
         mbar_init(m_drain, 1);
         *abort_flag = 0;
+        *last_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -127,22 +228,27 @@ __global__ void __launch_bounds__(kVThreads, 2)
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             int issued = 0;
-            mbar_expect_tx(w1_full, (uint32_t)p.m * 256u);
-            for (int mb = 0; mb < p.m / 128; ++mb)
-                for (int kc2 = 0; kc2 < 2; ++kc2)
-                    tma_load_2d(W1s + (mb * 2 + kc2) * kHalf, &tmW1, w1_full, kc2 * 64, h * p.m + mb * 128);
+            bool w1_issued = false;
             for (int kc = 0; kc < p.KC; ++kc) {
-                const int s = kc % p.NS, n = kc / p.NS;
+                const int s = kc % kNS, n = kc / kNS;
                 if (!mbar_wait(&empty[s], (n & 1) ^ 1, abort_flag)) break;
                 mbar_expect_tx(&fullB[s], kHalf);
                 tma_load_2d(ring + s * kStageBytes + kHalf, &tmW, &fullB[s], kc * 64, h * 128);
                 ++issued;
             }
+            // w1[h] goes into the ring once MMA1 is complete
+            if (issued == p.KC && mbar_wait(d1_full, 0, abort_flag)) {
+                mbar_expect_tx(w1_full, (uint32_t)p.m * 256u);
+                for (int mb = 0; mb < p.m / 128; ++mb)
+                    for (int kc2 = 0; kc2 < 2; ++kc2)
+                        tma_load_2d(W1s + (mb * 2 + kc2) * kHalf, &tmW1, w1_full, kc2 * 64, h * p.m + mb * 128);
+                w1_issued = true;
+            }
             if (*abort_flag) {
-                // loads older than the last NS were consumed by MMAs, so they have landed
-                for (int k = issued > p.NS ? issued - p.NS : 0; k < issued; ++k)
-                    mbar_wait_drain(&fullB[k % p.NS], (k / p.NS) & 1);
-                mbar_wait_drain(w1_full, 0);
+                // loads older than the last kNS were consumed by MMAs, so they have landed
+                for (int k = issued > kNS ? issued - kNS : 0; k < issued; ++k)
+                    mbar_wait_drain(&fullB[k % kNS], (k / kNS) & 1);
+                if (w1_issued) mbar_wait_drain(w1_full, 0);
             }
         }
     } else if (warp == 1) {
@@ -151,7 +257,7 @@ __global__ void __launch_bounds__(kVThreads, 2)
             const uint32_t idesc = idesc_bf16(128, 128);
             bool ok = true;
             for (int kc = 0; kc < p.KC && ok; ++kc) {
-                const int s = kc % p.NS, n = kc / p.NS;
+                const int s = kc % kNS, n = kc / kNS;
                 if (!mbar_wait(&fullB[s], n & 1, abort_flag) || !mbar_wait(&fullA[s], n & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -188,38 +294,14 @@ __global__ void __launch_bounds__(kVThreads, 2)
         const int et = threadIdx.x - 64;
         const int quarter = warp & 3;
         const int slot = quarter * 32 + lane;   // the TMEM lane (row) this thread reads
-        float sv[G];
+        int my_tok, my_hit;
         {
             const int j = chunk * kRows + slot;
             int tok = j < p.S_eff ? p.sel[bh * p.S_eff + j] : -1;
             if (tok >= p.T) tok = p.T - 1;      // the selection is always in range; keep the invariant explicit
-            int hit = -1;
-            if (tok >= 0 && p.n_res > 0) {
-                const int32_t* ridx = p.res_idx + bh * p.n_res;
-                int lo = 0, hi = p.n_res - 1;
-                while (lo <= hi) {
-                    const int mid = (lo + hi) >> 1;
-                    const int v = __ldg(ridx + mid);
-                    if (v == tok) {
-                        hit = mid;
-                        break;
-                    }
-                    if (v < tok) lo = mid + 1;
-                    else hi = mid - 1;
-                }
-            }
+            my_hit = (j < p.S_eff && p.hit && p.n_res > 0) ? p.hit[bh * p.S_eff + j] : -1;
             Tok[slot] = tok;
-            Hit[slot] = hit;
-#pragma unroll
-            for (int jq = 0; jq < G; ++jq)
-                sv[jq] = tok >= 0 ? __ldg(p.sall + ((int64_t)b * p.H_q + h * G + jq) * p.T + tok) : -INFINITY;
-        }
-        // one CTA per (b, h) validates the residual list: in range and strictly ascending
-        if (chunk == 0) {
-            const int32_t* ridx = p.res_idx + bh * p.n_res;
-            for (int j = et; j < p.n_res; j += kRows)
-                if (ridx[j] < 0 || ridx[j] >= p.T || (j > 0 && ridx[j] <= ridx[j - 1]))
-                    flag(p.check, LOWRAM_CHECK_RES_INDEX);
+            my_tok = tok;
         }
         named_bar_sync(1, kRows);
 
@@ -228,7 +310,7 @@ __global__ void __launch_bounds__(kVThreads, 2)
         {
             const int c16 = et & 7, rsub = et >> 3;
             for (int kc = 0; kc < p.KC; ++kc) {
-                const int s = kc % p.NS, n = kc / p.NS;
+                const int s = kc % kNS, n = kc / kNS;
                 if (ok && !mbar_wait(&empty[s], (n & 1) ^ 1, abort_flag)) ok = false;
                 if (ok) {
                     const uint32_t A = smem_u32(ring + s * kStageBytes);
@@ -242,18 +324,26 @@ __global__ void __launch_bounds__(kVThreads, 2)
                     }
                 }
                 cp_async_commit();
-                if (kc > 0) {
-                    cp_async_wait<1>();
+                // up to kNS - 1 stages of gathers stay in flight; stage kc - (kNS - 1) has landed
+                if (kc >= kNS - 1) {
+                    cp_async_wait<kNS - 1>();
                     fence_proxy_async();
-                    if (ok) mbar_arrive(&fullA[(kc - 1) % p.NS]);
+                    if (ok) mbar_arrive(&fullA[(kc - (kNS - 1)) % kNS]);
                 }
             }
             cp_async_wait<0>();
             fence_proxy_async();
-            if (ok) mbar_arrive(&fullA[(p.KC - 1) % p.NS]);
+            if (ok)
+                for (int kc = (p.KC > kNS - 1 ? p.KC - (kNS - 1) : 0); kc < p.KC; ++kc) mbar_arrive(&fullA[kc % kNS]);
         }
 
-        // D1 -> bf16 pre-RoPE keys, K-major and swizzled, into the ring's first stage (MMA1 is complete)
+        // while MMA1 finishes: the scaled logits of this slot's token
+        float sv[G];
+#pragma unroll
+        for (int jq = 0; jq < G; ++jq)
+            sv[jq] = my_tok >= 0 ? __ldg(p.sall + ((int64_t)b * p.H_q + h * G + jq) * p.T + my_tok) : -INFINITY;
+
+        // D1 -> bf16 pre-RoPE keys, K-major and swizzled, into the ring's first 32 KB (MMA1 is complete)
         bool have = ok && mbar_wait(d1_full, 0, abort_flag);
         if (have) {
             fence_after();
@@ -285,7 +375,21 @@ __global__ void __launch_bounds__(kVThreads, 2)
             const float mx = warp_max(sv[jq]);
             if (lane == 0) red[quarter * 8 + jq] = mx;
         }
+        const unsigned hb = __ballot_sync(0xffffffffu, my_hit >= 0);
+        int* hcount = (int*)(red + 64);
+        if (lane == 0) hcount[quarter] = __popc(hb);
         named_bar_sync(1, kRows);
+        int n_hit;
+        {
+            int before = 0;
+            for (int w = 0; w < quarter; ++w) before += hcount[w];
+            n_hit = hcount[0] + hcount[1] + hcount[2] + hcount[3];
+            if (my_hit >= 0) {
+                const int at = before + __popc(hb & ((1u << lane) - 1u));
+                Hit[at] = my_hit;
+                HitSlot[at] = slot;
+            }
+        }
 #pragma unroll
         for (int jq = 0; jq < G; ++jq) {
             M[jq] = fmaxf(fmaxf(red[jq], red[8 + jq]), fmaxf(red[16 + jq], red[24 + jq]));
@@ -306,14 +410,18 @@ __global__ void __launch_bounds__(kVThreads, 2)
             float rz[G];
 #pragma unroll
             for (int jq = 0; jq < G; ++jq) rz[jq] = 0.0f;
-            if (p.n_res > 0)
-                for (int t = 0; t < kRows; ++t) {
-                    const int hr = Hit[t];
-                    if (hr < 0) continue;
-                    const float v = p.res.get(bh * p.n_res + hr, slot);
+            for (int k0 = 0; k0 < n_hit; k0 += 16) {    // 16 independent row loads in flight
+                float v[16];
 #pragma unroll
-                    for (int jq = 0; jq < G; ++jq) rz[jq] = fmaf(Ps[jq * kRows + t], v, rz[jq]);
+                for (int u = 0; u < 16; ++u) v[u] = k0 + u < n_hit ? p.res.get(bh * p.n_res + Hit[k0 + u], slot) : 0.0f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    if (k0 + u >= n_hit) break;
+                    const int t = HitSlot[k0 + u];
+#pragma unroll
+                    for (int jq = 0; jq < G; ++jq) rz[jq] = fmaf(Ps[jq * kRows + t], v[u], rz[jq]);
                 }
+            }
 #pragma unroll
             for (int jq = 0; jq < G; ++jq) dst[jq * jq_stride + p.m + slot] = rz[jq];
 #pragma unroll
@@ -345,8 +453,8 @@ __global__ void __launch_bounds__(kVThreads, 2)
                         float hx[4], hy[4];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            hx[u] = silu(x[tt + u] + bj);
-                            hy[u] = silu(y[tt + u] + bj);
+                            hx[u] = silu_fast(x[tt + u] + bj);
+                            hy[u] = silu_fast(y[tt + u] + bj);
                         }
 #pragma unroll
                         for (int jq = 0; jq < G; ++jq) {
@@ -366,6 +474,20 @@ __global__ void __launch_bounds__(kVThreads, 2)
 #pragma unroll
                 for (int jq = 0; jq < G; ++jq) dst[jq * jq_stride + j] = z[jq];
             }
+        }
+
+        // the last CTA of this (b, h) to finish merges the chunks (partials made visible device-wide first);
+        // without a counter array the separate merge kernel does it
+        __threadfence();
+        fence_before();
+        named_bar_sync(1, kRows);
+        if (et == 0 && p.cnt) *last_flag = (atomicAdd(p.cnt + bh, 1) == p.n_chunks - 1) ? 1 : 0;
+        named_bar_sync(1, kRows);
+        if (*last_flag) {
+            __threadfence();
+            // the ring is free: MMA2 has completed (or the call has aborted and its results are void)
+            merge_last<G>(p, b, h, et, (float*)ring);
+            if (et == 0) p.cnt[bh] = 0;
         }
     }
 
@@ -404,7 +526,7 @@ __global__ void __launch_bounds__(128) merge_w2_kernel(int H_q, int G, int n_chu
     __shared__ float red[4];
     float* wts = msm;               // [n_chunks]
     float* zb = msm + n_chunks;     // [m + 128]: merged hidden sums, then merged residual sums
-    const int bhq = blockIdx.x, h = (bhq % H_q) / G, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int bhq = blockIdx.x, h = (bhq % H_q) / G, tid = threadIdx.x;
     const float* P = partial + (int64_t)bhq * n_chunks * PW;
     float M = -INFINITY;
     for (int c = tid; c < n_chunks; c += 128) M = fmaxf(M, P[(int64_t)c * PW + m + 128]);
@@ -424,37 +546,43 @@ __global__ void __launch_bounds__(128) merge_w2_kernel(int H_q, int G, int n_chu
         zb[j] = acc * inv;
     }
     __syncthreads();
-    const __nv_bfloat16* W2 = w2 + (int64_t)h * 128 * m;
-    for (int i = warp * 32; i < warp * 32 + 32; ++i) {
-        float acc = 0.0f;
-        for (int j = lane * 2; j < m; j += 64) {
-            const __nv_bfloat162 wv = *reinterpret_cast<const __nv_bfloat162*>(W2 + (int64_t)i * m + j);
-            acc = fmaf(__low2float(wv), zb[j], acc);
-            acc = fmaf(__high2float(wv), zb[j + 1], acc);
+    // thread i: out[i] = w2[h][i, :] . zbar; the row's 16-byte pieces are independent loads
+    const __nv_bfloat16* W2 = w2 + ((int64_t)h * 128 + tid) * m;
+    float acc = 0.0f;
+    for (int j0 = 0; j0 < m; j0 += 64) {
+        uint4 wv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) wv[u] = __ldg(reinterpret_cast<const uint4*>(W2 + j0 + u * 8));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&wv[u]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(pr[e]);
+                acc = fmaf(f.x, zb[j0 + u * 8 + 2 * e], acc);
+                acc = fmaf(f.y, zb[j0 + u * 8 + 2 * e + 1], acc);
+            }
         }
-        acc = warp_sum(acc);
-        if (lane == 0)
-            out[(int64_t)bhq * 128 + i] = L > 0.0f ? acc + (b2 ? b2[(int64_t)h * 128 + i] : 0.0f) + zb[m + i] : 0.0f;
     }
+    out[(int64_t)bhq * 128 + tid] = L > 0.0f ? acc + (b2 ? b2[(int64_t)h * 128 + tid] : 0.0f) + zb[m + tid] : 0.0f;
     if (lse && tid == 0) lse[bhq] = L > 0.0f ? M + logf(L) : -INFINITY;
 }
 
-int ns_for(int m) {
-    // two CTAs per SM when they fit, else the deepest ring that fits one
-    for (int ns = 4; ns >= 2; --ns)
-        if (2 * (vregen_smem_bytes(ns, m) + 1024) <= 233472) return ns;
-    for (int ns = 4; ns >= 2; --ns)
-        if (vregen_smem_bytes(ns, m) <= (size_t)kSmemLimit) return ns;
-    return 0;
-}
 
 }  // namespace
 
 bool tc_vregen_supported(const lowram_decode_shape& s) {
-    return tc_score_supported(s) && (s.m == 128 || s.m == 256) && ns_for(s.m) >= 2;
+    return tc_score_supported(s) && (s.m == 128 || s.m == 256) && s.d == 128;
 }
 
 int tc_partial_width(const lowram_decode_shape& s) { return s.m + s.d + 4; }
+
+// The last CTA of each (sequence, kv-head) merges in the value kernel when the merge's shared scratch
+// (chunk weights and merged sums of the G q-heads) fits in the ring.
+bool tc_fused_merge(const lowram_decode_shape& s, int n_chunks) {
+    const size_t g = s.H_q / s.H_kv, zw = s.m + 128, pw = tc_partial_width(s);
+    return (g * zw + (size_t)n_chunks * pw) * sizeof(float) <= (size_t)kNS * kStageBytes;
+}
 
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     const auto& s = a.s;
@@ -468,15 +596,19 @@ cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     p.n_chunks = a.n_chunks;
     p.n_res = s.n_res;
     p.KC = s.r / 64;
-    p.NS = ns_for(s.m);
     p.PW = a.PW;
     p.coef = (const __nv_bfloat16*)a.coef;
     p.sall = a.sall;
     p.b1 = a.b1;
+    p.b2 = a.b2;
+    p.w2 = (const __nv_bfloat16*)a.w2;
     p.sel = a.sel;
-    p.res_idx = a.res_idx;
+    p.hit = a.hit;
     p.res = ResView{s.res_dtype, a.res_val, (const __half*)a.res_scale, s.d};
     p.partial = a.partial;
+    p.cnt = a.cnt;
+    p.out = a.out;
+    p.lse = a.lse;
     p.check = a.check;
     if ((int64_t)s.B * a.n_chunks == 0) return cudaSuccess;
     CUtensorMap mW, mW1;
@@ -485,7 +617,7 @@ cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     const uint64_t dW1[2] = {(uint64_t)s.d, (uint64_t)s.H_kv * s.m};
     const uint32_t bW1[2] = {64, 128};
     if (!tc::make_map(&mW, a.basis, 2, dW, bW) || !tc::make_map(&mW1, a.w1, 2, dW1, bW1)) return cudaErrorInvalidValue;
-    const size_t smem = vregen_smem_bytes(p.NS, s.m);
+    const size_t smem = vregen_smem_bytes();
     dim3 grid((unsigned)a.n_chunks, (unsigned)s.H_kv, (unsigned)s.B);
     cudaError_t e = cudaSuccess;
     auto go = [&](auto kern) {
