@@ -3,23 +3,34 @@
 // path.  This is the cache the compressed one replaces (LowRAM abstract: the KV cache's memory
 // footprint caps batch size and throughput).
 //
-// HBM-bound: every K and V byte is read once with 16-byte loads.  A group of d/VEC lanes holds one
-// token (VEC elements per lane); the lanes of a group reduce the q.k dot products with xor shuffles
-// and keep an online softmax state per q-head; groups, then warps, merge their states at the end.
+// HBM-bound: every K and V byte is read once, 16 bytes per lane, streamed through a per-thread cp.async
+// ring in shared memory.  A group of d/VEC lanes holds one token (VEC elements per lane); the lanes of a
+// group reduce the q.k dot products with xor shuffles and keep an online softmax state per q-head;
+// groups, then warps, merge their states at the end.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace lowram {
 
 constexpr int kDenseThreads = 128;
+constexpr int kDenseU = 4;        // token steps per iteration
+constexpr int kDenseStages = 4;   // iterations of loads in flight
+constexpr size_t kDenseSmem = (size_t)kDenseStages * kDenseU * 2 * kDenseThreads * 16;
 
+// 16-byte global -> shared copy through L2; zero-filled when !ok.
+__device__ __forceinline__ void cp_async16(uint4* dst, const void* src, bool ok) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(ok ? 16u : 0u)
+                 : "memory");
+}
+
+// 16-byte pieces of a row converted to float.
 template <typename TE>
 struct Vec16;
 template <>
 struct Vec16<__nv_bfloat16> {
     static constexpr int N = 8;
-    __device__ __forceinline__ static void load(const __nv_bfloat16* p, float (&x)[8]) {
-        uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    __device__ __forceinline__ static void cvt(const uint4& u, float (&x)[8]) {
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -32,9 +43,8 @@ struct Vec16<__nv_bfloat16> {
 template <>
 struct Vec16<float> {
     static constexpr int N = 4;
-    __device__ __forceinline__ static void load(const float* p, float (&x)[4]) {
-        float4 u = __ldg(reinterpret_cast<const float4*>(p));
-        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    __device__ __forceinline__ static void cvt(const uint4& u, float (&x)[4]) {
+        x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y); x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
     }
 };
 
@@ -59,7 +69,7 @@ __global__ void __launch_bounds__(kDenseThreads) dense_kernel(int T, int H_q, in
     constexpr int LPT = D / VEC;          // lanes per token
     constexpr int TPW = 32 / LPT;         // tokens per warp step
     constexpr int NW = kDenseThreads / 32;
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, grp = lane / LPT, sub = lane % LPT;
     const int per = (int)cdiv(T, n_split);
     const int t_begin = split * per, t_end = min(T, t_begin + per);
@@ -78,34 +88,63 @@ __global__ void __launch_bounds__(kDenseThreads) dense_kernel(int T, int H_q, in
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[j][e] = 0.0f;
     }
-    for (int t0 = t_begin + warp * TPW; t0 < t_end; t0 += NW * TPW) {
-        const int t = t0 + grp;
-        const bool valid = t < t_end;
-        float kx[VEC], vx[VEC];
-        if (valid) {
-            const int64_t off = (((int64_t)b * T + t) * H_kv + h) * D + sub * VEC;
-            Vec16<TE>::load(K + off, kx);
-            Vec16<TE>::load(V + off, vx);
+    // Deep pipeline without registers: every thread streams exactly the 16-byte pieces of K and V it will
+    // use into its own shared-memory slots with cp.async, kDenseStages iterations ahead of the arithmetic,
+    // so each SM keeps tens of KB of HBM reads in flight.  No slot is shared, so no CTA barrier is needed.
+    constexpr int U = kDenseU;
+    extern __shared__ uint4 ring[];   // [kDenseStages][U][2][kDenseThreads]
+    const int tid = threadIdx.x;
+    const int n_it = (int)cdiv(t_end - t_begin, NW * TPW * U);
+    auto issue = [&](int it) {
+        if (it < n_it) {
+            const int s = it % kDenseStages;
+            const int t0 = t_begin + (it * NW + warp) * TPW * U;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + u * TPW + grp;
+                const bool ok = t < t_end;
+                const int64_t off = (((int64_t)b * T + (ok ? t : t_begin)) * H_kv + h) * D + sub * VEC;
+                cp_async16(&ring[((s * U + u) * 2 + 0) * kDenseThreads + tid], K + off, ok);
+                cp_async16(&ring[((s * U + u) * 2 + 1) * kDenseThreads + tid], V + off, ok);
+            }
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-            float s = 0.0f;
-            if (valid)
+    for (int it = 0; it < kDenseStages - 1; ++it) issue(it);
+    for (int it = 0; it < n_it; ++it) {
+        issue(it + kDenseStages - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kDenseStages - 1) : "memory");
+        const int s = it % kDenseStages;
+        const int t0 = t_begin + (it * NW + warp) * TPW * U;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) s = fmaf(qv[j][e], kx[e], s);
+        for (int u = 0; u < U; ++u) {
+            const int t = t0 + u * TPW + grp;
+            const bool valid = t < t_end;
+            float kx[VEC], vx[VEC];
+            Vec16<TE>::cvt(ring[((s * U + u) * 2 + 0) * kDenseThreads + tid], kx);
+            Vec16<TE>::cvt(ring[((s * U + u) * 2 + 1) * kDenseThreads + tid], vx);
 #pragma unroll
-            for (int o = LPT / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (valid) {
-                const float mn = fmaxf(m[j], s);
-                const float corr = (m[j] == -INFINITY) ? 0.0f : __expf(m[j] - mn);
-                const float p = __expf(s - mn);
-                l[j] = l[j] * corr + p;
+            for (int j = 0; j < G; ++j) {
+                float sc = 0.0f;
+                if (valid)
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) acc[j][e] = fmaf(p, vx[e], acc[j][e] * corr);
-                m[j] = mn;
+                    for (int e = 0; e < VEC; ++e) sc = fmaf(qv[j][e], kx[e], sc);
+#pragma unroll
+                for (int o = LPT / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
+                if (valid) {
+                    const float mn = fmaxf(m[j], sc);
+                    const float corr = (m[j] == -INFINITY) ? 0.0f : __expf(m[j] - mn);
+                    const float p = __expf(sc - mn);
+                    l[j] = l[j] * corr + p;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[j][e] = fmaf(p, vx[e], acc[j][e] * corr);
+                    m[j] = mn;
+                }
             }
         }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     // merge the token groups of the warp (lanes with the same sub hold the same features)
 #pragma unroll
     for (int o = LPT; o < 32; o <<= 1) {
@@ -167,17 +206,27 @@ int dense_splits(int B, int T, int H_kv) {
 template <typename TE, int D>
 static cudaError_t dense_g(int B, int T, int H_q, int H_kv, float scale, const void* q, const void* k, const void* v,
                            float* partial, int n_split, cudaStream_t st) {
-    dim3 grid((unsigned)n_split, (unsigned)H_kv, (unsigned)B);
+    // the kv-heads of one token range are adjacent in launch order: they run together and read the same
+    // [H_kv, d] token rows of K and V, so DRAM sees whole rows rather than one head's 2*d bytes per row
+    dim3 grid((unsigned)H_kv, (unsigned)n_split, (unsigned)B);
     const TE *Q = (const TE*)q, *K = (const TE*)k, *V = (const TE*)v;
+    cudaError_t e = cudaSuccess;
+    auto go = [&](auto kern) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDenseSmem);
+        if (e == cudaSuccess) {
+            kern<<<grid, kDenseThreads, kDenseSmem, st>>>(T, H_q, H_kv, scale, Q, K, V, partial, n_split);
+            e = cudaGetLastError();
+        }
+    };
     switch (H_q / H_kv) {
-        case 1: dense_kernel<TE, D, 1><<<grid, kDenseThreads, 0, st>>>(T, H_q, H_kv, scale, Q, K, V, partial, n_split); break;
-        case 2: dense_kernel<TE, D, 2><<<grid, kDenseThreads, 0, st>>>(T, H_q, H_kv, scale, Q, K, V, partial, n_split); break;
-        case 4: dense_kernel<TE, D, 4><<<grid, kDenseThreads, 0, st>>>(T, H_q, H_kv, scale, Q, K, V, partial, n_split); break;
-        case 7: dense_kernel<TE, D, 7><<<grid, kDenseThreads, 0, st>>>(T, H_q, H_kv, scale, Q, K, V, partial, n_split); break;
-        case 8: dense_kernel<TE, D, 8><<<grid, kDenseThreads, 0, st>>>(T, H_q, H_kv, scale, Q, K, V, partial, n_split); break;
+        case 1: go(dense_kernel<TE, D, 1>); break;
+        case 2: go(dense_kernel<TE, D, 2>); break;
+        case 4: go(dense_kernel<TE, D, 4>); break;
+        case 7: go(dense_kernel<TE, D, 7>); break;
+        case 8: go(dense_kernel<TE, D, 8>); break;
         default: return cudaErrorNotSupported;
     }
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_dense(int B, int T, int H_q, int H_kv, int d, int dtype, float scale, const void* q, const void* k,

@@ -7,7 +7,8 @@
 // Radix select on order-preserving uint32 keys: four 8-bit digit passes narrow the candidates to
 // the exact value of the n-th largest element (the threshold) and how many elements equal to it must
 // be kept; a final pass in index order keeps every element above the threshold and the
-// lowest-indexed equal ones, writing their indices ascending through a block-wide prefix sum.
+// lowest-indexed equal ones, writing their indices ascending (each warp compacts a contiguous segment
+// after one exchange of per-warp counts).
 // One CTA per row; rows up to 48K elements are read once into shared memory.
 #include "common.cuh"
 #include "kernels.h"
@@ -16,31 +17,6 @@ namespace lowram {
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelMaxStaged = 48 * 1024;   // row elements staged in shared memory (192 KB)
-
-// Exclusive block-wide prefix sum of a 0/1 flag (one per thread), plus the block total.
-__device__ __forceinline__ int block_excl_scan(bool f, int* warp_tot, int& total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    unsigned bal = __ballot_sync(0xffffffffu, f);
-    int in_warp = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[warp] = __popc(bal);
-    __syncthreads();
-    if (warp == 0) {
-        int v = lane < nw ? warp_tot[lane] : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int x = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += x;
-        }
-        if (lane < nw) warp_tot[lane] = incl - v;  // exclusive
-        if (lane == 31) warp_tot[32] = incl;        // total
-    }
-    __syncthreads();
-    int r = warp_tot[warp] + in_warp;
-    total = warp_tot[32];
-    __syncthreads();
-    return r;
-}
 
 // Residual lookup for the value pass: hit[row][j] = the position of token o[j] in the row's ascending
 // residual list, or -1.  The list is checked (in range, strictly ascending; LOWRAM_CHECK_RES_INDEX on
@@ -118,8 +94,9 @@ __global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_k
     int need = n_keep;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int i = tid; i < (kSelThreads / 32) * 256; i += kSelThreads) (&whist[0][0])[i] = 0;
-        __syncthreads();
+        // each warp owns one histogram row: clearing and filling it need only the warp
+        for (int i = lane; i < 256; i += 32) whist[warp][i] = 0;
+        __syncwarp();
         for (int t = tid; t < T; t += kSelThreads) {
             const uint32_t u = key_at(t);
             if ((u & mask) == prefix) atomicAdd(&whist[warp][(u >> shift) & 255u], 1u);
@@ -163,22 +140,49 @@ __global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_k
         prefix = s_prefix;
         need = s_need;
         mask |= 0xFFu << shift;
-        __syncthreads();
     }
-    // prefix is now the threshold key; keep all keys above it and the first `need` equal ones.
-    int taken = 0, eq_seen = 0;
-    for (int base = 0; base < T; base += kSelThreads) {
-        const int t = base + tid;
-        const uint32_t u = t < T ? key_at(t) : 0u;
-        const bool eq = t < T && u == prefix;
-        int eq_total;
-        const int eq_rank = eq_seen + block_excl_scan(eq, warp_tot, eq_total);
-        const bool take = (t < T && u > prefix) || (eq && eq_rank < need);
-        int take_total;
-        const int at = taken + block_excl_scan(take, warp_tot, take_total);
-        if (take && at < n_keep) o[at] = t;
-        taken += take_total;
-        eq_seen += eq_total;
+    // prefix is now the threshold key: keep every key above it and the `need` lowest-indexed equal ones.
+    // Warp w owns the contiguous segment [s0, s1); one exchange of the warps' counts gives each warp its
+    // output offset and the number of equal keys before it, so indices come out ascending.
+    {
+        constexpr int nw = kSelThreads / 32;
+        const int seg = (T + nw - 1) / nw;
+        const int s0 = min(T, warp * seg), s1 = min(T, s0 + seg);
+        int n_gt = 0, n_eq = 0;
+        for (int t = s0 + lane; t < s1; t += 32) {
+            const uint32_t u = key_at(t);
+            n_gt += u > prefix;
+            n_eq += u == prefix;
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) {
+            n_gt += __shfl_xor_sync(0xffffffffu, n_gt, o2);
+            n_eq += __shfl_xor_sync(0xffffffffu, n_eq, o2);
+        }
+        if (lane == 0) {
+            warp_tot[warp] = n_gt;
+            (&whist[0][0])[warp] = (uint32_t)n_eq;
+        }
+        __syncthreads();
+        int gt_before = 0, eq_before = 0;
+        for (int w = 0; w < warp; ++w) {
+            gt_before += warp_tot[w];
+            eq_before += (int)(&whist[0][0])[w];
+        }
+        int at = gt_before + min(need, eq_before);
+        int eq_rank = eq_before;
+        const unsigned lt = (1u << lane) - 1u;
+        for (int base = s0; base < s1; base += 32) {
+            const int t = base + lane;
+            const uint32_t u = t < s1 ? key_at(t) : 0u;
+            const bool eq = t < s1 && u == prefix;
+            const unsigned beq = __ballot_sync(0xffffffffu, eq);
+            const bool take = (t < s1 && u > prefix) || (eq && eq_rank + __popc(beq & lt) < need);
+            const unsigned btake = __ballot_sync(0xffffffffu, take);
+            if (take) o[at + __popc(btake & lt)] = t;
+            at += __popc(btake);
+            eq_rank += __popc(beq);
+        }
     }
     if (x.hit) match_residuals<Staged>(T, n_keep, o, x, row, staged);
 }

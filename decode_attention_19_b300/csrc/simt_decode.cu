@@ -183,39 +183,66 @@ __global__ void __launch_bounds__(kTileThreads) vregen_simt_kernel(DecodeArgs a,
 }
 
 // ------------------------------------------------------------------------------------------------
-// K4: merge split-softmax partials.  One warp per (b, q-head).
+// K4: merge split-softmax partials.  One CTA of 128 threads per (b, q-head):
+//   W = max_c m_c, w_c = exp(m_c - W), L = sum_c w_c l_c, out = sum_c w_c acc_c / L, lse = W + log L.
+// The per-chunk weights go to shared memory; each thread owns one output feature and reads the chunks'
+// values for it in batches of independent loads.
 // ------------------------------------------------------------------------------------------------
-__global__ void merge_kernel(int BH, int n_chunks, int d, const float* __restrict__ partial, float* __restrict__ out,
-                             float* __restrict__ lse) {
-    const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
-    if (w >= BH) return;
-    const float* P = partial + (int64_t)w * n_chunks * (d + 2);
+constexpr int kMergeThreads = 128;
+
+__device__ __forceinline__ float merge_reduce(float v, float* red, bool is_max) {
+    v = is_max ? warp_max(v) : warp_sum(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    const float r = is_max ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) : (red[0] + red[1]) + (red[2] + red[3]);
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(int n_chunks, int d, const float* __restrict__ partial,
+                                                              float* __restrict__ out, float* __restrict__ lse) {
+    extern __shared__ float wts[];   // [n_chunks]
+    __shared__ float red[4];
+    const int w = blockIdx.x, tid = threadIdx.x;
+    const int64_t rw = d + 2;
+    const float* P = partial + (int64_t)w * n_chunks * rw;
     float M = -INFINITY;
-    for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, P[(int64_t)c * (d + 2) + d]);
-    M = warp_max(M);
+    for (int c = tid; c < n_chunks; c += kMergeThreads) M = fmaxf(M, P[c * rw + d]);
+    M = merge_reduce(M, red, true);
     float L = 0.0f;
-    for (int c = lane; c < n_chunks; c += 32) {
-        float mc = P[(int64_t)c * (d + 2) + d];
-        L += (mc == -INFINITY) ? 0.0f : __expf(mc - M) * P[(int64_t)c * (d + 2) + d + 1];
+    for (int c = tid; c < n_chunks; c += kMergeThreads) {
+        const float mc = P[c * rw + d];
+        const float wc = (mc == -INFINITY) ? 0.0f : __expf(mc - M);
+        wts[c] = wc;
+        L = fmaf(wc, P[c * rw + d + 1], L);
     }
-    L = warp_sum(L);
+    L = merge_reduce(L, red, false);   // also orders the wts[] writes before their reads
     const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-    for (int i = lane; i < d; i += 32) {
+    if (tid < d) {
         float acc = 0.0f;
-        for (int c = 0; c < n_chunks; ++c) {
-            float mc = P[(int64_t)c * (d + 2) + d];
-            if (mc != -INFINITY) acc = fmaf(__expf(mc - M), P[(int64_t)c * (d + 2) + i], acc);
+        for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = (c0 + u < n_chunks) ? P[(c0 + u) * rw + tid] : 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + u < n_chunks) acc = fmaf(wts[c0 + u], v[u], acc);
         }
-        out[(int64_t)w * d + i] = acc * inv;
+        out[(int64_t)w * d + tid] = acc * inv;
     }
-    if (lse && lane == 0) lse[w] = (L > 0.0f) ? M + logf(L) : -INFINITY;
+    if (lse && tid == 0) lse[w] = (L > 0.0f) ? M + logf(L) : -INFINITY;
 }
 
 cudaError_t launch_merge(int B, int H_q, int n_chunks, int d, const float* partial, float* out, float* lse,
                          cudaStream_t st) {
     const int BH = B * H_q;
     if (BH == 0) return cudaSuccess;
-    merge_kernel<<<(unsigned)cdiv(BH, 8), 256, 0, st>>>(BH, n_chunks, d, partial, out, lse);
+    const size_t smem = sizeof(float) * (size_t)(n_chunks > 0 ? n_chunks : 1);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    merge_kernel<<<(unsigned)BH, kMergeThreads, smem, st>>>(n_chunks, d, partial, out, lse);
     return cudaGetLastError();
 }
 
