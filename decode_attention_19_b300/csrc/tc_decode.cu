@@ -8,23 +8,26 @@
 // the epilogue that reads the accumulators out of TMEM.  Every q-head's scaled logit is stored too: the
 // value pass takes the softmax of the selected tokens from exactly the scores the selection saw.
 //
-// Shape of the kernel (persistent, one CTA per SM, 320 threads; each CTA takes a contiguous range of
-// 128-token tiles, so the sequence -- and the query -- rarely changes inside a CTA):
-//   warp 0      TMA producer: a ring of NS stages, each one 64-wide k-chunk of the 128-token latent tile and
-//               of the unit's basis rows [UN x 64].  The latent tile is re-read from L2 for every unit rather
-//               than kept resident: the freed shared memory holds a deeper ring, and the basis stream, not the
-//               latent tile, is what the pass waits on (L2 latency x bytes in flight).
-//   warp 1      TMEM owner and MMA issuer (one thread): per unit of UN/128 kv-heads, M=128, N=UN, K=r in
-//               r/16 tcgen05.mma steps into one of two UN-column accumulators.
+// Shape of the kernel: persistent CTA pairs (clusters of two, at most one CTA per SM), 320 threads per CTA.
+// A pair walks a contiguous range of tile pairs; CTA r of the pair takes tile 2*pair + r.  The key rebuild
+// of a unit of UN/128 kv-heads is one pair MMA per k-step (tcgen05 cta_group::2, M=256, N=UN, K=16): each
+// CTA supplies its tile's 128 token rows of A and half of the unit's basis rows of B, and each CTA's TMEM
+// accumulates its own 128 tokens x UN features.  Compared with one CTA per tile, every SM reads only half
+// of each basis chunk from shared memory.
+//   warp 0      TMA producer (both CTAs): a ring of NS stages, each one 64-wide k-chunk of the CTA's
+//               latent tile [128 x 64] and of its half of the unit's basis rows [UN/2 x 64].  The odd CTA's
+//               copies complete on the even CTA's barrier, so one barrier covers the pair's stage.
+//   warp 1      TMEM owner (both CTAs allocate the pair's 2*UN columns together) and, in the even CTA, the
+//               MMA issuer; each stage's commit releases the stage in both CTAs.
 //   warps 2-9   epilogue, two groups of four warps taking alternate units (so one group's arithmetic overlaps
 //               the other's and the next unit's MMAs).  Warp w reads TMEM lane quarter w%4: one thread holds
-//               one token and, per 8 rotary frequencies, rotates the unit's heads and accumulates the dot
-//               products with the queries.  Per tile the token's cos/sin are fetched once (64 independent
-//               loads per thread) into shared memory and reused by every unit; the queries sit pre-scaled in
-//               float32 in shared memory.  Table fetches inside the unit loop would each be an L2 round trip
-//               on the critical path.
-// Every wait is bounded (see tc_common.cuh); on a timeout the kernel flags LOWRAM_CHECK_TIMEOUT, drains
-// the copies and MMAs it issued and returns.  The epilogue's named barriers are reached on every path.
+//               one token and, per 8 rotary frequencies, loads its cos/sin (prefetched a chunk ahead),
+//               rotates the unit's heads and accumulates the dot products with the queries, which sit
+//               pre-scaled in float32 in shared memory.  Both CTAs' epilogues release a TMEM buffer before
+//               the even CTA's MMAs reuse it.
+// Every wait is bounded (see tc_common.cuh); a failed wait stops both CTAs of the pair, which flag
+// LOWRAM_CHECK_TIMEOUT, let what they issued complete and return.  The epilogue's named barriers are reached
+// on every path, and the pair meets at a cluster barrier before either frees TMEM or exits.
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -54,35 +57,37 @@ struct ScoreTcParams {
 
 // Stage s of the ring: one 64-wide k-chunk of the latent tile [128 x 64] and of the unit's basis rows
 // [UN x 64], both 128B-swizzled as TMA writes them.
-// Beside the ring: the queries of the current sequence (fp32, pre-scaled) and the cos/sin of the current
-// tile's 128 tokens for the 64 rotary frequencies (fp32, [2][64][128]).
+// Beside the ring: the queries of the current sequence (fp32, pre-scaled).
 size_t score_smem_bytes(int NS, int UN, int H_q) {
-    return 1024 + (size_t)NS * (kAChunkBytes + UN * 128) + (size_t)H_q * 128 * 4 + 2 * 64 * 128 * 4 +
-           8 * (2 * NS + 5) + 16;
+    return 1024 + (size_t)NS * (kAChunkBytes + (UN / 2) * 128) + (size_t)H_q * 128 * 4 + 8 * (2 * NS + 5) + 16;
 }
 
 template <int G, int HPU>
-__global__ void __launch_bounds__(kScoreThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ScoreTcParams p) {
     using namespace tc;
-    constexpr int UN = HPU * 128;              // accumulator columns per unit
-    constexpr int kStage = kAChunkBytes + UN * 128;
+    constexpr int UN = HPU * 128;              // accumulator columns per unit = basis rows per pair MMA
+    constexpr int kBHalf = (UN / 2) * 128;     // this CTA's half of a basis chunk [UN/2 x 64]
+    constexpr int kStage = kAChunkBytes + kBHalf;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* St = smem;
     float* Qs = (float*)(St + p.NS * kStage);     // [H_q][128] query of the current sequence x scale
-    float* CS = Qs + p.H_q * 128;                  // [2][64][128] cos, sin of the tile's tokens
-    uint64_t* b_full = (uint64_t*)(CS + 2 * 64 * 128);
-    uint64_t* b_empty = b_full + p.NS;
+    uint64_t* b_full = (uint64_t*)(Qs + p.H_q * 128);    // (even CTA) both CTAs' copies of the stage landed
+    uint64_t* b_empty = b_full + p.NS;                   // the pair's MMAs are done with the stage
     uint64_t* t_full = b_empty + p.NS;
-    uint64_t* t_empty = t_full + 2;
+    uint64_t* t_empty = t_full + 2;                      // (even CTA) both epilogues released the buffer
     uint64_t* m_drain = t_empty + 2;
     uint32_t* tmem_slot = (uint32_t*)(m_drain + 1);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t_begin = (int)((int64_t)blockIdx.x * p.n_tiles / gridDim.x);
-    const int t_end = (int)((int64_t)(blockIdx.x + 1) * p.n_tiles / gridDim.x);
+    const uint32_t rank = cluster_rank();          // 0 issues the MMAs; 1 feeds its halves
+    const uint32_t peer = rank ^ 1u;
+    // the pair walks a contiguous range of tile pairs; CTA `rank` takes tile 2*pair + rank (a tile past the
+    // end is computed on the last tile's data and not written)
+    const int n_pairs = (p.n_tiles + 1) / 2, cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const int pr_begin = (int)((int64_t)cl * n_pairs / ncl), pr_end = (int)((int64_t)(cl + 1) * n_pairs / ncl);
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.NS; ++i) {
             mbar_init(&b_full[i], 1);
@@ -90,7 +95,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&t_full[i], 1);
-            mbar_init(&t_empty[i], 4 * 32);
+            mbar_init(&t_empty[i], 4 * 32 + 4);   // 128 local threads + one arrival per warp of the odd CTA
         }
         mbar_init(m_drain, 1);
         *abort_flag = 0;
@@ -101,64 +106,97 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 2 * UN);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, 2 * UN);
+        tmem_relinquish_pair();
     }
     fence_before();
     __syncthreads();
+    cluster_sync();      // both CTAs' barriers exist and TMEM is allocated before any cross-CTA traffic
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t peer_abort = peer_smem((const void*)abort_flag, peer);
+    // a failed wait stops both CTAs of the pair
+    auto fail = [&]() {
+        *abort_flag = 1;
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
+    };
 
     if (warp == 0) {
-        // ------------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
             uint32_t ib = 0;
-            for (int tile = t_begin; tile < t_end && !*abort_flag; ++tile) {
-                const int b = tile / p.tiles_per_seq, t0 = (tile % p.tiles_per_seq) * kTokTile;
+            for (int pr = pr_begin; pr < pr_end && !*abort_flag; ++pr) {
+                const int lt = min(2 * pr + (int)rank, p.n_tiles - 1);
+                const int b = lt / p.tiles_per_seq, t0 = (lt % p.tiles_per_seq) * kTokTile;
                 for (int u = 0; u < p.NU; ++u) {
                     for (int kc = 0; kc < p.KC; ++kc, ++ib) {
                         const uint32_t s = ib % p.NS, ph = (ib / p.NS) & 1;
-                        if (!mbar_wait(&b_empty[s], ph ^ 1, abort_flag)) goto produced;
-                        mbar_expect_tx(&b_full[s], kStage);
-                        tma_load_3d(St + s * kStage, &tmA, &b_full[s], kc * kChunkK, t0, b);
-                        tma_load_2d(St + s * kStage + kAChunkBytes, &tmB, &b_full[s], kc * kChunkK, u * UN);
+                        if (!mbar_wait_cluster(&b_empty[s], ph ^ 1, abort_flag)) {
+                            fail();
+                            goto produced;
+                        }
+                        uint8_t* dA = St + s * kStage;
+                        uint8_t* dB = dA + kAChunkBytes;
+                        const int brow = u * UN + (int)rank * (UN / 2);
+                        if (rank == 0) {   // the even CTA's barrier counts both CTAs' bytes
+                            mbar_expect_tx(&b_full[s], 2 * kStage);
+                            tma_load_3d(dA, &tmA, &b_full[s], kc * kChunkK, t0, b);
+                            tma_load_2d(dB, &tmB, &b_full[s], kc * kChunkK, brow);
+                        } else {
+                            const uint32_t bar = peer_smem(&b_full[s], 0);
+                            tma_load_3d_pair(dA, &tmA, bar, kc * kChunkK, t0, b);
+                            tma_load_2d_pair(dB, &tmB, bar, kc * kChunkK, brow);
+                        }
                     }
                 }
             }
         produced:
-            if (*abort_flag)   // stages older than the last NS were consumed by MMAs, so they have landed
-                for (uint32_t k = (ib > (uint32_t)p.NS ? ib - p.NS : 0); k < ib; ++k)
-                    mbar_wait_drain(&b_full[k % p.NS], (k / p.NS) & 1);
+            if (*abort_flag) {
+                if (rank == 0) {   // stages older than the last NS were consumed by MMAs, so they have landed
+                    for (uint32_t k = (ib > (uint32_t)p.NS ? ib - p.NS : 0); k < ib; ++k)
+                        mbar_wait_drain(&b_full[k % p.NS], (k / p.NS) & 1);
+                } else {           // this CTA's copies complete on the even CTA's barriers: give them time to land
+                    const long long c0 = clock64();
+                    while (clock64() - c0 < 4000000) {
+                    }
+                }
+            }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(kTokTile, UN);
+        if (rank == 0 && lane == 0) {
+            // -------------------------------------------------------------- MMA issuer (even CTA)
+            const uint32_t idesc = idesc_bf16(2 * kTokTile, UN);
             uint32_t ib = 0, j = 0;
-            for (int tile = t_begin; tile < t_end && !*abort_flag; ++tile) {
+            for (int pr = pr_begin; pr < pr_end && !*abort_flag; ++pr) {
                 for (int u = 0; u < p.NU; ++u, ++j) {
                     const uint32_t buf = j & 1;
-                    if (!mbar_wait(&t_empty[buf], ((j >> 1) & 1) ^ 1, abort_flag)) goto issued;
+                    if (!mbar_wait_cluster(&t_empty[buf], ((j >> 1) & 1) ^ 1, abort_flag)) {
+                        fail();
+                        goto issued;
+                    }
                     fence_after();
                     const uint32_t d_tmem = tmem + buf * UN;
                     for (int kc = 0; kc < p.KC; ++kc, ++ib) {
                         const uint32_t s = ib % p.NS, ph = (ib / p.NS) & 1;
-                        if (!mbar_wait(&b_full[s], ph, abort_flag)) goto issued;
+                        if (!mbar_wait(&b_full[s], ph, abort_flag)) {
+                            fail();
+                            goto issued;
+                        }
                         fence_after();
                         const uint32_t a_addr = smem_u32(St + s * kStage);
                         const uint32_t b_addr = a_addr + kAChunkBytes;
 #pragma unroll
                         for (int k = 0; k < kChunkK / 16; ++k)
-                            mma_bf16(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), idesc,
-                                     (kc | k) != 0);
-                        mma_commit(&b_empty[s]);
+                            mma_bf16_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), idesc,
+                                          (kc | k) != 0);
+                        mma_commit_pair(&b_empty[s], 0x3);
                     }
-                    mma_commit(&t_full[buf]);
+                    mma_commit_pair(&t_full[buf], 0x3);
                 }
             }
         issued:
-            // every MMA this thread issued completes before TMEM is released
-            mma_commit(m_drain);
+            // every MMA issued completes before TMEM is released
+            mma_commit_pair(m_drain, 0x1);
             mbar_wait_drain(m_drain, 0);
         }
     } else {
@@ -172,9 +210,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         int cur_b = -1;
         // no abort test in the loop conditions: every epilogue thread walks the same tiles and reaches the
         // same named barriers; after an abort the waits fail at once and the work is skipped
-        for (int tile = t_begin; tile < t_end; ++tile) {
-            const int b = tile / p.tiles_per_seq, t0 = (tile % p.tiles_per_seq) * kTokTile;
-            const int t = t0 + row;
+        for (int pr = pr_begin; pr < pr_end; ++pr) {
+            const int tile = 2 * pr + (int)rank;
+            const bool real = tile < p.n_tiles;
+            const int lt = real ? tile : p.n_tiles - 1;
+            const int b = lt / p.tiles_per_seq, t0 = (lt % p.tiles_per_seq) * kTokTile;
+            const int t = real ? t0 + row : p.T;   // a tile past the end writes nothing
             int ps = 0;
             if (t < p.T) {
                 ps = p.pos ? p.pos[(int64_t)b * p.T + t] : t;
@@ -183,31 +224,24 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     ps = ps < 0 ? 0 : p.max_pos - 1;
                 }
             }
-            named_bar_sync(1, 256);          // every epilogue thread is done with the previous tile
-            if (!*abort_flag) {
-                if (b != cur_b) {
+            if (b != cur_b) {
+                named_bar_sync(1, 256);      // every epilogue thread is done with the previous query
+                if (!*abort_flag) {
                     const __nv_bfloat16* qb = p.q + (int64_t)b * p.H_q * 128;
                     for (int e = et; e < p.H_q * 128; e += 256) Qs[e] = __bfloat162float(qb[e]) * p.scale;
                 }
-                // this row's cos/sin, half of the frequencies per group: 64 independent loads in flight
-                float cv[32], sv[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    cv[k] = __ldg(p.rcos + (int64_t)(grp * 32 + k) * mp + ps);
-                    sv[k] = __ldg(p.rsin + (int64_t)(grp * 32 + k) * mp + ps);
-                }
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    CS[(grp * 32 + k) * 128 + row] = cv[k];
-                    CS[(64 + grp * 32 + k) * 128 + row] = sv[k];
-                }
+                named_bar_sync(1, 256);
+                cur_b = b;
             }
-            cur_b = b;
-            named_bar_sync(1, 256);
+            const float* cb = p.rcos + ps;
+            const float* sb = p.rsin + ps;
             for (int u = 0; u < p.NU; ++u, ++j) {
                 if ((int)(j & 1) != grp) continue;
                 const uint32_t buf = j & 1;
-                if (!mbar_wait(&t_full[buf], (j >> 1) & 1, abort_flag)) continue;
+                if (!mbar_wait_cluster(&t_full[buf], (j >> 1) & 1, abort_flag)) {
+                    fail();
+                    continue;
+                }
                 fence_after();
                 const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + buf * UN;
                 float acc[HPU][G];
@@ -215,13 +249,26 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 for (int hx = 0; hx < HPU; ++hx)
 #pragma unroll
                     for (int jq = 0; jq < G; ++jq) acc[hx][jq] = 0.0f;
+                float cn[8], sn[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    cn[k] = __ldg(cb + k * mp);
+                    sn[k] = __ldg(sb + k * mp);
+                }
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {       // rotary frequencies c*8 .. c*8+7
+                for (int c = 0; c < 8; ++c) {       // rotary frequencies c*8 .. c*8+7; the next 8 are prefetched
                     float cc[8], ss[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        cc[k] = CS[(c * 8 + k) * 128 + row];
-                        ss[k] = CS[(64 + c * 8 + k) * 128 + row];
+                        cc[k] = cn[k];
+                        ss[k] = sn[k];
+                    }
+                    if (c < 7) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            cn[k] = __ldg(cb + ((c + 1) * 8 + k) * mp);
+                            sn[k] = __ldg(sb + ((c + 1) * 8 + k) * mp);
+                        }
                     }
                     float x[HPU][8], y[HPU][8];
                     if (HPU == 2)
@@ -268,7 +315,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                         }
                 }
                 fence_before();
-                mbar_arrive(&t_empty[buf]);
+                if (rank == 0) {
+                    mbar_arrive(&t_empty[buf]);
+                } else {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(peer_smem(&t_empty[buf], 0));
+                }
                 if (t < p.T) {
 #pragma unroll
                     for (int hx = 0; hx < HPU; ++hx) {
@@ -290,10 +342,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // ---------------------------------------------------------------------- teardown
     fence_before();
     __syncthreads();
+    cluster_sync();      // neither CTA leaves while the other may still touch its shared memory
     if (*abort_flag && threadIdx.x == 0) flag(p.check, LOWRAM_CHECK_TIMEOUT);
     if (warp == 1) {
         fence_after();
-        tmem_dealloc(tmem, 2 * UN);
+        tmem_dealloc_pair(tmem, 2 * UN);
     }
 }
 
@@ -357,10 +410,11 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     const uint64_t dA[3] = {(uint64_t)s.r, (uint64_t)s.T, (uint64_t)s.B};
     const uint32_t bA[3] = {kChunkK, kTokTile, 1};
     const uint64_t dB[2] = {(uint64_t)s.r, (uint64_t)s.H_kv * s.d};
-    const uint32_t bB[2] = {kChunkK, (uint32_t)cfg.UN};
+    const uint32_t bB[2] = {kChunkK, (uint32_t)cfg.UN / 2};
     if (!make_map(&mA, a.coef, 3, dA, bA) || !make_map(&mB, a.basis, 2, dB, bB)) return cudaErrorInvalidValue;
     const size_t smem = score_smem_bytes(p.NS, cfg.UN, s.H_q);
-    const int grid = std::min(p.n_tiles, sm_count());
+    // CTA pairs (cluster of two), at most one CTA per SM
+    const int grid = 2 * std::min((p.n_tiles + 1) / 2, std::max(1, sm_count() / 2));
     cudaError_t e = cudaSuccess;
     auto go = [&](auto kern) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
