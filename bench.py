@@ -107,6 +107,14 @@ def algorithmic(w):
     return bytes_, f_keys, f_sel, f_mlp
 
 
+def launches_per_call(w, tc_path):
+    """Kernels one decode call launches: keys, selection, values (+ a separate merge unless the tensor-core
+    value pass merges as it finishes, which it does for predictor widths of 128 or 256)."""
+    if w.S_eff == 0:
+        return 2
+    return 3 if (tc_path and w.m in (128, 256)) else 4
+
+
 def kernel_digest(paths):
     h = hashlib.sha256()
     for p in sorted(paths):
@@ -420,8 +428,7 @@ def main():
     # roofline of the dominant kernel
     bytes_call, f_keys, f_sel, f_mlp = algorithmic(w)
     src = [os.path.join(ROOT, "decode_attention_19_b300", "csrc", f) for f in
-           ("simt_decode.cu", "tc_decode.cu", "select.cu", "predict.cuh", "simt_tile.cuh", "common.cuh", "tc_common.cuh")
-           if os.path.exists(os.path.join(ROOT, "decode_attention_19_b300", "csrc", f))]
+           ("tc_decode.cu", "tc_common.cuh", "common.cuh", "kernels.h")]
     tc_path = L.lowram_decode_uses_tensor_cores(shape_probe)
     k1_ms = per_kernel_ms[0]
     if tc_path:
@@ -459,7 +466,7 @@ def main():
             "roofline": roof,
             "ms_per_step_no_flush": ms_b2b, "wall_ms_per_step": t_wall * 1e3 / args.steps,
             "compress_ms_per_group": float(np.mean(compress_ms)),
-            "gpu_launches": args.steps * w.L * (4 if w.S_eff > 0 else 2),
+            "gpu_launches": args.steps * w.L * launches_per_call(w, tc_path),
             "clocks": clk, "peaks": pk_kind}
     if e2e:
         line["e2e"] = e2e
