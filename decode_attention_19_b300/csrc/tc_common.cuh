@@ -242,6 +242,30 @@ __device__ __forceinline__ void tmem_ld_2x8(uint32_t t0, uint32_t t1, float (&a)
 }
 
 // ------------------------------------------------------------------------------------------------
+// packed fp32 pairs (sm_100 family): one instruction does two round-to-nearest fp32 multiplies or FMAs
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return make_float2(lo, hi);
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {   // a * b + c
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// ------------------------------------------------------------------------------------------------
 // CTA pairs (cluster of two): ranks, remote mbarrier arrivals, cluster barrier, and the pair forms of
 // the tcgen05 allocation, MMA and commit.  In a pair both CTAs allocate and free TMEM together; one
 // thread of the even CTA issues the MMAs, which read each CTA's half of A (M/2 rows) and of B (N/2

@@ -23,7 +23,8 @@
 //               the other's and the next unit's MMAs).  Warp w reads TMEM lane quarter w%4: one thread holds
 //               one token and, per 8 rotary frequencies, loads its cos/sin (prefetched a chunk ahead),
 //               rotates the unit's heads and accumulates the dot products with the queries, which sit
-//               pre-scaled in float32 in shared memory.  Both CTAs' epilogues release a TMEM buffer before
+//               pre-scaled in float32 in shared memory; the arithmetic runs on packed fp32 pairs (two
+//               adjacent frequencies per instruction).  Both CTAs' epilogues release a TMEM buffer before
 //               the even CTA's MMAs reuse it.
 // Every wait is bounded (see tc_common.cuh); a failed wait stops both CTAs of the pair, which flag
 // LOWRAM_CHECK_TIMEOUT, let what they issued complete and return.  The epilogue's named barriers are reached
@@ -244,11 +245,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                 }
                 fence_after();
                 const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + buf * UN;
-                float acc[HPU][G];
+                uint64_t acc2[HPU][G];     // (even, odd) frequency partial sums of each dot product
 #pragma unroll
                 for (int hx = 0; hx < HPU; ++hx)
 #pragma unroll
-                    for (int jq = 0; jq < G; ++jq) acc[hx][jq] = 0.0f;
+                    for (int jq = 0; jq < G; ++jq) acc2[hx][jq] = 0ull;
                 float cn[8], sn[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -276,44 +277,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                                     x[HPU - 1], y[HPU - 1]);
                     else
                         tmem_ld_2x8(tb + c * 8, tb + 64 + c * 8, x[0], y[0]);
+                    // packed over pairs of adjacent frequencies (2m, 2m+1): rotate, then dot with the queries
+                    uint64_t c2[4], s2[4], ns2[4];
 #pragma unroll
-                    for (int hx = 0; hx < HPU; ++hx)
+                    for (int m = 0; m < 4; ++m) {
+                        c2[m] = f2_pack(cc[2 * m], cc[2 * m + 1]);
+                        s2[m] = f2_pack(ss[2 * m], ss[2 * m + 1]);
+                        ns2[m] = f2_pack(-ss[2 * m], -ss[2 * m + 1]);
+                    }
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const float kx = x[hx][k] * cc[k] - y[hx][k] * ss[k];
-                            const float ky = y[hx][k] * cc[k] + x[hx][k] * ss[k];
-                            x[hx][k] = kx;
-                            y[hx][k] = ky;
+                    for (int hx = 0; hx < HPU; ++hx) {
+                        uint64_t kx2[4], ky2[4];
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const uint64_t x2 = f2_pack(x[hx][2 * m], x[hx][2 * m + 1]);
+                            const uint64_t y2 = f2_pack(y[hx][2 * m], y[hx][2 * m + 1]);
+                            kx2[m] = f2_fma(x2, c2[m], f2_mul(y2, ns2[m]));   // x cos - y sin
+                            ky2[m] = f2_fma(y2, c2[m], f2_mul(x2, s2[m]));    // y cos + x sin
                         }
-#pragma unroll
-                    for (int hx = 0; hx < HPU; ++hx)
 #pragma unroll
                         for (int jq = 0; jq < G; ++jq) {
                             const float* qv = Qs + ((u * HPU + hx) * G + jq) * 128 + c * 8;
-                            const float4 q0 = *reinterpret_cast<const float4*>(qv);
-                            const float4 q1 = *reinterpret_cast<const float4*>(qv + 4);
-                            const float4 q2 = *reinterpret_cast<const float4*>(qv + 64);
-                            const float4 q3 = *reinterpret_cast<const float4*>(qv + 68);
-                            float a = acc[hx][jq];
-                            a = fmaf(q0.x, x[hx][0], a);
-                            a = fmaf(q0.y, x[hx][1], a);
-                            a = fmaf(q0.z, x[hx][2], a);
-                            a = fmaf(q0.w, x[hx][3], a);
-                            a = fmaf(q1.x, x[hx][4], a);
-                            a = fmaf(q1.y, x[hx][5], a);
-                            a = fmaf(q1.z, x[hx][6], a);
-                            a = fmaf(q1.w, x[hx][7], a);
-                            a = fmaf(q2.x, y[hx][0], a);
-                            a = fmaf(q2.y, y[hx][1], a);
-                            a = fmaf(q2.z, y[hx][2], a);
-                            a = fmaf(q2.w, y[hx][3], a);
-                            a = fmaf(q3.x, y[hx][4], a);
-                            a = fmaf(q3.y, y[hx][5], a);
-                            a = fmaf(q3.z, y[hx][6], a);
-                            a = fmaf(q3.w, y[hx][7], a);
-                            acc[hx][jq] = a;
+                            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qv);
+                            const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qv + 4);
+                            const ulonglong2 qc = *reinterpret_cast<const ulonglong2*>(qv + 64);
+                            const ulonglong2 qd = *reinterpret_cast<const ulonglong2*>(qv + 68);
+                            uint64_t a2 = acc2[hx][jq];
+                            a2 = f2_fma(qa.x, kx2[0], a2);
+                            a2 = f2_fma(qa.y, kx2[1], a2);
+                            a2 = f2_fma(qb.x, kx2[2], a2);
+                            a2 = f2_fma(qb.y, kx2[3], a2);
+                            a2 = f2_fma(qc.x, ky2[0], a2);
+                            a2 = f2_fma(qc.y, ky2[1], a2);
+                            a2 = f2_fma(qd.x, ky2[2], a2);
+                            a2 = f2_fma(qd.y, ky2[3], a2);
+                            acc2[hx][jq] = a2;
                         }
+                    }
                 }
+                float acc[HPU][G];
+#pragma unroll
+                for (int hx = 0; hx < HPU; ++hx)
+#pragma unroll
+                    for (int jq = 0; jq < G; ++jq) {
+                        const float2 v = f2_unpack(acc2[hx][jq]);
+                        acc[hx][jq] = v.x + v.y;
+                    }
                 fence_before();
                 if (rank == 0) {
                     mbar_arrive(&t_empty[buf]);
