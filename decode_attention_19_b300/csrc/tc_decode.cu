@@ -19,13 +19,13 @@
 //               copies complete on the even CTA's barrier, so one barrier covers the pair's stage.
 //   warp 1      TMEM owner (both CTAs allocate the pair's 2*UN columns together) and, in the even CTA, the
 //               MMA issuer; each stage's commit releases the stage in both CTAs.
-//   warps 2-9   epilogue, two groups of four warps taking alternate units (so one group's arithmetic overlaps
-//               the other's and the next unit's MMAs).  Warp w reads TMEM lane quarter w%4: one thread holds
-//               one token and, per 8 rotary frequencies, loads its cos/sin (prefetched a chunk ahead),
-//               rotates the unit's heads and accumulates the dot products with the queries, which sit
-//               pre-scaled in float32 in shared memory; the arithmetic runs on packed fp32 pairs (two
-//               adjacent frequencies per instruction).  Both CTAs' epilogues release a TMEM buffer before
-//               the even CTA's MMAs reuse it.
+//   warps 2-9   epilogue, all eight warps on every unit: warp w reads TMEM lane quarter w%4 and one half of
+//               the 64 rotary frequencies.  One thread holds one token, fetches its cos/sin for those 32
+//               frequencies once per tile into registers, and per unit rotates the unit's heads and accumulates
+//               the dot products with the queries, which sit pre-scaled in float32 in shared memory; the arithmetic runs on
+//               packed fp32 pairs (two adjacent frequencies per instruction).  The upper half passes its
+//               partial sums to the lower half through shared memory.  Both CTAs' epilogues release a TMEM
+//               buffer (double-buffered by unit) before the even CTA's MMAs reuse it.
 // Every wait is bounded (see tc_common.cuh); a failed wait stops both CTAs of the pair, which flag
 // LOWRAM_CHECK_TIMEOUT, let what they issued complete and return.  The epilogue's named barriers are reached
 // on every path, and the pair meets at a cluster barrier before either frees TMEM or exits.
@@ -58,9 +58,11 @@ struct ScoreTcParams {
 
 // Stage s of the ring: one 64-wide k-chunk of the latent tile [128 x 64] and of the unit's basis rows
 // [UN x 64], both 128B-swizzled as TMA writes them.
-// Beside the ring: the queries of the current sequence (fp32, pre-scaled).
+// Beside the ring: the queries of the current sequence (fp32, pre-scaled) and, double-buffered by unit, the
+// exchange of the upper frequency half's partial dot products [2][128][16] fp32.
 size_t score_smem_bytes(int NS, int UN, int H_q) {
-    return 1024 + (size_t)NS * (kAChunkBytes + (UN / 2) * 128) + (size_t)H_q * 128 * 4 + 8 * (2 * NS + 5) + 16;
+    return 1024 + (size_t)NS * (kAChunkBytes + (UN / 2) * 128) + (size_t)H_q * 128 * 4 + 2 * 128 * 16 * 4 +
+           8 * (2 * NS + 5) + 16;
 }
 
 template <int G, int HPU>
@@ -74,7 +76,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* St = smem;
     float* Qs = (float*)(St + p.NS * kStage);     // [H_q][128] query of the current sequence x scale
-    uint64_t* b_full = (uint64_t*)(Qs + p.H_q * 128);    // (even CTA) both CTAs' copies of the stage landed
+    float* Xs = Qs + p.H_q * 128;                  // [2][128 rows][16] partial dots of the upper frequencies
+    uint64_t* b_full = (uint64_t*)(Xs + 2 * 128 * 16);   // (even CTA) both CTAs' copies of the stage landed
     uint64_t* b_empty = b_full + p.NS;                   // the pair's MMAs are done with the stage
     uint64_t* t_full = b_empty + p.NS;
     uint64_t* t_empty = t_full + 2;                      // (even CTA) both epilogues released the buffer
@@ -96,7 +99,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&t_full[i], 1);
-            mbar_init(&t_empty[i], 4 * 32 + 4);   // 128 local threads + one arrival per warp of the odd CTA
+            mbar_init(&t_empty[i], 8 * 32 + 8);   // 256 local threads + one arrival per warp of the odd CTA
         }
         mbar_init(m_drain, 1);
         *abort_flag = 0;
@@ -202,15 +205,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue
+        // all eight warps work on every unit: warp w reads TMEM lane quarter w%4 and takes frequency half
+        // `fh` (chunks fh*4 .. fh*4+3); the upper half hands its partial dot products to the lower half
+        // through shared memory, so a unit's epilogue takes half as long and the MMAs of the unit after
+        // next seldom wait for its accumulator
         const int et = threadIdx.x - 64;
-        const int grp = (warp - 2) >> 2;
+        const int fh = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const int64_t mp = p.max_pos;
         uint32_t j = 0;
         int cur_b = -1;
-        // no abort test in the loop conditions: every epilogue thread walks the same tiles and reaches the
-        // same named barriers; after an abort the waits fail at once and the work is skipped
+        // no abort test in the loop conditions: every epilogue thread walks the same tiles and units and
+        // reaches the same named barriers; after an abort the waits fail at once and the work is skipped
         for (int pr = pr_begin; pr < pr_end; ++pr) {
             const int tile = 2 * pr + (int)rank;
             const bool real = tile < p.n_tiles;
@@ -221,7 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
             if (t < p.T) {
                 ps = p.pos ? p.pos[(int64_t)b * p.T + t] : t;
                 if (ps < 0 || ps >= p.max_pos) {
-                    if (grp == 0) flag(p.check, LOWRAM_CHECK_POS_RANGE);
+                    if (fh == 0) flag(p.check, LOWRAM_CHECK_POS_RANGE);
                     ps = ps < 0 ? 0 : p.max_pos - 1;
                 }
             }
@@ -234,85 +241,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                 named_bar_sync(1, 256);
                 cur_b = b;
             }
-            const float* cb = p.rcos + ps;
-            const float* sb = p.rsin + ps;
-            for (int u = 0; u < p.NU; ++u, ++j) {
-                if ((int)(j & 1) != grp) continue;
-                const uint32_t buf = j & 1;
-                if (!mbar_wait_cluster(&t_full[buf], (j >> 1) & 1, abort_flag)) {
-                    fail();
-                    continue;
+            // this token's cos/sin for this half's 32 frequencies, fetched once per tile (64 independent loads)
+            // and kept in registers for every unit of the tile
+            uint64_t c2[16], s2[16];
+            {
+                const float* cb = p.rcos + (int64_t)(fh * 32) * mp + ps;
+                const float* sb = p.rsin + (int64_t)(fh * 32) * mp + ps;
+                float cv[32], sv[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    cv[k] = __ldg(cb + k * mp);
+                    sv[k] = __ldg(sb + k * mp);
                 }
-                fence_after();
-                const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + buf * UN;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    c2[m] = f2_pack(cv[2 * m], cv[2 * m + 1]);
+                    s2[m] = f2_pack(sv[2 * m], sv[2 * m + 1]);
+                }
+            }
+            for (int u = 0; u < p.NU; ++u, ++j) {
+                const uint32_t buf = j & 1;
+                float* xs = Xs + (buf * 128 + row) * 16;
+                const bool ok = mbar_wait_cluster(&t_full[buf], (j >> 1) & 1, abort_flag);
+                if (!ok) fail();
                 uint64_t acc2[HPU][G];     // (even, odd) frequency partial sums of each dot product
 #pragma unroll
                 for (int hx = 0; hx < HPU; ++hx)
 #pragma unroll
                     for (int jq = 0; jq < G; ++jq) acc2[hx][jq] = 0ull;
-                float cn[8], sn[8];
+                if (ok) {
+                    fence_after();
+                    const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + buf * UN + fh * 32;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    cn[k] = __ldg(cb + k * mp);
-                    sn[k] = __ldg(sb + k * mp);
-                }
-#pragma unroll 1
-                for (int c = 0; c < 8; ++c) {       // rotary frequencies c*8 .. c*8+7; the next 8 are prefetched
-                    float cc[8], ss[8];
+                    for (int c = 0; c < 4; ++c) {   // this half's frequencies fh*32 + c*8 .. +7
+                        float x[HPU][8], y[HPU][8];
+                        if (HPU == 2)
+                            tmem_ld_4x8(tb + c * 8, tb + 64 + c * 8, tb + 128 + c * 8, tb + 192 + c * 8, x[0], y[0],
+                                        x[HPU - 1], y[HPU - 1]);
+                        else
+                            tmem_ld_2x8(tb + c * 8, tb + 64 + c * 8, x[0], y[0]);
+                        // packed over pairs of adjacent frequencies (2m, 2m+1): rotate, then dot with the queries
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        cc[k] = cn[k];
-                        ss[k] = sn[k];
-                    }
-                    if (c < 7) {
+                        for (int hx = 0; hx < HPU; ++hx) {
+                            uint64_t kx2[4], ky2[4];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            cn[k] = __ldg(cb + ((c + 1) * 8 + k) * mp);
-                            sn[k] = __ldg(sb + ((c + 1) * 8 + k) * mp);
+                            for (int m = 0; m < 4; ++m) {
+                                const uint64_t x2 = f2_pack(x[hx][2 * m], x[hx][2 * m + 1]);
+                                const uint64_t y2 = f2_pack(y[hx][2 * m], y[hx][2 * m + 1]);
+                                kx2[m] = f2_sub(f2_mul(x2, c2[c * 4 + m]), f2_mul(y2, s2[c * 4 + m]));   // x cos - y sin
+                                ky2[m] = f2_fma(y2, c2[c * 4 + m], f2_mul(x2, s2[c * 4 + m]));    // y cos + x sin
+                            }
+#pragma unroll
+                            for (int jq = 0; jq < G; ++jq) {
+                                const float* qv = Qs + ((u * HPU + hx) * G + jq) * 128 + fh * 32 + c * 8;
+                                const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qv);
+                                const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qv + 4);
+                                const ulonglong2 qc = *reinterpret_cast<const ulonglong2*>(qv + 64);
+                                const ulonglong2 qd = *reinterpret_cast<const ulonglong2*>(qv + 68);
+                                uint64_t a2 = acc2[hx][jq];
+                                a2 = f2_fma(qa.x, kx2[0], a2);
+                                a2 = f2_fma(qa.y, kx2[1], a2);
+                                a2 = f2_fma(qb.x, kx2[2], a2);
+                                a2 = f2_fma(qb.y, kx2[3], a2);
+                                a2 = f2_fma(qc.x, ky2[0], a2);
+                                a2 = f2_fma(qc.y, ky2[1], a2);
+                                a2 = f2_fma(qd.x, ky2[2], a2);
+                                a2 = f2_fma(qd.y, ky2[3], a2);
+                                acc2[hx][jq] = a2;
+                            }
                         }
                     }
-                    float x[HPU][8], y[HPU][8];
-                    if (HPU == 2)
-                        tmem_ld_4x8(tb + c * 8, tb + 64 + c * 8, tb + 128 + c * 8, tb + 192 + c * 8, x[0], y[0],
-                                    x[HPU - 1], y[HPU - 1]);
-                    else
-                        tmem_ld_2x8(tb + c * 8, tb + 64 + c * 8, x[0], y[0]);
-                    // packed over pairs of adjacent frequencies (2m, 2m+1): rotate, then dot with the queries
-                    uint64_t c2[4], s2[4], ns2[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        c2[m] = f2_pack(cc[2 * m], cc[2 * m + 1]);
-                        s2[m] = f2_pack(ss[2 * m], ss[2 * m + 1]);
-                        ns2[m] = f2_pack(-ss[2 * m], -ss[2 * m + 1]);
-                    }
-#pragma unroll
-                    for (int hx = 0; hx < HPU; ++hx) {
-                        uint64_t kx2[4], ky2[4];
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const uint64_t x2 = f2_pack(x[hx][2 * m], x[hx][2 * m + 1]);
-                            const uint64_t y2 = f2_pack(y[hx][2 * m], y[hx][2 * m + 1]);
-                            kx2[m] = f2_fma(x2, c2[m], f2_mul(y2, ns2[m]));   // x cos - y sin
-                            ky2[m] = f2_fma(y2, c2[m], f2_mul(x2, s2[m]));    // y cos + x sin
-                        }
-#pragma unroll
-                        for (int jq = 0; jq < G; ++jq) {
-                            const float* qv = Qs + ((u * HPU + hx) * G + jq) * 128 + c * 8;
-                            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qv);
-                            const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qv + 4);
-                            const ulonglong2 qc = *reinterpret_cast<const ulonglong2*>(qv + 64);
-                            const ulonglong2 qd = *reinterpret_cast<const ulonglong2*>(qv + 68);
-                            uint64_t a2 = acc2[hx][jq];
-                            a2 = f2_fma(qa.x, kx2[0], a2);
-                            a2 = f2_fma(qa.y, kx2[1], a2);
-                            a2 = f2_fma(qb.x, kx2[2], a2);
-                            a2 = f2_fma(qb.y, kx2[3], a2);
-                            a2 = f2_fma(qc.x, ky2[0], a2);
-                            a2 = f2_fma(qc.y, ky2[1], a2);
-                            a2 = f2_fma(qd.x, ky2[2], a2);
-                            a2 = f2_fma(qd.y, ky2[3], a2);
-                            acc2[hx][jq] = a2;
-                        }
+                    fence_before();
+                    if (rank == 0) {
+                        mbar_arrive(&t_empty[buf]);
+                    } else {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote(peer_smem(&t_empty[buf], 0));
                     }
                 }
                 float acc[HPU][G];
@@ -323,25 +327,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                         const float2 v = f2_unpack(acc2[hx][jq]);
                         acc[hx][jq] = v.x + v.y;
                     }
-                fence_before();
-                if (rank == 0) {
-                    mbar_arrive(&t_empty[buf]);
-                } else {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(peer_smem(&t_empty[buf], 0));
-                }
-                if (t < p.T) {
+                if (fh == 1)
+#pragma unroll
+                    for (int hx = 0; hx < HPU; ++hx)
+#pragma unroll
+                        for (int jq = 0; jq < G; ++jq) xs[hx * G + jq] = acc[hx][jq];
+                named_bar_sync(1, 256);      // (exchange buffers alternate by unit, so one barrier per unit)
+                if (fh == 0 && ok && t < p.T) {
 #pragma unroll
                     for (int hx = 0; hx < HPU; ++hx) {
                         const int h = u * HPU + hx;
                         float best = -INFINITY;
 #pragma unroll
-                        for (int jq = 0; jq < G; ++jq) best = fmaxf(best, acc[hx][jq]);
+                        for (int jq = 0; jq < G; ++jq) {
+                            const float sc = acc[hx][jq] + xs[hx * G + jq];
+                            best = fmaxf(best, sc);
+                            if (p.sall) p.sall[((int64_t)b * p.H_q + h * G + jq) * p.T + t] = sc;
+                        }
                         p.key[((int64_t)b * p.H_kv + h) * p.T + t] = best;
-                        if (p.sall)
-#pragma unroll
-                            for (int jq = 0; jq < G; ++jq)
-                                p.sall[((int64_t)b * p.H_q + h * G + jq) * p.T + t] = acc[hx][jq];
                     }
                 }
             }
