@@ -9,9 +9,9 @@ Inputs are seeded synthetic tensors shaped like the workload; nothing is read fr
 
 Timing: W warm-up steps, then K steps.  L2 is flushed (a 256 MB buffer is zeroed) before every layer call,
 outside the CUDA events that bracket the call, so each call reads its cache cold from HBM (consecutive
-layers of a group share the latent coefficients, which would otherwise stay in L2).  Five events per call
-on the launching stream split it into its kernels.  ``value`` = 1000 / (mean over steps of the summed call
-times).  Multi-GPU (torchrun): every rank runs its own replica of the workload (no data-path collective);
+layers of a group share the latent coefficients, which would otherwise stay in L2).  Two events per call on
+the launching stream bracket it; ``value`` = 1000 / (mean over steps of the summed call times).  One more
+step with events between the kernels (which serialises them) gives the per-kernel breakdown.  Multi-GPU (torchrun): every rank runs its own replica of the workload (no data-path collective);
 the slowest rank's time and the sum of work give the job's throughput.
 
     python bench.py [--steps K] [--warmup W] [--workload llama8b] [--impl lowram|reference]
@@ -346,7 +346,8 @@ def main():
     if L.lowram_get_error(ws):
         raise RuntimeError("device check word set during warm-up")
 
-    # timed region: K steps x L calls, 5 events per call
+    # timed region: K steps x L calls; one event before and one after each call, none between its kernels (so
+    # the kernels' programmatic dependent launches overlap as they do in use)
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(w.L)] for _ in range(args.steps)]
     for step in evs:
         for e5 in step:
@@ -361,27 +362,37 @@ def main():
     for s in range(args.steps):
         for l in range(w.L):
             flush.zero_()
-            call(l, events=evs[s][l])
+            e5 = evs[s][l]
+            call(l, events=[e5[0], None, None, None, e5[4]])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     clk = clocks.stop()
-    stage = np.zeros((args.steps, w.L, 4))
-    for s in range(args.steps):
-        for l in range(w.L):
-            e = evs[s][l]
-            for k in range(4):
-                stage[s, l, k] = e[k].elapsed_time(e[k + 1])
-    step_ms = stage.sum(axis=(1, 2))
+    call_ms = np.array([[evs[s][l][0].elapsed_time(evs[s][l][4]) for l in range(w.L)] for s in range(args.steps)])
+    step_ms = call_ms.sum(axis=1)
     ms_per_step = float(step_ms.mean())
     if dist:
         t = torch.tensor([ms_per_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_per_step = float(t.item())
     value = world * 1000.0 / ms_per_step
-    per_kernel_ms = stage.mean(axis=(0, 1))          # K1 keys, K2 select, K3 values, K4 merge
+
+    # per-kernel breakdown (one more step with events between the kernels, which serialise them)
+    stage = np.zeros((w.L, 4))
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(w.L)]
+    for e5 in bev:
+        for e in e5:
+            e.record()
+    for l in range(w.L):
+        flush.zero_()
+        call(l, events=bev[l])
+    torch.cuda.synchronize()
+    for l in range(w.L):
+        for k in range(4):
+            stage[l, k] = bev[l][k].elapsed_time(bev[l][k + 1])
+    per_kernel_ms = stage.mean(axis=0)          # K1 keys, K2 select, K3 values (+ merge), K4 merge
     names = ["score", "select", "vregen", "merge"]
     dom = int(np.argmax(per_kernel_ms))
 

@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_k
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* v = values + (int64_t)row * T;
     int32_t* o = out + (int64_t)row * n_keep;
+    grid_dep_trigger();
+    grid_dep_wait();     // the keys come from the kernel before (launched with launch_pdl)
     if (x.zero_cnt && tid == 0) x.zero_cnt[row] = 0;
     if (n_keep <= 0) return;
     if (n_keep >= T) {
@@ -198,9 +200,12 @@ cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, in
         cudaError_t e = cudaFuncSetAttribute(select_topn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)(sizeof(uint32_t) * kSelMaxStaged));
         if (e != cudaSuccess) return e;
-        select_topn_kernel<true><<<(unsigned)P, kSelThreads, smem, st>>>(T, n_keep, values, out, x);
+        e = launch_pdl(select_topn_kernel<true>, dim3((unsigned)P), dim3(kSelThreads), smem, st, T, n_keep, values, out, x);
+        if (e != cudaSuccess) return e;
     } else {
-        select_topn_kernel<false><<<(unsigned)P, kSelThreads, 0, st>>>(T, n_keep, values, out, x);
+        cudaError_t e = launch_pdl(select_topn_kernel<false>, dim3((unsigned)P), dim3(kSelThreads), 0, st, T, n_keep,
+                                   values, out, x);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

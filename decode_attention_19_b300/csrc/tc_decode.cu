@@ -87,6 +87,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();          // 0 issues the MMAs; 1 feeds its halves
+    grid_dep_trigger();  // the selection kernel may be scheduled as SMs free up; it waits for this grid
     const uint32_t peer = rank ^ 1u;
     // the pair walks a contiguous range of tile pairs; CTA `rank` takes tile 2*pair + rank (a tile past the
     // end is computed on the last tile's data and not written)

@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(kVThreads, 2)
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dep_wait();     // selection, residual rows and logits come from the kernels before (launch_pdl)
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -623,8 +624,7 @@ cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     auto go = [&](auto kern) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess) {
-            kern<<<grid, kVThreads, smem, st>>>(mW, mW1, p);
-            e = cudaGetLastError();
+            e = launch_pdl(kern, grid, dim3(kVThreads), smem, st, mW, mW1, p);
         }
     };
     switch (s.H_q / s.H_kv) {
