@@ -9,6 +9,7 @@
 // groups, then warps, merge their states at the end.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace lowram {
 
@@ -194,6 +195,179 @@ __global__ void __launch_bounds__(kDenseThreads) dense_kernel(int T, int H_q, in
     }
 }
 
+// ------------------------------------------------------------------------------------------------
+// bf16, d = 128: instruction-lean form.  A CTA of four warps per (kv-head, token range, sequence); each warp
+// streams blocks of 16 tokens of K and V through its own two-stage cp.async ring in shared memory (16 KB per
+// warp, so twelve warps fit on an SM) and keeps an online softmax per q-head:
+//   scores   two lanes per token, 64 features each: the K row halves (read back swizzled, conflict-free)
+//            against the q-heads (pre-scaled, fp32 in shared memory), packed fp32x2 FMAs, one shuffle to add;
+//   weights  block max and sum by warp reductions, one exp per (token, q-head);
+//   values   lane = 4 features: each token's V row (8 bytes per lane) times its weight, broadcast by shuffle.
+// The CTA's warps merge their states in shared memory and write one partial record per (sequence, q-head).
+// ------------------------------------------------------------------------------------------------
+constexpr int kD2Warps = 4;
+constexpr int kD2Threads = 32 * kD2Warps;
+constexpr int kD2Rows = 16;                  // tokens per warp block
+constexpr int kD2Stage = kD2Rows * 256;      // 16 token rows of 128 bf16
+
+size_t dense2_smem(int G) {   // queries + rings; the rings also hold the warps' final states
+    return (size_t)G * 128 * 4 + std::max((size_t)kD2Warps * 4 * kD2Stage, (size_t)kD2Warps * G * 130 * 4);
+}
+
+__device__ __forceinline__ void bf16x2_to_f2(uint32_t w, uint64_t& out) {
+    out = tc::f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+template <int G>
+__global__ void __launch_bounds__(kD2Threads) dense_bf16_kernel(int T, int H_q, int H_kv, float scale,
+                                                                const __nv_bfloat16* __restrict__ q,
+                                                                const __nv_bfloat16* __restrict__ K,
+                                                                const __nv_bfloat16* __restrict__ V,
+                                                                float* __restrict__ partial, int n_split) {
+    using namespace tc;
+    extern __shared__ __align__(16) uint8_t dsm[];
+    float* Qs = reinterpret_cast<float*>(dsm);
+    const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint8_t* wbase = dsm + G * 128 * 4 + warp * 4 * kD2Stage;   // Kt[2], Vt[2]
+    const int per = (int)cdiv(T, n_split);
+    const int t_begin = split * per, t_end = min(T, t_begin + per);
+    for (int e = tid; e < G * 128; e += kD2Threads)
+        Qs[e] = __bfloat162float(q[((int64_t)b * H_q + h * G) * 128 + e]) * scale;
+    __syncthreads();
+    const int nblk = t_end > t_begin ? (int)cdiv(t_end - t_begin, kD2Rows) : 0;
+    auto issue = [&](int k) {
+        const int blk = warp + k * kD2Warps;
+        if (blk < nblk) {
+            const int t0 = t_begin + blk * kD2Rows;
+            uint8_t* Kt = wbase + (k & 1) * kD2Stage;
+            uint8_t* Vt = wbase + (2 + (k & 1)) * kD2Stage;
+#pragma unroll 4
+            for (int i = lane; i < kD2Rows * 16; i += 32) {
+                const int r = i >> 4, c = i & 15;
+                const int t = t0 + r;
+                const bool ok = t < t_end;
+                const int64_t off = (((int64_t)b * T + (ok ? t : t_begin)) * H_kv + h) * 128 + c * 8;
+                cp_async16(reinterpret_cast<uint4*>(Kt + r * 256 + ((c ^ (r & 15)) << 4)), K + off, ok);
+                cp_async16(reinterpret_cast<uint4*>(Vt + r * 256 + (c << 4)), V + off, ok);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    float m[G], l[G];
+    uint64_t acc[G][2];
+#pragma unroll
+    for (int jq = 0; jq < G; ++jq) {
+        m[jq] = -INFINITY;
+        l[jq] = 0.0f;
+        acc[jq][0] = acc[jq][1] = 0ull;
+    }
+    issue(0);
+    for (int k = 0; warp + k * kD2Warps < nblk; ++k) {
+        issue(k + 1);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncwarp();
+        const uint8_t* Kt = wbase + (k & 1) * kD2Stage;
+        const uint8_t* Vt = wbase + (2 + (k & 1)) * kD2Stage;
+        const int t0 = t_begin + (warp + k * kD2Warps) * kD2Rows;
+        const int r = lane >> 1, fh = lane & 1;          // scores: token r, feature half fh
+        const bool valid = t0 + r < t_end;
+        uint64_t s2[G];
+#pragma unroll
+        for (int jq = 0; jq < G; ++jq) s2[jq] = 0ull;
+#pragma unroll 4
+        for (int c8 = 0; c8 < 8; ++c8) {
+            const int c = fh * 8 + c8;
+            const uint4 kv = *reinterpret_cast<const uint4*>(Kt + r * 256 + ((c ^ (r & 15)) << 4));
+            uint64_t kp[4];
+            bf16x2_to_f2(kv.x, kp[0]);
+            bf16x2_to_f2(kv.y, kp[1]);
+            bf16x2_to_f2(kv.z, kp[2]);
+            bf16x2_to_f2(kv.w, kp[3]);
+#pragma unroll
+            for (int jq = 0; jq < G; ++jq) {
+                const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(Qs + jq * 128 + c * 8);
+                const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(Qs + jq * 128 + c * 8 + 4);
+                s2[jq] = f2_fma(qa.x, kp[0], s2[jq]);
+                s2[jq] = f2_fma(qa.y, kp[1], s2[jq]);
+                s2[jq] = f2_fma(qb.x, kp[2], s2[jq]);
+                s2[jq] = f2_fma(qb.y, kp[3], s2[jq]);
+            }
+        }
+        // weights of the block (both lanes of a token hold its score), online softmax update
+        float p[G];
+#pragma unroll
+        for (int jq = 0; jq < G; ++jq) {
+            const float2 sv = f2_unpack(s2[jq]);
+            float part = sv.x + sv.y;
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            const float sc = valid ? part : -INFINITY;
+            const float mn = fmaxf(m[jq], warp_max(sc));
+            const float f = (m[jq] == -INFINITY) ? 0.0f : __expf(m[jq] - mn);
+            p[jq] = valid ? __expf(sc - mn) : 0.0f;
+            l[jq] = l[jq] * f + 0.5f * warp_sum(p[jq]);   // every token counted by its two lanes
+            const uint64_t f2 = f2_pack(f, f);
+            acc[jq][0] = f2_mul(acc[jq][0], f2);
+            acc[jq][1] = f2_mul(acc[jq][1], f2);
+            m[jq] = mn;
+        }
+        // values: lane = features 4*lane .. 4*lane+3; token t's weight sits in lane 2t
+#pragma unroll 8
+        for (int t = 0; t < kD2Rows; ++t) {
+            const uint2 vv = *reinterpret_cast<const uint2*>(Vt + t * 256 + lane * 8);
+            uint64_t vp0, vp1;
+            bf16x2_to_f2(vv.x, vp0);
+            bf16x2_to_f2(vv.y, vp1);
+#pragma unroll
+            for (int jq = 0; jq < G; ++jq) {
+                const float pt = __shfl_sync(0xffffffffu, p[jq], 2 * t);
+                const uint64_t p2 = f2_pack(pt, pt);
+                acc[jq][0] = f2_fma(p2, vp0, acc[jq][0]);
+                acc[jq][1] = f2_fma(p2, vp1, acc[jq][1]);
+            }
+        }
+        __syncwarp();   // this stage is read; the next issue refills it
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // combine the warps' softmax states through shared memory (the rings are free): one record per CTA
+    __syncthreads();
+    float* st = reinterpret_cast<float*>(dsm + G * 128 * 4);     // [kD2Warps][G][130]
+#pragma unroll
+    for (int jq = 0; jq < G; ++jq) {
+        float* w = st + (warp * G + jq) * 130;
+        const float2 a0 = f2_unpack(acc[jq][0]), a1 = f2_unpack(acc[jq][1]);
+        *reinterpret_cast<float2*>(w + lane * 4) = a0;
+        *reinterpret_cast<float2*>(w + lane * 4 + 2) = a1;
+        if (lane == 0) {
+            w[128] = m[jq];
+            w[129] = l[jq];
+        }
+    }
+    __syncthreads();
+    for (int jq = warp; jq < G; jq += kD2Warps) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kD2Warps; ++w) M = fmaxf(M, st[(w * G + jq) * 130 + 128]);
+        float L = 0.0f, a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int w = 0; w < kD2Warps; ++w) {
+            const float* src = st + (w * G + jq) * 130;
+            const float mw = src[128];
+            const float f = (mw == -INFINITY) ? 0.0f : __expf(mw - M);
+            L = fmaf(f, src[129], L);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] = fmaf(f, src[lane * 4 + e], a[e]);
+        }
+        float* dst = partial + (((int64_t)b * H_q + h * G + jq) * n_split + split) * 130;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[lane * 4 + e] = a[e];
+        if (lane == 0) {
+            dst[128] = M;
+            dst[129] = L;
+        }
+    }
+}
+
 int dense_splits(int B, int T, int H_kv) {
     const int64_t units = (int64_t)B * H_kv;
     if (units == 0 || T == 0) return 1;
@@ -229,9 +403,35 @@ static cudaError_t dense_g(int B, int T, int H_q, int H_kv, float scale, const v
     return e;
 }
 
+int dense_records(int B, int T, int H_kv, int, int) { return dense_splits(B, T, H_kv); }
+
+template <int G>
+static cudaError_t dense2_go(int B, int T, int H_q, int H_kv, float scale, const void* q, const void* k, const void* v,
+                             float* partial, int n_split, cudaStream_t st) {
+    const size_t smem = dense2_smem(G);
+    cudaError_t e = cudaFuncSetAttribute(dense_bf16_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // the kv-heads of one token range are adjacent in launch order (they read the same token rows)
+    dim3 grid((unsigned)H_kv, (unsigned)n_split, (unsigned)B);
+    dense_bf16_kernel<G><<<grid, kD2Threads, smem, st>>>(T, H_q, H_kv, scale, (const __nv_bfloat16*)q,
+                                                        (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, partial,
+                                                        n_split);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_dense(int B, int T, int H_q, int H_kv, int d, int dtype, float scale, const void* q, const void* k,
                          const void* v, float* partial, int n_split, cudaStream_t st) {
     if (B == 0) return cudaSuccess;
+    if (dtype == LOWRAM_BF16 && d == 128) {
+        switch (H_q / H_kv) {
+            case 1: return dense2_go<1>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            case 2: return dense2_go<2>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            case 4: return dense2_go<4>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            case 7: return dense2_go<7>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            case 8: return dense2_go<8>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            default: return cudaErrorNotSupported;
+        }
+    }
     if (dtype == LOWRAM_BF16) {
         if (d == 128) return dense_g<__nv_bfloat16, 128>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
         if (d == 64) return dense_g<__nv_bfloat16, 64>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);

@@ -104,8 +104,9 @@ cudaError_t launch_project(const CompressArgs& a, cudaStream_t st);
 cudaError_t launch_predict_err(const CompressArgs& a, int layer, float* err, cudaStream_t st);
 cudaError_t launch_residual_rows(const CompressArgs& a, int layer, cudaStream_t st);
 
-// Comparator
+// Comparator: token splits, and partial records per (sequence, q-head) that launch_dense writes
 int dense_splits(int B, int T, int H_kv);
+int dense_records(int B, int T, int H_kv, int d, int dtype);
 cudaError_t launch_dense(int B, int T, int H_q, int H_kv, int d, int dtype, float scale, const void* q, const void* k,
                          const void* v, float* partial, int n_split, cudaStream_t st);
 

@@ -346,8 +346,8 @@ lowram_status lowram_compress(const lowram_compress_shape* shape, const void* ke
 lowram_status lowram_dense_workspace_size(int32_t B, int32_t T, int32_t H_q, int32_t H_kv, int32_t d, size_t* bytes) {
     if (B < 0 || T < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv || (d != 64 && d != 128) || !bytes)
         return fail(LOWRAM_ERR_INVALID_ARG, "bad dense shape");
-    const int ns = dense_splits(B, T, H_kv);
-    *bytes = kHeader + align256(sizeof(float) * (size_t)B * H_q * ns * (d + 2));
+    const int nr = dense_records(B, T, H_kv, d, LOWRAM_BF16);
+    *bytes = kHeader + align256(sizeof(float) * (size_t)B * H_q * nr * (d + 2));
     return LOWRAM_OK;
 }
 
@@ -375,7 +375,7 @@ lowram_status lowram_dense_decode_attn(int32_t B, int32_t T, int32_t H_q, int32_
         e = launch_dense(B, T, H_q, H_kv, d, dtype, scale, q, k, v, partial, ns, cs);
         if (e != cudaSuccess) return cuda_fail(e, "dense");
     }
-    e = launch_merge(B, H_q, T > 0 ? ns : 0, d, partial, out, lse, cs);
+    e = launch_merge(B, H_q, T > 0 ? dense_records(B, T, H_kv, d, dtype) : 0, d, partial, out, lse, cs);
     return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "merge");
 }
 
