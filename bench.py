@@ -107,6 +107,18 @@ def algorithmic(w):
     return bytes_, f_keys, f_sel, f_mlp
 
 
+def job_throughput(ms_per_step_local: float, world: int, dist=None, device=None):
+    """Whole-job steps/s of `world` replicas that each ran the same per-rank work: the slowest rank's step
+    time bounds the job (max over ranks, the only collective), and the job completes `world` steps in it.
+    Returns (steps/s, max ms per step)."""
+    ms = float(ms_per_step_local)
+    if dist is not None and world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return world * 1000.0 / ms, ms
+
+
 def launches_per_call(w, tc_path):
     """Kernels one decode call launches: keys, selection, values (+ a separate merge unless the tensor-core
     value pass merges as it finishes, which it does for predictor widths of 128 or 256)."""
@@ -372,12 +384,7 @@ def main():
     clk = clocks.stop()
     call_ms = np.array([[evs[s][l][0].elapsed_time(evs[s][l][4]) for l in range(w.L)] for s in range(args.steps)])
     step_ms = call_ms.sum(axis=1)
-    ms_per_step = float(step_ms.mean())
-    if dist:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = world * 1000.0 / ms_per_step
+    value, ms_per_step = job_throughput(float(step_ms.mean()), world, dist, dev)
 
     # per-kernel breakdown (one more step with events between the kernels, which serialise them)
     stage = np.zeros((w.L, 4))
@@ -427,12 +434,8 @@ def main():
             st.synchronize()
             if s >= args.warmup:
                 e2e_ms.append(sum(a.elapsed_time(b) for a, b in pairs))
-        m = float(np.mean(e2e_ms))
-        if dist:
-            t = torch.tensor([m], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            m = float(t.item())
-        e2e = {"value": world * 1000.0 / m, "unit": UNIT,
+        e2e_value, m = job_throughput(float(np.mean(e2e_ms)), world, dist, dev)
+        e2e = {"value": e2e_value, "unit": UNIT,
                "h2d_bytes_per_step": w.L * qs[0].numel() * qs[0].element_size(),
                "d2h_bytes_per_step": w.L * out.numel() * out.element_size(), "ms_per_step": m}
 
