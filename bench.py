@@ -484,6 +484,8 @@ def main():
             "clocks": clk, "peaks": pk_kind}
     if e2e:
         line["e2e"] = e2e
+    if args.dense and w.act == "bf16":   # before the CPU baseline, while the GPU is still at its working clocks
+        line["dense_comparator"] = dense_bench(w, dev, qs, flush, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle as O
         inp = oracle_sample_inputs(w)
@@ -492,8 +494,6 @@ def main():
         line["cpu_baseline"] = {"value": 1.0 / t_step, "unit": UNIT, "cores": O.max_threads(), "kind": "oracle",
                                 "sample": f"one layer call of 1 of {w.B} sequences (all kv-heads, T={w.T}), "
                                           f"median of 3, x{w.B * w.L} per step"}
-    if args.dense and w.act == "bf16":
-        line["dense_comparator"] = dense_bench(w, dev, qs, flush, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
