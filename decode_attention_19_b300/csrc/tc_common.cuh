@@ -224,6 +224,51 @@ __device__ __forceinline__ void tmem_ld_4x8(uint32_t t0, uint32_t t1, uint32_t t
         d[i] = __uint_as_float(r[24 + i]);
     }
 }
+// Four tcgen05.ld.16x256b.x2 loads, then one wait.  Each reads 16 TMEM lanes (L .. L+15, L from the address) and
+// 16 columns (C .. C+15): thread t receives lane L + t/4 at columns C + 2(t%4) and C + 2(t%4) + 1 in v[0], v[1],
+// lane L + 8 + t/4 at the same columns in v[2], v[3], and the same four for columns C + 8 .. C + 15 in v[4..7].
+__device__ __forceinline__ void tmem_ld_16x256b_4x2(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, float (&a)[8],
+                                                    float (&b)[8], float (&c)[8], float (&d)[8]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%33];\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%34];\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%24, %25, %26, %27, %28, %29, %30, %31}, [%35];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(t0), "r"(t1), "r"(t2), "r"(t3)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        a[i] = __uint_as_float(r[i]);
+        b[i] = __uint_as_float(r[8 + i]);
+        c[i] = __uint_as_float(r[16 + i]);
+        d[i] = __uint_as_float(r[24 + i]);
+    }
+}
+
+// Two tcgen05.ld.16x256b.x2 loads (fragment layout as for tmem_ld_16x256b_4x2), then one wait.
+__device__ __forceinline__ void tmem_ld_16x256b_2x2(uint32_t t0, uint32_t t1, float (&a)[8], float (&b)[8]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(t0), "r"(t1)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        a[i] = __uint_as_float(r[i]);
+        b[i] = __uint_as_float(r[8 + i]);
+    }
+}
+
 __device__ __forceinline__ void tmem_ld_2x8(uint32_t t0, uint32_t t1, float (&a)[8], float (&b)[8]) {
     uint32_t r[16];
     asm volatile(

@@ -9,8 +9,9 @@
 // value pass takes the softmax of the selected tokens from exactly the scores the selection saw.
 //
 // Shape of the kernel: persistent CTA pairs (clusters of two, at most one CTA per SM), 320 threads per CTA.
-// A pair walks a contiguous range of tile pairs; CTA r of the pair takes tile 2*pair + r.  The key rebuild
-// of a unit of UN/128 kv-heads is one pair MMA per k-step (tcgen05 cta_group::2, M=256, N=UN, K=16): each
+// The work items are (tile pair, unit) in that order; a pair of CTAs walks a contiguous range of items, so the
+// ranges differ by at most one unit (rather than by a whole tile pair of NU units), and CTA r of the pair takes
+// tile 2*pair + r.  The key rebuild of a unit of UN/128 kv-heads is one pair MMA per k-step (tcgen05 cta_group::2, M=256, N=UN, K=16): each
 // CTA supplies its tile's 128 token rows of A and half of the unit's basis rows of B, and each CTA's TMEM
 // accumulates its own 128 tokens x UN features.  Compared with one CTA per tile, every SM reads only half
 // of each basis chunk from shared memory.
@@ -58,8 +59,8 @@ struct ScoreTcParams {
 
 // Stage s of the ring: one 64-wide k-chunk of the latent tile [128 x 64] and of the unit's basis rows
 // [UN x 64], both 128B-swizzled as TMA writes them.
-// Beside the ring: the queries of the current sequence (fp32, pre-scaled) and, double-buffered by unit, the
-// exchange of the upper frequency half's partial dot products [2][128][16] fp32.
+// Beside the ring: the queries of the current sequence (fp32, pre-scaled, grouped by frequency pair) and,
+// double-buffered by unit, the exchange of partial dot products between the frequency halves [2][128][16] fp32.
 size_t score_smem_bytes(int NS, int UN, int H_q) {
     return 1024 + (size_t)NS * (kAChunkBytes + (UN / 2) * 128) + (size_t)H_q * 128 * 4 + 2 * 128 * 16 * 4 +
            8 * (2 * NS + 5) + 16;
@@ -75,7 +76,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* St = smem;
-    float* Qs = (float*)(St + p.NS * kStage);     // [H_q][128] query of the current sequence x scale
+    float* Qs = (float*)(St + p.NS * kStage);     // [H_q][32][4] query of the current sequence x scale
     float* Xs = Qs + p.H_q * 128;                  // [2][128 rows][16] partial dots of the upper frequencies
     uint64_t* b_full = (uint64_t*)(Xs + 2 * 128 * 16);   // (even CTA) both CTAs' copies of the stage landed
     uint64_t* b_empty = b_full + p.NS;                   // the pair's MMAs are done with the stage
@@ -89,10 +90,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
     const uint32_t rank = cluster_rank();          // 0 issues the MMAs; 1 feeds its halves
     grid_dep_trigger();  // the selection kernel may be scheduled as SMs free up; it waits for this grid
     const uint32_t peer = rank ^ 1u;
-    // the pair walks a contiguous range of tile pairs; CTA `rank` takes tile 2*pair + rank (a tile past the
-    // end is computed on the last tile's data and not written)
-    const int n_pairs = (p.n_tiles + 1) / 2, cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
-    const int pr_begin = (int)((int64_t)cl * n_pairs / ncl), pr_end = (int)((int64_t)(cl + 1) * n_pairs / ncl);
+    // the pair walks a contiguous range of (tile pair, unit) items; CTA `rank` takes tile 2*pair + rank (a tile
+    // past the end is computed on the last tile's data and not written)
+    const int n_items = (p.n_tiles + 1) / 2 * p.NU, cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const int it_begin = (int)((int64_t)cl * n_items / ncl), it_end = (int)((int64_t)(cl + 1) * n_items / ncl);
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.NS; ++i) {
             mbar_init(&b_full[i], 1);
@@ -130,10 +131,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
         // ------------------------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
             uint32_t ib = 0;
-            for (int pr = pr_begin; pr < pr_end && !*abort_flag; ++pr) {
+            for (int it = it_begin; it < it_end && !*abort_flag; ++it) {
+                const int pr = it / p.NU, u = it - pr * p.NU;
                 const int lt = min(2 * pr + (int)rank, p.n_tiles - 1);
                 const int b = lt / p.tiles_per_seq, t0 = (lt % p.tiles_per_seq) * kTokTile;
-                for (int u = 0; u < p.NU; ++u) {
+                {
                     for (int kc = 0; kc < p.KC; ++kc, ++ib) {
                         const uint32_t s = ib % p.NS, ph = (ib / p.NS) & 1;
                         if (!mbar_wait_cluster(&b_empty[s], ph ^ 1, abort_flag)) {
@@ -172,8 +174,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
             // -------------------------------------------------------------- MMA issuer (even CTA)
             const uint32_t idesc = idesc_bf16(2 * kTokTile, UN);
             uint32_t ib = 0, j = 0;
-            for (int pr = pr_begin; pr < pr_end && !*abort_flag; ++pr) {
-                for (int u = 0; u < p.NU; ++u, ++j) {
+            for (int it = it_begin; it < it_end && !*abort_flag; ++it, ++j) {
+                {
                     const uint32_t buf = j & 1;
                     if (!mbar_wait_cluster(&t_empty[buf], ((j >> 1) & 1) ^ 1, abort_flag)) {
                         fail();
@@ -206,147 +208,193 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue
-        // all eight warps work on every unit: warp w reads TMEM lane quarter w%4 and takes frequency half
-        // `fh` (chunks fh*4 .. fh*4+3); the upper half hands its partial dot products to the lower half
-        // through shared memory, so a unit's epilogue takes half as long and the MMAs of the unit after
-        // next seldom wait for its accumulator
+        // all eight warps work on every unit: warp w reads TMEM lane quarter w%4 and takes frequency half `fh`.
+        // TMEM is read in the 16x256b shape, so a thread holds four tokens (rows quarter*32 + 16*lh + 8*i + r8,
+        // lh, i in {0, 1}) and eight frequencies (fh*32 + 8c + 2*g4 + e, c in 0..3, e in {0, 1}); every query
+        // value it loads from shared memory serves LHP*2 tokens.  The partial dot products are summed over the four
+        // lanes that share a token (g4) with shuffles, and the two frequency halves meet through shared memory.
+        constexpr int LHP = (G <= 4) ? 2 : 1;     // lane halves (token pairs) per pass over the accumulator
+        constexpr int R = 2 * LHP;                // tokens per pass
         const int et = threadIdx.x - 64;
         const int fh = (warp - 2) >> 2;
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
+        const int g4 = lane & 3, r8 = lane >> 2, b0 = lane & 1, b1 = (lane >> 1) & 1;
         const int64_t mp = p.max_pos;
+        // the token this thread finishes (adds the other half's partial sums, takes the maximum and stores):
+        // LHP == 2: the lower frequency half finishes all rows, one per lane;
+        // LHP == 1: the frequency half fh finishes the rows of lane half lh == fh (lanes with b1 == 0)
+        const int frow = (LHP == 2) ? quarter * 32 + 16 * b0 + 8 * b1 + r8 : quarter * 32 + 16 * fh + 8 * b0 + r8;
+        const bool finisher = (LHP == 2) ? (fh == 0) : (b1 == 0);
         uint32_t j = 0;
-        int cur_b = -1;
-        // no abort test in the loop conditions: every epilogue thread walks the same tiles and units and
-        // reaches the same named barriers; after an abort the waits fail at once and the work is skipped
-        for (int pr = pr_begin; pr < pr_end; ++pr) {
-            const int tile = 2 * pr + (int)rank;
-            const bool real = tile < p.n_tiles;
-            const int lt = real ? tile : p.n_tiles - 1;
-            const int b = lt / p.tiles_per_seq, t0 = (lt % p.tiles_per_seq) * kTokTile;
-            const int t = real ? t0 + row : p.T;   // a tile past the end writes nothing
-            int ps = 0;
-            if (t < p.T) {
-                ps = p.pos ? p.pos[(int64_t)b * p.T + t] : t;
-                if (ps < 0 || ps >= p.max_pos) {
-                    if (fh == 0) flag(p.check, LOWRAM_CHECK_POS_RANGE);
-                    ps = ps < 0 ? 0 : p.max_pos - 1;
-                }
-            }
-            if (b != cur_b) {
-                named_bar_sync(1, 256);      // every epilogue thread is done with the previous query
-                if (!*abort_flag) {
-                    const __nv_bfloat16* qb = p.q + (int64_t)b * p.H_q * 128;
-                    for (int e = et; e < p.H_q * 128; e += 256) Qs[e] = __bfloat162float(qb[e]) * p.scale;
-                }
-                named_bar_sync(1, 256);
-                cur_b = b;
-            }
-            // this token's cos/sin for this half's 32 frequencies, fetched once per tile (64 independent loads)
-            // and kept in registers for every unit of the tile
-            uint64_t c2[16], s2[16];
-            {
-                const float* cb = p.rcos + (int64_t)(fh * 32) * mp + ps;
-                const float* sb = p.rsin + (int64_t)(fh * 32) * mp + ps;
-                float cv[32], sv[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    cv[k] = __ldg(cb + k * mp);
-                    sv[k] = __ldg(sb + k * mp);
-                }
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    c2[m] = f2_pack(cv[2 * m], cv[2 * m + 1]);
-                    s2[m] = f2_pack(sv[2 * m], sv[2 * m + 1]);
-                }
-            }
-            for (int u = 0; u < p.NU; ++u, ++j) {
-                const uint32_t buf = j & 1;
-                float* xs = Xs + (buf * 128 + row) * 16;
-                const bool ok = mbar_wait_cluster(&t_full[buf], (j >> 1) & 1, abort_flag);
-                if (!ok) fail();
-                uint64_t acc2[HPU][G];     // (even, odd) frequency partial sums of each dot product
-#pragma unroll
-                for (int hx = 0; hx < HPU; ++hx)
-#pragma unroll
-                    for (int jq = 0; jq < G; ++jq) acc2[hx][jq] = 0ull;
-                if (ok) {
-                    fence_after();
-                    const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + buf * UN + fh * 32;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {   // this half's frequencies fh*32 + c*8 .. +7
-                        float x[HPU][8], y[HPU][8];
-                        if (HPU == 2)
-                            tmem_ld_4x8(tb + c * 8, tb + 64 + c * 8, tb + 128 + c * 8, tb + 192 + c * 8, x[0], y[0],
-                                        x[HPU - 1], y[HPU - 1]);
-                        else
-                            tmem_ld_2x8(tb + c * 8, tb + 64 + c * 8, x[0], y[0]);
-                        // packed over pairs of adjacent frequencies (2m, 2m+1): rotate, then dot with the queries
-#pragma unroll
-                        for (int hx = 0; hx < HPU; ++hx) {
-                            uint64_t kx2[4], ky2[4];
-#pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                const uint64_t x2 = f2_pack(x[hx][2 * m], x[hx][2 * m + 1]);
-                                const uint64_t y2 = f2_pack(y[hx][2 * m], y[hx][2 * m + 1]);
-                                kx2[m] = f2_sub(f2_mul(x2, c2[c * 4 + m]), f2_mul(y2, s2[c * 4 + m]));   // x cos - y sin
-                                ky2[m] = f2_fma(y2, c2[c * 4 + m], f2_mul(x2, s2[c * 4 + m]));    // y cos + x sin
-                            }
-#pragma unroll
-                            for (int jq = 0; jq < G; ++jq) {
-                                const float* qv = Qs + ((u * HPU + hx) * G + jq) * 128 + fh * 32 + c * 8;
-                                const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qv);
-                                const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qv + 4);
-                                const ulonglong2 qc = *reinterpret_cast<const ulonglong2*>(qv + 64);
-                                const ulonglong2 qd = *reinterpret_cast<const ulonglong2*>(qv + 68);
-                                uint64_t a2 = acc2[hx][jq];
-                                a2 = f2_fma(qa.x, kx2[0], a2);
-                                a2 = f2_fma(qa.y, kx2[1], a2);
-                                a2 = f2_fma(qb.x, kx2[2], a2);
-                                a2 = f2_fma(qb.y, kx2[3], a2);
-                                a2 = f2_fma(qc.x, ky2[0], a2);
-                                a2 = f2_fma(qc.y, ky2[1], a2);
-                                a2 = f2_fma(qd.x, ky2[2], a2);
-                                a2 = f2_fma(qd.y, ky2[3], a2);
-                                acc2[hx][jq] = a2;
-                            }
+        int cur_b = -1, cur_pr = -1;
+        int b = 0, t0 = 0;
+        bool real = false;
+        // cos/sin of this thread's frequencies (f, f+1), f = fh*32 + 8c + 2*g4, at each of its four tokens'
+        // positions ([2*lh + i][c]); fetched once per tile and kept in registers for every unit of the tile
+        uint64_t c2[4][4], s2[4][4];
+        // no abort test in the loop conditions: every epilogue thread walks the same items and reaches the
+        // same named barriers; after an abort the waits fail at once and the work is skipped
+        for (int it = it_begin; it < it_end; ++it, ++j) {
+            const int pr = it / p.NU, u = it - pr * p.NU;
+            if (pr != cur_pr) {
+                cur_pr = pr;
+                const int tile = 2 * pr + (int)rank;
+                real = tile < p.n_tiles;      // a tile past the end is computed but writes nothing
+                const int lt = real ? tile : p.n_tiles - 1;
+                b = lt / p.tiles_per_seq;
+                t0 = (lt % p.tiles_per_seq) * kTokTile;
+                if (b != cur_b) {
+                    named_bar_sync(1, 256);      // every epilogue thread is done with the previous query
+                    if (!*abort_flag) {
+                        // Qs[q-head][frequency pair fp][4] = scale * (q[2fp], q[2fp+1], q[64+2fp], q[64+2fp+1])
+                        const __nv_bfloat16* qb = p.q + (int64_t)b * p.H_q * 128;
+                        for (int e = et; e < p.H_q * 128; e += 256) {
+                            const int qh = e >> 7, fp = (e >> 2) & 31, k = e & 3;
+                            const int dim = (k < 2) ? 2 * fp + k : 64 + 2 * fp + (k - 2);
+                            Qs[e] = __bfloat162float(qb[qh * 128 + dim]) * p.scale;
                         }
                     }
-                    fence_before();
-                    if (rank == 0) {
-                        mbar_arrive(&t_empty[buf]);
-                    } else {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_remote(peer_smem(&t_empty[buf], 0));
+                    named_bar_sync(1, 256);
+                    cur_b = b;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = t0 + quarter * 32 + 16 * (k >> 1) + 8 * (k & 1) + r8;
+                    int ps = 0;
+                    if (real && t < p.T) {
+                        ps = p.pos ? p.pos[(int64_t)b * p.T + t] : t;
+                        if (ps < 0 || ps >= p.max_pos) {
+                            flag(p.check, LOWRAM_CHECK_POS_RANGE);
+                            ps = ps < 0 ? 0 : p.max_pos - 1;
+                        }
+                    }
+                    const float* cb = p.rcos + (int64_t)(fh * 32 + 2 * g4) * mp + ps;
+                    const float* sb = p.rsin + (int64_t)(fh * 32 + 2 * g4) * mp + ps;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        c2[k][c] = f2_pack(__ldg(cb + (8 * c) * mp), __ldg(cb + (8 * c + 1) * mp));
+                        s2[k][c] = f2_pack(__ldg(sb + (8 * c) * mp), __ldg(sb + (8 * c + 1) * mp));
                     }
                 }
-                float acc[HPU][G];
+            }
+            const uint32_t buf = j & 1;
+            const bool ok = mbar_wait_cluster(&t_full[buf], (j >> 1) & 1, abort_flag);
+            if (!ok) fail();
+            float fin[HPU][G];     // this thread's sums for the token it finishes
 #pragma unroll
-                for (int hx = 0; hx < HPU; ++hx)
+            for (int hx = 0; hx < HPU; ++hx)
 #pragma unroll
-                    for (int jq = 0; jq < G; ++jq) {
-                        const float2 v = f2_unpack(acc2[hx][jq]);
-                        acc[hx][jq] = v.x + v.y;
-                    }
-                if (fh == 1)
+                for (int jq = 0; jq < G; ++jq) fin[hx][jq] = 0.0f;
+            if (ok) {
+                fence_after();
+                const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
-                    for (int hx = 0; hx < HPU; ++hx)
+                for (int hx = 0; hx < HPU; ++hx) {
 #pragma unroll
-                        for (int jq = 0; jq < G; ++jq) xs[hx * G + jq] = acc[hx][jq];
-                named_bar_sync(1, 256);      // (exchange buffers alternate by unit, so one barrier per unit)
-                if (fh == 0 && ok && t < p.T) {
+                    for (int pass = 0; pass < 2 / LHP; ++pass) {
+                        uint64_t acc2[R][G];   // (even, odd) frequency partial sums per token and q-head
 #pragma unroll
-                    for (int hx = 0; hx < HPU; ++hx) {
-                        const int h = u * HPU + hx;
-                        float best = -INFINITY;
+                        for (int k = 0; k < R; ++k)
+#pragma unroll
+                            for (int jq = 0; jq < G; ++jq) acc2[k][jq] = 0ull;
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {     // frequency blocks c = 2cc, 2cc+1
+                            const uint32_t col = buf * UN + hx * 128 + fh * 32 + cc * 16;
+                            float xv[LHP][8], yv[LHP][8];
+                            if (LHP == 2)
+                                tmem_ld_16x256b_4x2(lane_base + col, lane_base + (16u << 16) + col,
+                                                    lane_base + col + 64, lane_base + (16u << 16) + col + 64,
+                                                    xv[0], xv[LHP - 1], yv[0], yv[LHP - 1]);
+                            else
+                                tmem_ld_16x256b_2x2(lane_base + ((uint32_t)(16 * pass) << 16) + col,
+                                                    lane_base + ((uint32_t)(16 * pass) << 16) + col + 64, xv[0],
+                                                    yv[0]);
+#pragma unroll
+                            for (int cb = 0; cb < 2; ++cb) {
+                                const int c = 2 * cc + cb;
+                                uint64_t kx2[R], ky2[R];
+#pragma unroll
+                                for (int k = 0; k < R; ++k) {
+                                    const int lhk = (LHP == 2) ? (k >> 1) : 0, ik = (LHP == 2) ? (k & 1) : k;
+                                    const int kk = (LHP == 2) ? k : 2 * pass + k;   // index into c2/s2
+                                    const uint64_t x2 = f2_pack(xv[lhk][cb * 4 + 2 * ik], xv[lhk][cb * 4 + 2 * ik + 1]);
+                                    const uint64_t y2 = f2_pack(yv[lhk][cb * 4 + 2 * ik], yv[lhk][cb * 4 + 2 * ik + 1]);
+                                    kx2[k] = f2_sub(f2_mul(x2, c2[kk][c]), f2_mul(y2, s2[kk][c]));   // x cos - y sin
+                                    ky2[k] = f2_fma(y2, c2[kk][c], f2_mul(x2, s2[kk][c]));            // y cos + x sin
+                                }
+#pragma unroll
+                                for (int jq = 0; jq < G; ++jq) {
+                                    const ulonglong2 qq = *reinterpret_cast<const ulonglong2*>(
+                                        Qs + ((((u * HPU + hx) * G + jq) * 32) + fh * 16 + 4 * c + g4) * 4);
+#pragma unroll
+                                    for (int k = 0; k < R; ++k) {
+                                        acc2[k][jq] = f2_fma(qq.x, kx2[k], acc2[k][jq]);
+                                        acc2[k][jq] = f2_fma(qq.y, ky2[k], acc2[k][jq]);
+                                    }
+                                }
+                            }
+                        }
+                        // sum over the four lanes sharing a token (g4): reduce-scatter by lane bits
 #pragma unroll
                         for (int jq = 0; jq < G; ++jq) {
-                            const float sc = acc[hx][jq] + xs[hx * G + jq];
-                            best = fmaxf(best, sc);
-                            if (p.sall) p.sall[((int64_t)b * p.H_q + h * G + jq) * p.T + t] = sc;
+                            float v[R];
+#pragma unroll
+                            for (int k = 0; k < R; ++k) {
+                                const float2 h2 = f2_unpack(acc2[k][jq]);
+                                v[k] = h2.x + h2.y;
+                            }
+                            if (LHP == 2) {
+                                // keep lane half lh = b0, then token i = b1
+                                float k0 = b0 ? v[R - 2] : v[0], k1 = b0 ? v[R - 1] : v[1];
+                                const float s0 = b0 ? v[0] : v[R - 2], s1 = b0 ? v[1] : v[R - 1];
+                                k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+                                k1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+                                const float kk = b1 ? k1 : k0, ss = b1 ? k0 : k1;
+                                fin[hx][jq] = kk + __shfl_xor_sync(0xffffffffu, ss, 2);
+                            } else {
+                                // keep token i = b0, then sum the b1 pair (both lanes hold the total)
+                                float k0 = b0 ? v[R - 1] : v[0];
+                                const float s0 = b0 ? v[0] : v[R - 1];
+                                k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+                                k0 += __shfl_xor_sync(0xffffffffu, k0, 2);
+                                if (pass == fh) {
+                                    fin[hx][jq] = k0;
+                                } else if (b1 == 0) {   // the other half finishes this token
+                                    const int orow = quarter * 32 + 16 * pass + 8 * b0 + r8;
+                                    Xs[(buf * 128 + orow) * 16 + hx * G + jq] = k0;
+                                }
+                            }
                         }
-                        p.key[((int64_t)b * p.H_kv + h) * p.T + t] = best;
                     }
+                }
+                fence_before();
+                if (rank == 0) {
+                    mbar_arrive(&t_empty[buf]);
+                } else {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(peer_smem(&t_empty[buf], 0));
+                }
+            }
+            float* xs = Xs + (buf * 128 + frow) * 16;
+            if (LHP == 2 && fh == 1)
+#pragma unroll
+                for (int hx = 0; hx < HPU; ++hx)
+#pragma unroll
+                    for (int jq = 0; jq < G; ++jq) xs[hx * G + jq] = fin[hx][jq];
+            named_bar_sync(1, 256);      // (exchange buffers alternate by unit, so one barrier per unit)
+            const int t = t0 + frow;
+            if (finisher && ok && real && t < p.T) {
+#pragma unroll
+                for (int hx = 0; hx < HPU; ++hx) {
+                    const int h = u * HPU + hx;
+                    float best = -INFINITY;
+#pragma unroll
+                    for (int jq = 0; jq < G; ++jq) {
+                        const float sc = fin[hx][jq] + xs[hx * G + jq];
+                        best = fmaxf(best, sc);
+                        if (p.sall) p.sall[((int64_t)b * p.H_q + h * G + jq) * p.T + t] = sc;
+                    }
+                    p.key[((int64_t)b * p.H_kv + h) * p.T + t] = best;
                 }
             }
         }
@@ -427,7 +475,7 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     if (!make_map(&mA, a.coef, 3, dA, bA) || !make_map(&mB, a.basis, 2, dB, bB)) return cudaErrorInvalidValue;
     const size_t smem = score_smem_bytes(p.NS, cfg.UN, s.H_q);
     // CTA pairs (cluster of two), at most one CTA per SM
-    const int grid = 2 * std::min((p.n_tiles + 1) / 2, std::max(1, sm_count() / 2));
+    const int grid = 2 * std::min((p.n_tiles + 1) / 2 * p.NU, std::max(1, sm_count() / 2));
     cudaError_t e = cudaSuccess;
     auto go = [&](auto kern) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
