@@ -246,12 +246,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                 if (b != cur_b) {
                     named_bar_sync(1, 256);      // every epilogue thread is done with the previous query
                     if (!*abort_flag) {
-                        // Qs[q-head][frequency pair fp][4] = scale * (q[2fp], q[2fp+1], q[64+2fp], q[64+2fp+1])
-                        const __nv_bfloat16* qb = p.q + (int64_t)b * p.H_q * 128;
-                        for (int e = et; e < p.H_q * 128; e += 256) {
-                            const int qh = e >> 7, fp = (e >> 2) & 31, k = e & 3;
-                            const int dim = (k < 2) ? 2 * fp + k : 64 + 2 * fp + (k - 2);
-                            Qs[e] = __bfloat162float(qb[qh * 128 + dim]) * p.scale;
+                        // Qs[q-head][frequency pair fp][4] = scale * (q[2fp], q[2fp+1], q[64+2fp], q[64+2fp+1]);
+                        // one item = a q-head's dims 8a..8a+7 and 64+8a..64+8a+7 (two 16-byte loads); H_q*8 items,
+                        // one per thread for up to 32 q-heads
+                        const uint4* qb = reinterpret_cast<const uint4*>(p.q + (int64_t)b * p.H_q * 128);
+                        for (int e = et; e < p.H_q * 8; e += 256) {
+                            const uint4 vx = qb[(e >> 3) * 16 + (e & 7)];
+                            const uint4 vy = qb[(e >> 3) * 16 + 8 + (e & 7)];
+                            const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&vx);
+                            const __nv_bfloat162* y2 = reinterpret_cast<const __nv_bfloat162*>(&vy);
+                            float4* dst = reinterpret_cast<float4*>(Qs) + (e >> 3) * 32 + (e & 7) * 4;
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const float2 xf = __bfloat1622float2(x2[m]), yf = __bfloat1622float2(y2[m]);
+                                dst[m] = make_float4(xf.x * p.scale, xf.y * p.scale, yf.x * p.scale, yf.y * p.scale);
+                            }
                         }
                     }
                     named_bar_sync(1, 256);
@@ -438,7 +447,7 @@ bool g_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 7 || g == 8; }
 bool tc_score_supported(const lowram_decode_shape& s) {
     const int g = s.H_q / s.H_kv;
     return s.act_dtype == LOWRAM_BF16 && s.coef_dtype == LOWRAM_BF16 && s.d == 128 && s.r % kChunkK == 0 &&
-           s.r <= 1024 && g_ok(g) && s.T > 0 && score_config(s.H_q, s.H_kv).NS >= 2 &&
+           s.r <= 1024 && g_ok(g) && s.T > 0 && s.H_q <= 128 && score_config(s.H_q, s.H_kv).NS >= 2 &&
            encode_fn() != nullptr;
 }
 
