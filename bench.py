@@ -386,20 +386,23 @@ def main():
     step_ms = call_ms.sum(axis=1)
     value, ms_per_step = job_throughput(float(step_ms.mean()), world, dist, dev)
 
-    # per-kernel breakdown (one more step with events between the kernels, which serialise them)
-    stage = np.zeros((w.L, 4))
-    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(w.L)]
+    # per-kernel breakdown (three more steps with events between the kernels, which serialise them; median
+    # over the calls)
+    n_bd = 3
+    stage = np.zeros((n_bd * w.L, 4))
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_bd * w.L)]
     for e5 in bev:
         for e in e5:
             e.record()
-    for l in range(w.L):
-        flush.zero_()
-        call(l, events=bev[l])
     torch.cuda.synchronize()
-    for l in range(w.L):
+    for i in range(n_bd * w.L):
+        flush.zero_()
+        call(i % w.L, events=bev[i])
+    torch.cuda.synchronize()
+    for i in range(n_bd * w.L):
         for k in range(4):
-            stage[l, k] = bev[l][k].elapsed_time(bev[l][k + 1])
-    per_kernel_ms = stage.mean(axis=0)          # K1 keys, K2 select, K3 values (+ merge), K4 merge
+            stage[i, k] = bev[i][k].elapsed_time(bev[i][k + 1])
+    per_kernel_ms = np.median(stage, axis=0)    # K1 keys, K2 select, K3 values (+ merge), K4 merge
     names = ["score", "select", "vregen", "merge"]
     dom = int(np.argmax(per_kernel_ms))
 

@@ -130,14 +130,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            uint32_t ib = 0;
+            uint32_t ib = 0;           // ring stages issued
+            uint32_t s = 0, ph = 0;    // ring position of stage ib, kept incrementally (see the MMA issuer)
             for (int it = it_begin; it < it_end && !*abort_flag; ++it) {
                 const int pr = it / p.NU, u = it - pr * p.NU;
                 const int lt = min(2 * pr + (int)rank, p.n_tiles - 1);
                 const int b = lt / p.tiles_per_seq, t0 = (lt % p.tiles_per_seq) * kTokTile;
                 {
                     for (int kc = 0; kc < p.KC; ++kc, ++ib) {
-                        const uint32_t s = ib % p.NS, ph = (ib / p.NS) & 1;
                         if (!mbar_wait_cluster(&b_empty[s], ph ^ 1, abort_flag)) {
                             fail();
                             goto produced;
@@ -153,6 +153,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                             const uint32_t bar = peer_smem(&b_full[s], 0);
                             tma_load_3d_pair(dA, &tmA, bar, kc * kChunkK, t0, b);
                             tma_load_2d_pair(dB, &tmB, bar, kc * kChunkK, brow);
+                        }
+                        if (++s == (uint32_t)p.NS) {
+                            s = 0;
+                            ph ^= 1;
                         }
                     }
                 }
@@ -172,8 +176,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
     } else if (warp == 1) {
         if (rank == 0 && lane == 0) {
             // -------------------------------------------------------------- MMA issuer (even CTA)
+            // One thread feeds the tensor pipe (a 256x256x16 pair MMA every 128 SM cycles at full rate), so the
+            // loop keeps the ring position incrementally and rebuilds no descriptor: a stage adds its byte offset
+            // >> 4 to the descriptor of stage 0, a 16-wide k-step 32 bytes (2 units).
             const uint32_t idesc = idesc_bf16(2 * kTokTile, UN);
-            uint32_t ib = 0, j = 0;
+            const uint64_t st_desc = sdesc_sw128(smem_u32(St));
+            uint32_t s = 0, ph = 0, j = 0;
             for (int it = it_begin; it < it_end && !*abort_flag; ++it, ++j) {
                 {
                     const uint32_t buf = j & 1;
@@ -183,20 +191,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                     }
                     fence_after();
                     const uint32_t d_tmem = tmem + buf * UN;
-                    for (int kc = 0; kc < p.KC; ++kc, ++ib) {
-                        const uint32_t s = ib % p.NS, ph = (ib / p.NS) & 1;
+                    for (int kc = 0; kc < p.KC; ++kc) {
                         if (!mbar_wait(&b_full[s], ph, abort_flag)) {
                             fail();
                             goto issued;
                         }
                         fence_after();
-                        const uint32_t a_addr = smem_u32(St + s * kStage);
-                        const uint32_t b_addr = a_addr + kAChunkBytes;
+                        const uint64_t ad = st_desc + s * (uint32_t)(kStage >> 4), bd = ad + (kAChunkBytes >> 4);
 #pragma unroll
                         for (int k = 0; k < kChunkK / 16; ++k)
-                            mma_bf16_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), idesc,
-                                          (kc | k) != 0);
+                            mma_bf16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
                         mma_commit_pair(&b_empty[s], 0x3);
+                        if (++s == (uint32_t)p.NS) {
+                            s = 0;
+                            ph ^= 1;
+                        }
                     }
                     mma_commit_pair(&t_full[buf], 0x3);
                 }

@@ -65,6 +65,16 @@ def test_decode_small_matches_oracle(name, biases):
     C.check_decode(gpu, orc, w.S_eff)
 
 
+@pytest.mark.parametrize("H_q,H_kv,r", [(8, 8, 512), (6, 3, 256), (16, 2, 512), (4, 1, 384), (7, 1, 128),
+                                         (32, 8, 1024), (14, 2, 640)])
+def test_decode_head_ratios_and_ranks(H_q, H_kv, r):
+    """Every q-heads-per-kv-head ratio of the key pass, one and two kv-heads per unit (odd H_kv takes one),
+    the resident-latent and streamed feeding modes (r = 640 and 1024 stream)."""
+    w = SMALL["llama8b_small"].with_(B=2, T=700, S=200, H_q=H_q, H_kv=H_kv, r=r)
+    c = C.decode_case(w)
+    C.check_decode(C.run_gpu_decode(c), C.run_oracle_decode(c), w.S_eff)
+
+
 @pytest.mark.parametrize("S", [0, 1, 7, 129, 999, 1000, 5000])
 def test_decode_selection_sizes(S):
     w = SMALL["llama8b_small"].with_(S=S)
