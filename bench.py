@@ -121,10 +121,12 @@ def job_throughput(ms_per_step_local: float, world: int, dist=None, device=None)
 
 def launches_per_call(w, tc_path):
     """Kernels one decode call launches: keys, selection, values (+ a separate merge unless the tensor-core
-    value pass merges as it finishes, which it does for predictor widths of 128 or 256)."""
+    value pass merges as it finishes, which it does for predictor widths of 128 or 256), plus the two
+    kernels that split an int4 cache exactly into bf16 [hi | lo] and repeat the basis for the tensor cores."""
+    split = 2 if (tc_path and w.coef_fmt == "int4") else 0
     if w.S_eff == 0:
-        return 2
-    return 3 if (tc_path and w.m in (128, 256)) else 4
+        return 2 + split
+    return (3 if (tc_path and w.m in (128, 256)) else 4) + split
 
 
 def kernel_digest(paths):

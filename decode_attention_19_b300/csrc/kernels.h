@@ -76,6 +76,10 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st);
 // K4 for the tensor-core path: merge, then the predictor's second layer on the merged sums
 cudaError_t launch_merge_w2(const DecodeArgs& a, int n_chunks, cudaStream_t st);
+// int4 caches on the tensor-core path: the exact split of the dequantised coefficients into bf16 [hi | lo]
+// ([rows, 2r]), and the basis with its columns repeated ([rows, 2r]); see dequant.cu
+cudaError_t launch_int4_split(const void* codes, const void* scales, int64_t rows, int r, void* out, cudaStream_t st);
+cudaError_t launch_dup_cols(const void* W, int64_t rows, int r, void* out, cudaStream_t st);
 
 // Write side
 struct CompressArgs {

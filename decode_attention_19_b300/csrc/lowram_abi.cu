@@ -64,19 +64,31 @@ lowram_status check_decode_shape(const lowram_decode_shape* s) {
 
 struct DecodeLayout {
     bool tc_score, tc_vregen;
+    bool split;                 // int4 cache run on the tensor cores through the exact bf16 split (dequant.cu)
+    lowram_decode_shape sx;     // the shape the kernels see: with split, bf16 coefficients of rank 2r
     int chunk, n_chunks, S_eff, PW;
     bool fused_merge;
-    size_t off_key, off_sel, off_partial, off_sall, off_cnt, off_hit, total;
+    size_t off_key, off_sel, off_partial, off_sall, off_cnt, off_hit, off_asplit, off_bsplit, total;
 };
 
 DecodeLayout decode_layout(const lowram_decode_shape& s) {
     DecodeLayout L{};
     L.S_eff = s.S < s.T ? s.S : s.T;
-    L.tc_score = tc_score_supported(s);
-    L.tc_vregen = tc_vregen_supported(s);
+    L.sx = s;
+    if (s.coef_dtype == LOWRAM_INT4_G32 && s.act_dtype == LOWRAM_BF16) {
+        lowram_decode_shape x = s;
+        x.coef_dtype = LOWRAM_BF16;
+        x.r = 2 * s.r;
+        if (tc_score_supported(x) && tc_vregen_supported(x)) {
+            L.split = true;
+            L.sx = x;
+        }
+    }
+    L.tc_score = tc_score_supported(L.sx);
+    L.tc_vregen = tc_vregen_supported(L.sx);
     L.chunk = L.tc_vregen ? kTcChunk : kSimtChunk;
     L.n_chunks = (int)cdiv(L.S_eff, L.chunk);
-    L.PW = L.tc_vregen ? tc_partial_width(s) : s.d + 2;
+    L.PW = L.tc_vregen ? tc_partial_width(L.sx) : s.d + 2;
     size_t off = kHeader;
     L.off_key = off;
     off += align256(sizeof(float) * (size_t)s.B * s.H_kv * s.T);
@@ -86,11 +98,15 @@ DecodeLayout decode_layout(const lowram_decode_shape& s) {
     off += align256(sizeof(float) * (size_t)s.B * s.H_q * L.n_chunks * L.PW);
     L.off_sall = off;
     off += L.tc_vregen ? align256(sizeof(float) * (size_t)s.B * s.H_q * s.T) : 0;
-    L.fused_merge = L.tc_vregen && L.n_chunks > 0 && tc_fused_merge(s, L.n_chunks);
+    L.fused_merge = L.tc_vregen && L.n_chunks > 0 && tc_fused_merge(L.sx, L.n_chunks);
     L.off_cnt = off;
     off += L.fused_merge ? align256(sizeof(int32_t) * (size_t)s.B * s.H_kv) : 0;
     L.off_hit = off;
     off += L.tc_vregen ? align256(sizeof(int32_t) * (size_t)s.B * s.H_kv * L.S_eff) : 0;
+    L.off_asplit = off;
+    off += L.split ? align256(sizeof(uint16_t) * (size_t)s.B * s.T * L.sx.r) : 0;
+    L.off_bsplit = off;
+    off += L.split ? align256(sizeof(uint16_t) * (size_t)s.H_kv * s.d * L.sx.r) : 0;
     L.total = off;
     return L;
 }
@@ -181,7 +197,7 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
 
     char* ws = (char*)workspace;
     DecodeArgs a{};
-    a.s = s;
+    a.s = L.sx;
     a.g = s.H_q / s.H_kv;
     a.S_eff = L.S_eff;
     a.scale = s.sm_scale > 0.0f ? s.sm_scale : 1.0f / sqrtf((float)s.d);
@@ -197,12 +213,22 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     a.cnt = L.fused_merge ? (int32_t*)(ws + L.off_cnt) : nullptr;
     a.hit = (L.tc_vregen && s.n_res > 0) ? (int32_t*)(ws + L.off_hit) : nullptr;
     a.check = (uint32_t*)ws;
+    if (L.split) {   // the kernels read [hi | lo] and [W | W]: bf16 operands of rank 2r, exactly C W^T
+        a.coef = ws + L.off_asplit;
+        a.coef_scale = nullptr;
+        a.basis = ws + L.off_bsplit;
+    }
 
     // optional timing marks: before K1, after K1, after K2, after K3, after K4
     auto mark = [&](int i) -> cudaError_t {
         return (events && events[i]) ? cudaEventRecord((cudaEvent_t)events[i], cs) : cudaSuccess;
     };
     cudaError_t e = mark(0);
+    if (e == cudaSuccess && L.split && (int64_t)s.B * s.T > 0) {
+        e = launch_int4_split(coef, coef_scale, (int64_t)s.B * s.T, s.r, ws + L.off_asplit, cs);
+        if (e == cudaSuccess) e = launch_dup_cols(basis, (int64_t)s.H_kv * s.d, s.r, ws + L.off_bsplit, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "int4 split");
+    }
     if (e == cudaSuccess && (int64_t)s.B * s.T > 0 && (L.S_eff > 0 || key_out))
         e = L.tc_score ? launch_score_tc(a, cs) : launch_score_simt(a, cs);
     if (e != cudaSuccess) return cuda_fail(e, "score");

@@ -74,80 +74,94 @@ __device__ __forceinline__ void st_shared_16(uint8_t* p, uint32_t a, uint32_t b,
 // The last CTA of a (sequence, kv-head) to finish merges the chunks' partials of its G q-heads (threads =
 // the 128 epilogue threads, et = 0..127): W = max_c M_c, w_c = exp(M_c - W), L = sum_c w_c l_c,
 // out = w2[h] (sum_c w_c z_c / L) + b2[h] + sum_c w_c rz_c / L,  lse = W + log L.
-// The G q-heads' records are contiguous; they are copied into shared memory with batches of independent
-// 16-byte loads, all G at once when they fit, else one q-head at a time.
+// It is the tail of the kernel's last wave, so its global reads are issued together: the thread's row of w2
+// (output feature i = et) first, then the G q-heads' contiguous records in batches of 10 independent 16-byte
+// loads (all G at once when they fit, else one q-head at a time); the chunk weights w_c are computed once per
+// q-head.
 template <int G>
 __device__ __forceinline__ void merge_last(const VregenTcParams& p, int b, int h, int et, float* scratch) {
     const int64_t qstride = (int64_t)p.n_chunks * p.PW;
     const float* P0 = p.partial + ((int64_t)b * p.H_q + h * G) * qstride;
     const int ZW = p.m + 128;
     float* Z = scratch;                          // [G][m + 128] merged hidden sums, then residual sums
-    float* Pb = scratch + G * ZW;                // [G][n_chunks][PW] staged records
-    // all G q-heads' records at once when they fit beside Z, else one q-head at a time (tc_fused_merge
-    // guarantees one fits)
-    const int per = (G * (qstride + ZW) * sizeof(float) <= (size_t)kNS * kStageBytes) ? G : 1;
-    float M[G], L[G];
+    float* Wc = Z + G * ZW;                      // [G][n_chunks] chunk weights exp(M_c - W)
+    float* ML = Wc + G * p.n_chunks;             // [G][2] W and L
+    float* Pb = ML + 2 * G;                      // [G][n_chunks][PW] staged records (16-byte aligned: see below)
+    Pb = (float*)(((uintptr_t)Pb + 15) & ~(uintptr_t)15);
+    // all G q-heads' records at once when they fit, else one q-head at a time (tc_fused_merge guarantees one fits)
+    const size_t fixed = (size_t)(Pb - scratch) * sizeof(float);
+    const int per = (fixed + G * qstride * sizeof(float) <= (size_t)kNS * kStageBytes) ? G : 1;
+
+    constexpr int kW2Pre = 16;                   // 16-byte pieces of the w2 row fetched ahead (128 hidden units)
+    constexpr int kRecBatch = 10;                // independent 16-byte record loads per thread per batch
+    const uint4* W2r = reinterpret_cast<const uint4*>(p.w2 + ((int64_t)h * 128 + et) * p.m);
+    uint4 wpre[kW2Pre];
+#pragma unroll
+    for (int u = 0; u < kW2Pre; ++u)
+        if (u * 8 < p.m) wpre[u] = __ldg(W2r + u);
+
     for (int q0 = 0; q0 < G; q0 += per) {
-        {   // copy records of q-heads q0 .. q0+per-1: batches of 8 independent 16-byte loads per thread
+        {   // records of q-heads q0 .. q0+per-1
             const float4* src = reinterpret_cast<const float4*>(P0 + q0 * qstride);
             float4* d4 = reinterpret_cast<float4*>(Pb);
             const int n4 = (int)(per * qstride / 4);
-            for (int i0 = 0; i0 < n4; i0 += 8 * kRows) {
-                float4 v[8];
+            for (int i0 = 0; i0 < n4; i0 += kRecBatch * kRows) {
+                float4 v[kRecBatch];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < kRecBatch; ++u) {
                     const int i = i0 + u * kRows + et;
                     if (i < n4) v[u] = __ldcg(src + i);
                 }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < kRecBatch; ++u) {
                     const int i = i0 + u * kRows + et;
                     if (i < n4) d4[i] = v[u];
                 }
             }
             tc::named_bar_sync(1, kRows);
         }
-#pragma unroll
-        for (int jq = 0; jq < G; ++jq) {
-            if (jq < q0 || jq >= q0 + per) continue;
-            const float* Pq = Pb + (jq - q0) * qstride;
+        // one thread per q-head: W, L and the chunk weights
+        if (et < per) {
+            const int jq = q0 + et;
+            const float* Pq = Pb + et * qstride;
             float mx = -INFINITY;
             for (int c = 0; c < p.n_chunks; ++c) mx = fmaxf(mx, Pq[(int64_t)c * p.PW + p.m + 128]);
             float l = 0.0f;
             for (int c = 0; c < p.n_chunks; ++c) {
                 const float mc = Pq[(int64_t)c * p.PW + p.m + 128];
-                l = fmaf(mc == -INFINITY ? 0.0f : __expf(mc - mx), Pq[(int64_t)c * p.PW + p.m + 129], l);
+                const float w = mc == -INFINITY ? 0.0f : __expf(mc - mx);
+                Wc[jq * p.n_chunks + c] = w;
+                l = fmaf(w, Pq[(int64_t)c * p.PW + p.m + 129], l);
             }
-            M[jq] = mx;
-            L[jq] = l;
-            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            for (int j = et; j < ZW; j += kRows) {
-                float acc = 0.0f;
-                for (int c = 0; c < p.n_chunks; ++c) {
-                    const float mc = Pq[(int64_t)c * p.PW + p.m + 128];
-                    if (mc != -INFINITY) acc = fmaf(__expf(mc - mx), Pq[(int64_t)c * p.PW + j], acc);
-                }
-                Z[jq * ZW + j] = acc * inv;
-            }
+            ML[jq * 2] = mx;
+            ML[jq * 2 + 1] = l;
         }
-        tc::named_bar_sync(1, kRows);     // Pb is reused by the next group of q-heads
+        tc::named_bar_sync(1, kRows);
+        for (int e = et; e < per * ZW; e += kRows) {
+            const int jl = e / ZW, j = e - jl * ZW, jq = q0 + jl;
+            const float* Pq = Pb + jl * qstride;
+            const float l = ML[jq * 2 + 1];
+            float acc = 0.0f;
+            for (int c = 0; c < p.n_chunks; ++c) acc = fmaf(Wc[jq * p.n_chunks + c], Pq[(int64_t)c * p.PW + j], acc);
+            Z[jq * ZW + j] = l > 0.0f ? acc / l : 0.0f;
+        }
+        tc::named_bar_sync(1, kRows);     // Pb is reused by the next group of q-heads; Z is complete
     }
     // thread et = output feature i: the second predictor layer on the merged hidden sums
-    const __nv_bfloat16* W2 = p.w2 + ((int64_t)h * 128 + et) * p.m;
     float acc[G];
 #pragma unroll
     for (int jq = 0; jq < G; ++jq) acc[jq] = 0.0f;
-    for (int j0 = 0; j0 < p.m; j0 += 64) {
-        uint4 wv[8];
+    for (int j0 = 0; j0 < p.m; j0 += 8 * kW2Pre) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) wv[u] = __ldg(reinterpret_cast<const uint4*>(W2 + j0 + u * 8));
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&wv[u]);
+        for (int u = 0; u < kW2Pre; ++u) {
+            const int jb = j0 + u * 8;
+            if (jb >= p.m) break;
+            const uint4 wv = j0 == 0 ? wpre[u] : __ldg(W2r + jb / 8);
+            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&wv);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 f = __bfloat1622float2(pr[e]);
-                const int j = j0 + u * 8 + 2 * e;
+                const int j = jb + 2 * e;
 #pragma unroll
                 for (int jq = 0; jq < G; ++jq) {
                     acc[jq] = fmaf(f.x, Z[jq * ZW + j], acc[jq]);
@@ -160,8 +174,9 @@ __device__ __forceinline__ void merge_last(const VregenTcParams& p, int b, int h
 #pragma unroll
     for (int jq = 0; jq < G; ++jq) {
         const int64_t bhq = (int64_t)b * p.H_q + h * G + jq;
-        p.out[bhq * 128 + et] = L[jq] > 0.0f ? acc[jq] + bias + Z[jq * ZW + p.m + et] : 0.0f;
-        if (p.lse && et == jq) p.lse[bhq] = L[jq] > 0.0f ? M[jq] + logf(L[jq]) : -INFINITY;
+        const float Mq = ML[jq * 2], Lq = ML[jq * 2 + 1];
+        p.out[bhq * 128 + et] = Lq > 0.0f ? acc[jq] + bias + Z[jq * ZW + p.m + et] : 0.0f;
+        if (p.lse && et == jq) p.lse[bhq] = Lq > 0.0f ? Mq + logf(Lq) : -INFINITY;
     }
 }
 
@@ -581,8 +596,11 @@ int tc_partial_width(const lowram_decode_shape& s) { return s.m + s.d + 4; }
 // The last CTA of each (sequence, kv-head) merges in the value kernel when the merge's shared scratch
 // (chunk weights and merged sums of the G q-heads) fits in the ring.
 bool tc_fused_merge(const lowram_decode_shape& s, int n_chunks) {
+    // merge_last's shared memory: Z [G][m+128], chunk weights [G][n_chunks], W and L [G][2], 16 bytes of
+    // alignment, and one q-head's records [n_chunks][PW]
     const size_t g = s.H_q / s.H_kv, zw = s.m + 128, pw = tc_partial_width(s);
-    return (g * zw + (size_t)n_chunks * pw) * sizeof(float) <= (size_t)kNS * kStageBytes;
+    return (g * zw + g * (size_t)n_chunks + 2 * g + 4 + (size_t)n_chunks * pw) * sizeof(float) <=
+           (size_t)kNS * kStageBytes;
 }
 
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {

@@ -96,8 +96,9 @@ typedef struct {
 LOWRAM_API lowram_status lowram_decode_workspace_size(const lowram_decode_shape* shape, size_t* bytes);
 
 /* *yes = 1 if calls of this shape run the key pass and the value regeneration on the tensor cores
- * (tcgen05; bf16 or int4 caches), 0 if they run on the CUDA cores (float32 caches and shapes the
- * tensor-core kernels do not cover). */
+ * (tcgen05; bf16 caches, and int4 caches with bf16 activations and r <= 512: these are first split exactly
+ * into two bf16 terms, coefficient = hi + lo, stored in the workspace as a rank-2r bf16 cache), 0 if they run
+ * on the CUDA cores (float32 caches and shapes the tensor-core kernels do not cover). */
 LOWRAM_API lowram_status lowram_decode_uses_tensor_cores(const lowram_decode_shape* shape, int32_t* yes);
 
 /*

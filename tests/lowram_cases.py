@@ -70,8 +70,9 @@ def run_gpu_decode(c: dict, *, S=None, hooks=True, workspace=None):
     sel = torch.empty((B, w.H_kv, S_eff), dtype=torch.int32, device=dev) if hooks else None
     n_res = c["res_idx"].shape[-1]
     own_ws = workspace is None
-    if own_ws:
-        workspace = torch.zeros(1 << 26, dtype=torch.uint8, device=dev)
+    if own_ws:   # 64 MiB, plus room for an int4 cache's exact bf16 split (rank 2r) and the repeated basis
+        extra = 4 * w.r * (B * T + w.H_kv * w.d) + 4096 if w.coef_fmt == "int4" else 0
+        workspace = torch.zeros((1 << 26) + extra, dtype=torch.uint8, device=dev)
     out, lse = L.lowram_decode_attn(cu(c["q"]), cu(c["coef"]), cu(c["basis"]), cu(c["w1"]), cu(c["w2"]),
                                     rope_cos=cos, rope_sin=sin, S=S, coef_scale=cu(c["coef_scale"]), pos=cu(c["pos"]),
                                     b1=cu(c["b1"]), b2=cu(c["b2"]),

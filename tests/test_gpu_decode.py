@@ -33,7 +33,7 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
-def test_bf16_workloads_take_the_tensor_core_key_pass():
+def test_bf16_and_int4_workloads_take_the_tensor_core_key_pass():
     import decode_attention_19_b300 as L
     for name in ["llama8b", "long", "peak"]:
         w = W[name]
@@ -42,6 +42,12 @@ def test_bf16_workloads_take_the_tensor_core_key_pass():
     tiny = W["tiny"]
     sh = L.lowram_decode_shape(1, 256, 4, 2, 64, 32, 64, 256, 64, 0, 0, 0, 256, 0.0)
     assert not L.lowram_decode_uses_tensor_cores(sh)
+    # int4 coefficients with bf16 activations: exact two-term bf16 split of rank 2r, then the same kernels
+    w = W["evict_quant"]
+    sh = L.lowram_decode_shape(w.B, w.T, w.H_q, w.H_kv, w.d, w.r, w.m, w.S, w.n_res, 1, 2, 3, w.T_nominal, 0.0)
+    assert L.lowram_decode_uses_tensor_cores(sh)
+    sh = L.lowram_decode_shape(w.B, w.T, w.H_q, w.H_kv, w.d, 1024, w.m, w.S, w.n_res, 1, 2, 3, w.T_nominal, 0.0)
+    assert not L.lowram_decode_uses_tensor_cores(sh)   # rank 2r = 2048 is past the key pass's limit
 
 
 def test_rope_table_matches_fp64_angles():
