@@ -21,12 +21,14 @@
 //   warp 1      TMEM owner (both CTAs allocate the pair's 2*UN columns together) and, in the even CTA, the
 //               MMA issuer; each stage's commit releases the stage in both CTAs.
 //   warps 2-9   epilogue, all eight warps on every unit: warp w reads TMEM lane quarter w%4 and one half of
-//               the 64 rotary frequencies.  One thread holds one token, fetches its cos/sin for those 32
-//               frequencies once per tile into registers, and per unit rotates the unit's heads and accumulates
-//               the dot products with the queries, which sit pre-scaled in float32 in shared memory; the arithmetic runs on
-//               packed fp32 pairs (two adjacent frequencies per instruction).  The upper half passes its
-//               partial sums to the lower half through shared memory.  Both CTAs' epilogues release a TMEM
-//               buffer (double-buffered by unit) before the even CTA's MMAs reuse it.
+//               the 64 rotary frequencies in the 16x256b shape, so a thread holds four tokens and eight
+//               frequencies.  It fetches their cos/sin once per tile into registers and per unit rotates the
+//               unit's heads and accumulates the dot products with the queries (bf16 pairs in shared memory,
+//               each loaded value serving the thread's four tokens; the softmax scale multiplies the finished
+//               dot products) in packed fp32 pairs.  Shuffles sum over the four lanes that share a token; the
+//               upper frequency half passes its partial sums to the lower half through shared memory.  Both
+//               CTAs' epilogues release a TMEM buffer (double-buffered by unit) before the even CTA's MMAs
+//               reuse it.
 // Every wait is bounded (see tc_common.cuh); a failed wait stops both CTAs of the pair, which flag
 // LOWRAM_CHECK_TIMEOUT, let what they issued complete and return.  The epilogue's named barriers are reached
 // on every path, and the pair meets at a cluster barrier before either frees TMEM or exits.
@@ -59,10 +61,10 @@ struct ScoreTcParams {
 
 // Stage s of the ring: one 64-wide k-chunk of the latent tile [128 x 64] and of the unit's basis rows
 // [UN x 64], both 128B-swizzled as TMA writes them.
-// Beside the ring: the queries of the current sequence (fp32, pre-scaled, grouped by frequency pair) and,
+// Beside the ring: the queries of the current sequence (bf16 as given, grouped by frequency pair) and,
 // double-buffered by unit, the exchange of partial dot products between the frequency halves [2][128][16] fp32.
 size_t score_smem_bytes(int NS, int UN, int H_q) {
-    return 1024 + (size_t)NS * (kAChunkBytes + (UN / 2) * 128) + (size_t)H_q * 128 * 4 + 2 * 128 * 16 * 4 +
+    return 1024 + (size_t)NS * (kAChunkBytes + (UN / 2) * 128) + (size_t)H_q * 128 * 2 + 2 * 128 * 16 * 4 +
            8 * (2 * NS + 5) + 16;
 }
 
@@ -76,8 +78,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* St = smem;
-    float* Qs = (float*)(St + p.NS * kStage);     // [H_q][32][4] query of the current sequence x scale
-    float* Xs = Qs + p.H_q * 128;                  // [2][128 rows][16] partial dots of the upper frequencies
+    uint2* Qs = (uint2*)(St + p.NS * kStage);     // [H_q][32] query of the current sequence, bf16, by frequency pair
+    float* Xs = (float*)(Qs + p.H_q * 32);         // [2][128 rows][16] partial dots of the upper frequencies
     uint64_t* b_full = (uint64_t*)(Xs + 2 * 128 * 16);   // (even CTA) both CTAs' copies of the stage landed
     uint64_t* b_empty = b_full + p.NS;                   // the pair's MMAs are done with the stage
     uint64_t* t_full = b_empty + p.NS;
@@ -255,21 +257,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                 if (b != cur_b) {
                     named_bar_sync(1, 256);      // every epilogue thread is done with the previous query
                     if (!*abort_flag) {
-                        // Qs[q-head][frequency pair fp][4] = scale * (q[2fp], q[2fp+1], q[64+2fp], q[64+2fp+1]);
+                        // Qs[q-head][frequency pair fp] = (q[2fp], q[2fp+1]), (q[64+2fp], q[64+2fp+1]) as bf16 pairs
+                        // (the softmax scale is applied to the finished dot products);
                         // one item = a q-head's dims 8a..8a+7 and 64+8a..64+8a+7 (two 16-byte loads); H_q*8 items,
                         // one per thread for up to 32 q-heads
                         const uint4* qb = reinterpret_cast<const uint4*>(p.q + (int64_t)b * p.H_q * 128);
                         for (int e = et; e < p.H_q * 8; e += 256) {
                             const uint4 vx = qb[(e >> 3) * 16 + (e & 7)];
                             const uint4 vy = qb[(e >> 3) * 16 + 8 + (e & 7)];
-                            const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&vx);
-                            const __nv_bfloat162* y2 = reinterpret_cast<const __nv_bfloat162*>(&vy);
-                            float4* dst = reinterpret_cast<float4*>(Qs) + (e >> 3) * 32 + (e & 7) * 4;
-#pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                const float2 xf = __bfloat1622float2(x2[m]), yf = __bfloat1622float2(y2[m]);
-                                dst[m] = make_float4(xf.x * p.scale, xf.y * p.scale, yf.x * p.scale, yf.y * p.scale);
-                            }
+                            uint2* dst = Qs + (e >> 3) * 32 + (e & 7) * 4;
+                            dst[0] = make_uint2(vx.x, vy.x);
+                            dst[1] = make_uint2(vx.y, vy.y);
+                            dst[2] = make_uint2(vx.z, vy.z);
+                            dst[3] = make_uint2(vx.w, vy.w);
                         }
                     }
                     named_bar_sync(1, 256);
@@ -342,12 +342,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                                 }
 #pragma unroll
                                 for (int jq = 0; jq < G; ++jq) {
-                                    const ulonglong2 qq = *reinterpret_cast<const ulonglong2*>(
-                                        Qs + ((((u * HPU + hx) * G + jq) * 32) + fh * 16 + 4 * c + g4) * 4);
+                                    const uint2 qw = Qs[((u * HPU + hx) * G + jq) * 32 + fh * 16 + 4 * c + g4];
+                                    // bf16 pair -> fp32 pair: the low half shifted up, the high half masked
+                                    const uint64_t qx2 = f2_pack(__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xffff0000u));
+                                    const uint64_t qy2 = f2_pack(__uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xffff0000u));
 #pragma unroll
                                     for (int k = 0; k < R; ++k) {
-                                        acc2[k][jq] = f2_fma(qq.x, kx2[k], acc2[k][jq]);
-                                        acc2[k][jq] = f2_fma(qq.y, ky2[k], acc2[k][jq]);
+                                        acc2[k][jq] = f2_fma(qx2, kx2[k], acc2[k][jq]);
+                                        acc2[k][jq] = f2_fma(qy2, ky2[k], acc2[k][jq]);
                                     }
                                 }
                             }
@@ -408,7 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                     float best = -INFINITY;
 #pragma unroll
                     for (int jq = 0; jq < G; ++jq) {
-                        const float sc = fin[hx][jq] + xs[hx * G + jq];
+                        const float sc = (fin[hx][jq] + xs[hx * G + jq]) * p.scale;
                         best = fmaxf(best, sc);
                         if (p.sall) p.sall[((int64_t)b * p.H_q + h * G + jq) * p.T + t] = sc;
                     }
