@@ -27,6 +27,7 @@ import statistics
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 import numpy as np
@@ -119,6 +120,13 @@ def job_throughput(ms_per_step_local: float, world: int, dist=None, device=None)
     return world * 1000.0 / ms, ms
 
 
+def gpu_backlog(ms=10.0):
+    """Queue a GPU-side wait (outside every timed event pair) so the host runs ahead of the GPU: a host
+    hiccup while it enqueues a step then cannot leave the GPU idle between an event and the kernel after it."""
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
+
+
 def launches_per_call(w, tc_path):
     """Kernels one decode call launches: keys, selection, values (+ a separate merge unless the tensor-core
     value pass merges as it finishes, which it does for predictor widths of 128 or 256), plus the two
@@ -158,16 +166,58 @@ def profiled_traffic(name, src_files):
 # clocks during the timed region
 # ------------------------------------------------------------------------------------------------
 class Clocks:
+    """SM clock and throttle reasons sampled every 2 ms on a host thread (NVML reads only) while the timed
+    region runs; nvidia-smi at its 200 ms minimum period if NVML cannot be used."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
 
     def __init__(self, dev):
         self.proc = None
         self.f = None
+        self.thread = None
+        self.samples = []
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        self.nvml_error = None
         try:
-            uuid = str(torch.cuda.get_device_properties(dev).uuid)
-            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+            import pynvml
+            pynvml.nvmlInit()
+            h = None
+            for key in (ident, ident.encode()):
+                try:
+                    h = pynvml.nvmlDeviceGetHandleByUUID(key)
+                    break
+                except Exception as e:   # noqa: BLE001 -- try the next form of the identifier
+                    self.nvml_error = repr(e)
+            if h is None:
+                pr = torch.cuda.get_device_properties(dev)
+                bus = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+                h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+            reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+            self.stop_event = threading.Event()
+
+            def run():
+                while not self.stop_event.is_set():
+                    try:
+                        mhz = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+                        why = reasons_fn(h)
+                        self.samples.append((float(mhz), int(why)))
+                    except pynvml.NVMLError:
+                        pass
+                    time.sleep(0.002)
+
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
+            return
+        except Exception as e:   # noqa: BLE001 -- fall back to nvidia-smi below
+            self.nvml_error = repr(e)
+            self.thread = None
+        try:
             self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
@@ -176,6 +226,14 @@ class Clocks:
             self.proc = None
 
     def stop(self):
+        if self.thread is not None:
+            self.stop_event.set()
+            self.thread.join(timeout=5)
+            if not self.samples:
+                return None
+            reasons = sorted(n for n, bit in self.REASONS.items() if any(w & bit for _, w in self.samples))
+            return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(self.samples), "source": "nvml, 2 ms"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -202,7 +260,7 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, 200 ms", "nvml_error": self.nvml_error}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -374,6 +432,7 @@ def main():
     clocks = Clocks(dev)
     t_wall = time.perf_counter()
     for s in range(args.steps):
+        gpu_backlog()
         for l in range(w.L):
             flush.zero_()
             e5 = evs[s][l]
@@ -398,6 +457,8 @@ def main():
             e.record()
     torch.cuda.synchronize()
     for i in range(n_bd * w.L):
+        if i % w.L == 0:
+            gpu_backlog()
         flush.zero_()
         call(i % w.L, events=bev[i])
     torch.cuda.synchronize()
