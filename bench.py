@@ -165,6 +165,54 @@ def profiled_traffic(name, src_files):
 # ------------------------------------------------------------------------------------------------
 # clocks during the timed region
 # ------------------------------------------------------------------------------------------------
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (the Python binding when present, else ctypes):
+    current and maximum SM clock and the active clock-event reasons of one GPU."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, uuid):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.py = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            return
+        except ImportError:
+            self.py = None
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByUUID failed")
+        self.lib, self.ct = lib, ctypes
+        self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def max_sm_mhz(self):
+        if self.py is not None:
+            return float(self.py.nvmlDeviceGetMaxClockInfo(self.h, self.py.NVML_CLOCK_SM))
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.NVML_CLOCK_SM, self.ct.byref(v))
+        return float(v.value)
+
+    def sample(self):
+        try:
+            if self.py is not None:
+                return float(self.py.nvmlDeviceGetClockInfo(self.h, self.py.NVML_CLOCK_SM)), int(self.reasons(self.h))
+            mhz, why = self.ct.c_uint(), self.ct.c_ulonglong()
+            if self.lib.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, self.ct.byref(mhz)) != 0:
+                return None
+            if self.reason_fn(self.h, self.ct.byref(why)) != 0:
+                return None
+            return float(mhz.value), int(why.value)
+        except Exception:   # noqa: BLE001 -- a missed sample is skipped
+            return None
+
+
 class Clocks:
     """SM clock and throttle reasons sampled every 2 ms on a host thread (NVML reads only) while the timed
     region runs; nvidia-smi at its 200 ms minimum period if NVML cannot be used."""
@@ -183,32 +231,15 @@ class Clocks:
         ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
         self.nvml_error = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = None
-            for key in (ident, ident.encode()):
-                try:
-                    h = pynvml.nvmlDeviceGetHandleByUUID(key)
-                    break
-                except Exception as e:   # noqa: BLE001 -- try the next form of the identifier
-                    self.nvml_error = repr(e)
-            if h is None:
-                pr = torch.cuda.get_device_properties(dev)
-                bus = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
-                h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
-            reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
-            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+            nv = _Nvml(ident)
+            self.max_mhz = nv.max_sm_mhz()
             self.stop_event = threading.Event()
 
             def run():
                 while not self.stop_event.is_set():
-                    try:
-                        mhz = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
-                        why = reasons_fn(h)
-                        self.samples.append((float(mhz), int(why)))
-                    except pynvml.NVMLError:
-                        pass
+                    got = nv.sample()
+                    if got is not None:
+                        self.samples.append(got)
                     time.sleep(0.002)
 
             self.thread = threading.Thread(target=run, daemon=True)
@@ -233,7 +264,7 @@ class Clocks:
                 return None
             reasons = sorted(n for n, bit in self.REASONS.items() if any(w & bit for _, w in self.samples))
             return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
-                    "reasons": reasons, "samples": len(self.samples), "source": "nvml, 2 ms"}
+                    "reasons": reasons, "samples": len(self.samples), "source": "NVML every 2 ms"}
         if self.proc is None:
             return None
         self.proc.terminate()
