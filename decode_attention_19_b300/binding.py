@@ -60,6 +60,9 @@ def _load():
             "lowram_compress": [ctypes.POINTER(lowram_compress_shape)] + [_vp] * 18 + [sz, _vp],
             "lowram_dense_workspace_size": [i32, i32, i32, i32, i32, psz],
             "lowram_dense_decode_attn": [i32, i32, i32, i32, i32, i32, flt, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp],
+            "lowram_tail_append": [i32, i32, i32, i32, i32, i32, _vp, _vp, _vp, _vp, _vp],
+            "lowram_tail_decode_attn": [i32, i32, i32, i32, i32, i32, i32, flt, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp],
+            "lowram_merge_attn": [i32, i32, i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
             "lowram_get_error": [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)],
             "lowram_decode_uses_tensor_cores": [ctypes.POINTER(lowram_decode_shape), ctypes.POINTER(ctypes.c_int32)],
             "lowram_clear_error": [_vp, _vp],
@@ -311,6 +314,59 @@ def lowram_dense_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     ws = _workspace(lowram_dense_workspace_size(B, T, H_q, H_kv, d), workspace, dev)
     _check(_load().lowram_dense_decode_attn(B, T, H_q, H_kv, d, _act(q), float(sm_scale), _p(q), _p(k), _p(v),
                                             _p(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream()))
+    return out, lse
+
+
+# ------------------------------------------------------------------------------------------------
+# exact tail: tokens decoded after compression, kept as explicit rotated K and V
+# ------------------------------------------------------------------------------------------------
+def lowram_tail_append(k_new: torch.Tensor, v_new: torch.Tensor, tail_k: torch.Tensor, tail_v: torch.Tensor, t: int):
+    """Write one token's rotated keys and values [B, H_kv, d] into row t of the tail buffers [B, T_cap, H_kv, d]."""
+    B, T_cap, H_kv, d = tail_k.shape
+    _dev(k_new, v_new, tail_k, tail_v)
+    if k_new.shape != (B, H_kv, d) or v_new.shape != (B, H_kv, d) or tail_v.shape != tail_k.shape:
+        raise ValueError("k_new, v_new must be [B, H_kv, d] and the tail buffers [B, T_cap, H_kv, d]")
+    if not (k_new.dtype == v_new.dtype == tail_k.dtype == tail_v.dtype):
+        raise TypeError("k_new, v_new and the tail buffers must share one dtype")
+    _check(_load().lowram_tail_append(B, T_cap, H_kv, d, _act(tail_k), int(t), _p(k_new), _p(v_new), _p(tail_k),
+                                      _p(tail_v), _stream()))
+
+
+def lowram_tail_decode_attn(q: torch.Tensor, tail_k: torch.Tensor, tail_v: torch.Tensor, t_len: int, *,
+                            sm_scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                            lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                            want_lse: bool = True):
+    """Attention of q [B, H_q, d] over the first t_len rows of the tail buffers, read in place.  Returns (out, lse)."""
+    B, H_q, d = q.shape
+    T_cap, H_kv = tail_k.shape[1], tail_k.shape[2]
+    _dev(q, tail_k, tail_v)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=dev)
+    ws = _workspace(lowram_dense_workspace_size(B, int(t_len), H_q, H_kv, d), workspace, dev)
+    _check(_load().lowram_tail_decode_attn(B, T_cap, int(t_len), H_q, H_kv, d, _act(q), float(sm_scale), _p(q),
+                                           _p(tail_k), _p(tail_v), _p(out), _p(lse), _p(ws),
+                                           ws.numel() * ws.element_size(), _stream()))
+    return out, lse
+
+
+def lowram_merge_attn(out_a: torch.Tensor, lse_a: torch.Tensor, out_b: torch.Tensor, lse_b: torch.Tensor, *,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """Merge two attention results over disjoint token sets through their log-sum-exp.  Returns (out, lse);
+    out / lse may be given as out_a / lse_a for an in-place merge."""
+    B, H_q, d = out_a.shape
+    _dev(out_a, lse_a, out_b, lse_b)
+    for t in (out_a, lse_a, out_b, lse_b):
+        if t.dtype != torch.float32:
+            raise TypeError("merge operands are float32")
+    if out is None:
+        out = torch.empty_like(out_a)
+    if lse is None:
+        lse = torch.empty_like(lse_a)
+    _check(_load().lowram_merge_attn(B, H_q, d, _p(out_a), _p(lse_a), _p(out_b), _p(lse_b), _p(out), _p(lse),
+                                     _stream()))
     return out, lse
 
 

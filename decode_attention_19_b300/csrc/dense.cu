@@ -1,7 +1,8 @@
 // dense.cu -- comparator: split-T decode attention over an explicit, uncompressed, already rotated
-// K/V cache [B, T, H_kv, d].  Same split-softmax partial layout and merge kernel as the compressed
-// path.  This is the cache the compressed one replaces (LowRAM abstract: the KV cache's memory
-// footprint caps batch size and throughput).
+// K/V cache [B, T, H_kv, d]; sequence b's rows start at token b * Ts, so the exact tail of recent tokens is read
+// in place from its [B, T_cap, H_kv, d] buffer with Ts = T_cap.  Same split-softmax partial layout and merge
+// kernel as the compressed path.  This is the cache the compressed one replaces (LowRAM abstract: the KV
+// cache's memory footprint caps batch size and throughput).
 //
 // HBM-bound: every K and V byte is read once, 16 bytes per lane, streamed through a per-thread cp.async
 // ring in shared memory.  A group of d/VEC lanes holds one token (VEC elements per lane); the lanes of a
@@ -62,7 +63,7 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float (&a)[V], f
 }
 
 template <typename TE, int D, int G>
-__global__ void __launch_bounds__(kDenseThreads) dense_kernel(int T, int H_q, int H_kv, float scale,
+__global__ void __launch_bounds__(kDenseThreads) dense_kernel(int T, int Ts, int H_q, int H_kv, float scale,
                                                               const TE* __restrict__ q, const TE* __restrict__ K,
                                                               const TE* __restrict__ V, float* __restrict__ partial,
                                                               int n_split) {
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kDenseThreads) dense_kernel(int T, int H_q, in
             for (int u = 0; u < U; ++u) {
                 const int t = t0 + u * TPW + grp;
                 const bool ok = t < t_end;
-                const int64_t off = (((int64_t)b * T + (ok ? t : t_begin)) * H_kv + h) * D + sub * VEC;
+                const int64_t off = (((int64_t)b * Ts + (ok ? t : t_begin)) * H_kv + h) * D + sub * VEC;
                 cp_async16(&ring[((s * U + u) * 2 + 0) * kDenseThreads + tid], K + off, ok);
                 cp_async16(&ring[((s * U + u) * 2 + 1) * kDenseThreads + tid], V + off, ok);
             }
@@ -219,7 +220,7 @@ __device__ __forceinline__ void bf16x2_to_f2(uint32_t w, uint64_t& out) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kD2Threads) dense_bf16_kernel(int T, int H_q, int H_kv, float scale,
+__global__ void __launch_bounds__(kD2Threads) dense_bf16_kernel(int T, int Ts, int H_q, int H_kv, float scale,
                                                                 const __nv_bfloat16* __restrict__ q,
                                                                 const __nv_bfloat16* __restrict__ K,
                                                                 const __nv_bfloat16* __restrict__ V,
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kD2Threads) dense_bf16_kernel(int T, int H_q, 
                 const int r = i >> 4, c = i & 15;
                 const int t = t0 + r;
                 const bool ok = t < t_end;
-                const int64_t off = (((int64_t)b * T + (ok ? t : t_begin)) * H_kv + h) * 128 + c * 8;
+                const int64_t off = (((int64_t)b * Ts + (ok ? t : t_begin)) * H_kv + h) * 128 + c * 8;
                 cp_async16(reinterpret_cast<uint4*>(Kt + r * 256 + ((c ^ (r & 15)) << 4)), K + off, ok);
                 cp_async16(reinterpret_cast<uint4*>(Vt + r * 256 + (c << 4)), V + off, ok);
             }
@@ -378,7 +379,7 @@ int dense_splits(int B, int T, int H_kv) {
 }
 
 template <typename TE, int D>
-static cudaError_t dense_g(int B, int T, int H_q, int H_kv, float scale, const void* q, const void* k, const void* v,
+static cudaError_t dense_g(int B, int T, int Ts, int H_q, int H_kv, float scale, const void* q, const void* k, const void* v,
                            float* partial, int n_split, cudaStream_t st) {
     // the kv-heads of one token range are adjacent in launch order: they run together and read the same
     // [H_kv, d] token rows of K and V, so DRAM sees whole rows rather than one head's 2*d bytes per row
@@ -388,7 +389,7 @@ static cudaError_t dense_g(int B, int T, int H_q, int H_kv, float scale, const v
     auto go = [&](auto kern) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDenseSmem);
         if (e == cudaSuccess) {
-            kern<<<grid, kDenseThreads, kDenseSmem, st>>>(T, H_q, H_kv, scale, Q, K, V, partial, n_split);
+            kern<<<grid, kDenseThreads, kDenseSmem, st>>>(T, Ts, H_q, H_kv, scale, Q, K, V, partial, n_split);
             e = cudaGetLastError();
         }
     };
@@ -406,38 +407,38 @@ static cudaError_t dense_g(int B, int T, int H_q, int H_kv, float scale, const v
 int dense_records(int B, int T, int H_kv, int, int) { return dense_splits(B, T, H_kv); }
 
 template <int G>
-static cudaError_t dense2_go(int B, int T, int H_q, int H_kv, float scale, const void* q, const void* k, const void* v,
+static cudaError_t dense2_go(int B, int T, int Ts, int H_q, int H_kv, float scale, const void* q, const void* k, const void* v,
                              float* partial, int n_split, cudaStream_t st) {
     const size_t smem = dense2_smem(G);
     cudaError_t e = cudaFuncSetAttribute(dense_bf16_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // the kv-heads of one token range are adjacent in launch order (they read the same token rows)
     dim3 grid((unsigned)H_kv, (unsigned)n_split, (unsigned)B);
-    dense_bf16_kernel<G><<<grid, kD2Threads, smem, st>>>(T, H_q, H_kv, scale, (const __nv_bfloat16*)q,
+    dense_bf16_kernel<G><<<grid, kD2Threads, smem, st>>>(T, Ts, H_q, H_kv, scale, (const __nv_bfloat16*)q,
                                                         (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, partial,
                                                         n_split);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dense(int B, int T, int H_q, int H_kv, int d, int dtype, float scale, const void* q, const void* k,
+cudaError_t launch_dense(int B, int T, int Ts, int H_q, int H_kv, int d, int dtype, float scale, const void* q, const void* k,
                          const void* v, float* partial, int n_split, cudaStream_t st) {
     if (B == 0) return cudaSuccess;
     if (dtype == LOWRAM_BF16 && d == 128) {
         switch (H_q / H_kv) {
-            case 1: return dense2_go<1>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
-            case 2: return dense2_go<2>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
-            case 4: return dense2_go<4>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
-            case 7: return dense2_go<7>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
-            case 8: return dense2_go<8>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            case 1: return dense2_go<1>(B, T, Ts, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            case 2: return dense2_go<2>(B, T, Ts, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            case 4: return dense2_go<4>(B, T, Ts, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            case 7: return dense2_go<7>(B, T, Ts, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+            case 8: return dense2_go<8>(B, T, Ts, H_q, H_kv, scale, q, k, v, partial, n_split, st);
             default: return cudaErrorNotSupported;
         }
     }
     if (dtype == LOWRAM_BF16) {
-        if (d == 128) return dense_g<__nv_bfloat16, 128>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
-        if (d == 64) return dense_g<__nv_bfloat16, 64>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+        if (d == 128) return dense_g<__nv_bfloat16, 128>(B, T, Ts, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+        if (d == 64) return dense_g<__nv_bfloat16, 64>(B, T, Ts, H_q, H_kv, scale, q, k, v, partial, n_split, st);
     } else {
-        if (d == 128) return dense_g<float, 128>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
-        if (d == 64) return dense_g<float, 64>(B, T, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+        if (d == 128) return dense_g<float, 128>(B, T, Ts, H_q, H_kv, scale, q, k, v, partial, n_split, st);
+        if (d == 64) return dense_g<float, 64>(B, T, Ts, H_q, H_kv, scale, q, k, v, partial, n_split, st);
     }
     return cudaErrorNotSupported;
 }

@@ -108,10 +108,18 @@ cudaError_t launch_project(const CompressArgs& a, cudaStream_t st);
 cudaError_t launch_predict_err(const CompressArgs& a, int layer, float* err, cudaStream_t st);
 cudaError_t launch_residual_rows(const CompressArgs& a, int layer, cudaStream_t st);
 
-// Comparator: token splits, and partial records per (sequence, q-head) that launch_dense writes
+// Comparator (and the exact tail): token splits, and partial records per (sequence, q-head) that launch_dense
+// writes; sequence b's K/V rows start at token b * Ts
 int dense_splits(int B, int T, int H_kv);
 int dense_records(int B, int T, int H_kv, int d, int dtype);
-cudaError_t launch_dense(int B, int T, int H_q, int H_kv, int d, int dtype, float scale, const void* q, const void* k,
-                         const void* v, float* partial, int n_split, cudaStream_t st);
+cudaError_t launch_dense(int B, int T, int Ts, int H_q, int H_kv, int d, int dtype, float scale, const void* q,
+                         const void* k, const void* v, float* partial, int n_split, cudaStream_t st);
+
+// Exact tail: write one token's K and V [B, H_kv, d] into row t of [B, T_cap, H_kv, d]; merge two attention
+// results over disjoint token sets through their log-sum-exp
+cudaError_t launch_tail_append(int B, int T_cap, int H_kv, int d, int elem_bytes, int t, const void* k_new,
+                               const void* v_new, void* tail_k, void* tail_v, cudaStream_t st);
+cudaError_t launch_merge_attn(int B, int H_q, int d, const float* out_a, const float* lse_a, const float* out_b,
+                              const float* lse_b, float* out, float* lse, cudaStream_t st);
 
 }  // namespace lowram

@@ -377,9 +377,11 @@ lowram_status lowram_dense_workspace_size(int32_t B, int32_t T, int32_t H_q, int
     return LOWRAM_OK;
 }
 
-lowram_status lowram_dense_decode_attn(int32_t B, int32_t T, int32_t H_q, int32_t H_kv, int32_t d, int32_t dtype,
-                                       float sm_scale, const void* q, const void* k, const void* v, float* out,
-                                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+// Attention over explicit K/V rows [B, *, H_kv, d] whose sequence b starts at token b * Ts (Ts = T for a plain
+// cache, T_cap for the exact tail's buffers).
+static lowram_status dense_impl(int32_t B, int32_t T, int32_t Ts, int32_t H_q, int32_t H_kv, int32_t d,
+                                int32_t dtype, float sm_scale, const void* q, const void* k, const void* v, float* out,
+                                float* lse, void* workspace, size_t workspace_bytes, void* stream) {
     size_t need = 0;
     lowram_status st = lowram_dense_workspace_size(B, T, H_q, H_kv, d, &need);
     if (st != LOWRAM_OK) return st;
@@ -398,11 +400,58 @@ lowram_status lowram_dense_decode_attn(int32_t B, int32_t T, int32_t H_q, int32_
     const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf((float)d);
     cudaError_t e = cudaSuccess;
     if (T > 0) {
-        e = launch_dense(B, T, H_q, H_kv, d, dtype, scale, q, k, v, partial, ns, cs);
+        e = launch_dense(B, T, Ts, H_q, H_kv, d, dtype, scale, q, k, v, partial, ns, cs);
         if (e != cudaSuccess) return cuda_fail(e, "dense");
     }
     e = launch_merge(B, H_q, T > 0 ? dense_records(B, T, H_kv, d, dtype) : 0, d, partial, out, lse, cs);
     return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "merge");
+}
+
+lowram_status lowram_dense_decode_attn(int32_t B, int32_t T, int32_t H_q, int32_t H_kv, int32_t d, int32_t dtype,
+                                       float sm_scale, const void* q, const void* k, const void* v, float* out,
+                                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    return dense_impl(B, T, T, H_q, H_kv, d, dtype, sm_scale, q, k, v, out, lse, workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------------------------------------------------------------
+// exact tail
+// ------------------------------------------------------------------------------------------------
+lowram_status lowram_tail_append(int32_t B, int32_t T_cap, int32_t H_kv, int32_t d, int32_t dtype, int32_t t,
+                                 const void* k_new, const void* v_new, void* tail_k, void* tail_v, void* stream) {
+    if (B < 0 || T_cap < 1 || H_kv < 1 || (d != 64 && d != 128))
+        return fail(LOWRAM_ERR_INVALID_ARG, "B=%d T_cap=%d H_kv=%d d=%d", B, T_cap, H_kv, d);
+    if (!is_act(dtype)) return fail(LOWRAM_ERR_INVALID_ARG, "dtype=%d", dtype);
+    if (t < 0 || t >= T_cap) return fail(LOWRAM_ERR_INVALID_ARG, "row t=%d outside the tail's capacity %d", t, T_cap);
+    if (B == 0) return LOWRAM_OK;
+    if (!k_new || !v_new || !tail_k || !tail_v) return fail(LOWRAM_ERR_INVALID_ARG, "a required pointer is NULL");
+    const void* ptrs[] = {k_new, v_new, tail_k, tail_v};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
+    const cudaError_t e = launch_tail_append(B, T_cap, H_kv, d, dtype == LOWRAM_BF16 ? 2 : 4, t, k_new, v_new, tail_k,
+                                             tail_v, (cudaStream_t)stream);
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "tail_append");
+}
+
+lowram_status lowram_tail_decode_attn(int32_t B, int32_t T_cap, int32_t t_len, int32_t H_q, int32_t H_kv, int32_t d,
+                                      int32_t dtype, float sm_scale, const void* q, const void* tail_k,
+                                      const void* tail_v, float* out, float* lse, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    if (t_len < 0 || t_len > T_cap)
+        return fail(LOWRAM_ERR_INVALID_ARG, "t_len=%d outside the tail's capacity %d", t_len, T_cap);
+    return dense_impl(B, t_len, T_cap, H_q, H_kv, d, dtype, sm_scale, q, tail_k, tail_v, out, lse, workspace,
+                      workspace_bytes, stream);
+}
+
+lowram_status lowram_merge_attn(int32_t B, int32_t H_q, int32_t d, const float* out_a, const float* lse_a,
+                                const float* out_b, const float* lse_b, float* out, float* lse, void* stream) {
+    if (B < 0 || H_q < 1 || d < 1) return fail(LOWRAM_ERR_INVALID_ARG, "B=%d H_q=%d d=%d", B, H_q, d);
+    if (B == 0) return LOWRAM_OK;
+    if (!out_a || !lse_a || !out_b || !lse_b || !out) return fail(LOWRAM_ERR_INVALID_ARG, "a required pointer is NULL");
+    const void* ptrs[] = {out_a, lse_a, out_b, lse_b, out, lse};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
+    const cudaError_t e = launch_merge_attn(B, H_q, d, out_a, lse_a, out_b, lse_b, out, lse, (cudaStream_t)stream);
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "merge_attn");
 }
 
 // ------------------------------------------------------------------------------------------------

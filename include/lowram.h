@@ -257,6 +257,51 @@ LOWRAM_API lowram_status lowram_dense_decode_attn(int32_t B, int32_t T, int32_t 
                                        float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Exact tail (LowRAM Paper: Amortised Values and Low-Rank Keys for KV Compression, step-by-step:
+ * the prompt's cache is compressed; tokens decoded afterwards are appended).  The tokens generated
+ * after compression stay explicit: their already rotated keys and their values live in tail buffers
+ * tail_k, tail_v [B, T_cap, H_kv, d] (dtype), the same length t_len in every sequence.  A decode
+ * step attends the compressed body (lowram_decode_attn with lse) and the tail
+ * (lowram_tail_decode_attn), then merges the two with lowram_merge_attn; the result is attention
+ * over body and tail together.
+ * ------------------------------------------------------------------------------------------- */
+
+/*
+ * lowram_tail_append -- write one decoded token's rotated keys k_new and values v_new, each
+ * [B, H_kv, d] in dtype (LOWRAM_BF16 or LOWRAM_F32), into row t (0 <= t < T_cap) of every
+ * sequence's tail buffers.  d is 64 or 128; all pointers 16-byte aligned device memory owned by
+ * the caller.  Errors: LOWRAM_ERR_INVALID_ARG (shape, dtype, t out of range, NULL pointer),
+ * LOWRAM_ERR_ALIGNMENT.
+ */
+LOWRAM_API lowram_status lowram_tail_append(int32_t B, int32_t T_cap, int32_t H_kv, int32_t d, int32_t dtype, int32_t t,
+                                            const void* k_new, const void* v_new, void* tail_k, void* tail_v,
+                                            void* stream);
+
+/*
+ * lowram_tail_decode_attn -- softmax attention of q [B, H_q, d] (dtype) over the first t_len rows
+ * (0 <= t_len <= T_cap) of the tail buffers, read in place; out [B, H_q, d] float32, lse [B, H_q]
+ * float32 or NULL (-inf and a zero output when t_len = 0).  sm_scale <= 0 means 1/sqrt(d).  The
+ * workspace is lowram_dense_workspace_size(B, t_len, H_q, H_kv, d) bytes.  Same kernels and errors
+ * as lowram_dense_decode_attn.
+ */
+LOWRAM_API lowram_status lowram_tail_decode_attn(int32_t B, int32_t T_cap, int32_t t_len, int32_t H_q, int32_t H_kv,
+                                                 int32_t d, int32_t dtype, float sm_scale, const void* q,
+                                                 const void* tail_k, const void* tail_v, float* out, float* lse,
+                                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * lowram_merge_attn -- combine two attention results of the same queries over disjoint token sets:
+ * with W = max(lse_a, lse_b), a = exp(lse_a - W), b = exp(lse_b - W):
+ *   out = (a out_a + b out_b) / (a + b),  lse = W + log(a + b);
+ * an empty set has lse = -inf (both empty: out = 0, lse = -inf).  out_*, out [B, H_q, d] float32;
+ * lse_*, lse [B, H_q] float32 (lse may be NULL).  out may be out_a or out_b and lse may be lse_a or
+ * lse_b (in-place merge).  Errors: LOWRAM_ERR_INVALID_ARG, LOWRAM_ERR_ALIGNMENT.
+ */
+LOWRAM_API lowram_status lowram_merge_attn(int32_t B, int32_t H_q, int32_t d, const float* out_a, const float* lse_a,
+                                           const float* out_b, const float* lse_b, float* out, float* lse,
+                                           void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Status
  * ------------------------------------------------------------------------------------------- */
 /* Synchronises `stream`, returns the device check word accumulated in `workspace` since it was last

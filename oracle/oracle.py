@@ -31,7 +31,7 @@ __all__ = [
     "build", "lib", "Dims", "f64", "round_bf16", "round_f16", "round_f32", "quant_int4_g32",
     "dequant_int4_g32", "quant_int8_vec", "dequant_int8_vec", "rope", "rope_rows", "rope_angles", "mlp",
     "rebuild_keys", "predict_values", "decode", "project", "residuals", "compress_group",
-    "dense_decode", "top_n", "n_res_for", "max_threads", "store",
+    "dense_decode", "merge_attn", "top_n", "n_res_for", "max_threads", "store",
 ]
 
 
@@ -399,4 +399,23 @@ def dense_decode(q, k, v, *, sm_scale: float = 0.0, threads: int = 0):
     lse = np.empty((B, H_q))
     _chk(lib().lro_dense_decode(B, T, H_q, H_kv, d, float(sm_scale), _p(Q), _p(K), _p(V), _p(out), _p(lse),
                                 threads), "dense_decode")
+    return out, lse
+
+
+def merge_attn(out_a, lse_a, out_b, lse_b):
+    """Attention over the union of two disjoint token sets from the two sets' results: the tokens decoded after
+    the prompt's cache was compressed stay explicit and are attended next to the compressed body [EX
+    "Step-by-step mental model for one decoding session"].  With W = max(lse_a, lse_b), a = exp(lse_a - W),
+    b = exp(lse_b - W): out = (a out_a + b out_b) / (a + b), lse = W + log(a + b); an empty set has lse = -inf
+    (both empty: out = 0, lse = -inf).  Plain fp64 numpy."""
+    oa, la, ob, lb = f64(out_a), f64(lse_a), f64(out_b), f64(lse_b)
+    W = np.maximum(la, lb)
+    empty = np.isneginf(W)
+    Wf = np.where(empty, 0.0, W)
+    a = np.where(empty, 0.0, np.exp(la - Wf))
+    b = np.where(empty, 0.0, np.exp(lb - Wf))
+    s = a + b
+    with np.errstate(invalid="ignore", divide="ignore"):
+        out = np.where(empty[..., None], 0.0, (a[..., None] * oa + b[..., None] * ob) / np.where(s == 0, 1.0, s)[..., None])
+        lse = np.where(empty, -np.inf, Wf + np.log(np.where(s == 0, 1.0, s)))
     return out, lse

@@ -407,6 +407,58 @@ def test_dense_decode_matches_sdpa():
                                atol=1e-12)
 
 
+# ------------------------------------------------------------------------------------------------
+# exact tail: body and tail attended separately, merged through their log-sum-exp
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("cut", [1, 17, 32])
+def test_merge_of_a_split_equals_attention_over_the_union(cut):
+    B, T, H_q, H_kv, d = 2, 33, 8, 2, 16
+    q, k, v = RNG.normal(0, 1, (B, H_q, d)), RNG.normal(0, 2, (B, T, H_kv, d)), RNG.normal(0, 1, (B, T, H_kv, d))
+    oa, la = O.dense_decode(q, k[:, :cut], v[:, :cut])
+    ob, lb = O.dense_decode(q, k[:, cut:], v[:, cut:])
+    out, lse = O.merge_attn(oa, la, ob, lb)
+    np.testing.assert_allclose(out, sdpa(q, k, v), atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(torch.as_tensor(torch_logits(q, k, d ** -0.5)), -1).numpy(),
+                               atol=1e-12)
+    out2, lse2 = O.merge_attn(ob, lb, oa, la)          # order of the two sets does not matter
+    np.testing.assert_allclose(out2, out, atol=1e-14)
+    np.testing.assert_allclose(lse2, lse, atol=1e-14)
+
+
+def test_merge_with_empty_sets():
+    o = RNG.normal(0, 1, (2, 3, 4))
+    l = RNG.normal(0, 1, (2, 3))
+    ninf = np.full((2, 3), -np.inf)
+    out, lse = O.merge_attn(o, l, np.zeros_like(o), ninf)
+    np.testing.assert_array_equal(out, o)
+    np.testing.assert_array_equal(lse, l)
+    out, lse = O.merge_attn(np.zeros_like(o), ninf, np.zeros_like(o), ninf)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_compressed_body_plus_exact_tail_equals_sdpa_over_everything():
+    """Full rank, every residual kept, S = T: the body is exact, so body + tail merged is textbook attention over
+    the prompt's tokens followed by the explicitly kept decoded tokens."""
+    g = full_rank_group(seed=7)
+    B, T, H_q, H_kv, d, G = g["B"], g["T"], g["H_q"], g["H_kv"], g["d"], g["G"]
+    theta, n_tail = 1e4, 5
+    comp = O.compress_group(g["k_cat"], g["vs"], g["proj"], g["bases"], g["w1s"], g["w2s"], G=G, H_kv=H_kv, d=d,
+                            n_res=T, coef_fmt="f64", res_fmt="f64")
+    l = 1
+    k_body = rope_complex(g["k_cat"].reshape(B, T, G, H_kv, d)[:, :, l], np.arange(T)[None, :, None], theta)
+    k_tail_pre = RNG.normal(0, 1, (B, n_tail, H_kv, d))
+    k_tail = rope_complex(k_tail_pre, np.arange(T, T + n_tail)[None, :, None], theta)
+    v_tail = RNG.normal(0, 1, (B, n_tail, H_kv, d))
+    lay = comp["layers"][l]
+    body = O.decode(g["q"], comp["coef"], g["bases"][l], g["w1s"][l], g["w2s"][l], S=T, theta=theta,
+                    res_idx=lay["res_idx"], res_val=lay["res_val"])
+    ot, lt = O.dense_decode(g["q"], k_tail, v_tail)
+    out, lse = O.merge_attn(body.out, body.lse, ot, lt)
+    k_all = np.concatenate([k_body, k_tail], axis=1)
+    v_all = np.concatenate([g["vs"][l], v_tail], axis=1)
+    np.testing.assert_allclose(out, sdpa(g["q"], k_all, v_all), rtol=0, atol=1e-10)
+
+
 def test_residual_budgets_of_the_workloads():
     # ceil(rho * T): 0.25*256, 0.1*8192, 0.1*32768, 0.1*4096, 0.05*16384
     assert [O.n_res_for(r, T) for r, T in [(0.25, 256), (0.1, 8192), (0.1, 32768), (0.1, 4096), (0.05, 16384)]] \
