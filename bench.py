@@ -509,23 +509,37 @@ def main():
     torch.cuda.synchronize()
     ms_b2b = e0.elapsed_time(e1)
 
-    # end to end through the public API: q from pinned host memory in, out back to pinned host memory
+    # end to end through the public API: every step copies its inputs (the L layer calls' queries) from pinned host
+    # memory in one transfer before its first call, and reads its results (the L outputs) back to pinned host memory
+    # in one transfer after its last call; each call writes its own output buffer.  The timed intervals are the L
+    # calls, the first including the upload and the last the download (the L2 flush between calls stays outside).
     e2e = None
     if not args.no_e2e:
-        q_host = [q.cpu().pin_memory() for q in qs]
-        out_host = [torch.empty((w.B, w.H_q, w.d), dtype=torch.float32).pin_memory() for _ in range(w.L)]
-        q_dev = torch.empty_like(qs[0])
+        q_host = torch.stack([q.cpu() for q in qs]).pin_memory()                       # [L, B, H_q, d]
+        out_host = torch.empty((w.L, w.B, w.H_q, w.d), dtype=torch.float32).pin_memory()
+        q_dev = torch.empty((w.L,) + tuple(qs[0].shape), dtype=qs[0].dtype, device=dev)
+        out_dev = torch.empty((w.L, w.B, w.H_q, w.d), dtype=torch.float32, device=dev)
         st = torch.cuda.current_stream()
+
+        def call_e2e(l):
+            a = args_l[l]
+            L.lowram_decode_attn(q_dev[l], a["coef"], a["basis"], a["w1"], a["w2"], rope_cos=cos, rope_sin=sin, S=w.S,
+                                 coef_scale=a["coef_scale"], pos=pos, res_idx=a["res_idx"], res_val=a["res_val"],
+                                 res_scale=a["res_scale"], out=out_dev[l], workspace=ws, want_lse=False)
+
         e2e_ms = []
         for s in range(args.warmup + args.steps):
             pairs = []
+            gpu_backlog()
             for l in range(w.L):
                 flush.zero_()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
-                q_dev.copy_(q_host[l], non_blocking=True)
-                call(l, q=q_dev)
-                out_host[l].copy_(out, non_blocking=True)
+                if l == 0:
+                    q_dev.copy_(q_host, non_blocking=True)
+                call_e2e(l)
+                if l == w.L - 1:
+                    out_host.copy_(out_dev, non_blocking=True)
                 b.record()
                 pairs.append((a, b))
             st.synchronize()
@@ -533,8 +547,8 @@ def main():
                 e2e_ms.append(sum(a.elapsed_time(b) for a, b in pairs))
         e2e_value, m = job_throughput(float(np.mean(e2e_ms)), world, dist, dev)
         e2e = {"value": e2e_value, "unit": UNIT,
-               "h2d_bytes_per_step": w.L * qs[0].numel() * qs[0].element_size(),
-               "d2h_bytes_per_step": w.L * out.numel() * out.element_size(), "ms_per_step": m}
+               "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
+               "d2h_bytes_per_step": out_host.numel() * out_host.element_size(), "ms_per_step": m}
 
     # roofline of the dominant kernel
     bytes_call, f_keys, f_sel, f_mlp = algorithmic(w)
