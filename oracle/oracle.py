@@ -31,7 +31,7 @@ __all__ = [
     "build", "lib", "Dims", "f64", "round_bf16", "round_f16", "round_f32", "quant_int4_g32",
     "dequant_int4_g32", "quant_int8_vec", "dequant_int8_vec", "rope", "rope_rows", "rope_angles", "mlp",
     "rebuild_keys", "predict_values", "decode", "project", "residuals", "compress_group",
-    "dense_decode", "merge_attn", "top_n", "n_res_for", "max_threads", "store",
+    "dense_decode", "merge_attn", "fit_basis", "top_n", "n_res_for", "max_threads", "store",
 ]
 
 
@@ -419,3 +419,24 @@ def merge_attn(out_a, lse_a, out_b, lse_b):
         out = np.where(empty[..., None], 0.0, (a[..., None] * oa + b[..., None] * ob) / np.where(s == 0, 1.0, s)[..., None])
         lse = np.where(empty, -np.inf, Wf + np.log(np.where(s == 0, 1.0, s)))
     return out, lse
+
+
+def fit_basis(k_cat, r: int, G: int, H_kv: int, d: int, *, pos=None, keys_post_rope: bool = False,
+              theta: float = 1e4):
+    """The group's shared low-rank key basis from the prompt's keys, the cross-layer SVD of the RoPE-inverted
+    keys [EX "Asymmetric key compression with xKV": the G layers' keys are stacked and factored together, RoPE
+    inverted first].  With k_cat [N = B*T, D = G*H_kv*d] (rotated back by each token's position when the keys
+    are given rotated), the rank-r subspace of the largest singular values is spanned by the top-r eigenvectors
+    U [D, r] of the Gram matrix k_cat^T k_cat (fp64, numpy.linalg.eigh as the eigensolver).
+    Returns (proj [r, D] = U^T, bases [G] x [H_kv*d, r] = U's layer blocks, the r eigenvalues descending)."""
+    K = f64(k_cat)
+    B, T = K.shape[0], K.shape[1]
+    K = K.reshape(B, T, G, H_kv, d)
+    if keys_post_rope:
+        P = np.arange(T)[None, :].repeat(B, 0) if pos is None else _i32(pos).astype(np.float64)
+        K = rope_rows(K, np.broadcast_to(np.asarray(P)[:, :, None, None], (B, T, G, H_kv)), theta, inverse=True)
+    K = K.reshape(B * T, G * H_kv * d)
+    w, U = np.linalg.eigh(K.T @ K)
+    order = np.argsort(w)[::-1][:r]
+    U = U[:, order]
+    return U.T.copy(), [U[l * H_kv * d:(l + 1) * H_kv * d].copy() for l in range(G)], w[order]

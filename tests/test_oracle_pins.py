@@ -459,6 +459,53 @@ def test_compressed_body_plus_exact_tail_equals_sdpa_over_everything():
     np.testing.assert_allclose(out, sdpa(g["q"], k_all, v_all), rtol=0, atol=1e-10)
 
 
+# ------------------------------------------------------------------------------------------------
+# fitted basis (cross-layer SVD of the RoPE-inverted keys)
+# ------------------------------------------------------------------------------------------------
+def low_rank_keys(B, T, D, r, noise, seed):
+    rng = np.random.default_rng(seed)
+    U, _ = np.linalg.qr(rng.normal(0, 1, (D, r)))
+    sig = np.geomspace(10.0, 1.0, r)                     # decaying spectrum, well above the noise
+    C = rng.normal(0, 1, (B * T, r)) * sig
+    return (C @ U.T + noise * rng.normal(0, 1, (B * T, D))).reshape(B, T, D)
+
+
+def test_fit_basis_is_exact_for_low_rank_keys():
+    B, T, G, H_kv, d, r = 2, 50, 2, 2, 8, 6
+    K = low_rank_keys(B, T, G * H_kv * d, r, 0.0, 1)
+    proj, bases, w = O.fit_basis(K, r, G, H_kv, d)
+    Wst = np.concatenate(bases, axis=0)
+    np.testing.assert_allclose(proj @ Wst, np.eye(r), atol=1e-12)             # proj is a left inverse
+    Kf = K.reshape(B * T, -1)
+    np.testing.assert_allclose(Kf @ proj.T @ Wst.T, Kf, atol=1e-9)              # rank r keys are rebuilt
+    assert np.all(np.diff(w) <= 0)
+
+
+def test_fit_basis_meets_eckart_young():
+    """Rebuild error of the fitted subspace = the norm of the discarded singular values (numpy SVD of the keys
+    themselves, not of the Gram matrix), and the subspace is the top-r right singular subspace."""
+    B, T, G, H_kv, d, r = 2, 60, 2, 2, 8, 5
+    K = low_rank_keys(B, T, G * H_kv * d, r, 0.3, 2)
+    proj, bases, _ = O.fit_basis(K, r, G, H_kv, d)
+    Kf = K.reshape(B * T, -1)
+    s = np.linalg.svd(Kf, compute_uv=False)
+    err = np.linalg.norm(Kf - Kf @ proj.T @ proj)
+    assert abs(err - math.sqrt(float(np.sum(s[r:] ** 2)))) <= 1e-9 * err
+    Vt = np.linalg.svd(Kf, full_matrices=False)[2][:r]
+    np.testing.assert_allclose(proj.T @ proj, Vt.T @ Vt, atol=1e-9)
+
+
+def test_fit_basis_inverts_rope_of_rotated_keys():
+    B, T, G, H_kv, d, r, theta = 2, 40, 2, 2, 8, 5, 1e4
+    K = low_rank_keys(B, T, G * H_kv * d, r, 0.1, 3).reshape(B, T, G, H_kv, d)
+    pos = np.stack([np.sort(RNG.choice(200, T, replace=False)) for _ in range(B)]).astype(np.int32)
+    K_rot = rope_complex(K, pos[:, :, None, None], theta)
+    p1, _, w1 = O.fit_basis(K, r, G, H_kv, d)
+    p2, _, w2 = O.fit_basis(K_rot, r, G, H_kv, d, pos=pos, keys_post_rope=True, theta=theta)
+    np.testing.assert_allclose(w2, w1, rtol=1e-10)
+    np.testing.assert_allclose(p2.T @ p2, p1.T @ p1, atol=1e-9)
+
+
 def test_residual_budgets_of_the_workloads():
     # ceil(rho * T): 0.25*256, 0.1*8192, 0.1*32768, 0.1*4096, 0.05*16384
     assert [O.n_res_for(r, T) for r, T in [(0.25, 256), (0.1, 8192), (0.1, 32768), (0.1, 4096), (0.05, 16384)]] \
