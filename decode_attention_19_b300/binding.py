@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "liblowram.so")
 
 LOWRAM_F32, LOWRAM_BF16, LOWRAM_INT4_G32, LOWRAM_INT8_VEC = 0, 1, 2, 3
-CHECK_POS_RANGE, CHECK_RES_INDEX = 1, 2
+CHECK_POS_RANGE, CHECK_RES_INDEX, CHECK_TIMEOUT, CHECK_NOT_PD = 1, 2, 4, 8
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported", 4: "workspace", 5: "cuda",
           6: "device check"}
 
@@ -60,6 +60,9 @@ def _load():
             "lowram_compress": [ctypes.POINTER(lowram_compress_shape)] + [_vp] * 18 + [sz, _vp],
             "lowram_dense_workspace_size": [i32, i32, i32, i32, i32, psz],
             "lowram_dense_decode_attn": [i32, i32, i32, i32, i32, i32, flt, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp],
+            "lowram_fit_basis_workspace_size": [ctypes.POINTER(lowram_compress_shape), psz],
+            "lowram_fit_basis": [ctypes.POINTER(lowram_compress_shape), _vp, _vp, _vp, _vp, i32, ctypes.c_uint64, _vp,
+                                 _vp, _vp, sz, _vp],
             "lowram_tail_append": [i32, i32, i32, i32, i32, i32, _vp, _vp, _vp, _vp, _vp],
             "lowram_tail_decode_attn": [i32, i32, i32, i32, i32, i32, i32, flt, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp],
             "lowram_merge_attn": [i32, i32, i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
@@ -315,6 +318,31 @@ def lowram_dense_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     _check(_load().lowram_dense_decode_attn(B, T, H_q, H_kv, d, _act(q), float(sm_scale), _p(q), _p(k), _p(v),
                                             _p(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream()))
     return out, lse
+
+
+# ------------------------------------------------------------------------------------------------
+# fitted basis: cross-layer SVD of the RoPE-inverted keys (the proj and bases lowram_compress takes)
+# ------------------------------------------------------------------------------------------------
+def lowram_fit_basis(keys: torch.Tensor, r: int, *, pos: Optional[torch.Tensor] = None,
+                     rope_cos: Optional[torch.Tensor] = None, rope_sin: Optional[torch.Tensor] = None,
+                     keys_post_rope: bool = False, iters: int = 8, seed: int = 0,
+                     workspace: Optional[torch.Tensor] = None):
+    """keys [B, T, G, H_kv, d] -> (proj [r, G*H_kv*d] float32, bases G x [H_kv*d, r] in keys' dtype, workspace)."""
+    B, T, G, H_kv, d = keys.shape
+    dev = keys.device
+    _dev(keys, pos, rope_cos, rope_sin)
+    shape = lowram_compress_shape(B, T, G, H_kv, d, int(r), 32, 0, _act(keys), LOWRAM_BF16, LOWRAM_BF16,
+                                  int(bool(keys_post_rope)), 0 if rope_cos is None else rope_cos.shape[1])
+    n = ctypes.c_size_t(0)
+    _check(_load().lowram_fit_basis_workspace_size(ctypes.byref(shape), ctypes.byref(n)))
+    ws = _workspace(n.value, workspace, dev)
+    proj = torch.empty((int(r), G * H_kv * d), dtype=torch.float32, device=dev)
+    bases = [torch.empty((H_kv * d, int(r)), dtype=keys.dtype, device=dev) for _ in range(G)]
+    arr = _ptr_array(bases)
+    _check(_load().lowram_fit_basis(ctypes.byref(shape), _p(keys), _p(pos), _p(rope_cos), _p(rope_sin), int(iters),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, _p(proj), ctypes.cast(arr, _vp), _p(ws),
+                                    ws.numel() * ws.element_size(), _stream()))
+    return proj, bases, ws
 
 
 # ------------------------------------------------------------------------------------------------

@@ -115,6 +115,23 @@ int dense_records(int B, int T, int H_kv, int d, int dtype);
 cudaError_t launch_dense(int B, int T, int Ts, int H_q, int H_kv, int d, int dtype, float scale, const void* q,
                          const void* k, const void* v, float* partial, int n_split, cudaStream_t st);
 
+// Fitted basis (fit.cu): top-r eigenvectors of the RoPE-inverted keys' Gram matrix by subspace iteration
+struct FitArgs {
+    int B, T, G, H_kv, d, r, max_pos, post_rope, iters;
+    bool bf16;
+    uint64_t seed;
+    const void* keys;            // [B, T, G, H_kv, d]
+    const int32_t* pos;          // [B, T] or null
+    const float* rope_cos;
+    const float* rope_sin;
+    float* proj_out;             // [r, G*H_kv*d]
+    void* basis_out[16];         // G x [H_kv*d, r]
+    void* scratch;               // fit_workspace_bytes
+    uint32_t* check;
+};
+size_t fit_workspace_bytes(int64_t N, int D, int r);
+cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st);
+
 // Exact tail: write one token's K and V [B, H_kv, d] into row t of [B, T_cap, H_kv, d]; merge two attention
 // results over disjoint token sets through their log-sum-exp
 cudaError_t launch_tail_append(int B, int T_cap, int H_kv, int d, int elem_bytes, int t, const void* k_new,

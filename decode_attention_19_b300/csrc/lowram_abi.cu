@@ -292,6 +292,68 @@ static lowram_status check_compress_shape(const lowram_compress_shape* s) {
     return LOWRAM_OK;
 }
 
+// ------------------------------------------------------------------------------------------------
+// fitted basis
+// ------------------------------------------------------------------------------------------------
+static lowram_status check_fit_shape(const lowram_compress_shape* s) {
+    if (!s) return fail(LOWRAM_ERR_INVALID_ARG, "shape is NULL");
+    if (s->B < 0 || s->T < 0) return fail(LOWRAM_ERR_INVALID_ARG, "bad sizes (B=%d T=%d)", s->B, s->T);
+    if (s->G < 1 || s->G > 16) return fail(LOWRAM_ERR_UNSUPPORTED, "G=%d (1..16)", s->G);
+    if (s->H_kv < 1) return fail(LOWRAM_ERR_INVALID_ARG, "H_kv=%d", s->H_kv);
+    if (s->d != 64 && s->d != 128) return fail(LOWRAM_ERR_UNSUPPORTED, "d=%d (64 or 128 supported)", s->d);
+    const int64_t D = (int64_t)s->G * s->H_kv * s->d;
+    if (s->r < 32 || s->r % 32 != 0 || s->r > 1024 || s->r > D) return fail(LOWRAM_ERR_UNSUPPORTED, "r=%d", s->r);
+    if (D > 16384) return fail(LOWRAM_ERR_UNSUPPORTED, "G*H_kv*d=%lld (at most 16384)", (long long)D);
+    if ((int64_t)s->B * s->T < s->r)
+        return fail(LOWRAM_ERR_INVALID_ARG, "B*T=%lld tokens, fewer than the rank r=%d", (long long)s->B * s->T, s->r);
+    if (!is_act(s->act_dtype)) return fail(LOWRAM_ERR_INVALID_ARG, "act_dtype=%d", s->act_dtype);
+    if (s->keys_post_rope && s->max_pos < 1) return fail(LOWRAM_ERR_INVALID_ARG, "max_pos=%d", s->max_pos);
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_fit_basis_workspace_size(const lowram_compress_shape* shape, size_t* bytes) {
+    lowram_status st = check_fit_shape(shape);
+    if (st != LOWRAM_OK) return st;
+    if (!bytes) return fail(LOWRAM_ERR_INVALID_ARG, "bytes is NULL");
+    const int64_t N = (int64_t)shape->B * shape->T;
+    *bytes = kHeader + align256(fit_workspace_bytes(N, shape->G * shape->H_kv * shape->d, shape->r));
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_fit_basis(const lowram_compress_shape* shape, const void* keys, const int32_t* pos,
+                               const float* rope_cos, const float* rope_sin, int32_t iters, uint64_t seed,
+                               float* proj_out, void* const* basis_out, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    size_t need = 0;
+    lowram_status st = lowram_fit_basis_workspace_size(shape, &need);
+    if (st != LOWRAM_OK) return st;
+    const lowram_compress_shape& s = *shape;
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return fail(LOWRAM_ERR_WORKSPACE, "workspace %zu bytes, %zu needed", workspace ? workspace_bytes : 0, need);
+    if (iters < 1 || iters > 1000) return fail(LOWRAM_ERR_INVALID_ARG, "iters=%d (1..1000)", iters);
+    if (!keys || !proj_out || !basis_out) return fail(LOWRAM_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (s.keys_post_rope && (!rope_cos || !rope_sin)) return fail(LOWRAM_ERR_INVALID_ARG, "RoPE tables are NULL");
+    const void* ptrs[] = {keys, pos, rope_cos, rope_sin, proj_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
+    for (int l = 0; l < s.G; ++l) {
+        if (!basis_out[l]) return fail(LOWRAM_ERR_INVALID_ARG, "basis_out[%d] is NULL", l);
+        if (!aligned16(basis_out[l])) return fail(LOWRAM_ERR_ALIGNMENT, "basis_out[%d] is not 16-byte aligned", l);
+    }
+    FitArgs f{};
+    f.B = s.B; f.T = s.T; f.G = s.G; f.H_kv = s.H_kv; f.d = s.d; f.r = s.r;
+    f.max_pos = s.max_pos; f.post_rope = s.keys_post_rope ? 1 : 0; f.iters = iters;
+    f.bf16 = s.act_dtype == LOWRAM_BF16;
+    f.seed = seed;
+    f.keys = keys; f.pos = pos; f.rope_cos = rope_cos; f.rope_sin = rope_sin;
+    f.proj_out = proj_out;
+    for (int l = 0; l < s.G; ++l) f.basis_out[l] = basis_out[l];
+    f.scratch = (char*)workspace + kHeader;
+    f.check = (uint32_t*)workspace;
+    const cudaError_t e = launch_fit_basis(f, (cudaStream_t)stream);
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "fit_basis");
+}
+
 lowram_status lowram_compress_workspace_size(const lowram_compress_shape* shape, size_t* bytes) {
     lowram_status st = check_compress_shape(shape);
     if (st != LOWRAM_OK) return st;

@@ -72,6 +72,7 @@ typedef enum {
 #define LOWRAM_CHECK_POS_RANGE 1u      /* a position was < 0 or >= max_pos (clamped) */
 #define LOWRAM_CHECK_RES_INDEX 2u      /* a residual index was out of range or not strictly ascending */
 #define LOWRAM_CHECK_TIMEOUT 4u        /* a tensor-core pipeline wait gave up (internal error; results invalid) */
+#define LOWRAM_CHECK_NOT_PD 8u         /* lowram_fit_basis: an iterate lost rank (keys of rank < r); results invalid */
 
 /* ---------------------------------------------------------------------------------------------
  * Decode: one layer, all B sequences.
@@ -239,6 +240,38 @@ LOWRAM_API lowram_status lowram_compress(const lowram_compress_shape* shape, con
                               const float* const* b1, const float* const* b2, void* coef_out, void* coef_scale_out,
                               int32_t* const* res_idx_out, void* const* res_val_out, void* const* res_scale_out,
                               float* const* err_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Fitted basis: the group's shared low-rank key basis from the prompt's keys (before compress).
+ * ------------------------------------------------------------------------------------------- */
+/* Workspace bytes lowram_fit_basis needs (a multiple of 256; about 4*B*T*D + 4*D*D bytes, D = G*H_kv*d).
+ * Uses shape fields B, T, G, H_kv, d, r, act_dtype, keys_post_rope and max_pos. */
+LOWRAM_API lowram_status lowram_fit_basis_workspace_size(const lowram_compress_shape* shape, size_t* bytes);
+
+/*
+ * lowram_fit_basis -- the cross-layer SVD of the RoPE-inverted keys ("Asymmetric key compression with
+ * xKV": the G layers' keys are stacked and factored together, RoPE inverted first), producing the
+ * `proj` and `basis` that lowram_compress takes.  With k_cat [N = B*T, D = G*H_kv*d] the tokens'
+ * stacked keys (rotated back by their positions when keys_post_rope), the rank-r subspace of k_cat's
+ * largest singular values is the span of the top-r eigenvectors of k_cat^T k_cat.  They are found by
+ * `iters` steps of subspace iteration from a Gaussian start drawn from `seed`, each orthonormalised
+ * by Cholesky QR (fp64 Cholesky), and a final Cholesky QR; Q [D, r] then has orthonormal columns.
+ * The basis within the subspace is not ordered by singular value (the rebuilt keys do not depend on
+ * it).  Accuracy depends on the spectral gap: the subspace converges like (sigma_{r+1}/sigma_r)^(2 iters).
+ * Arguments:
+ *   keys       [B, T, G, H_kv, d] act_dtype; pos [B, T] int32 or NULL; rope_cos/rope_sin as for
+ *              decode, NULL unless keys_post_rope
+ *   proj_out   [r, D] float32 = Q^T (proj . stacked basis = I to float32 accuracy)
+ *   basis_out  host array of G device pointers, each [H_kv*d, r] act_dtype: layer l's block of Q
+ * Errors: LOWRAM_ERR_INVALID_ARG / _UNSUPPORTED (shape: r a multiple of 32, 32 <= r <= min(1024, D),
+ * D <= 16384, B*T >= r), LOWRAM_ERR_ALIGNMENT, LOWRAM_ERR_WORKSPACE.  Device check word:
+ * LOWRAM_CHECK_NOT_PD if an iterate lost rank (keys of rank below r: the r-th eigenvalue of the Gram
+ * matrix under 1e-5 of the largest), LOWRAM_CHECK_POS_RANGE.
+ */
+LOWRAM_API lowram_status lowram_fit_basis(const lowram_compress_shape* shape, const void* keys, const int32_t* pos,
+                                          const float* rope_cos, const float* rope_sin, int32_t iters, uint64_t seed,
+                                          float* proj_out, void* const* basis_out, void* workspace,
+                                          size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Comparator: the same kernel family on an uncompressed cache.
