@@ -58,6 +58,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dense", action="store_true", help="also time the uncompressed-cache comparator")
+    ap.add_argument("--fit-basis", action="store_true",
+                    help="time lowram_fit_basis (the group's cross-layer key basis) on the workload's group shape")
+    ap.add_argument("--fit-iters", type=int, default=8)
     return ap.parse_args()
 
 
@@ -423,6 +426,10 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     w = workload(args)
     pk, pk_kind = peaks()
+    if args.fit_basis:
+        if rank == 0:
+            fit_bench(w, dev, args, pk)
+        return
     groups, pos, compress_ms = build_cache(w, dev)
     cos, sin = L.lowram_rope_table(w.d, w.theta, w.T_nominal or w.T)
     qs = [synth.draw_query(w, l).to(dev) for l in range(w.L)]
@@ -609,6 +616,51 @@ def main():
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def fit_bench(w, dev, args, pk):
+    """lowram_fit_basis on one layer group of the workload: keys [B, T, G, H_kv, d] of rank r with a decaying
+    spectrum plus noise (seeded, made on the GPU), timed with CUDA events over --steps calls after --warmup."""
+    import decode_attention_19_b300 as L
+    B, T, G, H_kv, d, r = w.B, w.T, w.G, w.H_kv, w.d, w.r
+    D, N = G * H_kv * d, B * T
+    g = torch.Generator(device=dev).manual_seed(11)
+    U, _ = torch.linalg.qr(torch.randn((D, r), generator=g, device=dev))
+    sig = torch.logspace(1.0, 0.0, r, device=dev)
+    keys = torch.randn((N, r), generator=g, device=dev) * sig @ U.T
+    keys = (keys + 0.05 * torch.randn((N, D), generator=g, device=dev)).to(torch.bfloat16).view(B, T, G, H_kv, d)
+    del U
+    ws = None
+    for _ in range(args.warmup):
+        proj, bases, ws = L.lowram_fit_basis(keys, r, iters=args.fit_iters, workspace=ws)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        a.record()
+        proj, bases, ws = L.lowram_fit_basis(keys, r, iters=args.fit_iters, workspace=ws)
+        b.record()
+    torch.cuda.synchronize()
+    if L.lowram_get_error(ws):
+        raise RuntimeError("device check word set by lowram_fit_basis")
+    ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+    # rebuild error of the fitted subspace against the optimal one (the noise floor): a sampled check
+    Kf = keys.view(N, D)[:8192].float()
+    P = proj.float()
+    err = float(torch.linalg.norm(Kf - (Kf @ P.T) @ P) / torch.linalg.norm(Kf))
+    it = args.fit_iters + 1          # iterations plus the final Cholesky QR
+    flops = N * D * D + args.fit_iters * 2.0 * D * D * r + it * (4.0 * D * r * r + 2.0 * r ** 3 / 3.0)
+    peak_tf = NOMINAL_SM * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "fitted key basis: time per layer group", "value": ms, "unit": "ms", "higher_is_better": False,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "T": T, "G": G, "H_kv": H_kv, "d": d, "r": r, "D": D,
+                   "iters": args.fit_iters, "keys": "bf16, rank r (spectrum 10..1) + 0.05 noise"},
+        "rebuild_rel_err_sampled": err,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf,
+                     "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock",
+                     "work": "Gram N*D^2 (symmetric) + per iteration 2*D^2*r + 4*D*r^2 + 2r^3/3"}}))
 
 
 def dense_bench(w, dev, qs, flush, args):

@@ -14,7 +14,7 @@
 //
 // Kernels: a key prep pass (dtype, inverse RoPE), a Gram kernel (64 x 64 output tiles of the upper triangle,
 // mirrored, split over tokens with atomics when the tiles alone do not fill the GPU), a row-major SGEMM, a
-// single-CTA fp64 Cholesky with a triangular inverse, and the output pass.  All CUDA cores: the fit runs once
+// single-CTA fp64 Cholesky, a row-parallel triangular solve, and the output pass.  All CUDA cores: the fit runs once
 // per prompt and the Gram product needs fp32 accumulation of fp32 keys.
 #include "common.cuh"
 #include "kernels.h"
@@ -167,12 +167,11 @@ __global__ void init_normal_kernel(float* Q, int64_t n, uint64_t seed) {
     Q[i] = sqrtf(-2.0f * logf(u1)) * cospif(2.0f * u2);
 }
 
-// One CTA: S [r, r] fp64 (overwritten with its Cholesky factor L, lower) -> Rinv = (L^T)^-1 [r, r] float32, upper
-// triangular, row k holding column k of L^-1.  Linv [r, r] fp64 is scratch.  A pivot at or below 1e-10 of the
-// largest diagonal entry (rounding noise of float32 iterates: the keys have rank below r) sets LOWRAM_CHECK_NOT_PD
-// and stops; Rinv is then left unwritten and the fit's result is void.
-__global__ void __launch_bounds__(1024) chol_rinv_kernel(double* S, int r, double* Linv, float* Rinv,
-                                                         uint32_t* check) {
+// One CTA: S [r, r] fp64 is overwritten with its Cholesky factor (S = L L^T, L lower), which is also written
+// as float32 to Lf [r, r] (lower triangle; the strict upper triangle is not read).  A pivot at or below 1e-10 of
+// the largest diagonal entry (rounding noise of float32 iterates: the keys have rank below r) sets
+// LOWRAM_CHECK_NOT_PD and stops; Lf is then incomplete and the fit's result is void.
+__global__ void __launch_bounds__(1024) chol_kernel(double* S, int r, float* Lf, uint32_t* check) {
     __shared__ int bad;
     __shared__ double floor_pivot;
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -185,6 +184,7 @@ __global__ void __launch_bounds__(1024) chol_rinv_kernel(double* S, int r, doubl
         floor_pivot = 1e-10 * mx;
     }
     __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
     for (int k = 0; k < r; ++k) {
         if (tid == 0) {
             const double p = S[(int64_t)k * r + k];
@@ -196,17 +196,11 @@ __global__ void __launch_bounds__(1024) chol_rinv_kernel(double* S, int r, doubl
         const double lkk = S[(int64_t)k * r + k];
         for (int i = k + 1 + tid; i < r; i += nt) S[(int64_t)i * r + k] /= lkk;
         __syncthreads();
-        // trailing update of the lower triangle: S[i][j] -= L[i][k] L[j][k], k < j <= i
-        const int m = r - k - 1;
-        const int64_t cnt = (int64_t)m * (m + 1) / 2;
-        for (int64_t e = tid; e < cnt; e += nt) {
-            // e -> (ii, jj) with 0 <= jj <= ii < m, row-major over the lower triangle
-            int ii = (int)((sqrt(8.0 * (double)e + 1.0) - 1.0) * 0.5);
-            while ((int64_t)ii * (ii + 1) / 2 > e) --ii;
-            while ((int64_t)(ii + 1) * (ii + 2) / 2 <= e) ++ii;
-            const int jj = (int)(e - (int64_t)ii * (ii + 1) / 2);
-            const int i = k + 1 + ii, j = k + 1 + jj;
-            S[(int64_t)i * r + j] -= S[(int64_t)i * r + k] * S[(int64_t)j * r + k];
+        // trailing update of the lower triangle: S[i][j] -= L[i][k] L[j][k], k < j <= i; a warp per row i, its
+        // lanes along j
+        for (int i = k + 1 + warp; i < r; i += nwarps) {
+            const double lik = S[(int64_t)i * r + k];
+            for (int j = k + 1 + lane; j <= i; j += 32) S[(int64_t)i * r + j] -= lik * S[(int64_t)j * r + k];
         }
         __syncthreads();
     }
@@ -214,15 +208,35 @@ __global__ void __launch_bounds__(1024) chol_rinv_kernel(double* S, int r, doubl
         if (tid == 0) flag(check, LOWRAM_CHECK_NOT_PD);
         return;
     }
-    // column c of L^-1 by forward substitution (one thread per column), then Rinv[c][i] = Linv[i][c]
-    for (int c = tid; c < r; c += nt) {
-        for (int i = c; i < r; ++i) {
-            double acc = (i == c) ? 1.0 : 0.0;
-            for (int k = c; k < i; ++k) acc -= S[(int64_t)i * r + k] * Linv[(int64_t)k * r + c];
-            Linv[(int64_t)i * r + c] = acc / S[(int64_t)i * r + i];
-        }
-        for (int i = 0; i < r; ++i) Rinv[(int64_t)c * r + i] = i < c ? 0.0f : (float)Linv[(int64_t)i * r + c];
+    for (int64_t e = tid; e < (int64_t)r * r; e += nt) {
+        const int i = (int)(e / r), j = (int)(e - (int64_t)i * r);
+        Lf[e] = j <= i ? (float)S[e] : 0.0f;
     }
+}
+
+// Q = Z R^-1 with R = L^T: each row q of Q solves q L^T = z, i.e. q_j = (z_j - sum_{k<j} q_k L[j][k]) / L[j][j]
+// (forward substitution; L's row j is contiguous).  A warp per row; the row's solution so far in shared memory.
+constexpr int kTrsmWarps = 8;
+__global__ void __launch_bounds__(kTrsmWarps * 32) trsm_rows_kernel(const float* __restrict__ Z,
+                                                                    const float* __restrict__ Lf, int D, int r,
+                                                                    float* __restrict__ Q) {
+    extern __shared__ float xs[];   // [kTrsmWarps][r]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kTrsmWarps + warp;
+    if (row >= D) return;
+    float* x = xs + warp * r;
+    const float* z = Z + (int64_t)row * r;
+    for (int j = 0; j < r; ++j) {
+        const float* lj = Lf + (int64_t)j * r;
+        float acc = 0.0f;
+        for (int k = lane; k < j; k += 32) acc = fmaf(x[k], lj[k], acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        const float v = (z[j] - acc) / lj[j];
+        if (lane == 0) x[j] = v;
+        __syncwarp();
+    }
+    for (int j = lane; j < r; j += 32) Q[(int64_t)row * r + j] = x[j];
 }
 
 // The G output bases, passed by value.
@@ -270,7 +284,7 @@ cudaError_t sgemm(const float* A, const float* B, int M, int K, int Nc, float* C
 size_t fit_workspace_bytes(int64_t N, int D, int r) {
     auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
     return a(sizeof(float) * (size_t)N * D) + a(sizeof(float) * (size_t)D * D) + 2 * a(sizeof(float) * (size_t)D * r) +
-           2 * a(sizeof(double) * (size_t)r * r) + a(sizeof(float) * (size_t)r * r);
+           a(sizeof(double) * (size_t)r * r) + a(sizeof(float) * (size_t)r * r);
 }
 
 cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st) {
@@ -288,9 +302,7 @@ cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st) {
     w += a(sizeof(float) * (size_t)D * r);
     double* S = (double*)w;
     w += a(sizeof(double) * (size_t)r * r);
-    double* Linv = (double*)w;
-    w += a(sizeof(double) * (size_t)r * r);
-    float* Rinv = (float*)w;
+    float* Lf = (float*)w;
 
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -309,13 +321,18 @@ cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st) {
     if ((e = gram<float>(X, N, D, Gm, sms, st)) != cudaSuccess) return e;
     init_normal_kernel<<<(unsigned)cdiv((int64_t)D * r, 256), 256, 0, st>>>(Q, (int64_t)D * r, f.seed);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // Cholesky QR of Z into Q: Z^T Z = R^T R (fp64), Q = Z R^-1
+    // Cholesky QR of Z into Q: Z^T Z = L L^T (fp64), Q = Z L^-T by row-wise forward substitution
+    const size_t trsm_smem = sizeof(float) * (size_t)kTrsmWarps * r;
+    if ((e = cudaFuncSetAttribute(trsm_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)trsm_smem)) !=
+        cudaSuccess)
+        return e;
     auto chol_qr = [&](const float* Zin, float* Qout) -> cudaError_t {
         cudaError_t e2 = gram<double>(Zin, D, r, S, sms, st);
         if (e2 != cudaSuccess) return e2;
-        chol_rinv_kernel<<<1, 1024, 0, st>>>(S, r, Linv, Rinv, f.check);
+        chol_kernel<<<1, 1024, 0, st>>>(S, r, Lf, f.check);
         if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
-        return sgemm(Zin, Rinv, D, r, r, Qout, st);
+        trsm_rows_kernel<<<(unsigned)cdiv(D, kTrsmWarps), kTrsmWarps * 32, trsm_smem, st>>>(Zin, Lf, D, r, Qout);
+        return cudaGetLastError();
     };
     for (int it = 0; it < f.iters; ++it) {
         if ((e = sgemm(Gm, Q, D, D, r, Z, st)) != cudaSuccess) return e;
