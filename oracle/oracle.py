@@ -31,7 +31,7 @@ __all__ = [
     "build", "lib", "Dims", "f64", "round_bf16", "round_f16", "round_f32", "quant_int4_g32",
     "dequant_int4_g32", "quant_int8_vec", "dequant_int8_vec", "rope", "rope_rows", "rope_angles", "mlp",
     "rebuild_keys", "predict_values", "decode", "project", "residuals", "compress_group",
-    "dense_decode", "merge_attn", "fit_basis", "top_n", "n_res_for", "max_threads", "store",
+    "dense_decode", "merge_attn", "fit_basis", "predictor_loss_grad", "adam_step", "fit_predictor", "top_n", "n_res_for", "max_threads", "store",
 ]
 
 
@@ -440,3 +440,59 @@ def fit_basis(k_cat, r: int, G: int, H_kv: int, d: int, *, pos=None, keys_post_r
     order = np.argsort(w)[::-1][:r]
     U = U[:, order]
     return U.T.copy(), [U[l * H_kv * d:(l + 1) * H_kv * d].copy() for l in range(G)], w[order]
+
+
+def predictor_loss_grad(k_pre, v, w1, b1, w2, b2):
+    """Mean squared error of one kv-head's predictor over its tokens, and the gradient of that loss with respect
+    to the predictor's parameters [ABS: the predictor is fitted at test time on the prompt; EX "Value cache
+    amortisation in plain language": values are predicted from the pre-RoPE keys].  k_pre, v [N, d];
+    w1 [m, d], b1 [m], w2 [d, m], b2 [d];  loss = 1/(N d) sum_t || w2 silu(w1 k_t + b1) + b2 - v_t ||^2.
+    Plain fp64 numpy, the chain rule written out: silu'(z) = s + z s (1 - s) with s the logistic function.
+    Returns (loss, g_w1, g_b1, g_w2, g_b2)."""
+    K, V, W1, B1, W2, B2 = (f64(x) for x in (k_pre, v, w1, b1, w2, b2))
+    N, d = K.shape
+    Z = K @ W1.T + B1
+    S = 1.0 / (1.0 + np.exp(-Z))
+    H = Z * S
+    E = H @ W2.T + B2 - V
+    loss = float(np.sum(E * E) / (N * d))
+    dV = 2.0 * E / (N * d)
+    g_w2 = dV.T @ H
+    g_b2 = dV.sum(axis=0)
+    dZ = (dV @ W2) * (S + Z * S * (1.0 - S))
+    g_w1 = dZ.T @ K
+    g_b1 = dZ.sum(axis=0)
+    return loss, g_w1, g_b1, g_w2, g_b2
+
+
+def adam_step(p, g, m, v, step: int, lr: float, beta1: float, beta2: float, eps: float):
+    """One Adam update (Kingma and Ba, with bias correction) of parameters p with gradient g; `step` counts from 1.
+    Returns the new (p, m, v)."""
+    m = beta1 * m + (1.0 - beta1) * g
+    v = beta2 * v + (1.0 - beta2) * g * g
+    mh = m / (1.0 - beta1 ** step)
+    vh = v / (1.0 - beta2 ** step)
+    return p - lr * mh / (np.sqrt(vh) + eps), m, v
+
+
+def fit_predictor(k_pre, v, w1, b1, w2, b2, *, steps: int, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+                  eps: float = 1e-8):
+    """Test-time fit of every kv-head's predictor on the prompt's (pre-RoPE key, value) pairs: `steps` full-batch
+    Adam steps on predictor_loss_grad from the given start.  k_pre, v [B, T, H_kv, d]; w1 [H_kv, m, d],
+    b1 [H_kv, m], w2 [H_kv, d, m], b2 [H_kv, d].  Returns (w1, b1, w2, b2, losses [steps, H_kv]) where losses[s]
+    is the loss before step s+1."""
+    K, V = f64(k_pre), f64(v)
+    B, T, H_kv, d = K.shape
+    P = [f64(x).copy() for x in (w1, b1, w2, b2)]
+    M = [np.zeros_like(x) for x in P]
+    Vv = [np.zeros_like(x) for x in P]
+    losses = np.zeros((steps, H_kv))
+    for s in range(steps):
+        for h in range(H_kv):
+            Kh = K[:, :, h].reshape(B * T, d)
+            Vh = V[:, :, h].reshape(B * T, d)
+            loss, *g = predictor_loss_grad(Kh, Vh, P[0][h], P[1][h], P[2][h], P[3][h])
+            losses[s, h] = loss
+            for i in range(4):
+                P[i][h], M[i][h], Vv[i][h] = adam_step(P[i][h], g[i], M[i][h], Vv[i][h], s + 1, lr, beta1, beta2, eps)
+    return P[0], P[1], P[2], P[3], losses

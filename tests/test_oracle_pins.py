@@ -506,6 +506,65 @@ def test_fit_basis_inverts_rope_of_rotated_keys():
     np.testing.assert_allclose(p2.T @ p2, p1.T @ p1, atol=1e-9)
 
 
+# ------------------------------------------------------------------------------------------------
+# test-time fit of the predictor: loss gradient and Adam
+# ------------------------------------------------------------------------------------------------
+def predictor_params(d, m, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.normal(0, d ** -0.5, (m, d)), rng.normal(0, 0.1, m), rng.normal(0, m ** -0.5, (d, m)),
+            rng.normal(0, 0.1, d))
+
+
+def test_predictor_loss_is_the_mse_of_the_oracle_mlp():
+    N, d, m = 7, 4, 6
+    rng = np.random.default_rng(8)
+    K, V = rng.normal(0, 1, (N, d)), rng.normal(0, 1, (N, d))
+    w1, b1, w2, b2 = predictor_params(d, m, 9)
+    loss = O.predictor_loss_grad(K, V, w1, b1, w2, b2)[0]
+    want = np.mean([(O.mlp(K[t], w1, b1, w2, b2) - V[t]) ** 2 for t in range(N)])
+    assert abs(loss - want) <= 1e-14
+
+
+def test_predictor_gradient_matches_central_differences():
+    N, d, m = 9, 5, 4
+    rng = np.random.default_rng(10)
+    K, V = rng.normal(0, 1, (N, d)), rng.normal(0, 1, (N, d))
+    params = list(predictor_params(d, m, 11))
+    _, *grads = O.predictor_loss_grad(K, V, *params)
+    h = 1e-6
+    for i, (p, g) in enumerate(zip(params, grads)):
+        num = np.zeros_like(p)
+        for idx in np.ndindex(p.shape):
+            plus = [x.copy() for x in params]
+            minus = [x.copy() for x in params]
+            plus[i][idx] += h
+            minus[i][idx] -= h
+            num[idx] = (O.predictor_loss_grad(K, V, *plus)[0] - O.predictor_loss_grad(K, V, *minus)[0]) / (2 * h)
+        np.testing.assert_allclose(g, num, atol=1e-8, rtol=1e-6)
+
+
+def test_adam_first_steps_closed_form():
+    """Adam's first step moves each parameter by lr * sign(g) (up to eps); a constant gradient keeps that step."""
+    p, g = np.array([1.0, -2.0, 0.5]), np.array([0.3, -4.0, 1e-3])
+    p1, m, v = O.adam_step(p, g, 0.0, 0.0, 1, 0.01, 0.9, 0.999, 1e-12)
+    np.testing.assert_allclose(p1, p - 0.01 * np.sign(g), atol=1e-10)
+    p2, _, _ = O.adam_step(p1, g, m, v, 2, 0.01, 0.9, 0.999, 1e-12)
+    np.testing.assert_allclose(p2, p1 - 0.01 * np.sign(g), atol=1e-10)
+
+
+def test_fit_predictor_recovers_a_planted_predictor():
+    """Values generated by a predictor of the same shape: the fit's loss falls by orders of magnitude."""
+    B, T, H_kv, d, m = 1, 200, 2, 4, 8
+    rng = np.random.default_rng(12)
+    K = rng.normal(0, 1, (B, T, H_kv, d))
+    true = [predictor_params(d, m, 20 + h) for h in range(H_kv)]
+    V = np.stack([np.stack([O.mlp(K[0, t, h], *true[h]) for t in range(T)]) for h in range(H_kv)], axis=1)[None]
+    start = [np.stack(x) for x in zip(*[predictor_params(d, m, 40 + h) for h in range(H_kv)])]
+    *_, losses = O.fit_predictor(K, V, *start, steps=400, lr=0.02)
+    assert np.all(losses[-1] < 1e-2 * losses[0])
+    assert np.all(np.diff(losses[:50], axis=0) < 0)     # early steps descend
+
+
 def test_residual_budgets_of_the_workloads():
     # ceil(rho * T): 0.25*256, 0.1*8192, 0.1*32768, 0.1*4096, 0.05*16384
     assert [O.n_res_for(r, T) for r, T in [(0.25, 256), (0.1, 8192), (0.1, 32768), (0.1, 4096), (0.05, 16384)]] \
