@@ -60,6 +60,9 @@ def _load():
             "lowram_compress": [ctypes.POINTER(lowram_compress_shape)] + [_vp] * 18 + [sz, _vp],
             "lowram_dense_workspace_size": [i32, i32, i32, i32, i32, psz],
             "lowram_dense_decode_attn": [i32, i32, i32, i32, i32, i32, flt, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp],
+            "lowram_predictor_grad": [i32] * 6 + [_vp] * 11 + [_vp],
+            "lowram_fit_predictor_workspace_size": [i32, i32, i32, psz],
+            "lowram_fit_predictor": [i32] * 6 + [_vp, _vp, i32, flt, flt, flt, flt] + [_vp] * 6 + [sz, _vp],
             "lowram_fit_basis_workspace_size": [ctypes.POINTER(lowram_compress_shape), psz],
             "lowram_fit_basis": [ctypes.POINTER(lowram_compress_shape), _vp, _vp, _vp, _vp, i32, ctypes.c_uint64, _vp,
                                  _vp, _vp, sz, _vp],
@@ -318,6 +321,56 @@ def lowram_dense_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     _check(_load().lowram_dense_decode_attn(B, T, H_q, H_kv, d, _act(q), float(sm_scale), _p(q), _p(k), _p(v),
                                             _p(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream()))
     return out, lse
+
+
+# ------------------------------------------------------------------------------------------------
+# test-time fit of the value predictor (float32 master parameters, updated in place)
+# ------------------------------------------------------------------------------------------------
+def _pred_dims(keys, values, w1, w2):
+    B, T, H_kv, d = keys.shape
+    m = w1.shape[1]
+    _dev(keys, values)
+    if values.shape != keys.shape or values.dtype != keys.dtype:
+        raise ValueError("keys and values must share shape [B, T, H_kv, d] and dtype")
+    if w1.shape != (H_kv, m, d) or w2.shape != (H_kv, d, m):
+        raise ValueError("w1 [H_kv, m, d] and w2 [H_kv, d, m] expected")
+    return B, T, H_kv, d, m
+
+
+def lowram_predictor_grad(keys: torch.Tensor, values: torch.Tensor, w1: torch.Tensor, b1: torch.Tensor,
+                          w2: torch.Tensor, b2: torch.Tensor):
+    """Loss [H_kv] and gradient (g_w1, g_b1, g_w2, g_b2) of every head's predictor; parameters float32."""
+    B, T, H_kv, d, m = _pred_dims(keys, values, w1, w2)
+    for t in (w1, b1, w2, b2):
+        _dev(t)
+        if t.dtype != torch.float32:
+            raise TypeError("predictor parameters are float32")
+    loss = torch.empty(H_kv, dtype=torch.float32, device=keys.device)
+    g = [torch.empty_like(t) for t in (w1, b1, w2, b2)]
+    _check(_load().lowram_predictor_grad(B, T, H_kv, d, m, _act(keys), _p(keys), _p(values), _p(w1), _p(b1), _p(w2),
+                                         _p(b2), _p(loss), *[_p(x) for x in g], _stream()))
+    return (loss, *g)
+
+
+def lowram_fit_predictor(keys: torch.Tensor, values: torch.Tensor, w1: torch.Tensor, b1: torch.Tensor,
+                         w2: torch.Tensor, b2: torch.Tensor, *, steps: int, lr: float, beta1: float = 0.9,
+                         beta2: float = 0.999, eps: float = 1e-8, want_losses: bool = True,
+                         workspace: Optional[torch.Tensor] = None):
+    """`steps` full-batch Adam steps on every head's predictor, parameters (float32) updated in place.
+    Returns the losses [steps, H_kv] before each step (or None)."""
+    B, T, H_kv, d, m = _pred_dims(keys, values, w1, w2)
+    for t in (w1, b1, w2, b2):
+        _dev(t)
+        if t.dtype != torch.float32:
+            raise TypeError("predictor parameters are float32")
+    n = ctypes.c_size_t(0)
+    _check(_load().lowram_fit_predictor_workspace_size(H_kv, d, m, ctypes.byref(n)))
+    ws = _workspace(n.value, workspace, keys.device)
+    losses = torch.empty((int(steps), H_kv), dtype=torch.float32, device=keys.device) if want_losses else None
+    _check(_load().lowram_fit_predictor(B, T, H_kv, d, m, _act(keys), _p(keys), _p(values), int(steps), float(lr),
+                                        float(beta1), float(beta2), float(eps), _p(w1), _p(b1), _p(w2), _p(b2),
+                                        _p(losses), _p(ws), ws.numel() * ws.element_size(), _stream()))
+    return losses
 
 
 # ------------------------------------------------------------------------------------------------

@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "predict_fit.h"
 
 using namespace lowram;
 
@@ -290,6 +291,94 @@ static lowram_status check_compress_shape(const lowram_compress_shape* s) {
         return fail(LOWRAM_ERR_INVALID_ARG, "res_dtype=%d", s->res_dtype);
     if (s->keys_post_rope && s->T > 0 && s->max_pos < 1) return fail(LOWRAM_ERR_INVALID_ARG, "max_pos=%d", s->max_pos);
     return LOWRAM_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+// test-time fit of the value predictor
+// ------------------------------------------------------------------------------------------------
+static lowram_status check_predictor_shape(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m, int32_t dtype) {
+    if (B < 0 || T < 0 || H_kv < 1) return fail(LOWRAM_ERR_INVALID_ARG, "B=%d T=%d H_kv=%d", B, T, H_kv);
+    if (d != 64 && d != 128) return fail(LOWRAM_ERR_UNSUPPORTED, "d=%d (64 or 128 supported)", d);
+    if (m < 32 || m % 32 != 0 || m > 256) return fail(LOWRAM_ERR_UNSUPPORTED, "m=%d", m);
+    if (!is_act(dtype)) return fail(LOWRAM_ERR_INVALID_ARG, "dtype=%d", dtype);
+    return LOWRAM_OK;
+}
+
+static size_t predictor_params(int32_t H_kv, int32_t d, int32_t m) {
+    return (size_t)H_kv * ((size_t)2 * m * d + m + d);
+}
+
+lowram_status lowram_predictor_grad(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m, int32_t dtype,
+                                    const void* keys, const void* values, const float* w1, const float* b1,
+                                    const float* w2, const float* b2, float* loss_out, float* g_w1, float* g_b1,
+                                    float* g_w2, float* g_b2, void* stream) {
+    lowram_status st = check_predictor_shape(B, T, H_kv, d, m, dtype);
+    if (st != LOWRAM_OK) return st;
+    const void* need[] = {w1, b1, w2, b2, loss_out, g_w1, g_b1, g_w2, g_b2};
+    for (const void* p : need)
+        if (!p) return fail(LOWRAM_ERR_INVALID_ARG, "a required pointer is NULL");
+    if ((int64_t)B * T > 0 && (!keys || !values)) return fail(LOWRAM_ERR_INVALID_ARG, "keys or values is NULL");
+    const void* ptrs[] = {keys, values, w1, b1, w2, b2, loss_out, g_w1, g_b1, g_w2, g_b2};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
+    PredictorFitArgs a{B, T, H_kv, d, m, dtype == LOWRAM_BF16, keys, values, w1, b1, w2, b2, loss_out,
+                       g_w1, g_b1, g_w2, g_b2};
+    const cudaError_t e = launch_predictor_grad(a, (cudaStream_t)stream);
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "predictor_grad");
+}
+
+lowram_status lowram_fit_predictor_workspace_size(int32_t H_kv, int32_t d, int32_t m, size_t* bytes) {
+    lowram_status st = check_predictor_shape(0, 0, H_kv, d, m, LOWRAM_F32);
+    if (st != LOWRAM_OK) return st;
+    if (!bytes) return fail(LOWRAM_ERR_INVALID_ARG, "bytes is NULL");
+    // gradient, first and second moments of every parameter, and a loss row
+    *bytes = kHeader + 3 * align256(sizeof(float) * predictor_params(H_kv, d, m)) + align256(sizeof(float) * H_kv);
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m, int32_t dtype,
+                                   const void* keys, const void* values, int32_t steps, float lr, float beta1,
+                                   float beta2, float eps, float* w1, float* b1, float* w2, float* b2,
+                                   float* losses_out, void* workspace, size_t workspace_bytes, void* stream) {
+    lowram_status st = check_predictor_shape(B, T, H_kv, d, m, dtype);
+    if (st != LOWRAM_OK) return st;
+    size_t need = 0;
+    lowram_fit_predictor_workspace_size(H_kv, d, m, &need);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return fail(LOWRAM_ERR_WORKSPACE, "workspace %zu bytes, %zu needed", workspace ? workspace_bytes : 0, need);
+    if (steps < 0) return fail(LOWRAM_ERR_INVALID_ARG, "steps=%d", steps);
+    if (!(lr > 0.0f) || !(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f) || !(eps > 0.0f))
+        return fail(LOWRAM_ERR_INVALID_ARG, "Adam hyper-parameters lr=%g beta1=%g beta2=%g eps=%g", lr, beta1, beta2, eps);
+    if (!w1 || !b1 || !w2 || !b2) return fail(LOWRAM_ERR_INVALID_ARG, "a parameter pointer is NULL");
+    if ((int64_t)B * T > 0 && (!keys || !values)) return fail(LOWRAM_ERR_INVALID_ARG, "keys or values is NULL");
+    const void* ptrs[] = {keys, values, w1, b1, w2, b2, losses_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
+    const cudaStream_t cs = (cudaStream_t)stream;
+    const size_t np = predictor_params(H_kv, d, m), seg = align256(sizeof(float) * np);
+    char* ws = (char*)workspace + kHeader;
+    float* grad = (float*)ws;
+    float* mom = (float*)(ws + seg);
+    float* vel = (float*)(ws + 2 * seg);
+    float* loss_tmp = (float*)(ws + 3 * seg);
+    // the four parameter tensors and their slices of the gradient / moment buffers
+    const size_t n1 = (size_t)H_kv * m * d, nb1 = (size_t)H_kv * m, nb2 = (size_t)H_kv * d;
+    float* params[4] = {w1, b1, w2, b2};
+    const size_t count[4] = {n1, nb1, n1, nb2};
+    size_t off[4];
+    off[0] = 0;
+    for (int i = 1; i < 4; ++i) off[i] = off[i - 1] + count[i - 1];
+    cudaError_t e = cudaMemsetAsync(mom, 0, 2 * seg, cs);
+    for (int s_ = 0; s_ < steps && e == cudaSuccess; ++s_) {
+        PredictorFitArgs a{B, T, H_kv, d, m, dtype == LOWRAM_BF16, keys, values, w1, b1, w2, b2,
+                           losses_out ? losses_out + (size_t)s_ * H_kv : loss_tmp, grad + off[0], grad + off[1],
+                           grad + off[2], grad + off[3]};
+        e = launch_predictor_grad(a, cs);
+        for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+            e = launch_adam(params[i], grad + off[i], mom + off[i], vel + off[i], (int64_t)count[i], lr, beta1, beta2,
+                            eps, s_ + 1, cs);
+    }
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "fit_predictor");
 }
 
 // ------------------------------------------------------------------------------------------------

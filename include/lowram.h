@@ -242,6 +242,39 @@ LOWRAM_API lowram_status lowram_compress(const lowram_compress_shape* shape, con
                               float* const* err_out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Test-time fit of the value predictor (LowRAM abstract: the predictor is fitted at test time;
+ * "Value cache amortisation in plain language": values are predicted from pre-RoPE keys).  Per
+ * kv-head h the predictor v_hat = w2 silu(w1 k + b1) + b2 is fitted to the prompt's (pre-RoPE key,
+ * value) pairs by full-batch Adam on loss_h = 1/(N d) sum_t || v_hat(k_t) - v_t ||^2, N = B*T.
+ * Parameters are float32 master copies: w1 [H_kv, m, d], b1 [H_kv, m], w2 [H_kv, d, m],
+ * b2 [H_kv, d] (decode takes w1, w2 in the activation dtype: round them after the fit).
+ * keys, values [B, T, H_kv, d] in dtype (LOWRAM_F32 or LOWRAM_BF16); d is 64 or 128, m a multiple
+ * of 32 up to 256.  CUDA cores, float32.
+ * ------------------------------------------------------------------------------------------- */
+
+/* Loss [H_kv] and gradient of every head's predictor at the given parameters (outputs shaped like the
+ * parameters; overwritten). */
+LOWRAM_API lowram_status lowram_predictor_grad(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m, int32_t dtype,
+                                               const void* keys, const void* values, const float* w1, const float* b1,
+                                               const float* w2, const float* b2, float* loss_out, float* g_w1,
+                                               float* g_b1, float* g_w2, float* g_b2, void* stream);
+
+/* Workspace bytes lowram_fit_predictor needs (the gradient and Adam's two moments of every parameter). */
+LOWRAM_API lowram_status lowram_fit_predictor_workspace_size(int32_t H_kv, int32_t d, int32_t m, size_t* bytes);
+
+/*
+ * lowram_fit_predictor -- `steps` Adam steps (Kingma and Ba, bias-corrected; moments start at zero)
+ * from the parameters given, updated in place.  losses_out [steps, H_kv] float32 (the loss before each
+ * step) or NULL.  Errors: LOWRAM_ERR_INVALID_ARG (shape, steps < 0, lr <= 0, beta outside [0, 1),
+ * eps <= 0, NULL pointers), LOWRAM_ERR_UNSUPPORTED (d, m), LOWRAM_ERR_ALIGNMENT, LOWRAM_ERR_WORKSPACE.
+ */
+LOWRAM_API lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m, int32_t dtype,
+                                              const void* keys, const void* values, int32_t steps, float lr,
+                                              float beta1, float beta2, float eps, float* w1, float* b1, float* w2,
+                                              float* b2, float* losses_out, void* workspace, size_t workspace_bytes,
+                                              void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Fitted basis: the group's shared low-rank key basis from the prompt's keys (before compress).
  * ------------------------------------------------------------------------------------------- */
 /* Workspace bytes lowram_fit_basis needs (a multiple of 256; about 4*B*T*D + 4*D*D bytes, D = G*H_kv*d).

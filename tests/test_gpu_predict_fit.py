@@ -1,0 +1,81 @@
+"""GPU parity of the test-time fit of the value predictor against the fp64 oracle.
+
+The gradient at a given point is compared element by element (float32 accumulation over the tokens).  Adam
+steps are compared along the trajectory: the losses before each step, and the parameters, which may differ by
+at most lr per step in elements whose gradient sign the float32 and fp64 sums decide differently (Adam moves
+each element by about lr times the sign of its gradient early on).  Shapes: both head dims, hidden widths below,
+at and above 128 (two hidden halves), float32 and bf16 inputs, a ragged last token tile.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def problem(B, T, H_kv, d, m, dtype, seed):
+    rng = np.random.default_rng(seed)
+    K = rng.normal(0, 1, (B, T, H_kv, d))
+    V = 0.5 * np.tanh(K[..., ::-1]) + 0.1 * rng.normal(0, 1, (B, T, H_kv, d))      # a learnable map plus noise
+    w1 = rng.normal(0, d ** -0.5, (H_kv, m, d))
+    b1 = rng.normal(0, 0.1, (H_kv, m))
+    w2 = rng.normal(0, m ** -0.5, (H_kv, d, m))
+    b2 = rng.normal(0, 0.1, (H_kv, d))
+    keys = torch.as_tensor(K, dtype=torch.float32).to(dtype)
+    values = torch.as_tensor(V, dtype=torch.float32).to(dtype)
+    params = [torch.as_tensor(x, dtype=torch.float32) for x in (w1, b1, w2, b2)]
+    return keys, values, params
+
+
+@pytest.mark.parametrize("d,m", [(128, 128), (64, 96), (128, 256), (64, 32)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_predictor_gradient_matches_oracle(d, m, dtype):
+    import decode_attention_19_b300 as L
+    B, T, H_kv = 2, 157, 2
+    keys, values, params = problem(B, T, H_kv, d, m, dtype, 1)
+    loss, *grads = L.lowram_predictor_grad(keys.cuda(), values.cuda(), *[p.cuda() for p in params])
+    torch.cuda.synchronize()
+    K, V = O.f64(keys), O.f64(values)
+    for h in range(H_kv):
+        ref = O.predictor_loss_grad(K[:, :, h].reshape(-1, d), V[:, :, h].reshape(-1, d),
+                                    *[O.f64(p)[h] for p in params])
+        assert abs(float(loss[h]) - ref[0]) <= 1e-5 * ref[0]
+        for g, r in zip(grads, ref[1:]):
+            got = O.f64(g.cpu())[h]
+            assert np.linalg.norm(got - r) <= 1e-4 * np.linalg.norm(r) + 1e-9
+            np.testing.assert_allclose(got, r, atol=1e-4 * np.abs(r).max() + 1e-9, rtol=0)
+
+
+@pytest.mark.parametrize("d,m,dtype", [(128, 128, torch.bfloat16), (64, 256, torch.float32)])
+def test_fit_predictor_follows_the_oracle_trajectory(d, m, dtype):
+    import decode_attention_19_b300 as L
+    B, T, H_kv, steps, lr = 1, 300, 2, 6, 1e-3
+    keys, values, params = problem(B, T, H_kv, d, m, dtype, 2)
+    dev = [p.clone().cuda() for p in params]
+    losses = L.lowram_fit_predictor(keys.cuda(), values.cuda(), *dev, steps=steps, lr=lr)
+    torch.cuda.synchronize()
+    *ref, ref_losses = O.fit_predictor(keys, values, *params, steps=steps, lr=lr)
+    np.testing.assert_allclose(O.f64(losses.cpu()), ref_losses, rtol=1e-4, atol=0)
+    for got, want in zip(dev, ref):
+        diff = np.abs(O.f64(got.cpu()) - want)
+        assert diff.max() <= 2 * lr * steps
+        assert diff.mean() <= 0.05 * lr * steps            # flips are rare
+
+
+def test_fit_predictor_reduces_the_loss():
+    import decode_attention_19_b300 as L
+    keys, values, params = problem(2, 400, 1, 64, 64, torch.float32, 3)
+    dev = [p.clone().cuda() for p in params]
+    losses = L.lowram_fit_predictor(keys.cuda(), values.cuda(), *dev, steps=300, lr=3e-3)
+    torch.cuda.synchronize()
+    ls = O.f64(losses.cpu())[:, 0]
+    assert ls[-1] < 0.5 * ls[0]
+    assert np.all(np.isfinite(ls))
