@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--fit-basis", action="store_true",
                     help="time lowram_fit_basis (the group's cross-layer key basis) on the workload's group shape")
     ap.add_argument("--fit-iters", type=int, default=8)
+    ap.add_argument("--fit-predictor", action="store_true",
+                    help="time one Adam step of lowram_fit_predictor on the workload's layer shape")
     return ap.parse_args()
 
 
@@ -430,6 +432,10 @@ def main():
         if rank == 0:
             fit_bench(w, dev, args, pk)
         return
+    if args.fit_predictor:
+        if rank == 0:
+            fit_predictor_bench(w, dev, args, pk)
+        return
     groups, pos, compress_ms = build_cache(w, dev)
     cos, sin = L.lowram_rope_table(w.d, w.theta, w.T_nominal or w.T)
     qs = [synth.draw_query(w, l).to(dev) for l in range(w.L)]
@@ -661,6 +667,40 @@ def fit_bench(w, dev, args, pk):
                      "frac": achieved / peak_tf,
                      "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock",
                      "work": "Gram N*D^2 (symmetric) + per iteration 2*D^2*r + 4*D*r^2 + 2r^3/3"}}))
+
+
+def fit_predictor_bench(w, dev, args, pk):
+    """lowram_fit_predictor on one layer of the workload (all kv-heads, B*T prompt tokens): the time of one full-batch
+    Adam step (gradient of every head's predictor + the update), from --steps steps after --warmup."""
+    import decode_attention_19_b300 as L
+    B, T, H_kv, d, m = w.B, w.T, w.H_kv, w.d, w.m
+    g = torch.Generator(device=dev).manual_seed(12)
+    keys = torch.randn((B, T, H_kv, d), generator=g, device=dev).to(torch.bfloat16)
+    values = (0.5 * torch.tanh(keys.float().flip(-1)) + 0.1 * torch.randn((B, T, H_kv, d), generator=g, device=dev))
+    values = values.to(torch.bfloat16)
+    params = [torch.randn(s, generator=g, device=dev) * sc for s, sc in
+              (((H_kv, m, d), d ** -0.5), ((H_kv, m), 0.1), ((H_kv, d, m), m ** -0.5), ((H_kv, d), 0.1))]
+    L.lowram_fit_predictor(keys, values, *params, steps=max(1, args.warmup), lr=1e-3)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    losses = L.lowram_fit_predictor(keys, values, *params, steps=args.steps, lr=1e-3)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    flops = 10.0 * B * T * d * m * H_kv            # forward (2 products), backward (3 products), 2 FLOP per MAC
+    peak_tf = NOMINAL_SM * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
+    ls = losses.float().cpu().numpy()
+    print(json.dumps({
+        "metric": "predictor fit: time per Adam step per layer", "value": ms, "unit": "ms", "higher_is_better": False,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "T": T, "H_kv": H_kv, "d": d, "m": m, "inputs": "bf16 keys/values"},
+        "loss_first_last": [float(ls[0].mean()), float(ls[-1].mean())],
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf,
+                     "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock",
+                     "work": "10 * B*T * d * m * H_kv per step"}}))
 
 
 def dense_bench(w, dev, qs, flush, args):
