@@ -97,3 +97,50 @@ def test_rope_table_rejects_bad_arguments():
     assert lib.lowram_rope_table(7, 1e4, 10, None, None, None) == 1
     assert lib.lowram_rope_table(8, -1.0, 10, None, None, None) == 1
     assert lib.lowram_rope_table(8, 1e4, 0, None, None, None) == 0
+
+
+def test_tail_merge_and_fit_entry_points_check_arguments_on_the_host():
+    """Host-side argument checks of the exact tail, the merge, the fitted basis and the predictor fit: each
+    rejects a bad argument with its status before any device work (no GPU needed)."""
+    import ctypes
+    lib = L.lib()
+    INVALID, UNSUPPORTED, WORKSPACE = 1, 3, 4
+    # tail append: row outside the capacity, bad head dim, bad dtype
+    assert lib.lowram_tail_append(2, 8, 2, 128, 1, 8, None, None, None, None, None) == INVALID
+    assert lib.lowram_tail_append(2, 8, 2, 96, 1, 0, None, None, None, None, None) == INVALID
+    assert lib.lowram_tail_append(2, 8, 2, 128, 7, 0, None, None, None, None, None) == INVALID
+    assert lib.lowram_tail_append(0, 8, 2, 128, 1, 0, None, None, None, None, None) == 0     # nothing to do
+    # tail attention: length past the capacity
+    assert lib.lowram_tail_decode_attn(2, 8, 9, 8, 2, 128, 1, 0.0, None, None, None, None, None, None, 0,
+                                       None) == INVALID
+    # merge: missing operands
+    assert lib.lowram_merge_attn(2, 8, 128, None, None, None, None, None, None, None) == INVALID
+    assert lib.lowram_merge_attn(0, 8, 128, None, None, None, None, None, None, None) == 0
+    # fitted basis: rank above G*H_kv*d, fewer tokens than the rank, rank not a multiple of 32
+    n = ctypes.c_size_t(0)
+    assert lib.lowram_fit_basis_workspace_size(ctypes.byref(L.lowram_compress_shape(2, 100, 1, 1, 64, 96, 32, 0, 1, 1,
+                                                                                    1, 0, 0)), ctypes.byref(n)) == UNSUPPORTED
+    assert lib.lowram_fit_basis_workspace_size(ctypes.byref(L.lowram_compress_shape(1, 20, 2, 2, 64, 32, 32, 0, 1, 1,
+                                                                                    1, 0, 0)), ctypes.byref(n)) == INVALID
+    assert lib.lowram_fit_basis_workspace_size(ctypes.byref(L.lowram_compress_shape(2, 100, 2, 2, 64, 40, 32, 0, 1, 1,
+                                                                                    1, 0, 0)), ctypes.byref(n)) == UNSUPPORTED
+    good = L.lowram_compress_shape(8, 8192, 4, 8, 128, 512, 128, 0, 1, 1, 1, 0, 0)
+    assert lib.lowram_fit_basis_workspace_size(ctypes.byref(good), ctypes.byref(n)) == 0
+    assert n.value >= 4 * 8 * 8192 * 4096 + 4 * 4096 * 4096       # the float32 keys and the Gram matrix
+    assert lib.lowram_fit_basis(ctypes.byref(good), None, None, None, None, 8, 0, None, None, None, 0,
+                                None) == WORKSPACE
+    # predictor fit: hidden width, head dim, Adam hyper-parameters, workspace
+    assert lib.lowram_fit_predictor_workspace_size(8, 128, 300, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.lowram_fit_predictor_workspace_size(8, 96, 128, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.lowram_fit_predictor_workspace_size(8, 128, 128, ctypes.byref(n)) == 0
+    assert n.value >= 3 * 4 * 8 * (2 * 128 * 128 + 256)
+    ws = ctypes.create_string_buffer(n.value + 256)
+    wsp = ctypes.c_void_p((ctypes.addressof(ws) + 255) & ~255)
+    assert lib.lowram_fit_predictor(1, 10, 8, 128, 128, 1, None, None, 5, 0.0, 0.9, 0.999, 1e-8, None, None, None,
+                                    None, None, wsp, n.value, None) == INVALID                    # lr <= 0
+    assert lib.lowram_fit_predictor(1, 10, 8, 128, 128, 1, None, None, 5, 1e-3, 1.0, 0.999, 1e-8, None, None, None,
+                                    None, None, wsp, n.value, None) == INVALID                    # beta1 = 1
+    assert lib.lowram_fit_predictor(1, 10, 8, 128, 128, 1, None, None, 5, 1e-3, 0.9, 0.999, 1e-8, None, None, None,
+                                    None, None, None, 0, None) == WORKSPACE
+    assert lib.lowram_predictor_grad(1, 10, 8, 128, 128, 1, None, None, None, None, None, None, None, None, None, None,
+                                     None, None) == INVALID
