@@ -5,12 +5,12 @@
 // Gradient (one kv-head, N tokens, E = v_hat - v, c = 2 / (N d)):
 //   g_w2 = c E^T H,  g_b2 = c sum_t E_t,  dZ = (E w2) * silu'(Z),  g_w1 = c dZ^T K,  g_b1 = c sum_t dZ_t,
 //   with Z = K w1^T + b1, H = silu(Z), silu'(z) = s + z s (1 - s), s = 1 / (1 + e^-z); loss = sum E^2 / (N d).
-// K1' predictor_grad_kernel: CTAs over (token range, kv-head, half of the hidden units).  A CTA walks its tokens
+// predictor_grad_kernel: CTAs over (token range, kv-head, half of the hidden units).  A CTA walks its tokens
 // in tiles of 32: the forward pass over all m hidden units (the output needs all of them), then the backward
 // pass for its 128 hidden units; each thread keeps an 8-column block of g_w2 and of g_w1 in registers across
 // the tiles and adds them to the global gradient once, with atomics.  fp32 CUDA cores throughout: the fit
 // compares with an fp64 reference step by step.
-// K2' adam_kernel: one Adam step with bias correction on a flat parameter array.
+// adam_kernel: one Adam step with bias correction on a flat parameter array.
 #include "common.cuh"
 #include "kernels.h"
 #include "predict_fit.h"
