@@ -31,7 +31,8 @@ __all__ = [
     "build", "lib", "Dims", "f64", "round_bf16", "round_f16", "round_f32", "quant_int4_g32",
     "dequant_int4_g32", "quant_int8_vec", "dequant_int8_vec", "rope", "rope_rows", "rope_angles", "mlp",
     "rebuild_keys", "predict_values", "decode", "project", "residuals", "compress_group",
-    "dense_decode", "merge_attn", "fit_basis", "predictor_loss_grad", "adam_step", "fit_predictor", "top_n", "n_res_for", "max_threads", "store",
+    "dense_decode", "merge_attn", "fit_basis", "predictor_loss_grad", "adam_step", "fit_predictor",
+    "attention_mass", "evict_plan", "top_n", "n_res_for", "max_threads", "store",
 ]
 
 
@@ -496,3 +497,38 @@ def fit_predictor(k_pre, v, w1, b1, w2, b2, *, steps: int, lr: float, beta1: flo
             for i in range(4):
                 P[i][h], M[i][h], Vv[i][h] = adam_step(P[i][h], g[i], M[i][h], Vv[i][h], s + 1, lr, beta1, beta2, eps)
     return P[0], P[1], P[2], P[3], losses
+
+
+def attention_mass(q_win, k, *, sm_scale: float = 0.0):
+    """Attention mass each prompt token receives from an observation window of queries, for choosing the heavy
+    hitters an evicted cache keeps [CB Key points / EX benchmarks: eviction keeps sinks, recent tokens and heavy
+    hitters].  q_win [B, W, H_q, d] and k [B, T, H_kv, d] rotated; every window query attends all T tokens;
+    mass[b, t] = sum_i sum_hq softmax_t(scale * q_win[b, i, hq] . k[b, t, hq // g])[t], g = H_q / H_kv.
+    Plain fp64 numpy; the row sums are W * H_q."""
+    Q, K = f64(q_win), f64(k)
+    B, W, H_q, d = Q.shape
+    T, H_kv = K.shape[1], K.shape[2]
+    g = H_q // H_kv
+    scale = sm_scale if sm_scale > 0 else d ** -0.5
+    mass = np.zeros((B, T))
+    for b in range(B):
+        for hq in range(H_q):
+            s = (Q[b, :, hq] @ K[b, :, hq // g].T) * scale            # [W, T]
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
+            mass[b] += (p / p.sum(axis=1, keepdims=True)).sum(axis=0)
+    return mass
+
+
+def evict_plan(mass, n_sink: int, n_recent: int, T_keep: int) -> np.ndarray:
+    """Tokens an evicted cache keeps, per sequence, ascending: the first n_sink, the last n_recent, and the
+    T_keep - n_sink - n_recent others of largest attention mass (ties to the lower index)."""
+    M = f64(mass)
+    B, T = M.shape
+    keep = np.empty((B, T_keep), dtype=np.int32)
+    for b in range(B):
+        forced = set(range(min(n_sink, T))) | set(range(max(0, T - n_recent), T))
+        rest = sorted((t for t in range(T) if t not in forced), key=lambda t: (-M[b, t], t))
+        chosen = sorted(forced | set(rest[:T_keep - len(forced)]))
+        keep[b] = chosen
+    return keep

@@ -565,6 +565,41 @@ def test_fit_predictor_recovers_a_planted_predictor():
     assert np.all(np.diff(losses[:50], axis=0) < 0)     # early steps descend
 
 
+# ------------------------------------------------------------------------------------------------
+# heavy hitters from accumulated attention (eviction)
+# ------------------------------------------------------------------------------------------------
+def test_attention_mass_matches_torch_softmax_and_sums_to_the_window():
+    B, W, H_q, H_kv, T, d = 2, 3, 4, 2, 17, 8
+    q, k = RNG.normal(0, 1, (B, W, H_q, d)), RNG.normal(0, 1, (B, T, H_kv, d))
+    mass = O.attention_mass(q, k)
+    want = np.zeros((B, T))
+    for b in range(B):
+        for hq in range(H_q):
+            lg = torch.as_tensor(q[b, :, hq]) @ torch.as_tensor(k[b, :, hq // 2]).T * d ** -0.5
+            want[b] += torch.softmax(lg, dim=-1).sum(0).numpy()
+    np.testing.assert_allclose(mass, want, atol=1e-12)
+    np.testing.assert_allclose(mass.sum(axis=1), W * H_q, atol=1e-10)
+
+
+def test_evict_plan_keeps_sinks_recents_and_the_heaviest():
+    T, n_sink, n_recent, T_keep = 30, 3, 5, 14
+    mass = RNG.random((2, T))
+    mass[1, 10] = mass[1, 11] = 5.0                   # a tie among the heaviest: both kept
+    keep = O.evict_plan(mass, n_sink, n_recent, T_keep)
+    for b in range(2):
+        kb = keep[b].tolist()
+        assert kb == sorted(kb) and len(set(kb)) == T_keep
+        assert set(range(n_sink)) <= set(kb) and set(range(T - n_recent, T)) <= set(kb)
+        middle = [t for t in range(n_sink, T - n_recent)]
+        heavy = sorted(middle, key=lambda t: (-mass[b, t], t))[:T_keep - n_sink - n_recent]   # brute force
+        assert set(kb) == set(range(n_sink)) | set(range(T - n_recent, T)) | set(heavy)
+    assert {10, 11} <= set(keep[1].tolist())
+    flat = np.ones((1, T))                               # all equal: the lowest middle indices win
+    assert O.evict_plan(flat, n_sink, n_recent, T_keep)[0].tolist() == \
+        list(range(n_sink + T_keep - n_sink - n_recent)) + list(range(T - n_recent, T))
+    assert O.evict_plan(mass, n_sink, n_recent, T)[0].tolist() == list(range(T))
+
+
 def test_residual_budgets_of_the_workloads():
     # ceil(rho * T): 0.25*256, 0.1*8192, 0.1*32768, 0.1*4096, 0.05*16384
     assert [O.n_res_for(r, T) for r, T in [(0.25, 256), (0.1, 8192), (0.1, 32768), (0.1, 4096), (0.05, 16384)]] \
