@@ -60,6 +60,10 @@ def _load():
             "lowram_compress": [ctypes.POINTER(lowram_compress_shape)] + [_vp] * 18 + [sz, _vp],
             "lowram_dense_workspace_size": [i32, i32, i32, i32, i32, psz],
             "lowram_dense_decode_attn": [i32, i32, i32, i32, i32, i32, flt, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp],
+            "lowram_attention_mass_workspace_size": [i32] * 7 + [psz],
+            "lowram_attention_mass": [i32] * 7 + [flt, _vp, _vp, _vp, _vp, sz, _vp],
+            "lowram_evict_plan_workspace_size": [i32, i32, psz],
+            "lowram_evict_plan": [i32] * 5 + [_vp, _vp, _vp, sz, _vp],
             "lowram_predictor_grad": [i32] * 6 + [_vp] * 11 + [_vp],
             "lowram_fit_predictor_workspace_size": [i32, i32, i32, psz],
             "lowram_fit_predictor": [i32] * 6 + [_vp, _vp, i32, flt, flt, flt, flt] + [_vp] * 6 + [sz, _vp],
@@ -321,6 +325,38 @@ def lowram_dense_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     _check(_load().lowram_dense_decode_attn(B, T, H_q, H_kv, d, _act(q), float(sm_scale), _p(q), _p(k), _p(v),
                                             _p(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream()))
     return out, lse
+
+
+# ------------------------------------------------------------------------------------------------
+# heavy hitters from accumulated attention: the tokens an evicted cache keeps
+# ------------------------------------------------------------------------------------------------
+def lowram_attention_mass(q_win: torch.Tensor, k: torch.Tensor, *, sm_scale: float = 0.0,
+                          workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Attention mass [B, T] of every prompt token from the window queries q_win [B, W, H_q, d] (k [B, T, H_kv, d])."""
+    B, W, H_q, d = q_win.shape
+    T, H_kv = k.shape[1], k.shape[2]
+    _dev(q_win, k)
+    n = ctypes.c_size_t(0)
+    _check(_load().lowram_attention_mass_workspace_size(B, T, W, H_q, H_kv, d, _act(k), ctypes.byref(n)))
+    ws = _workspace(n.value, workspace, k.device)
+    mass = torch.empty((B, T), dtype=torch.float32, device=k.device)
+    _check(_load().lowram_attention_mass(B, T, W, H_q, H_kv, d, _act(k), float(sm_scale), _p(q_win), _p(k), _p(mass),
+                                         _p(ws), ws.numel() * ws.element_size(), _stream()))
+    return mass
+
+
+def lowram_evict_plan(mass: torch.Tensor, *, n_sink: int, n_recent: int, T_keep: int,
+                      workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Kept token indices [B, T_keep] (ascending): sinks, recents and the heaviest others by mass [B, T]."""
+    B, T = mass.shape
+    _dev(mass)
+    n = ctypes.c_size_t(0)
+    _check(_load().lowram_evict_plan_workspace_size(B, T, ctypes.byref(n)))
+    ws = _workspace(n.value, workspace, mass.device)
+    keep = torch.empty((B, int(T_keep)), dtype=torch.int32, device=mass.device)
+    _check(_load().lowram_evict_plan(B, T, int(n_sink), int(n_recent), int(T_keep), _p(mass), _p(keep), _p(ws),
+                                     ws.numel() * ws.element_size(), _stream()))
+    return keep
 
 
 # ------------------------------------------------------------------------------------------------

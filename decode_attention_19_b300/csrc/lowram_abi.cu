@@ -7,6 +7,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "predict_fit.h"
+#include "evict.h"
 
 using namespace lowram;
 
@@ -291,6 +292,75 @@ static lowram_status check_compress_shape(const lowram_compress_shape* s) {
         return fail(LOWRAM_ERR_INVALID_ARG, "res_dtype=%d", s->res_dtype);
     if (s->keys_post_rope && s->T > 0 && s->max_pos < 1) return fail(LOWRAM_ERR_INVALID_ARG, "max_pos=%d", s->max_pos);
     return LOWRAM_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+// heavy hitters from accumulated attention (eviction plan)
+// ------------------------------------------------------------------------------------------------
+static lowram_status check_mass_shape(int32_t B, int32_t T, int32_t W, int32_t H_q, int32_t H_kv, int32_t d) {
+    if (B < 0 || T < 0 || W < 1 || H_kv < 1 || H_q < 1 || H_q % H_kv != 0)
+        return fail(LOWRAM_ERR_INVALID_ARG, "B=%d T=%d W=%d H_q=%d H_kv=%d", B, T, W, H_q, H_kv);
+    const int g = H_q / H_kv;
+    if (g != 1 && g != 2 && g != 4 && g != 7 && g != 8) return fail(LOWRAM_ERR_UNSUPPORTED, "H_q/H_kv=%d", g);
+    if (d != 64 && d != 128) return fail(LOWRAM_ERR_UNSUPPORTED, "d=%d (64 or 128 supported)", d);
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_attention_mass_workspace_size(int32_t B, int32_t T, int32_t W, int32_t H_q, int32_t H_kv,
+                                                   int32_t d, int32_t dtype, size_t* bytes) {
+    lowram_status st = check_mass_shape(B, T, W, H_q, H_kv, d);
+    if (st != LOWRAM_OK) return st;
+    if (!is_act(dtype)) return fail(LOWRAM_ERR_INVALID_ARG, "dtype=%d", dtype);
+    if (!bytes) return fail(LOWRAM_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = kHeader + align256(mass_workspace_bytes(B, T, W, H_q, H_kv, d, dtype));
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_attention_mass(int32_t B, int32_t T, int32_t W, int32_t H_q, int32_t H_kv, int32_t d,
+                                    int32_t dtype, float sm_scale, const void* q_win, const void* k, float* mass_out,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+    size_t need = 0;
+    lowram_status st = lowram_attention_mass_workspace_size(B, T, W, H_q, H_kv, d, dtype, &need);
+    if (st != LOWRAM_OK) return st;
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return fail(LOWRAM_ERR_WORKSPACE, "workspace %zu bytes, %zu needed", workspace ? workspace_bytes : 0, need);
+    if ((int64_t)B * T == 0) return LOWRAM_OK;
+    if (!q_win || !k || !mass_out) return fail(LOWRAM_ERR_INVALID_ARG, "a required pointer is NULL");
+    const void* ptrs[] = {q_win, k, mass_out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
+    const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf((float)d);
+    const cudaError_t e = launch_attention_mass(B, T, W, H_q, H_kv, d, dtype, scale, q_win, k, mass_out,
+                                                (char*)workspace + kHeader, (cudaStream_t)stream);
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "attention_mass");
+}
+
+lowram_status lowram_evict_plan_workspace_size(int32_t B, int32_t T, size_t* bytes) {
+    if (B < 0 || T < 0) return fail(LOWRAM_ERR_INVALID_ARG, "B=%d T=%d", B, T);
+    if (!bytes) return fail(LOWRAM_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = kHeader + align256(sizeof(float) * (size_t)B * T);
+    return LOWRAM_OK;
+}
+
+lowram_status lowram_evict_plan(int32_t B, int32_t T, int32_t n_sink, int32_t n_recent, int32_t T_keep,
+                                const float* mass, int32_t* keep_out, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    size_t need = 0;
+    lowram_status st = lowram_evict_plan_workspace_size(B, T, &need);
+    if (st != LOWRAM_OK) return st;
+    if (n_sink < 0 || n_recent < 0 || T_keep < 0 || T_keep > T ||
+        T_keep < (n_sink + n_recent < T ? n_sink + n_recent : T))
+        return fail(LOWRAM_ERR_INVALID_ARG, "n_sink=%d n_recent=%d T_keep=%d T=%d (need sinks + recents <= T_keep <= T)",
+                    n_sink, n_recent, T_keep, T);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return fail(LOWRAM_ERR_WORKSPACE, "workspace %zu bytes, %zu needed", workspace ? workspace_bytes : 0, need);
+    if ((int64_t)B * T_keep == 0) return LOWRAM_OK;
+    if (!mass || !keep_out) return fail(LOWRAM_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(mass) || !aligned16(keep_out)) return fail(LOWRAM_ERR_ALIGNMENT, "a pointer is not 16-byte aligned");
+    const cudaError_t e = launch_evict_plan(B, T, n_sink, n_recent, T_keep, mass,
+                                            (float*)((char*)workspace + kHeader), keep_out, (uint32_t*)workspace,
+                                            (cudaStream_t)stream);
+    return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "evict_plan");
 }
 
 // ------------------------------------------------------------------------------------------------

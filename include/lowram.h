@@ -242,6 +242,37 @@ LOWRAM_API lowram_status lowram_compress(const lowram_compress_shape* shape, con
                               float* const* err_out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Heavy hitters from accumulated attention: which prompt tokens an evicted cache keeps ("LowRAM:
+ * predict values from keys, store only the misses", Key points; the eviction composed with the
+ * compressed cache keeps sinks, recent tokens and heavy hitters).  The plan is made before
+ * compression: compress the kept tokens' keys and values with their positions (pos).
+ * ------------------------------------------------------------------------------------------- */
+LOWRAM_API lowram_status lowram_attention_mass_workspace_size(int32_t B, int32_t T, int32_t W, int32_t H_q, int32_t H_kv,
+                                                              int32_t d, int32_t dtype, size_t* bytes);
+
+/*
+ * lowram_attention_mass -- attention mass each of the T prompt tokens receives from an observation
+ * window of W queries per sequence: mass[b, t] = sum_i sum_hq softmax_t(scale q_win[b, i, hq] .
+ * k[b, t, hq / g])[t], every window query attending all T tokens (no causal mask), so each row sums
+ * to W * H_q.  q_win [B, W, H_q, d] and k [B, T, H_kv, d] rotated, in dtype (LOWRAM_F32 or
+ * LOWRAM_BF16); mass_out [B, T] float32; sm_scale <= 0 means 1/sqrt(d).  H_q/H_kv in {1, 2, 4, 7, 8}.
+ */
+LOWRAM_API lowram_status lowram_attention_mass(int32_t B, int32_t T, int32_t W, int32_t H_q, int32_t H_kv, int32_t d,
+                                               int32_t dtype, float sm_scale, const void* q_win, const void* k,
+                                               float* mass_out, void* workspace, size_t workspace_bytes, void* stream);
+
+LOWRAM_API lowram_status lowram_evict_plan_workspace_size(int32_t B, int32_t T, size_t* bytes);
+
+/*
+ * lowram_evict_plan -- keep_out [B, T_keep] int32, ascending per sequence: tokens t < n_sink and
+ * t >= T - n_recent, and the T_keep - n_sink - n_recent others of largest mass (ties to the lower
+ * index; exact selection).  Requires n_sink + n_recent <= T_keep <= T (or T_keep = T).
+ */
+LOWRAM_API lowram_status lowram_evict_plan(int32_t B, int32_t T, int32_t n_sink, int32_t n_recent, int32_t T_keep,
+                                           const float* mass, int32_t* keep_out, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Test-time fit of the value predictor (LowRAM abstract: the predictor is fitted at test time;
  * "Value cache amortisation in plain language": values are predicted from pre-RoPE keys).  Per
  * kv-head h the predictor v_hat = w2 silu(w1 k + b1) + b2 is fitted to the prompt's (pre-RoPE key,
