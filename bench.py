@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--fit-iters", type=int, default=8)
     ap.add_argument("--fit-predictor", action="store_true",
                     help="time one Adam step of lowram_fit_predictor on the workload's layer shape")
+    ap.add_argument("--evict-plan", action="store_true",
+                    help="time lowram_attention_mass + lowram_evict_plan on the workload's prompt (T_nominal tokens)")
+    ap.add_argument("--window", type=int, default=32, help="observation-window queries for --evict-plan")
     return ap.parse_args()
 
 
@@ -436,6 +439,10 @@ def main():
         if rank == 0:
             fit_predictor_bench(w, dev, args, pk)
         return
+    if args.evict_plan:
+        if rank == 0:
+            evict_bench(w, dev, args, pk)
+        return
     groups, pos, compress_ms = build_cache(w, dev)
     cos, sin = L.lowram_rope_table(w.d, w.theta, w.T_nominal or w.T)
     qs = [synth.draw_query(w, l).to(dev) for l in range(w.L)]
@@ -701,6 +708,40 @@ def fit_predictor_bench(w, dev, args, pk):
                      "frac": achieved / peak_tf,
                      "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock",
                      "work": "10 * B*T * d * m * H_kv per step"}}))
+
+
+def evict_bench(w, dev, args, pk):
+    """The heavy-hitter eviction plan of one layer's prompt: attention mass of a --window query window over the
+    T_nominal prompt tokens (rotated K, bf16), then the kept tokens (64 sinks, 2048 recents, to w.T)."""
+    import decode_attention_19_b300 as L
+    Tn = w.T_nominal or w.T
+    g = torch.Generator(device=dev).manual_seed(13)
+    q = (torch.randn((w.B, args.window, w.H_q, w.d), generator=g, device=dev) * 2 * w.d ** -0.5).to(torch.bfloat16)
+    k = torch.randn((w.B, Tn, w.H_kv, w.d), generator=g, device=dev).to(torch.bfloat16)
+    n_sink, n_recent = 64, min(2048, Tn // 4)
+    T_keep = max(w.T, n_sink + n_recent) if w.T < Tn else Tn // 4 + n_sink + n_recent
+    for _ in range(max(1, args.warmup)):
+        keep = L.lowram_evict_plan(L.lowram_attention_mass(q, k), n_sink=n_sink, n_recent=n_recent, T_keep=T_keep)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        a.record()
+        keep = L.lowram_evict_plan(L.lowram_attention_mass(q, k), n_sink=n_sink, n_recent=n_recent, T_keep=T_keep)
+        b.record()
+    torch.cuda.synchronize()
+    ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+    # bytes: the window's log-sum-exp reads K (and K again as the value operand) once per window query, the mass
+    # kernel reads K once; FLOPs: the logits twice
+    kbytes = w.B * Tn * w.H_kv * w.d * 2
+    flops = 2 * 2.0 * w.B * Tn * args.window * w.H_q * w.d
+    print(json.dumps({
+        "metric": "eviction plan: time per layer", "value": ms, "unit": "ms", "higher_is_better": False,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T_prompt": Tn, "window": args.window, "H_q": w.H_q,
+                   "H_kv": w.H_kv, "d": w.d, "n_sink": n_sink, "n_recent": n_recent, "T_keep": T_keep},
+        "kept_first_row_head": keep[0, :4].tolist(),
+        "work": {"K_bytes": kbytes, "bytes_read_estimate": kbytes * (2 * args.window + 1), "flops": flops,
+                 "tflops_achieved": flops / (ms * 1e-3) / 1e12}}))
 
 
 def dense_bench(w, dev, qs, flush, args):
