@@ -730,18 +730,30 @@ def evict_bench(w, dev, args, pk):
         b.record()
     torch.cuda.synchronize()
     ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
-    # bytes: the window's log-sum-exp reads K (and K again as the value operand) once per window query, the mass
-    # kernel reads K once; FLOPs: the logits twice
+    em = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in em:
+        a.record()
+        L.lowram_attention_mass(q, k)
+        b.record()
+    torch.cuda.synchronize()
+    mass_ms = float(np.median([a.elapsed_time(b) for a, b in em]))
+    # bytes: the window's log-sum-exp pass and the mass pass each read K once; FLOPs: the logits, twice
     kbytes = w.B * Tn * w.H_kv * w.d * 2
     flops = 2 * 2.0 * w.B * Tn * args.window * w.H_q * w.d
+    peak_tf = NOMINAL_SM * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
     print(json.dumps({
         "metric": "eviction plan: time per layer", "value": ms, "unit": "ms", "higher_is_better": False,
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T_prompt": Tn, "window": args.window, "H_q": w.H_q,
                    "H_kv": w.H_kv, "d": w.d, "n_sink": n_sink, "n_recent": n_recent, "T_keep": T_keep},
         "kept_first_row_head": keep[0, :4].tolist(),
-        "work": {"K_bytes": kbytes, "bytes_read_estimate": kbytes * (2 * args.window + 1), "flops": flops,
-                 "tflops_achieved": flops / (ms * 1e-3) / 1e12}}))
+        "mass_ms": mass_ms,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf,
+                     "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock",
+                     "work": "2 passes x 2 * B*T * W*H_q * d (the window logits)"},
+        "work": {"K_bytes": kbytes, "bytes_read_estimate": 2 * kbytes, "flops": flops}}))
 
 
 def dense_bench(w, dev, qs, flush, args):

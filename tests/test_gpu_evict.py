@@ -31,6 +31,7 @@ def window_case(B, T, W, H_q, H_kv, d, dtype, seed):
     (1, 777, 4, 28, 4, 128, torch.bfloat16),
     (2, 300, 1, 16, 2, 64, torch.float32),
     (3, 65, 8, 8, 8, 64, torch.bfloat16),
+    (1, 160013, 2, 4, 1, 64, torch.bfloat16),    # long prompt: several token tiles per log-sum-exp CTA, ragged tail
 ])
 def test_attention_mass_matches_oracle(B, T, W, H_q, H_kv, d, dtype):
     import decode_attention_19_b300 as L
