@@ -181,45 +181,50 @@ __global__ void evict_scores_kernel(const float* __restrict__ mass, int64_t n, i
 }  // namespace
 
 size_t mass_workspace_bytes(int B, int T, int W, int H_q, int H_kv, int d, int dtype) {
-    (void)H_kv, (void)d, (void)dtype;
     auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t lse_bytes = a(sizeof(float) * (size_t)B * W * H_q);
+    if (dtype == LOWRAM_BF16)
+        return lse_bytes + a(sizeof(float2) * (size_t)B * window_tc_n_chunks(B, T) * W * H_q) +
+               a((size_t)2 * B * H_kv * window_tc_qpad(W, H_q, H_kv) * d);    // the packed window queries
     const int ct = lse_chunk_tiles(B, T);
     const size_t n_chunks = T > 0 ? (size_t)cdiv(cdiv(T, kTileRows), ct) : 0;
-    return a(sizeof(float) * (size_t)B * W * H_q) +                      // lse of every window query-head
-           a(sizeof(float2) * (size_t)B * n_chunks * W * H_q);           // the chunks' (max, sum) pairs
+    return lse_bytes + a(sizeof(float2) * (size_t)B * n_chunks * W * H_q);   // the chunks' (max, sum) pairs
 }
 
 cudaError_t launch_attention_mass(int B, int T, int W, int H_q, int H_kv, int d, int dtype, float scale,
-                                  const void* q_win, const void* k, float* mass, void* scratch, cudaStream_t st) {
+                                  const void* q_win, const void* k, float* mass, void* scratch, uint32_t* check,
+                                  cudaStream_t st) {
     auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
     if ((int64_t)B * T == 0) return cudaSuccess;
-    const int ct = lse_chunk_tiles(B, T);
-    const int n_chunks = cdiv(cdiv(T, kTileRows), ct);
     float* lse = (float*)scratch;
     float2* part = (float2*)((char*)scratch + a(sizeof(float) * (size_t)B * W * H_q));
-    const bool bf = dtype == LOWRAM_BF16;
-    const size_t lse_smem = sizeof(float) * (tile_smem_floats(4) + 2 * 8 * 128);
-    const dim3 lse_grid((unsigned)n_chunks, (unsigned)B);
-    if (bf)
-        lse_partial_kernel<__nv_bfloat16><<<lse_grid, kTileThreads, lse_smem, st>>>(
-            T, W, H_q, H_kv, d, scale, ct, (const __nv_bfloat16*)q_win, (const __nv_bfloat16*)k, part);
-    else
-        lse_partial_kernel<float><<<lse_grid, kTileThreads, lse_smem, st>>>(T, W, H_q, H_kv, d, scale, ct,
-                                                                           (const float*)q_win, (const float*)k, part);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     const int NQall = W * H_q;
-    lse_reduce_kernel<<<dim3((unsigned)cdiv(NQall, 32), (unsigned)B), 256, 0, st>>>(n_chunks, NQall, part, lse);
+    const dim3 reduce_grid((unsigned)cdiv(NQall, 32), (unsigned)B);
+    cudaError_t e;
+    if (dtype == LOWRAM_BF16) {
+        // tensor cores: pack the window queries, log-sum-exp pass, fold the chunks, mass pass
+        const int n_chunks = window_tc_n_chunks(B, T);
+        void* qp = (char*)part + a(sizeof(float2) * (size_t)B * n_chunks * NQall);
+        if ((e = launch_pack_window(B, W, H_q, H_kv, d, q_win, qp, st)) != cudaSuccess) return e;
+        if ((e = launch_window_tc(false, B, T, W, H_q, H_kv, d, scale, qp, k, part, nullptr, nullptr, check, st)) !=
+            cudaSuccess)
+            return e;
+        lse_reduce_kernel<<<reduce_grid, 256, 0, st>>>(n_chunks, NQall, part, lse);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        return launch_window_tc(true, B, T, W, H_q, H_kv, d, scale, qp, k, nullptr, lse, mass, check, st);
+    }
+    // float32 prompts: the fp32 tile product on CUDA cores
+    const int ct = lse_chunk_tiles(B, T);
+    const int n_chunks = cdiv(cdiv(T, kTileRows), ct);
+    const size_t lse_smem = sizeof(float) * (tile_smem_floats(4) + 2 * 8 * 128);
+    lse_partial_kernel<float><<<dim3((unsigned)n_chunks, (unsigned)B), kTileThreads, lse_smem, st>>>(
+        T, W, H_q, H_kv, d, scale, ct, (const float*)q_win, (const float*)k, part);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    lse_reduce_kernel<<<reduce_grid, 256, 0, st>>>(n_chunks, NQall, part, lse);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t smem = sizeof(float) * tile_smem_floats(4);
-    const dim3 grid((unsigned)cdiv(T, kTileRows), (unsigned)B);
-    if (bf)
-        mass_kernel<__nv_bfloat16><<<grid, kTileThreads, smem, st>>>(T, W, H_q, H_kv, d, scale,
-                                                                     (const __nv_bfloat16*)q_win,
-                                                                     (const __nv_bfloat16*)k, lse, mass);
-    else
-        mass_kernel<float><<<grid, kTileThreads, smem, st>>>(T, W, H_q, H_kv, d, scale, (const float*)q_win,
-                                                             (const float*)k, lse, mass);
+    mass_kernel<float><<<dim3((unsigned)cdiv(T, kTileRows), (unsigned)B), kTileThreads, smem, st>>>(
+        T, W, H_q, H_kv, d, scale, (const float*)q_win, (const float*)k, lse, mass);
     return cudaGetLastError();
 }
 

@@ -331,7 +331,7 @@ lowram_status lowram_attention_mass(int32_t B, int32_t T, int32_t W, int32_t H_q
         if (!aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
     const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf((float)d);
     const cudaError_t e = launch_attention_mass(B, T, W, H_q, H_kv, d, dtype, scale, q_win, k, mass_out,
-                                                (char*)workspace + kHeader, (cudaStream_t)stream);
+                                                (char*)workspace + kHeader, (uint32_t*)workspace, (cudaStream_t)stream);
     return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "attention_mass");
 }
 

@@ -256,6 +256,9 @@ LOWRAM_API lowram_status lowram_attention_mass_workspace_size(int32_t B, int32_t
  * k[b, t, hq / g])[t], every window query attending all T tokens (no causal mask), so each row sums
  * to W * H_q.  q_win [B, W, H_q, d] and k [B, T, H_kv, d] rotated, in dtype (LOWRAM_F32 or
  * LOWRAM_BF16); mass_out [B, T] float32; sm_scale <= 0 means 1/sqrt(d).  H_q/H_kv in {1, 2, 4, 7, 8}.
+ * bf16 logits run on the tensor cores (fp32 accumulation), float32 ones on CUDA cores.  Device check
+ * word (lowram_get_error): LOWRAM_CHECK_TIMEOUT if a tensor-core pipeline wait gave up (mass_out is
+ * then incomplete).
  */
 LOWRAM_API lowram_status lowram_attention_mass(int32_t B, int32_t T, int32_t W, int32_t H_q, int32_t H_kv, int32_t d,
                                                int32_t dtype, float sm_scale, const void* q_win, const void* k,

@@ -1,7 +1,8 @@
 """GPU parity of the heavy-hitter eviction plan: the attention mass of an observation window over the prompt's
-tokens (against the oracle's fp64 softmax sums), and the kept tokens (exact index sets: sinks, recents, the
-heaviest others, ties to the lower index).  Shapes: several q-heads per kv-head ratios, both head dims, bf16 and
-float32, ragged token tiles, windows of 1 to 32 queries.
+tokens (against the oracle's fp64 softmax sums; bf16 prompts take the tensor-core path, float32 ones the CUDA
+cores), and the kept tokens (exact index sets: sinks, recents, the heaviest others, ties to the lower index).
+Shapes: several q-heads per kv-head ratios, both head dims, bf16 and float32, ragged token tiles, windows of 1 to
+40 queries, long prompts with several token tiles per CTA.
 """
 import numpy as np
 import pytest
@@ -31,7 +32,9 @@ def window_case(B, T, W, H_q, H_kv, d, dtype, seed):
     (1, 777, 4, 28, 4, 128, torch.bfloat16),
     (2, 300, 1, 16, 2, 64, torch.float32),
     (3, 65, 8, 8, 8, 64, torch.bfloat16),
-    (1, 160013, 2, 4, 1, 64, torch.bfloat16),    # long prompt: several token tiles per log-sum-exp CTA, ragged tail
+    (1, 160013, 2, 4, 1, 64, torch.bfloat16),    # long prompt: several token tiles per CTA, ragged tail
+    (1, 160013, 2, 4, 1, 64, torch.float32),
+    (2, 4000, 40, 8, 1, 128, torch.bfloat16),    # 320 window query-heads per kv-head: three query tiles
 ])
 def test_attention_mass_matches_oracle(B, T, W, H_q, H_kv, d, dtype):
     import decode_attention_19_b300 as L
