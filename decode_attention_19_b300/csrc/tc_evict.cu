@@ -16,9 +16,11 @@
 // box is one operand tile.  K tiles come straight from the [B*T, H_kv, d] cache through a 3D TMA map (rows past
 // the sequence's end are masked; past the cache's end TMA fills zeros).
 //
-// One CTA of 128 threads per (chunk of token tiles, b), two CTAs per SM.  Thread 0 issues the TMA loads and the
-// MMAs; the next step's K tile is in flight (two stages) while the current step multiplies and all four warps
-// read TMEM.  Every wait is bounded (tc_common.cuh): on a timeout the CTA sets LOWRAM_CHECK_TIMEOUT, waits for
+// One CTA of 256 threads per (chunk of token tiles, b), two CTAs per SM.  Thread 0 issues the TMA loads and the
+// MMAs; the next step's K tile is in flight (two stages) while the current step multiplies and all eight warps
+// read TMEM: warp w takes lanes 32 (w % 4) .. + 31 and columns 64 (w / 4) .. + 63, so the two column halves of
+// a row keep separate partial results, combined once per chunk through shared memory.  Exponentials are base 2
+// on one fused multiply-add: exp(scale x - m) = 2^(x (scale log2 e) - m log2 e).  Every wait is bounded (tc_common.cuh): on a timeout the CTA sets LOWRAM_CHECK_TIMEOUT, waits for
 // what it issued, frees TMEM and returns.
 #include "evict.h"
 #include "tc_common.cuh"
@@ -29,12 +31,22 @@ namespace lowram {
 
 namespace {
 
-constexpr int kWThreads = 128;
+constexpr int kWThreads = 256;            // two warps per TMEM lane quarter, one per half of the columns
 constexpr int kWTile = 128;               // tokens per K tile, query-heads per Q tile
 constexpr int kWChunk = 16384;            // one 64-wide k-chunk of a 128-row tile, bf16, 128-byte swizzled
-constexpr int kWMaxChunkTiles = 16;       // token tiles per CTA at most
+constexpr int kWMaxChunkTiles = 8;        // token tiles per CTA at most
 constexpr int kWSmem = 1024 /* alignment */ + 2 * kWChunk /* Q */ + 4 * kWChunk /* K, two stages */ +
-                       kWTile * 4 /* lse of the Q tile */ + kWMaxChunkTiles * kWTile * 4 /* token mass */ + 64;
+                       kWTile * 4 /* lse of the Q tile */ + 2 * kWMaxChunkTiles * kWTile * 4 /* token mass */ +
+                       kWTile * 8 /* column-half exchange */ + 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// 2^x on the special-function unit (ex2.approx.ftz: relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // qp[(b*H_kv + h)*NQpad + n][:] = q_win[b, n / g, h*g + n % g, :] for n < NQ = W*g, zero rows up to NQpad.
 __global__ void pack_window_kernel(const uint4* __restrict__ q, int B, int W, int H_q, int H_kv, int d, int NQpad,
@@ -74,14 +86,15 @@ __global__ void __launch_bounds__(kWThreads, 2)
     uint8_t* Qs = smem;                                        // [d/64][128 rows x 128 B]
     uint8_t* Ks = Qs + 2 * kWChunk;                            // [2 stages][d/64][128 rows x 128 B]
     float* lse_s = (float*)(Ks + 4 * kWChunk);                 // [128]
-    float* mass_s = lse_s + kWTile;                            // [chunk tiles][128]
-    uint64_t* kfull = (uint64_t*)(mass_s + kWMaxChunkTiles * kWTile);   // [2]
+    float* mass_s = lse_s + kWTile;                            // [2 halves][chunk tiles][128]
+    float2* xch = (float2*)(mass_s + 2 * kWMaxChunkTiles * kWTile);     // [128]
+    uint64_t* kfull = (uint64_t*)(xch + kWTile);               // [2]
     uint64_t* qfull = kfull + 2;
     uint64_t* mdone = qfull + 1;
     uint32_t* tmem_slot = (uint32_t*)(mdone + 1);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, row = tid & (kWTile - 1), half = warp >> 2;
     const int b = blockIdx.y, c = blockIdx.x;
     const int n_tiles = (int)cdiv(p.T, kWTile);
     const int tile_begin = c * p.chunk_tiles;
@@ -105,12 +118,13 @@ __global__ void __launch_bounds__(kWThreads, 2)
         tmem_relinquish();
     }
     if (kMass)
-        for (int tl = 0; tl < ntl; ++tl) mass_s[tl * kWTile + tid] = 0.0f;
+        for (int tl = 0; tl < ntl; ++tl) mass_s[(half * kWMaxChunkTiles + tl) * kWTile + row] = 0.0f;
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)half * 64;
+    const float c2 = p.scale * kLog2e;       // logit in base-2 units per unit of q . k
 
     // thread 0's outstanding asynchronous work (and the phase parity each completes), for the drain after a
     // timeout
@@ -142,7 +156,8 @@ __global__ void __launch_bounds__(kWThreads, 2)
         issue_q(0);
         issue_k(0);
     }
-    float run_m = -INFINITY, run_s = 0.0f;       // log-sum-exp pass: this thread's query over the chunk
+    float run_m = -INFINITY, run_s = 0.0f;       // log-sum-exp pass: this thread's query and column half over
+                                                 // the chunk, max in base-2 units
     bool aborted = false;
     for (int i = 0; i < S; ++i) {
         const int h = step_h(i), qc = step_qc(i), tl = step_tl(i);
@@ -171,12 +186,12 @@ __global__ void __launch_bounds__(kWThreads, 2)
                 mma_par = (uint32_t)i & 1u;
             }
         }
-        if (kMass && tl == 0) {
+        if (kMass && tl == 0 && tid < kWTile) {
             const int n = qc * kWTile + tid;
-            float v = INFINITY;                  // padding query-heads: exp(logit - inf) = 0
+            float v = INFINITY;                  // padding query-heads: 2^(x c2 - inf) = 0
             if (n < NQ) {
                 const int iw = n / g, hq = h * g + (n - iw * g);
-                v = p.lse[((int64_t)b * p.W + iw) * p.H_q + hq];
+                v = p.lse[((int64_t)b * p.W + iw) * p.H_q + hq] * kLog2e;
             }
             lse_s[tid] = v;
         }
@@ -195,53 +210,62 @@ __global__ void __launch_bounds__(kWThreads, 2)
         const int t0 = (tile_begin + tl) * kWTile;
         const int nvalid = min(kWTile, p.T - t0);
         if (!kMass) {
-            // lane = query-head qc*128 + tid, columns = the tile's tokens
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                float x[32], y[32];
-                tmem_ld_2x32(taddr + cb * 64, taddr + cb * 64 + 32, x, y);
-                float m = -INFINITY;
+            // lane = query-head qc*128 + row, columns = tokens half*64 .. half*64 + 63 of the tile
+            const int cv = nvalid - half * 64;   // valid columns of this half
+            float x[32], y[32];
+            tmem_ld_2x32(taddr, taddr + 32, x, y);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j < cv) mx = fmaxf(mx, x[j]);
+                if (32 + j < cv) mx = fmaxf(mx, y[j]);
+            }
+            if (cv > 0) {
+                const float m2 = mx * c2;        // scale > 0: the largest scaled logit, base 2
+                float s = 0.0f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    if (cb * 64 + j < nvalid) m = fmaxf(m, x[j] * p.scale);
-                    if (cb * 64 + 32 + j < nvalid) m = fmaxf(m, y[j] * p.scale);
+                    if (j < cv) s += ex2(fmaf(x[j], c2, -m2));
+                    if (32 + j < cv) s += ex2(fmaf(y[j], c2, -m2));
                 }
-                if (m != -INFINITY) {
-                    float s = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (cb * 64 + j < nvalid) s += __expf(x[j] * p.scale - m);
-                        if (cb * 64 + 32 + j < nvalid) s += __expf(y[j] * p.scale - m);
-                    }
-                    const float M = fmaxf(run_m, m);
-                    run_s = (run_m == -INFINITY ? 0.0f : run_s * __expf(run_m - M)) + s * __expf(m - M);
-                    run_m = M;
-                }
+                const float M = fmaxf(run_m, m2);
+                run_s = (run_m == -INFINITY ? 0.0f : run_s * ex2(run_m - M)) + s * ex2(m2 - M);
+                run_m = M;
             }
             if (tl == ntl - 1) {
-                const int n = qc * kWTile + tid;
-                if (n < NQ) {
-                    const int iw = n / g, hq = h * g + (n - iw * g);
-                    p.part[((int64_t)b * gridDim.x + c) * ((int64_t)p.W * p.H_q) + (int64_t)iw * p.H_q + hq] =
-                        make_float2(run_m, run_s);
+                // the column halves of each query-head meet; the pair goes out in natural-log units
+                if (half == 1) xch[row] = make_float2(run_m, run_s);
+                __syncthreads();
+                if (half == 0) {
+                    const float2 o = xch[row];
+                    const float M = fmaxf(run_m, o.x);
+                    if (M != -INFINITY) {
+                        run_s = (run_m == -INFINITY ? 0.0f : run_s * ex2(run_m - M)) +
+                                (o.x == -INFINITY ? 0.0f : o.y * ex2(o.x - M));
+                        run_m = M;
+                    }
+                    const int n = qc * kWTile + row;
+                    if (n < NQ) {
+                        const int iw = n / g, hq = h * g + (n - iw * g);
+                        p.part[((int64_t)b * gridDim.x + c) * ((int64_t)p.W * p.H_q) + (int64_t)iw * p.H_q + hq] =
+                            make_float2(run_m * kLn2, run_s);
+                    }
                 }
                 run_m = -INFINITY;
                 run_s = 0.0f;
             }
         } else {
-            // lane = token t0 + tid, columns = query-heads qc*128 + j
+            // lane = token t0 + row, columns = query-heads qc*128 + half*64 .. + 63
+            float x[32], y[32];
+            tmem_ld_2x32(taddr, taddr + 32, x, y);
+            const float* ls = lse_s + half * 64;
             float acc = 0.0f;
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                float x[32], y[32];
-                tmem_ld_2x32(taddr + cb * 64, taddr + cb * 64 + 32, x, y);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    acc += __expf(x[j] * p.scale - lse_s[cb * 64 + j]);
-                    acc += __expf(y[j] * p.scale - lse_s[cb * 64 + 32 + j]);
-                }
+            for (int j = 0; j < 32; ++j) {
+                acc += ex2(fmaf(x[j], c2, -ls[j]));
+                acc += ex2(fmaf(y[j], c2, -ls[32 + j]));
             }
-            mass_s[tl * kWTile + tid] += acc;
+            mass_s[(half * kWMaxChunkTiles + tl) * kWTile + row] += acc;
         }
         fence_before();
         __syncthreads();                          // TMEM and lse_s are read before the next step overwrites them
@@ -254,10 +278,11 @@ __global__ void __launch_bounds__(kWThreads, 2)
         if (mma_out) mbar_wait_drain(mdone, mma_par);
         flag(p.check, LOWRAM_CHECK_TIMEOUT);
     }
-    if (kMass && !aborted)
+    if (kMass && !aborted && tid < kWTile)       // the last step's closing barrier ordered every half's sums
         for (int tl = 0; tl < ntl; ++tl) {
             const int t = (tile_begin + tl) * kWTile + tid;
-            if (t < p.T) p.mass[(int64_t)b * p.T + t] = mass_s[tl * kWTile + tid];
+            if (t < p.T)
+                p.mass[(int64_t)b * p.T + t] = mass_s[tl * kWTile + tid] + mass_s[(kWMaxChunkTiles + tl) * kWTile + tid];
         }
     fence_before();
     __syncthreads();
