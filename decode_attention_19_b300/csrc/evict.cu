@@ -4,13 +4,16 @@
 // hitters are kept).
 //
 // Attention mass of an observation window: W rotated queries per sequence (the prompt's last ones) each attend all
-// T prompt tokens; mass[b, t] = sum_i sum_hq softmax_t(scale * q[b, i, hq] . k[b, t, hq / g])[t].
+// T prompt tokens; mass[b, t] = sum_i sum_hq softmax_t(scale * q[b, i, hq] . k[b, t, hq / g])[t].  Two passes over
+// the logits, the first for the log-sum-exp of every (window query, q-head), the second for the mass.  bf16 prompts
+// run both on the tensor cores (tc_evict.cu); float32 prompts on CUDA cores here:
 //   1. lse_partial_kernel: CTAs of a few 32-token tiles; per kv-head the logits of each tile's tokens against the
 //      head's W*g window queries come from the register-blocked tile product (each key row is read once for all
 //      of them), and every query's (max, sum of exp) over the CTA's tokens is written out; lse_reduce_kernel folds
 //      the CTAs' pairs into the log-sum-exp of every (window query, q-head);
 //   2. mass_kernel: CTAs of 32 tokens; the same logits again, exp(logit - lse) summed over the queries with warp
 //      shuffles, and each token's mass written once.
+// lse_reduce_kernel serves both paths (the chunks' pairs share one layout).
 // Eviction plan: the first n_sink and last n_recent tokens are forced (score +inf), the rest ranked by mass; the
 // exact top-T_keep selection (select.cu: ties to the lower index, output ascending) gives the kept tokens.
 #include "common.cuh"
