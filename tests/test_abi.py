@@ -144,3 +144,38 @@ def test_tail_merge_and_fit_entry_points_check_arguments_on_the_host():
                                     None, None, None, 0, None) == WORKSPACE
     assert lib.lowram_predictor_grad(1, 10, 8, 128, 128, 1, None, None, None, None, None, None, None, None, None, None,
                                      None, None) == INVALID
+
+
+def test_eviction_entry_points_and_batch_limit_check_arguments_on_the_host():
+    """Host-side checks of the attention mass and the eviction plan (shape, dtype, window, workspace, the plan's
+    budget) and of the per-call batch limit shared by the kernels with one grid row per sequence."""
+    import ctypes
+    lib = L.lib()
+    INVALID, UNSUPPORTED, WORKSPACE = 1, 3, 4
+    n = ctypes.c_size_t(0)
+    # attention mass: empty window, head ratio 3, head dim 96, bad dtype, batch above the grid limit
+    assert lib.lowram_attention_mass_workspace_size(2, 100, 0, 32, 8, 128, 1, ctypes.byref(n)) == INVALID
+    assert lib.lowram_attention_mass_workspace_size(2, 100, 4, 24, 8, 128, 1, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.lowram_attention_mass_workspace_size(2, 100, 4, 32, 8, 96, 1, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.lowram_attention_mass_workspace_size(2, 100, 4, 32, 8, 128, 7, ctypes.byref(n)) == INVALID
+    assert lib.lowram_attention_mass_workspace_size(65536, 100, 4, 32, 8, 128, 1, ctypes.byref(n)) == UNSUPPORTED
+    # bf16 scratch: the log-sum-exps, the chunks' (max, sum) pairs and the packed window queries
+    assert lib.lowram_attention_mass_workspace_size(4, 65536, 32, 32, 8, 128, 1, ctypes.byref(n)) == 0
+    assert n.value >= 4 * 4 * 32 * 32 + 2 * 4 * 8 * 128 * 128
+    bf16_bytes = n.value
+    assert lib.lowram_attention_mass_workspace_size(4, 65536, 32, 32, 8, 128, 0, ctypes.byref(n)) == 0
+    assert n.value >= 4 * 4 * 32 * 32 and n.value != bf16_bytes
+    assert lib.lowram_attention_mass(4, 100, 32, 32, 8, 128, 1, 0.0, None, None, None, None, 0, None) == WORKSPACE
+    ws = ctypes.create_string_buffer((1 << 21) + 256)
+    wsp = ctypes.c_void_p((ctypes.addressof(ws) + 255) & ~255)
+    assert lib.lowram_attention_mass(0, 100, 32, 32, 8, 128, 1, 0.0, None, None, None, wsp, 1 << 21, None) == 0
+    assert lib.lowram_attention_mass(2, 100, 4, 32, 8, 128, 1, 0.0, None, None, None, wsp, 1 << 21, None) == INVALID
+    # eviction plan: budget above T, forced tokens above the budget, workspace
+    assert lib.lowram_evict_plan_workspace_size(2, 100, ctypes.byref(n)) == 0
+    assert n.value >= 4 * 2 * 100
+    assert lib.lowram_evict_plan(2, 100, 4, 8, 101, None, None, wsp, n.value, None) == INVALID
+    assert lib.lowram_evict_plan(2, 100, 40, 40, 60, None, None, wsp, n.value, None) == INVALID
+    assert lib.lowram_evict_plan(2, 100, 4, 8, 50, None, None, None, 0, None) == WORKSPACE
+    # the batch limit on the other entry points with one grid row per sequence
+    assert lib.lowram_dense_workspace_size(65536, 100, 32, 8, 128, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.lowram_dense_workspace_size(65535, 100, 32, 8, 128, ctypes.byref(n)) == 0
