@@ -11,7 +11,8 @@
 //                     its query's logits over the tile's tokens into a running (max, sum of exp) and writes the
 //                     pair once per chunk of tiles (the reduction kernel in evict.cu folds the chunks);
 //   mass pass         A = K tile, B = Q_h tile: TMEM lane = token, column = query-head, so each thread sums
-//                     exp(logit - lse) over its token's row; sums over kv-heads accumulate in shared memory.
+//                     exp(logit - lse) over its token's row; sums over kv-heads (and the two column halves)
+//                     accumulate in shared memory.
 // The window queries are first packed per kv-head, zero-padded to a multiple of 128 rows, so that one 2D TMA
 // box is one operand tile.  K tiles come straight from the [B*T, H_kv, d] cache through a 3D TMA map (rows past
 // the sequence's end are masked; past the cache's end TMA fills zeros).
@@ -20,8 +21,9 @@
 // MMAs; the next step's K tile is in flight (two stages) while the current step multiplies and all eight warps
 // read TMEM: warp w takes lanes 32 (w % 4) .. + 31 and columns 64 (w / 4) .. + 63, so the two column halves of
 // a row keep separate partial results, combined once per chunk through shared memory.  Exponentials are base 2
-// on one fused multiply-add: exp(scale x - m) = 2^(x (scale log2 e) - m log2 e).  Every wait is bounded (tc_common.cuh): on a timeout the CTA sets LOWRAM_CHECK_TIMEOUT, waits for
-// what it issued, frees TMEM and returns.
+// on one fused multiply-add: exp(scale x - m) = 2^(x (scale log2 e) - m log2 e).  Every wait is bounded
+// (tc_common.cuh): on a timeout the CTA sets LOWRAM_CHECK_TIMEOUT, waits for what it issued, frees TMEM and
+// returns.
 #include "evict.h"
 #include "tc_common.cuh"
 
