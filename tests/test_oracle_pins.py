@@ -581,6 +581,26 @@ def test_attention_mass_matches_torch_softmax_and_sums_to_the_window():
     np.testing.assert_allclose(mass.sum(axis=1), W * H_q, atol=1e-10)
 
 
+def test_attention_mass_closed_form_and_head_grouping():
+    """kv-head 0 holds one key repeated, so its q-heads attend uniformly (1/T per token); kv-head 1 holds zero keys
+    except a large multiple of the shared direction u of its q-heads at token 5, so each of those rows puts
+    p5 = e^s / (e^s + T - 1) on token 5 and (1 - p5)/(T - 1) elsewhere.  A q-head to kv-head map other than
+    hq // g breaks the sum."""
+    W, H_q, H_kv, T, d = 2, 4, 2, 9, 8
+    g = H_q // H_kv
+    u = RNG.normal(0, 1, d)
+    q = RNG.normal(0, 1, (1, W, H_q, d))
+    q[0, :, 2:] = u                                           # kv-head 1's q-heads
+    k = np.zeros((1, T, H_kv, d))
+    k[0, :, 0] = RNG.normal(0, 1, d)
+    k[0, 5, 1] = 0.5 * u
+    s = 0.5 * (u @ u) * d ** -0.5
+    p5 = np.exp(s) / (np.exp(s) + T - 1)
+    want = np.full(T, W * g / T + W * g * (1 - p5) / (T - 1))
+    want[5] = W * g / T + W * g * p5
+    np.testing.assert_allclose(O.attention_mass(q, k)[0], want, rtol=1e-12)
+
+
 def test_evict_plan_keeps_sinks_recents_and_the_heaviest():
     T, n_sink, n_recent, T_keep = 30, 3, 5, 14
     mass = RNG.random((2, T))
