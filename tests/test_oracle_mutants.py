@@ -2,11 +2,14 @@
 
 Each case plants one mistake in a temporary copy of the oracle's C source (a flipped sign, a
 transposed operand, a dropped term, a wrong index, a reversed tie-break ...), builds it, and runs the
-pin suite against that build in a subprocess.  The suite must fail for every mutant.  Nothing here
-touches the real oracle build or a GPU.
+pin suite against that build in a subprocess.  The numpy parts of the oracle (the log-sum-exp merge,
+the basis fit, the predictor's gradient and Adam, the attention mass and the eviction plan) get the
+same treatment through a temporary copy of the oracle package that the subprocess imports first.  The
+suite must fail for every mutant.  Nothing here touches the real oracle build or a GPU.
 """
 import concurrent.futures as cf
 import os
+import shutil
 import subprocess
 import sys
 import tempfile
@@ -69,5 +72,55 @@ def test_every_planted_mistake_fails_a_pin():
     with tempfile.TemporaryDirectory() as tmp:
         with cf.ThreadPoolExecutor(max_workers=max(2, min(8, os.cpu_count() or 2))) as ex:
             results = list(ex.map(lambda kv: _run_mutant(kv[0], *kv[1], tmp), MUTANTS.items()))
+    survivors = [(n, out) for n, rc, out in results if rc == 0]
+    assert not survivors, "mutants not caught by any pin: " + ", ".join(n for n, _ in survivors)
+
+
+PY_SRC = os.path.join(ROOT, "oracle", "oracle.py")
+
+PY_MUTANTS = {
+    "merge_weight_sign": ("b = np.where(empty, 0.0, np.exp(lb - Wf))", "b = np.where(empty, 0.0, np.exp(Wf - lb))"),
+    "merge_lse_without_max": ("lse = np.where(empty, -np.inf, Wf + np.log(", "lse = np.where(empty, -np.inf, np.log("),
+    "basis_smallest_eigenvectors": ("order = np.argsort(w)[::-1][:r]", "order = np.argsort(w)[:r]"),
+    "basis_rope_not_inverted": ("K = rope_rows(K, np.broadcast_to(np.asarray(P)[:, :, None, None], (B, T, G, H_kv)), "
+                                "theta, inverse=True)",
+                                "K = rope_rows(K, np.broadcast_to(np.asarray(P)[:, :, None, None], (B, T, G, H_kv)), "
+                                "theta, inverse=False)"),
+    "basis_layer_blocks_reversed": ("[U[l * H_kv * d:(l + 1) * H_kv * d].copy() for l in range(G)]",
+                                    "[U[(G - 1 - l) * H_kv * d:(G - l) * H_kv * d].copy() for l in range(G)]"),
+    "grad_silu_derivative": ("dZ = (dV @ W2) * (S + Z * S * (1.0 - S))", "dZ = (dV @ W2) * (S * (1.0 - S))"),
+    "grad_factor_two_dropped": ("dV = 2.0 * E / (N * d)", "dV = E / (N * d)"),
+    "grad_b2_from_hidden": ("g_b2 = dV.sum(axis=0)", "g_b2 = dV.sum(axis=0) + H.sum(axis=0)[:d] * 0.0 + dV.mean(axis=0)"),
+    "adam_no_bias_correction": ("mh = m / (1.0 - beta1 ** step)", "mh = m"),
+    "adam_second_moment_unsquared": ("v = beta2 * v + (1.0 - beta2) * g * g", "v = beta2 * v + (1.0 - beta2) * np.abs(g)"),
+    "mass_interleaved_heads": ("s = (Q[b, :, hq] @ K[b, :, hq // g].T) * scale", "s = (Q[b, :, hq] @ K[b, :, hq % H_kv].T) * scale"),
+    "mass_softmax_over_window": ("mass[b] += (p / p.sum(axis=1, keepdims=True)).sum(axis=0)",
+                                 "mass[b] += (p / p.sum(axis=0, keepdims=True)).sum(axis=0)"),
+    "evict_ties_to_higher_index": ("key=lambda t: (-M[b, t], t))", "key=lambda t: (-M[b, t], -t))"),
+    "evict_recents_shifted": ("set(range(max(0, T - n_recent), T))", "set(range(max(0, T - n_recent - 1), T - 1))"),
+}
+
+
+def _run_py_mutant(name, find, repl, tmp, oracle_so):
+    src = open(PY_SRC).read()
+    assert src.count(find) == 1, f"mutation site of {name} not found once"
+    pkg = os.path.join(tmp, name, "oracle")
+    shutil.copytree(os.path.join(ROOT, "oracle"), pkg, ignore=shutil.ignore_patterns("*.so", "__pycache__"))
+    open(os.path.join(pkg, "oracle.py"), "w").write(src.replace(find, repl))
+    env = dict(os.environ, LOWRAM_ORACLE_LIB=oracle_so, OMP_NUM_THREADS="1",
+               PYTHONPATH=os.pathsep.join([os.path.dirname(pkg), ROOT]))
+    # run from the copy's folder, so that `import oracle` finds the mutant before the real package
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")], cwd=os.path.dirname(pkg), env=env,
+                       capture_output=True, text=True, timeout=600)
+    return name, r.returncode, r.stdout[-400:]
+
+
+def test_every_planted_mistake_in_the_numpy_oracle_fails_a_pin():
+    import oracle
+    so = oracle.build()
+    with tempfile.TemporaryDirectory() as tmp:
+        with cf.ThreadPoolExecutor(max_workers=max(2, min(8, os.cpu_count() or 2))) as ex:
+            results = list(ex.map(lambda kv: _run_py_mutant(kv[0], *kv[1], tmp, so), PY_MUTANTS.items()))
     survivors = [(n, out) for n, rc, out in results if rc == 0]
     assert not survivors, "mutants not caught by any pin: " + ", ".join(n for n, _ in survivors)
