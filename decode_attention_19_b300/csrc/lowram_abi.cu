@@ -1,5 +1,6 @@
 // lowram_abi.cu -- the C ABI of liblowram.so: argument and alignment checks, workspace carving,
 // and the launch sequence of each call.  See include/lowram.h for the contract of every entry point.
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -34,10 +35,16 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 bool is_act(int dt) { return dt == LOWRAM_F32 || dt == LOWRAM_BF16; }
 
-// Kernels that give each sequence its own grid row (y or z) take at most 65535 sequences per call.
+// Kernels that give each sequence its own grid row (y or z) take at most 65535 sequences per call, and token
+// rows b*T + t are 32-bit TMA coordinates and loop indices, so B*T stays below 2^31.
 constexpr int32_t kMaxGridRows = 65535;
 lowram_status check_grid_rows(int32_t B) {
     return B > kMaxGridRows ? fail(LOWRAM_ERR_UNSUPPORTED, "B=%d > %d sequences per call", B, kMaxGridRows) : LOWRAM_OK;
+}
+lowram_status check_token_rows(int32_t B, int32_t T) {
+    return (int64_t)B * T > (int64_t)INT32_MAX
+               ? fail(LOWRAM_ERR_UNSUPPORTED, "B*T=%lld token rows per call (below 2^31)", (long long)B * T)
+               : LOWRAM_OK;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -47,7 +54,7 @@ lowram_status check_decode_shape(const lowram_decode_shape* s) {
     if (!s) return fail(LOWRAM_ERR_INVALID_ARG, "shape is NULL");
     if (s->B < 0 || s->T < 0 || s->S < 0 || s->n_res < 0)
         return fail(LOWRAM_ERR_INVALID_ARG, "negative size (B=%d T=%d S=%d n_res=%d)", s->B, s->T, s->S, s->n_res);
-    if (check_grid_rows(s->B) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
+    if (check_grid_rows(s->B) != LOWRAM_OK || check_token_rows(s->B, s->T) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
     if (s->H_kv < 1 || s->H_q < 1 || s->H_q % s->H_kv != 0)
         return fail(LOWRAM_ERR_INVALID_ARG, "H_q=%d must be a positive multiple of H_kv=%d", s->H_q, s->H_kv);
     if (s->H_q / s->H_kv > 8) return fail(LOWRAM_ERR_UNSUPPORTED, "H_q/H_kv=%d > 8", s->H_q / s->H_kv);
@@ -287,7 +294,7 @@ static lowram_status check_compress_shape(const lowram_compress_shape* s) {
     if (!s) return fail(LOWRAM_ERR_INVALID_ARG, "shape is NULL");
     if (s->B < 0 || s->T < 0 || s->n_res < 0 || s->n_res > s->T)
         return fail(LOWRAM_ERR_INVALID_ARG, "bad sizes (B=%d T=%d n_res=%d)", s->B, s->T, s->n_res);
-    if (check_grid_rows(s->B) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
+    if (check_grid_rows(s->B) != LOWRAM_OK || check_token_rows(s->B, s->T) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
     if (s->G < 1 || s->G > 16) return fail(LOWRAM_ERR_UNSUPPORTED, "G=%d (1..16)", s->G);
     if (s->H_kv < 1) return fail(LOWRAM_ERR_INVALID_ARG, "H_kv=%d", s->H_kv);
     if (s->d != 64 && s->d != 128) return fail(LOWRAM_ERR_UNSUPPORTED, "d=%d (64 or 128 supported)", s->d);
@@ -308,7 +315,7 @@ static lowram_status check_compress_shape(const lowram_compress_shape* s) {
 static lowram_status check_mass_shape(int32_t B, int32_t T, int32_t W, int32_t H_q, int32_t H_kv, int32_t d) {
     if (B < 0 || T < 0 || W < 1 || H_kv < 1 || H_q < 1 || H_q % H_kv != 0)
         return fail(LOWRAM_ERR_INVALID_ARG, "B=%d T=%d W=%d H_q=%d H_kv=%d", B, T, W, H_q, H_kv);
-    if (check_grid_rows(B) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
+    if (check_grid_rows(B) != LOWRAM_OK || check_token_rows(B, T) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
     const int g = H_q / H_kv;
     if (g != 1 && g != 2 && g != 4 && g != 7 && g != 8) return fail(LOWRAM_ERR_UNSUPPORTED, "H_q/H_kv=%d", g);
     if (d != 64 && d != 128) return fail(LOWRAM_ERR_UNSUPPORTED, "d=%d (64 or 128 supported)", d);
@@ -377,6 +384,7 @@ lowram_status lowram_evict_plan(int32_t B, int32_t T, int32_t n_sink, int32_t n_
 // ------------------------------------------------------------------------------------------------
 static lowram_status check_predictor_shape(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m, int32_t dtype) {
     if (B < 0 || T < 0 || H_kv < 1) return fail(LOWRAM_ERR_INVALID_ARG, "B=%d T=%d H_kv=%d", B, T, H_kv);
+    if (check_token_rows(B, T) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
     if (d != 64 && d != 128) return fail(LOWRAM_ERR_UNSUPPORTED, "d=%d (64 or 128 supported)", d);
     if (m < 32 || m % 32 != 0 || m > 256) return fail(LOWRAM_ERR_UNSUPPORTED, "m=%d", m);
     if (!is_act(dtype)) return fail(LOWRAM_ERR_INVALID_ARG, "dtype=%d", dtype);
@@ -466,6 +474,7 @@ lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d
 static lowram_status check_fit_shape(const lowram_compress_shape* s) {
     if (!s) return fail(LOWRAM_ERR_INVALID_ARG, "shape is NULL");
     if (s->B < 0 || s->T < 0) return fail(LOWRAM_ERR_INVALID_ARG, "bad sizes (B=%d T=%d)", s->B, s->T);
+    if (check_token_rows(s->B, s->T) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
     if (s->G < 1 || s->G > 16) return fail(LOWRAM_ERR_UNSUPPORTED, "G=%d (1..16)", s->G);
     if (s->H_kv < 1) return fail(LOWRAM_ERR_INVALID_ARG, "H_kv=%d", s->H_kv);
     if (s->d != 64 && s->d != 128) return fail(LOWRAM_ERR_UNSUPPORTED, "d=%d (64 or 128 supported)", s->d);
@@ -602,7 +611,7 @@ lowram_status lowram_compress(const lowram_compress_shape* shape, const void* ke
 lowram_status lowram_dense_workspace_size(int32_t B, int32_t T, int32_t H_q, int32_t H_kv, int32_t d, size_t* bytes) {
     if (B < 0 || T < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv || (d != 64 && d != 128) || !bytes)
         return fail(LOWRAM_ERR_INVALID_ARG, "bad dense shape");
-    if (check_grid_rows(B) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
+    if (check_grid_rows(B) != LOWRAM_OK || check_token_rows(B, T) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
     const int nr = dense_records(B, T, H_kv, d, LOWRAM_BF16);
     *bytes = kHeader + align256(sizeof(float) * (size_t)B * H_q * nr * (d + 2));
     return LOWRAM_OK;

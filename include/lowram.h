@@ -33,8 +33,9 @@
  *     workspace that lowram_get_error() reads and clears.  No kernel waits on another CTA.
  *   - q-head hq reads kv-head hq / (H_q / H_kv).
  *   - Calls over B sequences that give each sequence its own grid row (decode, compress, the
- *     comparator and the exact tail's attention, the attention mass) take B <= 65535 per call
- *     (LOWRAM_ERR_UNSUPPORTED otherwise); split larger batches into several calls.
+ *     comparator and the exact tail's attention, the attention mass) take B <= 65535 per call, and
+ *     calls over B*T token rows take B*T < 2^31 (LOWRAM_ERR_UNSUPPORTED otherwise); split larger
+ *     batches into several calls.
  */
 #ifndef LOWRAM_H
 #define LOWRAM_H

@@ -179,3 +179,8 @@ def test_eviction_entry_points_and_batch_limit_check_arguments_on_the_host():
     # the batch limit on the other entry points with one grid row per sequence
     assert lib.lowram_dense_workspace_size(65536, 100, 32, 8, 128, ctypes.byref(n)) == UNSUPPORTED
     assert lib.lowram_dense_workspace_size(65535, 100, 32, 8, 128, ctypes.byref(n)) == 0
+    # and on the token rows: B*T below 2^31
+    assert lib.lowram_attention_mass_workspace_size(2, 1 << 30, 1, 8, 8, 64, 1, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.lowram_fit_predictor_workspace_size(8, 128, 128, ctypes.byref(n)) == 0
+    assert lib.lowram_predictor_grad(2, 1 << 30, 8, 128, 128, 1, None, None, None, None, None, None, None, None, None,
+                                     None, None, None) == UNSUPPORTED
