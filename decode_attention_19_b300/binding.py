@@ -38,6 +38,33 @@ class LowramError(RuntimeError):
         self.status = status
 
 
+class LowramShapeError(ValueError):
+    """A tensor is smaller than the layout its call reads or writes, or holds elements of another size.  The C
+    entry points see pointers and sizes only, so the binding checks every buffer against the sizes it passes."""
+
+
+_ESZ = {LOWRAM_F32: 4, LOWRAM_BF16: 2}
+
+
+def _need(name: str, t: Optional[torch.Tensor], numel: int, itemsize: int):
+    """t (if given) holds at least `numel` elements of `itemsize` bytes."""
+    if t is None:
+        return
+    if t.element_size() != itemsize:
+        raise LowramShapeError(f"{name}: elements of {itemsize} bytes expected, got {t.dtype}")
+    if t.numel() < numel:
+        raise LowramShapeError(f"{name}: at least {numel} elements expected, got shape {tuple(t.shape)}")
+
+
+def _need_list(name: str, ts, n: int, numel: int, itemsize: int):
+    if ts is None:
+        return
+    if len(ts) != n:
+        raise LowramShapeError(f"{name}: {n} tensors expected, got {len(ts)}")
+    for i, t in enumerate(ts):
+        _need(f"{name}[{i}]", t, numel, itemsize)
+
+
 _lib = None
 _vp = ctypes.c_void_p
 
@@ -155,6 +182,35 @@ def decode_shape(q, coef, w1, *, S: int, n_res: int, max_pos: int, res_dtype: in
                                float(sm_scale))
 
 
+def _check_decode_buffers(s: lowram_decode_shape, *, q, coef, coef_scale, pos, rope_cos, rope_sin, basis, w1, w2,
+                          b1, b2, res_idx, res_val, res_scale, out, lse, sel_out=None, key_out=None):
+    B, T, H_q, H_kv, d, r, m = s.B, s.T, s.H_q, s.H_kv, s.d, s.r, s.m
+    act = _ESZ[s.act_dtype]
+    _need("q", q, B * H_q * d, act)
+    if s.coef_dtype == LOWRAM_INT4_G32:
+        _need("coef", coef, B * T * r // 2, 1)
+        if coef_scale is None:
+            raise LowramShapeError("coef_scale is required for int4 coefficients")
+        _need("coef_scale", coef_scale, B * T * r // 32, 2)
+    else:
+        _need("coef", coef, B * T * r, _ESZ[s.coef_dtype])
+    _need("pos", pos, B * T, 4)
+    _need("rope_cos", rope_cos, d // 2 * s.max_pos, 4)
+    _need("rope_sin", rope_sin, d // 2 * s.max_pos, 4)
+    _need("basis", basis, H_kv * d * r, act)
+    _need("w1", w1, H_kv * m * d, act)
+    _need("w2", w2, H_kv * d * m, act)
+    _need("b1", b1, H_kv * m, 4)
+    _need("b2", b2, H_kv * d, 4)
+    _need("res_idx", res_idx, B * H_kv * s.n_res, 4)
+    _need("res_val", res_val, B * H_kv * s.n_res * d, 1 if s.res_dtype == LOWRAM_INT8_VEC else _ESZ[s.res_dtype])
+    _need("res_scale", res_scale, B * H_kv * s.n_res, 2)
+    _need("out", out, B * H_q * d, 4)
+    _need("lse", lse, B * H_q, 4)
+    _need("sel_out", sel_out, B * H_kv * min(s.S, T), 4)
+    _need("key_out", key_out, B * H_kv * T, 4)
+
+
 def lowram_decode_uses_tensor_cores(shape: lowram_decode_shape) -> bool:
     y = ctypes.c_int32(0)
     _check(_load().lowram_decode_uses_tensor_cores(ctypes.byref(shape), ctypes.byref(y)))
@@ -195,6 +251,9 @@ def lowram_decode_attn(q: torch.Tensor, coef: torch.Tensor, basis: torch.Tensor,
         res_dtype = _act(res_val)
     shape = decode_shape(q, coef, w1, S=S, n_res=n_res, max_pos=rope_cos.shape[1], res_dtype=res_dtype,
                          sm_scale=sm_scale, coef_int4=coef_int4)
+    _check_decode_buffers(shape, q=q, coef=coef, coef_scale=coef_scale, pos=pos, rope_cos=rope_cos, rope_sin=rope_sin,
+                          basis=basis, w1=w1, w2=w2, b1=b1, b2=b2, res_idx=res_idx, res_val=res_val,
+                          res_scale=res_scale, out=out, lse=lse, sel_out=sel_out, key_out=key_out)
     _dev(q, coef, basis, w1, w2, rope_cos, rope_sin, coef_scale, pos, b1, b2, res_idx, res_val, res_scale)
     B, H_q, d = q.shape
     dev = q.device
@@ -234,6 +293,11 @@ def lowram_decode_attn_static(q: torch.Tensor, coef: torch.Tensor, basis: torch.
         res_dtype = _act(res_val)
     shape = decode_shape(q, coef, w1, S=S, n_res=n_res, max_pos=rope_cos.shape[1], res_dtype=res_dtype,
                          sm_scale=sm_scale, coef_int4=coef_int4)
+    if out is None:
+        raise LowramShapeError("out is required (this call allocates nothing)")
+    _check_decode_buffers(shape, q=q, coef=coef, coef_scale=coef_scale, pos=pos, rope_cos=rope_cos, rope_sin=rope_sin,
+                          basis=basis, w1=w1, w2=w2, b1=b1, b2=b2, res_idx=res_idx, res_val=res_val,
+                          res_scale=res_scale, out=out, lse=lse)
     _dev(q, coef, basis, w1, w2, rope_cos, rope_sin, coef_scale, pos, b1, b2, res_idx, res_val, res_scale, out, lse)
     _check(_load().lowram_decode_attn_static(ctypes.byref(shape), _p(q), _p(coef), _p(coef_scale), _p(pos),
                                              _p(rope_cos), _p(rope_sin), _p(basis), _p(w1), _p(w2), _p(b1), _p(b2),
@@ -271,6 +335,18 @@ def lowram_compress(keys: torch.Tensor, values: Sequence[torch.Tensor], proj: to
     dev = keys.device
     shape = lowram_compress_shape(B, T, G, H_kv, d, r, m, int(n_res), _act(keys), int(coef_dtype), int(res_dtype),
                                   int(bool(keys_post_rope)), 0 if rope_cos is None else rope_cos.shape[1])
+    act = _ESZ[_act(keys)]
+    D = G * H_kv * d
+    _need_list("values", values, G, B * T * H_kv * d, act)
+    _need("proj", proj, r * D, 4)
+    _need("pos", pos, B * T, 4)
+    _need("rope_cos", rope_cos, d // 2 * shape.max_pos, 4)
+    _need("rope_sin", rope_sin, d // 2 * shape.max_pos, 4)
+    _need_list("bases", bases, G, H_kv * d * r, act)
+    _need_list("w1s", w1s, G, H_kv * m * d, act)
+    _need_list("w2s", w2s, G, H_kv * d * m, act)
+    _need_list("b1s", b1s, G, H_kv * m, 4)
+    _need_list("b2s", b2s, G, H_kv * d, 4)
     _dev(keys, proj, pos, rope_cos, rope_sin, *values, *bases, *w1s, *w2s)
     if coef_dtype == LOWRAM_INT4_G32:
         coef = torch.empty((B, T, r // 2), dtype=torch.uint8, device=dev)
@@ -315,6 +391,11 @@ def lowram_dense_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     """Plain decode attention over explicit rotated K and V [B,T,H_kv,d]; q [B,H_q,d].  Returns (out, lse)."""
     B, H_q, d = q.shape
     T, H_kv = k.shape[1], k.shape[2]
+    act = _ESZ[_act(q)]
+    _need("k", k, B * T * H_kv * d, act)
+    _need("v", v, B * T * H_kv * d, act)
+    _need("out", out, B * H_q * d, 4)
+    _need("lse", lse, B * H_q, 4)
     _dev(q, k, v)
     dev = q.device
     if out is None:
@@ -335,6 +416,9 @@ def lowram_attention_mass(q_win: torch.Tensor, k: torch.Tensor, *, sm_scale: flo
     """Attention mass [B, T] of every prompt token from the window queries q_win [B, W, H_q, d] (k [B, T, H_kv, d])."""
     B, W, H_q, d = q_win.shape
     T, H_kv = k.shape[1], k.shape[2]
+    if q_win.dtype != k.dtype:
+        raise TypeError("q_win and k must share one dtype")
+    _need("k", k, B * T * H_kv * d, _ESZ[_act(k)])
     _dev(q_win, k)
     n = ctypes.c_size_t(0)
     _check(_load().lowram_attention_mass_workspace_size(B, T, W, H_q, H_kv, d, _act(k), ctypes.byref(n)))
@@ -373,14 +457,20 @@ def _pred_dims(keys, values, w1, w2):
     return B, T, H_kv, d, m
 
 
-def lowram_predictor_grad(keys: torch.Tensor, values: torch.Tensor, w1: torch.Tensor, b1: torch.Tensor,
-                          w2: torch.Tensor, b2: torch.Tensor):
-    """Loss [H_kv] and gradient (g_w1, g_b1, g_w2, g_b2) of every head's predictor; parameters float32."""
-    B, T, H_kv, d, m = _pred_dims(keys, values, w1, w2)
+def _pred_params(H_kv, d, m, w1, b1, w2, b2):
     for t in (w1, b1, w2, b2):
         _dev(t)
         if t.dtype != torch.float32:
             raise TypeError("predictor parameters are float32")
+    _need("b1", b1, H_kv * m, 4)
+    _need("b2", b2, H_kv * d, 4)
+
+
+def lowram_predictor_grad(keys: torch.Tensor, values: torch.Tensor, w1: torch.Tensor, b1: torch.Tensor,
+                          w2: torch.Tensor, b2: torch.Tensor):
+    """Loss [H_kv] and gradient (g_w1, g_b1, g_w2, g_b2) of every head's predictor; parameters float32."""
+    B, T, H_kv, d, m = _pred_dims(keys, values, w1, w2)
+    _pred_params(H_kv, d, m, w1, b1, w2, b2)
     loss = torch.empty(H_kv, dtype=torch.float32, device=keys.device)
     g = [torch.empty_like(t) for t in (w1, b1, w2, b2)]
     _check(_load().lowram_predictor_grad(B, T, H_kv, d, m, _act(keys), _p(keys), _p(values), _p(w1), _p(b1), _p(w2),
@@ -395,10 +485,7 @@ def lowram_fit_predictor(keys: torch.Tensor, values: torch.Tensor, w1: torch.Ten
     """`steps` full-batch Adam steps on every head's predictor, parameters (float32) updated in place.
     Returns the losses [steps, H_kv] before each step (or None)."""
     B, T, H_kv, d, m = _pred_dims(keys, values, w1, w2)
-    for t in (w1, b1, w2, b2):
-        _dev(t)
-        if t.dtype != torch.float32:
-            raise TypeError("predictor parameters are float32")
+    _pred_params(H_kv, d, m, w1, b1, w2, b2)
     n = ctypes.c_size_t(0)
     _check(_load().lowram_fit_predictor_workspace_size(H_kv, d, m, ctypes.byref(n)))
     ws = _workspace(n.value, workspace, keys.device)
@@ -419,9 +506,12 @@ def lowram_fit_basis(keys: torch.Tensor, r: int, *, pos: Optional[torch.Tensor] 
     """keys [B, T, G, H_kv, d] -> (proj [r, G*H_kv*d] float32, bases G x [H_kv*d, r] in keys' dtype, workspace)."""
     B, T, G, H_kv, d = keys.shape
     dev = keys.device
-    _dev(keys, pos, rope_cos, rope_sin)
     shape = lowram_compress_shape(B, T, G, H_kv, d, int(r), 32, 0, _act(keys), LOWRAM_BF16, LOWRAM_BF16,
                                   int(bool(keys_post_rope)), 0 if rope_cos is None else rope_cos.shape[1])
+    _need("pos", pos, B * T, 4)
+    _need("rope_cos", rope_cos, d // 2 * shape.max_pos, 4)
+    _need("rope_sin", rope_sin, d // 2 * shape.max_pos, 4)
+    _dev(keys, pos, rope_cos, rope_sin)
     n = ctypes.c_size_t(0)
     _check(_load().lowram_fit_basis_workspace_size(ctypes.byref(shape), ctypes.byref(n)))
     ws = _workspace(n.value, workspace, dev)
@@ -456,6 +546,11 @@ def lowram_tail_decode_attn(q: torch.Tensor, tail_k: torch.Tensor, tail_v: torch
     """Attention of q [B, H_q, d] over the first t_len rows of the tail buffers, read in place.  Returns (out, lse)."""
     B, H_q, d = q.shape
     T_cap, H_kv = tail_k.shape[1], tail_k.shape[2]
+    act = _ESZ[_act(q)]
+    _need("tail_k", tail_k, B * T_cap * H_kv * d, act)
+    _need("tail_v", tail_v, B * T_cap * H_kv * d, act)
+    _need("out", out, B * H_q * d, 4)
+    _need("lse", lse, B * H_q, 4)
     _dev(q, tail_k, tail_v)
     dev = q.device
     if out is None:
@@ -474,10 +569,15 @@ def lowram_merge_attn(out_a: torch.Tensor, lse_a: torch.Tensor, out_b: torch.Ten
     """Merge two attention results over disjoint token sets through their log-sum-exp.  Returns (out, lse);
     out / lse may be given as out_a / lse_a for an in-place merge."""
     B, H_q, d = out_a.shape
-    _dev(out_a, lse_a, out_b, lse_b)
     for t in (out_a, lse_a, out_b, lse_b):
         if t.dtype != torch.float32:
             raise TypeError("merge operands are float32")
+    _need("lse_a", lse_a, B * H_q, 4)
+    _need("out_b", out_b, B * H_q * d, 4)
+    _need("lse_b", lse_b, B * H_q, 4)
+    _need("out", out, B * H_q * d, 4)
+    _need("lse", lse, B * H_q, 4)
+    _dev(out_a, lse_a, out_b, lse_b, out, lse)
     if out is None:
         out = torch.empty_like(out_a)
     if lse is None:
