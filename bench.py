@@ -662,7 +662,8 @@ def fit_bench(w, dev, args, pk):
     err = float(torch.linalg.norm(Kf - (Kf @ P.T) @ P) / torch.linalg.norm(Kf))
     it = args.fit_iters + 1          # iterations plus the final Cholesky QR
     flops = N * D * D + args.fit_iters * 2.0 * D * D * r + it * (4.0 * D * r * r + 2.0 * r ** 3 / 3.0)
-    # bf16: both passes stream K through the tensor cores, so the mass is HBM-bound (K read twice)
+    peak_tf = NOMINAL_SM * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
     print(json.dumps({
         "metric": "fitted key basis: time per layer group", "value": ms, "unit": "ms", "higher_is_better": False,
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
@@ -695,7 +696,8 @@ def fit_predictor_bench(w, dev, args, pk):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
     flops = 10.0 * B * T * d * m * H_kv            # forward (2 products), backward (3 products), 2 FLOP per MAC
-    # bf16: both passes stream K through the tensor cores, so the mass is HBM-bound (K read twice)
+    peak_tf = NOMINAL_SM * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
     ls = losses.float().cpu().numpy()
     print(json.dumps({
         "metric": "predictor fit: time per Adam step per layer", "value": ms, "unit": "ms", "higher_is_better": False,
