@@ -671,7 +671,7 @@ def fit_bench(w, dev, args, pk):
                    "iters": args.fit_iters, "keys": "bf16, rank r (spectrum 10..1) + 0.05 noise"},
         "rebuild_rel_err_sampled": err,
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf,
+                     "frac": achieved / peak_tf, "traffic": None,
                      "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock",
                      "work": "Gram N*D^2 (symmetric) + per iteration 2*D^2*r + 4*D*r^2 + 2r^3/3"}}))
 
@@ -705,7 +705,7 @@ def fit_predictor_bench(w, dev, args, pk):
         "config": {"workload": w.name, "B": B, "T": T, "H_kv": H_kv, "d": d, "m": m, "inputs": "bf16 keys/values"},
         "loss_first_last": [float(ls[0].mean()), float(ls[-1].mean())],
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf,
+                     "frac": achieved / peak_tf, "traffic": None,
                      "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock",
                      "work": "10 * B*T * d * m * H_kv per step"}}))
 
