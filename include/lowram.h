@@ -24,7 +24,9 @@
  *   - Tensor pointers are DEVICE pointers owned by the caller, row-major and contiguous, 16-byte
  *     aligned (LOWRAM_ERR_ALIGNMENT otherwise).  Arrays of pointers (one per layer of a group) are
  *     HOST arrays holding device pointers.  The library allocates no device memory: scratch comes
- *     from the caller's workspace, sized by the matching *_workspace_size query.
+ *     from the caller's workspace, sized by the matching *_workspace_size query.  The library sees
+ *     pointers and sizes only, never buffer extents: every buffer must hold at least the layout its
+ *     argument documents (the Python binding checks element counts and sizes before each call).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Calls enqueue
  *     work on it and return without synchronising, after checking their arguments on the host.
  *   - Errors are return codes; no C++ exception crosses the ABI.  lowram_last_error() gives a
