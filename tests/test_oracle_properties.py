@@ -8,7 +8,9 @@ lengths and selections at or above T:
   - the log-sum-exp merge is commutative and associative, including empty sets (lse = -inf);
   - the attention mass is non-negative and each sequence's mass sums to W * H_q;
   - the eviction plan holds exactly T_keep ascending tokens, every sink and recent token, and no dropped token
-    outweighs a kept one (equal weights go to the lower index).
+    outweighs a kept one (equal weights go to the lower index);
+  - the int4 and int8 quantisers stay within half a step of their input at magnitudes from 1e-3 to 1e4, keep their
+    codes in range, take their scales from the group's (vector's) largest entry, and map an all-zero group to 0.
 """
 import numpy as np
 import pytest
@@ -114,3 +116,31 @@ def test_evict_plan_keeps_the_forced_and_the_heaviest(T, data):
     for t in kept_free:
         for u in dropped:
             assert (mass[0, t], -t) > (mass[0, u], -u)        # heavier, or as heavy and earlier
+
+
+@SETTINGS
+@given(st.integers(1, 6), st.sampled_from([32, 64, 128]), st.floats(-3, 4), st.integers(0, 2 ** 31 - 1))
+def test_int4_quantiser_bound_range_and_zero_groups(rows, r, log_mag, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(0, 10.0 ** log_mag, (rows, r))
+    x[0, :32] = 0.0                                          # an all-zero group: scale 0, codes 0
+    packed, scales = O.quant_int4_g32(x)
+    deq = O.dequant_int4_g32(packed, scales)
+    s = np.repeat(scales, 32, axis=1)
+    assert scales[0, 0] == 0 and np.all(deq[0, :32] == 0)
+    assert np.all(np.abs(x - deq) <= s / 2 * (1 + 1e-3) + 1e-300)
+    nz = s > 0
+    assert np.all(np.abs(np.round(deq[nz] / s[nz])) <= 7)
+    amax = np.abs(x).reshape(rows, r // 32, 32).max(-1)
+    np.testing.assert_array_equal(scales, np.float16(amax / 7).astype(np.float64))
+
+
+@SETTINGS
+@given(st.integers(1, 6), st.sampled_from([64, 128]), st.floats(-3, 4), st.integers(0, 2 ** 31 - 1))
+def test_int8_quantiser_bound_and_range(rows, d, log_mag, seed):
+    x = np.random.default_rng(seed).normal(0, 10.0 ** log_mag, (rows, d))
+    codes, sc = O.quant_int8_vec(x)
+    deq = O.dequant_int8_vec(codes, sc)
+    assert np.abs(codes.astype(int)).max() <= 127
+    assert np.all(np.abs(x - deq) <= sc[:, None] / 2 * (1 + 1e-3) + 1e-300)
+    np.testing.assert_array_equal(sc, np.float16(np.abs(x).max(axis=1) / 127).astype(np.float64))
