@@ -720,20 +720,29 @@ def evict_bench(w, dev, args, pk):
     k = torch.randn((w.B, Tn, w.H_kv, w.d), generator=g, device=dev).to(torch.bfloat16)
     n_sink, n_recent = 64, min(2048, Tn // 4)
     T_keep = max(w.T, n_sink + n_recent) if w.T < Tn else Tn // 4 + n_sink + n_recent
+    # workspaces allocated once, outside the timed region (the calls would otherwise allocate them each time)
+    B_, W_, H_q_, d_ = q.shape
+    ws_mass = torch.zeros(L.lowram_attention_mass_workspace_size(B_, Tn, W_, H_q_, w.H_kv, d_, L.LOWRAM_BF16),
+                          dtype=torch.uint8, device=dev)
+    ws_plan = torch.zeros(L.lowram_evict_plan_workspace_size(w.B, Tn), dtype=torch.uint8, device=dev)
+
+    def plan():
+        return L.lowram_evict_plan(L.lowram_attention_mass(q, k, workspace=ws_mass), n_sink=n_sink,
+                                   n_recent=n_recent, T_keep=T_keep, workspace=ws_plan)
     for _ in range(max(1, args.warmup)):
-        keep = L.lowram_evict_plan(L.lowram_attention_mass(q, k), n_sink=n_sink, n_recent=n_recent, T_keep=T_keep)
+        keep = plan()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in ev:
         a.record()
-        keep = L.lowram_evict_plan(L.lowram_attention_mass(q, k), n_sink=n_sink, n_recent=n_recent, T_keep=T_keep)
+        keep = plan()
         b.record()
     torch.cuda.synchronize()
     ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
     em = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in em:
         a.record()
-        L.lowram_attention_mass(q, k)
+        L.lowram_attention_mass(q, k, workspace=ws_mass)
         b.record()
     torch.cuda.synchronize()
     mass_ms = float(np.median([a.elapsed_time(b) for a, b in em]))

@@ -10,5 +10,5 @@ from .binding import (  # noqa: F401
     lowram_decode_attn, lowram_decode_attn_static, lowram_decode_shape, lowram_decode_uses_tensor_cores, lowram_compress_shape, lowram_decode_workspace_size,
     lowram_dense_decode_attn, lowram_dense_workspace_size, lowram_merge_attn, lowram_tail_append,
     lowram_tail_decode_attn, lowram_fit_basis, lowram_predictor_grad, lowram_fit_predictor,
-    lowram_attention_mass, lowram_evict_plan, lowram_get_error, lowram_rope_table, lowram_version,
+    lowram_attention_mass, lowram_evict_plan, lowram_attention_mass_workspace_size, lowram_evict_plan_workspace_size, lowram_get_error, lowram_rope_table, lowram_version,
 )

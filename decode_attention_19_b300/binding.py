@@ -411,6 +411,18 @@ def lowram_dense_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
 # ------------------------------------------------------------------------------------------------
 # heavy hitters from accumulated attention: the tokens an evicted cache keeps
 # ------------------------------------------------------------------------------------------------
+def lowram_attention_mass_workspace_size(B: int, T: int, W: int, H_q: int, H_kv: int, d: int, dtype: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_load().lowram_attention_mass_workspace_size(B, T, W, H_q, H_kv, d, int(dtype), ctypes.byref(n)))
+    return int(n.value)
+
+
+def lowram_evict_plan_workspace_size(B: int, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_load().lowram_evict_plan_workspace_size(B, T, ctypes.byref(n)))
+    return int(n.value)
+
+
 def lowram_attention_mass(q_win: torch.Tensor, k: torch.Tensor, *, sm_scale: float = 0.0,
                           workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Attention mass [B, T] of every prompt token from the window queries q_win [B, W, H_q, d] (k [B, T, H_kv, d])."""
@@ -420,9 +432,7 @@ def lowram_attention_mass(q_win: torch.Tensor, k: torch.Tensor, *, sm_scale: flo
         raise TypeError("q_win and k must share one dtype")
     _need("k", k, B * T * H_kv * d, _ESZ[_act(k)])
     _dev(q_win, k)
-    n = ctypes.c_size_t(0)
-    _check(_load().lowram_attention_mass_workspace_size(B, T, W, H_q, H_kv, d, _act(k), ctypes.byref(n)))
-    ws = _workspace(n.value, workspace, k.device)
+    ws = _workspace(lowram_attention_mass_workspace_size(B, T, W, H_q, H_kv, d, _act(k)), workspace, k.device)
     mass = torch.empty((B, T), dtype=torch.float32, device=k.device)
     _check(_load().lowram_attention_mass(B, T, W, H_q, H_kv, d, _act(k), float(sm_scale), _p(q_win), _p(k), _p(mass),
                                          _p(ws), ws.numel() * ws.element_size(), _stream()))
@@ -434,9 +444,7 @@ def lowram_evict_plan(mass: torch.Tensor, *, n_sink: int, n_recent: int, T_keep:
     """Kept token indices [B, T_keep] (ascending): sinks, recents and the heaviest others by mass [B, T]."""
     B, T = mass.shape
     _dev(mass)
-    n = ctypes.c_size_t(0)
-    _check(_load().lowram_evict_plan_workspace_size(B, T, ctypes.byref(n)))
-    ws = _workspace(n.value, workspace, mass.device)
+    ws = _workspace(lowram_evict_plan_workspace_size(B, T), workspace, mass.device)
     keep = torch.empty((B, int(T_keep)), dtype=torch.int32, device=mass.device)
     _check(_load().lowram_evict_plan(B, T, int(n_sink), int(n_recent), int(T_keep), _p(mass), _p(keep), _p(ws),
                                      ws.numel() * ws.element_size(), _stream()))
