@@ -4,6 +4,52 @@ workspaces with torch, and passes raw device pointers and the current CUDA strea
 
 The functions carry the names of the C entry points in include/lowram.h.  If the library is not
 built the first call raises (there is no other implementation to fall back to).
+
+Example: one layer group of a prefilled prompt, then a decode step (all tensors on the GPU; shapes as in
+include/lowram.h)::
+
+    import torch
+    import decode_attention_19_b300 as L
+
+    B, T, G, H_q, H_kv, d, r, m = 2, 2048, 4, 32, 8, 128, 512, 128
+    dev, bf = "cuda", torch.bfloat16
+    keys = torch.randn(B, T, G, H_kv, d, device=dev).to(bf)            # the G layers' pre-RoPE keys
+    values = [torch.randn(B, T, H_kv, d, device=dev).to(bf) for _ in range(G)]
+
+    # fit the group's shared key basis, and each layer's value predictor (float32 master copies)
+    proj, bases, _ = L.lowram_fit_basis(keys, r)
+    W1, B1, W2, B2 = [], [], [], []
+    for l in range(G):
+        w1, b1 = torch.randn(H_kv, m, d, device=dev) * d ** -0.5, torch.zeros(H_kv, m, device=dev)
+        w2, b2 = torch.randn(H_kv, d, m, device=dev) * m ** -0.5, torch.zeros(H_kv, d, device=dev)
+        L.lowram_fit_predictor(keys[:, :, l].contiguous(), values[l], w1, b1, w2, b2, steps=50, lr=1e-3)
+        W1.append(w1.to(bf))
+        W2.append(w2.to(bf))
+        B1.append(b1)
+        B2.append(b2)
+
+    # write the compressed cache: latent coefficients shared by the group, residuals for the worst 10 % per layer
+    cache = L.lowram_compress(keys, values, proj, bases, W1, W2, n_res=T // 10, coef_dtype=L.LOWRAM_BF16,
+                              res_dtype=L.LOWRAM_BF16, b1s=B1, b2s=B2)
+
+    # one decode step of layer l: attend the compressed body, then the exact tail of tokens decoded since
+    l = 0
+    cos, sin = L.lowram_rope_table(d, 5e5, T + 256)
+    q = torch.randn(B, H_q, d, device=dev).to(bf)                      # already rotated at its position
+    out, lse = L.lowram_decode_attn(q, cache["coef"], bases[l], W1[l], W2[l], rope_cos=cos, rope_sin=sin, S=512,
+                                    b1=B1[l], b2=B2[l], res_idx=cache["res_idx"][l], res_val=cache["res_val"][l])
+    tail_k = torch.zeros(B, 256, H_kv, d, device=dev, dtype=bf)
+    tail_v = torch.zeros_like(tail_k)
+    L.lowram_tail_append(torch.randn(B, H_kv, d, device=dev).to(bf), torch.randn(B, H_kv, d, device=dev).to(bf),
+                         tail_k, tail_v, 0)
+    out_t, lse_t = L.lowram_tail_decode_attn(q, tail_k, tail_v, 1)
+    out, lse = L.lowram_merge_attn(out, lse, out_t, lse_t)
+    assert L.lowram_get_error(cache["workspace"]) == 0               # no out-of-range data seen by the kernels
+
+    # an evicted cache: choose the kept tokens from the last 32 queries' attention, then compress only those
+    q_window = torch.randn(B, 32, H_q, d, device=dev).to(bf)
+    k_rotated = torch.randn(B, T, H_kv, d, device=dev).to(bf)
+    keep = L.lowram_evict_plan(L.lowram_attention_mass(q_window, k_rotated), n_sink=64, n_recent=256, T_keep=T // 4)
 """
 from __future__ import annotations
 
@@ -82,6 +128,7 @@ def _load():
             "lowram_decode_attn": [ctypes.POINTER(lowram_decode_shape)] + [_vp] * 18 + [_vp, sz, _vp],
             "lowram_decode_attn_events": [ctypes.POINTER(lowram_decode_shape)] + [_vp] * 18 + [_vp, sz, _vp, _vp],
             "lowram_decode_attn_static": [ctypes.POINTER(lowram_decode_shape)] + [_vp] * 18 + [_vp],
+            "lowram_decode_attn_static_get_error": [_vp, ctypes.POINTER(ctypes.c_uint32)],
             "lowram_rope_table": [i32, dbl, i32, _vp, _vp, _vp],
             "lowram_compress_workspace_size": [ctypes.POINTER(lowram_compress_shape), psz],
             "lowram_compress": [ctypes.POINTER(lowram_compress_shape)] + [_vp] * 18 + [sz, _vp],
@@ -143,9 +190,25 @@ def _act(t: torch.Tensor) -> int:
 
 
 def _dev(*ts):
+    """Every tensor given is a contiguous CUDA tensor, and all of them live on one device, which is returned.  The
+    C entry points launch on the current device and stream, so each wrapper makes that device current for its call
+    (`_on`); a pointer of another GPU would be read by this device's kernels."""
+    dev = None
     for t in ts:
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
             raise ValueError("tensors must be contiguous CUDA tensors")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise LowramShapeError(f"tensors on {dev} and {t.device}: every tensor of a call must be on one device")
+    return dev
+
+
+def _on(dev):
+    """Make `dev` the current CUDA device for the library call (its stream, launches and device queries)."""
+    return torch.cuda.device(dev)
 
 
 def _workspace(nbytes: int, workspace: Optional[torch.Tensor], device) -> torch.Tensor:
@@ -163,7 +226,8 @@ def lowram_rope_table(d: int, theta: float, max_pos: int, device="cuda"):
     """cos/sin tables [d/2, max_pos] float32 (frequency-major) built on the device in fp64."""
     cos = torch.empty((d // 2, max_pos), dtype=torch.float32, device=device)
     sin = torch.empty_like(cos)
-    _check(_load().lowram_rope_table(int(d), float(theta), int(max_pos), _p(cos), _p(sin), _stream()))
+    with _on(_dev(cos, sin)):
+        _check(_load().lowram_rope_table(int(d), float(theta), int(max_pos), _p(cos), _p(sin), _stream()))
     return cos, sin
 
 
@@ -254,22 +318,23 @@ def lowram_decode_attn(q: torch.Tensor, coef: torch.Tensor, basis: torch.Tensor,
     _check_decode_buffers(shape, q=q, coef=coef, coef_scale=coef_scale, pos=pos, rope_cos=rope_cos, rope_sin=rope_sin,
                           basis=basis, w1=w1, w2=w2, b1=b1, b2=b2, res_idx=res_idx, res_val=res_val,
                           res_scale=res_scale, out=out, lse=lse, sel_out=sel_out, key_out=key_out)
-    _dev(q, coef, basis, w1, w2, rope_cos, rope_sin, coef_scale, pos, b1, b2, res_idx, res_val, res_scale)
+    dev = _dev(q, coef, basis, w1, w2, rope_cos, rope_sin, coef_scale, pos, b1, b2, res_idx, res_val, res_scale,
+               out, lse, sel_out, key_out, workspace)
     B, H_q, d = q.shape
-    dev = q.device
     if out is None:
         out = torch.empty((B, H_q, d), dtype=torch.float32, device=dev)
     if lse is None and want_lse:
         lse = torch.empty((B, H_q), dtype=torch.float32, device=dev)
     ws = _workspace(lowram_decode_workspace_size(shape), workspace, dev)
-    args = (ctypes.byref(shape), _p(q), _p(coef), _p(coef_scale), _p(pos), _p(rope_cos), _p(rope_sin), _p(basis),
-            _p(w1), _p(w2), _p(b1), _p(b2), _p(res_idx), _p(res_val), _p(res_scale), _p(out), _p(lse), _p(sel_out),
-            _p(key_out), _p(ws), ws.numel() * ws.element_size(), _stream())
-    if events is None:
-        _check(_load().lowram_decode_attn(*args))
-    else:
-        arr = (ctypes.c_void_p * 5)(*[None if e is None else e.cuda_event for e in events])
-        _check(_load().lowram_decode_attn_events(*args, ctypes.cast(arr, _vp)))
+    with _on(dev):
+        args = (ctypes.byref(shape), _p(q), _p(coef), _p(coef_scale), _p(pos), _p(rope_cos), _p(rope_sin), _p(basis),
+                _p(w1), _p(w2), _p(b1), _p(b2), _p(res_idx), _p(res_val), _p(res_scale), _p(out), _p(lse),
+                _p(sel_out), _p(key_out), _p(ws), ws.numel() * ws.element_size(), _stream())
+        if events is None:
+            _check(_load().lowram_decode_attn(*args))
+        else:
+            arr = (ctypes.c_void_p * 5)(*[None if e is None else e.cuda_event for e in events])
+            _check(_load().lowram_decode_attn_events(*args, ctypes.cast(arr, _vp)))
     return out, lse
 
 
@@ -298,12 +363,25 @@ def lowram_decode_attn_static(q: torch.Tensor, coef: torch.Tensor, basis: torch.
     _check_decode_buffers(shape, q=q, coef=coef, coef_scale=coef_scale, pos=pos, rope_cos=rope_cos, rope_sin=rope_sin,
                           basis=basis, w1=w1, w2=w2, b1=b1, b2=b2, res_idx=res_idx, res_val=res_val,
                           res_scale=res_scale, out=out, lse=lse)
-    _dev(q, coef, basis, w1, w2, rope_cos, rope_sin, coef_scale, pos, b1, b2, res_idx, res_val, res_scale, out, lse)
-    _check(_load().lowram_decode_attn_static(ctypes.byref(shape), _p(q), _p(coef), _p(coef_scale), _p(pos),
-                                             _p(rope_cos), _p(rope_sin), _p(basis), _p(w1), _p(w2), _p(b1), _p(b2),
-                                             _p(res_idx), _p(res_val), _p(res_scale), _p(out), _p(lse), None, None,
-                                             _stream()))
+    dev = _dev(q, coef, basis, w1, w2, rope_cos, rope_sin, coef_scale, pos, b1, b2, res_idx, res_val, res_scale,
+               out, lse)
+    with _on(dev):
+        _check(_load().lowram_decode_attn_static(ctypes.byref(shape), _p(q), _p(coef), _p(coef_scale), _p(pos),
+                                                 _p(rope_cos), _p(rope_sin), _p(basis), _p(w1), _p(w2), _p(b1),
+                                                 _p(b2), _p(res_idx), _p(res_val), _p(res_scale), _p(out), _p(lse),
+                                                 None, None, _stream()))
     return out, lse
+
+
+def lowram_decode_attn_static_get_error(device=None) -> int:
+    """Device check word of the static scratch of `device` (default: the current device), cleared afterwards.
+    Synchronises the current stream of that device."""
+    w = ctypes.c_uint32(0)
+    with _on(torch.cuda.current_device() if device is None else device):
+        st = _load().lowram_decode_attn_static_get_error(_stream(), ctypes.byref(w))
+    if st not in (0, 6):
+        _check(st)
+    return int(w.value)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -347,7 +425,8 @@ def lowram_compress(keys: torch.Tensor, values: Sequence[torch.Tensor], proj: to
     _need_list("w2s", w2s, G, H_kv * d * m, act)
     _need_list("b1s", b1s, G, H_kv * m, 4)
     _need_list("b2s", b2s, G, H_kv * d, 4)
-    _dev(keys, proj, pos, rope_cos, rope_sin, *values, *bases, *w1s, *w2s)
+    dev = _dev(keys, proj, pos, rope_cos, rope_sin, workspace, *values, *bases, *w1s, *w2s, *(b1s or []),
+               *(b2s or []))
     if coef_dtype == LOWRAM_INT4_G32:
         coef = torch.empty((B, T, r // 2), dtype=torch.uint8, device=dev)
         coef_scale = torch.empty((B, T, r // 32), dtype=torch.float16, device=dev)
@@ -368,10 +447,11 @@ def lowram_compress(keys: torch.Tensor, values: Sequence[torch.Tensor], proj: to
                                                    ("b1", b1s), ("b2", b2s), ("res_idx", res_idx),
                                                    ("res_val", res_val), ("res_scale", res_scale), ("err", err))}
     ap = {k: (None if v is None else ctypes.cast(v, _vp)) for k, v in arrays.items()}
-    _check(_load().lowram_compress(ctypes.byref(shape), _p(keys), ap["values"], _p(proj), _p(pos), _p(rope_cos),
-                                   _p(rope_sin), ap["basis"], ap["w1"], ap["w2"], ap["b1"], ap["b2"], _p(coef),
-                                   _p(coef_scale), ap["res_idx"], ap["res_val"], ap["res_scale"], ap["err"], _p(ws),
-                                   ws.numel() * ws.element_size(), _stream()))
+    with _on(dev):
+        _check(_load().lowram_compress(ctypes.byref(shape), _p(keys), ap["values"], _p(proj), _p(pos), _p(rope_cos),
+                                       _p(rope_sin), ap["basis"], ap["w1"], ap["w2"], ap["b1"], ap["b2"], _p(coef),
+                                       _p(coef_scale), ap["res_idx"], ap["res_val"], ap["res_scale"], ap["err"],
+                                       _p(ws), ws.numel() * ws.element_size(), _stream()))
     return {"coef": coef, "coef_scale": coef_scale, "res_idx": res_idx, "res_val": res_val, "res_scale": res_scale,
             "err": err, "workspace": ws}
 
@@ -396,15 +476,15 @@ def lowram_dense_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     _need("v", v, B * T * H_kv * d, act)
     _need("out", out, B * H_q * d, 4)
     _need("lse", lse, B * H_q, 4)
-    _dev(q, k, v)
-    dev = q.device
+    dev = _dev(q, k, v, out, lse, workspace)
     if out is None:
         out = torch.empty((B, H_q, d), dtype=torch.float32, device=dev)
     if lse is None and want_lse:
         lse = torch.empty((B, H_q), dtype=torch.float32, device=dev)
     ws = _workspace(lowram_dense_workspace_size(B, T, H_q, H_kv, d), workspace, dev)
-    _check(_load().lowram_dense_decode_attn(B, T, H_q, H_kv, d, _act(q), float(sm_scale), _p(q), _p(k), _p(v),
-                                            _p(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream()))
+    with _on(dev):
+        _check(_load().lowram_dense_decode_attn(B, T, H_q, H_kv, d, _act(q), float(sm_scale), _p(q), _p(k), _p(v),
+                                                _p(out), _p(lse), _p(ws), ws.numel() * ws.element_size(), _stream()))
     return out, lse
 
 
@@ -431,11 +511,12 @@ def lowram_attention_mass(q_win: torch.Tensor, k: torch.Tensor, *, sm_scale: flo
     if q_win.dtype != k.dtype:
         raise TypeError("q_win and k must share one dtype")
     _need("k", k, B * T * H_kv * d, _ESZ[_act(k)])
-    _dev(q_win, k)
-    ws = _workspace(lowram_attention_mass_workspace_size(B, T, W, H_q, H_kv, d, _act(k)), workspace, k.device)
-    mass = torch.empty((B, T), dtype=torch.float32, device=k.device)
-    _check(_load().lowram_attention_mass(B, T, W, H_q, H_kv, d, _act(k), float(sm_scale), _p(q_win), _p(k), _p(mass),
-                                         _p(ws), ws.numel() * ws.element_size(), _stream()))
+    dev = _dev(q_win, k, workspace)
+    ws = _workspace(lowram_attention_mass_workspace_size(B, T, W, H_q, H_kv, d, _act(k)), workspace, dev)
+    mass = torch.empty((B, T), dtype=torch.float32, device=dev)
+    with _on(dev):
+        _check(_load().lowram_attention_mass(B, T, W, H_q, H_kv, d, _act(k), float(sm_scale), _p(q_win), _p(k),
+                                             _p(mass), _p(ws), ws.numel() * ws.element_size(), _stream()))
     return mass
 
 
@@ -443,11 +524,12 @@ def lowram_evict_plan(mass: torch.Tensor, *, n_sink: int, n_recent: int, T_keep:
                       workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Kept token indices [B, T_keep] (ascending): sinks, recents and the heaviest others by mass [B, T]."""
     B, T = mass.shape
-    _dev(mass)
-    ws = _workspace(lowram_evict_plan_workspace_size(B, T), workspace, mass.device)
-    keep = torch.empty((B, int(T_keep)), dtype=torch.int32, device=mass.device)
-    _check(_load().lowram_evict_plan(B, T, int(n_sink), int(n_recent), int(T_keep), _p(mass), _p(keep), _p(ws),
-                                     ws.numel() * ws.element_size(), _stream()))
+    dev = _dev(mass, workspace)
+    ws = _workspace(lowram_evict_plan_workspace_size(B, T), workspace, dev)
+    keep = torch.empty((B, int(T_keep)), dtype=torch.int32, device=dev)
+    with _on(dev):
+        _check(_load().lowram_evict_plan(B, T, int(n_sink), int(n_recent), int(T_keep), _p(mass), _p(keep), _p(ws),
+                                         ws.numel() * ws.element_size(), _stream()))
     return keep
 
 
@@ -457,7 +539,7 @@ def lowram_evict_plan(mass: torch.Tensor, *, n_sink: int, n_recent: int, T_keep:
 def _pred_dims(keys, values, w1, w2):
     B, T, H_kv, d = keys.shape
     m = w1.shape[1]
-    _dev(keys, values)
+    _dev(keys, values, w1, w2)
     if values.shape != keys.shape or values.dtype != keys.dtype:
         raise ValueError("keys and values must share shape [B, T, H_kv, d] and dtype")
     if w1.shape != (H_kv, m, d) or w2.shape != (H_kv, d, m):
@@ -467,7 +549,6 @@ def _pred_dims(keys, values, w1, w2):
 
 def _pred_params(H_kv, d, m, w1, b1, w2, b2):
     for t in (w1, b1, w2, b2):
-        _dev(t)
         if t.dtype != torch.float32:
             raise TypeError("predictor parameters are float32")
     _need("b1", b1, H_kv * m, 4)
@@ -479,10 +560,12 @@ def lowram_predictor_grad(keys: torch.Tensor, values: torch.Tensor, w1: torch.Te
     """Loss [H_kv] and gradient (g_w1, g_b1, g_w2, g_b2) of every head's predictor; parameters float32."""
     B, T, H_kv, d, m = _pred_dims(keys, values, w1, w2)
     _pred_params(H_kv, d, m, w1, b1, w2, b2)
-    loss = torch.empty(H_kv, dtype=torch.float32, device=keys.device)
+    dev = _dev(keys, values, w1, b1, w2, b2)
+    loss = torch.empty(H_kv, dtype=torch.float32, device=dev)
     g = [torch.empty_like(t) for t in (w1, b1, w2, b2)]
-    _check(_load().lowram_predictor_grad(B, T, H_kv, d, m, _act(keys), _p(keys), _p(values), _p(w1), _p(b1), _p(w2),
-                                         _p(b2), _p(loss), *[_p(x) for x in g], _stream()))
+    with _on(dev):
+        _check(_load().lowram_predictor_grad(B, T, H_kv, d, m, _act(keys), _p(keys), _p(values), _p(w1), _p(b1),
+                                             _p(w2), _p(b2), _p(loss), *[_p(x) for x in g], _stream()))
     return (loss, *g)
 
 
@@ -494,13 +577,15 @@ def lowram_fit_predictor(keys: torch.Tensor, values: torch.Tensor, w1: torch.Ten
     Returns the losses [steps, H_kv] before each step (or None)."""
     B, T, H_kv, d, m = _pred_dims(keys, values, w1, w2)
     _pred_params(H_kv, d, m, w1, b1, w2, b2)
+    dev = _dev(keys, values, w1, b1, w2, b2, workspace)
     n = ctypes.c_size_t(0)
     _check(_load().lowram_fit_predictor_workspace_size(H_kv, d, m, ctypes.byref(n)))
-    ws = _workspace(n.value, workspace, keys.device)
-    losses = torch.empty((int(steps), H_kv), dtype=torch.float32, device=keys.device) if want_losses else None
-    _check(_load().lowram_fit_predictor(B, T, H_kv, d, m, _act(keys), _p(keys), _p(values), int(steps), float(lr),
-                                        float(beta1), float(beta2), float(eps), _p(w1), _p(b1), _p(w2), _p(b2),
-                                        _p(losses), _p(ws), ws.numel() * ws.element_size(), _stream()))
+    ws = _workspace(n.value, workspace, dev)
+    losses = torch.empty((int(steps), H_kv), dtype=torch.float32, device=dev) if want_losses else None
+    with _on(dev):
+        _check(_load().lowram_fit_predictor(B, T, H_kv, d, m, _act(keys), _p(keys), _p(values), int(steps), float(lr),
+                                            float(beta1), float(beta2), float(eps), _p(w1), _p(b1), _p(w2), _p(b2),
+                                            _p(losses), _p(ws), ws.numel() * ws.element_size(), _stream()))
     return losses
 
 
@@ -519,16 +604,17 @@ def lowram_fit_basis(keys: torch.Tensor, r: int, *, pos: Optional[torch.Tensor] 
     _need("pos", pos, B * T, 4)
     _need("rope_cos", rope_cos, d // 2 * shape.max_pos, 4)
     _need("rope_sin", rope_sin, d // 2 * shape.max_pos, 4)
-    _dev(keys, pos, rope_cos, rope_sin)
+    dev = _dev(keys, pos, rope_cos, rope_sin, workspace)
     n = ctypes.c_size_t(0)
     _check(_load().lowram_fit_basis_workspace_size(ctypes.byref(shape), ctypes.byref(n)))
     ws = _workspace(n.value, workspace, dev)
     proj = torch.empty((int(r), G * H_kv * d), dtype=torch.float32, device=dev)
     bases = [torch.empty((H_kv * d, int(r)), dtype=keys.dtype, device=dev) for _ in range(G)]
     arr = _ptr_array(bases)
-    _check(_load().lowram_fit_basis(ctypes.byref(shape), _p(keys), _p(pos), _p(rope_cos), _p(rope_sin), int(iters),
-                                    int(seed) & 0xFFFFFFFFFFFFFFFF, _p(proj), ctypes.cast(arr, _vp), _p(ws),
-                                    ws.numel() * ws.element_size(), _stream()))
+    with _on(dev):
+        _check(_load().lowram_fit_basis(ctypes.byref(shape), _p(keys), _p(pos), _p(rope_cos), _p(rope_sin),
+                                        int(iters), int(seed) & 0xFFFFFFFFFFFFFFFF, _p(proj), ctypes.cast(arr, _vp),
+                                        _p(ws), ws.numel() * ws.element_size(), _stream()))
     return proj, bases, ws
 
 
@@ -538,13 +624,14 @@ def lowram_fit_basis(keys: torch.Tensor, r: int, *, pos: Optional[torch.Tensor] 
 def lowram_tail_append(k_new: torch.Tensor, v_new: torch.Tensor, tail_k: torch.Tensor, tail_v: torch.Tensor, t: int):
     """Write one token's rotated keys and values [B, H_kv, d] into row t of the tail buffers [B, T_cap, H_kv, d]."""
     B, T_cap, H_kv, d = tail_k.shape
-    _dev(k_new, v_new, tail_k, tail_v)
+    dev = _dev(k_new, v_new, tail_k, tail_v)
     if k_new.shape != (B, H_kv, d) or v_new.shape != (B, H_kv, d) or tail_v.shape != tail_k.shape:
         raise ValueError("k_new, v_new must be [B, H_kv, d] and the tail buffers [B, T_cap, H_kv, d]")
     if not (k_new.dtype == v_new.dtype == tail_k.dtype == tail_v.dtype):
         raise TypeError("k_new, v_new and the tail buffers must share one dtype")
-    _check(_load().lowram_tail_append(B, T_cap, H_kv, d, _act(tail_k), int(t), _p(k_new), _p(v_new), _p(tail_k),
-                                      _p(tail_v), _stream()))
+    with _on(dev):
+        _check(_load().lowram_tail_append(B, T_cap, H_kv, d, _act(tail_k), int(t), _p(k_new), _p(v_new), _p(tail_k),
+                                          _p(tail_v), _stream()))
 
 
 def lowram_tail_decode_attn(q: torch.Tensor, tail_k: torch.Tensor, tail_v: torch.Tensor, t_len: int, *,
@@ -559,16 +646,16 @@ def lowram_tail_decode_attn(q: torch.Tensor, tail_k: torch.Tensor, tail_v: torch
     _need("tail_v", tail_v, B * T_cap * H_kv * d, act)
     _need("out", out, B * H_q * d, 4)
     _need("lse", lse, B * H_q, 4)
-    _dev(q, tail_k, tail_v)
-    dev = q.device
+    dev = _dev(q, tail_k, tail_v, out, lse, workspace)
     if out is None:
         out = torch.empty((B, H_q, d), dtype=torch.float32, device=dev)
     if lse is None and want_lse:
         lse = torch.empty((B, H_q), dtype=torch.float32, device=dev)
     ws = _workspace(lowram_dense_workspace_size(B, int(t_len), H_q, H_kv, d), workspace, dev)
-    _check(_load().lowram_tail_decode_attn(B, T_cap, int(t_len), H_q, H_kv, d, _act(q), float(sm_scale), _p(q),
-                                           _p(tail_k), _p(tail_v), _p(out), _p(lse), _p(ws),
-                                           ws.numel() * ws.element_size(), _stream()))
+    with _on(dev):
+        _check(_load().lowram_tail_decode_attn(B, T_cap, int(t_len), H_q, H_kv, d, _act(q), float(sm_scale), _p(q),
+                                               _p(tail_k), _p(tail_v), _p(out), _p(lse), _p(ws),
+                                               ws.numel() * ws.element_size(), _stream()))
     return out, lse
 
 
@@ -585,13 +672,14 @@ def lowram_merge_attn(out_a: torch.Tensor, lse_a: torch.Tensor, out_b: torch.Ten
     _need("lse_b", lse_b, B * H_q, 4)
     _need("out", out, B * H_q * d, 4)
     _need("lse", lse, B * H_q, 4)
-    _dev(out_a, lse_a, out_b, lse_b, out, lse)
+    dev = _dev(out_a, lse_a, out_b, lse_b, out, lse)
     if out is None:
         out = torch.empty_like(out_a)
     if lse is None:
         lse = torch.empty_like(lse_a)
-    _check(_load().lowram_merge_attn(B, H_q, d, _p(out_a), _p(lse_a), _p(out_b), _p(lse_b), _p(out), _p(lse),
-                                     _stream()))
+    with _on(dev):
+        _check(_load().lowram_merge_attn(B, H_q, d, _p(out_a), _p(lse_a), _p(out_b), _p(lse_b), _p(out), _p(lse),
+                                         _stream()))
     return out, lse
 
 
@@ -601,14 +689,16 @@ def lowram_merge_attn(out_a: torch.Tensor, lse_a: torch.Tensor, out_b: torch.Ten
 def lowram_get_error(workspace: torch.Tensor) -> int:
     """Device check word of a workspace (LOWRAM_CHECK_* bits), cleared afterwards.  Synchronises the stream."""
     w = ctypes.c_uint32(0)
-    st = _load().lowram_get_error(_p(workspace), _stream(), ctypes.byref(w))
+    with _on(_dev(workspace)):
+        st = _load().lowram_get_error(_p(workspace), _stream(), ctypes.byref(w))
     if st not in (0, 6):
         _check(st)
     return int(w.value)
 
 
 def lowram_clear_error(workspace: torch.Tensor):
-    _check(_load().lowram_clear_error(_p(workspace), _stream()))
+    with _on(_dev(workspace)):
+        _check(_load().lowram_clear_error(_p(workspace), _stream()))
 
 
 def lowram_version() -> int:

@@ -20,26 +20,29 @@ constexpr size_t kStaticBytes = (size_t)32 << 20;   // 32 MiB
 constexpr int kMaxDevices = 64;
 
 // The scratch array.  In host code this name is a host-side stand-in, not a device address: host code
-// must use the address cudaGetSymbolAddress returns for the current device.
+// must use the address cudaGetSymbolAddress returns for the current device.  A module's __device__ arrays
+// start zeroed, so the device check word in its first bytes starts clear.
 static __device__ __align__(256) unsigned char g_static_ws[kStaticBytes];
 
-std::once_flag g_once[kMaxDevices];
+std::mutex g_mu[kMaxDevices];
 void* g_addr[kMaxDevices] = {};
-cudaError_t g_setup_err[kMaxDevices] = {};
 
-// Once per device, with that device current: look up the array's device address.
+// With the caller's device current: the array's device address on that device.  Only a successful lookup
+// is kept; a failed one (during a stream capture, say) is retried by the next call.
 cudaError_t static_scratch(void** addr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::call_once(g_once[dev], [dev] {
+    std::lock_guard<std::mutex> lock(g_mu[dev]);
+    if (g_addr[dev] == nullptr) {
         void* p = nullptr;
-        g_setup_err[dev] = cudaGetSymbolAddress(&p, g_static_ws);
-        g_addr[dev] = (g_setup_err[dev] == cudaSuccess) ? p : nullptr;
-    });
+        e = cudaGetSymbolAddress(&p, g_static_ws);
+        if (e != cudaSuccess) return e;
+        g_addr[dev] = p;
+    }
     *addr = g_addr[dev];
-    return g_setup_err[dev];
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -64,12 +67,23 @@ extern "C" LOWRAM_API lowram_status lowram_decode_attn_static(
         lowram::set_error_message("lowram_decode_attn_static: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
         return LOWRAM_ERR_CUDA;
     }
-    // the device check word must start at zero; the rest of the scratch is written before it is read
-    e = cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream);
-    if (e != cudaSuccess) {
-        lowram::set_error_message("lowram_decode_attn_static: clearing the check word failed: %s", cudaGetErrorString(e));
-        return LOWRAM_ERR_CUDA;
-    }
+    // the device check word is sticky across calls until lowram_decode_attn_static_get_error reads it; the rest of
+    // the scratch is written before it is read
     return lowram_decode_attn(shape, q, coef, coef_scale, pos, rope_cos, rope_sin, basis, w1, w2, b1, b2, res_idx,
                               res_val, res_scale, out, lse, sel_out, key_out, ws, kStaticBytes, stream);
+}
+
+extern "C" LOWRAM_API lowram_status lowram_decode_attn_static_get_error(void* stream, uint32_t* check_word) {
+    if (!check_word) {
+        lowram::set_error_message("lowram_decode_attn_static_get_error: check_word is NULL");
+        return LOWRAM_ERR_INVALID_ARG;
+    }
+    void* ws = nullptr;
+    cudaError_t e = static_scratch(&ws);
+    if (e != cudaSuccess || ws == nullptr) {
+        lowram::set_error_message("lowram_decode_attn_static_get_error: cudaGetSymbolAddress failed: %s",
+                                  cudaGetErrorString(e));
+        return LOWRAM_ERR_CUDA;
+    }
+    return lowram_get_error(ws, stream, check_word);
 }

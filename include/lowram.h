@@ -175,8 +175,11 @@ LOWRAM_API lowram_status lowram_decode_attn_events(const lowram_decode_shape* sh
  *   - Every call shares the one array per device, which keeps the last call's contents: calls that
  *     overlap on the GPU (different streams, or threads without ordering) race and corrupt each other's
  *     results.  Order them on one stream.
- *   - Each call clears the device check word at its start; that word cannot be read through this call,
- *     so data checks (LOWRAM_CHECK_*) are not reported here.
+ *   - The device check word (LOWRAM_CHECK_* bits, including LOWRAM_CHECK_TIMEOUT) lives in the array too.
+ *     It starts clear, stays set across calls once a kernel sets it, and is read and cleared by
+ *     lowram_decode_attn_static_get_error().
+ *   - A failed address lookup (for example one attempted during a stream capture) returns LOWRAM_ERR_CUDA
+ *     and is retried by the next call.
  */
 LOWRAM_API lowram_status lowram_decode_attn_static(const lowram_decode_shape* shape, const void* q, const void* coef,
                                                    const void* coef_scale, const int32_t* pos, const float* rope_cos,
@@ -185,6 +188,14 @@ LOWRAM_API lowram_status lowram_decode_attn_static(const lowram_decode_shape* sh
                                                    const int32_t* res_idx, const void* res_val, const void* res_scale,
                                                    float* out, float* lse, int32_t* sel_out, float* key_out,
                                                    void* stream);
+
+/*
+ * lowram_decode_attn_static_get_error -- the device check word of lowram_decode_attn_static's scratch on the
+ * current device, as lowram_get_error() gives it for a workspace: synchronises `stream`, stores the word in
+ * *check_word, clears it, and returns LOWRAM_ERR_DEVICE_CHECK if it was set (LOWRAM_OK if clear).  Allocates
+ * nothing.  Order it after the static calls it reports on (same stream).
+ */
+LOWRAM_API lowram_status lowram_decode_attn_static_get_error(void* stream, uint32_t* check_word);
 
 /*
  * lowram_rope_table -- cos/sin tables of the rotary embedding re-applied at decode ("Asymmetric key

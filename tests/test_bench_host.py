@@ -47,8 +47,8 @@ def _roofline(line):
     assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
 
 
-@pytest.mark.parametrize("workload,extra", [("llama8b", ["--dense", "--no-cpu-baseline"]),
-                                            ("evict_quant", ["--no-cpu-baseline"]),
+@pytest.mark.parametrize("workload,extra", [("llama8b", ["--no-cpu-baseline"]),
+                                            ("evict_quant", ["--no-cpu-baseline", "--no-dense"]),
                                             ("tiny", [])])
 def test_decode_mode_prints_the_contract_line(workload, extra):
     line = run_bench(workload, *extra)
@@ -61,6 +61,9 @@ def test_decode_mode_prints_the_contract_line(workload, extra):
         assert key in line["e2e"], key
     assert line["e2e"]["h2d_bytes_per_step"] > 0 and line["e2e"]["d2h_bytes_per_step"] > 0
     assert line["gpu_launches"] > 0
+    assert line["e2e"]["host_us_per_call"] > 0 and line["host_us_per_call"] == line["e2e"]["host_us_per_call"]
+    if "--no-dense" not in extra and workload != "tiny":
+        assert line["dense_comparator"]["t_call_us"] > 0     # the comparator is timed by default
     _roofline(line)
     if "--no-cpu-baseline" not in extra:
         cb = line["cpu_baseline"]

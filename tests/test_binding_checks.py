@@ -94,3 +94,21 @@ def test_dense_tail_merge_and_mass_refuse_mismatched_buffers():
         L.lowram_attention_mass(torch.zeros(2, 4, 8, 64, dtype=f32), k)
     with pytest.raises(L.LowramShapeError, match="k"):
         L.lowram_attention_mass(torch.zeros(2, 4, 8, 128, dtype=bf), k)       # head dim 128 against 64
+
+
+class _OnDevice:
+    """Stand-in for a contiguous CUDA tensor on device `idx` (the check reads only these attributes)."""
+
+    def __init__(self, idx):
+        self.is_cuda = True
+        self.device = torch.device("cuda", idx)
+
+    def is_contiguous(self):
+        return True
+
+
+def test_every_tensor_of_a_call_must_share_one_device():
+    from decode_attention_19_b300 import binding as B
+    assert B._dev(_OnDevice(1), None, _OnDevice(1)) == torch.device("cuda", 1)
+    with pytest.raises(L.LowramShapeError, match="one device"):
+        B._dev(_OnDevice(0), _OnDevice(1))

@@ -38,6 +38,22 @@ def test_compress_keys_given_after_rope(name):
     C.check_compress(C.run_gpu_compress(c), C.run_oracle_compress(c), w, c)
 
 
+@pytest.mark.parametrize("name", ["llama8b_small", "peak_small"])
+def test_compress_exact_projection_has_no_exemptions(name):
+    """With a 0/1 selection projection nothing can round differently: every stored coefficient equals the oracle's
+    (and the selected key feature) bit for bit, and the residual index sets match the oracle's except within 1e-3
+    of the cut-off, with no token exempt."""
+    w = SMALL[name]
+    c = C.exact_projection_case(w)
+    gpu = C.run_gpu_compress(c)
+    orc = C.run_oracle_compress(c)
+    stats = C.check_compress(gpu, orc, w, c)
+    assert stats["flipped_coef_frac"] == 0.0 and stats["flipped_row_frac"] == 0.0
+    sel = c["proj"].argmax(dim=1)
+    want = c["keys"].reshape(w.B, w.T, -1)[:, :, sel]
+    assert torch.equal(gpu["coef"].cpu(), want)
+
+
 @pytest.mark.parametrize("rho", [0.0, 1.0])
 def test_compress_residual_extremes(rho):
     w = SMALL["llama8b_small"].with_(rho=rho)

@@ -64,10 +64,20 @@ def test_fit_predictor_follows_the_oracle_trajectory(d, m, dtype):
     torch.cuda.synchronize()
     *ref, ref_losses = O.fit_predictor(keys, values, *params, steps=steps, lr=lr)
     np.testing.assert_allclose(O.f64(losses.cpu()), ref_losses, rtol=1e-4, atol=0)
-    for got, want in zip(dev, ref):
-        diff = np.abs(O.f64(got.cpu()) - want)
+    # Adam moves each parameter by about lr per step whatever the gradient's size, so the two trajectories can part
+    # only where a gradient is near zero and its float32 and fp64 signs differ.  Such parameters are rare: all but
+    # 1% must follow the oracle to within 1% of one step (a wrong learning rate, a dropped bias correction or a
+    # wrong gradient moves nearly every parameter by a step or more), and none may drift more than two steps a step.
+    for name, got, start, want in zip(("w1", "b1", "w2", "b2"), dev, params, ref):
+        g = O.f64(got.cpu())
+        diff = np.abs(g - want)
+        moved = np.abs(want - O.f64(start))
+        off = float(np.mean(diff > 1e-2 * lr))
+        print(f"{name}: max |diff| {diff.max():.3g}, fraction off by more than 1% of a step {off:.4f}, "
+              f"median move {np.median(moved):.3g}")
+        assert np.median(moved) >= 0.5 * lr * steps         # the oracle trajectory itself moves the parameters
+        assert off <= 0.01, f"{name}: {off:.3%} of the parameters leave the oracle trajectory"
         assert diff.max() <= 2 * lr * steps
-        assert diff.mean() <= 0.05 * lr * steps            # flips are rare
 
 
 def test_fit_predictor_reduces_the_loss():

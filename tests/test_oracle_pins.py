@@ -641,3 +641,24 @@ def test_empty_and_degenerate_shapes():
     # B = 0
     res = O.decode(np.zeros((0, 2, 4)), np.zeros((0, 5, 3)), W, w1, w2, S=4, theta=1e4)
     assert res.out.shape == (0, 2, 4)
+
+
+def test_selection_projection_copies_key_features_exactly():
+    """A 0/1 selection projection makes the oracle's latent coefficients exact copies of the selected key
+    features (no rounding anywhere), and its bases rebuild exactly those features with zeros elsewhere."""
+    import lowram_cases as C
+    from decode_attention_19_b300 import synth
+    w = synth.WORKLOADS["llama8b"].with_(B=1, T=48, G=2, H_kv=2, r=64, S=48)
+    c = C.exact_projection_case(w)
+    orc = C.run_oracle_compress(c)
+    sel = c["proj"].argmax(dim=1).numpy()
+    keys = O.f64(c["keys"]).reshape(w.B, w.T, -1)
+    assert np.array_equal(orc["coef_raw"], keys[:, :, sel])
+    assert np.array_equal(orc["coef"], keys[:, :, sel])
+    rows = w.H_kv * w.d
+    for l in range(w.G):
+        rebuilt = O.rebuild_keys(orc["coef"], c["bases"][l], w.H_kv, w.d).reshape(w.B, w.T, -1)
+        want = np.zeros_like(rebuilt)
+        mine = (sel >= l * rows) & (sel < (l + 1) * rows)
+        want[:, :, sel[mine] - l * rows] = keys[:, :, sel[mine]]
+        assert np.array_equal(rebuilt, want)
