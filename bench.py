@@ -78,6 +78,8 @@ def workload(args) -> synth.Workload:
     if args.T:
         kw["T"] = args.T
     if args.layers:
+        if args.layers % w.G:
+            raise SystemExit(f"--layers {args.layers}: must be a multiple of the layer-group size G={w.G}")
         kw["L"] = args.layers
     return w.with_(**kw) if kw else w
 

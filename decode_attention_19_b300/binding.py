@@ -64,13 +64,15 @@ LIB_PATH = os.path.join(_HERE, "liblowram.so")
 
 LOWRAM_F32, LOWRAM_BF16, LOWRAM_INT4_G32, LOWRAM_INT8_VEC = 0, 1, 2, 3
 CHECK_POS_RANGE, CHECK_RES_INDEX, CHECK_TIMEOUT, CHECK_NOT_PD = 1, 2, 4, 8
+FLAG_INT4_EXACT_SPLIT = 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported", 4: "workspace", 5: "cuda",
           6: "device check"}
 
 
 class lowram_decode_shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("B", "T", "H_q", "H_kv", "d", "r", "m", "S", "n_res", "act_dtype",
-                                              "coef_dtype", "res_dtype", "max_pos")] + [("sm_scale", ctypes.c_float)]
+                                              "coef_dtype", "res_dtype", "max_pos")] + [("sm_scale", ctypes.c_float)] + \
+        [("basis_batch_stride", ctypes.c_int64), ("mlp_batch_stride", ctypes.c_int64), ("flags", ctypes.c_uint32)]
 
 
 class lowram_compress_shape(ctypes.Structure):
@@ -150,6 +152,7 @@ def _load():
             "lowram_get_error": [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)],
             "lowram_decode_uses_tensor_cores": [ctypes.POINTER(lowram_decode_shape), ctypes.POINTER(ctypes.c_int32)],
             "lowram_clear_error": [_vp, _vp],
+            "lowram_set_wait_limit": [ctypes.c_int64],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -235,15 +238,26 @@ def lowram_rope_table(d: int, theta: float, max_pos: int, device="cuda"):
 # decode
 # ------------------------------------------------------------------------------------------------
 def decode_shape(q, coef, w1, *, S: int, n_res: int, max_pos: int, res_dtype: int, sm_scale: float = 0.0,
-                 coef_int4: bool = False) -> lowram_decode_shape:
+                 coef_int4: bool = False, basis=None, int4_exact_split: bool = False) -> lowram_decode_shape:
+    """The C shape of a decode call.  A basis [B, H_kv*d, r] (one per sequence) or a w1 [B, H_kv, m, d] (a predictor
+    per sequence) sets the matching batch stride to one sequence's elements; [H_kv*d, r] / [H_kv, m, d] share
+    them across the batch (stride 0)."""
     B, H_q, d = q.shape
     T = coef.shape[1]
     r = coef.shape[2] * 2 if coef_int4 else coef.shape[2]
-    H_kv, m = w1.shape[0], w1.shape[1]
+    per_seq_mlp = w1.dim() == 4
+    H_kv, m = (w1.shape[1], w1.shape[2]) if per_seq_mlp else (w1.shape[0], w1.shape[1])
     act = _act(q)
-    return lowram_decode_shape(B, T, H_q, H_kv, d, r, m, int(S), int(n_res), act,
-                               LOWRAM_INT4_G32 if coef_int4 else _act(coef), int(res_dtype), int(max_pos),
-                               float(sm_scale))
+    sh = lowram_decode_shape(B, T, H_q, H_kv, d, r, m, int(S), int(n_res), act,
+                             LOWRAM_INT4_G32 if coef_int4 else _act(coef), int(res_dtype), int(max_pos),
+                             float(sm_scale))
+    if basis is not None and basis.dim() == 3:
+        sh.basis_batch_stride = basis[0].numel()
+    if per_seq_mlp:
+        sh.mlp_batch_stride = w1[0].numel()
+    if int4_exact_split:
+        sh.flags |= FLAG_INT4_EXACT_SPLIT
+    return sh
 
 
 def _check_decode_buffers(s: lowram_decode_shape, *, q, coef, coef_scale, pos, rope_cos, rope_sin, basis, w1, w2,
@@ -261,11 +275,14 @@ def _check_decode_buffers(s: lowram_decode_shape, *, q, coef, coef_scale, pos, r
     _need("pos", pos, B * T, 4)
     _need("rope_cos", rope_cos, d // 2 * s.max_pos, 4)
     _need("rope_sin", rope_sin, d // 2 * s.max_pos, 4)
-    _need("basis", basis, H_kv * d * r, act)
-    _need("w1", w1, H_kv * m * d, act)
-    _need("w2", w2, H_kv * d * m, act)
-    _need("b1", b1, H_kv * m, 4)
-    _need("b2", b2, H_kv * d, 4)
+    sb, sm = s.basis_batch_stride, s.mlp_batch_stride
+    nb = (B - 1) * sb + H_kv * d * r if (sb and B) else H_kv * d * r
+    nm = (B - 1) * sm + H_kv * m * d if (sm and B) else H_kv * m * d
+    _need("basis", basis, nb, act)
+    _need("w1", w1, nm, act)
+    _need("w2", w2, nm, act)
+    _need("b1", b1, (B if sm else 1) * H_kv * m, 4)
+    _need("b2", b2, (B if sm else 1) * H_kv * d, 4)
     _need("res_idx", res_idx, B * H_kv * s.n_res, 4)
     _need("res_val", res_val, B * H_kv * s.n_res * d, 1 if s.res_dtype == LOWRAM_INT8_VEC else _ESZ[s.res_dtype])
     _need("res_scale", res_scale, B * H_kv * s.n_res, 2)
@@ -295,15 +312,21 @@ def lowram_decode_attn(q: torch.Tensor, coef: torch.Tensor, basis: torch.Tensor,
                        res_scale: Optional[torch.Tensor] = None, sm_scale: float = 0.0,
                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                        sel_out: Optional[torch.Tensor] = None, key_out: Optional[torch.Tensor] = None,
-                       workspace: Optional[torch.Tensor] = None, want_lse: bool = True, events=None):
+                       workspace: Optional[torch.Tensor] = None, want_lse: bool = True, events=None,
+                       int4_exact_split: bool = False):
     """Decode-step attention of one layer read from the compressed cache.  Returns (out, lse).
+
+    int4_exact_split: int4 coefficients reach the tensor cores as an exact two-term bf16 split (rank 2r) instead of
+    the default fp16 copy (LOWRAM_FLAG_INT4_EXACT_SPLIT).
 
     events: optional sequence of five recorded torch.cuda.Event objects (timing marks between the kernels,
     see lowram_decode_attn_events).
 
     Layouts as in include/lowram.h: q [B,H_q,d]; coef [B,T,r] (uint8 [B,T,r/2] + coef_scale fp16 [B,T,r/32] for
-    int4); basis [H_kv*d, r]; w1 [H_kv,m,d]; w2 [H_kv,d,m]; res_idx int32 [B,H_kv,n_res]; res_val [B,H_kv,n_res,d]
-    (int8 + res_scale fp16 [B,H_kv,n_res] for the int8 format); rope tables [d/2, max_pos].
+    int4); basis [H_kv*d, r], or [B, H_kv*d, r] for a basis per sequence; w1 [H_kv,m,d] and w2 [H_kv,d,m], or
+    [B,H_kv,m,d] and [B,H_kv,d,m] (with b1 [B,H_kv,m], b2 [B,H_kv,d]) for a predictor per sequence;
+    res_idx int32 [B,H_kv,n_res]; res_val [B,H_kv,n_res,d] (int8 + res_scale fp16 [B,H_kv,n_res] for the int8
+    format); rope tables [d/2, max_pos].
     """
     coef_int4 = coef.dtype == torch.uint8
     n_res = 0 if res_idx is None else int(res_idx.shape[-1])
@@ -314,7 +337,7 @@ def lowram_decode_attn(q: torch.Tensor, coef: torch.Tensor, basis: torch.Tensor,
     else:
         res_dtype = _act(res_val)
     shape = decode_shape(q, coef, w1, S=S, n_res=n_res, max_pos=rope_cos.shape[1], res_dtype=res_dtype,
-                         sm_scale=sm_scale, coef_int4=coef_int4)
+                         sm_scale=sm_scale, coef_int4=coef_int4, basis=basis, int4_exact_split=int4_exact_split)
     _check_decode_buffers(shape, q=q, coef=coef, coef_scale=coef_scale, pos=pos, rope_cos=rope_cos, rope_sin=rope_sin,
                           basis=basis, w1=w1, w2=w2, b1=b1, b2=b2, res_idx=res_idx, res_val=res_val,
                           res_scale=res_scale, out=out, lse=lse, sel_out=sel_out, key_out=key_out)
@@ -357,7 +380,7 @@ def lowram_decode_attn_static(q: torch.Tensor, coef: torch.Tensor, basis: torch.
     else:
         res_dtype = _act(res_val)
     shape = decode_shape(q, coef, w1, S=S, n_res=n_res, max_pos=rope_cos.shape[1], res_dtype=res_dtype,
-                         sm_scale=sm_scale, coef_int4=coef_int4)
+                         sm_scale=sm_scale, coef_int4=coef_int4, basis=basis)
     if out is None:
         raise LowramShapeError("out is required (this call allocates nothing)")
     _check_decode_buffers(shape, q=q, coef=coef, coef_scale=coef_scale, pos=pos, rope_cos=rope_cos, rope_sin=rope_sin,
@@ -703,3 +726,9 @@ def lowram_clear_error(workspace: torch.Tensor):
 
 def lowram_version() -> int:
     return int(_load().lowram_version())
+
+
+def lowram_set_wait_limit(cycles: int):
+    """Testing aid: pipeline waits of the tensor-core value pass give up after `cycles` SM cycles (0: the default,
+    about a second).  A call whose wait gives up sets CHECK_TIMEOUT in its workspace's check word."""
+    _check(_load().lowram_set_wait_limit(int(cycles)))

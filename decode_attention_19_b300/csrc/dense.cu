@@ -197,26 +197,104 @@ __global__ void __launch_bounds__(kDenseThreads) dense_kernel(int T, int Ts, int
 }
 
 // ------------------------------------------------------------------------------------------------
-// bf16, d = 128: instruction-lean form.  A CTA of four warps per (kv-head, token range, sequence); each warp
-// streams blocks of 16 tokens of K and V through its own two-stage cp.async ring in shared memory (16 KB per
-// warp, so twelve warps fit on an SM) and keeps an online softmax per q-head:
-//   scores   two lanes per token, 64 features each: the K row halves (read back swizzled, conflict-free)
-//            against the q-heads (pre-scaled, fp32 in shared memory), packed fp32x2 FMAs, one shuffle to add;
-//   weights  block max and sum by warp reductions, one exp per (token, q-head);
+// bf16, d = 128.  A CTA of four warps per (kv-head, token range, sequence); each warp streams blocks of 16 tokens of
+// K and V through its own two-stage cp.async ring in shared memory (16 KB per warp) and keeps an online softmax
+// per q-head:
+//   scores   eight lanes per token, 16 features each, four tokens per pass: the K row slices (read back swizzled)
+//            against the q-heads held in registers (pre-scaled fp32 pairs), packed fp32x2 FMAs, three shuffles
+//            to add;
+//   weights  block max and sum by shuffles, one exp per (token, q-head);
 //   values   lane = 4 features: each token's V row (8 bytes per lane) times its weight, broadcast by shuffle.
+// Only K and V pass through shared memory (the queries never do), so its traffic is twice the bytes streamed.
 // The CTA's warps merge their states in shared memory and write one partial record per (sequence, q-head).
+// Up to four q-heads per kv-head; more (whose queries would not fit in registers) take dense_bf16_smemq_kernel,
+// which reads the pre-scaled queries from shared memory, two lanes per token.
 // ------------------------------------------------------------------------------------------------
 constexpr int kD2Warps = 4;
 constexpr int kD2Threads = 32 * kD2Warps;
 constexpr int kD2Rows = 16;                  // tokens per warp block
 constexpr int kD2Stage = kD2Rows * 256;      // 16 token rows of 128 bf16
 
-size_t dense2_smem(int G) {   // queries + rings; the rings also hold the warps' final states
-    return (size_t)G * 128 * 4 + std::max((size_t)kD2Warps * 4 * kD2Stage, (size_t)kD2Warps * G * 130 * 4);
+size_t dense2_smem(int G) {   // rings (they also hold the warps' final states); with more than four q-heads, the queries
+    return (G > 4 ? (size_t)G * 128 * 4 : 0) + std::max((size_t)kD2Warps * 4 * kD2Stage, (size_t)kD2Warps * G * 130 * 4);
 }
 
 __device__ __forceinline__ void bf16x2_to_f2(uint32_t w, uint64_t& out) {
     out = tc::f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// One 16-token block of a warp's state: scores of tokens 4 ps + tg (every lane of a token group ends with the
+// token's score), the online softmax update, and the weighted values.
+template <int G, int J0 = 0, int GH = G>
+__device__ __forceinline__ void dense_block_heads(const uint8_t* Kt, const uint8_t* Vt, int t0, int t_end, int tg, int fo,
+                                                  int lane, const uint64_t (&q2)[G][8], float (&m)[G], float (&l)[G],
+                                                  uint64_t (&acc)[G][2]) {
+    using namespace tc;
+    float sc[GH][4];
+#pragma unroll
+    for (int ps = 0; ps < 4; ++ps) {
+        const int r = 4 * ps + tg;
+        const uint4 ka = *reinterpret_cast<const uint4*>(Kt + r * 256 + (((2 * fo) ^ (r & 15)) << 4));
+        const uint4 kb = *reinterpret_cast<const uint4*>(Kt + r * 256 + (((2 * fo + 1) ^ (r & 15)) << 4));
+        const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+        uint64_t kp[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bf16x2_to_f2(kw[e], kp[e]);
+#pragma unroll
+        for (int jj = 0; jj < GH; ++jj) {
+            const int jq = J0 + jj;
+            uint64_t s2 = 0ull;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                s2 = f2_fma(q2[jq][e], kp[e], s2);
+            }
+            const float2 sv = f2_unpack(s2);
+            float v = sv.x + sv.y;
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            sc[jj][ps] = (t0 + r < t_end) ? v : -INFINITY;
+        }
+    }
+    // online softmax over the block: max and weight sum across the four token groups (weights overwrite scores)
+#pragma unroll
+    for (int jj = 0; jj < GH; ++jj) {
+        const int jq = J0 + jj;
+        float bm = fmaxf(fmaxf(sc[jj][0], sc[jj][1]), fmaxf(sc[jj][2], sc[jj][3]));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+        const float mn = fmaxf(m[jq], bm);
+        const float f = (m[jq] == -INFINITY) ? 0.0f : __expf(m[jq] - mn);
+        float ls = 0.0f;
+#pragma unroll
+        for (int ps = 0; ps < 4; ++ps) {
+            sc[jj][ps] = sc[jj][ps] == -INFINITY ? 0.0f : __expf(sc[jj][ps] - mn);
+            ls += sc[jj][ps];
+        }
+        ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 16);
+        l[jq] = l[jq] * f + ls;
+        const uint64_t f2 = f2_pack(f, f);
+        acc[jq][0] = f2_mul(acc[jq][0], f2);
+        acc[jq][1] = f2_mul(acc[jq][1], f2);
+        m[jq] = mn;
+    }
+    // values: lane = features 4 lane .. 4 lane + 3; token 4 ps + g's weight sits in lanes 8 g .. 8 g + 7
+#pragma unroll
+    for (int t = 0; t < kD2Rows; ++t) {
+        const uint2 vv = *reinterpret_cast<const uint2*>(Vt + t * 256 + lane * 8);
+        uint64_t vp0, vp1;
+        bf16x2_to_f2(vv.x, vp0);
+        bf16x2_to_f2(vv.y, vp1);
+#pragma unroll
+        for (int jj = 0; jj < GH; ++jj) {
+            const int jq = J0 + jj;
+            const float pt = __shfl_sync(0xffffffffu, sc[jj][t >> 2], (t & 3) * 8);
+            const uint64_t p2 = f2_pack(pt, pt);
+            acc[jq][0] = f2_fma(p2, vp0, acc[jq][0]);
+            acc[jq][1] = f2_fma(p2, vp1, acc[jq][1]);
+        }
+    }
 }
 
 template <int G>
@@ -227,7 +305,112 @@ __global__ void __launch_bounds__(kD2Threads) dense_bf16_kernel(int T, int Ts, i
                                                                 float* __restrict__ partial, int n_split) {
     using namespace tc;
     extern __shared__ __align__(16) uint8_t dsm[];
-    float* Qs = reinterpret_cast<float*>(dsm);
+    const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tg = lane >> 3, fo = lane & 7;            // scores: token tg of a pass, features 16 fo .. 16 fo + 15
+    uint8_t* wbase = dsm + warp * 4 * kD2Stage;         // Kt[2], Vt[2]
+    const int per = (int)cdiv(T, n_split);
+    const int t_begin = split * per, t_end = min(T, t_begin + per);
+    // this lane's 16 query features of every q-head, pre-scaled
+    uint64_t q2[G][8];
+#pragma unroll
+    for (int jq = 0; jq < G; ++jq) {
+        const uint4* src = reinterpret_cast<const uint4*>(q + ((int64_t)b * H_q + h * G + jq) * 128 + 16 * fo);
+        const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float lo = __uint_as_float(w[e] << 16) * scale, hi = __uint_as_float(w[e] & 0xffff0000u) * scale;
+            q2[jq][e] = f2_pack(lo, hi);
+        }
+    }
+    const int nblk = t_end > t_begin ? (int)cdiv(t_end - t_begin, kD2Rows) : 0;
+    auto issue = [&](int k) {
+        const int blk = warp + k * kD2Warps;
+        if (blk < nblk) {
+            const int t0 = t_begin + blk * kD2Rows;
+            uint8_t* Kt = wbase + (k & 1) * kD2Stage;
+            uint8_t* Vt = wbase + (2 + (k & 1)) * kD2Stage;
+#pragma unroll 4
+            for (int i = lane; i < kD2Rows * 16; i += 32) {
+                const int r = i >> 4, c = i & 15;
+                const int t = t0 + r;
+                const bool ok = t < t_end;
+                const int64_t off = (((int64_t)b * Ts + (ok ? t : t_begin)) * H_kv + h) * 128 + c * 8;
+                cp_async16(reinterpret_cast<uint4*>(Kt + r * 256 + ((c ^ (r & 15)) << 4)), K + off, ok);
+                cp_async16(reinterpret_cast<uint4*>(Vt + r * 256 + (c << 4)), V + off, ok);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    float m[G], l[G];
+    uint64_t acc[G][2];
+#pragma unroll
+    for (int jq = 0; jq < G; ++jq) {
+        m[jq] = -INFINITY;
+        l[jq] = 0.0f;
+        acc[jq][0] = acc[jq][1] = 0ull;
+    }
+    issue(0);
+    for (int k = 0; warp + k * kD2Warps < nblk; ++k) {
+        issue(k + 1);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncwarp();
+        const uint8_t* Kt = wbase + (k & 1) * kD2Stage;
+        const uint8_t* Vt = wbase + (2 + (k & 1)) * kD2Stage;
+        const int t0 = t_begin + (warp + k * kD2Warps) * kD2Rows;
+        dense_block_heads<G>(Kt, Vt, t0, t_end, tg, fo, lane, q2, m, l, acc);
+        __syncwarp();   // this stage is read; the next issue refills it
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // combine the warps' softmax states through shared memory (the rings are free): one record per CTA
+    __syncthreads();
+    float* st = reinterpret_cast<float*>(dsm);     // [kD2Warps][G][130]
+#pragma unroll
+    for (int jq = 0; jq < G; ++jq) {
+        float* w = st + (warp * G + jq) * 130;
+        const float2 a0 = f2_unpack(acc[jq][0]), a1 = f2_unpack(acc[jq][1]);
+        *reinterpret_cast<float2*>(w + lane * 4) = a0;
+        *reinterpret_cast<float2*>(w + lane * 4 + 2) = a1;
+        if (lane == 0) {
+            w[128] = m[jq];
+            w[129] = l[jq];
+        }
+    }
+    __syncthreads();
+    for (int jq = warp; jq < G; jq += kD2Warps) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kD2Warps; ++w) M = fmaxf(M, st[(w * G + jq) * 130 + 128]);
+        float L = 0.0f, a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int w = 0; w < kD2Warps; ++w) {
+            const float* src = st + (w * G + jq) * 130;
+            const float mw = src[128];
+            const float f = (mw == -INFINITY) ? 0.0f : __expf(mw - M);
+            L = fmaf(f, src[129], L);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] = fmaf(f, src[lane * 4 + e], a[e]);
+        }
+        float* dst = partial + (((int64_t)b * H_q + h * G + jq) * n_split + split) * 130;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[lane * 4 + e] = a[e];
+        if (lane == 0) {
+            dst[128] = M;
+            dst[129] = L;
+        }
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kD2Threads) dense_bf16_smemq_kernel(int T, int Ts, int H_q, int H_kv, float scale,
+                                                                const __nv_bfloat16* __restrict__ q,
+                                                                const __nv_bfloat16* __restrict__ K,
+                                                                const __nv_bfloat16* __restrict__ V,
+                                                                float* __restrict__ partial, int n_split) {
+    using namespace tc;
+    extern __shared__ __align__(16) uint8_t dsm[];
+    float* Qs = reinterpret_cast<float*>(dsm);   // [G][128] pre-scaled queries
     const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint8_t* wbase = dsm + G * 128 * 4 + warp * 4 * kD2Stage;   // Kt[2], Vt[2]
@@ -410,14 +593,17 @@ template <int G>
 static cudaError_t dense2_go(int B, int T, int Ts, int H_q, int H_kv, float scale, const void* q, const void* k, const void* v,
                              float* partial, int n_split, cudaStream_t st) {
     const size_t smem = dense2_smem(G);
-    cudaError_t e = cudaFuncSetAttribute(dense_bf16_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     // the kv-heads of one token range are adjacent in launch order (they read the same token rows)
     dim3 grid((unsigned)H_kv, (unsigned)n_split, (unsigned)B);
-    dense_bf16_kernel<G><<<grid, kD2Threads, smem, st>>>(T, Ts, H_q, H_kv, scale, (const __nv_bfloat16*)q,
-                                                        (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, partial,
-                                                        n_split);
-    return cudaGetLastError();
+    auto go = [&](auto kern) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kD2Threads, smem, st>>>(T, Ts, H_q, H_kv, scale, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
+                                             (const __nv_bfloat16*)v, partial, n_split);
+        return cudaGetLastError();
+    };
+    if constexpr (G <= 4) return go(dense_bf16_kernel<G>);
+    else return go(dense_bf16_smemq_kernel<G>);
 }
 
 cudaError_t launch_dense(int B, int T, int Ts, int H_q, int H_kv, int d, int dtype, float scale, const void* q, const void* k,

@@ -1,5 +1,9 @@
-// dequant.cu -- int4 latent caches on the tensor-core path: an exact two-term bf16 split of the dequantised
-// coefficients, and the matching column duplication of the layer's basis.
+// dequant.cu -- int4 latent caches on the tensor-core path: by default an fp16 copy of the dequantised
+// coefficients (and of the layer's basis), or with LOWRAM_FLAG_INT4_EXACT_SPLIT an exact two-term bf16 split of
+// them and the matching column duplication of the basis.
+//
+// fp16 copy: code * scale rounded to fp16 (11-bit significand, 2^-12 relative); the basis, bf16, is exact in fp16
+// down to magnitudes of 2^-14, and the tensor-core kernels' kind::f16 MMAs take fp16 A and B alike.
 //
 // Composing the low-rank key cache with quantisation ("LowRAM Paper: Amortised Values and Low-Rank Keys for KV
 // Compression", the quantisation / eviction composition) stores the latent coefficients as int4 codes with one
@@ -46,19 +50,83 @@ __global__ void int4_split_kernel(const uint32_t* __restrict__ codes, const __ha
     dst[(r + k) / 8] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-// out[n] = [W[n] | W[n]] for the n rows of the basis, 16 bytes per thread.
-__global__ void dup_cols_kernel(const uint4* __restrict__ W, int64_t rows, int r, uint4* __restrict__ out) {
+// out[n] = [W[n] | W[n]] for the rows of `batches` bases of `rows` rows each (basis c starts c * stride8 16-byte
+// pieces into W; the outputs are packed), 16 bytes per thread.
+__global__ void dup_cols_kernel(const uint4* __restrict__ W, int64_t rows, int batches, int64_t stride8, int r,
+                                uint4* __restrict__ out) {
     const int per_row = r / 8;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= rows * per_row) return;
-    const int64_t row = i / per_row;
+    if (i >= rows * batches * per_row) return;
+    const int64_t row = i / per_row;                 // packed row over all bases
     const int k = (int)(i - row * per_row);
-    const uint4 v = __ldg(W + i);
+    const int64_t c = row / rows, rl = row - c * rows;
+    const uint4 v = __ldg(W + c * stride8 + rl * per_row + k);
     out[row * 2 * per_row + k] = v;
     out[row * 2 * per_row + per_row + k] = v;
 }
 
+// One thread per 8 consecutive coefficients: fp16(code * scale), 16 bytes out.
+__global__ void int4_f16_kernel(const uint32_t* __restrict__ codes, const __half* __restrict__ scales, int64_t rows,
+                                int r, __half* __restrict__ out) {
+    const int per_row = r / 8;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= rows * per_row) return;
+    const int64_t row = i / per_row;
+    const int k = (int)(i - row * per_row) * 8;
+    const uint32_t w = __ldg(codes + i);
+    const float sc = __half2float(__ldg(scales + row * (r / 32) + (k >> 5)));
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int n0 = (int)((w >> (8 * e)) & 0xFu), n1 = (int)((w >> (8 * e + 4)) & 0xFu);
+        const __half2 h2 = __floats2half2_rn((float)(n0 >= 8 ? n0 - 16 : n0) * sc, (float)(n1 >= 8 ? n1 - 16 : n1) * sc);
+        o[e] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// fp16 copies of `batches` bf16 bases of `rows` rows (basis c starts c * stride8 16-byte pieces into W; outputs
+// packed): every bf16 value whose magnitude is at least 2^-14 is exact in fp16.
+__global__ void bf16_f16_kernel(const uint4* __restrict__ W, int64_t rows, int batches, int64_t stride8, int r,
+                                uint4* __restrict__ out) {
+    const int per_row = r / 8;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= rows * batches * per_row) return;
+    const int64_t row = i / per_row;
+    const int k = (int)(i - row * per_row);
+    const int64_t c = row / rows, rl = row - c * rows;
+    const uint4 v = __ldg(W + c * stride8 + rl * per_row + k);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(u[e] << 16), __uint_as_float(u[e] & 0xffff0000u));
+        o[e] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 }  // namespace
+
+cudaError_t launch_int4_to_f16(const void* codes, const void* scales, int64_t rows, int r, void* out,
+                               cudaStream_t st) {
+    const int64_t n = rows * (r / 8);
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    int4_f16_kernel<<<(unsigned)cdiv(n, threads), threads, 0, st>>>((const uint32_t*)codes, (const __half*)scales,
+                                                                      rows, r, (__half*)out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bf16_to_f16(const void* W, int64_t rows, int r, void* out, cudaStream_t st, int batches,
+                               int64_t batch_stride) {
+    const int64_t n = rows * batches * (r / 8);
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    bf16_f16_kernel<<<(unsigned)cdiv(n, threads), threads, 0, st>>>((const uint4*)W, rows, batches, batch_stride / 8, r,
+                                                                      (uint4*)out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_int4_split(const void* codes, const void* scales, int64_t rows, int r, void* out,
                               cudaStream_t st) {
@@ -70,11 +138,13 @@ cudaError_t launch_int4_split(const void* codes, const void* scales, int64_t row
     return cudaGetLastError();
 }
 
-cudaError_t launch_dup_cols(const void* W, int64_t rows, int r, void* out, cudaStream_t st) {
-    const int64_t n = rows * (r / 8);
+cudaError_t launch_dup_cols(const void* W, int64_t rows, int r, void* out, cudaStream_t st, int batches,
+                            int64_t batch_stride) {
+    const int64_t n = rows * batches * (r / 8);
     if (n == 0) return cudaSuccess;
     const int threads = 256;
-    dup_cols_kernel<<<(unsigned)cdiv(n, threads), threads, 0, st>>>((const uint4*)W, rows, r, (uint4*)out);
+    dup_cols_kernel<<<(unsigned)cdiv(n, threads), threads, 0, st>>>((const uint4*)W, rows, batches, batch_stride / 8, r,
+                                                                      (uint4*)out);
     return cudaGetLastError();
 }
 

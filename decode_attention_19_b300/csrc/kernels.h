@@ -1,6 +1,7 @@
 // kernels.h -- host launchers of liblowram.so's kernels (internal; the public ABI is include/lowram.h).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -10,6 +11,11 @@
 namespace lowram {
 
 void set_error_message(const char* fmt, ...);
+
+// Internal coefficient dtype of the decode kernels' view of a shape: an fp16 copy of an int4 cache's dequantised
+// coefficients in the workspace (the key and value passes then take fp16 operands: that copy, an fp16 copy of the
+// basis, and the folded predictor weights in fp16).  Not a public lowram_dtype.
+constexpr int32_t kCoefF16 = 100;
 
 // Everything a decode call needs, already validated by the ABI layer.
 struct DecodeArgs {
@@ -41,7 +47,22 @@ struct DecodeArgs {
     float* sall;         // [B, H_q, T] scaled logits of every q-head (tensor-core path), or null
     int32_t* cnt;        // [B, H_kv] finished-chunk counters for the merge fused into K3, or null
     int32_t* hit;        // [B, H_kv, S_eff] residual row of each selected token or -1 (tensor-core path), or null
+    void* fold;          // [copies, H_kv, m, r] bf16: w1[h] . basis_h, folded by the selection kernel (tensor-core
+                         // path); one copy per sequence when a basis or a predictor is given per sequence
+    long long wait_cycles;   // pipeline wait limit of the value pass in SM cycles; 0 = the default
     uint32_t* check;
+};
+
+// The value predictor's first layer folded into the basis (tensor-core value pass): F[h] = w1[h] . basis_h,
+// [H_kv, m, r] bf16, made by spare CTAs of the selection kernel.
+struct FoldArgs {
+    const __nv_bfloat16* w1;      // [H_kv, m, d] (sequence c's at c * mlp_stride)
+    const __nv_bfloat16* basis;   // [H_kv*d, r] (sequence c's at c * basis_stride)
+    void* F;                      // [copies, H_kv, m, r] bf16 (fp16 with f16_out); null: no folding
+    int H_kv, d, m, r;
+    int copies;                   // 1, or B when a basis or a predictor is given per sequence
+    int64_t basis_stride, mlp_stride;
+    bool f16_out;
 };
 
 // Chunk (selected tokens per vregen CTA) used by each path.
@@ -54,9 +75,10 @@ cudaError_t launch_score_simt(const DecodeArgs& a, cudaStream_t st);
 // K2: exact top-n per problem row (values [P][T] -> ascending indices [P][n]).  For the value pass it can also
 // zero zero_cnt[row] (merge counters) and write hit[row][j] = position of token out[row][j] in the row's
 // ascending residual list res_idx[row][0..n_res) or -1, checking the list (LOWRAM_CHECK_RES_INDEX into check).
+// With `fold`, spare CTAs of the same launch also compute the folded weights (they do not wait for the kernel before).
 cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, int32_t* out, cudaStream_t st,
                                int32_t* zero_cnt = nullptr, int32_t* hit = nullptr, const int32_t* res_idx = nullptr,
-                               int n_res = 0, uint32_t* check = nullptr);
+                               int n_res = 0, uint32_t* check = nullptr, const FoldArgs* fold = nullptr);
 size_t select_scratch_bytes(int P, int T, int n_keep);
 // K3: value regeneration + softmax partials for selected chunks of 32 (CUDA-core path)
 cudaError_t launch_vregen_simt(const DecodeArgs& a, cudaStream_t st);
@@ -66,7 +88,7 @@ cudaError_t launch_merge(int B, int H_q, int n_chunks, int d, const float* parti
 
 // Tensor-core path (bf16 caches): which of K1 / K3 cover a shape.  K3 on the tensor cores needs K1 on them
 // too (it reads the scaled logits K1 stores) and writes partial records of tc_partial_width floats: the
-// weighted hidden-unit sums [m], the weighted residual sums [d], the chunk's max logit and weight sum.
+// softmax-weighted value sum [d], the chunk's max logit and weight sum (the layout launch_merge reads).
 bool tc_score_supported(const lowram_decode_shape& s);
 bool tc_vregen_supported(const lowram_decode_shape& s);
 int tc_partial_width(const lowram_decode_shape& s);
@@ -74,12 +96,15 @@ bool tc_fused_merge(const lowram_decode_shape& s, int n_chunks);
 constexpr int kTcChunk = 128;
 cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st);
-// K4 for the tensor-core path: merge, then the predictor's second layer on the merged sums
-cudaError_t launch_merge_w2(const DecodeArgs& a, int n_chunks, cudaStream_t st);
 // int4 caches on the tensor-core path: the exact split of the dequantised coefficients into bf16 [hi | lo]
 // ([rows, 2r]), and the basis with its columns repeated ([rows, 2r]); see dequant.cu
 cudaError_t launch_int4_split(const void* codes, const void* scales, int64_t rows, int r, void* out, cudaStream_t st);
-cudaError_t launch_dup_cols(const void* W, int64_t rows, int r, void* out, cudaStream_t st);
+// int4 caches, default: out [rows, r] fp16 = fp16(code * scale); and an fp16 copy of bf16 basis rows (batched)
+cudaError_t launch_int4_to_f16(const void* codes, const void* scales, int64_t rows, int r, void* out, cudaStream_t st);
+cudaError_t launch_bf16_to_f16(const void* W, int64_t rows, int r, void* out, cudaStream_t st, int batches = 1,
+                               int64_t batch_stride = 0);
+cudaError_t launch_dup_cols(const void* W, int64_t rows, int r, void* out, cudaStream_t st, int batches = 1,
+                            int64_t batch_stride = 0);
 
 // Write side
 struct CompressArgs {

@@ -5,6 +5,8 @@
 #include <cstdio>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "predict_fit.h"
@@ -14,7 +16,20 @@ using namespace lowram;
 
 namespace {
 
+// A named NVTX range around a library call or one stage of its launch sequence, for timeline tools (Nsight Systems,
+// Nsight Compute's range filters); without a tool attached a push and a pop cost a call through a null hook each.
+struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range&) = delete;
+    Range& operator=(const Range&) = delete;
+};
+
 thread_local char g_msg[512] = "";
+
+// Pipeline wait limit of the tensor-core value pass in SM clock cycles (0: the kernels' default of ~1 s); set by
+// lowram_set_wait_limit, a testing aid for the timeout path.
+long long g_wait_cycles = 0;
 
 lowram_status fail(lowram_status st, const char* fmt, ...) {
     va_list ap;
@@ -75,16 +90,26 @@ lowram_status check_decode_shape(const lowram_decode_shape* s) {
         return fail(LOWRAM_ERR_INVALID_ARG, "res_dtype=%d", s->res_dtype);
     if (s->T > 0 && s->max_pos < 1) return fail(LOWRAM_ERR_INVALID_ARG, "max_pos=%d", s->max_pos);
     if ((int64_t)s->B * s->T * s->r > ((int64_t)1 << 40)) return fail(LOWRAM_ERR_UNSUPPORTED, "cache too large");
+    const int64_t nb = (int64_t)s->H_kv * s->d * s->r, nm = (int64_t)s->H_kv * s->m * s->d;
+    if (s->basis_batch_stride != 0 && (s->basis_batch_stride < nb || s->basis_batch_stride % 8 != 0))
+        return fail(LOWRAM_ERR_INVALID_ARG, "basis_batch_stride=%lld (0, or >= H_kv*d*r = %lld and a multiple of 8)",
+                    (long long)s->basis_batch_stride, (long long)nb);
+    if (s->mlp_batch_stride != 0 && (s->mlp_batch_stride < nm || s->mlp_batch_stride % 8 != 0))
+        return fail(LOWRAM_ERR_INVALID_ARG, "mlp_batch_stride=%lld (0, or >= H_kv*m*d = %lld and a multiple of 8)",
+                    (long long)s->mlp_batch_stride, (long long)nm);
+    if (s->flags & ~LOWRAM_FLAG_INT4_EXACT_SPLIT) return fail(LOWRAM_ERR_INVALID_ARG, "flags=0x%x", s->flags);
     return LOWRAM_OK;
 }
 
 struct DecodeLayout {
     bool tc_score, tc_vregen;
     bool split;                 // int4 cache run on the tensor cores through the exact bf16 split (dequant.cu)
-    lowram_decode_shape sx;     // the shape the kernels see: with split, bf16 coefficients of rank 2r
+    bool f16;                   // int4 cache run on the tensor cores through an fp16 copy (the default)
+    lowram_decode_shape sx;     // the shape the kernels see: with split, bf16 coefficients of rank 2r; with f16,
+                                // fp16 coefficients (kCoefF16) and an fp16 basis
     int chunk, n_chunks, S_eff, PW;
     bool fused_merge;
-    size_t off_key, off_sel, off_partial, off_sall, off_cnt, off_hit, off_asplit, off_bsplit, total;
+    size_t off_key, off_sel, off_partial, off_sall, off_cnt, off_hit, off_fold, off_asplit, off_bsplit, total;
 };
 
 DecodeLayout decode_layout(const lowram_decode_shape& s) {
@@ -93,10 +118,13 @@ DecodeLayout decode_layout(const lowram_decode_shape& s) {
     L.sx = s;
     if (s.coef_dtype == LOWRAM_INT4_G32 && s.act_dtype == LOWRAM_BF16) {
         lowram_decode_shape x = s;
-        x.coef_dtype = LOWRAM_BF16;
-        x.r = 2 * s.r;
+        const bool exact = (s.flags & LOWRAM_FLAG_INT4_EXACT_SPLIT) != 0;
+        x.coef_dtype = exact ? LOWRAM_BF16 : kCoefF16;
+        x.r = exact ? 2 * s.r : s.r;
+        // the repeated bases [W | W] (or the fp16 bases) are packed in the workspace, one per sequence when they differ
+        x.basis_batch_stride = s.basis_batch_stride ? (int64_t)s.H_kv * s.d * x.r : 0;
         if (tc_score_supported(x) && tc_vregen_supported(x)) {
-            L.split = true;
+            (exact ? L.split : L.f16) = true;
             L.sx = x;
         }
     }
@@ -119,10 +147,15 @@ DecodeLayout decode_layout(const lowram_decode_shape& s) {
     off += L.fused_merge ? align256(sizeof(int32_t) * (size_t)s.B * s.H_kv) : 0;
     L.off_hit = off;
     off += L.tc_vregen ? align256(sizeof(int32_t) * (size_t)s.B * s.H_kv * L.S_eff) : 0;
+    L.off_fold = off;
+    const size_t copies = (s.basis_batch_stride || s.mlp_batch_stride) ? (size_t)s.B : 1;
+    off += L.tc_vregen ? align256(sizeof(uint16_t) * copies * s.H_kv * s.m * L.sx.r) : 0;
     L.off_asplit = off;
-    off += L.split ? align256(sizeof(uint16_t) * (size_t)s.B * s.T * L.sx.r) : 0;
+    off += (L.split || L.f16) ? align256(sizeof(uint16_t) * (size_t)s.B * s.T * L.sx.r) : 0;
     L.off_bsplit = off;
-    off += L.split ? align256(sizeof(uint16_t) * (size_t)s.H_kv * s.d * L.sx.r) : 0;
+    off += (L.split || L.f16)
+               ? align256(sizeof(uint16_t) * (s.basis_batch_stride ? (size_t)s.B : 1) * s.H_kv * s.d * L.sx.r)
+               : 0;
     L.total = off;
     return L;
 }
@@ -141,7 +174,13 @@ void set_error_message(const char* fmt, ...) {
 
 extern "C" {
 
-int32_t lowram_version(void) { return 100; }
+int32_t lowram_version(void) { return 200; }
+
+lowram_status lowram_set_wait_limit(int64_t cycles) {
+    if (cycles < 0) return fail(LOWRAM_ERR_INVALID_ARG, "cycles=%lld", (long long)cycles);
+    g_wait_cycles = (long long)cycles;
+    return LOWRAM_OK;
+}
 
 const char* lowram_last_error(void) { return g_msg; }
 
@@ -176,6 +215,7 @@ lowram_status lowram_decode_uses_tensor_cores(const lowram_decode_shape* shape, 
 
 lowram_status lowram_rope_table(int32_t d, double theta, int32_t max_pos, float* cos_out, float* sin_out,
                                 void* stream) {
+    const Range nvtx_range(__func__);
     if (d <= 0 || d % 2 || max_pos < 0 || !(theta > 0.0)) return fail(LOWRAM_ERR_INVALID_ARG, "d=%d max_pos=%d theta=%g", d, max_pos, theta);
     if (max_pos == 0) return LOWRAM_OK;
     if (!cos_out || !sin_out) return fail(LOWRAM_ERR_INVALID_ARG, "NULL table pointer");
@@ -228,8 +268,10 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     a.sall = L.tc_vregen ? (float*)(ws + L.off_sall) : nullptr;
     a.cnt = L.fused_merge ? (int32_t*)(ws + L.off_cnt) : nullptr;
     a.hit = (L.tc_vregen && s.n_res > 0) ? (int32_t*)(ws + L.off_hit) : nullptr;
+    a.fold = L.tc_vregen ? (void*)(ws + L.off_fold) : nullptr;
+    a.wait_cycles = g_wait_cycles;
     a.check = (uint32_t*)ws;
-    if (L.split) {   // the kernels read [hi | lo] and [W | W]: bf16 operands of rank 2r, exactly C W^T
+    if (L.split || L.f16) {   // the kernels read [hi | lo] and [W | W] (bf16, rank 2r, exactly C W^T), or fp16 copies
         a.coef = ws + L.off_asplit;
         a.coef_scale = nullptr;
         a.basis = ws + L.off_bsplit;
@@ -241,25 +283,48 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     };
     cudaError_t e = mark(0);
     if (e == cudaSuccess && L.split && (int64_t)s.B * s.T > 0) {
+        const Range stage("lowram int4 split");
         e = launch_int4_split(coef, coef_scale, (int64_t)s.B * s.T, s.r, ws + L.off_asplit, cs);
-        if (e == cudaSuccess) e = launch_dup_cols(basis, (int64_t)s.H_kv * s.d, s.r, ws + L.off_bsplit, cs);
+        if (e == cudaSuccess)
+            e = launch_dup_cols(basis, (int64_t)s.H_kv * s.d, s.r, ws + L.off_bsplit, cs,
+                                s.basis_batch_stride ? s.B : 1, s.basis_batch_stride);
         if (e != cudaSuccess) return cuda_fail(e, "int4 split");
     }
-    if (e == cudaSuccess && (int64_t)s.B * s.T > 0 && (L.S_eff > 0 || key_out))
+    if (e == cudaSuccess && L.f16 && (int64_t)s.B * s.T > 0) {
+        const Range stage("lowram int4 to fp16");
+        e = launch_int4_to_f16(coef, coef_scale, (int64_t)s.B * s.T, s.r, ws + L.off_asplit, cs);
+        if (e == cudaSuccess)
+            e = launch_bf16_to_f16(basis, (int64_t)s.H_kv * s.d, s.r, ws + L.off_bsplit, cs,
+                                   s.basis_batch_stride ? s.B : 1, s.basis_batch_stride);
+        if (e != cudaSuccess) return cuda_fail(e, "int4 to fp16");
+    }
+    if (e == cudaSuccess && (int64_t)s.B * s.T > 0 && (L.S_eff > 0 || key_out)) {
+        const Range stage("lowram key pass");
         e = L.tc_score ? launch_score_tc(a, cs) : launch_score_simt(a, cs);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "score");
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event");
-    if ((int64_t)s.B * L.S_eff > 0)
-        e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs, a.cnt, a.hit, res_idx, s.n_res, a.check);
+    // the fold takes bf16 bases: the caller's with an fp16 copy for the kernels, else the ones the kernels read
+    const FoldArgs fold{(const __nv_bfloat16*)a.w1, (const __nv_bfloat16*)(L.f16 ? basis : a.basis), a.fold, s.H_kv,
+                        s.d, s.m, L.sx.r, (s.basis_batch_stride || s.mlp_batch_stride) ? s.B : 1,
+                        L.f16 ? s.basis_batch_stride : L.sx.basis_batch_stride, s.mlp_batch_stride, L.f16};
+    if ((int64_t)s.B * L.S_eff > 0) {
+        const Range stage("lowram selection");
+        e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs, a.cnt, a.hit, res_idx, s.n_res, a.check,
+                               L.tc_vregen ? &fold : nullptr);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "select");
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event");
-    if ((int64_t)s.B * L.S_eff > 0) e = L.tc_vregen ? launch_vregen_tc(a, cs) : launch_vregen_simt(a, cs);
+    if ((int64_t)s.B * L.S_eff > 0) {
+        const Range stage("lowram value pass");
+        e = L.tc_vregen ? launch_vregen_tc(a, cs) : launch_vregen_simt(a, cs);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "vregen");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event");
     const bool merged = L.fused_merge && (int64_t)s.B * L.S_eff > 0;   // K3 merged as it finished
     if (any && !merged) {
         const int nc = (int64_t)s.B * L.S_eff > 0 ? L.n_chunks : 0;
-        e = L.tc_vregen ? launch_merge_w2(a, nc, cs) : launch_merge(s.B, s.H_q, nc, s.d, a.partial, out, lse, cs);
+        e = launch_merge(s.B, s.H_q, nc, s.d, a.partial, out, lse, cs);
     }
     if (e != cudaSuccess) return cuda_fail(e, "merge");
     if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "event");
@@ -272,6 +337,7 @@ lowram_status lowram_decode_attn(const lowram_decode_shape* shape, const void* q
                                  const float* b1, const float* b2, const int32_t* res_idx, const void* res_val,
                                  const void* res_scale, float* out, float* lse, int32_t* sel_out, float* key_out,
                                  void* workspace, size_t workspace_bytes, void* stream) {
+    const Range nvtx_range(__func__);
     return decode_impl(shape, q, coef, coef_scale, pos, rope_cos, rope_sin, basis, w1, w2, b1, b2, res_idx, res_val,
                        res_scale, out, lse, sel_out, key_out, workspace, workspace_bytes, stream, nullptr);
 }
@@ -283,6 +349,7 @@ lowram_status lowram_decode_attn_events(const lowram_decode_shape* shape, const 
                                         const void* res_val, const void* res_scale, float* out, float* lse,
                                         int32_t* sel_out, float* key_out, void* workspace, size_t workspace_bytes,
                                         void* stream, void* const* events) {
+    const Range nvtx_range(__func__);
     return decode_impl(shape, q, coef, coef_scale, pos, rope_cos, rope_sin, basis, w1, w2, b1, b2, res_idx, res_val,
                        res_scale, out, lse, sel_out, key_out, workspace, workspace_bytes, stream, events);
 }
@@ -335,6 +402,7 @@ lowram_status lowram_attention_mass_workspace_size(int32_t B, int32_t T, int32_t
 lowram_status lowram_attention_mass(int32_t B, int32_t T, int32_t W, int32_t H_q, int32_t H_kv, int32_t d,
                                     int32_t dtype, float sm_scale, const void* q_win, const void* k, float* mass_out,
                                     void* workspace, size_t workspace_bytes, void* stream) {
+    const Range nvtx_range(__func__);
     size_t need = 0;
     lowram_status st = lowram_attention_mass_workspace_size(B, T, W, H_q, H_kv, d, dtype, &need);
     if (st != LOWRAM_OK) return st;
@@ -361,6 +429,7 @@ lowram_status lowram_evict_plan_workspace_size(int32_t B, int32_t T, size_t* byt
 lowram_status lowram_evict_plan(int32_t B, int32_t T, int32_t n_sink, int32_t n_recent, int32_t T_keep,
                                 const float* mass, int32_t* keep_out, void* workspace, size_t workspace_bytes,
                                 void* stream) {
+    const Range nvtx_range(__func__);
     size_t need = 0;
     lowram_status st = lowram_evict_plan_workspace_size(B, T, &need);
     if (st != LOWRAM_OK) return st;
@@ -399,6 +468,7 @@ lowram_status lowram_predictor_grad(int32_t B, int32_t T, int32_t H_kv, int32_t 
                                     const void* keys, const void* values, const float* w1, const float* b1,
                                     const float* w2, const float* b2, float* loss_out, float* g_w1, float* g_b1,
                                     float* g_w2, float* g_b2, void* stream) {
+    const Range nvtx_range(__func__);
     lowram_status st = check_predictor_shape(B, T, H_kv, d, m, dtype);
     if (st != LOWRAM_OK) return st;
     const void* need[] = {w1, b1, w2, b2, loss_out, g_w1, g_b1, g_w2, g_b2};
@@ -427,6 +497,7 @@ lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d
                                    const void* keys, const void* values, int32_t steps, float lr, float beta1,
                                    float beta2, float eps, float* w1, float* b1, float* w2, float* b2,
                                    float* losses_out, void* workspace, size_t workspace_bytes, void* stream) {
+    const Range nvtx_range(__func__);
     lowram_status st = check_predictor_shape(B, T, H_kv, d, m, dtype);
     if (st != LOWRAM_OK) return st;
     size_t need = 0;
@@ -501,6 +572,7 @@ lowram_status lowram_fit_basis(const lowram_compress_shape* shape, const void* k
                                const float* rope_cos, const float* rope_sin, int32_t iters, uint64_t seed,
                                float* proj_out, void* const* basis_out, void* workspace, size_t workspace_bytes,
                                void* stream) {
+    const Range nvtx_range(__func__);
     size_t need = 0;
     lowram_status st = lowram_fit_basis_workspace_size(shape, &need);
     if (st != LOWRAM_OK) return st;
@@ -545,6 +617,7 @@ lowram_status lowram_compress(const lowram_compress_shape* shape, const void* ke
                               const float* const* b1, const float* const* b2, void* coef_out, void* coef_scale_out,
                               int32_t* const* res_idx_out, void* const* res_val_out, void* const* res_scale_out,
                               float* const* err_out, void* workspace, size_t workspace_bytes, void* stream) {
+    const Range nvtx_range(__func__);
     lowram_status st = check_compress_shape(shape);
     if (st != LOWRAM_OK) return st;
     const lowram_compress_shape& s = *shape;
@@ -650,6 +723,7 @@ static lowram_status dense_impl(int32_t B, int32_t T, int32_t Ts, int32_t H_q, i
 lowram_status lowram_dense_decode_attn(int32_t B, int32_t T, int32_t H_q, int32_t H_kv, int32_t d, int32_t dtype,
                                        float sm_scale, const void* q, const void* k, const void* v, float* out,
                                        float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    const Range nvtx_range(__func__);
     return dense_impl(B, T, T, H_q, H_kv, d, dtype, sm_scale, q, k, v, out, lse, workspace, workspace_bytes, stream);
 }
 
@@ -658,6 +732,7 @@ lowram_status lowram_dense_decode_attn(int32_t B, int32_t T, int32_t H_q, int32_
 // ------------------------------------------------------------------------------------------------
 lowram_status lowram_tail_append(int32_t B, int32_t T_cap, int32_t H_kv, int32_t d, int32_t dtype, int32_t t,
                                  const void* k_new, const void* v_new, void* tail_k, void* tail_v, void* stream) {
+    const Range nvtx_range(__func__);
     if (B < 0 || T_cap < 1 || H_kv < 1 || (d != 64 && d != 128))
         return fail(LOWRAM_ERR_INVALID_ARG, "B=%d T_cap=%d H_kv=%d d=%d", B, T_cap, H_kv, d);
     if (!is_act(dtype)) return fail(LOWRAM_ERR_INVALID_ARG, "dtype=%d", dtype);
@@ -676,6 +751,7 @@ lowram_status lowram_tail_decode_attn(int32_t B, int32_t T_cap, int32_t t_len, i
                                       int32_t dtype, float sm_scale, const void* q, const void* tail_k,
                                       const void* tail_v, float* out, float* lse, void* workspace,
                                       size_t workspace_bytes, void* stream) {
+    const Range nvtx_range(__func__);
     if (t_len < 0 || t_len > T_cap)
         return fail(LOWRAM_ERR_INVALID_ARG, "t_len=%d outside the tail's capacity %d", t_len, T_cap);
     return dense_impl(B, t_len, T_cap, H_q, H_kv, d, dtype, sm_scale, q, tail_k, tail_v, out, lse, workspace,
@@ -684,6 +760,7 @@ lowram_status lowram_tail_decode_attn(int32_t B, int32_t T_cap, int32_t t_len, i
 
 lowram_status lowram_merge_attn(int32_t B, int32_t H_q, int32_t d, const float* out_a, const float* lse_a,
                                 const float* out_b, const float* lse_b, float* out, float* lse, void* stream) {
+    const Range nvtx_range(__func__);
     if (B < 0 || H_q < 1 || d < 1) return fail(LOWRAM_ERR_INVALID_ARG, "B=%d H_q=%d d=%d", B, H_q, d);
     if (B == 0) return LOWRAM_OK;
     if (!out_a || !lse_a || !out_b || !lse_b || !out) return fail(LOWRAM_ERR_INVALID_ARG, "a required pointer is NULL");

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kTileThreads) score_simt_kernel(DecodeArgs a, 
     }
     for (int e = tid; e < g * d; e += kTileThreads) Qs[e] = ld((const TA*)a.q, ((int64_t)b * s.H_q + h * g) * d + e);
     __syncthreads();
-    rebuild_rows<TA>(Rows, coef, r, (const TA*)a.basis + (int64_t)h * d * r, d, As, Bs, Ks);
+    rebuild_rows<TA>(Rows, coef, r, (const TA*)a.basis + b * s.basis_batch_stride + (int64_t)h * d * r, d, As, Bs, Ks);
 
     for (int u = 0; u < 4; ++u) {
         const int t = warp * 4 + u;
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kTileThreads) vregen_simt_kernel(DecodeArgs a,
             if (ridx[j] < 0 || ridx[j] >= T || (j > 0 && ridx[j] <= ridx[j - 1])) flag(a.check, LOWRAM_CHECK_RES_INDEX);
     __syncthreads();
 
-    rebuild_rows<TA>(Rows, coef, r, (const TA*)a.basis + (int64_t)h * d * r, d, As, Bs, Ks);
+    rebuild_rows<TA>(Rows, coef, r, (const TA*)a.basis + b * s.basis_batch_stride + (int64_t)h * d * r, d, As, Bs, Ks);
     // scaled logits of the selected tokens (RoPE re-applied on the fly)
     for (int u = 0; u < 4; ++u) {
         const int t = warp * 4 + u;
@@ -143,8 +143,10 @@ __global__ void __launch_bounds__(kTileThreads) vregen_simt_kernel(DecodeArgs a,
             if (lane == 0) Ss[jq * kTileRows + t] = Tok[t] >= 0 ? v : -INFINITY;
         }
     }
-    predict_from_keys<TA, NJm, false>((const TA*)a.w1 + (int64_t)h * m * d, a.b1 ? a.b1 + (int64_t)h * m : nullptr,
-                                      (const TA*)a.w2 + (int64_t)h * d * m, a.b2 ? a.b2 + (int64_t)h * d : nullptr, d, m,
+    // a predictor per sequence: sequence b's weights mlp_batch_stride elements on, its biases [B, H_kv, .]
+    const int64_t mo = b * s.mlp_batch_stride, bias_bh = s.mlp_batch_stride ? bh : h;
+    predict_from_keys<TA, NJm, false>((const TA*)a.w1 + mo + (int64_t)h * m * d, a.b1 ? a.b1 + bias_bh * m : nullptr,
+                                      (const TA*)a.w2 + mo + (int64_t)h * d * m, a.b2 ? a.b2 + bias_bh * d : nullptr, d, m,
                                       As, Bs, Ks, Hs, Vs);
     // residual add: binary search of each selected token in the ascending residual list
     for (int u = 0; u < 4; ++u) {

@@ -56,6 +56,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// mbar_wait with a caller-given limit in SM clock cycles (a kernel parameter, so a test can shorten it).
+__device__ __forceinline__ bool mbar_wait_lim(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              long long limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > limit) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 // Bounded wait that ignores the abort flag: used while draining after an abort.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
     const long long t0 = clock64();
@@ -114,6 +129,16 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// Four rows of a 2D tensor map (box one row high, `x` the first column) at rows y0..y3, written to `dst` as four
+// consecutive box rows (the map's swizzle applies as for a tile load of those rows at that address).
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y0, int y1,
+                                            int y2, int y3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+        "%5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1, int c2) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
@@ -157,6 +182,10 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// The same with fp16 A and B (format code 0 in both operand fields).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor of a K-major operand stored as TMA's 128-byte swizzle writes it: rows
@@ -414,8 +443,10 @@ inline int sm_count() {
     return n > 0 ? n : 148;
 }
 
-// bf16 tensor [dims[rank-1]] ... [dims[0]] (dims[0] innermost), box of box[i] elements, 128B swizzle.
-inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box) {
+// bf16 (or fp16) tensor [dims[rank-1]] ... [dims[0]] (dims[0] innermost), box of box[i] elements, 128B swizzle.
+// Packed unless `outer_stride` (elements between consecutive indices of the outermost dimension, rank 3) is given.
+inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box,
+                     uint64_t outer_stride = 0, bool f16 = false) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t gdim[3], gstride[2];
@@ -427,7 +458,9 @@ inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
         if (i > 0) gstride[i - 1] = stride;
         stride *= dims[i];
     }
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gdim, gstride, bdim,
+    if (rank == 3 && outer_stride) gstride[1] = outer_stride * 2;
+    CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                    const_cast<void*>(base), gdim, gstride, bdim,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;

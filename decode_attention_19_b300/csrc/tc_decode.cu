@@ -49,6 +49,9 @@ constexpr int kSmemLimit = 232448;
 
 struct ScoreTcParams {
     int B, T, H_q, H_kv, r, max_pos, tiles_per_seq, n_tiles, KC, NU, NS;
+    int pps;            // tile pairs per sequence when every sequence has its own basis (pairs stay within a
+                        // sequence, whose basis both CTAs load), else 0 (pairs run over the whole batch)
+    uint32_t idesc;     // MMA instruction descriptor: bf16 operands, or fp16 (an int4 cache's fp16 copy)
     float scale;
     const __nv_bfloat16* q;
     const int32_t* pos;
@@ -66,6 +69,23 @@ struct ScoreTcParams {
 size_t score_smem_bytes(int NS, int UN, int H_q) {
     return 1024 + (size_t)NS * (kAChunkBytes + (UN / 2) * 128) + (size_t)H_q * 128 * 2 + 2 * 128 * 16 * 4 +
            8 * (2 * NS + 5) + 16;
+}
+
+// Tile of CTA `rank` in tile pair `pr`: its sequence b, first token t0, and whether it is real (a tile past the end
+// is computed on the last tile's data and not written).
+__device__ __forceinline__ void pair_tile(const ScoreTcParams& p, int pr, int rank, int& b, int& t0, bool& real) {
+    if (p.pps) {
+        b = pr / p.pps;
+        const int lt = 2 * (pr - b * p.pps) + rank;
+        real = lt < p.tiles_per_seq;
+        t0 = min(lt, p.tiles_per_seq - 1) * kTokTile;
+    } else {
+        const int tile = 2 * pr + rank;
+        real = tile < p.n_tiles;
+        const int lt = real ? tile : p.n_tiles - 1;
+        b = lt / p.tiles_per_seq;
+        t0 = (lt % p.tiles_per_seq) * kTokTile;
+    }
 }
 
 template <int G, int HPU>
@@ -94,8 +114,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
     const uint32_t peer = rank ^ 1u;
     // the pair walks a contiguous range of (tile pair, unit) items; CTA `rank` takes tile 2*pair + rank (a tile
     // past the end is computed on the last tile's data and not written)
-    const int n_items = (p.n_tiles + 1) / 2 * p.NU, cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const int n_pairs = p.pps ? p.B * p.pps : (p.n_tiles + 1) / 2;
+    const int n_items = n_pairs * p.NU, cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
     const int it_begin = (int)((int64_t)cl * n_items / ncl), it_end = (int)((int64_t)(cl + 1) * n_items / ncl);
+    // work item -> (tile pair pr, unit u)
+    auto item_up = [&](int it, int& u, int& pr) {
+        pr = it / p.NU;
+        u = it - pr * p.NU;
+    };
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.NS; ++i) {
             mbar_init(&b_full[i], 1);
@@ -135,9 +161,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
             uint32_t ib = 0;           // ring stages issued
             uint32_t s = 0, ph = 0;    // ring position of stage ib, kept incrementally (see the MMA issuer)
             for (int it = it_begin; it < it_end && !*abort_flag; ++it) {
-                const int pr = it / p.NU, u = it - pr * p.NU;
-                const int lt = min(2 * pr + (int)rank, p.n_tiles - 1);
-                const int b = lt / p.tiles_per_seq, t0 = (lt % p.tiles_per_seq) * kTokTile;
+                int u, pr;
+                item_up(it, u, pr);
+                int b, t0;
+                bool real_t;
+                pair_tile(p, pr, (int)rank, b, t0, real_t);
+                (void)real_t;   // a tile past the end is loaded like the last one
+                const int brow = u * UN + (int)rank * (UN / 2);
                 {
                     for (int kc = 0; kc < p.KC; ++kc, ++ib) {
                         if (!mbar_wait_cluster(&b_empty[s], ph ^ 1, abort_flag)) {
@@ -146,15 +176,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                         }
                         uint8_t* dA = St + s * kStage;
                         uint8_t* dB = dA + kAChunkBytes;
-                        const int brow = u * UN + (int)rank * (UN / 2);
                         if (rank == 0) {   // the even CTA's barrier counts both CTAs' bytes
                             mbar_expect_tx(&b_full[s], 2 * kStage);
                             tma_load_3d(dA, &tmA, &b_full[s], kc * kChunkK, t0, b);
-                            tma_load_2d(dB, &tmB, &b_full[s], kc * kChunkK, brow);
+                            if (p.pps) tma_load_3d(dB, &tmB, &b_full[s], kc * kChunkK, brow, b);
+                            else tma_load_2d(dB, &tmB, &b_full[s], kc * kChunkK, brow);
                         } else {
                             const uint32_t bar = peer_smem(&b_full[s], 0);
                             tma_load_3d_pair(dA, &tmA, bar, kc * kChunkK, t0, b);
-                            tma_load_2d_pair(dB, &tmB, bar, kc * kChunkK, brow);
+                            if (p.pps) tma_load_3d_pair(dB, &tmB, bar, kc * kChunkK, brow, b);
+                            else tma_load_2d_pair(dB, &tmB, bar, kc * kChunkK, brow);
                         }
                         if (++s == (uint32_t)p.NS) {
                             s = 0;
@@ -181,7 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
             // One thread feeds the tensor pipe (a 256x256x16 pair MMA every 128 SM cycles at full rate), so the
             // loop keeps the ring position incrementally and rebuilds no descriptor: a stage adds its byte offset
             // >> 4 to the descriptor of stage 0, a 16-wide k-step 32 bytes (2 units).
-            const uint32_t idesc = idesc_bf16(2 * kTokTile, UN);
+            const uint32_t idesc = p.idesc;
             const uint64_t st_desc = sdesc_sw128(smem_u32(St));
             uint32_t s = 0, ph = 0, j = 0;
             for (int it = it_begin; it < it_end && !*abort_flag; ++it, ++j) {
@@ -246,14 +277,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
         // no abort test in the loop conditions: every epilogue thread walks the same items and reaches the
         // same named barriers; after an abort the waits fail at once and the work is skipped
         for (int it = it_begin; it < it_end; ++it, ++j) {
-            const int pr = it / p.NU, u = it - pr * p.NU;
+            int u, pr;
+            item_up(it, u, pr);
             if (pr != cur_pr) {
                 cur_pr = pr;
-                const int tile = 2 * pr + (int)rank;
-                real = tile < p.n_tiles;      // a tile past the end is computed but writes nothing
-                const int lt = real ? tile : p.n_tiles - 1;
-                b = lt / p.tiles_per_seq;
-                t0 = (lt % p.tiles_per_seq) * kTokTile;
+                pair_tile(p, pr, (int)rank, b, t0, real);   // a tile past the end is computed but writes nothing
                 if (b != cur_b) {
                     named_bar_sync(1, 256);      // every epilogue thread is done with the previous query
                     if (!*abort_flag) {
@@ -457,7 +485,8 @@ bool g_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 7 || g == 8; }
 
 bool tc_score_supported(const lowram_decode_shape& s) {
     const int g = s.H_q / s.H_kv;
-    return s.act_dtype == LOWRAM_BF16 && s.coef_dtype == LOWRAM_BF16 && s.d == 128 && s.r % kChunkK == 0 &&
+    return s.act_dtype == LOWRAM_BF16 && (s.coef_dtype == LOWRAM_BF16 || s.coef_dtype == kCoefF16) && s.d == 128 &&
+           s.r % kChunkK == 0 &&
            s.r <= 1024 && g_ok(g) && s.T > 0 && s.H_q <= 128 && score_config(s.H_q, s.H_kv).NS >= 2 &&
            encode_fn() != nullptr;
 }
@@ -473,9 +502,12 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     p.max_pos = s.max_pos;
     p.tiles_per_seq = (int)cdiv(s.T, kTokTile);
     p.n_tiles = p.tiles_per_seq * s.B;
+    p.pps = s.basis_batch_stride ? (p.tiles_per_seq + 1) / 2 : 0;
+    const bool f16 = s.coef_dtype == kCoefF16;
     p.KC = s.r / kChunkK;
     const ScoreConfig cfg = score_config(s.H_q, s.H_kv);
     p.NU = s.H_kv * s.d / cfg.UN;
+    p.idesc = s.coef_dtype == kCoefF16 ? tc::idesc_f16(2 * kTokTile, cfg.UN) : tc::idesc_bf16(2 * kTokTile, cfg.UN);
     p.NS = cfg.NS;
     p.scale = a.scale;
     p.q = (const __nv_bfloat16*)a.q;
@@ -490,12 +522,15 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
     CUtensorMap mA, mB;
     const uint64_t dA[3] = {(uint64_t)s.r, (uint64_t)s.T, (uint64_t)s.B};
     const uint32_t bA[3] = {kChunkK, kTokTile, 1};
-    const uint64_t dB[2] = {(uint64_t)s.r, (uint64_t)s.H_kv * s.d};
-    const uint32_t bB[2] = {kChunkK, (uint32_t)cfg.UN / 2};
-    if (!make_map(&mA, a.coef, 3, dA, bA) || !make_map(&mB, a.basis, 2, dB, bB)) return cudaErrorInvalidValue;
+    const uint64_t dB[3] = {(uint64_t)s.r, (uint64_t)s.H_kv * s.d, (uint64_t)s.B};
+    const uint32_t bB[3] = {kChunkK, (uint32_t)cfg.UN / 2, 1};
+    if (!make_map(&mA, a.coef, 3, dA, bA, 0, f16) ||
+        !make_map(&mB, a.basis, p.pps ? 3 : 2, dB, bB, p.pps ? (uint64_t)s.basis_batch_stride : 0, f16))
+        return cudaErrorInvalidValue;
     const size_t smem = score_smem_bytes(p.NS, cfg.UN, s.H_q);
     // CTA pairs (cluster of two), at most one CTA per SM
-    const int grid = 2 * std::min((p.n_tiles + 1) / 2 * p.NU, std::max(1, sm_count() / 2));
+    const int n_pairs = p.pps ? s.B * p.pps : (p.n_tiles + 1) / 2;
+    const int grid = 2 * std::min(n_pairs * p.NU, std::max(1, sm_count() / 2));
     cudaError_t e = cudaSuccess;
     auto go = [&](auto kern) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -505,14 +540,16 @@ cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st) {
         }
     };
     const bool two = cfg.UN == 256;
+#define LOWRAM_SCORE_GO(G_) (two ? go(score_tc_kernel<G_, 2>) : go(score_tc_kernel<G_, 1>))
     switch (s.H_q / s.H_kv) {
-        case 1: two ? go(score_tc_kernel<1, 2>) : go(score_tc_kernel<1, 1>); break;
-        case 2: two ? go(score_tc_kernel<2, 2>) : go(score_tc_kernel<2, 1>); break;
-        case 4: two ? go(score_tc_kernel<4, 2>) : go(score_tc_kernel<4, 1>); break;
-        case 7: two ? go(score_tc_kernel<7, 2>) : go(score_tc_kernel<7, 1>); break;
-        case 8: two ? go(score_tc_kernel<8, 2>) : go(score_tc_kernel<8, 1>); break;
+        case 1: LOWRAM_SCORE_GO(1); break;
+        case 2: LOWRAM_SCORE_GO(2); break;
+        case 4: LOWRAM_SCORE_GO(4); break;
+        case 7: LOWRAM_SCORE_GO(7); break;
+        case 8: LOWRAM_SCORE_GO(8); break;
         default: return cudaErrorNotSupported;
     }
+#undef LOWRAM_SCORE_GO
     return e;
 }
 

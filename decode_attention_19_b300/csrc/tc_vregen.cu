@@ -1,5 +1,5 @@
-// tc_vregen.cu -- tensor-core (tcgen05) value regeneration for the selected tokens of bf16 caches (K3), and
-// the merge of its softmax partials (K4).
+// tc_vregen.cu -- tensor-core (tcgen05) value regeneration for the selected tokens of bf16 caches (K3), with the
+// softmax partials of its chunks merged by the CTA that finishes a (sequence, kv-head) last.
 //
 // The method: each decode step rebuilds only a selected subset of KV pairs (LowRAM abstract); a selected
 // token's value is predicted from its pre-RoPE key by the head's MLP, plus the stored residual when the
@@ -8,24 +8,36 @@
 // of the wiki page).  The key itself comes from the low-rank factors ("Asymmetric key compression with
 // xKV").
 //
-// K3, one CTA per (sequence b, kv-head h, chunk of 128 selected tokens), 192 threads:
-//   warp 0      TMA producer: the basis rows of head h [128 x r] in 64-wide k-chunks through an NS-stage
-//               ring, and the head's first predictor layer w1[h] [m x d] (resident).
-//   warp 1      TMEM owner and MMA issuer (one thread):
-//                 MMA1  D1[128 tok x 128] = C_sel . basis_h^T   (M=128, N=128, K=r): pre-RoPE keys
-//                 MMA2  D2[m x 128 tok]   = w1_h . K^T          (M=128 per 128 hidden units, N=128, K=d)
-//               MMA2 runs transposed (hidden units on TMEM lanes, tokens on columns), so the softmax-weighted
-//               sum over tokens is a loop over one thread's own TMEM row.
-//   warps 2-5   gather + epilogue: cp.async of the selected latent rows into the 128B-swizzled operand
-//               layout; D1 -> bf16 keys in shared memory (MMA2's B operand); softmax weights of the chunk
-//               from the scaled logits the key pass stored; SiLU of D2 and the weighted sums
-//               z[jq] = sum_t p[jq,t] SiLU(w1 k_t + b1); weighted sums of the chunk's residual rows.
-// The second predictor layer is linear, so sum_t p_t (w2 h_t + b2 + r_t) = w2 (sum_t p_t h_t) + b2 sum_t p_t
-// + sum_t p_t r_t: the merge kernel applies w2 and b2 once per (sequence, q-head) to the merged sums instead
-// of once per selected token.  Values are never materialised; the result is the same up to rounding order.
+// Two reassociations, exact in real arithmetic, shape the kernel:
+//   - the predictor's first layer acts on the rebuilt key, w1 (basis_h c) = (w1 basis_h) c, so the hidden
+//     pre-activations of a selected token are one product of its latent row with F_h = w1[h] basis_h [m x r]
+//     (folded once per call by spare CTAs of the selection kernel, stored bf16 -- fp16 for an int4 cache's fp16
+//     copy -- in the workspace);
+//   - the second layer is linear, so sum_t p_t (w2 s_t + b2 + r_t) = w2 (sum_t p_t s_t) + b2 sum_t p_t +
+//     sum_t p_t r_t: a chunk applies w2 once per q-head to its softmax-weighted hidden sums, never forming the
+//     tokens' values, and writes a plain flash-decoding record (weighted value sum, max logit, weight sum).
+// The result equals "regenerate the selected values, then attend" up to rounding order; F in bf16 rounds the
+// folded weights where the unfolded chain would round the rebuilt keys.
 //
-// Every wait is bounded (tc_common.cuh).  On a timeout the kernel sets LOWRAM_CHECK_TIMEOUT, lets what it
-// issued complete, frees TMEM and returns; every named barrier is reached on every path.
+// K3 is persistent: one CTA per SM walks a contiguous range of work items (kv-head h, sequence b, chunk of 128
+// selected tokens), kv-head-major, so consecutive items share F_h, which stays resident in shared memory while
+// it fits (else each ring stage carries its F chunk).  448 threads:
+//   warp 0      TMA: F_h's k-chunks [m x 64] (once per kv-head, or per stage when streamed).
+//   warp 1      TMEM owner (two accumulators of m columns) and MMA issuer (one thread):
+//               D[m hidden x 128 tokens] = F_h . C_sel^T (M = 128 per 128 hidden units, N = 128, K = r), hidden
+//               units on TMEM lanes, tokens on columns; item j accumulates into buffer j % 2.
+//   warps 2-5   gather: 16-byte cp.async of the selected tokens' latent rows into the 128B-swizzled ring, one
+//               64-wide k-chunk per stage, running ahead into the next items.
+//   warps 6-13  epilogue, one item after another while the next item's rows land and multiply: softmax weights
+//               of the chunk from the scaled logits the key pass stored, weighted residual rows; then per thread
+//               one hidden unit and half of the tokens: SiLU(D + b1) weighted by the softmax, summed; the TMEM
+//               buffer is released; w2 on the hidden sums; the chunk's record.
+// The CTA finishing a (b, h)'s last chunk merges its chunks' records into out and lse (a counter per (b, h),
+// zeroed by the selection kernel; records read through L2).
+//
+// Every pipeline wait is bounded by the call's wait limit (a parameter); on a timeout the kernel sets
+// LOWRAM_CHECK_TIMEOUT, lets the copies and MMAs it issued complete, frees TMEM and returns.  Every named
+// barrier is reached on every path.
 #include "kernels.h"
 #include "predict.cuh"
 #include "tc_common.cuh"
@@ -34,476 +46,547 @@ namespace lowram {
 
 namespace {
 
-constexpr int kVThreads = 192;
-constexpr int kRows = 128;              // selected tokens per CTA
-constexpr int kStageBytes = 32768;      // latent chunk [128 x 64] + basis chunk [128 x 64], bf16
-constexpr int kHalf = 16384;
-constexpr int kNS = 3;                  // ring stages; after MMA1 the ring holds the keys and w1[h]
+constexpr int kVThreads = 448;
+constexpr int kGat = 128;                // gathering threads (warps 2-5)
+constexpr int kEpi = 256;                // epilogue threads (warps 6-13)
+constexpr int kRows = 128;               // selected tokens per item
+constexpr int kCBytes = kRows * 128;     // latent chunk [128 tokens x 64] bf16, 128B-swizzled
+constexpr int kMaxStages = 8;
+constexpr int kMaxMergeChunks = 64;      // chunks per (b, h) the fused merge takes (S <= 8192)
+constexpr size_t kSmemMax = 232448;
 
 struct VregenTcParams {
-    int T, H_q, H_kv, r, m, S_eff, n_chunks, n_res, KC, PW;
-    const __nv_bfloat16* coef;
+    int B, T, H_q, H_kv, m, r, S_eff, n_chunks, n_res, KC, NS, n_items;
+    int f_resident;           // F_h stays in shared memory for all of a kv-head's items (else streamed per stage)
+    int fold_per_seq;         // the folded weights hold one copy per sequence
+    uint32_t idesc;           // MMA instruction descriptor: bf16 operands, or fp16 (an int4 cache's fp16 copy)
+    long long mlp_stride;     // elements from sequence b's w2 to b+1's (0: shared); biases are then per sequence
+    long long wait_cycles;
+    const __nv_bfloat16* coef;   // [B, T, r] latent coefficients (2-byte elements; fp16 for an int4 cache's copy)
     const float* sall;        // [B, H_q, T] scaled logits written by the key pass
-    const float* b1;          // [H_kv, m] or null
-    const float* b2;          // [H_kv, d] or null
-    const __nv_bfloat16* w2;  // [H_kv, d, m]
+    const float* b1;          // [H_kv, m] ([B, H_kv, m] with a predictor per sequence) or null
+    const float* b2;          // [H_kv, d] ([B, H_kv, d] likewise) or null
+    const __nv_bfloat16* w2;  // [H_kv, d, m], sequence b's at b * mlp_stride
     const int32_t* sel;       // [B, H_kv, S_eff]
-    const int32_t* hit;       // [B, H_kv, S_eff] residual row of each selected token, or -1
+    const int32_t* hit;       // [B, H_kv, S_eff] residual row of each selected token, or -1; null without residuals
     ResView res;
-    float* partial;           // [B, H_q, n_chunks, PW]
-    int32_t* cnt;             // [B, H_kv] chunks finished per (b, h); zeroed by the selection kernel
+    float* partial;           // [B, H_q, n_chunks, d + 2]
+    int32_t* cnt;             // [B, H_kv] chunks finished per (b, h); zeroed by the selection kernel; null: no merge
     float* out;               // [B, H_q, d]
     float* lse;               // [B, H_q] or null
     uint32_t* check;
 };
 
-size_t vregen_smem_bytes() {
-    return 1024 + (size_t)kNS * kStageBytes + 8 * 128 * 4 + 3 * 128 * 4 + 72 * 4 + 8 * (3 * kNS + 5) + 16;
+// Epilogue scratch beside the ring: softmax weights [8][128], weighted residual sums [2][8][128], hidden sums
+// [2][8][m], the upper half's value sums [8][128], merge weights [8][64] and (W, L) [8][2], compacted hits
+// (rows, slots), reductions [2][32] + counts [4], then the barriers and the TMEM slot / flags.
+size_t scratch_bytes(int m) {
+    return (size_t)4 * (8 * kRows + 2 * 8 * kRows + 2 * 8 * m + 8 * kRows + 8 * kMaxMergeChunks + 16 + 2 * kRows +
+                        64 + 4) +
+           8 + 8 * (3 * kMaxStages + 2 + 4 + 1) + 16;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
+struct VregenConfig {
+    bool f_resident;
+    int NS;
+    size_t smem;
+};
 
-__device__ __forceinline__ void st_shared_16(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tc::smem_u32(p)), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-
-// The last CTA of a (sequence, kv-head) to finish merges the chunks' partials of its G q-heads (threads =
-// the 128 epilogue threads, et = 0..127): W = max_c M_c, w_c = exp(M_c - W), L = sum_c w_c l_c,
-// out = w2[h] (sum_c w_c z_c / L) + b2[h] + sum_c w_c rz_c / L,  lse = W + log L.
-// It is the tail of the kernel's last wave, so its global reads are issued together: the thread's row of w2
-// (output feature i = et) first, then the G q-heads' contiguous records in batches of 10 independent 16-byte
-// loads (all G at once when they fit, else one q-head at a time); the chunk weights w_c are computed once per
-// q-head.
-template <int G>
-__device__ __forceinline__ void merge_last(const VregenTcParams& p, int b, int h, int et, float* scratch) {
-    const int64_t qstride = (int64_t)p.n_chunks * p.PW;
-    const float* P0 = p.partial + ((int64_t)b * p.H_q + h * G) * qstride;
-    const int ZW = p.m + 128;
-    float* Z = scratch;                          // [G][m + 128] merged hidden sums, then residual sums
-    float* Wc = Z + G * ZW;                      // [G][n_chunks] chunk weights exp(M_c - W)
-    float* ML = Wc + G * p.n_chunks;             // [G][2] W and L
-    float* Pb = ML + 2 * G;                      // [G][n_chunks][PW] staged records (16-byte aligned: see below)
-    Pb = (float*)(((uintptr_t)Pb + 15) & ~(uintptr_t)15);
-    // all G q-heads' records at once when they fit, else one q-head at a time (tc_fused_merge guarantees one fits)
-    const size_t fixed = (size_t)(Pb - scratch) * sizeof(float);
-    const int per = (fixed + G * qstride * sizeof(float) <= (size_t)kNS * kStageBytes) ? G : 1;
-
-    constexpr int kW2Pre = 16;                   // 16-byte pieces of the w2 row fetched ahead (128 hidden units)
-    constexpr int kRecBatch = 10;                // independent 16-byte record loads per thread per batch
-    const uint4* W2r = reinterpret_cast<const uint4*>(p.w2 + ((int64_t)h * 128 + et) * p.m);
-    uint4 wpre[kW2Pre];
-#pragma unroll
-    for (int u = 0; u < kW2Pre; ++u)
-        if (u * 8 < p.m) wpre[u] = __ldg(W2r + u);
-
-    for (int q0 = 0; q0 < G; q0 += per) {
-        {   // records of q-heads q0 .. q0+per-1
-            const float4* src = reinterpret_cast<const float4*>(P0 + q0 * qstride);
-            float4* d4 = reinterpret_cast<float4*>(Pb);
-            const int n4 = (int)(per * qstride / 4);
-            for (int i0 = 0; i0 < n4; i0 += kRecBatch * kRows) {
-                float4 v[kRecBatch];
-#pragma unroll
-                for (int u = 0; u < kRecBatch; ++u) {
-                    const int i = i0 + u * kRows + et;
-                    if (i < n4) v[u] = __ldcg(src + i);
-                }
-#pragma unroll
-                for (int u = 0; u < kRecBatch; ++u) {
-                    const int i = i0 + u * kRows + et;
-                    if (i < n4) d4[i] = v[u];
-                }
-            }
-            tc::named_bar_sync(1, kRows);
-        }
-        // one thread per q-head: W, L and the chunk weights
-        if (et < per) {
-            const int jq = q0 + et;
-            const float* Pq = Pb + et * qstride;
-            float mx = -INFINITY;
-            for (int c = 0; c < p.n_chunks; ++c) mx = fmaxf(mx, Pq[(int64_t)c * p.PW + p.m + 128]);
-            float l = 0.0f;
-            for (int c = 0; c < p.n_chunks; ++c) {
-                const float mc = Pq[(int64_t)c * p.PW + p.m + 128];
-                const float w = mc == -INFINITY ? 0.0f : __expf(mc - mx);
-                Wc[jq * p.n_chunks + c] = w;
-                l = fmaf(w, Pq[(int64_t)c * p.PW + p.m + 129], l);
-            }
-            ML[jq * 2] = mx;
-            ML[jq * 2 + 1] = l;
-        }
-        tc::named_bar_sync(1, kRows);
-        for (int e = et; e < per * ZW; e += kRows) {
-            const int jl = e / ZW, j = e - jl * ZW, jq = q0 + jl;
-            const float* Pq = Pb + jl * qstride;
-            const float l = ML[jq * 2 + 1];
-            float acc = 0.0f;
-            for (int c = 0; c < p.n_chunks; ++c) acc = fmaf(Wc[jq * p.n_chunks + c], Pq[(int64_t)c * p.PW + j], acc);
-            Z[jq * ZW + j] = l > 0.0f ? acc / l : 0.0f;
-        }
-        tc::named_bar_sync(1, kRows);     // Pb is reused by the next group of q-heads; Z is complete
+VregenConfig vregen_config(int m, int r) {
+    const int KC = r / 64;
+    const size_t fres = (size_t)KC * m * 128, fixed = 1024 + scratch_bytes(m);
+    VregenConfig c{};
+    if (fres + fixed + 3 * (size_t)kCBytes <= kSmemMax) {
+        c.f_resident = true;
+        c.NS = (int)std::min<size_t>(kMaxStages, (kSmemMax - fres - fixed) / kCBytes);
+        c.smem = fres + fixed + (size_t)c.NS * kCBytes;
+    } else {
+        const size_t stage = kCBytes + (size_t)m * 128;
+        c.f_resident = false;
+        c.NS = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed) / stage);
+        c.smem = fixed + (size_t)c.NS * stage;
     }
-    // thread et = output feature i: the second predictor layer on the merged hidden sums
-    float acc[G];
-#pragma unroll
-    for (int jq = 0; jq < G; ++jq) acc[jq] = 0.0f;
-    for (int j0 = 0; j0 < p.m; j0 += 8 * kW2Pre) {
-#pragma unroll
-        for (int u = 0; u < kW2Pre; ++u) {
-            const int jb = j0 + u * 8;
-            if (jb >= p.m) break;
-            const uint4 wv = j0 == 0 ? wpre[u] : __ldg(W2r + jb / 8);
-            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&wv);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(pr[e]);
-                const int j = jb + 2 * e;
-#pragma unroll
-                for (int jq = 0; jq < G; ++jq) {
-                    acc[jq] = fmaf(f.x, Z[jq * ZW + j], acc[jq]);
-                    acc[jq] = fmaf(f.y, Z[jq * ZW + j + 1], acc[jq]);
-                }
-            }
-        }
-    }
-    const float bias = p.b2 ? __ldg(p.b2 + (int64_t)h * 128 + et) : 0.0f;
-#pragma unroll
-    for (int jq = 0; jq < G; ++jq) {
-        const int64_t bhq = (int64_t)b * p.H_q + h * G + jq;
-        const float Mq = ML[jq * 2], Lq = ML[jq * 2 + 1];
-        p.out[bhq * 128 + et] = Lq > 0.0f ? acc[jq] + bias + Z[jq * ZW + p.m + et] : 0.0f;
-        if (p.lse && et == jq) p.lse[bhq] = Lq > 0.0f ? Mq + logf(Lq) : -INFINITY;
+    return c;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// cp.async.wait_group with a run-time count of groups allowed to stay pending (at most kMaxStages - 1)
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+    switch (n) {
+        case 0: tc::cp_async_wait<0>(); break;
+        case 1: tc::cp_async_wait<1>(); break;
+        case 2: tc::cp_async_wait<2>(); break;
+        case 3: tc::cp_async_wait<3>(); break;
+        case 4: tc::cp_async_wait<4>(); break;
+        case 5: tc::cp_async_wait<5>(); break;
+        case 6: tc::cp_async_wait<6>(); break;
+        default: tc::cp_async_wait<7>(); break;
     }
 }
 
-template <int G>
-__global__ void __launch_bounds__(kVThreads, 2)
-    vregen_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW1,
-                     VregenTcParams p) {
+template <int G, int MB>
+__global__ void __launch_bounds__(kVThreads, 1)
+    vregen_tc_kernel(const __grid_constant__ CUtensorMap tmF, VregenTcParams p) {
     using namespace tc;
+    constexpr int M = MB * 128;              // hidden units (TMEM lanes x column blocks)
+    constexpr uint32_t kFChunk = M * 128;    // one k-chunk of F_h [M x 64]
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* ring = smem;                        // MMA1: stages; then keys [0, 32K) and w1[h] [32K, 32K + m*256)
-    uint8_t* W1s = ring + 2 * kHalf;
-    float* Ps = (float*)(ring + kNS * kStageBytes);   // [G][128] softmax weights of the chunk
-    int* Tok = (int*)(Ps + 8 * kRows);           // token of each slot, -1 past the selection
-    int* Hit = Tok + kRows;                      // compacted: residual rows of the chunk's slots that have one
-    int* HitSlot = Hit + kRows;                  // ... and those slots, ascending
-    float* red = (float*)(HitSlot + kRows);      // [2][4 warps][8] partial max / sum, then 4 hit counts
-    uint64_t* fullA = (uint64_t*)(red + 72);
-    uint64_t* fullB = fullA + kNS;
-    uint64_t* empty = fullB + kNS;
-    uint64_t* w1_full = empty + kNS;
-    uint64_t* d1_full = w1_full + 1;
-    uint64_t* kbf_full = d1_full + 1;
-    uint64_t* d2_full = kbf_full + 1;
-    uint64_t* m_drain = d2_full + 1;
+    const int NS = p.NS, KC = p.KC;
+    const bool fres = p.f_resident != 0;
+    const uint32_t kStage = kCBytes + (fres ? 0u : kFChunk);
+    uint8_t* Fres = smem;                                        // [KC][M x 64] when resident
+    uint8_t* ring = smem + (fres ? (size_t)KC * kFChunk : 0);    // NS stages: C chunk [128 x 64] (+ F chunk)
+    float* Ps = (float*)(ring + (size_t)NS * kStage);            // [G][128] softmax weights (0 on padding slots)
+    float* RZ = Ps + 8 * kRows;                                  // [2 halves][G][128] weighted residual rows
+    float* Z = RZ + 2 * 8 * kRows;                               // [2 token halves][G][M] hidden sums
+    float* X = Z + 2 * 8 * M;                                    // [G][128] the upper half's value sums
+    float* Wc = X + 8 * kRows;                                   // [G][n_chunks] merge weights
+    float* ML = Wc + 8 * kMaxMergeChunks;                        // [G][2] W and L of the merge
+    int* HitRow = (int*)(ML + 16);                               // compacted residual rows of the chunk's slots
+    int* HitSlot = HitRow + kRows;                               // ... and those slots, ascending
+    float* redM = (float*)(HitSlot + kRows);                     // [4 slot quarters][8] partial max
+    float* redL = redM + 32;                                     // [4][8] partial sums
+    int* hcount = (int*)(redL + 32);                             // [4] residual hits per slot quarter
+    uint64_t* fullF = (uint64_t*)(((uintptr_t)(hcount + 4) + 7) & ~(uintptr_t)7);   // streamed F chunk landed
+    uint64_t* fullC = fullF + kMaxStages;        // the 128 gathering threads' rows of the stage landed
+    uint64_t* empty = fullC + kMaxStages;        // the MMAs are done with the stage
+    uint64_t* f_full = empty + kMaxStages;       // resident F_h landed
+    uint64_t* f_empty = f_full + 1;              // the MMAs are done with the resident F_h
+    uint64_t* t_full = f_empty + 1;              // [2] accumulator ready
+    uint64_t* t_empty = t_full + 2;              // [2] epilogue done reading the accumulator
+    uint64_t* m_drain = t_empty + 2;
     uint32_t* tmem_slot = (uint32_t*)(m_drain + 1);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     volatile int* last_flag = (volatile int*)(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int64_t bh = (int64_t)b * p.H_kv + h;
-    const uint32_t tcols = p.m > 128 ? 256u : 128u;
+    const int it_begin = (int)((int64_t)blockIdx.x * p.n_items / gridDim.x);
+    const int it_end = (int)((int64_t)(blockIdx.x + 1) * p.n_items / gridDim.x);
+    const int n_local = it_end - it_begin;
+    // item -> (h, b, chunk), kv-head-major; the folded weights of an item sit at row fh(it) * M of the F map
+    auto item_hbc = [&](int it, int& h, int& b, int& c) {
+        c = it % p.n_chunks;
+        const int hb = it / p.n_chunks;
+        b = hb % p.B;
+        h = hb / p.B;
+    };
+    auto item_fh = [&](int it) {
+        int h, b, c;
+        item_hbc(it, h, b, c);
+        return (p.fold_per_seq ? b * p.H_kv : 0) + h;
+    };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kNS; ++s) {
-            mbar_init(&fullA[s], kRows);
-            mbar_init(&fullB[s], 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&fullF[s], 1);
+            mbar_init(&fullC[s], kGat);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(w1_full, 1);
-        mbar_init(d1_full, 1);
-        mbar_init(kbf_full, kRows);
-        mbar_init(d2_full, 1);
+        mbar_init(f_full, 1);
+        mbar_init(f_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&t_full[i], 1);
+            mbar_init(&t_empty[i], kEpi);
+        }
         mbar_init(m_drain, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmW);
-        prefetch_tmap(&tmW1);
-    }
+    if (warp == 0 && lane == 0) prefetch_tmap(&tmF);
     if (warp == 1) {
-        tmem_alloc(tmem_slot, tcols);
+        tmem_alloc(tmem_slot, (uint32_t)(2 * M));
         tmem_relinquish();
     }
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    grid_dep_wait();     // selection, residual rows and logits come from the kernels before (launch_pdl)
+    grid_dep_wait();     // selection, residual rows, folded weights and logits come from the kernels before
 
     if (warp == 0) {
-        // ------------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------------ TMA: F_h
         if (lane == 0) {
-            int issued = 0;
-            bool w1_issued = false;
-            for (int kc = 0; kc < p.KC; ++kc) {
-                const int s = kc % kNS, n = kc / kNS;
-                if (!mbar_wait(&empty[s], (n & 1) ^ 1, abort_flag)) break;
-                mbar_expect_tx(&fullB[s], kHalf);
-                tma_load_2d(ring + s * kStageBytes + kHalf, &tmW, &fullB[s], kc * 64, h * 128);
-                ++issued;
+            int n_seg = 0, cur_fh = -1;                 // resident: kv-head segments loaded
+            uint32_t issued = 0;                        // streamed: stages issued
+            for (int j = 0; j < n_local && !*abort_flag; ++j) {
+                const int fh = item_fh(it_begin + j);
+                if (fres) {
+                    if (fh == cur_fh) continue;
+                    // the MMAs of the previous segment are done with F before it is overwritten
+                    if (n_seg > 0 && !mbar_wait_lim(f_empty, (n_seg - 1) & 1, abort_flag, p.wait_cycles)) break;
+                    mbar_expect_tx(f_full, (uint32_t)KC * kFChunk);
+                    for (int kc = 0; kc < KC; ++kc)
+#pragma unroll
+                        for (int mb = 0; mb < MB; ++mb)
+                            tma_load_2d(Fres + kc * kFChunk + mb * 16384, &tmF, f_full, kc * 64, fh * M + mb * 128);
+                    cur_fh = fh;
+                    ++n_seg;
+                } else {
+                    bool ok = true;
+                    for (int kc = 0; kc < KC; ++kc, ++issued) {
+                        const uint32_t s = issued % NS, n = issued / NS;
+                        if (!mbar_wait_lim(&empty[s], (n & 1) ^ 1, abort_flag, p.wait_cycles)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(&fullF[s], kFChunk);
+#pragma unroll
+                        for (int mb = 0; mb < MB; ++mb)
+                            tma_load_2d(ring + s * kStage + kCBytes + mb * 16384, &tmF, &fullF[s], kc * 64,
+                                        fh * M + mb * 128);
+                    }
+                    if (!ok) break;
+                }
             }
-            // w1[h] goes into the ring once MMA1 is complete
-            if (issued == p.KC && mbar_wait(d1_full, 0, abort_flag)) {
-                mbar_expect_tx(w1_full, (uint32_t)p.m * 256u);
-                for (int mb = 0; mb < p.m / 128; ++mb)
-                    for (int kc2 = 0; kc2 < 2; ++kc2)
-                        tma_load_2d(W1s + (mb * 2 + kc2) * kHalf, &tmW1, w1_full, kc2 * 64, h * p.m + mb * 128);
-                w1_issued = true;
-            }
-            if (*abort_flag) {
-                // loads older than the last kNS were consumed by MMAs, so they have landed
-                for (int k = issued > kNS ? issued - kNS : 0; k < issued; ++k)
-                    mbar_wait_drain(&fullB[k % kNS], (k / kNS) & 1);
-                if (w1_issued) mbar_wait_drain(w1_full, 0);
+            if (*abort_flag) {   // copies issued complete before the CTA frees its shared memory
+                if (fres && n_seg > 0) mbar_wait_drain(f_full, (n_seg - 1) & 1);
+                if (!fres)
+                    for (uint32_t k = issued > (uint32_t)NS ? issued - NS : 0; k < issued; ++k)
+                        mbar_wait_drain(&fullF[k % NS], (k / NS) & 1);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(128, 128);
             bool ok = true;
-            for (int kc = 0; kc < p.KC && ok; ++kc) {
-                const int s = kc % kNS, n = kc / kNS;
-                if (!mbar_wait(&fullB[s], n & 1, abort_flag) || !mbar_wait(&fullA[s], n & 1, abort_flag)) {
-                    ok = false;
-                    break;
+            int n_seg = 0, cur_fh = -1;
+            uint32_t g = 0;                                      // stages consumed
+            for (int j = 0; j < n_local && ok; ++j) {
+                const int fh = item_fh(it_begin + j);
+                if (fres && fh != cur_fh) {
+                    if (!mbar_wait_lim(f_full, n_seg & 1, abort_flag, p.wait_cycles)) break;
+                    cur_fh = fh;
+                    ++n_seg;
                 }
+                const uint32_t buf = j & 1;
+                if (!mbar_wait_lim(&t_empty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.wait_cycles)) break;
                 fence_after();
-                const uint32_t a = smem_u32(ring + s * kStageBytes), bb = a + kHalf;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem, sdesc_sw128(a + k * 32), sdesc_sw128(bb + k * 32), idesc, (kc | k) != 0);
-                mma_commit(&empty[s]);
-            }
-            if (ok) {
-                mma_commit(d1_full);
-                if (mbar_wait(kbf_full, 0, abort_flag) && mbar_wait(w1_full, 0, abort_flag)) {
+                for (int kc = 0; kc < KC; ++kc, ++g) {
+                    const uint32_t s = g % NS, par = (g / NS) & 1;
+                    if (!mbar_wait_lim(&fullC[s], par, abort_flag, p.wait_cycles) ||
+                        (!fres && !mbar_wait_lim(&fullF[s], par, abort_flag, p.wait_cycles))) {
+                        ok = false;
+                        break;
+                    }
                     fence_after();
-                    const uint32_t kb = smem_u32(ring);
-                    for (int mb = 0; mb < p.m / 128; ++mb)
-                        for (int kc2 = 0; kc2 < 2; ++kc2) {
-                            const uint32_t a = smem_u32(W1s + (mb * 2 + kc2) * kHalf), bb = kb + kc2 * kHalf;
+                    const uint32_t c_addr = smem_u32(ring + s * kStage);
+                    const uint32_t f_addr = fres ? smem_u32(Fres + kc * kFChunk) : c_addr + kCBytes;
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                mma_bf16(tmem + mb * 128, sdesc_sw128(a + k * 32), sdesc_sw128(bb + k * 32), idesc,
-                                         (kc2 | k) != 0);
-                        }
-                    mma_commit(d2_full);
+                    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_bf16(tmem + buf * M + mb * 128, sdesc_sw128(f_addr + mb * 16384 + k * 32),
+                                     sdesc_sw128(c_addr + k * 32), p.idesc, (kc | k) != 0);
+                    mma_commit(&empty[s]);
                 }
+                if (!ok) break;
+                mma_commit(&t_full[buf]);
+                // the last item of a kv-head segment: its MMAs release the resident F_h
+                if (fres && (j + 1 == n_local || item_fh(it_begin + j + 1) != fh)) mma_commit(f_empty);
             }
-            // every MMA issued completes before TMEM is released
+            // every MMA issued completes before TMEM is released or shared memory is reused
             mma_commit(m_drain);
             mbar_wait_drain(m_drain, 0);
         }
-    } else {
-        // ------------------------------------------------------------------ gather + epilogue
-        const int et = threadIdx.x - 64;
-        const int quarter = warp & 3;
-        const int slot = quarter * 32 + lane;   // the TMEM lane (row) this thread reads
-        int my_tok, my_hit;
-        {
-            const int j = chunk * kRows + slot;
-            int tok = j < p.S_eff ? p.sel[bh * p.S_eff + j] : -1;
-            if (tok >= p.T) tok = p.T - 1;      // the selection is always in range; keep the invariant explicit
-            my_hit = (j < p.S_eff && p.hit && p.n_res > 0) ? p.hit[bh * p.S_eff + j] : -1;
-            Tok[slot] = tok;
-            my_tok = tok;
-        }
-        named_bar_sync(1, kRows);
-
-        // gather the selected latent rows: 8 threads per 128-byte row segment, 16 rows per pass
-        bool ok = true;
-        {
-            const int c16 = et & 7, rsub = et >> 3;
-            for (int kc = 0; kc < p.KC; ++kc) {
-                const int s = kc % kNS, n = kc / kNS;
-                if (ok && !mbar_wait(&empty[s], (n & 1) ^ 1, abort_flag)) ok = false;
-                if (ok) {
-                    const uint32_t A = smem_u32(ring + s * kStageBytes);
+    } else if (warp < 6) {
+        // ------------------------------------------------------------------ gather (128 threads)
+        // thread gt copies the 16-byte piece c16 of rows rsub + 16 rr (rr < 8) of every k-chunk; a padding slot
+        // re-reads its sequence's token 0 (its softmax weight is 0)
+        const int gt = threadIdx.x - 64, c16 = gt & 7, rsub = gt >> 3;
+        const uint32_t total = (uint32_t)n_local * KC;
+        uint32_t issued = 0, published = 0;
+        const __nv_bfloat16* srow[8];
+        bool gok = true;
+        while (published < total) {
+            if (gok && issued < total && issued - published < (uint32_t)NS) {
+                const uint32_t s = issued % NS, n = issued / NS;
+                const int kc = (int)(issued % KC);
+                if (kc == 0) {   // the item's rows
+                    int h, b, c;
+                    item_hbc(it_begin + (int)(issued / KC), h, b, c);
+                    const int64_t bh = (int64_t)b * p.H_kv + h;
 #pragma unroll
                     for (int rr = 0; rr < 8; ++rr) {
-                        const int row = rr * 16 + rsub;
-                        const int tok = Tok[row];
-                        const __nv_bfloat16* src =
-                            p.coef + ((int64_t)b * p.T + (tok >= 0 ? tok : 0)) * p.r + kc * 64 + c16 * 8;
-                        cp_async_16(A + row * 128 + ((c16 ^ (row & 7)) << 4), src, tok >= 0 ? 16u : 0u);
+                        const int jr = c * kRows + rr * 16 + rsub;
+                        int t = jr < p.S_eff ? __ldg(p.sel + bh * p.S_eff + jr) : 0;
+                        t = min(max(t, 0), p.T - 1);
+                        srow[rr] = p.coef + ((int64_t)b * p.T + t) * p.r + c16 * 8;
                     }
+                }
+                if (!mbar_wait_lim(&empty[s], (n & 1) ^ 1, abort_flag, p.wait_cycles)) {
+                    gok = false;
+                    continue;
+                }
+                const uint32_t A = smem_u32(ring + s * kStage);
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int row = rr * 16 + rsub;
+                    cp_async_16(A + row * 128 + ((c16 ^ (row & 7)) << 4), srow[rr] + kc * 64, 16u);
                 }
                 cp_async_commit();
-                // up to kNS - 1 stages of gathers stay in flight; stage kc - (kNS - 1) has landed
-                if (kc >= kNS - 1) {
-                    cp_async_wait<kNS - 1>();
-                    fence_proxy_async();
-                    if (ok) mbar_arrive(&fullA[(kc - (kNS - 1)) % kNS]);
-                }
-            }
-            cp_async_wait<0>();
-            fence_proxy_async();
-            if (ok)
-                for (int kc = (p.KC > kNS - 1 ? p.KC - (kNS - 1) : 0); kc < p.KC; ++kc) mbar_arrive(&fullA[kc % kNS]);
-        }
-
-        // while MMA1 finishes: the scaled logits of this slot's token
-        float sv[G];
-#pragma unroll
-        for (int jq = 0; jq < G; ++jq)
-            sv[jq] = my_tok >= 0 ? __ldg(p.sall + ((int64_t)b * p.H_q + h * G + jq) * p.T + my_tok) : -INFINITY;
-
-        // D1 -> bf16 pre-RoPE keys, K-major and swizzled, into the ring's first 32 KB (MMA1 is complete)
-        bool have = ok && mbar_wait(d1_full, 0, abort_flag);
-        if (have) {
-            fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                float x[32], y[32];
-                tmem_ld_2x32(taddr + c * 64, taddr + c * 64 + 32, x, y);
-                uint8_t* row = ring + c * kHalf + slot * 128;
-#pragma unroll
-                for (int sg = 0; sg < 4; ++sg) {
-                    st_shared_16(row + ((sg ^ (slot & 7)) << 4), pack_bf16x2(x[sg * 8], x[sg * 8 + 1]),
-                                 pack_bf16x2(x[sg * 8 + 2], x[sg * 8 + 3]), pack_bf16x2(x[sg * 8 + 4], x[sg * 8 + 5]),
-                                 pack_bf16x2(x[sg * 8 + 6], x[sg * 8 + 7]));
-                    st_shared_16(row + (((sg + 4) ^ (slot & 7)) << 4), pack_bf16x2(y[sg * 8], y[sg * 8 + 1]),
-                                 pack_bf16x2(y[sg * 8 + 2], y[sg * 8 + 3]), pack_bf16x2(y[sg * 8 + 4], y[sg * 8 + 5]),
-                                 pack_bf16x2(y[sg * 8 + 6], y[sg * 8 + 7]));
-                }
+                ++issued;
+            } else if (published < issued) {
+                // the oldest stage in flight has landed: make it visible to the tensor cores and publish it
+                cp_async_wait_pending((int)(issued - published) - 1);
+                fence_proxy_async();
+                if (gok) mbar_arrive(&fullC[published % NS]);
+                ++published;
+            } else {
+                break;   // aborted with nothing in flight
             }
         }
-        fence_proxy_async();
-        fence_before();
-        mbar_arrive(kbf_full);
-
-        // softmax weights of the chunk per q-head
-        float M[G], l[G];
+        cp_async_wait<0>();
+    } else {
+        // ------------------------------------------------------------------ epilogue (256 threads)
+        const int et = threadIdx.x - 192;
+        const int slot = et & (kRows - 1), jh = et >> 7;         // jh: which half of the work this thread takes
+        const int sq = slot >> 5;                                 // slot quarter (warp within its half)
+        const int q = warp & 3, ch = (warp - 6) >> 2;            // TMEM lane quarter, token half
+        const int i_out = slot;
+        auto chunk_max = [&](int jq) {
+            return fmaxf(fmaxf(redM[jq], redM[8 + jq]), fmaxf(redM[16 + jq], redM[24 + jq]));
+        };
+        auto chunk_sum = [&](int jq) { return (redL[jq] + redL[8 + jq]) + (redL[16 + jq] + redL[24 + jq]); };
+        const int64_t rw = 128 + 2;
+        const int64_t qstride = (int64_t)p.n_chunks * rw;
+        for (int j = 0; j < n_local; ++j) {
+            int h, b, chunk;
+            item_hbc(it_begin + j, h, b, chunk);
+            const int64_t bh = (int64_t)b * p.H_kv + h;
+            const int64_t bias_bh = p.mlp_stride ? bh : h;
+            const int jsel = chunk * kRows + slot;
+            const bool valid = jsel < p.S_eff;
+            int tok = valid ? __ldg(p.sel + bh * p.S_eff + jsel) : -1;
+            if (tok >= p.T) tok = p.T - 1;   // the selection is always in range; keep the invariant explicit
+            const int my_hit = (valid && p.hit) ? __ldg(p.hit + bh * p.S_eff + jsel) : -1;
+            // scaled logits of this slot for q-heads jq = jh, jh + 2, ...
+            float sv[(G + 1) / 2];
 #pragma unroll
-        for (int jq = 0; jq < G; ++jq) {
-            const float mx = warp_max(sv[jq]);
-            if (lane == 0) red[quarter * 8 + jq] = mx;
-        }
-        const unsigned hb = __ballot_sync(0xffffffffu, my_hit >= 0);
-        int* hcount = (int*)(red + 64);
-        if (lane == 0) hcount[quarter] = __popc(hb);
-        named_bar_sync(1, kRows);
-        int n_hit;
-        {
-            int before = 0;
-            for (int w = 0; w < quarter; ++w) before += hcount[w];
-            n_hit = hcount[0] + hcount[1] + hcount[2] + hcount[3];
-            if (my_hit >= 0) {
-                const int at = before + __popc(hb & ((1u << lane) - 1u));
-                Hit[at] = my_hit;
-                HitSlot[at] = slot;
+            for (int u = 0; u < (G + 1) / 2; ++u) {
+                const int jq = jh + 2 * u;
+                sv[u] = (jq < G && valid) ? __ldg(p.sall + ((int64_t)b * p.H_q + h * G + jq) * p.T + tok) : -INFINITY;
             }
-        }
+            named_bar_sync(1, kEpi);   // the previous item's readers of Ps, RZ, the hits and the reductions are done
 #pragma unroll
-        for (int jq = 0; jq < G; ++jq) {
-            M[jq] = fmaxf(fmaxf(red[jq], red[8 + jq]), fmaxf(red[16 + jq], red[24 + jq]));
-            const float pv = (sv[jq] == -INFINITY || M[jq] == -INFINITY) ? 0.0f : __expf(sv[jq] - M[jq]);
-            Ps[jq * kRows + slot] = pv;
-            const float ps = warp_sum(pv);
-            if (lane == 0) red[32 + quarter * 8 + jq] = ps;
-        }
-        named_bar_sync(1, kRows);
+            for (int u = 0; u < (G + 1) / 2; ++u) {
+                const int jq = jh + 2 * u;
+                const float mx = warp_max(sv[u]);
+                if (lane == 0 && jq < G) redM[sq * 8 + jq] = mx;
+            }
+            const unsigned hb = __ballot_sync(0xffffffffu, my_hit >= 0);
+            if (jh == 0 && lane == 0) hcount[sq] = __popc(hb);
+            named_bar_sync(1, kEpi);
 #pragma unroll
-        for (int jq = 0; jq < G; ++jq) l[jq] = (red[32 + jq] + red[40 + jq]) + (red[48 + jq] + red[56 + jq]);
-
-        float* dst = p.partial + (((int64_t)b * p.H_q + h * G) * p.n_chunks + chunk) * p.PW;
-        const int64_t jq_stride = (int64_t)p.n_chunks * p.PW;
-
-        // residual rows of the chunk, weighted: thread = feature
-        {
-            float rz[G];
-#pragma unroll
-            for (int jq = 0; jq < G; ++jq) rz[jq] = 0.0f;
-            for (int k0 = 0; k0 < n_hit; k0 += 16) {    // 16 independent row loads in flight
-                float v[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) v[u] = k0 + u < n_hit ? p.res.get(bh * p.n_res + Hit[k0 + u], slot) : 0.0f;
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    if (k0 + u >= n_hit) break;
-                    const int t = HitSlot[k0 + u];
-#pragma unroll
-                    for (int jq = 0; jq < G; ++jq) rz[jq] = fmaf(Ps[jq * kRows + t], v[u], rz[jq]);
+            for (int u = 0; u < (G + 1) / 2; ++u) {
+                const int jq = jh + 2 * u;
+                if (jq < G) {
+                    const float mq = chunk_max(jq);
+                    const float pv = (sv[u] == -INFINITY || mq == -INFINITY) ? 0.0f : __expf(sv[u] - mq);
+                    Ps[jq * kRows + slot] = pv;
+                    const float ps = warp_sum(pv);
+                    if (lane == 0) redL[sq * 8 + jq] = ps;
                 }
             }
+            int n_hit = 0;
+            {
+                int before = 0;
 #pragma unroll
-            for (int jq = 0; jq < G; ++jq) dst[jq * jq_stride + p.m + slot] = rz[jq];
-#pragma unroll
-            for (int jq = 0; jq < G; ++jq)
-                if (slot == jq) {
-                    dst[jq * jq_stride + p.m + 128] = M[jq];
-                    dst[jq * jq_stride + p.m + 129] = l[jq];
+                for (int w = 0; w < 4; ++w) {
+                    before += (w < sq) ? hcount[w] : 0;
+                    n_hit += hcount[w];
                 }
-        }
+                if (jh == 0 && my_hit >= 0) {
+                    const int at = before + __popc(hb & ((1u << lane) - 1u));
+                    HitRow[at] = my_hit;
+                    HitSlot[at] = slot;
+                }
+            }
+            named_bar_sync(1, kEpi);
 
-        // hidden units: thread = unit j of each 128-block; z[jq] = sum_t p[jq,t] SiLU(D2[j,t] + b1[j])
-        have = have && mbar_wait(d2_full, 0, abort_flag);
-        if (have) {
-            fence_after();
-#pragma unroll 1
-            for (int mb = 0; mb < p.m / 128; ++mb) {
-                const int j = mb * 128 + slot;
-                const float bj = p.b1 ? __ldg(p.b1 + (int64_t)h * p.m + j) : 0.0f;
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + mb * 128;
-                float z[G];
+            // weighted residual rows: feature i_out, hits k = jh, jh + 2, ... (8 independent loads in flight); the
+            // sums wait in shared memory while the hidden units take the registers
+            {
+                float rz[G];
 #pragma unroll
-                for (int jq = 0; jq < G; ++jq) z[jq] = 0.0f;
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    float x[32], y[32];
-                    tmem_ld_2x32(taddr + c * 64, taddr + c * 64 + 32, x, y);
+                for (int jq = 0; jq < G; ++jq) rz[jq] = 0.0f;
+                for (int k0 = jh; k0 < n_hit; k0 += 16) {
+                    float v[8];
 #pragma unroll
-                    for (int tt = 0; tt < 32; tt += 4) {
-                        float hx[4], hy[4];
+                    for (int u = 0; u < 8; ++u) {
+                        const int k = k0 + 2 * u;
+                        v[u] = k < n_hit ? p.res.get(bh * p.n_res + HitRow[k], i_out) : 0.0f;
+                    }
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            hx[u] = silu_fast(x[tt + u] + bj);
-                            hy[u] = silu_fast(y[tt + u] + bj);
-                        }
+                    for (int u = 0; u < 8; ++u) {
+                        const int k = k0 + 2 * u;
+                        if (k >= n_hit) break;
+                        const int t = HitSlot[k];
 #pragma unroll
-                        for (int jq = 0; jq < G; ++jq) {
-                            const float4 px = *reinterpret_cast<const float4*>(Ps + jq * kRows + c * 64 + tt);
-                            const float4 py = *reinterpret_cast<const float4*>(Ps + jq * kRows + c * 64 + 32 + tt);
-                            z[jq] = fmaf(px.x, hx[0], z[jq]);
-                            z[jq] = fmaf(px.y, hx[1], z[jq]);
-                            z[jq] = fmaf(px.z, hx[2], z[jq]);
-                            z[jq] = fmaf(px.w, hx[3], z[jq]);
-                            z[jq] = fmaf(py.x, hy[0], z[jq]);
-                            z[jq] = fmaf(py.y, hy[1], z[jq]);
-                            z[jq] = fmaf(py.z, hy[2], z[jq]);
-                            z[jq] = fmaf(py.w, hy[3], z[jq]);
-                        }
+                        for (int jq = 0; jq < G; ++jq) rz[jq] = fmaf(Ps[jq * kRows + t], v[u], rz[jq]);
                     }
                 }
 #pragma unroll
-                for (int jq = 0; jq < G; ++jq) dst[jq * jq_stride + j] = z[jq];
+                for (int jq = 0; jq < G; ++jq) RZ[(jh * 8 + jq) * kRows + i_out] = rz[jq];
             }
-        }
 
-        // the last CTA of this (b, h) to finish merges the chunks (partials made visible device-wide first);
-        // without a counter array the separate merge kernel does it
-        __threadfence();
-        fence_before();
-        named_bar_sync(1, kRows);
-        if (et == 0 && p.cnt) *last_flag = (atomicAdd(p.cnt + bh, 1) == p.n_chunks - 1) ? 1 : 0;
-        named_bar_sync(1, kRows);
-        if (*last_flag) {
-            __threadfence();
-            // the ring is free: MMA2 has completed (or the call has aborted and its results are void)
-            merge_last<G>(p, b, h, et, (float*)ring);
-            if (et == 0) p.cnt[bh] = 0;
+            // hidden units: thread = hidden unit jj of each 128-block, tokens of half ch;
+            // z[jq] = sum over the half's tokens of p[jq, t] SiLU(D[jj, t] + b1[jj])
+            const uint32_t buf = j & 1;
+            const bool have = mbar_wait_lim(&t_full[buf], (j >> 1) & 1, abort_flag, p.wait_cycles);
+            if (have) {
+                fence_after();
+#pragma unroll 1
+                for (int mb = 0; mb < MB; ++mb) {
+                    const int jj = mb * 128 + q * 32 + lane;
+                    const float bj = p.b1 ? __ldg(p.b1 + bias_bh * M + jj) : 0.0f;
+                    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * M + mb * 128 + ch * 64;
+                    float z[G];
+#pragma unroll
+                    for (int jq = 0; jq < G; ++jq) z[jq] = 0.0f;
+#pragma unroll 1
+                    for (int cg = 0; cg < 4; ++cg) {           // 16 token columns per TMEM read
+                        float xv[2][8];
+                        tmem_ld_2x8(taddr + cg * 16, taddr + cg * 16 + 8, xv[0], xv[1]);
+                        const float* pc = Ps + ch * 64 + cg * 16;
+#pragma unroll
+                        for (int g8 = 0; g8 < 2; ++g8) {
+#pragma unroll
+                            for (int t4 = 0; t4 < 8; t4 += 4) {
+                                float hv[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) hv[u] = silu_fast(xv[g8][t4 + u] + bj);
+#pragma unroll
+                                for (int jq = 0; jq < G; ++jq) {
+                                    const float4 pw = *reinterpret_cast<const float4*>(pc + jq * kRows + g8 * 8 + t4);
+                                    z[jq] = fmaf(pw.x, hv[0], z[jq]);
+                                    z[jq] = fmaf(pw.y, hv[1], z[jq]);
+                                    z[jq] = fmaf(pw.z, hv[2], z[jq]);
+                                    z[jq] = fmaf(pw.w, hv[3], z[jq]);
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int jq = 0; jq < G; ++jq) Z[(ch * 8 + jq) * M + jj] = z[jq];
+                }
+            }
+            fence_before();
+            mbar_arrive(&t_empty[buf]);   // the accumulator is read: the MMAs of item j + 2 may use it
+            named_bar_sync(1, kEpi);
+
+            // second layer on the chunk's hidden sums: thread (i_out, jh) takes hidden units [jh M/2, (jh+1) M/2)
+            float acc[G];
+#pragma unroll
+            for (int jq = 0; jq < G; ++jq) acc[jq] = RZ[(jh * 8 + jq) * kRows + i_out];
+            if (have) {
+                constexpr int kW2 = 4;                                 // 16-byte pieces of the w2 row per batch
+                const uint4* w2src = reinterpret_cast<const uint4*>(p.w2 + b * p.mlp_stride +
+                                                                    ((int64_t)h * 128 + i_out) * M + jh * (M / 2));
+#pragma unroll 1
+                for (int bt = 0; bt < (M / 2) / (8 * kW2); ++bt) {
+                    uint4 w2v[kW2];
+#pragma unroll
+                    for (int u = 0; u < kW2; ++u) w2v[u] = __ldg(w2src + bt * kW2 + u);
+#pragma unroll
+                    for (int u = 0; u < kW2; ++u) {
+                        const int j0 = jh * (M / 2) + 8 * kW2 * bt + 8 * u;
+                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(&w2v[u]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float wa = bf_lo(wp[e]), wb = bf_hi(wp[e]);
+                            const int jj = j0 + 2 * e;
+#pragma unroll
+                            for (int jq = 0; jq < G; ++jq) {
+                                const float za = Z[jq * M + jj] + Z[(8 + jq) * M + jj];
+                                const float zb = Z[jq * M + jj + 1] + Z[(8 + jq) * M + jj + 1];
+                                acc[jq] = fmaf(wa, za, fmaf(wb, zb, acc[jq]));
+                            }
+                        }
+                    }
+                }
+            }
+            if (jh == 1)
+#pragma unroll
+                for (int jq = 0; jq < G; ++jq) X[jq * kRows + i_out] = acc[jq];
+            named_bar_sync(1, kEpi);
+            float* rec = p.partial + (((int64_t)b * p.H_q + h * G) * p.n_chunks + chunk) * rw;
+            if (jh == 0) {
+                const float bias = p.b2 ? __ldg(p.b2 + bias_bh * 128 + i_out) : 0.0f;
+#pragma unroll
+                for (int jq = 0; jq < G; ++jq)
+                    rec[jq * qstride + i_out] = acc[jq] + X[jq * kRows + i_out] + chunk_sum(jq) * bias;
+            } else if (i_out < G) {
+                rec[i_out * qstride + 128] = chunk_max(i_out);
+                rec[i_out * qstride + 129] = chunk_sum(i_out);
+            }
+
+            // the CTA finishing a (b, h)'s last chunk merges its chunks' records (made visible device-wide first)
+            if (p.cnt) {
+                __threadfence();
+                named_bar_sync(1, kEpi);
+                if (et == 0) *last_flag = (atomicAdd(p.cnt + bh, 1) == p.n_chunks - 1) ? 1 : 0;
+                named_bar_sync(1, kEpi);
+                if (*last_flag) {
+                    __threadfence();
+                    const float* P0 = p.partial + ((int64_t)b * p.H_q + h * G) * qstride;
+                    if (et < G) {
+                        const float* Pq = P0 + et * qstride;
+                        float mx = -INFINITY;
+                        for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
+                            float mc[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                mc[u] = c0 + u < p.n_chunks ? __ldcg(Pq + (c0 + u) * rw + 128) : -INFINITY;
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) mx = fmaxf(mx, mc[u]);
+                        }
+                        float l = 0.0f;
+                        for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
+                            float mc[8], lc[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const bool in = c0 + u < p.n_chunks;
+                                mc[u] = in ? __ldcg(Pq + (c0 + u) * rw + 128) : -INFINITY;
+                                lc[u] = in ? __ldcg(Pq + (c0 + u) * rw + 129) : 0.0f;
+                            }
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                if (c0 + u >= p.n_chunks) break;
+                                const float w = mc[u] == -INFINITY ? 0.0f : __expf(mc[u] - mx);
+                                Wc[et * kMaxMergeChunks + c0 + u] = w;
+                                l = fmaf(w, lc[u], l);
+                            }
+                        }
+                        ML[et * 2] = mx;
+                        ML[et * 2 + 1] = l;
+                    }
+                    named_bar_sync(1, kEpi);
+                    for (int e = et; e < G * 128; e += kEpi) {
+                        const int jq = e >> 7, i = e & 127;
+                        const float* Pq = P0 + jq * qstride + i;
+                        float a = 0.0f;
+                        for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
+                            float v[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) v[u] = c0 + u < p.n_chunks ? __ldcg(Pq + (c0 + u) * rw) : 0.0f;
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                if (c0 + u < p.n_chunks) a = fmaf(Wc[jq * kMaxMergeChunks + c0 + u], v[u], a);
+                        }
+                        const float L = ML[jq * 2 + 1];
+                        p.out[((int64_t)b * p.H_q + h * G + jq) * 128 + i] = L > 0.0f ? a / L : 0.0f;
+                    }
+                    if (p.lse && et < G) {
+                        const float L = ML[et * 2 + 1];
+                        p.lse[(int64_t)b * p.H_q + h * G + et] = L > 0.0f ? ML[et * 2] + logf(L) : -INFINITY;
+                    }
+                    if (et == 0) p.cnt[bh] = 0;
+                }
+            }
         }
     }
 
@@ -513,110 +596,45 @@ __global__ void __launch_bounds__(kVThreads, 2)
     if (*abort_flag && threadIdx.x == 0) flag(p.check, LOWRAM_CHECK_TIMEOUT);
     if (warp == 1) {
         fence_after();
-        tmem_dealloc(tmem, tcols);
+        tmem_dealloc(tmem, (uint32_t)(2 * M));
     }
 }
-
-// ------------------------------------------------------------------------------------------------
-// K4 for the tensor-core path: merge the chunks' partials of one (sequence, q-head), then apply the
-// predictor's second layer and bias to the merged hidden-unit sums:
-//   W = max_c M_c, w_c = exp(M_c - W), L = sum_c w_c l_c,
-//   out = w2[h] (sum_c w_c z_c / L) + b2[h] + sum_c w_c rz_c / L,  lse = W + log L.
-// One CTA of 128 threads per (sequence, q-head).
-// ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ float block_reduce_128(float v, float* red, bool is_max) {
-    v = is_max ? warp_max(v) : warp_sum(v);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = is_max ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) : (red[0] + red[1]) + (red[2] + red[3]);
-    __syncthreads();
-    return r;
-}
-
-__global__ void __launch_bounds__(128) merge_w2_kernel(int H_q, int G, int n_chunks, int m, int PW,
-                                                       const float* __restrict__ partial,
-                                                       const __nv_bfloat16* __restrict__ w2,
-                                                       const float* __restrict__ b2, float* __restrict__ out,
-                                                       float* __restrict__ lse) {
-    extern __shared__ float msm[];
-    __shared__ float red[4];
-    float* wts = msm;               // [n_chunks]
-    float* zb = msm + n_chunks;     // [m + 128]: merged hidden sums, then merged residual sums
-    const int bhq = blockIdx.x, h = (bhq % H_q) / G, tid = threadIdx.x;
-    const float* P = partial + (int64_t)bhq * n_chunks * PW;
-    float M = -INFINITY;
-    for (int c = tid; c < n_chunks; c += 128) M = fmaxf(M, P[(int64_t)c * PW + m + 128]);
-    M = block_reduce_128(M, red, true);
-    float L = 0.0f;
-    for (int c = tid; c < n_chunks; c += 128) {
-        const float mc = P[(int64_t)c * PW + m + 128];
-        const float w = (mc == -INFINITY) ? 0.0f : __expf(mc - M);
-        wts[c] = w;
-        L = fmaf(w, P[(int64_t)c * PW + m + 129], L);
-    }
-    L = block_reduce_128(L, red, false);
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    for (int j = tid; j < m + 128; j += 128) {
-        float acc = 0.0f;
-        for (int c = 0; c < n_chunks; ++c) acc = fmaf(wts[c], P[(int64_t)c * PW + j], acc);
-        zb[j] = acc * inv;
-    }
-    __syncthreads();
-    // thread i: out[i] = w2[h][i, :] . zbar; the row's 16-byte pieces are independent loads
-    const __nv_bfloat16* W2 = w2 + ((int64_t)h * 128 + tid) * m;
-    float acc = 0.0f;
-    for (int j0 = 0; j0 < m; j0 += 64) {
-        uint4 wv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) wv[u] = __ldg(reinterpret_cast<const uint4*>(W2 + j0 + u * 8));
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&wv[u]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(pr[e]);
-                acc = fmaf(f.x, zb[j0 + u * 8 + 2 * e], acc);
-                acc = fmaf(f.y, zb[j0 + u * 8 + 2 * e + 1], acc);
-            }
-        }
-    }
-    out[(int64_t)bhq * 128 + tid] = L > 0.0f ? acc + (b2 ? b2[(int64_t)h * 128 + tid] : 0.0f) + zb[m + tid] : 0.0f;
-    if (lse && tid == 0) lse[bhq] = L > 0.0f ? M + logf(L) : -INFINITY;
-}
-
 
 }  // namespace
 
 bool tc_vregen_supported(const lowram_decode_shape& s) {
-    return tc_score_supported(s) && (s.m == 128 || s.m == 256) && s.d == 128;
+    return tc_score_supported(s) && (s.m == 128 || s.m == 256) && s.d == 128 && vregen_config(s.m, s.r).NS >= 2;
 }
 
-int tc_partial_width(const lowram_decode_shape& s) { return s.m + s.d + 4; }
+int tc_partial_width(const lowram_decode_shape& s) { return s.d + 2; }
 
-// The last CTA of each (sequence, kv-head) merges in the value kernel when the merge's shared scratch
-// (chunk weights and merged sums of the G q-heads) fits in the ring.
-bool tc_fused_merge(const lowram_decode_shape& s, int n_chunks) {
-    // merge_last's shared memory: Z [G][m+128], chunk weights [G][n_chunks], W and L [G][2], 16 bytes of
-    // alignment, and one q-head's records [n_chunks][PW]
-    const size_t g = s.H_q / s.H_kv, zw = s.m + 128, pw = tc_partial_width(s);
-    return (g * zw + g * (size_t)n_chunks + 2 * g + 4 + (size_t)n_chunks * pw) * sizeof(float) <=
-           (size_t)kNS * kStageBytes;
-}
+// The CTA finishing a (sequence, kv-head) merges its chunks when their weights fit the merge scratch.
+bool tc_fused_merge(const lowram_decode_shape&, int n_chunks) { return n_chunks <= kMaxMergeChunks; }
 
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     const auto& s = a.s;
     VregenTcParams p{};
+    p.B = s.B;
     p.T = s.T;
     p.H_q = s.H_q;
     p.H_kv = s.H_kv;
-    p.r = s.r;
     p.m = s.m;
+    p.r = s.r;
+    p.coef = (const __nv_bfloat16*)a.coef;
     p.S_eff = a.S_eff;
     p.n_chunks = a.n_chunks;
     p.n_res = s.n_res;
     p.KC = s.r / 64;
-    p.PW = a.PW;
-    p.coef = (const __nv_bfloat16*)a.coef;
+    const VregenConfig cfg = vregen_config(s.m, s.r);
+    p.NS = cfg.NS;
+    p.f_resident = cfg.f_resident ? 1 : 0;
+    p.n_items = s.B * s.H_kv * a.n_chunks;
+    const int copies = (s.basis_batch_stride || s.mlp_batch_stride) ? s.B : 1;
+    p.fold_per_seq = copies > 1 ? 1 : 0;
+    p.mlp_stride = s.mlp_batch_stride;
+    const bool f16 = s.coef_dtype == kCoefF16;
+    p.idesc = f16 ? tc::idesc_f16(128, 128) : tc::idesc_bf16(128, 128);
+    p.wait_cycles = a.wait_cycles > 0 ? a.wait_cycles : tc::kWaitCycles;
     p.sall = a.sall;
     p.b1 = a.b1;
     p.b2 = a.b2;
@@ -629,45 +647,28 @@ cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     p.out = a.out;
     p.lse = a.lse;
     p.check = a.check;
-    if ((int64_t)s.B * a.n_chunks == 0) return cudaSuccess;
-    CUtensorMap mW, mW1;
-    const uint64_t dW[2] = {(uint64_t)s.r, (uint64_t)s.H_kv * s.d};
-    const uint32_t bW[2] = {64, 128};
-    const uint64_t dW1[2] = {(uint64_t)s.d, (uint64_t)s.H_kv * s.m};
-    const uint32_t bW1[2] = {64, 128};
-    if (!tc::make_map(&mW, a.basis, 2, dW, bW) || !tc::make_map(&mW1, a.w1, 2, dW1, bW1)) return cudaErrorInvalidValue;
-    const size_t smem = vregen_smem_bytes();
-    dim3 grid((unsigned)a.n_chunks, (unsigned)s.H_kv, (unsigned)s.B);
+    if (p.n_items == 0) return cudaSuccess;
+    if (!a.fold || cfg.NS < 2) return cudaErrorInvalidValue;
+    CUtensorMap mF;
+    const uint64_t dF[2] = {(uint64_t)s.r, (uint64_t)copies * s.H_kv * s.m};
+    const uint32_t bF[2] = {64, 128};
+    if (!tc::make_map(&mF, a.fold, 2, dF, bF, 0, f16)) return cudaErrorInvalidValue;
+    const int grid = std::min(p.n_items, tc::sm_count());
     cudaError_t e = cudaSuccess;
     auto go = [&](auto kern) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) {
-            e = launch_pdl(kern, grid, dim3(kVThreads), smem, st, mW, mW1, p);
-        }
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
+        if (e == cudaSuccess) e = launch_pdl(kern, dim3(grid), dim3(kVThreads), cfg.smem, st, mF, p);
     };
+    const bool two = s.m == 256;
     switch (s.H_q / s.H_kv) {
-        case 1: go(vregen_tc_kernel<1>); break;
-        case 2: go(vregen_tc_kernel<2>); break;
-        case 4: go(vregen_tc_kernel<4>); break;
-        case 7: go(vregen_tc_kernel<7>); break;
-        case 8: go(vregen_tc_kernel<8>); break;
+        case 1: two ? go(vregen_tc_kernel<1, 2>) : go(vregen_tc_kernel<1, 1>); break;
+        case 2: two ? go(vregen_tc_kernel<2, 2>) : go(vregen_tc_kernel<2, 1>); break;
+        case 4: two ? go(vregen_tc_kernel<4, 2>) : go(vregen_tc_kernel<4, 1>); break;
+        case 7: two ? go(vregen_tc_kernel<7, 2>) : go(vregen_tc_kernel<7, 1>); break;
+        case 8: two ? go(vregen_tc_kernel<8, 2>) : go(vregen_tc_kernel<8, 1>); break;
         default: return cudaErrorNotSupported;
     }
     return e;
-}
-
-cudaError_t launch_merge_w2(const DecodeArgs& a, int n_chunks, cudaStream_t st) {
-    const auto& s = a.s;
-    const int BH = s.B * s.H_q;
-    if (BH == 0) return cudaSuccess;
-    const size_t smem = sizeof(float) * ((size_t)n_chunks + s.m + 128);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(merge_w2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    merge_w2_kernel<<<(unsigned)BH, 128, smem, st>>>(s.H_q, a.g, n_chunks, s.m, a.PW, a.partial,
-                                                     (const __nv_bfloat16*)a.w2, a.b2, a.out, a.lse);
-    return cudaGetLastError();
 }
 
 }  // namespace lowram

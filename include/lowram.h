@@ -97,15 +97,27 @@ typedef struct {
     int32_t res_dtype;  /* LOWRAM_F32, LOWRAM_BF16 or LOWRAM_INT8_VEC */
     int32_t max_pos;    /* rows of the RoPE tables: positions are in [0, max_pos) */
     float sm_scale;     /* softmax scale; <= 0 selects 1/sqrt(d) */
+    int64_t basis_batch_stride; /* elements from sequence b's basis to b+1's; 0: one basis for every sequence.
+                                   Else >= H_kv*d*r and a multiple of 8 (16-byte rows for the TMA maps) */
+    int64_t mlp_batch_stride;   /* elements from sequence b's w1 (and w2) to b+1's; 0: one predictor for every
+                                   sequence.  Else >= H_kv*m*d and a multiple of 8; b1, b2 (when given) are then
+                                   [B, H_kv, m] and [B, H_kv, d] */
+    uint32_t flags;             /* LOWRAM_FLAG_* bits; 0 for the defaults */
 } lowram_decode_shape;
+
+/* int4 caches with bf16 activations on the tensor cores: split each dequantised coefficient exactly into two bf16
+ * terms (rank 2r: twice the key-rebuild work and a 4r-byte copy per token) instead of the default single fp16 term
+ * (code * scale rounded to fp16, 2^-12 relative; the basis and the folded predictor weights taken in fp16). */
+#define LOWRAM_FLAG_INT4_EXACT_SPLIT 1u
 
 /* Workspace bytes lowram_decode_attn needs for this shape (a multiple of 256). */
 LOWRAM_API lowram_status lowram_decode_workspace_size(const lowram_decode_shape* shape, size_t* bytes);
 
 /* *yes = 1 if calls of this shape run the key pass and the value regeneration on the tensor cores
- * (tcgen05; bf16 caches, and int4 caches with bf16 activations and r <= 512: these are first split exactly
- * into two bf16 terms, coefficient = hi + lo, stored in the workspace as a rank-2r bf16 cache), 0 if they run
- * on the CUDA cores (float32 caches and shapes the tensor-core kernels do not cover). */
+ * (tcgen05; bf16 caches, and int4 caches with bf16 activations: these are first dequantised into an fp16 copy in
+ * the workspace, or with LOWRAM_FLAG_INT4_EXACT_SPLIT and r <= 512 split exactly into two bf16 terms,
+ * coefficient = hi + lo, stored as a rank-2r bf16 cache), 0 if they run on the CUDA cores (float32 caches and
+ * shapes the tensor-core kernels do not cover). */
 LOWRAM_API lowram_status lowram_decode_uses_tensor_cores(const lowram_decode_shape* shape, int32_t* yes);
 
 /*
@@ -126,9 +138,13 @@ LOWRAM_API lowram_status lowram_decode_uses_tensor_cores(const lowram_decode_sha
  *   coef_scale LOWRAM_INT4_G32 only: [B, T, r/32] fp16 scales; else NULL
  *   pos        [B, T] int32 original positions (eviction); NULL means position t
  *   rope_cos, rope_sin  [d/2, max_pos] float32 each (frequency-major), see lowram_rope_table
- *   basis      [H_kv*d, r] act_dtype (row h*d+i: latent coefficients of key feature (h, i))
+ *   basis      [H_kv*d, r] act_dtype (row h*d+i: latent coefficients of key feature (h, i)); with
+ *              basis_batch_stride != 0, sequence b's basis starts basis_batch_stride elements after b-1's
  *   w1         [H_kv, m, d] act_dtype;  b1 [H_kv, m] float32 or NULL
- *   w2         [H_kv, d, m] act_dtype;  b2 [H_kv, d] float32 or NULL
+ *   w2         [H_kv, d, m] act_dtype;  b2 [H_kv, d] float32 or NULL; with mlp_batch_stride != 0, sequence
+ *              b's w1 and w2 start mlp_batch_stride elements after b-1's, and b1, b2 are [B, H_kv, m], [B, H_kv, d]
+ *              (a predictor fitted per prompt, LowRAM abstract: "fits a lightweight per-head predictor at test
+ *              time")
  *   res_idx    [B, H_kv, n_res] int32, strictly ascending per (b, h), in [0, T)
  *   res_val    [B, H_kv, n_res, d] res_dtype
  *   res_scale  LOWRAM_INT8_VEC only: [B, H_kv, n_res] fp16; else NULL
@@ -432,6 +448,16 @@ LOWRAM_API const char* lowram_status_string(lowram_status status);
 LOWRAM_API const char* lowram_last_error(void);
 /* Library version: major * 10000 + minor * 100 + patch. */
 LOWRAM_API int32_t lowram_version(void);
+
+/*
+ * lowram_set_wait_limit -- testing aid for the failure path of the tensor-core value pass (no counterpart on
+ * the pages).  Every pipeline wait of that kernel (TMA stage landed, MMA done) gives up after `cycles` SM
+ * clock cycles; 0 restores the default (~1 s at 2 GHz).  A limit shorter than a wait legitimately takes makes
+ * the kernel give up on purpose: it then drains what it issued, frees its tensor memory, returns, and sets
+ * LOWRAM_CHECK_TIMEOUT in the workspace's check word; that call's out and lse are invalid.  Process-wide; not
+ * thread-safe against concurrent decode calls.  Errors: LOWRAM_ERR_INVALID_ARG for cycles < 0.
+ */
+LOWRAM_API lowram_status lowram_set_wait_limit(int64_t cycles);
 
 #ifdef __cplusplus
 }

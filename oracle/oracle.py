@@ -310,7 +310,24 @@ def decode(q, coef, basis, w1, w2, *, S: int, theta: float, pos=None, b1=None, b
     coef must already be decoded to values (``dequant_int4_g32`` for the int4 format); res_val likewise
     (``dequant_int8_vec``).  Shapes: q [B,H_q,d], coef [B,T,r], basis [H_kv*d,r], w1 [H_kv,m,d],
     w2 [H_kv,d,m], res_idx [B,H_kv,n_res], res_val [B,H_kv,n_res,d], pos [B,T] or None.
+
+    A basis [B,H_kv*d,r] gives each sequence its own basis, and w1 [B,H_kv,m,d], w2 [B,H_kv,d,m] (with b1
+    [B,H_kv,m], b2 [B,H_kv,d]) its own predictor: sequence b is then decoded with its own weights, one call
+    per sequence (the sequences of a call share nothing else).
     """
+    per_basis = np.ndim(basis) == 3
+    per_mlp = np.ndim(w1) == 4
+    if per_basis or per_mlp:
+        parts = []
+        for b in range(np.shape(q)[0]):
+            pick = lambda x, on: None if x is None else (f64(x)[b] if on else x)
+            sl = lambda x: None if x is None else f64(x)[b:b + 1]
+            parts.append(decode(sl(q), sl(coef), pick(basis, per_basis), pick(w1, per_mlp), pick(w2, per_mlp), S=S,
+                                theta=theta, pos=None if pos is None else _i32(pos)[b:b + 1],
+                                b1=pick(b1, per_mlp), b2=pick(b2, per_mlp),
+                                res_idx=None if res_idx is None else _i32(res_idx)[b:b + 1], res_val=sl(res_val),
+                                sm_scale=sm_scale, threads=threads))
+        return DecodeResult(*[np.concatenate([getattr(r, f) for r in parts]) for f in ("out", "lse", "key", "sel")])
     Q, C, W, W1, W2 = f64(q), f64(coef), f64(basis), f64(w1), f64(w2)
     B1, B2, RV = f64(b1), f64(b2), f64(res_val)
     RI, P = _i32(res_idx), _i32(pos)

@@ -15,6 +15,10 @@ import oracle as O
 from decode_attention_19_b300 import synth
 
 KEY_TOL = 1e-4       # |gpu key - oracle key|, selection keys (scaled logits)
+# int4 caches reach the tensor cores as an fp16 copy of code * scale (2^-12 relative rounding): the oracle's keys
+# from fp16-rounded coefficients differ from its exact ones by up to 7.9e-5 at these shapes, so int4 keys get twice
+# the bf16 tolerance (the exact two-term split, LOWRAM_FLAG_INT4_EXACT_SPLIT, keeps KEY_TOL)
+KEY_TOL_INT4_F16 = 2e-4
 BAND = 1e-3          # index sets may differ only within this distance of the cut-off
 OUT_MAX_ABS = 1e-2   # bf16 inputs, fp32 accumulation
 OUT_REL_L2 = 5e-3
@@ -56,7 +60,7 @@ def decode_case(w: synth.Workload, layer: int = 0, biases: bool = False) -> dict
     return c
 
 
-def run_gpu_decode(c: dict, *, S=None, hooks=True, workspace=None):
+def run_gpu_decode(c: dict, *, S=None, hooks=True, workspace=None, int4_exact_split=False):
     import decode_attention_19_b300 as L
     w = c["w"]
     S = w.S if S is None else S
@@ -79,11 +83,12 @@ def run_gpu_decode(c: dict, *, S=None, hooks=True, workspace=None):
                                     res_idx=cu(c["res_idx"]) if n_res else None,
                                     res_val=cu(c["res_val"]) if n_res else None,
                                     res_scale=cu(c["res_scale"]) if n_res else None, sel_out=sel, key_out=key,
-                                    workspace=workspace)
+                                    workspace=workspace, int4_exact_split=int4_exact_split)
     torch.cuda.synchronize()
     if own_ws:
         assert L.lowram_get_error(workspace) == 0, "device check word set"
-    r = {"out": out.cpu().double().numpy(), "lse": lse.cpu().double().numpy()}
+    r = {"out": out.cpu().double().numpy(), "lse": lse.cpu().double().numpy(),
+         "key_tol": KEY_TOL_INT4_F16 if (w.coef_fmt == "int4" and not int4_exact_split) else KEY_TOL}
     if hooks:
         r["key"] = key.cpu().double().numpy()
         r["sel"] = sel.cpu().numpy()
@@ -151,7 +156,9 @@ def check_out(gpu_out, orc_out, max_abs=OUT_MAX_ABS, rel_l2=OUT_REL_L2):
     return ma, rl
 
 
-def check_decode(gpu: dict, orc, S_eff: int, *, key_tol=KEY_TOL, max_abs=OUT_MAX_ABS, rel_l2=OUT_REL_L2):
+def check_decode(gpu: dict, orc, S_eff: int, *, key_tol=None, max_abs=OUT_MAX_ABS, rel_l2=OUT_REL_L2):
+    if key_tol is None:
+        key_tol = gpu.get("key_tol", KEY_TOL)
     P = orc.key.shape[0] * orc.key.shape[1]
     if "key" in gpu:
         kd = np.abs(gpu["key"] - orc.key)
@@ -260,9 +267,11 @@ def exact_projection_case(w: synth.Workload) -> dict:
 
 # Bounds on the rows whose stored coefficients differ between the float32 GPU projection and the fp64 one.  A bf16
 # coefficient flips with probability ~4e-4 (float32 emulation), so a row of r <= 640 flips with probability up
-# to ~1 - (1 - 4e-4)^640 = 23 %; an int4 group flips only where a quotient or a scale sits on a rounding tie.
+# to ~1 - (1 - 4e-4)^640 = 23 %; an int4 group flips only where a quotient or a scale sits on a rounding tie, and
+# a flipped fp16 group scale changes all 32 coefficients of its group (at most ~one group per flipped row:
+# 0.05 of the rows x 32 / 512 coefficients = 3.1e-3).
 FLIP_ROWS_MAX = {"bf16": 0.35, "int4": 0.05, "f32": 0.0}
-FLIP_COEF_MAX = {"bf16": 2e-3, "int4": 1e-3, "f32": 0.0}
+FLIP_COEF_MAX = {"bf16": 2e-3, "int4": 4e-3, "f32": 0.0}
 
 
 def check_compress(gpu: dict, orc: dict, w: synth.Workload, c: dict, bs=None):

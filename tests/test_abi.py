@@ -35,7 +35,7 @@ def test_status_strings_and_version():
 
 def shape(**kw):
     base = dict(B=8, T=8192, H_q=32, H_kv=8, d=128, r=512, m=128, S=1024, n_res=820, act_dtype=1, coef_dtype=1,
-                res_dtype=1, max_pos=8192, sm_scale=0.0)
+                res_dtype=1, max_pos=8192, sm_scale=0.0, basis_batch_stride=0, mlp_batch_stride=0, flags=0)
     base.update(kw)
     return L.lowram_decode_shape(*[base[f] for f, _ in L.lowram_decode_shape._fields_])
 
@@ -184,3 +184,26 @@ def test_eviction_entry_points_and_batch_limit_check_arguments_on_the_host():
     assert lib.lowram_fit_predictor_workspace_size(8, 128, 128, ctypes.byref(n)) == 0
     assert lib.lowram_predictor_grad(2, 1 << 30, 8, 128, 128, 1, None, None, None, None, None, None, None, None, None,
                                      None, None, None) == UNSUPPORTED
+
+
+def test_wait_limit_is_checked_on_the_host():
+    with pytest.raises(Bd.LowramError) as ei:
+        L.lowram_set_wait_limit(-1)
+    assert ei.value.status == 1
+    L.lowram_set_wait_limit(0)          # the default
+
+
+def test_batch_strides_are_checked_and_size_the_workspace():
+    per = 8 * 128 * 512
+    for kw in (dict(basis_batch_stride=per - 8), dict(basis_batch_stride=per + 4), dict(basis_batch_stride=-8),
+               dict(mlp_batch_stride=8 * 128 * 128 - 8), dict(mlp_batch_stride=8 * 128 * 128 + 2)):
+        with pytest.raises(Bd.LowramError) as ei:
+            L.lowram_decode_workspace_size(shape(**kw))
+        assert ei.value.status == 1, kw
+    shared = L.lowram_decode_workspace_size(shape())
+    own = L.lowram_decode_workspace_size(shape(basis_batch_stride=per, mlp_batch_stride=8 * 128 * 128))
+    if L.lowram_decode_uses_tensor_cores(shape()):    # (needs the driver's tensor-map encoder)
+        # one folded first layer [H_kv, m, r] bf16 per sequence instead of one for all
+        assert own - shared >= 7 * 8 * 128 * 512 * 2
+    else:
+        assert own == shared

@@ -112,3 +112,23 @@ def test_every_tensor_of_a_call_must_share_one_device():
     assert B._dev(_OnDevice(1), None, _OnDevice(1)) == torch.device("cuda", 1)
     with pytest.raises(L.LowramShapeError, match="one device"):
         B._dev(_OnDevice(0), _OnDevice(1))
+
+
+def test_batch_strides_follow_the_weight_ranks():
+    x = _decode_inputs(B=3)
+    shared = L.decode_shape(x["q"], x["coef"], x["w1"], S=8, n_res=4, max_pos=40, res_dtype=1, basis=x["basis"])
+    assert shared.basis_batch_stride == 0 and shared.mlp_batch_stride == 0
+    basis = torch.zeros(3, 2 * 64, 64, dtype=bf)
+    w1 = torch.zeros(3, 2, 32, 64, dtype=bf)
+    sh = L.decode_shape(x["q"], x["coef"], w1, S=8, n_res=4, max_pos=40, res_dtype=1, basis=basis)
+    assert sh.basis_batch_stride == 2 * 64 * 64 and sh.mlp_batch_stride == 2 * 32 * 64
+    assert (sh.H_kv, sh.m) == (2, 32)
+
+
+def test_per_sequence_weights_must_cover_every_sequence():
+    x = _decode_inputs(B=3)
+    with pytest.raises(L.LowramShapeError, match="w2"):
+        _decode(x, w1=torch.zeros(3, 2, 32, 64, dtype=bf), w2=torch.zeros(2, 2, 64, 32, dtype=bf))
+    with pytest.raises(L.LowramShapeError, match="b1"):
+        _decode(x, w1=torch.zeros(3, 2, 32, 64, dtype=bf), w2=torch.zeros(3, 2, 64, 32, dtype=bf),
+                b1=torch.zeros(2, 32, dtype=f32))

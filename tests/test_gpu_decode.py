@@ -42,11 +42,16 @@ def test_bf16_and_int4_workloads_take_the_tensor_core_key_pass():
     tiny = W["tiny"]
     sh = L.lowram_decode_shape(1, 256, 4, 2, 64, 32, 64, 256, 64, 0, 0, 0, 256, 0.0)
     assert not L.lowram_decode_uses_tensor_cores(sh)
-    # int4 coefficients with bf16 activations: exact two-term bf16 split of rank 2r, then the same kernels
+    # int4 coefficients with bf16 activations: an fp16 copy (or the exact two-term bf16 split of rank 2r), then
+    # the same kernels
     w = W["evict_quant"]
     sh = L.lowram_decode_shape(w.B, w.T, w.H_q, w.H_kv, w.d, w.r, w.m, w.S, w.n_res, 1, 2, 3, w.T_nominal, 0.0)
     assert L.lowram_decode_uses_tensor_cores(sh)
+    sh.flags = L.FLAG_INT4_EXACT_SPLIT
+    assert L.lowram_decode_uses_tensor_cores(sh)
     sh = L.lowram_decode_shape(w.B, w.T, w.H_q, w.H_kv, w.d, 1024, w.m, w.S, w.n_res, 1, 2, 3, w.T_nominal, 0.0)
+    assert L.lowram_decode_uses_tensor_cores(sh)        # fp16 copy of rank 1024
+    sh.flags = L.FLAG_INT4_EXACT_SPLIT
     assert not L.lowram_decode_uses_tensor_cores(sh)   # rank 2r = 2048 is past the key pass's limit
 
 
@@ -180,3 +185,44 @@ def test_decode_full_size_sampled(name):
         part = {"out": gpu["out"][b:b + 1, h * g:(h + 1) * g], "lse": gpu["lse"][b:b + 1, h * g:(h + 1) * g],
                 "key": gpu["key"][b:b + 1, h:h + 1], "sel": gpu["sel"][b:b + 1, h:h + 1]}
         C.check_decode(part, orc, w.S_eff)
+
+
+def _per_sequence(c, per_basis, per_mlp):
+    """Sequence b gets layer b's basis and/or predictor (with biases) of the same draw: different weights per
+    sequence, stacked along a leading batch dimension."""
+    w = c["w"]
+    raw = synth.draw_group(w.with_(G=max(w.G, w.B)), 0, with_noise=False)
+    c = dict(c)
+    act = c["w1"].dtype
+    if per_basis:
+        c["basis"] = torch.stack([raw["basis"][b] for b in range(w.B)]).to(act)
+    if per_mlp:
+        c["w1"] = torch.stack([raw["w1"][b] for b in range(w.B)]).to(act)
+        c["w2"] = torch.stack([raw["w2"][b] for b in range(w.B)]).to(act)
+        c["b1"] = synth.gaussian((w.B, w.H_kv, w.m), 0.1, w.seed, w.name, "b1-seq", 0)
+        c["b2"] = synth.gaussian((w.B, w.H_kv, w.d), 0.1, w.seed, w.name, "b2-seq", 0)
+    return c
+
+
+@pytest.mark.parametrize("name,per_basis,per_mlp", [
+    ("llama8b_small", True, False), ("llama8b_small", False, True), ("llama8b_small", True, True),
+    ("peak_small", True, True), ("tiny_ragged_S", True, True), ("evict_quant_small", True, True)])
+def test_decode_per_sequence_bases_and_predictors(name, per_basis, per_mlp):
+    """A basis and a predictor per sequence (the batch strides of the C shape): each sequence is decoded with its
+    own weights.  peak_small has an odd number of 128-token tiles per sequence, so the key pass's tile pairs must
+    stay inside a sequence; the int4 workload runs with a repeated basis per sequence."""
+    w = SMALL[name].with_(B=3)
+    c = _per_sequence(C.decode_case(w), per_basis, per_mlp)
+    C.check_decode(C.run_gpu_decode(c), C.run_oracle_decode(c), w.S_eff)
+
+
+@pytest.mark.parametrize("exact", [False, True])
+@pytest.mark.parametrize("H_q,H_kv,r", [(32, 8, 512), (28, 4, 384), (16, 2, 1024)])
+def test_decode_int4_fp16_copy_and_exact_split(exact, H_q, H_kv, r):
+    """int4 caches on the tensor cores: the default fp16 copy of code * scale (keys within KEY_TOL_INT4_F16) and
+    the exact two-term bf16 split (keys within KEY_TOL); r = 1024 takes the fp16 copy only."""
+    if exact and r > 512:
+        pytest.skip("the exact split doubles the rank past the key pass's limit")
+    w = SMALL["evict_quant_small"].with_(H_q=H_q, H_kv=H_kv, r=r)
+    c = C.decode_case(w)
+    C.check_decode(C.run_gpu_decode(c, int4_exact_split=exact), C.run_oracle_decode(c), w.S_eff)

@@ -662,3 +662,35 @@ def test_selection_projection_copies_key_features_exactly():
         mine = (sel >= l * rows) & (sel < (l + 1) * rows)
         want[:, :, sel[mine] - l * rows] = keys[:, :, sel[mine]]
         assert np.array_equal(rebuilt, want)
+
+
+def test_per_sequence_bases_and_predictors_pair_with_their_sequence():
+    """A basis and a predictor given per sequence are used with that sequence only: permuting sequence b's latent
+    dimensions (in its coefficients and its basis together) and its hidden units (w1 rows, b1, w2 columns
+    together) leaves every output as with the shared weights, while giving sequence 0 sequence 1's basis changes
+    sequence 0's output and no other."""
+    from decode_attention_19_b300 import synth
+    w = synth.WORKLOADS["tiny"].with_(B=3, T=40, S=17, r=32, m=64)
+    raw = synth.draw_group(w, 0, with_noise=False)
+    q = synth.draw_query(w, 0)
+    coef = O.f64(raw["coef"])
+    W, W1, W2 = O.f64(raw["basis"][0]), O.f64(raw["w1"][0]), O.f64(raw["w2"][0])
+    b1 = RNG.normal(0, 0.1, (w.H_kv, w.m))
+    b2 = RNG.normal(0, 0.1, (w.H_kv, w.d))
+    ref = O.decode(q, coef, W, W1, W2, S=w.S, theta=w.theta, b1=b1, b2=b2)
+    perms_r = [RNG.permutation(w.r) for _ in range(w.B)]
+    perms_m = [RNG.permutation(w.m) for _ in range(w.B)]
+    coef_p = np.stack([coef[b][:, p] for b, p in enumerate(perms_r)])
+    Wb = np.stack([W[:, p] for p in perms_r])
+    W1b = np.stack([W1[:, p, :] for p in perms_m])
+    b1b = np.stack([b1[:, p] for p in perms_m])
+    W2b = np.stack([W2[:, :, p] for p in perms_m])
+    b2b = np.stack([b2] * w.B)
+    got = O.decode(q, coef_p, Wb, W1b, W2b, S=w.S, theta=w.theta, b1=b1b, b2=b2b)
+    np.testing.assert_allclose(got.out, ref.out, atol=1e-12)
+    np.testing.assert_allclose(got.key, ref.key, atol=1e-12)
+    assert np.array_equal(got.sel, ref.sel)
+    Wswap = np.stack([W * 1.5, W, W])
+    sw = O.decode(q, coef, Wswap, W1, W2, S=w.S, theta=w.theta, b1=b1, b2=b2)
+    assert not np.allclose(sw.out[0], ref.out[0])
+    np.testing.assert_allclose(sw.out[1:], ref.out[1:], atol=1e-12)
