@@ -63,7 +63,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "liblowram.so")
 
 LOWRAM_F32, LOWRAM_BF16, LOWRAM_INT4_G32, LOWRAM_INT8_VEC = 0, 1, 2, 3
-CHECK_POS_RANGE, CHECK_RES_INDEX, CHECK_TIMEOUT, CHECK_NOT_PD = 1, 2, 4, 8
+CHECK_POS_RANGE, CHECK_RES_INDEX, CHECK_TIMEOUT, CHECK_NOT_PD, CHECK_LAYOUT = 1, 2, 4, 8, 16
 FLAG_INT4_EXACT_SPLIT = 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported", 4: "workspace", 5: "cuda",
           6: "device check"}

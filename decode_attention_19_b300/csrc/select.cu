@@ -1,17 +1,18 @@
 // select.cu -- K2: exact top-n of each row of a float matrix, ties to the lower index, output
-// ascending.  Used for the per-(sequence, kv-head) token selection of decode (LowRAM abstract:
-// "reconstructing only a selected subset of KV pairs at each decoding step"; the rule -- exact
-// largest scores -- is this library's reading) and for the worst-n_res residual tokens of the write
-// side ("stores residuals only for the tokens it reconstructs worst").
+// ascending.  Used for the per-(sequence, kv-head) token selection of decode (the LowRAM abstract has each
+// decoding step rebuild only a chosen subset of the cached tokens; taking the exactly largest scores is this
+// library's reading) and for the worst-n_res residual tokens of the write side (the abstract keeps residuals
+// for the tokens the predictor rebuilds worst).
 //
 // Radix select on order-preserving uint32 keys: four 8-bit digit passes narrow the candidates to
 // the exact value of the n-th largest element (the threshold) and how many elements equal to it must
 // be kept; a final pass in index order keeps every element above the threshold and the
-// lowest-indexed equal ones, writing their indices ascending (each warp compacts a contiguous segment
-// after one exchange of per-warp counts).
-// One CTA per row; rows up to 48K elements are read once into shared memory.
+// lowest-indexed equal ones, writing their indices ascending.
+// Rows of up to 256K elements are held in registers across a cluster of up to eight CTAs; longer rows take
+// one CTA each and stream from memory (rows up to 48K elements read once into shared memory).
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace lowram {
 
@@ -43,7 +44,7 @@ constexpr int kFoldPadA = 8, kFoldPadB = 8;   // bf16 of padding per shared row:
 size_t fold_smem_bytes(int d) {
     return sizeof(uint16_t) * ((size_t)kFoldJ * (d + kFoldPadA) + (size_t)d * (kFoldK + kFoldPadB));
 }
-int fold_blocks(const FoldArgs& f) {
+__host__ __device__ int fold_blocks(const FoldArgs& f) {
     return f.F ? f.copies * f.H_kv * (int)cdiv(f.m, kFoldJ) * (int)cdiv(f.r, kFoldK) : 0;
 }
 
@@ -297,50 +298,122 @@ __global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_k
     if (x.hit) match_residuals<Staged>(T, n_keep, o, x, row, staged);
 }
 
-// Rows of up to 32K elements: each of the 1024 threads holds E consecutive elements' order keys in registers
-// (thread t: elements [t E, t E + E)), so no pass reads memory.  One shared 256-bin histogram per pass
-// (double-buffered: the next pass's is cleared during this one), the first digit's atomics aggregated per warp
-// (its few distinct exponents would otherwise collide), two barriers per pass, and an early stop once the
-// threshold bin is kept whole.  One block-wide scan of (above, equal) counts gives each thread its output offset,
-// and the residual list (a caller input, staged in shared memory before waiting for the keys) is searched for the
-// thread's own kept tokens.
+// cluster helpers: the cluster's CTA count, and loads from a cluster CTA's shared memory (address from mapa)
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void ld_cluster_8(uint32_t addr, uint32_t (&v)[8]) {   // 32 bytes, 16-byte aligned
+    asm volatile(
+        "ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%8];\n\t"
+        "ld.shared::cluster.v4.u32 {%4, %5, %6, %7}, [%9];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+        : "r"(addr), "r"(addr + 16)
+        : "memory");
+}
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Rows of up to 256K elements, each split over a cluster of CL CTAs (CL = 1, 2, 4 or 8, the cluster's size; more
+// than one only for rows longer than 8192 elements, where the keys of one CTA would not fit its registers):
+// CTA c of a row holds elements [c Tc, c Tc + Tc), Tc = 1024 E, thread t the E consecutive ones from c Tc + t E,
+// as order keys in registers, so no pass reads memory.  Each pass builds a 256-bin histogram per CTA (the first
+// digit's atomics aggregated per warp: its few distinct exponents would otherwise collide), the cluster barrier
+// publishes it, and every CTA sums the CL histograms through distributed shared memory and finds the same
+// threshold bin (three histogram buffers in rotation: the one a pass clears was last read two barriers ago).  The
+// passes stop early once the threshold bin is kept whole.  Each CTA then counts its (above, equal) elements, the
+// cluster barrier publishes the counts, and a CTA's output starts after the lower-ranked CTAs' kept elements.
+// The residual row of a kept token is its rank in the row's ascending residual list: a bitmap of the list's
+// tokens in the CTA's range and the running count of its words (both built before the keys exist) give it in
+// constant time.  The kept tokens and their residual rows are staged in shared memory and written out coalesced.
 template <int E>
-__global__ void __launch_bounds__(kSelThreads) select_reg_kernel(int T, int n_keep, const float* __restrict__ values,
-                                                                int32_t* __restrict__ out, SelectExtras x) {
-    extern __shared__ uint32_t dyn[];               // the row's residual list (n_res ints), or the fold's tiles
-    __shared__ uint32_t hist[2][256];
-    __shared__ uint32_t s_prefix[2];
-    __shared__ int s_need[2], s_whole[2];
+__global__ void __launch_bounds__(kSelThreads) select_cl_kernel(int T, int n_keep, int cap, const float* __restrict__ values,
+                                                               int32_t* __restrict__ out, SelectExtras x) {
+    constexpr int Tc = E * kSelThreads, kWords = Tc / 32;   // elements and bitmap words per CTA
+    extern __shared__ uint32_t dyn[];   // fold tiles, or: bitmap [kWords], word prefix [kWords], staged output [2][cap]
+    __shared__ uint32_t hist[3][256];
+    __shared__ uint32_t s_prefix[3];
+    __shared__ int s_need[3], s_whole[3];
     __shared__ int wsum_gt[32], wsum_eq[32];
-    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ int s_tot[2];            // this CTA's elements above the threshold and equal to it (read by the peers)
+    __shared__ int s_res_below;         // residual tokens before this CTA's range
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int CL = (int)cluster_size(), crank = (int)tc::cluster_rank();
     grid_dep_trigger();
-    if (row >= x.rows) {   // a folding CTA: reads the caller's weights only
-        fold_block(x.fold, row - x.rows, reinterpret_cast<uint8_t*>(dyn));
+    const int row = blockIdx.x / CL;
+    if (row >= x.rows) {   // a folding CTA: reads the caller's weights only (no cluster traffic)
+        const int fi = blockIdx.x - x.rows * CL;
+        if (fi < fold_blocks(x.fold)) fold_block(x.fold, fi, reinterpret_cast<uint8_t*>(dyn));
         return;
     }
-    // before the keys exist: clear the first histogram, stage and check the residual list (caller inputs)
-    if (tid < 256) hist[0][tid] = 0;
+    const int lo = crank * Tc, hi = min(T, lo + Tc);   // this CTA's elements (lo may be >= T: an idle CTA)
+    uint32_t* bm = dyn;
+    uint32_t* bpre = dyn + kWords;
+    int32_t* so = reinterpret_cast<int32_t*>(dyn + 2 * kWords);
+    int32_t* sh = so + cap;
+    // before the keys exist: clear the first histogram; mark the residual list's tokens of this range, check the
+    // list (caller input; this CTA checks every CL-th entry) and count its tokens before the range
     const bool want_hit = x.hit != nullptr;
-    const int32_t* ri = want_hit ? x.res_idx + (int64_t)row * x.n_res : nullptr;
+    if (tid < 256) hist[0][tid] = 0;
+    if (tid == 0) s_res_below = 0;
+    if (want_hit)
+        for (int w = tid; w < kWords; w += kSelThreads) bm[w] = 0;
+    __syncthreads();
     if (want_hit) {
+        const int32_t* ri = x.res_idx + (int64_t)row * x.n_res;
         bool bad = false;
+        int below = 0;
         for (int j = tid; j < x.n_res; j += kSelThreads) {
             const int v = __ldg(ri + j);
-            bad |= v < 0 || v >= T || (j > 0 && v <= __ldg(ri + j - 1));
-            dyn[j] = (uint32_t)v;
+            if (j % CL == crank) bad |= v < 0 || v >= T || (j > 0 && v <= __ldg(ri + j - 1));
+            if (v >= lo && v < hi) atomicOr(&bm[(v - lo) >> 5], 1u << ((v - lo) & 31));
+            below += v < lo;
         }
         if (bad) flag(x.check, LOWRAM_CHECK_RES_INDEX);
+        below = warp_sum_int(below);
+        if (lane == 0 && below) atomicAdd(&s_res_below, below);
+        __syncthreads();
+        // bpre[w] = marked tokens in words before w (kWords <= 1024: one word per thread)
+        const int c = tid < kWords ? __popc(bm[tid]) : 0;
+        int incl = c;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o2);
+            if (lane >= o2) incl += y;
+        }
+        if (lane == 31) wsum_gt[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int a = wsum_gt[lane];
+            int s = a;
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, s, o2);
+                if (lane >= o2) s += y;
+            }
+            wsum_gt[lane] = s - a;
+        }
+        __syncthreads();
+        if (tid < kWords) bpre[tid] = wsum_gt[warp] + incl - c;
+        __syncthreads();   // wsum_gt is free again (the passes may be skipped)
     }
-    __syncthreads();     // the cleared histogram and the staged list before any use
     grid_dep_wait();     // the keys come from the kernel before (launched with launch_pdl)
-    if (x.zero_cnt && tid == 0) x.zero_cnt[row] = 0;
-    if (n_keep <= 0) return;
-    int32_t* o = out + (int64_t)row * n_keep;
-    const int t0 = tid * E;
+    if (x.zero_cnt && crank == 0 && tid == 0) x.zero_cnt[row] = 0;
+    if (n_keep <= 0) return;   // uniform over the cluster: no CTA touched another's memory
+    const int t0 = lo + tid * E;
     uint32_t k[E];
     {
         const float* v = values + (int64_t)row * T + t0;
-        if (t0 + E <= T && (((uintptr_t)v) & 15u) == 0) {
+        if (t0 + E <= hi && (((uintptr_t)v) & 15u) == 0) {
 #pragma unroll
             for (int i = 0; i < E; i += 4) {
                 const float4 f = __ldcg(reinterpret_cast<const float4*>(v + i));
@@ -351,19 +424,19 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(int T, int n_ke
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < E; ++i) k[i] = t0 + i < T ? order_key(__ldcg(v + i)) : 0u;
+            for (int i = 0; i < E; ++i) k[i] = t0 + i < hi ? order_key(__ldcg(v + i)) : 0u;
         }
     }
-    // keys past T are 0, the smallest order key: they are never counted (counting stops at T) nor taken
+    // elements past the range hold key 0 and are never counted (counting stops at hi) nor taken
     uint32_t prefix = 0, mask = 0;
     int need = n_keep;
     bool whole = n_keep >= T;       // every element is kept
     for (int pass = 0; pass < 4 && !whole; ++pass) {
-        const int shift = 24 - 8 * pass, cur = pass & 1;
-        if (tid < 256) hist[cur ^ 1][tid] = 0;      // the next pass's histogram (last read two barriers ago)
+        const int shift = 24 - 8 * pass, cur = pass % 3, nxt = (pass + 1) % 3;
+        if (tid < 256) hist[nxt][tid] = 0;
 #pragma unroll
         for (int i = 0; i < E; ++i) {
-            const bool in = t0 + i < T && (k[i] & mask) == prefix;
+            const bool in = t0 + i < hi && (k[i] & mask) == prefix;
             const uint32_t dg = (k[i] >> shift) & 255u;
             if (pass == 0) {
                 const unsigned act = __ballot_sync(0xffffffffu, in);
@@ -375,15 +448,21 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(int T, int n_ke
                 atomicAdd(&hist[cur][dg], 1u);
             }
         }
-        __syncthreads();
+        if (CL > 1) tc::cluster_sync();   // every CTA's histogram of this pass is complete and visible
+        else __syncthreads();
         if (warp == 0) {
-            // lane L owns bins [8L, 8L+8); suffix sums over lanes from the top bin down
+            // lane L owns bins [8L, 8L+8), summed over the cluster; suffix sums over lanes from the top bin down
             uint32_t c8[8], mine = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                c8[j] = hist[cur][lane * 8 + j];
-                mine += c8[j];
+            for (int j = 0; j < 8; ++j) c8[j] = 0;
+            for (int r = 0; r < CL; ++r) {
+                uint32_t v8[8];
+                ld_cluster_8(tc::peer_smem(&hist[cur][lane * 8], (uint32_t)r), v8);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) c8[j] += v8[j];
             }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mine += c8[j];
             uint32_t suf = mine;
 #pragma unroll
             for (int o2 = 1; o2 < 32; o2 <<= 1) {
@@ -408,23 +487,20 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(int T, int n_ke
         prefix = s_prefix[cur];
         need = s_need[cur];
         mask |= 0xFFu << shift;
-        if (s_whole[cur]) {
-            // the threshold bin is kept whole: keep every element whose resolved digits reach the bin
-            whole = true;
-        }
+        if (s_whole[cur]) whole = true;   // the threshold bin is kept whole: keep all that reach the bin
     }
     // take: above the threshold (resolved digits), or in the threshold bin -- all of it when the bin is kept whole,
-    // else the `need` lowest-indexed equal keys (the bin is one key value once all four digits are resolved)
+    // else the `need` lowest-indexed equal keys of the row (the bin is one key value once all digits are resolved)
     const bool all_T = n_keep >= T;
     int n_gt = 0, n_eq = 0;
 #pragma unroll
     for (int i = 0; i < E; ++i) {
-        if (t0 + i >= T) break;
+        if (t0 + i >= hi) break;
         const uint32_t u = k[i] & mask;
         if (all_T || u > prefix || (whole && u == prefix)) ++n_gt;
         else if (u == prefix) ++n_eq;
     }
-    // block-wide exclusive scan of (n_gt, n_eq)
+    // block-wide exclusive scan of (n_gt, n_eq), then the cluster's: the counts of the lower-ranked CTAs
     int gi = n_gt, ei = n_eq;
 #pragma unroll
     for (int o2 = 1; o2 < 32; o2 <<= 1) {
@@ -449,40 +525,61 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(int T, int n_ke
                 c += c2;
             }
         }
+        if (lane == 31) {
+            s_tot[0] = a;
+            s_tot[1] = c;
+        }
         wsum_gt[lane] = a - wsum_gt[lane];     // exclusive prefix over warps
         wsum_eq[lane] = c - wsum_eq[lane];
     }
-    __syncthreads();
-    const int gt_before = wsum_gt[warp] + gi - n_gt, eq_before = wsum_eq[warp] + ei - n_eq;
+    if (CL > 1) tc::cluster_sync();   // every CTA's totals are visible
+    else __syncthreads();
+    int gt_base = 0, eq_base = 0;
+    for (int r = 0; r < crank; ++r) {
+        gt_base += (int)ld_cluster_u32(tc::peer_smem(&s_tot[0], (uint32_t)r));
+        eq_base += (int)ld_cluster_u32(tc::peer_smem(&s_tot[1], (uint32_t)r));
+    }
+    const int out_base = gt_base + min(need, eq_base);
+    const int n_out = gt_base + s_tot[0] + min(need, eq_base + s_tot[1]) - out_base;
+    const int gt_before = gt_base + wsum_gt[warp] + gi - n_gt, eq_before = eq_base + wsum_eq[warp] + ei - n_eq;
     int at = gt_before + min(need, eq_before);
     int eq_rank = eq_before;
+    int32_t* o = out + (int64_t)row * n_keep;
     int32_t* hit = want_hit ? x.hit + (int64_t)row * n_keep : nullptr;
+    const int res_below = want_hit ? s_res_below : 0;
+    const bool staged = n_out <= cap;
 #pragma unroll
     for (int i = 0; i < E; ++i) {
         const int t = t0 + i;
-        if (t >= T) break;
+        if (t >= hi) break;
         const uint32_t u = k[i] & mask;
         bool take = all_T || u > prefix || (whole && u == prefix);
         if (!take && u == prefix) take = eq_rank++ < need;
         if (take) {
-            o[at] = t;
+            int found = -1;
             if (want_hit) {
-                int lo = 0, hi = x.n_res - 1, found = -1;
-                while (lo <= hi) {
-                    const int mid = (lo + hi) >> 1;
-                    const int v = (int)dyn[mid];
-                    if (v == t) {
-                        found = mid;
-                        break;
-                    }
-                    if (v < t) lo = mid + 1;
-                    else hi = mid - 1;
-                }
-                hit[at] = found;
+                const int w = (t - lo) >> 5, b = (t - lo) & 31;
+                const uint32_t word = bm[w];
+                if ((word >> b) & 1u) found = res_below + (int)bpre[w] + __popc(word & ((1u << b) - 1u));
+            }
+            if (staged) {
+                so[at - out_base] = t;
+                sh[at - out_base] = found;
+            } else {
+                o[at] = t;
+                if (want_hit) hit[at] = found;
             }
             ++at;
         }
     }
+    if (staged) {
+        __syncthreads();
+        for (int i = tid; i < n_out; i += kSelThreads) {
+            o[out_base + i] = so[i];
+            if (want_hit) hit[out_base + i] = sh[i];
+        }
+    }
+    if (CL > 1) tc::cluster_sync();   // no CTA leaves while a peer may still read its counts
 }
 
 size_t select_scratch_bytes(int, int, int) { return 0; }
@@ -495,23 +592,48 @@ cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, in
     if (fold) x.fold = *fold;
     const int nf = fold_blocks(x.fold);
     const size_t fold_smem = nf ? fold_smem_bytes(x.fold.d) : 0;
-    const dim3 grid((unsigned)(P + nf));
-    if (T <= 32 * kSelThreads) {
-        // register-resident rows; the residual list (n_res <= T ints) or the fold's tiles in dynamic shared memory
-        size_t smem = x.hit ? sizeof(uint32_t) * (size_t)n_res : 0;
+    // rows split over clusters while the CTAs stay within one wave and each keeps more than 4096 elements
+    // a row stays in one CTA up to 8 keys a thread (the barriers of a cluster cost more than the extra keys); longer
+    // rows split over a cluster while the CTAs still fit one wave
+    int CL = 1;
+    const int sms = tc::sm_count();
+    while (CL < 8 && (int64_t)P * CL * 2 <= sms && T > CL * 8 * kSelThreads) CL *= 2;
+    int E = 4;
+    while (E < 32 && (int64_t)E * kSelThreads * CL < T) E *= 2;
+    if ((int64_t)E * kSelThreads * CL >= T) {
+        const int Tc = E * kSelThreads;
+        const int cap = std::min(Tc, std::max(n_keep, 0)) <= 12288 ? std::min(Tc, std::max(n_keep, 0)) : 0;
+        size_t smem = sizeof(uint32_t) * (2 * (size_t)(Tc / 32) + 2 * (size_t)cap);
         if (fold_smem > smem) smem = fold_smem;
+        const int nfc = (int)cdiv(nf, CL) * CL;
         auto go = [&](auto kern) -> cudaError_t {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)(sizeof(uint32_t) * 32 * kSelThreads));
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            e = launch_pdl(kern, grid, dim3(kSelThreads), smem, st, T, n_keep, values, out, x);
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(P * CL + nfc));
+            cfg.blockDim = dim3(kSelThreads);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[2];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = (unsigned)CL;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 2;
+            e = cudaLaunchKernelEx(&cfg, kern, T, n_keep, cap, values, out, x);
             return e != cudaSuccess ? e : cudaGetLastError();
         };
-        if (T <= 4 * kSelThreads) return go(select_reg_kernel<4>);
-        if (T <= 8 * kSelThreads) return go(select_reg_kernel<8>);
-        if (T <= 16 * kSelThreads) return go(select_reg_kernel<16>);
-        return go(select_reg_kernel<32>);
+        switch (E) {
+            case 4: return go(select_cl_kernel<4>);
+            case 8: return go(select_cl_kernel<8>);
+            case 16: return go(select_cl_kernel<16>);
+            default: return go(select_cl_kernel<32>);
+        }
     }
+    const dim3 grid((unsigned)(P + nf));
     const bool staged = n_keep > 0 && T <= kSelMaxStaged;
     size_t smem = staged ? sizeof(uint32_t) * (size_t)T : 0;   // the staged keys also hold the residual list (n_res <= T)
     if (fold_smem > smem) smem = fold_smem;

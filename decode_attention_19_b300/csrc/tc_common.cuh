@@ -71,6 +71,21 @@ __device__ __forceinline__ bool mbar_wait_lim(uint64_t* bar, uint32_t parity, vo
     }
 }
 
+// Bytes of dynamic shared memory the launch gave this CTA.
+__device__ __forceinline__ uint32_t dyn_smem_bytes() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+    return n;
+}
+// True when a shared-memory layout that starts at the dynamic base and ends at `end` runs past the launch's
+// allocation; thread 0 then sets LOWRAM_CHECK_LAYOUT.  Every thread gets the same answer, so a kernel checks it before
+// any barrier or TMEM allocation and returns at once.
+__device__ __forceinline__ bool layout_overflows(const void* base, const void* end, uint32_t* check) {
+    const bool over = (uintptr_t)end - (uintptr_t)base > (uintptr_t)dyn_smem_bytes();
+    if (over && threadIdx.x == 0 && check) atomicOr(check, LOWRAM_CHECK_LAYOUT);
+    return over;
+}
+
 // Bounded wait that ignores the abort flag: used while draining after an abort.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
     const long long t0 = clock64();

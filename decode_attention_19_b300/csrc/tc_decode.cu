@@ -107,6 +107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
     uint64_t* m_drain = t_empty + 2;
     uint32_t* tmem_slot = (uint32_t*)(m_drain + 1);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+    if (layout_overflows(smem_raw, (const void*)(abort_flag + 1), p.check)) return;   // both CTAs of the pair alike
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();          // 0 issues the MMAs; 1 feeds its halves

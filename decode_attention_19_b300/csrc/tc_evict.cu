@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kWThreads, 2)
     uint64_t* mdone = qfull + 1;
     uint32_t* tmem_slot = (uint32_t*)(mdone + 1);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+    if (layout_overflows(smem_raw, (const void*)(abort_flag + 1), p.check)) return;
 
     const int tid = threadIdx.x, warp = tid >> 5, row = tid & (kWTile - 1), half = warp >> 2;
     const int b = blockIdx.y, c = blockIdx.x;

@@ -16,22 +16,24 @@
 //   - the second layer is linear, so sum_t p_t (w2 s_t + b2 + r_t) = w2 (sum_t p_t s_t) + b2 sum_t p_t +
 //     sum_t p_t r_t: a chunk applies w2 once per q-head to its softmax-weighted hidden sums, never forming the
 //     tokens' values, and writes a plain flash-decoding record (weighted value sum, max logit, weight sum).
-// The result equals "regenerate the selected values, then attend" up to rounding order; F in bf16 rounds the
+// The result equals regenerating the selected values and then attending, up to rounding order; F in bf16 rounds the
 // folded weights where the unfolded chain would round the rebuilt keys.
 //
 // K3 is persistent: one CTA per SM walks a contiguous range of work items (kv-head h, sequence b, chunk of 128
 // selected tokens), kv-head-major, so consecutive items share F_h, which stays resident in shared memory while
-// it fits (else each ring stage carries its F chunk).  448 threads:
-//   warp 0      TMA: F_h's k-chunks [m x 64] (once per kv-head, or per stage when streamed).
+// it fits (else each ring stage carries its F chunk).  384 threads (168 registers each):
+//   warp 0      lane 0: TMA of F_h's k-chunks [m x 64] (once per kv-head, or per stage when streamed);
+//               lane 1: merge tickets (the per-(b, h) chunk counter, one item behind the epilogue).
 //   warp 1      TMEM owner (two accumulators of m columns) and MMA issuer (one thread):
 //               D[m hidden x 128 tokens] = F_h . C_sel^T (M = 128 per 128 hidden units, N = 128, K = r), hidden
 //               units on TMEM lanes, tokens on columns; item j accumulates into buffer j % 2.
-//   warps 2-5   gather: 16-byte cp.async of the selected tokens' latent rows into the 128B-swizzled ring, one
+//   warps 2-3   gather: 16-byte cp.async of the selected tokens' latent rows into the 128B-swizzled ring, one
 //               64-wide k-chunk per stage, running ahead into the next items.
-//   warps 6-13  epilogue, one item after another while the next item's rows land and multiply: softmax weights
-//               of the chunk from the scaled logits the key pass stored, weighted residual rows; then per thread
-//               one hidden unit and half of the tokens: SiLU(D + b1) weighted by the softmax, summed; the TMEM
-//               buffer is released; w2 on the hidden sums; the chunk's record.
+//   warps 4-11  epilogue, one item after another while the next item's rows land and multiply: softmax weights
+//               of the chunk from the scaled logits the key pass stored (fetched an item ahead), the residual
+//               rows of the chunk's hits (loads issued before, used after, the accumulator read); per thread one
+//               hidden unit and half of the tokens: SiLU(D + b1) weighted by the softmax, summed; the TMEM buffer
+//               is released; w2 (rows held in registers per kv-head) on the hidden sums; the chunk's record.
 // The CTA finishing a (b, h)'s last chunk merges its chunks' records into out and lse (a counter per (b, h),
 // zeroed by the selection kernel; records read through L2).
 //
@@ -46,11 +48,12 @@ namespace lowram {
 
 namespace {
 
-constexpr int kVThreads = 448;
-constexpr int kGat = 128;                // gathering threads (warps 2-5)
+constexpr int kVThreads = 384;            // 12 warps: 168 registers a thread
+constexpr int kGat = 64;                 // gathering threads (warps 2-3)
 constexpr int kEpi = 256;                // epilogue threads (warps 6-13)
 constexpr int kRows = 128;               // selected tokens per item
 constexpr int kCBytes = kRows * 128;     // latent chunk [128 tokens x 64] bf16, 128B-swizzled
+constexpr int kGatRows = kRows / (kGat / 8);   // rows each gathering thread copies per stage
 constexpr int kMaxStages = 8;
 constexpr int kMaxMergeChunks = 64;      // chunks per (b, h) the fused merge takes (S <= 8192)
 constexpr size_t kSmemMax = 232448;
@@ -77,13 +80,12 @@ struct VregenTcParams {
     uint32_t* check;
 };
 
-// Epilogue scratch beside the ring: softmax weights [8][128], weighted residual sums [2][8][128], hidden sums
-// [2][8][m], the upper half's value sums [8][128], merge weights [8][64] and (W, L) [8][2], compacted hits
-// (rows, slots), reductions [2][32] + counts [4], then the barriers and the TMEM slot / flags.
-size_t scratch_bytes(int m) {
-    return (size_t)4 * (8 * kRows + 2 * 8 * kRows + 2 * 8 * m + 8 * kRows + 8 * kMaxMergeChunks + 16 + 2 * kRows +
-                        64 + 4) +
-           8 + 8 * (3 * kMaxStages + 2 + 4 + 1) + 16;
+// Epilogue scratch beside the ring, for g q-heads per kv-head: softmax weights [g][128], hidden sums [2][g][m],
+// the upper half's value sums [g][128], merge weights [g][64] and (W, L) [8][2], compacted hits (rows, slots),
+// reductions [2][32] + counts [4], then the barriers and the TMEM slot / flags.
+size_t scratch_bytes(int m, int g) {
+    return (size_t)4 * (g * kRows + 2 * g * m + g * kRows + g * kMaxMergeChunks + 16 + 2 * kRows + 64 + 4) + 8 +
+           8 * (3 * kMaxStages + 2 + 4 + 1 + 4) + 32;
 }
 
 struct VregenConfig {
@@ -92,9 +94,9 @@ struct VregenConfig {
     size_t smem;
 };
 
-VregenConfig vregen_config(int m, int r) {
+VregenConfig vregen_config(int m, int r, int g) {
     const int KC = r / 64;
-    const size_t fres = (size_t)KC * m * 128, fixed = 1024 + scratch_bytes(m);
+    const size_t fres = (size_t)KC * m * 128, fixed = 1024 + scratch_bytes(m, g);
     VregenConfig c{};
     if (fres + fixed + 3 * (size_t)kCBytes <= kSmemMax) {
         c.f_resident = true;
@@ -140,11 +142,10 @@ __global__ void __launch_bounds__(kVThreads, 1)
     uint8_t* Fres = smem;                                        // [KC][M x 64] when resident
     uint8_t* ring = smem + (fres ? (size_t)KC * kFChunk : 0);    // NS stages: C chunk [128 x 64] (+ F chunk)
     float* Ps = (float*)(ring + (size_t)NS * kStage);            // [G][128] softmax weights (0 on padding slots)
-    float* RZ = Ps + 8 * kRows;                                  // [2 halves][G][128] weighted residual rows
-    float* Z = RZ + 2 * 8 * kRows;                               // [2 token halves][G][M] hidden sums
-    float* X = Z + 2 * 8 * M;                                    // [G][128] the upper half's value sums
-    float* Wc = X + 8 * kRows;                                   // [G][n_chunks] merge weights
-    float* ML = Wc + 8 * kMaxMergeChunks;                        // [G][2] W and L of the merge
+    float* Z = Ps + G * kRows;                                   // [2 token halves][G][M] hidden sums
+    float* X = Z + 2 * G * M;                                    // [G][128] the upper half's value sums
+    float* Wc = X + G * kRows;                                   // [G][n_chunks] merge weights
+    float* ML = Wc + G * kMaxMergeChunks;                        // [G][2] W and L of the merge (16 floats)
     int* HitRow = (int*)(ML + 16);                               // compacted residual rows of the chunk's slots
     int* HitSlot = HitRow + kRows;                               // ... and those slots, ascending
     float* redM = (float*)(HitSlot + kRows);                     // [4 slot quarters][8] partial max
@@ -158,9 +159,12 @@ __global__ void __launch_bounds__(kVThreads, 1)
     uint64_t* t_full = f_empty + 1;              // [2] accumulator ready
     uint64_t* t_empty = t_full + 2;              // [2] epilogue done reading the accumulator
     uint64_t* m_drain = t_empty + 2;
-    uint32_t* tmem_slot = (uint32_t*)(m_drain + 1);
+    uint64_t* rec_done = m_drain + 1;            // [2] the item's record is written (one arrival, epilogue)
+    uint64_t* tick = rec_done + 2;               // [2] the helper lane took the item's merge ticket
+    uint32_t* tmem_slot = (uint32_t*)(tick + 2);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-    volatile int* last_flag = (volatile int*)(tmem_slot + 2);
+    volatile int* last_flag = (volatile int*)(tmem_slot + 2);   // [2] the ticket was the (b, h)'s last
+    if (layout_overflows(smem_raw, (const void*)(last_flag + 2), p.check)) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int it_begin = (int)((int64_t)blockIdx.x * p.n_items / gridDim.x);
@@ -192,8 +196,12 @@ __global__ void __launch_bounds__(kVThreads, 1)
             mbar_init(&t_empty[i], kEpi);
         }
         mbar_init(m_drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&rec_done[i], 1);
+            mbar_init(&tick[i], 1);
+            last_flag[i] = 0;
+        }
         *abort_flag = 0;
-        *last_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) prefetch_tmap(&tmF);
@@ -248,6 +256,20 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     for (uint32_t k = issued > (uint32_t)NS ? issued - NS : 0; k < issued; ++k)
                         mbar_wait_drain(&fullF[k % NS], (k / NS) & 1);
             }
+        } else if (lane == 1 && p.cnt) {
+            // ------------------------------------------------------------------ merge tickets
+            // once an item's record is written (the epilogue's writes ordered before rec_done at CTA scope, then
+            // made visible device-wide by this lane's fence), count the chunk for its (b, h); the count that
+            // completes the (b, h) tells the epilogue to merge it.  The epilogue waits for the ticket one item
+            // later, so the atomic's round trip overlaps the next item.
+            for (int j = 0; j < n_local; ++j) {
+                if (!mbar_wait_lim(&rec_done[j & 1], (j >> 1) & 1, abort_flag, p.wait_cycles)) break;
+                int h, b, c;
+                item_hbc(it_begin + j, h, b, c);
+                __threadfence();
+                last_flag[j & 1] = (atomicAdd(p.cnt + (int64_t)b * p.H_kv + h, 1) == p.n_chunks - 1) ? 1 : 0;
+                mbar_arrive(&tick[j & 1]);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
@@ -292,14 +314,14 @@ __global__ void __launch_bounds__(kVThreads, 1)
             mma_commit(m_drain);
             mbar_wait_drain(m_drain, 0);
         }
-    } else if (warp < 6) {
+    } else if (warp < 4) {
         // ------------------------------------------------------------------ gather (128 threads)
-        // thread gt copies the 16-byte piece c16 of rows rsub + 16 rr (rr < 8) of every k-chunk; a padding slot
+        // thread gt copies the 16-byte piece c16 of rows rsub + 8 rr (rr < 16) of every k-chunk; a padding slot
         // re-reads its sequence's token 0 (its softmax weight is 0)
         const int gt = threadIdx.x - 64, c16 = gt & 7, rsub = gt >> 3;
         const uint32_t total = (uint32_t)n_local * KC;
         uint32_t issued = 0, published = 0;
-        const __nv_bfloat16* srow[8];
+        const __nv_bfloat16* srow[kGatRows];
         bool gok = true;
         while (published < total) {
             if (gok && issued < total && issued - published < (uint32_t)NS) {
@@ -310,8 +332,8 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     item_hbc(it_begin + (int)(issued / KC), h, b, c);
                     const int64_t bh = (int64_t)b * p.H_kv + h;
 #pragma unroll
-                    for (int rr = 0; rr < 8; ++rr) {
-                        const int jr = c * kRows + rr * 16 + rsub;
+                    for (int rr = 0; rr < kGatRows; ++rr) {
+                        const int jr = c * kRows + rr * (kGat / 8) + rsub;
                         int t = jr < p.S_eff ? __ldg(p.sel + bh * p.S_eff + jr) : 0;
                         t = min(max(t, 0), p.T - 1);
                         srow[rr] = p.coef + ((int64_t)b * p.T + t) * p.r + c16 * 8;
@@ -323,8 +345,8 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 }
                 const uint32_t A = smem_u32(ring + s * kStage);
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    const int row = rr * 16 + rsub;
+                for (int rr = 0; rr < kGatRows; ++rr) {
+                    const int row = rr * (kGat / 8) + rsub;
                     cp_async_16(A + row * 128 + ((c16 ^ (row & 7)) << 4), srow[rr] + kc * 64, 16u);
                 }
                 cp_async_commit();
@@ -342,10 +364,10 @@ __global__ void __launch_bounds__(kVThreads, 1)
         cp_async_wait<0>();
     } else {
         // ------------------------------------------------------------------ epilogue (256 threads)
-        const int et = threadIdx.x - 192;
+        const int et = threadIdx.x - 128;
         const int slot = et & (kRows - 1), jh = et >> 7;         // jh: which half of the work this thread takes
         const int sq = slot >> 5;                                 // slot quarter (warp within its half)
-        const int q = warp & 3, ch = (warp - 6) >> 2;            // TMEM lane quarter, token half
+        const int q = warp & 3, ch = (warp - 4) >> 2;            // TMEM lane quarter, token half
         const int i_out = slot;
         auto chunk_max = [&](int jq) {
             return fmaxf(fmaxf(redM[jq], redM[8 + jq]), fmaxf(redM[16 + jq], redM[24 + jq]));
@@ -353,26 +375,132 @@ __global__ void __launch_bounds__(kVThreads, 1)
         auto chunk_sum = [&](int jq) { return (redL[jq] + redL[8 + jq]) + (redL[16 + jq] + redL[24 + jq]); };
         const int64_t rw = 128 + 2;
         const int64_t qstride = (int64_t)p.n_chunks * rw;
+        constexpr int SV = (G + 1) / 2;
+        // this slot's selection data of an item, fetched an item ahead in two steps so that no load waits on the
+        // critical path: the token and its residual row when the item before starts, then (once the token has
+        // landed) the scaled logits of q-heads jh, jh + 2, ...
+        auto fetch_sel = [&](int it, int& tok, int& hit) {
+            int h, b, c;
+            item_hbc(it, h, b, c);
+            const int64_t bh = (int64_t)b * p.H_kv + h;
+            const int jsel = c * kRows + slot;
+            const bool valid = jsel < p.S_eff;
+            tok = valid ? __ldg(p.sel + bh * p.S_eff + jsel) : -1;
+            hit = (valid && p.hit) ? __ldg(p.hit + bh * p.S_eff + jsel) : -1;
+        };
+        auto fetch_logits = [&](int it, int& tok, float (&sv)[SV]) {
+            int h, b, c;
+            item_hbc(it, h, b, c);
+            if (tok >= p.T) tok = p.T - 1;   // the selection is always in range; keep the invariant explicit
+#pragma unroll
+            for (int u = 0; u < SV; ++u) {
+                const int jq = jh + 2 * u;
+                sv[u] = (jq < G && tok >= 0) ? __ldg(p.sall + ((int64_t)b * p.H_q + h * G + jq) * p.T + tok) : -INFINITY;
+            }
+        };
+        // merge of (b, h) by the CTA that finished its last chunk: the records of its chunks, read through L2
+        auto merge = [&](int h, int b) {
+            const int64_t bh = (int64_t)b * p.H_kv + h;
+            __threadfence();
+            const float* P0 = p.partial + ((int64_t)b * p.H_q + h * G) * qstride;
+            if (et < G) {
+                const float* Pq = P0 + et * qstride;
+                float mx = -INFINITY;
+                for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
+                    float mc[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) mc[u] = c0 + u < p.n_chunks ? __ldcg(Pq + (c0 + u) * rw + 128) : -INFINITY;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) mx = fmaxf(mx, mc[u]);
+                }
+                float l = 0.0f;
+                for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
+                    float mc[8], lc[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const bool in = c0 + u < p.n_chunks;
+                        mc[u] = in ? __ldcg(Pq + (c0 + u) * rw + 128) : -INFINITY;
+                        lc[u] = in ? __ldcg(Pq + (c0 + u) * rw + 129) : 0.0f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (c0 + u >= p.n_chunks) break;
+                        const float w = mc[u] == -INFINITY ? 0.0f : __expf(mc[u] - mx);
+                        Wc[et * kMaxMergeChunks + c0 + u] = w;
+                        l = fmaf(w, lc[u], l);
+                    }
+                }
+                ML[et * 2] = mx;
+                ML[et * 2 + 1] = l;
+            }
+            named_bar_sync(1, kEpi);
+            for (int e = et; e < G * 128; e += kEpi) {
+                const int jq = e >> 7, i = e & 127;
+                const float* Pq = P0 + jq * qstride + i;
+                float a = 0.0f;
+                for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = c0 + u < p.n_chunks ? __ldcg(Pq + (c0 + u) * rw) : 0.0f;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (c0 + u < p.n_chunks) a = fmaf(Wc[jq * kMaxMergeChunks + c0 + u], v[u], a);
+                }
+                const float L = ML[jq * 2 + 1];
+                p.out[((int64_t)b * p.H_q + h * G + jq) * 128 + i] = L > 0.0f ? a / L : 0.0f;
+            }
+            if (p.lse && et < G) {
+                const float L = ML[et * 2 + 1];
+                p.lse[(int64_t)b * p.H_q + h * G + et] = L > 0.0f ? ML[et * 2] + logf(L) : -INFINITY;
+            }
+            if (et == 0) p.cnt[bh] = 0;
+            named_bar_sync(1, kEpi);   // Wc and ML are free again
+        };
+        // the ticket of item jp (taken by the helper lane): merge its (b, h) when this CTA finished it last
+        auto settle = [&](int jp) {
+            const bool ok = mbar_wait_lim(&tick[jp & 1], (jp >> 1) & 1, abort_flag, p.wait_cycles);
+            if (ok && last_flag[jp & 1]) {
+                int h, b, c;
+                item_hbc(it_begin + jp, h, b, c);
+                merge(h, b);
+            }
+        };
+
+        // w2 rows of this thread (output feature i_out, hidden units [jh M/2, (jh+1) M/2)), held in registers while
+        // the items' kv-head (and, with a predictor per sequence, sequence) stays; M = 128 only (else they are
+        // loaded per item)
+        constexpr bool kW2Reg = (M == 128);
+        uint4 w2r[kW2Reg ? 8 : 1];
+        int w2_key = -1;
+        int nx_tok = -1, nx_hit = -1;
+        float nx_sv[SV];
+        if (n_local > 0) {
+            fetch_sel(it_begin, nx_tok, nx_hit);
+            fetch_logits(it_begin, nx_tok, nx_sv);
+        }
         for (int j = 0; j < n_local; ++j) {
             int h, b, chunk;
             item_hbc(it_begin + j, h, b, chunk);
             const int64_t bh = (int64_t)b * p.H_kv + h;
             const int64_t bias_bh = p.mlp_stride ? bh : h;
-            const int jsel = chunk * kRows + slot;
-            const bool valid = jsel < p.S_eff;
-            int tok = valid ? __ldg(p.sel + bh * p.S_eff + jsel) : -1;
-            if (tok >= p.T) tok = p.T - 1;   // the selection is always in range; keep the invariant explicit
-            const int my_hit = (valid && p.hit) ? __ldg(p.hit + bh * p.S_eff + jsel) : -1;
-            // scaled logits of this slot for q-heads jq = jh, jh + 2, ...
-            float sv[(G + 1) / 2];
+            const int tok = nx_tok, my_hit = nx_hit;
+            float sv[SV];
 #pragma unroll
-            for (int u = 0; u < (G + 1) / 2; ++u) {
-                const int jq = jh + 2 * u;
-                sv[u] = (jq < G && valid) ? __ldg(p.sall + ((int64_t)b * p.H_q + h * G + jq) * p.T + tok) : -INFINITY;
+            for (int u = 0; u < SV; ++u) sv[u] = nx_sv[u];
+            (void)tok;
+            if (j + 1 < n_local) fetch_sel(it_begin + j + 1, nx_tok, nx_hit);
+            const __nv_bfloat16* w2row = p.w2 + b * p.mlp_stride + ((int64_t)h * 128 + i_out) * M + jh * (M / 2);
+            if (kW2Reg) {
+                const int key = p.mlp_stride ? (int)bh : h;
+                if (key != w2_key) {
+                    w2_key = key;
+#pragma unroll
+                    for (int u = 0; u < (kW2Reg ? 8 : 1); ++u) w2r[u] = __ldg(reinterpret_cast<const uint4*>(w2row) + u);
+                }
             }
-            named_bar_sync(1, kEpi);   // the previous item's readers of Ps, RZ, the hits and the reductions are done
+            named_bar_sync(1, kEpi);   // the previous item's readers of Ps, Z, X, the hits and the reductions are done
 #pragma unroll
-            for (int u = 0; u < (G + 1) / 2; ++u) {
+            for (int u = 0; u < SV; ++u) {
                 const int jq = jh + 2 * u;
                 const float mx = warp_max(sv[u]);
                 if (lane == 0 && jq < G) redM[sq * 8 + jq] = mx;
@@ -381,7 +509,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
             if (jh == 0 && lane == 0) hcount[sq] = __popc(hb);
             named_bar_sync(1, kEpi);
 #pragma unroll
-            for (int u = 0; u < (G + 1) / 2; ++u) {
+            for (int u = 0; u < SV; ++u) {
                 const int jq = jh + 2 * u;
                 if (jq < G) {
                     const float mq = chunk_max(jq);
@@ -407,30 +535,32 @@ __global__ void __launch_bounds__(kVThreads, 1)
             }
             named_bar_sync(1, kEpi);
 
-            // weighted residual rows: feature i_out, hits k = jh, jh + 2, ... (8 independent loads in flight); the
-            // sums wait in shared memory while the hidden units take the registers
-            {
-                float rz[G];
+            // residual rows of the first 16 hits (feature i_out, hits k = jh, jh + 2, ...): loads issued now, their
+            // bits converted after the hidden units, so they land while the accumulator is read (one branch on the
+            // storage type around all eight loads: no conversion, hence no wait, between them)
+            uint32_t rr[8];
+            const int64_t rbase = bh * p.n_res;
+            if (p.res.dtype == LOWRAM_BF16) {
+                const unsigned short* rv16 = reinterpret_cast<const unsigned short*>(p.res.val);
 #pragma unroll
-                for (int jq = 0; jq < G; ++jq) rz[jq] = 0.0f;
-                for (int k0 = jh; k0 < n_hit; k0 += 16) {
-                    float v[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int k = k0 + 2 * u;
-                        v[u] = k < n_hit ? p.res.get(bh * p.n_res + HitRow[k], i_out) : 0.0f;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int k = k0 + 2 * u;
-                        if (k >= n_hit) break;
-                        const int t = HitSlot[k];
-#pragma unroll
-                        for (int jq = 0; jq < G; ++jq) rz[jq] = fmaf(Ps[jq * kRows + t], v[u], rz[jq]);
-                    }
+                for (int u = 0; u < 8; ++u) {
+                    const int k = jh + 2 * u;
+                    rr[u] = k < n_hit ? (uint32_t)rv16[(rbase + HitRow[k]) * 128 + i_out] : 0u;
                 }
+            } else if (p.res.dtype == LOWRAM_INT8_VEC) {   // the rows' scales are read with the conversion
+                const signed char* rv8 = reinterpret_cast<const signed char*>(p.res.val);
 #pragma unroll
-                for (int jq = 0; jq < G; ++jq) RZ[(jh * 8 + jq) * kRows + i_out] = rz[jq];
+                for (int u = 0; u < 8; ++u) {
+                    const int k = jh + 2 * u;
+                    rr[u] = k < n_hit ? (uint32_t)(int)rv8[(rbase + HitRow[k]) * 128 + i_out] : 0u;
+                }
+            } else {
+                const uint32_t* rv32 = reinterpret_cast<const uint32_t*>(p.res.val);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int k = jh + 2 * u;
+                    rr[u] = k < n_hit ? rv32[(rbase + HitRow[k]) * 128 + i_out] : 0u;
+                }
             }
 
             // hidden units: thread = hidden unit jj of each 128-block, tokens of half ch;
@@ -448,12 +578,13 @@ __global__ void __launch_bounds__(kVThreads, 1)
 #pragma unroll
                     for (int jq = 0; jq < G; ++jq) z[jq] = 0.0f;
 #pragma unroll 1
-                    for (int cg = 0; cg < 4; ++cg) {           // 16 token columns per TMEM read
-                        float xv[2][8];
-                        tmem_ld_2x8(taddr + cg * 16, taddr + cg * 16 + 8, xv[0], xv[1]);
+                    for (int cg = 0; cg < 4; cg += 2) {        // 32 token columns per TMEM wait
+                        float xv[4][8];
+                        tmem_ld_4x8(taddr + cg * 16, taddr + cg * 16 + 8, taddr + cg * 16 + 16, taddr + cg * 16 + 24,
+                                    xv[0], xv[1], xv[2], xv[3]);
                         const float* pc = Ps + ch * 64 + cg * 16;
 #pragma unroll
-                        for (int g8 = 0; g8 < 2; ++g8) {
+                        for (int g8 = 0; g8 < 4; ++g8) {
 #pragma unroll
                             for (int t4 = 0; t4 < 8; t4 += 4) {
                                 float hv[4];
@@ -471,41 +602,88 @@ __global__ void __launch_bounds__(kVThreads, 1)
                         }
                     }
 #pragma unroll
-                    for (int jq = 0; jq < G; ++jq) Z[(ch * 8 + jq) * M + jj] = z[jq];
+                    for (int jq = 0; jq < G; ++jq) Z[(ch * G + jq) * M + jj] = z[jq];
                 }
             }
             fence_before();
             mbar_arrive(&t_empty[buf]);   // the accumulator is read: the MMAs of item j + 2 may use it
-            named_bar_sync(1, kEpi);
+            if (j + 1 < n_local) fetch_logits(it_begin + j + 1, nx_tok, nx_sv);
 
-            // second layer on the chunk's hidden sums: thread (i_out, jh) takes hidden units [jh M/2, (jh+1) M/2)
+            // weighted residual rows, then the second layer on the chunk's hidden sums
             float acc[G];
 #pragma unroll
-            for (int jq = 0; jq < G; ++jq) acc[jq] = RZ[(jh * 8 + jq) * kRows + i_out];
+            for (int jq = 0; jq < G; ++jq) acc[jq] = 0.0f;
+            float rv[8];
+            if (p.res.dtype == LOWRAM_INT8_VEC) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int k = jh + 2 * u;
+                    rv[u] = k < n_hit ? (float)(int)rr[u] * __half2float(p.res.scale[rbase + HitRow[k]]) : 0.0f;
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    rv[u] = p.res.dtype == LOWRAM_BF16 ? __uint_as_float(rr[u] << 16) : __uint_as_float(rr[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int k = jh + 2 * u;
+                if (k < n_hit) {
+                    const int t = HitSlot[k];
+#pragma unroll
+                    for (int jq = 0; jq < G; ++jq) acc[jq] = fmaf(Ps[jq * kRows + t], rv[u], acc[jq]);
+                }
+            }
+            for (int k0 = jh + 16; k0 < n_hit; k0 += 16) {    // more than 16 hits in the chunk
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int k = k0 + 2 * u;
+                    v[u] = k < n_hit ? p.res.get(bh * p.n_res + HitRow[k], i_out) : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int k = k0 + 2 * u;
+                    if (k >= n_hit) break;
+                    const int t = HitSlot[k];
+#pragma unroll
+                    for (int jq = 0; jq < G; ++jq) acc[jq] = fmaf(Ps[jq * kRows + t], v[u], acc[jq]);
+                }
+            }
+            named_bar_sync(1, kEpi);   // every hidden sum is in Z
             if (have) {
-                constexpr int kW2 = 4;                                 // 16-byte pieces of the w2 row per batch
-                const uint4* w2src = reinterpret_cast<const uint4*>(p.w2 + b * p.mlp_stride +
-                                                                    ((int64_t)h * 128 + i_out) * M + jh * (M / 2));
-#pragma unroll 1
-                for (int bt = 0; bt < (M / 2) / (8 * kW2); ++bt) {
-                    uint4 w2v[kW2];
+                // acc[jq] += sum over this thread's hidden units jj of w2[i_out, jj] (Z0[jq, jj] + Z1[jq, jj])
+                auto w2_step = [&](const uint4& wv, int j0) {
+                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&wv);
 #pragma unroll
-                    for (int u = 0; u < kW2; ++u) w2v[u] = __ldg(w2src + bt * kW2 + u);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const float w0 = bf_lo(wp[2 * hf]), w1v = bf_hi(wp[2 * hf]);
+                        const float w2v = bf_lo(wp[2 * hf + 1]), w3 = bf_hi(wp[2 * hf + 1]);
+                        const int jj = j0 + 4 * hf;
 #pragma unroll
-                    for (int u = 0; u < kW2; ++u) {
-                        const int j0 = jh * (M / 2) + 8 * kW2 * bt + 8 * u;
-                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(&w2v[u]);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float wa = bf_lo(wp[e]), wb = bf_hi(wp[e]);
-                            const int jj = j0 + 2 * e;
-#pragma unroll
-                            for (int jq = 0; jq < G; ++jq) {
-                                const float za = Z[jq * M + jj] + Z[(8 + jq) * M + jj];
-                                const float zb = Z[jq * M + jj + 1] + Z[(8 + jq) * M + jj + 1];
-                                acc[jq] = fmaf(wa, za, fmaf(wb, zb, acc[jq]));
-                            }
+                        for (int jq = 0; jq < G; ++jq) {
+                            const float4 za = *reinterpret_cast<const float4*>(Z + jq * M + jj);
+                            const float4 zb = *reinterpret_cast<const float4*>(Z + (G + jq) * M + jj);
+                            acc[jq] = fmaf(w0, za.x + zb.x, acc[jq]);
+                            acc[jq] = fmaf(w1v, za.y + zb.y, acc[jq]);
+                            acc[jq] = fmaf(w2v, za.z + zb.z, acc[jq]);
+                            acc[jq] = fmaf(w3, za.w + zb.w, acc[jq]);
                         }
+                    }
+                };
+                if (kW2Reg) {
+#pragma unroll
+                    for (int u = 0; u < (kW2Reg ? 8 : 1); ++u) w2_step(w2r[u], jh * (M / 2) + 8 * u);
+                } else {
+                    constexpr int kW2 = 4;                             // 16-byte pieces of the w2 row per batch
+                    const uint4* w2src = reinterpret_cast<const uint4*>(w2row);
+#pragma unroll 1
+                    for (int bt = 0; bt < (M / 2) / (8 * kW2); ++bt) {
+                        uint4 w2v[kW2];
+#pragma unroll
+                        for (int u = 0; u < kW2; ++u) w2v[u] = __ldg(w2src + bt * kW2 + u);
+#pragma unroll
+                        for (int u = 0; u < kW2; ++u) w2_step(w2v[u], jh * (M / 2) + 8 * kW2 * bt + 8 * u);
                     }
                 }
             }
@@ -523,71 +701,15 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 rec[i_out * qstride + 128] = chunk_max(i_out);
                 rec[i_out * qstride + 129] = chunk_sum(i_out);
             }
-
-            // the CTA finishing a (b, h)'s last chunk merges its chunks' records (made visible device-wide first)
             if (p.cnt) {
-                __threadfence();
+                // the record is written: the helper lane takes this chunk's ticket while the next item starts;
+                // the ticket of the item before is settled here (merged if this CTA finished that (b, h))
                 named_bar_sync(1, kEpi);
-                if (et == 0) *last_flag = (atomicAdd(p.cnt + bh, 1) == p.n_chunks - 1) ? 1 : 0;
-                named_bar_sync(1, kEpi);
-                if (*last_flag) {
-                    __threadfence();
-                    const float* P0 = p.partial + ((int64_t)b * p.H_q + h * G) * qstride;
-                    if (et < G) {
-                        const float* Pq = P0 + et * qstride;
-                        float mx = -INFINITY;
-                        for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
-                            float mc[8];
-#pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                mc[u] = c0 + u < p.n_chunks ? __ldcg(Pq + (c0 + u) * rw + 128) : -INFINITY;
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) mx = fmaxf(mx, mc[u]);
-                        }
-                        float l = 0.0f;
-                        for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
-                            float mc[8], lc[8];
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const bool in = c0 + u < p.n_chunks;
-                                mc[u] = in ? __ldcg(Pq + (c0 + u) * rw + 128) : -INFINITY;
-                                lc[u] = in ? __ldcg(Pq + (c0 + u) * rw + 129) : 0.0f;
-                            }
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                if (c0 + u >= p.n_chunks) break;
-                                const float w = mc[u] == -INFINITY ? 0.0f : __expf(mc[u] - mx);
-                                Wc[et * kMaxMergeChunks + c0 + u] = w;
-                                l = fmaf(w, lc[u], l);
-                            }
-                        }
-                        ML[et * 2] = mx;
-                        ML[et * 2 + 1] = l;
-                    }
-                    named_bar_sync(1, kEpi);
-                    for (int e = et; e < G * 128; e += kEpi) {
-                        const int jq = e >> 7, i = e & 127;
-                        const float* Pq = P0 + jq * qstride + i;
-                        float a = 0.0f;
-                        for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
-                            float v[8];
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) v[u] = c0 + u < p.n_chunks ? __ldcg(Pq + (c0 + u) * rw) : 0.0f;
-#pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                if (c0 + u < p.n_chunks) a = fmaf(Wc[jq * kMaxMergeChunks + c0 + u], v[u], a);
-                        }
-                        const float L = ML[jq * 2 + 1];
-                        p.out[((int64_t)b * p.H_q + h * G + jq) * 128 + i] = L > 0.0f ? a / L : 0.0f;
-                    }
-                    if (p.lse && et < G) {
-                        const float L = ML[et * 2 + 1];
-                        p.lse[(int64_t)b * p.H_q + h * G + et] = L > 0.0f ? ML[et * 2] + logf(L) : -INFINITY;
-                    }
-                    if (et == 0) p.cnt[bh] = 0;
-                }
+                if (et == 0) mbar_arrive(&rec_done[j & 1]);
+                if (j > 0) settle(j - 1);
             }
         }
+        if (p.cnt && n_local > 0) settle(n_local - 1);
     }
 
     // ---------------------------------------------------------------------- teardown
@@ -603,7 +725,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
 }  // namespace
 
 bool tc_vregen_supported(const lowram_decode_shape& s) {
-    return tc_score_supported(s) && (s.m == 128 || s.m == 256) && s.d == 128 && vregen_config(s.m, s.r).NS >= 2;
+    return tc_score_supported(s) && (s.m == 128 || s.m == 256) && s.d == 128 && vregen_config(s.m, s.r, s.H_q / s.H_kv).NS >= 2;
 }
 
 int tc_partial_width(const lowram_decode_shape& s) { return s.d + 2; }
@@ -625,7 +747,7 @@ cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     p.n_chunks = a.n_chunks;
     p.n_res = s.n_res;
     p.KC = s.r / 64;
-    const VregenConfig cfg = vregen_config(s.m, s.r);
+    const VregenConfig cfg = vregen_config(s.m, s.r, s.H_q / s.H_kv);
     p.NS = cfg.NS;
     p.f_resident = cfg.f_resident ? 1 : 0;
     p.n_items = s.B * s.H_kv * a.n_chunks;

@@ -79,6 +79,9 @@ typedef enum {
 #define LOWRAM_CHECK_RES_INDEX 2u      /* a residual index was out of range or not strictly ascending */
 #define LOWRAM_CHECK_TIMEOUT 4u        /* a tensor-core pipeline wait gave up (internal error; results invalid) */
 #define LOWRAM_CHECK_NOT_PD 8u         /* lowram_fit_basis: an iterate lost rank (keys of rank < r); results invalid */
+#define LOWRAM_CHECK_LAYOUT 16u        /* a tensor-core kernel's shared-memory layout did not fit its launch's
+                                          allocation (internal error): the kernel returned at once, touching no
+                                          memory; results invalid */
 
 /* ---------------------------------------------------------------------------------------------
  * Decode: one layer, all B sequences.
@@ -143,8 +146,8 @@ LOWRAM_API lowram_status lowram_decode_uses_tensor_cores(const lowram_decode_sha
  *   w1         [H_kv, m, d] act_dtype;  b1 [H_kv, m] float32 or NULL
  *   w2         [H_kv, d, m] act_dtype;  b2 [H_kv, d] float32 or NULL; with mlp_batch_stride != 0, sequence
  *              b's w1 and w2 start mlp_batch_stride elements after b-1's, and b1, b2 are [B, H_kv, m], [B, H_kv, d]
- *              (a predictor fitted per prompt, LowRAM abstract: "fits a lightweight per-head predictor at test
- *              time")
+ *              (a predictor fitted per prompt: the LowRAM abstract fits the small per-head predictor at test
+ *              time)
  *   res_idx    [B, H_kv, n_res] int32, strictly ascending per (b, h), in [0, T)
  *   res_val    [B, H_kv, n_res, d] res_dtype
  *   res_scale  LOWRAM_INT8_VEC only: [B, H_kv, n_res] fp16; else NULL
@@ -241,7 +244,7 @@ LOWRAM_API lowram_status lowram_compress_workspace_size(const lowram_compress_sh
 
 /*
  * lowram_compress -- latent coefficients and worst-token residual lists of one layer group.
- * Steps (LowRAM abstract: "stores residuals only for the tokens it reconstructs worst"; "Value
+ * Steps (LowRAM abstract: residuals are kept only for the tokens the predictor rebuilds worst; "Value
  * cache amortisation in plain language": scores the per-token reconstruction error and keeps sparse
  * residuals for the worst predictions; "Step-by-step mental model", step 1; "Asymmetric key
  * compression with xKV"):

@@ -207,3 +207,13 @@ def test_batch_strides_are_checked_and_size_the_workspace():
         assert own - shared >= 7 * 8 * 128 * 512 * 2
     else:
         assert own == shared
+
+
+def test_check_word_bits_match_the_header():
+    import re
+    import decode_attention_19_b300 as L
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lowram.h")).read()
+    bits = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define LOWRAM_CHECK_(\w+) (\d+)u", hdr)}
+    assert bits == {"POS_RANGE": 1, "RES_INDEX": 2, "TIMEOUT": 4, "NOT_PD": 8, "LAYOUT": 16}
+    for name, v in bits.items():
+        assert getattr(L, "CHECK_" + name) == v

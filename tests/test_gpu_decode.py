@@ -136,6 +136,31 @@ def test_decode_exact_ties_take_the_lower_index():
         assert kept == list(range(10, 10 + len(kept)))
 
 
+def test_decode_ties_across_the_cluster_split():
+    # a row long enough to be split over a cluster of two CTAs (8192 keys each, the second partly filled), a
+    # block of equal keys straddling the split, and S chosen so that kv-head 0's cut falls inside the block
+    w = SMALL["llama8b_small"].with_(B=1, T=12000, S=100)
+    c = C.decode_case(w)
+    t0, t1 = 8180, 8206
+    coef = c["coef"].clone()
+    coef[0, t0 + 1:t1] = coef[0, t0]
+    c["coef"] = coef
+    c["coef_vals"] = O.f64(coef)
+    pos = torch.arange(w.T, dtype=torch.int32)[None].clone()
+    pos[0, t0 + 1:t1] = t0
+    c["pos"] = pos
+    probe = C.run_gpu_decode(c)
+    k0 = probe["key"][0, 0]
+    assert np.all(k0[t0:t1] == k0[t0])
+    S = int((k0 > k0[t0]).sum()) + 20
+    gpu = C.run_gpu_decode(c, S=S)
+    orc = C.run_oracle_decode(c, S=S)
+    C.check_decode(gpu, orc, S)
+    kept = [int(t) for t in gpu["sel"][0, 0] if t0 <= t < t1]
+    assert kept == list(range(t0, t0 + 20))
+    assert np.all(np.diff(gpu["sel"][0], axis=-1) > 0)
+
+
 def test_decode_empty_batch_and_empty_cache():
     import decode_attention_19_b300 as L
     w = SMALL["llama8b_small"].with_(T=0, S=10, rho=0.0)
