@@ -48,15 +48,6 @@ __host__ __device__ int fold_blocks(const FoldArgs& f) {
     return f.F ? f.copies * f.H_kv * (int)cdiv(f.m, kFoldJ) * (int)cdiv(f.r, kFoldK) : 0;
 }
 
-__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 __device__ void fold_block(const FoldArgs& f, int blk, uint8_t* smem) {
     const int kb = (int)cdiv(f.r, kFoldK), jb = (int)cdiv(f.m, kFoldJ);
     const int per_copy = f.H_kv * jb * kb;
@@ -109,7 +100,7 @@ __device__ void fold_block(const FoldArgs& f, int blk, uint8_t* smem) {
             const uint16_t* br = Bs + (ks + 2 * tq) * SB + kw + 8 * nt + g;
             const uint32_t b0 = pair(br[0], br[SB]);
             const uint32_t b1 = pair(br[8 * SB], br[9 * SB]);
-            mma_16816(acc[nt], a0, a1, a2, a3, b0, b1);
+            tc::mma_16816(acc[nt], a0, a1, a2, a3, b0, b1);
         }
     }
     // C fragment: rows jw + g (+8), columns kw + 8nt + 2tq (+1); stored bf16, or fp16 for an int4 cache's fp16 path

@@ -80,12 +80,18 @@ struct VregenTcParams {
     uint32_t* check;
 };
 
+// The second layer's operand: the chunk's hidden sums as bf16 hi + lo columns, 2g of them in n-tiles of 8.
+__host__ __device__ constexpr int w2_ntiles(int g) { return (2 * g + 7) / 8; }
+constexpr int kWoStride = 132;           // floats per row of the second layer's output (conflict-free stores)
+
 // Epilogue scratch beside the ring, for g q-heads per kv-head: softmax weights [g][128], hidden sums [2][g][m],
-// the upper half's value sums [g][128], merge weights [g][64] and (W, L) [8][2], compacted hits (rows, slots),
-// reductions [2][32] + counts [4], then the barriers and the TMEM slot / flags.
+// the upper half's residual sums [g][128], the second layer's output [8 nt][132] and operand [8 nt][m + 8] bf16,
+// merge weights [g][64] and (W, L) [8][2], compacted hits (rows, slots), reductions [2][32] + counts [4], then
+// the barriers and the TMEM slot / flags.
 size_t scratch_bytes(int m, int g) {
-    return (size_t)4 * (g * kRows + 2 * g * m + g * kRows + g * kMaxMergeChunks + 16 + 2 * kRows + 64 + 4) + 8 +
-           8 * (3 * kMaxStages + 2 + 4 + 1 + 4) + 32;
+    const int nt = w2_ntiles(g);
+    return (size_t)4 * (g * kRows + 2 * g * m + g * kRows + nt * 8 * kWoStride) + (size_t)2 * nt * 8 * (m + 8) +
+           (size_t)4 * (g * kMaxMergeChunks + 16 + 2 * kRows + 64 + 4) + 8 + 8 * (3 * kMaxStages + 2 + 4 + 1 + 4) + 32;
 }
 
 struct VregenConfig {
@@ -111,8 +117,16 @@ VregenConfig vregen_config(int m, int r, int g) {
     return c;
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+// SiLU(x) = x sigmoid(x), with sigmoid(x) = (1 + tanh(x / 2)) / 2 and tanh from the hardware approximation
+// (tanh.approx.f32, relative error about 2^-11): one special-function operation per unit instead of an exponential
+// and a reciprocal.  The error it adds is far below the bf16 rounding of the folded weights.
+__device__ __forceinline__ float silu_tanh(float x) {
+    const float h = 0.5f * x;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
+
 
 // cp.async.wait_group with a run-time count of groups allowed to stay pending (at most kMaxStages - 1)
 __device__ __forceinline__ void cp_async_wait_pending(int n) {
@@ -143,8 +157,11 @@ __global__ void __launch_bounds__(kVThreads, 1)
     uint8_t* ring = smem + (fres ? (size_t)KC * kFChunk : 0);    // NS stages: C chunk [128 x 64] (+ F chunk)
     float* Ps = (float*)(ring + (size_t)NS * kStage);            // [G][128] softmax weights (0 on padding slots)
     float* Z = Ps + G * kRows;                                   // [2 token halves][G][M] hidden sums
-    float* X = Z + 2 * G * M;                                    // [G][128] the upper half's value sums
-    float* Wc = X + G * kRows;                                   // [G][n_chunks] merge weights
+    float* X = Z + 2 * G * M;                                    // [G][128] the upper half's residual sums
+    constexpr int NT = w2_ntiles(G);
+    float* Wo = X + G * kRows;                                   // [8 NT][132] second layer: rows n, features i
+    __nv_bfloat16* Zs = reinterpret_cast<__nv_bfloat16*>(Wo + NT * 8 * kWoStride);   // [8 NT][M + 8] its operand
+    float* Wc = reinterpret_cast<float*>(Zs + NT * 8 * (M + 8)); // [G][n_chunks] merge weights
     float* ML = Wc + G * kMaxMergeChunks;                        // [G][2] W and L of the merge (16 floats)
     int* HitRow = (int*)(ML + 16);                               // compacted residual rows of the chunk's slots
     int* HitSlot = HitRow + kRows;                               // ... and those slots, ascending
@@ -322,22 +339,46 @@ __global__ void __launch_bounds__(kVThreads, 1)
         const uint32_t total = (uint32_t)n_local * KC;
         uint32_t issued = 0, published = 0;
         const __nv_bfloat16* srow[kGatRows];
+        int nsel[kGatRows];   // the next item's selected tokens, loaded an item ahead
+        auto load_sel = [&](int jl) {
+            int h, b, c;
+            item_hbc(it_begin + jl, h, b, c);
+            const int64_t bh = (int64_t)b * p.H_kv + h;
+#pragma unroll
+            for (int rr = 0; rr < kGatRows; ++rr) {
+                const int jr = c * kRows + rr * (kGat / 8) + rsub;
+                nsel[rr] = jr < p.S_eff ? __ldg(p.sel + bh * p.S_eff + jr) : 0;
+            }
+        };
+        if (n_local > 0) load_sel(0);
         bool gok = true;
+        // the oldest stage in flight has landed: make it visible to the tensor cores and publish it
+        auto publish = [&]() {
+            cp_async_wait_pending((int)(issued - published) - 1);
+            fence_proxy_async();
+            if (gok) mbar_arrive(&fullC[published % NS]);
+            ++published;
+        };
         while (published < total) {
             if (gok && issued < total && issued - published < (uint32_t)NS) {
                 const uint32_t s = issued % NS, n = issued / NS;
+                // the slot frees when the MMAs of its previous round are done; until then publish what has landed
+                // (a stage waiting behind this slot must not hold up the MMAs that would free it)
+                if (n > 0 && published < issued && !mbar_test_wait(&empty[s], (n & 1) ^ 1)) {
+                    publish();
+                    continue;
+                }
                 const int kc = (int)(issued % KC);
-                if (kc == 0) {   // the item's rows
+                if (kc == 0) {   // the item's rows; then the next item's tokens
+                    const int jl = (int)(issued / KC);
                     int h, b, c;
-                    item_hbc(it_begin + (int)(issued / KC), h, b, c);
-                    const int64_t bh = (int64_t)b * p.H_kv + h;
+                    item_hbc(it_begin + jl, h, b, c);
 #pragma unroll
                     for (int rr = 0; rr < kGatRows; ++rr) {
-                        const int jr = c * kRows + rr * (kGat / 8) + rsub;
-                        int t = jr < p.S_eff ? __ldg(p.sel + bh * p.S_eff + jr) : 0;
-                        t = min(max(t, 0), p.T - 1);
+                        const int t = min(max(nsel[rr], 0), p.T - 1);
                         srow[rr] = p.coef + ((int64_t)b * p.T + t) * p.r + c16 * 8;
                     }
+                    if (jl + 1 < n_local) load_sel(jl + 1);
                 }
                 if (!mbar_wait_lim(&empty[s], (n & 1) ^ 1, abort_flag, p.wait_cycles)) {
                     gok = false;
@@ -352,11 +393,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 cp_async_commit();
                 ++issued;
             } else if (published < issued) {
-                // the oldest stage in flight has landed: make it visible to the tensor cores and publish it
-                cp_async_wait_pending((int)(issued - published) - 1);
-                fence_proxy_async();
-                if (gok) mbar_arrive(&fullC[published % NS]);
-                ++published;
+                publish();
             } else {
                 break;   // aborted with nothing in flight
             }
@@ -466,11 +503,23 @@ __global__ void __launch_bounds__(kVThreads, 1)
             }
         };
 
-        // w2 rows of this thread (output feature i_out, hidden units [jh M/2, (jh+1) M/2)), held in registers while
-        // the items' kv-head (and, with a predictor per sequence, sequence) stays; M = 128 only (else they are
-        // loaded per item)
-        constexpr bool kW2Reg = (M == 128);
-        uint4 w2r[kW2Reg ? 8 : 1];
+        // The second layer on warp MMAs: warp ew = warp - 4 makes output features [16 ew, 16 ew + 16) of every
+        // q-head, W[i][n] = sum_k w2[i][k] Zs[n][k], from its w2 rows in m16n8k16 A fragments.  With M = 128 the
+        // fragments stay in registers while the items' kv-head (and, with a predictor per sequence, sequence)
+        // stays; with M = 256 they are loaded per item.
+        constexpr int KB = M / 16;
+        const int ew = warp - 4, fg = lane >> 2, ft = lane & 3;
+        uint32_t af[KB][4];
+        auto load_af = [&](int h, int b) {
+            const __nv_bfloat16* w = p.w2 + b * p.mlp_stride + ((int64_t)h * 128 + 16 * ew + fg) * M + 2 * ft;
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) {
+                af[kb][0] = __ldg(reinterpret_cast<const uint32_t*>(w + kb * 16));
+                af[kb][1] = __ldg(reinterpret_cast<const uint32_t*>(w + 8 * M + kb * 16));
+                af[kb][2] = __ldg(reinterpret_cast<const uint32_t*>(w + kb * 16 + 8));
+                af[kb][3] = __ldg(reinterpret_cast<const uint32_t*>(w + 8 * M + kb * 16 + 8));
+            }
+        };
         int w2_key = -1;
         int nx_tok = -1, nx_hit = -1;
         float nx_sv[SV];
@@ -489,13 +538,11 @@ __global__ void __launch_bounds__(kVThreads, 1)
             for (int u = 0; u < SV; ++u) sv[u] = nx_sv[u];
             (void)tok;
             if (j + 1 < n_local) fetch_sel(it_begin + j + 1, nx_tok, nx_hit);
-            const __nv_bfloat16* w2row = p.w2 + b * p.mlp_stride + ((int64_t)h * 128 + i_out) * M + jh * (M / 2);
-            if (kW2Reg) {
+            if (M == 128) {
                 const int key = p.mlp_stride ? (int)bh : h;
                 if (key != w2_key) {
                     w2_key = key;
-#pragma unroll
-                    for (int u = 0; u < (kW2Reg ? 8 : 1); ++u) w2r[u] = __ldg(reinterpret_cast<const uint4*>(w2row) + u);
+                    load_af(h, b);
                 }
             }
             named_bar_sync(1, kEpi);   // the previous item's readers of Ps, Z, X, the hits and the reductions are done
@@ -589,7 +636,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
                             for (int t4 = 0; t4 < 8; t4 += 4) {
                                 float hv[4];
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) hv[u] = silu_fast(xv[g8][t4 + u] + bj);
+                                for (int u = 0; u < 4; ++u) hv[u] = silu_tanh(xv[g8][t4 + u] + bj);
 #pragma unroll
                                 for (int jq = 0; jq < G; ++jq) {
                                     const float4 pw = *reinterpret_cast<const float4*>(pc + jq * kRows + g8 * 8 + t4);
@@ -651,40 +698,45 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 }
             }
             named_bar_sync(1, kEpi);   // every hidden sum is in Z
+            if (M != 128) load_af(h, b);
             if (have) {
-                // acc[jq] += sum over this thread's hidden units jj of w2[i_out, jj] (Z0[jq, jj] + Z1[jq, jj])
-                auto w2_step = [&](const uint4& wv, int j0) {
-                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&wv);
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const float w0 = bf_lo(wp[2 * hf]), w1v = bf_hi(wp[2 * hf]);
-                        const float w2v = bf_lo(wp[2 * hf + 1]), w3 = bf_hi(wp[2 * hf + 1]);
-                        const int jj = j0 + 4 * hf;
-#pragma unroll
-                        for (int jq = 0; jq < G; ++jq) {
-                            const float4 za = *reinterpret_cast<const float4*>(Z + jq * M + jj);
-                            const float4 zb = *reinterpret_cast<const float4*>(Z + (G + jq) * M + jj);
-                            acc[jq] = fmaf(w0, za.x + zb.x, acc[jq]);
-                            acc[jq] = fmaf(w1v, za.y + zb.y, acc[jq]);
-                            acc[jq] = fmaf(w2v, za.z + zb.z, acc[jq]);
-                            acc[jq] = fmaf(w3, za.w + zb.w, acc[jq]);
+                // the hidden sums, both token halves added, as bf16 hi + lo: Zs[n][k] = hi(z[n][k]) for n < G,
+                // lo(z[n - G][k]) = bf16(z - hi) for G <= n < 2G (hi + lo holds z to 2^-16), 0 beyond
+                for (int e = et; e < NT * 8 * (M / 2); e += kEpi) {
+                    const int n = e / (M / 2), k = (e - n * (M / 2)) * 2;
+                    uint32_t packed = 0u;
+                    if (n < 2 * G) {
+                        const int jq = n < G ? n : n - G;
+                        const float2 za = *reinterpret_cast<const float2*>(Z + jq * M + k);
+                        const float2 zb = *reinterpret_cast<const float2*>(Z + (G + jq) * M + k);
+                        const float z0 = za.x + zb.x, z1 = za.y + zb.y;
+                        __nv_bfloat162 v = __floats2bfloat162_rn(z0, z1);
+                        if (n >= G) {
+                            const float2 hf = __bfloat1622float2(v);
+                            v = __floats2bfloat162_rn(z0 - hf.x, z1 - hf.y);
                         }
+                        packed = *reinterpret_cast<const uint32_t*>(&v);
                     }
-                };
-                if (kW2Reg) {
+                    *reinterpret_cast<uint32_t*>(Zs + n * (M + 8) + k) = packed;
+                }
+            }
+            named_bar_sync(1, kEpi);
+            if (have) {
 #pragma unroll
-                    for (int u = 0; u < (kW2Reg ? 8 : 1); ++u) w2_step(w2r[u], jh * (M / 2) + 8 * u);
-                } else {
-                    constexpr int kW2 = 4;                             // 16-byte pieces of the w2 row per batch
-                    const uint4* w2src = reinterpret_cast<const uint4*>(w2row);
-#pragma unroll 1
-                    for (int bt = 0; bt < (M / 2) / (8 * kW2); ++bt) {
-                        uint4 w2v[kW2];
+                for (int nt = 0; nt < NT; ++nt) {
+                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    const __nv_bfloat16* zr = Zs + (nt * 8 + fg) * (M + 8) + 2 * ft;
 #pragma unroll
-                        for (int u = 0; u < kW2; ++u) w2v[u] = __ldg(w2src + bt * kW2 + u);
-#pragma unroll
-                        for (int u = 0; u < kW2; ++u) w2_step(w2v[u], jh * (M / 2) + 8 * kW2 * bt + 8 * u);
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(zr + kb * 16);
+                        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(zr + kb * 16 + 8);
+                        mma_16816(d, af[kb][0], af[kb][1], af[kb][2], af[kb][3], b0, b1);
                     }
+                    float* wo = Wo + (nt * 8 + 2 * ft) * kWoStride + 16 * ew + fg;
+                    wo[0] = d[0];
+                    wo[kWoStride] = d[1];
+                    wo[8] = d[2];
+                    wo[kWoStride + 8] = d[3];
                 }
             }
             if (jh == 1)
@@ -696,7 +748,9 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 const float bias = p.b2 ? __ldg(p.b2 + bias_bh * 128 + i_out) : 0.0f;
 #pragma unroll
                 for (int jq = 0; jq < G; ++jq)
-                    rec[jq * qstride + i_out] = acc[jq] + X[jq * kRows + i_out] + chunk_sum(jq) * bias;
+                    rec[jq * qstride + i_out] = (acc[jq] + X[jq * kRows + i_out]) +
+                                                (Wo[jq * kWoStride + i_out] + Wo[(G + jq) * kWoStride + i_out]) +
+                                                chunk_sum(jq) * bias;
             } else if (i_out < G) {
                 rec[i_out * qstride + 128] = chunk_max(i_out);
                 rec[i_out * qstride + 129] = chunk_sum(i_out);
