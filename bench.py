@@ -607,7 +607,7 @@ def main():
                 "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = "score (selection keys of every token)"
-    traffic = profiled_traffic("score_llama8b.txt", src) if w.name == "llama8b" else None
+    traffic = profiled_traffic("score_tc_llama8b.md", src) if w.name == "llama8b" else None
     roof["traffic"] = traffic
     t_bytes_us = bytes_call / (pk["hbm_gbs"] * 1e9) * 1e6
     # a decode call lasts ~0.1 ms between L2 flushes: the burst bf16 peak applies (the sustained one is also given)
