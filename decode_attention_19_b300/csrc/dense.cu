@@ -197,18 +197,18 @@ __global__ void __launch_bounds__(kDenseThreads) dense_kernel(int T, int Ts, int
 }
 
 // ------------------------------------------------------------------------------------------------
-// bf16, d = 128.  A CTA of four warps per (kv-head, token range, sequence); each warp streams blocks of 16 tokens of
-// K and V through its own two-stage cp.async ring in shared memory (16 KB per warp) and keeps an online softmax
-// per q-head:
+// bf16, d = 128.  Each warp streams blocks of 16 tokens of K and V through its own cp.async ring in shared memory
+// and keeps an online softmax per q-head:
 //   scores   eight lanes per token, 16 features each, four tokens per pass: the K row slices (read back swizzled)
 //            against the q-heads held in registers (pre-scaled fp32 pairs), packed fp32x2 FMAs, three shuffles
 //            to add;
 //   weights  block max and sum by shuffles, one exp per (token, q-head);
 //   values   lane = 4 features: each token's V row (8 bytes per lane) times its weight, broadcast by shuffle.
 // Only K and V pass through shared memory (the queries never do), so its traffic is twice the bytes streamed.
-// The CTA's warps merge their states in shared memory and write one partial record per (sequence, q-head).
-// Up to four q-heads per kv-head; more (whose queries would not fit in registers) take dense_bf16_smemq_kernel,
-// which reads the pre-scaled queries from shared memory, two lanes per token.
+// Up to four q-heads per kv-head: dense_bf16_pw_kernel (persistent, one record per warp and work item).  More
+// q-heads (whose queries would not fit in registers) take dense_bf16_smemq_kernel: a CTA of four warps per
+// (kv-head, token range, sequence), two ring stages per warp, the pre-scaled queries in shared memory read by two
+// lanes per token, and the warps' states merged in shared memory into one record per (sequence, q-head).
 // ------------------------------------------------------------------------------------------------
 constexpr int kD2Warps = 4;
 constexpr int kD2Threads = 32 * kD2Warps;
@@ -297,109 +297,133 @@ __device__ __forceinline__ void dense_block_heads(const uint8_t* Kt, const uint8
     }
 }
 
+// Persistent variant for up to four q-heads per kv-head: one CTA of 8 warps per SM, and every warp an independent
+// stream over its own work items (a sequence, a kv-head and a token split each; items gw, gw + warps, ...), with
+// a 3-stage ring of 16-token K/V blocks running across item boundaries, so two blocks (16 KB) per warp, 128 KB per
+// SM, are in flight whenever the warp computes.  A warp writes one flash-decoding record per item: no CTA-wide
+// merge, no barrier.
+constexpr int kPwWarps = 8, kPwStages = 3;
+constexpr size_t kPwSmem = (size_t)kPwWarps * kPwStages * 2 * kD2Stage;
+
 template <int G>
-__global__ void __launch_bounds__(kD2Threads) dense_bf16_kernel(int T, int Ts, int H_q, int H_kv, float scale,
-                                                                const __nv_bfloat16* __restrict__ q,
-                                                                const __nv_bfloat16* __restrict__ K,
-                                                                const __nv_bfloat16* __restrict__ V,
-                                                                float* __restrict__ partial, int n_split) {
+__global__ void __launch_bounds__(32 * kPwWarps, 1) dense_bf16_pw_kernel(int B, int T, int Ts, int H_q, int H_kv,
+                                                                         float scale, const __nv_bfloat16* __restrict__ q,
+                                                                         const __nv_bfloat16* __restrict__ K,
+                                                                         const __nv_bfloat16* __restrict__ V,
+                                                                         float* __restrict__ partial, int n_split) {
     using namespace tc;
     extern __shared__ __align__(16) uint8_t dsm[];
-    const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int tg = lane >> 3, fo = lane & 7;            // scores: token tg of a pass, features 16 fo .. 16 fo + 15
-    uint8_t* wbase = dsm + warp * 4 * kD2Stage;         // Kt[2], Vt[2]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tg = lane >> 3, fo = lane & 7;
+    uint8_t* wbase = dsm + (size_t)warp * kPwStages * 2 * kD2Stage;   // stage s: K at 2s, V at 2s + 1
+    const int gw = blockIdx.x * kPwWarps + warp, nw = gridDim.x * kPwWarps;
+    const int n_items = B * H_kv * n_split;
     const int per = (int)cdiv(T, n_split);
-    const int t_begin = split * per, t_end = min(T, t_begin + per);
-    // this lane's 16 query features of every q-head, pre-scaled
-    uint64_t q2[G][8];
-#pragma unroll
-    for (int jq = 0; jq < G; ++jq) {
-        const uint4* src = reinterpret_cast<const uint4*>(q + ((int64_t)b * H_q + h * G + jq) * 128 + 16 * fo);
-        const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float lo = __uint_as_float(w[e] << 16) * scale, hi = __uint_as_float(w[e] & 0xffff0000u) * scale;
-            q2[jq][e] = f2_pack(lo, hi);
+    // item -> (b, h, split): splits of one (b, h) adjacent, kv-heads of one sequence next
+    auto item_of = [&](int it, int& b, int& h, int& sp, int& tb, int& te) {
+        sp = it % n_split;
+        const int bh = it / n_split;
+        h = bh % H_kv;
+        b = bh / H_kv;
+        tb = sp * per;
+        te = min(T, tb + per);
+    };
+    auto nblocks = [&](int tb, int te) { return te > tb ? (int)cdiv(te - tb, kD2Rows) : 0; };
+    // issue cursor: the warp's item ordinal and block within it
+    int iss_io = 0, iss_kb = 0, iss_n = 0;
+    uint32_t iss_k = 0;   // blocks issued
+    int ib = 0, ih = 0, isp = 0, itb = 0, ite = 0;
+    auto iss_item = [&]() {
+        const int it = gw + iss_io * nw;
+        if (it < n_items) {
+            item_of(it, ib, ih, isp, itb, ite);
+            iss_n = nblocks(itb, ite);
+        } else {
+            iss_n = -1;
         }
-    }
-    const int nblk = t_end > t_begin ? (int)cdiv(t_end - t_begin, kD2Rows) : 0;
-    auto issue = [&](int k) {
-        const int blk = warp + k * kD2Warps;
-        if (blk < nblk) {
-            const int t0 = t_begin + blk * kD2Rows;
-            uint8_t* Kt = wbase + (k & 1) * kD2Stage;
-            uint8_t* Vt = wbase + (2 + (k & 1)) * kD2Stage;
+    };
+    iss_item();
+    // issue the next block of the warp's sequence (or an empty group past its end)
+    auto issue = [&]() {
+        while (iss_n == 0) {   // an empty item (T split finer than the tokens): skip it
+            ++iss_io;
+            iss_kb = 0;
+            iss_item();
+        }
+        if (iss_n > 0) {
+            const int s = (int)(iss_k % kPwStages);
+            uint8_t* Kt = wbase + (2 * s) * kD2Stage;
+            uint8_t* Vt = wbase + (2 * s + 1) * kD2Stage;
+            const int t0 = itb + iss_kb * kD2Rows;
 #pragma unroll 4
             for (int i = lane; i < kD2Rows * 16; i += 32) {
                 const int r = i >> 4, c = i & 15;
                 const int t = t0 + r;
-                const bool ok = t < t_end;
-                const int64_t off = (((int64_t)b * Ts + (ok ? t : t_begin)) * H_kv + h) * 128 + c * 8;
+                const bool ok = t < ite;
+                const int64_t off = (((int64_t)ib * Ts + (ok ? t : itb)) * H_kv + ih) * 128 + c * 8;
                 cp_async16(reinterpret_cast<uint4*>(Kt + r * 256 + ((c ^ (r & 15)) << 4)), K + off, ok);
                 cp_async16(reinterpret_cast<uint4*>(Vt + r * 256 + (c << 4)), V + off, ok);
             }
+            if (++iss_kb == iss_n) {
+                ++iss_io;
+                iss_kb = 0;
+                iss_item();
+            }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
+        ++iss_k;
     };
-    float m[G], l[G];
-    uint64_t acc[G][2];
+    for (int k = 0; k < kPwStages - 1; ++k) issue();
+    // compute cursor
+    uint32_t cmp_k = 0;
+    for (int io = 0;; ++io) {
+        const int it = gw + io * nw;
+        if (it >= n_items) break;
+        int b, h, sp, tb, te;
+        item_of(it, b, h, sp, tb, te);
+        const int nb = nblocks(tb, te);
+        // this item's queries: 16 features of every q-head per lane, pre-scaled
+        uint64_t q2[G][8];
 #pragma unroll
-    for (int jq = 0; jq < G; ++jq) {
-        m[jq] = -INFINITY;
-        l[jq] = 0.0f;
-        acc[jq][0] = acc[jq][1] = 0ull;
-    }
-    issue(0);
-    for (int k = 0; warp + k * kD2Warps < nblk; ++k) {
-        issue(k + 1);
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
-        __syncwarp();
-        const uint8_t* Kt = wbase + (k & 1) * kD2Stage;
-        const uint8_t* Vt = wbase + (2 + (k & 1)) * kD2Stage;
-        const int t0 = t_begin + (warp + k * kD2Warps) * kD2Rows;
-        dense_block_heads<G>(Kt, Vt, t0, t_end, tg, fo, lane, q2, m, l, acc);
-        __syncwarp();   // this stage is read; the next issue refills it
+        for (int jq = 0; jq < G; ++jq) {
+            const uint4* src = reinterpret_cast<const uint4*>(q + ((int64_t)b * H_q + h * G + jq) * 128 + 16 * fo);
+            const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+            const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                q2[jq][e] = f2_pack(__uint_as_float(w[e] << 16) * scale, __uint_as_float(w[e] & 0xffff0000u) * scale);
+        }
+        float m[G], l[G];
+        uint64_t acc[G][2];
+#pragma unroll
+        for (int jq = 0; jq < G; ++jq) {
+            m[jq] = -INFINITY;
+            l[jq] = 0.0f;
+            acc[jq][0] = acc[jq][1] = 0ull;
+        }
+        for (int kb = 0; kb < nb; ++kb, ++cmp_k) {
+            issue();   // the block kPwStages - 1 ahead
+            asm volatile("cp.async.wait_group %0;" ::"n"(kPwStages - 1) : "memory");
+            __syncwarp();
+            const int s = (int)(cmp_k % kPwStages);
+            dense_block_heads<G>(wbase + (2 * s) * kD2Stage, wbase + (2 * s + 1) * kD2Stage, tb + kb * kD2Rows, te, tg,
+                                 fo, lane, q2, m, l, acc);
+            __syncwarp();   // this stage is read; a later issue refills it
+        }
+        // the item's record: weighted value sum (features 4 lane .. 4 lane + 3), max logit, weight sum
+#pragma unroll
+        for (int jq = 0; jq < G; ++jq) {
+            float* dst = partial + (((int64_t)b * H_q + h * G + jq) * n_split + sp) * 130;
+            const float2 a0 = f2_unpack(acc[jq][0]), a1 = f2_unpack(acc[jq][1]);
+            *reinterpret_cast<float2*>(dst + lane * 4) = a0;
+            *reinterpret_cast<float2*>(dst + lane * 4 + 2) = a1;
+            if (lane == 0) {
+                dst[128] = m[jq];
+                dst[129] = l[jq];
+            }
+        }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    // combine the warps' softmax states through shared memory (the rings are free): one record per CTA
-    __syncthreads();
-    float* st = reinterpret_cast<float*>(dsm);     // [kD2Warps][G][130]
-#pragma unroll
-    for (int jq = 0; jq < G; ++jq) {
-        float* w = st + (warp * G + jq) * 130;
-        const float2 a0 = f2_unpack(acc[jq][0]), a1 = f2_unpack(acc[jq][1]);
-        *reinterpret_cast<float2*>(w + lane * 4) = a0;
-        *reinterpret_cast<float2*>(w + lane * 4 + 2) = a1;
-        if (lane == 0) {
-            w[128] = m[jq];
-            w[129] = l[jq];
-        }
-    }
-    __syncthreads();
-    for (int jq = warp; jq < G; jq += kD2Warps) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kD2Warps; ++w) M = fmaxf(M, st[(w * G + jq) * 130 + 128]);
-        float L = 0.0f, a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int w = 0; w < kD2Warps; ++w) {
-            const float* src = st + (w * G + jq) * 130;
-            const float mw = src[128];
-            const float f = (mw == -INFINITY) ? 0.0f : __expf(mw - M);
-            L = fmaf(f, src[129], L);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) a[e] = fmaf(f, src[lane * 4 + e], a[e]);
-        }
-        float* dst = partial + (((int64_t)b * H_q + h * G + jq) * n_split + split) * 130;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dst[lane * 4 + e] = a[e];
-        if (lane == 0) {
-            dst[128] = M;
-            dst[129] = L;
-        }
-    }
 }
 
 template <int G>
@@ -552,10 +576,17 @@ __global__ void __launch_bounds__(kD2Threads) dense_bf16_smemq_kernel(int T, int
     }
 }
 
-int dense_splits(int B, int T, int H_kv) {
+// Token splits per (sequence, kv-head), at least 128 tokens each: about two work items per warp of the persistent
+// kernel (bf16, d = 128, up to four q-heads per kv-head; 8 warps on every SM), else about eight CTAs per SM.
+static bool dense_persistent(int H_q, int H_kv, int d, int dtype) {
+    return dtype == LOWRAM_BF16 && d == 128 && H_q / H_kv <= 4;
+}
+int dense_splits(int B, int T, int H_kv, int H_q, int d, int dtype) {
     const int64_t units = (int64_t)B * H_kv;
     if (units == 0 || T == 0) return 1;
-    int64_t s = cdiv(148 * 8, units);
+    const int64_t target = dense_persistent(H_q, H_kv, d, dtype) ? 2 * (int64_t)tc::sm_count() * kPwWarps
+                                                                 : 8 * (int64_t)tc::sm_count();
+    int64_t s = cdiv(target, units);
     s = s < 1 ? 1 : s;
     const int64_t cap = cdiv(T, 128);
     return (int)(s > cap ? cap : s);
@@ -587,7 +618,9 @@ static cudaError_t dense_g(int B, int T, int Ts, int H_q, int H_kv, float scale,
     return e;
 }
 
-int dense_records(int B, int T, int H_kv, int, int) { return dense_splits(B, T, H_kv); }
+int dense_records_max(int B, int T, int H_kv, int H_q, int d) {
+    return std::max(dense_splits(B, T, H_kv, H_q, d, LOWRAM_BF16), dense_splits(B, T, H_kv, H_q, d, LOWRAM_F32));
+}
 
 template <int G>
 static cudaError_t dense2_go(int B, int T, int Ts, int H_q, int H_kv, float scale, const void* q, const void* k, const void* v,
@@ -602,8 +635,19 @@ static cudaError_t dense2_go(int B, int T, int Ts, int H_q, int H_kv, float scal
                                              (const __nv_bfloat16*)v, partial, n_split);
         return cudaGetLastError();
     };
-    if constexpr (G <= 4) return go(dense_bf16_kernel<G>);
-    else return go(dense_bf16_smemq_kernel<G>);
+    if constexpr (G <= 4) {
+        const int n_items = B * H_kv * n_split;
+        const int grid = std::min(tc::sm_count(), (int)cdiv(n_items, kPwWarps));
+        cudaError_t e = cudaFuncSetAttribute(dense_bf16_pw_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kPwSmem);
+        if (e != cudaSuccess) return e;
+        dense_bf16_pw_kernel<G><<<grid, 32 * kPwWarps, kPwSmem, st>>>(B, T, Ts, H_q, H_kv, scale,
+                                                                        (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
+                                                                        (const __nv_bfloat16*)v, partial, n_split);
+        return cudaGetLastError();
+    } else {
+        return go(dense_bf16_smemq_kernel<G>);
+    }
 }
 
 cudaError_t launch_dense(int B, int T, int Ts, int H_q, int H_kv, int d, int dtype, float scale, const void* q, const void* k,

@@ -135,8 +135,8 @@ cudaError_t launch_residual_rows(const CompressArgs& a, int layer, cudaStream_t 
 
 // Comparator (and the exact tail): token splits, and partial records per (sequence, q-head) that launch_dense
 // writes; sequence b's K/V rows start at token b * Ts
-int dense_splits(int B, int T, int H_kv);
-int dense_records(int B, int T, int H_kv, int d, int dtype);
+int dense_splits(int B, int T, int H_kv, int H_q, int d, int dtype);   // token splits of one comparator call
+int dense_records_max(int B, int T, int H_kv, int H_q, int d);       // most splits any dtype takes (workspace)
 cudaError_t launch_dense(int B, int T, int Ts, int H_q, int H_kv, int d, int dtype, float scale, const void* q,
                          const void* k, const void* v, float* partial, int n_split, cudaStream_t st);
 

@@ -685,7 +685,7 @@ lowram_status lowram_dense_workspace_size(int32_t B, int32_t T, int32_t H_q, int
     if (B < 0 || T < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv || (d != 64 && d != 128) || !bytes)
         return fail(LOWRAM_ERR_INVALID_ARG, "bad dense shape");
     if (check_grid_rows(B) != LOWRAM_OK || check_token_rows(B, T) != LOWRAM_OK) return LOWRAM_ERR_UNSUPPORTED;
-    const int nr = dense_records(B, T, H_kv, d, LOWRAM_BF16);
+    const int nr = dense_records_max(B, T, H_kv, H_q, d);
     *bytes = kHeader + align256(sizeof(float) * (size_t)B * H_q * nr * (d + 2));
     return LOWRAM_OK;
 }
@@ -708,7 +708,7 @@ static lowram_status dense_impl(int32_t B, int32_t T, int32_t Ts, int32_t H_q, i
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(LOWRAM_ERR_ALIGNMENT, "pointer %p is not 16-byte aligned", p);
     const cudaStream_t cs = (cudaStream_t)stream;
-    const int ns = dense_splits(B, T, H_kv);
+    const int ns = dense_splits(B, T, H_kv, H_q, d, dtype);
     float* partial = (float*)((char*)workspace + kHeader);
     const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf((float)d);
     cudaError_t e = cudaSuccess;
@@ -716,7 +716,7 @@ static lowram_status dense_impl(int32_t B, int32_t T, int32_t Ts, int32_t H_q, i
         e = launch_dense(B, T, Ts, H_q, H_kv, d, dtype, scale, q, k, v, partial, ns, cs);
         if (e != cudaSuccess) return cuda_fail(e, "dense");
     }
-    e = launch_merge(B, H_q, T > 0 ? dense_records(B, T, H_kv, d, dtype) : 0, d, partial, out, lse, cs);
+    e = launch_merge(B, H_q, T > 0 ? ns : 0, d, partial, out, lse, cs);
     return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "merge");
 }
 

@@ -185,18 +185,21 @@ __global__ void __launch_bounds__(kTileThreads) vregen_simt_kernel(DecodeArgs a,
 }
 
 // ------------------------------------------------------------------------------------------------
-// K4: merge split-softmax partials.  One CTA of 128 threads per (b, q-head):
+// K4: merge split-softmax partials.  One CTA of 256 threads per (b, q-head):
 //   W = max_c m_c, w_c = exp(m_c - W), L = sum_c w_c l_c, out = sum_c w_c acc_c / L, lse = W + log L.
-// The per-chunk weights go to shared memory; each thread owns one output feature and reads the chunks'
-// values for it in batches of independent loads.
+// The per-chunk weights go to shared memory; each output feature is summed by two threads, each taking
+// alternate groups of 16 chunks as one batch of independent loads, and the two halves add in shared memory.
 // ------------------------------------------------------------------------------------------------
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeBatch = 16;
 
 __device__ __forceinline__ float merge_reduce(float v, float* red, bool is_max) {
     v = is_max ? warp_max(v) : warp_sum(v);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    const float r = is_max ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) : (red[0] + red[1]) + (red[2] + red[3]);
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < kMergeThreads / 32; ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
     __syncthreads();
     return r;
 }
@@ -204,7 +207,8 @@ __device__ __forceinline__ float merge_reduce(float v, float* red, bool is_max) 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(int n_chunks, int d, const float* __restrict__ partial,
                                                               float* __restrict__ out, float* __restrict__ lse) {
     extern __shared__ float wts[];   // [n_chunks]
-    __shared__ float red[4];
+    __shared__ float red[kMergeThreads / 32];
+    __shared__ float half_sum[kMaxD];
     const int w = blockIdx.x, tid = threadIdx.x;
     const int64_t rw = d + 2;
     const float* P = partial + (int64_t)w * n_chunks * rw;
@@ -220,18 +224,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(int n_chunks, int 
     }
     L = merge_reduce(L, red, false);   // also orders the wts[] writes before their reads
     const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-    if (tid < d) {
-        float acc = 0.0f;
-        for (int c0 = 0; c0 < n_chunks; c0 += 8) {
-            float v[8];
+    const int f = tid & (kMaxD - 1), half = tid / kMaxD;
+    float acc = 0.0f;
+    if (f < d) {
+        for (int c0 = half * kMergeBatch; c0 < n_chunks; c0 += 2 * kMergeBatch) {
+            float v[kMergeBatch];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = (c0 + u < n_chunks) ? P[(c0 + u) * rw + tid] : 0.0f;
+            for (int u = 0; u < kMergeBatch; ++u) v[u] = (c0 + u < n_chunks) ? P[(c0 + u) * rw + f] : 0.0f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < kMergeBatch; ++u)
                 if (c0 + u < n_chunks) acc = fmaf(wts[c0 + u], v[u], acc);
         }
-        out[(int64_t)w * d + tid] = acc * inv;
+        if (half == 1) half_sum[f] = acc;
     }
+    __syncthreads();
+    if (half == 0 && f < d) out[(int64_t)w * d + f] = (acc + half_sum[f]) * inv;
     if (lse && tid == 0) lse[w] = (L > 0.0f) ? M + logf(L) : -INFINITY;
 }
 

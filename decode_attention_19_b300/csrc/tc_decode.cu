@@ -275,12 +275,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
         // cos/sin of this thread's frequencies (f, f+1), f = fh*32 + 8c + 2*g4, at each of its four tokens'
         // positions ([2*lh + i][c]); fetched once per tile and kept in registers for every unit of the tile
         uint64_t c2[4][4], s2[4][4];
+        // positions are the token indices (no position array): the tables are read at the thread's first token
+        // only and its other three tokens, 8, 16 and 24 positions on, come from rotations by 8 positions
+        // (the angle-addition formula with the tables at position 8; three fp32 steps, ~1e-7 relative)
+        const bool rot = p.pos == nullptr && p.max_pos >= p.T && p.max_pos > 8;
+        auto load_tables = [&](int bb, int tt0, bool rl) {
+            if (rot) {
+                const int t = tt0 + quarter * 32 + r8;
+                const int ps = (rl && t < p.T) ? t : 0;
+                const float* cb = p.rcos + (int64_t)(fh * 32 + 2 * g4) * mp;
+                const float* sb = p.rsin + (int64_t)(fh * 32 + 2 * g4) * mp;
+                uint64_t c8[4], s8[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    c2[0][c] = f2_pack(__ldg(cb + (8 * c) * mp + ps), __ldg(cb + (8 * c + 1) * mp + ps));
+                    s2[0][c] = f2_pack(__ldg(sb + (8 * c) * mp + ps), __ldg(sb + (8 * c + 1) * mp + ps));
+                    c8[c] = f2_pack(__ldg(cb + (8 * c) * mp + 8), __ldg(cb + (8 * c + 1) * mp + 8));
+                    s8[c] = f2_pack(__ldg(sb + (8 * c) * mp + 8), __ldg(sb + (8 * c + 1) * mp + 8));
+                }
+#pragma unroll
+                for (int k = 1; k < 4; ++k)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        c2[k][c] = f2_sub(f2_mul(c2[k - 1][c], c8[c]), f2_mul(s2[k - 1][c], s8[c]));
+                        s2[k][c] = f2_fma(s2[k - 1][c], c8[c], f2_mul(c2[k - 1][c], s8[c]));
+                    }
+                return;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int t = tt0 + quarter * 32 + 16 * (k >> 1) + 8 * (k & 1) + r8;
+                int ps = 0;
+                if (rl && t < p.T) {
+                    ps = p.pos ? p.pos[(int64_t)bb * p.T + t] : t;
+                    if (ps < 0 || ps >= p.max_pos) {
+                        flag(p.check, LOWRAM_CHECK_POS_RANGE);
+                        ps = ps < 0 ? 0 : p.max_pos - 1;
+                    }
+                }
+                const float* cb = p.rcos + (int64_t)(fh * 32 + 2 * g4) * mp + ps;
+                const float* sb = p.rsin + (int64_t)(fh * 32 + 2 * g4) * mp + ps;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    c2[k][c] = f2_pack(__ldg(cb + (8 * c) * mp), __ldg(cb + (8 * c + 1) * mp));
+                    s2[k][c] = f2_pack(__ldg(sb + (8 * c) * mp), __ldg(sb + (8 * c + 1) * mp));
+                }
+            }
+        };
         // no abort test in the loop conditions: every epilogue thread walks the same items and reaches the
         // same named barriers; after an abort the waits fail at once and the work is skipped
         for (int it = it_begin; it < it_end; ++it, ++j) {
             int u, pr;
             item_up(it, u, pr);
-            if (pr != cur_pr) {
+            if (pr != cur_pr) {   // a new tile not fetched at the end of the item before
                 cur_pr = pr;
                 pair_tile(p, pr, (int)rank, b, t0, real);   // a tile past the end is computed but writes nothing
                 if (b != cur_b) {
@@ -304,25 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                     named_bar_sync(1, 256);
                     cur_b = b;
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int t = t0 + quarter * 32 + 16 * (k >> 1) + 8 * (k & 1) + r8;
-                    int ps = 0;
-                    if (real && t < p.T) {
-                        ps = p.pos ? p.pos[(int64_t)b * p.T + t] : t;
-                        if (ps < 0 || ps >= p.max_pos) {
-                            flag(p.check, LOWRAM_CHECK_POS_RANGE);
-                            ps = ps < 0 ? 0 : p.max_pos - 1;
-                        }
-                    }
-                    const float* cb = p.rcos + (int64_t)(fh * 32 + 2 * g4) * mp + ps;
-                    const float* sb = p.rsin + (int64_t)(fh * 32 + 2 * g4) * mp + ps;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        c2[k][c] = f2_pack(__ldg(cb + (8 * c) * mp), __ldg(cb + (8 * c + 1) * mp));
-                        s2[k][c] = f2_pack(__ldg(sb + (8 * c) * mp), __ldg(sb + (8 * c + 1) * mp));
-                    }
-                }
+                load_tables(b, t0, real);
             }
             const uint32_t buf = j & 1;
             const bool ok = mbar_wait_cluster(&t_full[buf], (j >> 1) & 1, abort_flag);
@@ -424,6 +453,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                     if (lane == 0) mbar_arrive_remote(peer_smem(&t_empty[buf], 0));
                 }
             }
+            // this item's tile, for the stores below; then, when the next item starts a new tile of the same
+            // sequence, its tables are fetched now (this item's math is done with them), so that the loads run
+            // during the exchange, the stores and the next accumulator wait
+            const int sb = b, st0 = t0;
+            const bool sreal = real;
+            if (it + 1 < it_end) {
+                int u2, pr2;
+                item_up(it + 1, u2, pr2);
+                if (pr2 != cur_pr) {
+                    int b2, t02;
+                    bool real2;
+                    pair_tile(p, pr2, (int)rank, b2, t02, real2);
+                    if (b2 == cur_b) {
+                        cur_pr = pr2;
+                        b = b2;
+                        t0 = t02;
+                        real = real2;
+                        load_tables(b, t0, real);
+                    }
+                }
+            }
             float* xs = Xs + (buf * 128 + frow) * 16;
             if (LHP == 2 && fh == 1)
 #pragma unroll
@@ -431,8 +481,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
                     for (int jq = 0; jq < G; ++jq) xs[hx * G + jq] = fin[hx][jq];
             named_bar_sync(1, 256);      // (exchange buffers alternate by unit, so one barrier per unit)
-            const int t = t0 + frow;
-            if (finisher && ok && real && t < p.T) {
+            const int t = st0 + frow;
+            if (finisher && ok && sreal && t < p.T) {
 #pragma unroll
                 for (int hx = 0; hx < HPU; ++hx) {
                     const int h = u * HPU + hx;
@@ -441,9 +491,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                     for (int jq = 0; jq < G; ++jq) {
                         const float sc = (fin[hx][jq] + xs[hx * G + jq]) * p.scale;
                         best = fmaxf(best, sc);
-                        if (p.sall) p.sall[((int64_t)b * p.H_q + h * G + jq) * p.T + t] = sc;
+                        if (p.sall) p.sall[((int64_t)sb * p.H_q + h * G + jq) * p.T + t] = sc;
                     }
-                    p.key[((int64_t)b * p.H_kv + h) * p.T + t] = best;
+                    p.key[((int64_t)sb * p.H_kv + h) * p.T + t] = best;
                 }
             }
         }
