@@ -65,16 +65,8 @@ __global__ void dup_cols_kernel(const uint4* __restrict__ W, int64_t rows, int b
     out[row * 2 * per_row + per_row + k] = v;
 }
 
-// One thread per 8 consecutive coefficients: fp16(code * scale), 16 bytes out.
-__global__ void int4_f16_kernel(const uint32_t* __restrict__ codes, const __half* __restrict__ scales, int64_t rows,
-                                int r, __half* __restrict__ out) {
-    const int per_row = r / 8;
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= rows * per_row) return;
-    const int64_t row = i / per_row;
-    const int k = (int)(i - row * per_row) * 8;
-    const uint32_t w = __ldg(codes + i);
-    const float sc = __half2float(__ldg(scales + row * (r / 32) + (k >> 5)));
+// fp16(code * scale) of 8 coefficients packed in one 32-bit word (even entry in the low nibble).
+__device__ __forceinline__ uint4 int4x8_to_f16(uint32_t w, float sc) {
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -82,20 +74,34 @@ __global__ void int4_f16_kernel(const uint32_t* __restrict__ codes, const __half
         const __half2 h2 = __floats2half2_rn((float)(n0 >= 8 ? n0 - 16 : n0) * sc, (float)(n1 >= 8 ? n1 - 16 : n1) * sc);
         o[e] = *reinterpret_cast<const uint32_t*>(&h2);
     }
-    reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// fp16 copies of `batches` bf16 bases of `rows` rows (basis c starts c * stride8 16-byte pieces into W; outputs
-// packed): every bf16 value whose magnitude is at least 2^-14 is exact in fp16.
-__global__ void bf16_f16_kernel(const uint4* __restrict__ W, int64_t rows, int batches, int64_t stride8, int r,
-                                uint4* __restrict__ out) {
-    const int per_row = r / 8;
+// Both fp16 copies of an int4 call in one launch: threads [0, rows r / 16) take 16 consecutive coefficients each
+// (8 bytes of codes, the one scale of their group of 32, 32 bytes out); the threads after them copy the bases,
+// 16 bytes each (every bf16 value whose magnitude is at least 2^-14 is exact in fp16).
+__global__ void int4_f16_copies_kernel(const uint2* __restrict__ codes, const __half* __restrict__ scales, int64_t rows,
+                                       int r, uint4* __restrict__ out, const uint4* __restrict__ W, int64_t wrows,
+                                       int wbatches, int64_t wstride8, uint4* __restrict__ wout) {
+    const int64_t n16 = rows * (r / 16);
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= rows * batches * per_row) return;
-    const int64_t row = i / per_row;
-    const int k = (int)(i - row * per_row);
-    const int64_t c = row / rows, rl = row - c * rows;
-    const uint4 v = __ldg(W + c * stride8 + rl * per_row + k);
+    if (i < n16) {
+        const int per_row = r / 16;
+        const int64_t row = i / per_row;
+        const int k = (int)(i - row * per_row) * 16;
+        const uint2 w = __ldg(codes + i);
+        const float sc = __half2float(__ldg(scales + row * (r / 32) + (k >> 5)));
+        out[2 * i] = int4x8_to_f16(w.x, sc);
+        out[2 * i + 1] = int4x8_to_f16(w.y, sc);
+        return;
+    }
+    const int64_t j = i - n16;
+    const int per_row = r / 8;
+    if (j >= wrows * wbatches * per_row) return;
+    const int64_t row = j / per_row;
+    const int k = (int)(j - row * per_row);
+    const int64_t c = row / wrows, rl = row - c * wrows;
+    const uint4 v = __ldg(W + c * wstride8 + rl * per_row + k);
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
@@ -103,28 +109,20 @@ __global__ void bf16_f16_kernel(const uint4* __restrict__ W, int64_t rows, int b
         const __half2 h2 = __floats2half2_rn(__uint_as_float(u[e] << 16), __uint_as_float(u[e] & 0xffff0000u));
         o[e] = *reinterpret_cast<const uint32_t*>(&h2);
     }
-    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    wout[j] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace
 
-cudaError_t launch_int4_to_f16(const void* codes, const void* scales, int64_t rows, int r, void* out,
-                               cudaStream_t st) {
-    const int64_t n = rows * (r / 8);
+cudaError_t launch_int4_f16_copies(const void* codes, const void* scales, int64_t rows, int r, void* out,
+                                   const void* W, int64_t wrows, int wbatches, int64_t wstride, void* wout,
+                                   cudaStream_t st) {
+    const int64_t n = rows * (r / 16) + wrows * wbatches * (r / 8);
     if (n == 0) return cudaSuccess;
     const int threads = 256;
-    int4_f16_kernel<<<(unsigned)cdiv(n, threads), threads, 0, st>>>((const uint32_t*)codes, (const __half*)scales,
-                                                                      rows, r, (__half*)out);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_bf16_to_f16(const void* W, int64_t rows, int r, void* out, cudaStream_t st, int batches,
-                               int64_t batch_stride) {
-    const int64_t n = rows * batches * (r / 8);
-    if (n == 0) return cudaSuccess;
-    const int threads = 256;
-    bf16_f16_kernel<<<(unsigned)cdiv(n, threads), threads, 0, st>>>((const uint4*)W, rows, batches, batch_stride / 8, r,
-                                                                      (uint4*)out);
+    int4_f16_copies_kernel<<<(unsigned)cdiv(n, threads), threads, 0, st>>>(
+        (const uint2*)codes, (const __half*)scales, rows, r, (uint4*)out, (const uint4*)W, wrows, wbatches,
+        wstride / 8, (uint4*)wout);
     return cudaGetLastError();
 }
 

@@ -100,9 +100,12 @@ cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st);
 // ([rows, 2r]), and the basis with its columns repeated ([rows, 2r]); see dequant.cu
 cudaError_t launch_int4_split(const void* codes, const void* scales, int64_t rows, int r, void* out, cudaStream_t st);
 // int4 caches, default: out [rows, r] fp16 = fp16(code * scale); and an fp16 copy of bf16 basis rows (batched)
-cudaError_t launch_int4_to_f16(const void* codes, const void* scales, int64_t rows, int r, void* out, cudaStream_t st);
-cudaError_t launch_bf16_to_f16(const void* W, int64_t rows, int r, void* out, cudaStream_t st, int batches = 1,
-                               int64_t batch_stride = 0);
+// fp16(code * scale) of an int4 cache [rows, r] and fp16 copies of `wbatches` bf16 bases [wrows, r] (basis c at
+// c * wstride elements of W), in one launch.
+cudaError_t launch_int4_f16_copies(const void* codes, const void* scales, int64_t rows, int r, void* out,
+                                   const void* W, int64_t wrows, int wbatches, int64_t wstride, void* wout,
+                                   cudaStream_t st);
+
 cudaError_t launch_dup_cols(const void* W, int64_t rows, int r, void* out, cudaStream_t st, int batches = 1,
                             int64_t batch_stride = 0);
 

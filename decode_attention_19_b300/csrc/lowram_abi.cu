@@ -292,10 +292,9 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     }
     if (e == cudaSuccess && L.f16 && (int64_t)s.B * s.T > 0) {
         const Range stage("lowram int4 to fp16");
-        e = launch_int4_to_f16(coef, coef_scale, (int64_t)s.B * s.T, s.r, ws + L.off_asplit, cs);
-        if (e == cudaSuccess)
-            e = launch_bf16_to_f16(basis, (int64_t)s.H_kv * s.d, s.r, ws + L.off_bsplit, cs,
-                                   s.basis_batch_stride ? s.B : 1, s.basis_batch_stride);
+        e = launch_int4_f16_copies(coef, coef_scale, (int64_t)s.B * s.T, s.r, ws + L.off_asplit, basis,
+                                   (int64_t)s.H_kv * s.d, s.basis_batch_stride ? s.B : 1, s.basis_batch_stride,
+                                   ws + L.off_bsplit, cs);
         if (e != cudaSuccess) return cuda_fail(e, "int4 to fp16");
     }
     if (e == cudaSuccess && (int64_t)s.B * s.T > 0 && (L.S_eff > 0 || key_out)) {
