@@ -26,7 +26,9 @@
 //               lane 1: merge tickets (the per-(b, h) chunk counter, one item behind the epilogue).
 //   warp 1      TMEM owner (two accumulators of m columns) and MMA issuer (one thread):
 //               D[m hidden x 128 tokens] = F_h . C_sel^T (M = 128 per 128 hidden units, N = 128, K = r), hidden
-//               units on TMEM lanes, tokens on columns; item j accumulates into buffer j % 2.
+//               units on TMEM lanes, tokens on columns; item j accumulates into buffer j % 2.  With m = 128 and
+//               r <= 512 the resident F_h is also copied into TMEM (tcgen05.cp, once per kv-head) and the MMAs read
+//               their A operand there, so shared memory serves only the latent chunks to the tensor cores.
 //   warps 2-3   gather: 16-byte cp.async of the selected tokens' latent rows into the 128B-swizzled ring, one
 //               64-wide k-chunk per stage, running ahead into the next items.
 //   warps 4-11  epilogue, one item after another while the next item's rows land and multiply: softmax weights
@@ -61,6 +63,7 @@ constexpr size_t kSmemMax = 232448;
 struct VregenTcParams {
     int B, T, H_q, H_kv, m, r, S_eff, n_chunks, n_res, KC, NS, n_items;
     int f_resident;           // F_h stays in shared memory for all of a kv-head's items (else streamed per stage)
+    int f_tmem;               // the resident F_h is copied into TMEM and the MMAs read A there (M = 128, r <= 512)
     int fold_per_seq;         // the folded weights hold one copy per sequence
     uint32_t idesc;           // MMA instruction descriptor: bf16 operands, or fp16 (an int4 cache's fp16 copy)
     long long mlp_stride;     // elements from sequence b's w2 to b+1's (0: shared); biases are then per sequence
@@ -152,6 +155,8 @@ __global__ void __launch_bounds__(kVThreads, 1)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int NS = p.NS, KC = p.KC;
     const bool fres = p.f_resident != 0;
+    const bool ftm = fres && p.f_tmem != 0;
+    const uint32_t tmem_cols = ftm ? 512u : (uint32_t)(2 * M);
     const uint32_t kStage = kCBytes + (fres ? 0u : kFChunk);
     uint8_t* Fres = smem;                                        // [KC][M x 64] when resident
     uint8_t* ring = smem + (fres ? (size_t)KC * kFChunk : 0);    // NS stages: C chunk [128 x 64] (+ F chunk)
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
     }
     if (warp == 0 && lane == 0) prefetch_tmap(&tmF);
     if (warp == 1) {
-        tmem_alloc(tmem_slot, (uint32_t)(2 * M));
+        tmem_alloc(tmem_slot, tmem_cols);
         tmem_relinquish();
     }
     fence_before();
@@ -292,14 +297,32 @@ __global__ void __launch_bounds__(kVThreads, 1)
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool ok = true;
-            int n_seg = 0, cur_fh = -1;
+            int n_seg = 0, cur_fh = -1, n_drain = 0;
             uint32_t g = 0;                                      // stages consumed
             for (int j = 0; j < n_local && ok; ++j) {
                 const int fh = item_fh(it_begin + j);
                 if (fres && fh != cur_fh) {
                     if (!mbar_wait_lim(f_full, n_seg & 1, abort_flag, p.wait_cycles)) break;
+                    if (ftm && n_seg > 0) {
+                        // the MMAs of the kv-head before still read its F_h from TMEM: let them finish first (a copy
+                        // is not ordered after earlier MMAs)
+                        mma_commit(m_drain);
+                        if (!mbar_wait_lim(m_drain, n_drain & 1, abort_flag, p.wait_cycles)) break;
+                        ++n_drain;
+                    }
                     cur_fh = fh;
                     ++n_seg;
+                    if (ftm) {
+                        // F_h into TMEM columns [2M, 2M + r/2): k-chunk kc at column 32 kc, 8 columns per 16 k-values;
+                        // the shared copy is free once the copies have read it
+                        fence_after();
+                        for (int kc = 0; kc < KC; ++kc)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tmem_cp_128x256b(tmem + 2 * M + kc * 32 + k * 8,
+                                                 sdesc_sw128(smem_u32(Fres + kc * kFChunk) + k * 32));
+                        mma_commit(f_empty);
+                    }
                 }
                 const uint32_t buf = j & 1;
                 if (!mbar_wait_lim(&t_empty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.wait_cycles)) break;
@@ -313,23 +336,31 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     }
                     fence_after();
                     const uint32_t c_addr = smem_u32(ring + s * kStage);
-                    const uint32_t f_addr = fres ? smem_u32(Fres + kc * kFChunk) : c_addr + kCBytes;
-#pragma unroll
-                    for (int mb = 0; mb < MB; ++mb)
+                    if (ftm) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            mma_bf16(tmem + buf * M + mb * 128, sdesc_sw128(f_addr + mb * 16384 + k * 32),
-                                     sdesc_sw128(c_addr + k * 32), p.idesc, (kc | k) != 0);
+                            mma_bf16_ts(tmem + buf * M, tmem + 2 * M + kc * 32 + k * 8, sdesc_sw128(c_addr + k * 32),
+                                        p.idesc, (kc | k) != 0);
+                    } else {
+                        const uint32_t f_addr = fres ? smem_u32(Fres + kc * kFChunk) : c_addr + kCBytes;
+#pragma unroll
+                        for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_bf16(tmem + buf * M + mb * 128, sdesc_sw128(f_addr + mb * 16384 + k * 32),
+                                         sdesc_sw128(c_addr + k * 32), p.idesc, (kc | k) != 0);
+                    }
                     mma_commit(&empty[s]);
                 }
                 if (!ok) break;
                 mma_commit(&t_full[buf]);
-                // the last item of a kv-head segment: its MMAs release the resident F_h
-                if (fres && (j + 1 == n_local || item_fh(it_begin + j + 1) != fh)) mma_commit(f_empty);
+                // the last item of a kv-head segment: its MMAs release the resident F_h (with the TMEM copy, the
+                // copy released it already)
+                if (fres && !ftm && (j + 1 == n_local || item_fh(it_begin + j + 1) != fh)) mma_commit(f_empty);
             }
             // every MMA issued completes before TMEM is released or shared memory is reused
             mma_commit(m_drain);
-            mbar_wait_drain(m_drain, 0);
+            mbar_wait_drain(m_drain, n_drain & 1);
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------------ gather (128 threads)
@@ -772,7 +803,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
     if (*abort_flag && threadIdx.x == 0) flag(p.check, LOWRAM_CHECK_TIMEOUT);
     if (warp == 1) {
         fence_after();
-        tmem_dealloc(tmem, (uint32_t)(2 * M));
+        tmem_dealloc(tmem, tmem_cols);
     }
 }
 
@@ -804,6 +835,7 @@ cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     const VregenConfig cfg = vregen_config(s.m, s.r, s.H_q / s.H_kv);
     p.NS = cfg.NS;
     p.f_resident = cfg.f_resident ? 1 : 0;
+    p.f_tmem = (cfg.f_resident && s.m == 128 && 2 * s.m + s.r / 2 <= 512) ? 1 : 0;
     p.n_items = s.B * s.H_kv * a.n_chunks;
     const int copies = (s.basis_batch_stride || s.mlp_batch_stride) ? s.B : 1;
     p.fold_per_seq = copies > 1 ? 1 : 0;
