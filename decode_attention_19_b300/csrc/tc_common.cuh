@@ -125,6 +125,32 @@ __device__ __forceinline__ void cp_async_wait() {
 // Shared-memory writes of the generic proxy (st.shared, cp.async) made visible to the async proxy, which
 // tcgen05.mma reads operands through.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Read-only global loads issued exactly where they stand (volatile: the compiler keeps them in order with the
+// other volatile asm, e.g. TMEM loads and barrier waits, instead of sinking them to their first use), so that a
+// prefetch overlaps the work between the load and its use.
+__device__ __forceinline__ uint32_t ldg_pin_u16(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ int ldg_pin_s8(const void* p) {
+    short v;
+    asm volatile("ld.global.nc.s8 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_pin_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ldg_pin_f32(const void* p) { return __uint_as_float(ldg_pin_u32(p)); }
+__device__ __forceinline__ int ldg_pin_s32(const void* p) { return (int)ldg_pin_u32(p); }
+// One arrival on `bar` once every cp.async this thread issued before has landed (the barrier's expected count
+// includes it); the thread does not wait.  The consumer orders the landed bytes before its async-proxy reads with
+// fence_proxy_async after its wait on the barrier.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 // Warp-level bf16 MMA, D[16 x 8] += A[16 x 16] B[16 x 8] with float32 accumulation (fragments in the m16n8k16
 // register layout: g = lane / 4, t = lane % 4; a0 = A[g][2t, 2t+1], a1 = A[g+8][..], a2 = A[g][2t+8, 2t+9],

@@ -20,22 +20,28 @@
 // folded weights where the unfolded chain would round the rebuilt keys.
 //
 // K3 is persistent: one CTA per SM walks a contiguous range of work items (kv-head h, sequence b, chunk of 128
-// selected tokens), kv-head-major, so consecutive items share F_h, which stays resident in shared memory while
-// it fits (else each ring stage carries its F chunk).  384 threads (168 registers each):
-//   warp 0      lane 0: TMA of F_h's k-chunks [m x 64] (once per kv-head, or per stage when streamed);
+// selected tokens), kv-head-major, so consecutive items share F_h, which stays resident in TMEM (m = 128,
+// r <= 512) or in shared memory while it fits (else each ring stage carries its F chunk).  512 threads, launched at 128 registers each and re-split
+// per warpgroup (setmaxnreg): 56 for warps 0-7, 200 for the epilogue warps 8-15:
+//   warp 0      lane 0: TMA of F_h's k-chunks [m x 64] once per kv-head (into two staging buffers in TMEM
+//               mode, into the resident copy otherwise) or per stage when streamed;
 //               lane 1: merge tickets (the per-(b, h) chunk counter, one item behind the epilogue).
 //   warp 1      TMEM owner (two accumulators of m columns) and MMA issuer (one thread):
 //               D[m hidden x 128 tokens] = F_h . C_sel^T (M = 128 per 128 hidden units, N = 128, K = r), hidden
-//               units on TMEM lanes, tokens on columns; item j accumulates into buffer j % 2.  With m = 128 and
-//               r <= 512 the resident F_h is also copied into TMEM (tcgen05.cp, once per kv-head) and the MMAs read
-//               their A operand there, so shared memory serves only the latent chunks to the tensor cores.
-//   warps 2-3   gather: 16-byte cp.async of the selected tokens' latent rows into the 128B-swizzled ring, one
-//               64-wide k-chunk per stage, running ahead into the next items.
-//   warps 4-11  epilogue, one item after another while the next item's rows land and multiply: softmax weights
-//               of the chunk from the scaled logits the key pass stored (fetched an item ahead), the residual
-//               rows of the chunk's hits (loads issued before, used after, the accumulator read); per thread one
-//               hidden unit and half of the tokens: SiLU(D + b1) weighted by the softmax, summed; the TMEM buffer
-//               is released; w2 (rows held in registers per kv-head) on the hidden sums; the chunk's record.
+//               units on TMEM lanes, tokens on columns; item j accumulates into buffer j % 2.  In TMEM mode it
+//               copies F_h's staged chunks into TMEM beside the accumulators (tcgen05.cp, once per kv-head) and
+//               the MMAs read their A operand there: shared memory holds only 32 KB of staging and a deeper ring.
+//   warps 2-3   idle (their warpgroup's registers go to the epilogue).
+//   warps 4-7   gather: 16-byte cp.async of the selected tokens' latent rows into the 128B-swizzled ring, one
+//               64-wide k-chunk per stage; the copies arrive on the stage's barrier when they land, so the warps
+//               never wait for them and run ahead into the next items as far as the free slots allow.
+//   warps 8-15  epilogue in two teams of four warps: team t takes the items j = t, t + 2, ... (TMEM buffer t),
+//               each with its own scratch and named barrier, while the next items' rows land and multiply:
+//               softmax weights of the chunk from the scaled logits the key pass stored (fetched a team item
+//               ahead), the residual rows of the chunk's hits (loads issued before, used after, the accumulator
+//               read); per thread one hidden unit and all 128 tokens: SiLU(D + b1) weighted by the softmax,
+//               summed; the TMEM buffer is released; w2 (rows held in registers per kv-head) on the hidden sums;
+//               the chunk's record.
 // The CTA finishing a (b, h)'s last chunk merges its chunks' records into out and lse (a counter per (b, h),
 // zeroed by the selection kernel; records read through L2).
 //
@@ -50,20 +56,24 @@ namespace lowram {
 
 namespace {
 
-constexpr int kVThreads = 384;            // 12 warps: 168 registers a thread
-constexpr int kGat = 64;                 // gathering threads (warps 2-3)
-constexpr int kEpi = 256;                // epilogue threads (warps 6-13)
+constexpr int kVThreads = 512;            // 16 warps launched at 128 registers a thread, then re-split:
+constexpr int kProdRegs = 56;             //   warps 0-7 (TMA, MMA, gather) give registers back,
+constexpr int kEpiRegs = 200;             //   warps 8-15 (epilogue) take them: 256 x 56 + 256 x 200 = 512 x 128
+constexpr int kGat = 128;                 // gathering threads (warps 4-7)
+constexpr int kTeam = 128;                // epilogue team: warps 8-11 and warps 12-15
 constexpr int kRows = 128;               // selected tokens per item
 constexpr int kCBytes = kRows * 128;     // latent chunk [128 tokens x 64] bf16, 128B-swizzled
 constexpr int kGatRows = kRows / (kGat / 8);   // rows each gathering thread copies per stage
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
+constexpr int kFStage = 2;               // TMEM mode: F_h staging buffers of 16 KB
 constexpr int kMaxMergeChunks = 64;      // chunks per (b, h) the fused merge takes (S <= 8192)
 constexpr size_t kSmemMax = 232448;
 
 struct VregenTcParams {
     int B, T, H_q, H_kv, m, r, S_eff, n_chunks, n_res, KC, NS, n_items;
-    int f_resident;           // F_h stays in shared memory for all of a kv-head's items (else streamed per stage)
-    int f_tmem;               // the resident F_h is copied into TMEM and the MMAs read A there (M = 128, r <= 512)
+    int f_resident;           // F_h stays in shared memory for all of a kv-head's items
+    int f_tmem;               // F_h stays in TMEM (M = 128, r <= 512), loaded once per kv-head through
+                              // kFStage staging buffers; neither: F_h streamed with every ring stage
     int fold_per_seq;         // the folded weights hold one copy per sequence
     uint32_t idesc;           // MMA instruction descriptor: bf16 operands, or fp16 (an int4 cache's fp16 copy)
     long long mlp_stride;     // elements from sequence b's w2 to b+1's (0: shared); biases are then per sequence
@@ -87,18 +97,20 @@ struct VregenTcParams {
 __host__ __device__ constexpr int w2_ntiles(int g) { return (2 * g + 7) / 8; }
 constexpr int kWoStride = 132;           // floats per row of the second layer's output (conflict-free stores)
 
-// Epilogue scratch beside the ring, for g q-heads per kv-head: softmax weights [g][128], hidden sums [2][g][m],
-// the upper half's residual sums [g][128], the second layer's output [8 nt][132] and operand [8 nt][m + 8] bf16,
-// merge weights [g][64] and (W, L) [8][2], compacted hits (rows, slots), reductions [2][32] + counts [4], then
-// the barriers and the TMEM slot / flags.
+// One epilogue team's scratch in 4-byte words, for g q-heads per kv-head: softmax weights [g][128], hidden sums
+// [g][m], the second layer's output [8 nt][132] and operand [8 nt][m + 8] bf16, merge weights [g][64] and (W, L)
+// [8][2], compacted hits (rows, slots), reductions [2][32] + counts [4]; a multiple of 4 words (16-byte aligned).
+__host__ __device__ constexpr int team_words(int m, int g) {
+    return (g * kRows + g * m + w2_ntiles(g) * 8 * kWoStride + w2_ntiles(g) * 4 * (m + 8) + g * kMaxMergeChunks + 16 +
+            2 * kRows + 64 + 4 + 3) & ~3;
+}
+// Scratch beside the ring: two teams' scratch, then the barriers and the TMEM slot / flags.
 size_t scratch_bytes(int m, int g) {
-    const int nt = w2_ntiles(g);
-    return (size_t)4 * (g * kRows + 2 * g * m + g * kRows + nt * 8 * kWoStride) + (size_t)2 * nt * 8 * (m + 8) +
-           (size_t)4 * (g * kMaxMergeChunks + 16 + 2 * kRows + 64 + 4) + 8 + 8 * (3 * kMaxStages + 2 + 4 + 1 + 4) + 32;
+    return (size_t)8 * team_words(m, g) + 8 + 8 * (3 * kMaxStages + 2 * kFStage + 4 + 1 + 8) + 32;
 }
 
 struct VregenConfig {
-    bool f_resident;
+    bool f_tmem, f_resident;
     int NS;
     size_t smem;
 };
@@ -107,7 +119,13 @@ VregenConfig vregen_config(int m, int r, int g) {
     const int KC = r / 64;
     const size_t fres = (size_t)KC * m * 128, fixed = 1024 + scratch_bytes(m, g);
     VregenConfig c{};
-    if (fres + fixed + 3 * (size_t)kCBytes <= kSmemMax) {
+    if (m == 128 && 2 * m + r / 2 <= 512) {
+        // two accumulators and F_h fit the SM's 512 TMEM columns: F_h passes through kFStage 16 KB staging buffers
+        const size_t fst = kFStage * (size_t)kCBytes;
+        c.f_tmem = true;
+        c.NS = (int)std::min<size_t>(kMaxStages, (kSmemMax - fst - fixed) / kCBytes);
+        c.smem = fst + fixed + (size_t)c.NS * kCBytes;
+    } else if (fres + fixed + 3 * (size_t)kCBytes <= kSmemMax) {
         c.f_resident = true;
         c.NS = (int)std::min<size_t>(kMaxStages, (kSmemMax - fres - fixed) / kCBytes);
         c.smem = fres + fixed + (size_t)c.NS * kCBytes;
@@ -131,20 +149,6 @@ __device__ __forceinline__ float silu_tanh(float x) {
 }
 
 
-// cp.async.wait_group with a run-time count of groups allowed to stay pending (at most kMaxStages - 1)
-__device__ __forceinline__ void cp_async_wait_pending(int n) {
-    switch (n) {
-        case 0: tc::cp_async_wait<0>(); break;
-        case 1: tc::cp_async_wait<1>(); break;
-        case 2: tc::cp_async_wait<2>(); break;
-        case 3: tc::cp_async_wait<3>(); break;
-        case 4: tc::cp_async_wait<4>(); break;
-        case 5: tc::cp_async_wait<5>(); break;
-        case 6: tc::cp_async_wait<6>(); break;
-        default: tc::cp_async_wait<7>(); break;
-    }
-}
-
 template <int G, int MB>
 __global__ void __launch_bounds__(kVThreads, 1)
     vregen_tc_kernel(const __grid_constant__ CUtensorMap tmF, VregenTcParams p) {
@@ -155,38 +159,29 @@ __global__ void __launch_bounds__(kVThreads, 1)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int NS = p.NS, KC = p.KC;
     const bool fres = p.f_resident != 0;
-    const bool ftm = fres && p.f_tmem != 0;
+    const bool ftm = p.f_tmem != 0;
     const uint32_t tmem_cols = ftm ? 512u : (uint32_t)(2 * M);
-    const uint32_t kStage = kCBytes + (fres ? 0u : kFChunk);
-    uint8_t* Fres = smem;                                        // [KC][M x 64] when resident
-    uint8_t* ring = smem + (fres ? (size_t)KC * kFChunk : 0);    // NS stages: C chunk [128 x 64] (+ F chunk)
-    float* Ps = (float*)(ring + (size_t)NS * kStage);            // [G][128] softmax weights (0 on padding slots)
-    float* Z = Ps + G * kRows;                                   // [2 token halves][G][M] hidden sums
-    float* X = Z + 2 * G * M;                                    // [G][128] the upper half's residual sums
+    const uint32_t kStage = kCBytes + (fres || ftm ? 0u : kFChunk);
+    uint8_t* Fres = smem;   // [KC][M x 64] when resident; [kFStage][M x 64] staging buffers in TMEM mode
+    uint8_t* ring = smem + (fres ? (size_t)KC * kFChunk : ftm ? kFStage * (size_t)kFChunk : 0);   // NS stages: C
+                                                                                               // chunk (+ F chunk)
+    float* epi = (float*)(ring + (size_t)NS * kStage);           // [2 teams][team_words] epilogue scratch
     constexpr int NT = w2_ntiles(G);
-    float* Wo = X + G * kRows;                                   // [8 NT][132] second layer: rows n, features i
-    __nv_bfloat16* Zs = reinterpret_cast<__nv_bfloat16*>(Wo + NT * 8 * kWoStride);   // [8 NT][M + 8] its operand
-    float* Wc = reinterpret_cast<float*>(Zs + NT * 8 * (M + 8)); // [G][n_chunks] merge weights
-    float* ML = Wc + G * kMaxMergeChunks;                        // [G][2] W and L of the merge (16 floats)
-    int* HitRow = (int*)(ML + 16);                               // compacted residual rows of the chunk's slots
-    int* HitSlot = HitRow + kRows;                               // ... and those slots, ascending
-    float* redM = (float*)(HitSlot + kRows);                     // [4 slot quarters][8] partial max
-    float* redL = redM + 32;                                     // [4][8] partial sums
-    int* hcount = (int*)(redL + 32);                             // [4] residual hits per slot quarter
-    uint64_t* fullF = (uint64_t*)(((uintptr_t)(hcount + 4) + 7) & ~(uintptr_t)7);   // streamed F chunk landed
+    uint64_t* fullF = (uint64_t*)(((uintptr_t)(epi + 2 * team_words(M, G)) + 7) & ~(uintptr_t)7);   // streamed F
+                                                                                                  // chunk landed
     uint64_t* fullC = fullF + kMaxStages;        // the 128 gathering threads' rows of the stage landed
     uint64_t* empty = fullC + kMaxStages;        // the MMAs are done with the stage
-    uint64_t* f_full = empty + kMaxStages;       // resident F_h landed
-    uint64_t* f_empty = f_full + 1;              // the MMAs are done with the resident F_h
-    uint64_t* t_full = f_empty + 1;              // [2] accumulator ready
+    uint64_t* f_full = empty + kMaxStages;       // resident F_h landed ([kFStage]: a staging buffer landed)
+    uint64_t* f_empty = f_full + kFStage;        // the MMAs are done with the resident F_h ([kFStage]: in TMEM)
+    uint64_t* t_full = f_empty + kFStage;        // [2] accumulator ready
     uint64_t* t_empty = t_full + 2;              // [2] epilogue done reading the accumulator
     uint64_t* m_drain = t_empty + 2;
-    uint64_t* rec_done = m_drain + 1;            // [2] the item's record is written (one arrival, epilogue)
-    uint64_t* tick = rec_done + 2;               // [2] the helper lane took the item's merge ticket
-    uint32_t* tmem_slot = (uint32_t*)(tick + 2);
+    uint64_t* rec_done = m_drain + 1;            // [4] item j's record is written (slot j % 4, one arrival)
+    uint64_t* tick = rec_done + 4;               // [4] the helper lane took item j's merge ticket
+    uint32_t* tmem_slot = (uint32_t*)(tick + 4);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-    volatile int* last_flag = (volatile int*)(tmem_slot + 2);   // [2] the ticket was the (b, h)'s last
-    if (layout_overflows(smem_raw, (const void*)(last_flag + 2), p.check)) return;
+    volatile int* last_flag = (volatile int*)(tmem_slot + 2);   // [4] the ticket was the (b, h)'s last
+    if (layout_overflows(smem_raw, (const void*)(last_flag + 4), p.check)) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int it_begin = (int)((int64_t)blockIdx.x * p.n_items / gridDim.x);
@@ -211,14 +206,16 @@ __global__ void __launch_bounds__(kVThreads, 1)
             mbar_init(&fullC[s], kGat);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(f_full, 1);
-        mbar_init(f_empty, 1);
+        for (int i = 0; i < kFStage; ++i) {
+            mbar_init(&f_full[i], 1);
+            mbar_init(&f_empty[i], 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&t_full[i], 1);
-            mbar_init(&t_empty[i], kEpi);
+            mbar_init(&t_empty[i], kTeam);
         }
         mbar_init(m_drain, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&rec_done[i], 1);
             mbar_init(&tick[i], 1);
             last_flag[i] = 0;
@@ -237,168 +234,187 @@ __global__ void __launch_bounds__(kVThreads, 1)
     const uint32_t tmem = *tmem_slot;
     grid_dep_wait();     // selection, residual rows, folded weights and logits come from the kernels before
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ TMA: F_h
-        if (lane == 0) {
-            int n_seg = 0, cur_fh = -1;                 // resident: kv-head segments loaded
-            uint32_t issued = 0;                        // streamed: stages issued
-            for (int j = 0; j < n_local && !*abort_flag; ++j) {
-                const int fh = item_fh(it_begin + j);
-                if (fres) {
-                    if (fh == cur_fh) continue;
-                    // the MMAs of the previous segment are done with F before it is overwritten
-                    if (n_seg > 0 && !mbar_wait_lim(f_empty, (n_seg - 1) & 1, abort_flag, p.wait_cycles)) break;
-                    mbar_expect_tx(f_full, (uint32_t)KC * kFChunk);
-                    for (int kc = 0; kc < KC; ++kc)
-#pragma unroll
-                        for (int mb = 0; mb < MB; ++mb)
-                            tma_load_2d(Fres + kc * kFChunk + mb * 16384, &tmF, f_full, kc * 64, fh * M + mb * 128);
-                    cur_fh = fh;
-                    ++n_seg;
-                } else {
-                    bool ok = true;
-                    for (int kc = 0; kc < KC; ++kc, ++issued) {
-                        const uint32_t s = issued % NS, n = issued / NS;
-                        if (!mbar_wait_lim(&empty[s], (n & 1) ^ 1, abort_flag, p.wait_cycles)) {
-                            ok = false;
-                            break;
+    if (warp < 8) {
+        // warpgroups 0-1 drop to 56 registers a thread so that warpgroups 2-3 can rise to 200
+        // (256 x 56 + 256 x 200 = 512 x 128, the registers the CTA was launched with)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+        if (warp == 0) {
+            // ------------------------------------------------------------------ TMA: F_h
+            if (lane == 0) {
+                int n_seg = 0, cur_fh = -1;                 // resident: kv-head segments loaded
+                uint32_t issued = 0;                        // streamed: stages issued; TMEM mode: chunks staged
+                for (int j = 0; j < n_local && !*abort_flag; ++j) {
+                    const int fh = item_fh(it_begin + j);
+                    if (ftm) {
+                        // TMEM mode: the segment's KC chunks through the staging buffers, each reused once the MMA
+                        // thread has copied what it held into TMEM
+                        if (fh == cur_fh) continue;
+                        bool ok = true;
+                        for (int kc = 0; kc < KC; ++kc, ++issued) {
+                            const uint32_t fb = issued % kFStage, n = issued / kFStage;
+                            if (!mbar_wait_lim(&f_empty[fb], (n & 1) ^ 1, abort_flag, p.wait_cycles)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_expect_tx(&f_full[fb], kFChunk);
+                            tma_load_2d(Fres + fb * kFChunk, &tmF, &f_full[fb], kc * 64, fh * M);
                         }
-                        mbar_expect_tx(&fullF[s], kFChunk);
+                        if (!ok) break;
+                        cur_fh = fh;
+                    } else if (fres) {
+                        if (fh == cur_fh) continue;
+                        // the MMAs of the previous segment are done with F before it is overwritten
+                        if (n_seg > 0 && !mbar_wait_lim(f_empty, (n_seg - 1) & 1, abort_flag, p.wait_cycles)) break;
+                        mbar_expect_tx(f_full, (uint32_t)KC * kFChunk);
+                        for (int kc = 0; kc < KC; ++kc)
 #pragma unroll
-                        for (int mb = 0; mb < MB; ++mb)
-                            tma_load_2d(ring + s * kStage + kCBytes + mb * 16384, &tmF, &fullF[s], kc * 64,
-                                        fh * M + mb * 128);
+                            for (int mb = 0; mb < MB; ++mb)
+                                tma_load_2d(Fres + kc * kFChunk + mb * 16384, &tmF, f_full, kc * 64, fh * M + mb * 128);
+                        cur_fh = fh;
+                        ++n_seg;
+                    } else {
+                        bool ok = true;
+                        for (int kc = 0; kc < KC; ++kc, ++issued) {
+                            const uint32_t s = issued % NS, n = issued / NS;
+                            if (!mbar_wait_lim(&empty[s], (n & 1) ^ 1, abort_flag, p.wait_cycles)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_expect_tx(&fullF[s], kFChunk);
+#pragma unroll
+                            for (int mb = 0; mb < MB; ++mb)
+                                tma_load_2d(ring + s * kStage + kCBytes + mb * 16384, &tmF, &fullF[s], kc * 64,
+                                            fh * M + mb * 128);
+                        }
+                        if (!ok) break;
                     }
-                    if (!ok) break;
+                }
+                if (*abort_flag) {   // copies issued complete before the CTA frees its shared memory
+                    if (ftm)
+                        for (uint32_t k = issued > (uint32_t)kFStage ? issued - kFStage : 0; k < issued; ++k)
+                            mbar_wait_drain(&f_full[k % kFStage], (k / kFStage) & 1);
+                    else if (fres && n_seg > 0)
+                        mbar_wait_drain(f_full, (n_seg - 1) & 1);
+                    else if (!fres)
+                        for (uint32_t k = issued > (uint32_t)NS ? issued - NS : 0; k < issued; ++k)
+                            mbar_wait_drain(&fullF[k % NS], (k / NS) & 1);
+                }
+            } else if (lane == 1 && p.cnt) {
+                // ------------------------------------------------------------------ merge tickets
+                // once an item's record is written (the epilogue's writes ordered before rec_done at CTA scope, then
+                // made visible device-wide by this lane's fence), count the chunk for its (b, h); the count that
+                // completes the (b, h) tells the epilogue to merge it.  The epilogue waits for the ticket one item
+                // later, so the atomic's round trip overlaps the next item.
+                for (int j = 0; j < n_local; ++j) {
+                    if (!mbar_wait_lim(&rec_done[j & 3], (j >> 2) & 1, abort_flag, p.wait_cycles)) break;
+                    int h, b, c;
+                    item_hbc(it_begin + j, h, b, c);
+                    __threadfence();
+                    last_flag[j & 3] = (atomicAdd(p.cnt + (int64_t)b * p.H_kv + h, 1) == p.n_chunks - 1) ? 1 : 0;
+                    mbar_arrive(&tick[j & 3]);
                 }
             }
-            if (*abort_flag) {   // copies issued complete before the CTA frees its shared memory
-                if (fres && n_seg > 0) mbar_wait_drain(f_full, (n_seg - 1) & 1);
-                if (!fres)
-                    for (uint32_t k = issued > (uint32_t)NS ? issued - NS : 0; k < issued; ++k)
-                        mbar_wait_drain(&fullF[k % NS], (k / NS) & 1);
-            }
-        } else if (lane == 1 && p.cnt) {
-            // ------------------------------------------------------------------ merge tickets
-            // once an item's record is written (the epilogue's writes ordered before rec_done at CTA scope, then
-            // made visible device-wide by this lane's fence), count the chunk for its (b, h); the count that
-            // completes the (b, h) tells the epilogue to merge it.  The epilogue waits for the ticket one item
-            // later, so the atomic's round trip overlaps the next item.
-            for (int j = 0; j < n_local; ++j) {
-                if (!mbar_wait_lim(&rec_done[j & 1], (j >> 1) & 1, abort_flag, p.wait_cycles)) break;
-                int h, b, c;
-                item_hbc(it_begin + j, h, b, c);
-                __threadfence();
-                last_flag[j & 1] = (atomicAdd(p.cnt + (int64_t)b * p.H_kv + h, 1) == p.n_chunks - 1) ? 1 : 0;
-                mbar_arrive(&tick[j & 1]);
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            bool ok = true;
-            int n_seg = 0, cur_fh = -1, n_drain = 0;
-            uint32_t g = 0;                                      // stages consumed
-            for (int j = 0; j < n_local && ok; ++j) {
-                const int fh = item_fh(it_begin + j);
-                if (fres && fh != cur_fh) {
-                    if (!mbar_wait_lim(f_full, n_seg & 1, abort_flag, p.wait_cycles)) break;
-                    if (ftm && n_seg > 0) {
-                        // the MMAs of the kv-head before still read its F_h from TMEM: let them finish first (a copy
-                        // is not ordered after earlier MMAs)
-                        mma_commit(m_drain);
-                        if (!mbar_wait_lim(m_drain, n_drain & 1, abort_flag, p.wait_cycles)) break;
-                        ++n_drain;
-                    }
-                    cur_fh = fh;
-                    ++n_seg;
-                    if (ftm) {
-                        // F_h into TMEM columns [2M, 2M + r/2): k-chunk kc at column 32 kc, 8 columns per 16 k-values;
-                        // the shared copy is free once the copies have read it
-                        fence_after();
-                        for (int kc = 0; kc < KC; ++kc)
+        } else if (warp == 1) {
+            // ------------------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                bool ok = true;
+                int n_seg = 0, cur_fh = -1, n_drain = 0;
+                uint32_t n_fst = 0;                                  // TMEM mode: staged F chunks copied
+                uint32_t g = 0;                                      // stages consumed
+                for (int j = 0; j < n_local && ok; ++j) {
+                    const int fh = item_fh(it_begin + j);
+                    if ((fres || ftm) && fh != cur_fh) {
+                        if (fres && !mbar_wait_lim(f_full, n_seg & 1, abort_flag, p.wait_cycles)) break;
+                        if (ftm && n_seg > 0) {
+                            // the MMAs of the kv-head before still read its F_h from TMEM: let them finish first (a copy
+                            // is not ordered after earlier MMAs)
+                            mma_commit(m_drain);
+                            if (!mbar_wait_lim(m_drain, n_drain & 1, abort_flag, p.wait_cycles)) break;
+                            ++n_drain;
+                        }
+                        cur_fh = fh;
+                        ++n_seg;
+                        // TMEM mode: F_h into TMEM columns [2M, 2M + r/2), k-chunk kc at column 32 kc, 8 columns per
+                        // 16 k-values, from the staging buffers (each freed once its copies have read it)
+                        for (int kc = 0; ftm && kc < KC; ++kc, ++n_fst) {
+                            const uint32_t fb = n_fst % kFStage;
+                            if (!mbar_wait_lim(&f_full[fb], (n_fst / kFStage) & 1, abort_flag, p.wait_cycles)) {
+                                ok = false;
+                                break;
+                            }
+                            fence_after();
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 tmem_cp_128x256b(tmem + 2 * M + kc * 32 + k * 8,
-                                                 sdesc_sw128(smem_u32(Fres + kc * kFChunk) + k * 32));
-                        mma_commit(f_empty);
+                                                 sdesc_sw128(smem_u32(Fres + fb * kFChunk) + k * 32));
+                            mma_commit(&f_empty[fb]);
+                        }
+                        if (!ok) break;
                     }
-                }
-                const uint32_t buf = j & 1;
-                if (!mbar_wait_lim(&t_empty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.wait_cycles)) break;
-                fence_after();
-                for (int kc = 0; kc < KC; ++kc, ++g) {
-                    const uint32_t s = g % NS, par = (g / NS) & 1;
-                    if (!mbar_wait_lim(&fullC[s], par, abort_flag, p.wait_cycles) ||
-                        (!fres && !mbar_wait_lim(&fullF[s], par, abort_flag, p.wait_cycles))) {
-                        ok = false;
-                        break;
-                    }
+                    const uint32_t buf = j & 1;
+                    if (!mbar_wait_lim(&t_empty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.wait_cycles)) break;
                     fence_after();
-                    const uint32_t c_addr = smem_u32(ring + s * kStage);
-                    if (ftm) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_bf16_ts(tmem + buf * M, tmem + 2 * M + kc * 32 + k * 8, sdesc_sw128(c_addr + k * 32),
-                                        p.idesc, (kc | k) != 0);
-                    } else {
-                        const uint32_t f_addr = fres ? smem_u32(Fres + kc * kFChunk) : c_addr + kCBytes;
-#pragma unroll
-                        for (int mb = 0; mb < MB; ++mb)
+                    for (int kc = 0; kc < KC; ++kc, ++g) {
+                        const uint32_t s = g % NS, par = (g / NS) & 1;
+                        if (!mbar_wait_lim(&fullC[s], par, abort_flag, p.wait_cycles) ||
+                            (!fres && !ftm && !mbar_wait_lim(&fullF[s], par, abort_flag, p.wait_cycles))) {
+                            ok = false;
+                            break;
+                        }
+                        // the gatherers' cp.async bytes (generic proxy) before the MMAs' reads (async proxy)
+                        fence_proxy_async();
+                        fence_after();
+                        const uint32_t c_addr = smem_u32(ring + s * kStage);
+                        if (ftm) {
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                mma_bf16(tmem + buf * M + mb * 128, sdesc_sw128(f_addr + mb * 16384 + k * 32),
-                                         sdesc_sw128(c_addr + k * 32), p.idesc, (kc | k) != 0);
-                    }
-                    mma_commit(&empty[s]);
-                }
-                if (!ok) break;
-                mma_commit(&t_full[buf]);
-                // the last item of a kv-head segment: its MMAs release the resident F_h (with the TMEM copy, the
-                // copy released it already)
-                if (fres && !ftm && (j + 1 == n_local || item_fh(it_begin + j + 1) != fh)) mma_commit(f_empty);
-            }
-            // every MMA issued completes before TMEM is released or shared memory is reused
-            mma_commit(m_drain);
-            mbar_wait_drain(m_drain, n_drain & 1);
-        }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------------ gather (128 threads)
-        // thread gt copies the 16-byte piece c16 of rows rsub + 8 rr (rr < 16) of every k-chunk; a padding slot
-        // re-reads its sequence's token 0 (its softmax weight is 0)
-        const int gt = threadIdx.x - 64, c16 = gt & 7, rsub = gt >> 3;
-        const uint32_t total = (uint32_t)n_local * KC;
-        uint32_t issued = 0, published = 0;
-        const __nv_bfloat16* srow[kGatRows];
-        int nsel[kGatRows];   // the next item's selected tokens, loaded an item ahead
-        auto load_sel = [&](int jl) {
-            int h, b, c;
-            item_hbc(it_begin + jl, h, b, c);
-            const int64_t bh = (int64_t)b * p.H_kv + h;
+                                mma_bf16_ts(tmem + buf * M, tmem + 2 * M + kc * 32 + k * 8, sdesc_sw128(c_addr + k * 32),
+                                            p.idesc, (kc | k) != 0);
+                        } else {
+                            const uint32_t f_addr = fres ? smem_u32(Fres + kc * kFChunk) : c_addr + kCBytes;
 #pragma unroll
-            for (int rr = 0; rr < kGatRows; ++rr) {
-                const int jr = c * kRows + rr * (kGat / 8) + rsub;
-                nsel[rr] = jr < p.S_eff ? __ldg(p.sel + bh * p.S_eff + jr) : 0;
-            }
-        };
-        if (n_local > 0) load_sel(0);
-        bool gok = true;
-        // the oldest stage in flight has landed: make it visible to the tensor cores and publish it
-        auto publish = [&]() {
-            cp_async_wait_pending((int)(issued - published) - 1);
-            fence_proxy_async();
-            if (gok) mbar_arrive(&fullC[published % NS]);
-            ++published;
-        };
-        while (published < total) {
-            if (gok && issued < total && issued - published < (uint32_t)NS) {
-                const uint32_t s = issued % NS, n = issued / NS;
-                // the slot frees when the MMAs of its previous round are done; until then publish what has landed
-                // (a stage waiting behind this slot must not hold up the MMAs that would free it)
-                if (n > 0 && published < issued && !mbar_test_wait(&empty[s], (n & 1) ^ 1)) {
-                    publish();
-                    continue;
+                            for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    mma_bf16(tmem + buf * M + mb * 128, sdesc_sw128(f_addr + mb * 16384 + k * 32),
+                                             sdesc_sw128(c_addr + k * 32), p.idesc, (kc | k) != 0);
+                        }
+                        mma_commit(&empty[s]);
+                    }
+                    if (!ok) break;
+                    mma_commit(&t_full[buf]);
+                    // the last item of a kv-head segment: its MMAs release the resident F_h
+                    if (fres && (j + 1 == n_local || item_fh(it_begin + j + 1) != fh)) mma_commit(f_empty);
                 }
+                // every MMA issued completes before TMEM is released or shared memory is reused
+                mma_commit(m_drain);
+                mbar_wait_drain(m_drain, n_drain & 1);
+            }
+        } else if (warp < 4) {
+            // warps 2-3 idle
+        } else if (warp < 8) {
+            // ------------------------------------------------------------------ gather (128 threads)
+            // thread gt copies the 16-byte piece c16 of rows rsub + 16 rr (rr < 8) of every k-chunk; a padding slot
+            // re-reads its sequence's token 0 (its softmax weight is 0).  The copies of a stage arrive on its full
+            // barrier by themselves once they land (one arrival per thread), so the warps never wait for a copy:
+            // they run ahead as far as the ring's free slots allow.
+            const int gt = threadIdx.x - 128, c16 = gt & 7, rsub = gt >> 3;
+            const uint32_t total = (uint32_t)n_local * KC;
+            const __nv_bfloat16* srow[kGatRows];
+            int nsel[kGatRows];   // the next item's selected tokens, loaded an item ahead
+            auto load_sel = [&](int jl) {
+                int h, b, c;
+                item_hbc(it_begin + jl, h, b, c);
+                const int64_t bh = (int64_t)b * p.H_kv + h;
+#pragma unroll
+                for (int rr = 0; rr < kGatRows; ++rr) {
+                    const int jr = c * kRows + rr * (kGat / 8) + rsub;
+                    nsel[rr] = jr < p.S_eff ? __ldg(p.sel + bh * p.S_eff + jr) : 0;
+                }
+            };
+            if (n_local > 0) load_sel(0);
+            for (uint32_t issued = 0; issued < total; ++issued) {
+                const uint32_t s = issued % NS, n = issued / NS;
                 const int kc = (int)(issued % KC);
                 if (kc == 0) {   // the item's rows; then the next item's tokens
                     const int jl = (int)(issued / KC);
@@ -411,62 +427,67 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     }
                     if (jl + 1 < n_local) load_sel(jl + 1);
                 }
-                if (!mbar_wait_lim(&empty[s], (n & 1) ^ 1, abort_flag, p.wait_cycles)) {
-                    gok = false;
-                    continue;
-                }
+                // the slot frees when the MMAs of its previous round are done
+                if (!mbar_wait_lim(&empty[s], (n & 1) ^ 1, abort_flag, p.wait_cycles)) break;
                 const uint32_t A = smem_u32(ring + s * kStage);
 #pragma unroll
                 for (int rr = 0; rr < kGatRows; ++rr) {
                     const int row = rr * (kGat / 8) + rsub;
                     cp_async_16(A + row * 128 + ((c16 ^ (row & 7)) << 4), srow[rr] + kc * 64, 16u);
                 }
-                cp_async_commit();
-                ++issued;
-            } else if (published < issued) {
-                publish();
-            } else {
-                break;   // aborted with nothing in flight
+                cp_async_mbar_arrive(&fullC[s]);
             }
+            cp_async_wait<0>();
         }
-        cp_async_wait<0>();
     } else {
-        // ------------------------------------------------------------------ epilogue (256 threads)
-        const int et = threadIdx.x - 128;
-        const int slot = et & (kRows - 1), jh = et >> 7;         // jh: which half of the work this thread takes
-        const int sq = slot >> 5;                                 // slot quarter (warp within its half)
-        const int q = warp & 3, ch = (warp - 4) >> 2;            // TMEM lane quarter, token half
-        const int i_out = slot;
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+        // ------------------------------------------------------------------ epilogue (two teams of 128 threads)
+        // Team tm (warps 8 + 4 tm .. 11 + 4 tm) takes the items j = tm, tm + 2, ... and TMEM buffer tm, with its
+        // own scratch and named barrier, so that one team's barrier and load waits overlap the other's arithmetic.
+        // Thread et of a team: token slot et for the softmax, hidden unit 32 q + lane (its TMEM lane) for the
+        // hidden layer, output feature et for the residual rows and the record.
+        const int tm = (warp - 8) >> 2, et = threadIdx.x - 256 - kTeam * tm;
+        const int q = warp & 3;                      // TMEM lane quarter = slot quarter of the softmax
+        const int slot = et, i_out = et;
+        float* Ps = epi + (size_t)tm * team_words(M, G);        // [G][128] softmax weights (0 on padding slots)
+        float* Z = Ps + G * kRows;                               // [G][M] hidden sums
+        float* Wo = Z + G * M;                                   // [8 NT][132] second layer: rows n, features i
+        __nv_bfloat16* Zs = reinterpret_cast<__nv_bfloat16*>(Wo + NT * 8 * kWoStride);   // [8 NT][M + 8] its operand
+        float* Wc = reinterpret_cast<float*>(Zs + NT * 8 * (M + 8));   // [G][n_chunks] merge weights
+        float* ML = Wc + G * kMaxMergeChunks;                    // [G][2] W and L of the merge (16 floats)
+        int* HitRow = (int*)(ML + 16);                           // compacted residual rows of the chunk's slots
+        int* HitSlot = HitRow + kRows;                           // ... and those slots, ascending
+        float* redM = (float*)(HitSlot + kRows);                 // [4 slot quarters][8] partial max
+        float* redL = redM + 32;                                 // [4][8] partial sums
+        int* hcount = (int*)(redL + 32);                         // [4] residual hits per slot quarter
+        auto team_sync = [&]() { named_bar_sync(1 + tm, kTeam); };
         auto chunk_max = [&](int jq) {
             return fmaxf(fmaxf(redM[jq], redM[8 + jq]), fmaxf(redM[16 + jq], redM[24 + jq]));
         };
         auto chunk_sum = [&](int jq) { return (redL[jq] + redL[8 + jq]) + (redL[16 + jq] + redL[24 + jq]); };
         const int64_t rw = 128 + 2;
         const int64_t qstride = (int64_t)p.n_chunks * rw;
-        constexpr int SV = (G + 1) / 2;
-        // this slot's selection data of an item, fetched an item ahead in two steps so that no load waits on the
-        // critical path: the token and its residual row when the item before starts, then (once the token has
-        // landed) the scaled logits of q-heads jh, jh + 2, ...
+        // this slot's selection data of an item, fetched a team item ahead in two steps so that no load waits on
+        // the critical path: the token and its residual row when the item before starts, then (once the token
+        // has landed) the scaled logits of the G q-heads
         auto fetch_sel = [&](int it, int& tok, int& hit) {
             int h, b, c;
             item_hbc(it, h, b, c);
             const int64_t bh = (int64_t)b * p.H_kv + h;
             const int jsel = c * kRows + slot;
             const bool valid = jsel < p.S_eff;
-            tok = valid ? __ldg(p.sel + bh * p.S_eff + jsel) : -1;
-            hit = (valid && p.hit) ? __ldg(p.hit + bh * p.S_eff + jsel) : -1;
+            tok = valid ? ldg_pin_s32(p.sel + bh * p.S_eff + jsel) : -1;
+            hit = (valid && p.hit) ? ldg_pin_s32(p.hit + bh * p.S_eff + jsel) : -1;
         };
-        auto fetch_logits = [&](int it, int& tok, float (&sv)[SV]) {
+        auto fetch_logits = [&](int it, int& tok, float (&sv)[G]) {
             int h, b, c;
             item_hbc(it, h, b, c);
             if (tok >= p.T) tok = p.T - 1;   // the selection is always in range; keep the invariant explicit
 #pragma unroll
-            for (int u = 0; u < SV; ++u) {
-                const int jq = jh + 2 * u;
-                sv[u] = (jq < G && tok >= 0) ? __ldg(p.sall + ((int64_t)b * p.H_q + h * G + jq) * p.T + tok) : -INFINITY;
-            }
+            for (int jq = 0; jq < G; ++jq)
+                sv[jq] = tok >= 0 ? ldg_pin_f32(p.sall + ((int64_t)b * p.H_q + h * G + jq) * p.T + tok) : -INFINITY;
         };
-        // merge of (b, h) by the CTA that finished its last chunk: the records of its chunks, read through L2
+        // merge of (b, h) by the team that finished its last chunk: the records of its chunks, read through L2
         auto merge = [&](int h, int b) {
             const int64_t bh = (int64_t)b * p.H_kv + h;
             __threadfence();
@@ -501,10 +522,9 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 ML[et * 2] = mx;
                 ML[et * 2 + 1] = l;
             }
-            named_bar_sync(1, kEpi);
-            for (int e = et; e < G * 128; e += kEpi) {
-                const int jq = e >> 7, i = e & 127;
-                const float* Pq = P0 + jq * qstride + i;
+            team_sync();
+            for (int jq = 0; jq < G; ++jq) {
+                const float* Pq = P0 + jq * qstride + i_out;
                 float a = 0.0f;
                 for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
                     float v[8];
@@ -515,135 +535,134 @@ __global__ void __launch_bounds__(kVThreads, 1)
                         if (c0 + u < p.n_chunks) a = fmaf(Wc[jq * kMaxMergeChunks + c0 + u], v[u], a);
                 }
                 const float L = ML[jq * 2 + 1];
-                p.out[((int64_t)b * p.H_q + h * G + jq) * 128 + i] = L > 0.0f ? a / L : 0.0f;
+                p.out[((int64_t)b * p.H_q + h * G + jq) * 128 + i_out] = L > 0.0f ? a / L : 0.0f;
             }
             if (p.lse && et < G) {
                 const float L = ML[et * 2 + 1];
                 p.lse[(int64_t)b * p.H_q + h * G + et] = L > 0.0f ? ML[et * 2] + logf(L) : -INFINITY;
             }
             if (et == 0) p.cnt[bh] = 0;
-            named_bar_sync(1, kEpi);   // Wc and ML are free again
+            team_sync();   // Wc and ML are free again
         };
         // the ticket of item jp (taken by the helper lane): merge its (b, h) when this CTA finished it last
         auto settle = [&](int jp) {
-            const bool ok = mbar_wait_lim(&tick[jp & 1], (jp >> 1) & 1, abort_flag, p.wait_cycles);
-            if (ok && last_flag[jp & 1]) {
+            const bool ok = mbar_wait_lim(&tick[jp & 3], (jp >> 2) & 1, abort_flag, p.wait_cycles);
+            if (ok && last_flag[jp & 3]) {
                 int h, b, c;
                 item_hbc(it_begin + jp, h, b, c);
                 merge(h, b);
             }
         };
 
-        // The second layer on warp MMAs: warp ew = warp - 4 makes output features [16 ew, 16 ew + 16) of every
-        // q-head, W[i][n] = sum_k w2[i][k] Zs[n][k], from its w2 rows in m16n8k16 A fragments.  With M = 128 the
-        // fragments stay in registers while the items' kv-head (and, with a predictor per sequence, sequence)
-        // stays; with M = 256 they are loaded per item.
+        // The second layer on warp MMAs: warp q of the team makes output features [32 q, 32 q + 32) of every
+        // q-head (two m16 tiles), W[i][n] = sum_k w2[i][k] Zs[n][k], from its w2 rows in m16n8k16 A fragments.
+        // With M = 128 the fragments stay in registers while the items' kv-head (and, with a predictor per
+        // sequence, sequence) stays; with M = 256 they are loaded per item and tile.
         constexpr int KB = M / 16;
-        const int ew = warp - 4, fg = lane >> 2, ft = lane & 3;
-        uint32_t af[KB][4];
-        auto load_af = [&](int h, int b) {
-            const __nv_bfloat16* w = p.w2 + b * p.mlp_stride + ((int64_t)h * 128 + 16 * ew + fg) * M + 2 * ft;
+        constexpr int AT = M == 128 ? 2 : 1;                      // m16 tiles held at once
+        const int fg = lane >> 2, ft = lane & 3;
+        uint32_t af[AT][KB][4];
+        auto load_af = [&](int h, int b, int mt, uint32_t (&a)[KB][4]) {
+            const __nv_bfloat16* w = p.w2 + b * p.mlp_stride + ((int64_t)h * 128 + 32 * q + 16 * mt + fg) * M + 2 * ft;
 #pragma unroll
             for (int kb = 0; kb < KB; ++kb) {
-                af[kb][0] = __ldg(reinterpret_cast<const uint32_t*>(w + kb * 16));
-                af[kb][1] = __ldg(reinterpret_cast<const uint32_t*>(w + 8 * M + kb * 16));
-                af[kb][2] = __ldg(reinterpret_cast<const uint32_t*>(w + kb * 16 + 8));
-                af[kb][3] = __ldg(reinterpret_cast<const uint32_t*>(w + 8 * M + kb * 16 + 8));
+                a[kb][0] = __ldg(reinterpret_cast<const uint32_t*>(w + kb * 16));
+                a[kb][1] = __ldg(reinterpret_cast<const uint32_t*>(w + 8 * M + kb * 16));
+                a[kb][2] = __ldg(reinterpret_cast<const uint32_t*>(w + kb * 16 + 8));
+                a[kb][3] = __ldg(reinterpret_cast<const uint32_t*>(w + 8 * M + kb * 16 + 8));
             }
         };
         int w2_key = -1;
         int nx_tok = -1, nx_hit = -1;
-        float nx_sv[SV];
-        if (n_local > 0) {
-            fetch_sel(it_begin, nx_tok, nx_hit);
-            fetch_logits(it_begin, nx_tok, nx_sv);
+        float nx_sv[G];
+        if (tm < n_local) {
+            fetch_sel(it_begin + tm, nx_tok, nx_hit);
+            fetch_logits(it_begin + tm, nx_tok, nx_sv);
         }
-        for (int j = 0; j < n_local; ++j) {
+        for (int j = tm; j < n_local; j += 2) {
             int h, b, chunk;
             item_hbc(it_begin + j, h, b, chunk);
             const int64_t bh = (int64_t)b * p.H_kv + h;
             const int64_t bias_bh = p.mlp_stride ? bh : h;
-            const int tok = nx_tok, my_hit = nx_hit;
-            float sv[SV];
+            const int my_hit = nx_hit;
+            float sv[G];
 #pragma unroll
-            for (int u = 0; u < SV; ++u) sv[u] = nx_sv[u];
-            (void)tok;
-            if (j + 1 < n_local) fetch_sel(it_begin + j + 1, nx_tok, nx_hit);
+            for (int jq = 0; jq < G; ++jq) sv[jq] = nx_sv[jq];
+            if (j + 2 < n_local) fetch_sel(it_begin + j + 2, nx_tok, nx_hit);
             if (M == 128) {
                 const int key = p.mlp_stride ? (int)bh : h;
                 if (key != w2_key) {
                     w2_key = key;
-                    load_af(h, b);
+#pragma unroll
+                    for (int mt = 0; mt < AT; ++mt) load_af(h, b, mt, af[mt]);
                 }
             }
-            named_bar_sync(1, kEpi);   // the previous item's readers of Ps, Z, X, the hits and the reductions are done
+            team_sync();   // the previous item's readers of Ps, Z, the hits and the reductions are done
 #pragma unroll
-            for (int u = 0; u < SV; ++u) {
-                const int jq = jh + 2 * u;
-                const float mx = warp_max(sv[u]);
-                if (lane == 0 && jq < G) redM[sq * 8 + jq] = mx;
+            for (int jq = 0; jq < G; ++jq) {
+                const float mx = warp_max(sv[jq]);
+                if (lane == 0) redM[q * 8 + jq] = mx;
             }
             const unsigned hb = __ballot_sync(0xffffffffu, my_hit >= 0);
-            if (jh == 0 && lane == 0) hcount[sq] = __popc(hb);
-            named_bar_sync(1, kEpi);
+            if (lane == 0) hcount[q] = __popc(hb);
+            team_sync();
 #pragma unroll
-            for (int u = 0; u < SV; ++u) {
-                const int jq = jh + 2 * u;
-                if (jq < G) {
-                    const float mq = chunk_max(jq);
-                    const float pv = (sv[u] == -INFINITY || mq == -INFINITY) ? 0.0f : __expf(sv[u] - mq);
-                    Ps[jq * kRows + slot] = pv;
-                    const float ps = warp_sum(pv);
-                    if (lane == 0) redL[sq * 8 + jq] = ps;
-                }
+            for (int jq = 0; jq < G; ++jq) {
+                const float mq = chunk_max(jq);
+                const float pv = (sv[jq] == -INFINITY || mq == -INFINITY) ? 0.0f : __expf(sv[jq] - mq);
+                Ps[jq * kRows + slot] = pv;
+                const float ps = warp_sum(pv);
+                if (lane == 0) redL[q * 8 + jq] = ps;
             }
             int n_hit = 0;
             {
                 int before = 0;
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    before += (w < sq) ? hcount[w] : 0;
+                    before += (w < q) ? hcount[w] : 0;
                     n_hit += hcount[w];
                 }
-                if (jh == 0 && my_hit >= 0) {
+                if (my_hit >= 0) {
                     const int at = before + __popc(hb & ((1u << lane) - 1u));
                     HitRow[at] = my_hit;
                     HitSlot[at] = slot;
                 }
             }
-            named_bar_sync(1, kEpi);
+            team_sync();
 
-            // residual rows of the first 16 hits (feature i_out, hits k = jh, jh + 2, ...): loads issued now, their
-            // bits converted after the hidden units, so they land while the accumulator is read (one branch on the
-            // storage type around all eight loads: no conversion, hence no wait, between them)
-            uint32_t rr[8];
+            // residual rows of the first 16 hits (feature i_out; int8 rows with their scales): loads issued now,
+            // pinned here, their bits converted after the hidden units, so they land while the accumulator is read
+            uint32_t rr[16], rs[16];
             const int64_t rbase = bh * p.n_res;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                rr[k] = 0u;
+                rs[k] = 0u;
+            }
             if (p.res.dtype == LOWRAM_BF16) {
                 const unsigned short* rv16 = reinterpret_cast<const unsigned short*>(p.res.val);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int k = jh + 2 * u;
-                    rr[u] = k < n_hit ? (uint32_t)rv16[(rbase + HitRow[k]) * 128 + i_out] : 0u;
-                }
-            } else if (p.res.dtype == LOWRAM_INT8_VEC) {   // the rows' scales are read with the conversion
+                for (int k = 0; k < 16; ++k)
+                    if (k < n_hit) rr[k] = ldg_pin_u16(rv16 + (rbase + HitRow[k]) * 128 + i_out);
+            } else if (p.res.dtype == LOWRAM_INT8_VEC) {
                 const signed char* rv8 = reinterpret_cast<const signed char*>(p.res.val);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int k = jh + 2 * u;
-                    rr[u] = k < n_hit ? (uint32_t)(int)rv8[(rbase + HitRow[k]) * 128 + i_out] : 0u;
-                }
+                for (int k = 0; k < 16; ++k)
+                    if (k < n_hit) {
+                        const int64_t row = rbase + HitRow[k];
+                        rr[k] = (uint32_t)ldg_pin_s8(rv8 + row * 128 + i_out);
+                        rs[k] = ldg_pin_u16(p.res.scale + row);
+                    }
             } else {
                 const uint32_t* rv32 = reinterpret_cast<const uint32_t*>(p.res.val);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int k = jh + 2 * u;
-                    rr[u] = k < n_hit ? rv32[(rbase + HitRow[k]) * 128 + i_out] : 0u;
-                }
+                for (int k = 0; k < 16; ++k)
+                    if (k < n_hit) rr[k] = ldg_pin_u32(rv32 + (rbase + HitRow[k]) * 128 + i_out);
             }
 
-            // hidden units: thread = hidden unit jj of each 128-block, tokens of half ch;
-            // z[jq] = sum over the half's tokens of p[jq, t] SiLU(D[jj, t] + b1[jj])
-            const uint32_t buf = j & 1;
+            // hidden units: thread = hidden unit jj of each 128-block, all 128 tokens;
+            // z[jq] = sum over the tokens of p[jq, t] SiLU(D[jj, t] + b1[jj])
+            const uint32_t buf = (uint32_t)tm;
             const bool have = mbar_wait_lim(&t_full[buf], (j >> 1) & 1, abort_flag, p.wait_cycles);
             if (have) {
                 fence_after();
@@ -651,26 +670,32 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 for (int mb = 0; mb < MB; ++mb) {
                     const int jj = mb * 128 + q * 32 + lane;
                     const float bj = p.b1 ? __ldg(p.b1 + bias_bh * M + jj) : 0.0f;
-                    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * M + mb * 128 + ch * 64;
+                    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * M + mb * 128;
                     float z[G];
 #pragma unroll
                     for (int jq = 0; jq < G; ++jq) z[jq] = 0.0f;
+                    constexpr int XG = G >= 7 ? 1 : 2;               // 32-column groups per TMEM wait (registers)
 #pragma unroll 1
-                    for (int cg = 0; cg < 4; cg += 2) {        // 32 token columns per TMEM wait
-                        float xv[4][8];
-                        tmem_ld_4x8(taddr + cg * 16, taddr + cg * 16 + 8, taddr + cg * 16 + 16, taddr + cg * 16 + 24,
-                                    xv[0], xv[1], xv[2], xv[3]);
-                        const float* pc = Ps + ch * 64 + cg * 16;
+                    for (int c0 = 0; c0 < kRows; c0 += 32 * XG) {
+                        float xv[XG][32];
+                        if constexpr (XG == 2) {
+                            tmem_ld_2x32(taddr + c0, taddr + c0 + 32, xv[0], xv[XG - 1]);
+                        } else {
+                            float (&x8)[4][8] = *reinterpret_cast<float (*)[4][8]>(&xv[0][0]);
+                            tmem_ld_4x8(taddr + c0, taddr + c0 + 8, taddr + c0 + 16, taddr + c0 + 24, x8[0], x8[1], x8[2],
+                                        x8[3]);
+                        }
+                        const float* pc = Ps + c0;
 #pragma unroll
-                        for (int g8 = 0; g8 < 4; ++g8) {
+                        for (int g = 0; g < XG; ++g) {
 #pragma unroll
-                            for (int t4 = 0; t4 < 8; t4 += 4) {
+                            for (int t4 = 0; t4 < 32; t4 += 4) {
                                 float hv[4];
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) hv[u] = silu_tanh(xv[g8][t4 + u] + bj);
+                                for (int u = 0; u < 4; ++u) hv[u] = silu_tanh(xv[g][t4 + u] + bj);
 #pragma unroll
                                 for (int jq = 0; jq < G; ++jq) {
-                                    const float4 pw = *reinterpret_cast<const float4*>(pc + jq * kRows + g8 * 8 + t4);
+                                    const float4 pw = *reinterpret_cast<const float4*>(pc + jq * kRows + g * 32 + t4);
                                     z[jq] = fmaf(pw.x, hv[0], z[jq]);
                                     z[jq] = fmaf(pw.y, hv[1], z[jq]);
                                     z[jq] = fmaf(pw.z, hv[2], z[jq]);
@@ -680,121 +705,118 @@ __global__ void __launch_bounds__(kVThreads, 1)
                         }
                     }
 #pragma unroll
-                    for (int jq = 0; jq < G; ++jq) Z[(ch * G + jq) * M + jj] = z[jq];
+                    for (int jq = 0; jq < G; ++jq) Z[jq * M + jj] = z[jq];
                 }
             }
             fence_before();
             mbar_arrive(&t_empty[buf]);   // the accumulator is read: the MMAs of item j + 2 may use it
-            if (j + 1 < n_local) fetch_logits(it_begin + j + 1, nx_tok, nx_sv);
+            if (j + 2 < n_local) fetch_logits(it_begin + j + 2, nx_tok, nx_sv);
 
             // weighted residual rows, then the second layer on the chunk's hidden sums
             float acc[G];
 #pragma unroll
             for (int jq = 0; jq < G; ++jq) acc[jq] = 0.0f;
-            float rv[8];
+            float rv[16];
             if (p.res.dtype == LOWRAM_INT8_VEC) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int k = jh + 2 * u;
-                    rv[u] = k < n_hit ? (float)(int)rr[u] * __half2float(p.res.scale[rbase + HitRow[k]]) : 0.0f;
-                }
+                for (int k = 0; k < 16; ++k) rv[k] = (float)(int)rr[k] * __half2float(__ushort_as_half((unsigned short)rs[k]));
             } else {
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    rv[u] = p.res.dtype == LOWRAM_BF16 ? __uint_as_float(rr[u] << 16) : __uint_as_float(rr[u]);
+                for (int k = 0; k < 16; ++k)
+                    rv[k] = p.res.dtype == LOWRAM_BF16 ? __uint_as_float(rr[k] << 16) : __uint_as_float(rr[k]);
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int k = jh + 2 * u;
+            for (int k = 0; k < 16; ++k) {
                 if (k < n_hit) {
                     const int t = HitSlot[k];
 #pragma unroll
-                    for (int jq = 0; jq < G; ++jq) acc[jq] = fmaf(Ps[jq * kRows + t], rv[u], acc[jq]);
+                    for (int jq = 0; jq < G; ++jq) acc[jq] = fmaf(Ps[jq * kRows + t], rv[k], acc[jq]);
                 }
             }
-            for (int k0 = jh + 16; k0 < n_hit; k0 += 16) {    // more than 16 hits in the chunk
+            for (int k0 = 16; k0 < n_hit; k0 += 8) {    // more than 16 hits in the chunk
                 float v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const int k = k0 + 2 * u;
+                    const int k = k0 + u;
                     v[u] = k < n_hit ? p.res.get(bh * p.n_res + HitRow[k], i_out) : 0.0f;
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const int k = k0 + 2 * u;
+                    const int k = k0 + u;
                     if (k >= n_hit) break;
                     const int t = HitSlot[k];
 #pragma unroll
                     for (int jq = 0; jq < G; ++jq) acc[jq] = fmaf(Ps[jq * kRows + t], v[u], acc[jq]);
                 }
             }
-            named_bar_sync(1, kEpi);   // every hidden sum is in Z
-            if (M != 128) load_af(h, b);
+            team_sync();   // every hidden sum is in Z
             if (have) {
-                // the hidden sums, both token halves added, as bf16 hi + lo: Zs[n][k] = hi(z[n][k]) for n < G,
-                // lo(z[n - G][k]) = bf16(z - hi) for G <= n < 2G (hi + lo holds z to 2^-16), 0 beyond
-                for (int e = et; e < NT * 8 * (M / 2); e += kEpi) {
+                // the hidden sums as bf16 hi + lo: Zs[n][k] = hi(z[n][k]) for n < G, lo(z[n - G][k]) =
+                // bf16(z - hi) for G <= n < 2G (hi + lo holds z to 2^-16), 0 beyond
+                for (int e = et; e < NT * 8 * (M / 2); e += kTeam) {
                     const int n = e / (M / 2), k = (e - n * (M / 2)) * 2;
                     uint32_t packed = 0u;
                     if (n < 2 * G) {
                         const int jq = n < G ? n : n - G;
-                        const float2 za = *reinterpret_cast<const float2*>(Z + jq * M + k);
-                        const float2 zb = *reinterpret_cast<const float2*>(Z + (G + jq) * M + k);
-                        const float z0 = za.x + zb.x, z1 = za.y + zb.y;
-                        __nv_bfloat162 v = __floats2bfloat162_rn(z0, z1);
+                        const float2 zz = *reinterpret_cast<const float2*>(Z + jq * M + k);
+                        __nv_bfloat162 v = __floats2bfloat162_rn(zz.x, zz.y);
                         if (n >= G) {
                             const float2 hf = __bfloat1622float2(v);
-                            v = __floats2bfloat162_rn(z0 - hf.x, z1 - hf.y);
+                            v = __floats2bfloat162_rn(zz.x - hf.x, zz.y - hf.y);
                         }
                         packed = *reinterpret_cast<const uint32_t*>(&v);
                     }
                     *reinterpret_cast<uint32_t*>(Zs + n * (M + 8) + k) = packed;
                 }
             }
-            named_bar_sync(1, kEpi);
+            team_sync();
             if (have) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    const __nv_bfloat16* zr = Zs + (nt * 8 + fg) * (M + 8) + 2 * ft;
+                for (int mt = 0; mt < 2; ++mt) {
+                    uint32_t (&a)[KB][4] = af[AT == 2 ? mt : 0];
+                    if (AT == 1) load_af(h, b, mt, a);
 #pragma unroll
-                    for (int kb = 0; kb < KB; ++kb) {
-                        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(zr + kb * 16);
-                        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(zr + kb * 16 + 8);
-                        mma_16816(d, af[kb][0], af[kb][1], af[kb][2], af[kb][3], b0, b1);
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        const __nv_bfloat16* zr = Zs + (nt * 8 + fg) * (M + 8) + 2 * ft;
+#pragma unroll
+                        for (int kb = 0; kb < KB; ++kb) {
+                            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(zr + kb * 16);
+                            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(zr + kb * 16 + 8);
+                            mma_16816(d, a[kb][0], a[kb][1], a[kb][2], a[kb][3], b0, b1);
+                        }
+                        float* wo = Wo + (nt * 8 + 2 * ft) * kWoStride + 32 * q + 16 * mt + fg;
+                        wo[0] = d[0];
+                        wo[kWoStride] = d[1];
+                        wo[8] = d[2];
+                        wo[kWoStride + 8] = d[3];
                     }
-                    float* wo = Wo + (nt * 8 + 2 * ft) * kWoStride + 16 * ew + fg;
-                    wo[0] = d[0];
-                    wo[kWoStride] = d[1];
-                    wo[8] = d[2];
-                    wo[kWoStride + 8] = d[3];
                 }
             }
-            if (jh == 1)
-#pragma unroll
-                for (int jq = 0; jq < G; ++jq) X[jq * kRows + i_out] = acc[jq];
-            named_bar_sync(1, kEpi);
+            team_sync();
             float* rec = p.partial + (((int64_t)b * p.H_q + h * G) * p.n_chunks + chunk) * rw;
-            if (jh == 0) {
-                const float bias = p.b2 ? __ldg(p.b2 + bias_bh * 128 + i_out) : 0.0f;
+            const float bias = p.b2 ? __ldg(p.b2 + bias_bh * 128 + i_out) : 0.0f;
 #pragma unroll
-                for (int jq = 0; jq < G; ++jq)
-                    rec[jq * qstride + i_out] = (acc[jq] + X[jq * kRows + i_out]) +
-                                                (Wo[jq * kWoStride + i_out] + Wo[(G + jq) * kWoStride + i_out]) +
-                                                chunk_sum(jq) * bias;
-            } else if (i_out < G) {
+            for (int jq = 0; jq < G; ++jq)
+                rec[jq * qstride + i_out] =
+                    acc[jq] + (Wo[jq * kWoStride + i_out] + Wo[(G + jq) * kWoStride + i_out]) + chunk_sum(jq) * bias;
+            if (i_out < G) {
                 rec[i_out * qstride + 128] = chunk_max(i_out);
                 rec[i_out * qstride + 129] = chunk_sum(i_out);
             }
             if (p.cnt) {
-                // the record is written: the helper lane takes this chunk's ticket while the next item starts;
-                // the ticket of the item before is settled here (merged if this CTA finished that (b, h))
-                named_bar_sync(1, kEpi);
-                if (et == 0) mbar_arrive(&rec_done[j & 1]);
-                if (j > 0) settle(j - 1);
+                // the record is written: the helper lane takes this chunk's ticket while the team's next item
+                // starts; the ticket of the team's item before is settled here (merged if this CTA finished that
+                // (b, h)); tickets rotate over four slots, so a slot is reused only after its item was settled
+                team_sync();
+                if (et == 0) mbar_arrive(&rec_done[j & 3]);
+                if (j >= 2) settle(j - 2);
             }
         }
-        if (p.cnt && n_local > 0) settle(n_local - 1);
+        if (p.cnt) {
+            const int j_last = tm + ((n_local - 1 - tm) >> 1) * 2;   // the team's last item
+            if (tm < n_local) settle(j_last);
+        }
     }
 
     // ---------------------------------------------------------------------- teardown
@@ -835,7 +857,7 @@ cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     const VregenConfig cfg = vregen_config(s.m, s.r, s.H_q / s.H_kv);
     p.NS = cfg.NS;
     p.f_resident = cfg.f_resident ? 1 : 0;
-    p.f_tmem = (cfg.f_resident && s.m == 128 && 2 * s.m + s.r / 2 <= 512) ? 1 : 0;
+    p.f_tmem = cfg.f_tmem ? 1 : 0;
     p.n_items = s.B * s.H_kv * a.n_chunks;
     const int copies = (s.basis_batch_stride || s.mlp_batch_stride) ? s.B : 1;
     p.fold_per_seq = copies > 1 ? 1 : 0;
