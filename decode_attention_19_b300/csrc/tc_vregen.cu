@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 bool ok = true;
                 int n_seg = 0, cur_fh = -1, n_drain = 0;
                 uint32_t n_fst = 0;                                  // TMEM mode: staged F chunks copied
-                uint32_t g = 0;                                      // stages consumed
+                uint32_t s = 0, par = 0;                             // ring slot and phase of the next stage
                 for (int j = 0; j < n_local && ok; ++j) {
                     const int fh = item_fh(it_begin + j);
                     if ((fres || ftm) && fh != cur_fh) {
@@ -354,8 +354,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     const uint32_t buf = j & 1;
                     if (!mbar_wait_lim(&t_empty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.wait_cycles)) break;
                     fence_after();
-                    for (int kc = 0; kc < KC; ++kc, ++g) {
-                        const uint32_t s = g % NS, par = (g / NS) & 1;
+                    for (int kc = 0; kc < KC; ++kc) {
                         if (!mbar_wait_lim(&fullC[s], par, abort_flag, p.wait_cycles) ||
                             (!fres && !ftm && !mbar_wait_lim(&fullF[s], par, abort_flag, p.wait_cycles))) {
                             ok = false;
@@ -380,6 +379,10 @@ __global__ void __launch_bounds__(kVThreads, 1)
                                              sdesc_sw128(c_addr + k * 32), p.idesc, (kc | k) != 0);
                         }
                         mma_commit(&empty[s]);
+                        if (++s == (uint32_t)NS) {
+                            s = 0;
+                            par ^= 1;
+                        }
                     }
                     if (!ok) break;
                     mma_commit(&t_full[buf]);
@@ -660,6 +663,13 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     if (k < n_hit) rr[k] = ldg_pin_u32(rv32 + (rbase + HitRow[k]) * 128 + i_out);
             }
 
+            // first- and second-layer biases of this thread's hidden units and output feature, pinned here too
+            float bjs[MB];
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb)
+                bjs[mb] = p.b1 ? ldg_pin_f32(p.b1 + bias_bh * M + mb * 128 + q * 32 + lane) : 0.0f;
+            const float bias = p.b2 ? ldg_pin_f32(p.b2 + bias_bh * 128 + i_out) : 0.0f;
+
             // hidden units: thread = hidden unit jj of each 128-block, all 128 tokens;
             // z[jq] = sum over the tokens of p[jq, t] SiLU(D[jj, t] + b1[jj])
             const uint32_t buf = (uint32_t)tm;
@@ -669,7 +679,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
 #pragma unroll 1
                 for (int mb = 0; mb < MB; ++mb) {
                     const int jj = mb * 128 + q * 32 + lane;
-                    const float bj = p.b1 ? __ldg(p.b1 + bias_bh * M + jj) : 0.0f;
+                    const float bj = bjs[mb];
                     const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * M + mb * 128;
                     float z[G];
 #pragma unroll
@@ -795,7 +805,6 @@ __global__ void __launch_bounds__(kVThreads, 1)
             }
             team_sync();
             float* rec = p.partial + (((int64_t)b * p.H_q + h * G) * p.n_chunks + chunk) * rw;
-            const float bias = p.b2 ? __ldg(p.b2 + bias_bh * 128 + i_out) : 0.0f;
 #pragma unroll
             for (int jq = 0; jq < G; ++jq)
                 rec[jq * qstride + i_out] =
