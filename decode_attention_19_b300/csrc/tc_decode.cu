@@ -447,10 +447,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
                 }
                 fence_before();
                 if (rank == 0) {
-                    mbar_arrive(&t_empty[buf]);
+                    mbar_arrive_relaxed(&t_empty[buf]);
                 } else {
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(peer_smem(&t_empty[buf], 0));
+                    if (lane == 0) mbar_arrive_remote_relaxed(peer_smem(&t_empty[buf], 0));
                 }
             }
             // this item's tile, for the stores below; then, when the next item starts a new tile of the same
