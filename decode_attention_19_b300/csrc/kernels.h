@@ -44,7 +44,7 @@ struct DecodeArgs {
     float* partial;
     int n_chunks;        // partial chunks per (b, q-head)
     int PW;              // floats per partial record
-    float* sall;         // [B, H_q, T] scaled logits of every q-head (tensor-core path), or null
+    float* sall;         // [B, T, H_q] scaled logits of every q-head (tensor-core path), or null
     int32_t* cnt;        // [B, H_kv] finished-chunk counters for the merge fused into K3, or null
     int32_t* hit;        // [B, H_kv, S_eff] residual row of each selected token or -1 (tensor-core path), or null
     void* fold;          // [copies, H_kv, m, r] bf16: w1[h] . basis_h, folded by the selection kernel (tensor-core

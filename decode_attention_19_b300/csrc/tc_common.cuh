@@ -144,6 +144,11 @@ __device__ __forceinline__ uint32_t ldg_pin_u32(const void* p) {
     return v;
 }
 __device__ __forceinline__ float ldg_pin_f32(const void* p) { return __uint_as_float(ldg_pin_u32(p)); }
+__device__ __forceinline__ float4 ldg_pin_f32x4(const void* p) {   // 16-byte aligned
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ int ldg_pin_s32(const void* p) { return (int)ldg_pin_u32(p); }
 // One arrival on `bar` once every cp.async this thread issued before has landed (the barrier's expected count
 // includes it); the thread does not wait.  The consumer orders the landed bytes before its async-proxy reads with

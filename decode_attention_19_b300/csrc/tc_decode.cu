@@ -58,7 +58,7 @@ struct ScoreTcParams {
     const float* rcos;
     const float* rsin;
     float* key;
-    float* sall;        // [B, H_q, T] scaled logits of every q-head, or null
+    float* sall;        // [B, T, H_q] scaled logits of every q-head (a token's q-heads contiguous), or null
     uint32_t* check;
 };
 
@@ -483,17 +483,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScoreThreads, 1)
             named_bar_sync(1, 256);      // (exchange buffers alternate by unit, so one barrier per unit)
             const int t = st0 + frow;
             if (finisher && ok && sreal && t < p.T) {
+                // the unit's HPU * G q-heads of token t are contiguous in sall: vector stores where they align
+                float sc[HPU * G];
 #pragma unroll
                 for (int hx = 0; hx < HPU; ++hx) {
                     const int h = u * HPU + hx;
                     float best = -INFINITY;
 #pragma unroll
                     for (int jq = 0; jq < G; ++jq) {
-                        const float sc = (fin[hx][jq] + xs[hx * G + jq]) * p.scale;
-                        best = fmaxf(best, sc);
-                        if (p.sall) p.sall[((int64_t)sb * p.H_q + h * G + jq) * p.T + t] = sc;
+                        sc[hx * G + jq] = (fin[hx][jq] + xs[hx * G + jq]) * p.scale;
+                        best = fmaxf(best, sc[hx * G + jq]);
                     }
                     p.key[((int64_t)sb * p.H_kv + h) * p.T + t] = best;
+                }
+                if (p.sall) {
+                    float* dst = p.sall + ((int64_t)sb * p.T + t) * p.H_q + u * HPU * G;
+                    if constexpr ((HPU * G) % 4 == 0) {
+#pragma unroll
+                        for (int v = 0; v < HPU * G; v += 4)
+                            *reinterpret_cast<float4*>(dst + v) = make_float4(sc[v], sc[v + 1], sc[v + 2], sc[v + 3]);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < HPU * G; ++v) dst[v] = sc[v];
+                    }
                 }
             }
         }

@@ -79,7 +79,7 @@ struct VregenTcParams {
     long long mlp_stride;     // elements from sequence b's w2 to b+1's (0: shared); biases are then per sequence
     long long wait_cycles;
     const __nv_bfloat16* coef;   // [B, T, r] latent coefficients (2-byte elements; fp16 for an int4 cache's copy)
-    const float* sall;        // [B, H_q, T] scaled logits written by the key pass
+    const float* sall;        // [B, T, H_q] scaled logits written by the key pass
     const float* b1;          // [H_kv, m] ([B, H_kv, m] with a predictor per sequence) or null
     const float* b2;          // [H_kv, d] ([B, H_kv, d] likewise) or null
     const __nv_bfloat16* w2;  // [H_kv, d, m], sequence b's at b * mlp_stride
@@ -486,9 +486,24 @@ __global__ void __launch_bounds__(kVThreads, 1)
             int h, b, c;
             item_hbc(it, h, b, c);
             if (tok >= p.T) tok = p.T - 1;   // the selection is always in range; keep the invariant explicit
+            // the kv-head's G logits of the token are contiguous (vector loads where they align)
+            const float* src = p.sall + ((int64_t)b * p.T + (tok >= 0 ? tok : 0)) * p.H_q + h * G;
+            if constexpr (G % 4 == 0) {
 #pragma unroll
-            for (int jq = 0; jq < G; ++jq)
-                sv[jq] = tok >= 0 ? ldg_pin_f32(p.sall + ((int64_t)b * p.H_q + h * G + jq) * p.T + tok) : -INFINITY;
+                for (int v = 0; v < G; v += 4) {
+                    const float4 x = ldg_pin_f32x4(src + v);
+                    sv[v] = x.x;
+                    sv[v + 1] = x.y;
+                    sv[v + 2] = x.z;
+                    sv[v + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int jq = 0; jq < G; ++jq) sv[jq] = ldg_pin_f32(src + jq);
+            }
+            if (tok < 0)
+#pragma unroll
+                for (int jq = 0; jq < G; ++jq) sv[jq] = -INFINITY;
         };
         // merge of (b, h) by the team that finished its last chunk: the records of its chunks, read through L2
         auto merge = [&](int h, int b) {
