@@ -584,10 +584,11 @@ __global__ void __launch_bounds__(kVThreads, 1)
             const __nv_bfloat16* w = p.w2 + b * p.mlp_stride + ((int64_t)h * 128 + 32 * q + 16 * mt + fg) * M + 2 * ft;
 #pragma unroll
             for (int kb = 0; kb < KB; ++kb) {
-                a[kb][0] = __ldg(reinterpret_cast<const uint32_t*>(w + kb * 16));
-                a[kb][1] = __ldg(reinterpret_cast<const uint32_t*>(w + 8 * M + kb * 16));
-                a[kb][2] = __ldg(reinterpret_cast<const uint32_t*>(w + kb * 16 + 8));
-                a[kb][3] = __ldg(reinterpret_cast<const uint32_t*>(w + 8 * M + kb * 16 + 8));
+                // pinned where they stand (the item's start): they land during the accumulator wait
+                a[kb][0] = ldg_pin_u32(w + kb * 16);
+                a[kb][1] = ldg_pin_u32(w + 8 * M + kb * 16);
+                a[kb][2] = ldg_pin_u32(w + kb * 16 + 8);
+                a[kb][3] = ldg_pin_u32(w + 8 * M + kb * 16 + 8);
             }
         };
         int w2_key = -1;
