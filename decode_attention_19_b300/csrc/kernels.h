@@ -45,7 +45,6 @@ struct DecodeArgs {
     int n_chunks;        // partial chunks per (b, q-head)
     int PW;              // floats per partial record
     float* sall;         // [B, T, H_q] scaled logits of every q-head (tensor-core path), or null
-    int32_t* cnt;        // [B, H_kv] finished-chunk counters for the merge fused into K3, or null
     int32_t* hit;        // [B, H_kv, S_eff] residual row of each selected token or -1 (tensor-core path), or null
     void* fold;          // [copies, H_kv, m, r] bf16: w1[h] . basis_h, folded by the selection kernel (tensor-core
                          // path); one copy per sequence when a basis or a predictor is given per sequence
@@ -92,7 +91,6 @@ cudaError_t launch_merge(int B, int H_q, int n_chunks, int d, const float* parti
 bool tc_score_supported(const lowram_decode_shape& s);
 bool tc_vregen_supported(const lowram_decode_shape& s);
 int tc_partial_width(const lowram_decode_shape& s);
-bool tc_fused_merge(const lowram_decode_shape& s, int n_chunks);
 constexpr int kTcChunk = 128;
 cudaError_t launch_score_tc(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st);

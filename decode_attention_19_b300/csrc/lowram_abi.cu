@@ -108,8 +108,7 @@ struct DecodeLayout {
     lowram_decode_shape sx;     // the shape the kernels see: with split, bf16 coefficients of rank 2r; with f16,
                                 // fp16 coefficients (kCoefF16) and an fp16 basis
     int chunk, n_chunks, S_eff, PW;
-    bool fused_merge;
-    size_t off_key, off_sel, off_partial, off_sall, off_cnt, off_hit, off_fold, off_asplit, off_bsplit, total;
+    size_t off_key, off_sel, off_partial, off_sall, off_hit, off_fold, off_asplit, off_bsplit, total;
 };
 
 DecodeLayout decode_layout(const lowram_decode_shape& s) {
@@ -142,9 +141,6 @@ DecodeLayout decode_layout(const lowram_decode_shape& s) {
     off += align256(sizeof(float) * (size_t)s.B * s.H_q * L.n_chunks * L.PW);
     L.off_sall = off;
     off += L.tc_vregen ? align256(sizeof(float) * (size_t)s.B * s.H_q * s.T) : 0;
-    L.fused_merge = L.tc_vregen && L.n_chunks > 0 && tc_fused_merge(L.sx, L.n_chunks);
-    L.off_cnt = off;
-    off += L.fused_merge ? align256(sizeof(int32_t) * (size_t)s.B * s.H_kv) : 0;
     L.off_hit = off;
     off += L.tc_vregen ? align256(sizeof(int32_t) * (size_t)s.B * s.H_kv * L.S_eff) : 0;
     L.off_fold = off;
@@ -266,7 +262,6 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     a.n_chunks = L.n_chunks;
     a.PW = L.PW;
     a.sall = L.tc_vregen ? (float*)(ws + L.off_sall) : nullptr;
-    a.cnt = L.fused_merge ? (int32_t*)(ws + L.off_cnt) : nullptr;
     a.hit = (L.tc_vregen && s.n_res > 0) ? (int32_t*)(ws + L.off_hit) : nullptr;
     a.fold = L.tc_vregen ? (void*)(ws + L.off_fold) : nullptr;
     a.wait_cycles = g_wait_cycles;
@@ -309,7 +304,7 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
                         L.f16 ? s.basis_batch_stride : L.sx.basis_batch_stride, s.mlp_batch_stride, L.f16};
     if ((int64_t)s.B * L.S_eff > 0) {
         const Range stage("lowram selection");
-        e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs, a.cnt, a.hit, res_idx, s.n_res, a.check,
+        e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs, nullptr, a.hit, res_idx, s.n_res, a.check,
                                L.tc_vregen ? &fold : nullptr);
     }
     if (e != cudaSuccess) return cuda_fail(e, "select");
@@ -320,8 +315,7 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
     }
     if (e != cudaSuccess) return cuda_fail(e, "vregen");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event");
-    const bool merged = L.fused_merge && (int64_t)s.B * L.S_eff > 0;   // K3 merged as it finished
-    if (any && !merged) {
+    if (any) {
         const int nc = (int64_t)s.B * L.S_eff > 0 ? L.n_chunks : 0;
         e = launch_merge(s.B, s.H_q, nc, s.d, a.partial, out, lse, cs);
     }

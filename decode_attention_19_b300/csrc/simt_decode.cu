@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(int n_chunks, int 
     const int w = blockIdx.x, tid = threadIdx.x;
     const int64_t rw = d + 2;
     const float* P = partial + (int64_t)w * n_chunks * rw;
+    grid_dep_wait();   // the records come from the kernel before
     float M = -INFINITY;
     for (int c = tid; c < n_chunks; c += kMergeThreads) M = fmaxf(M, P[c * rw + d]);
     M = merge_reduce(M, red, true);
@@ -242,17 +243,56 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(int n_chunks, int 
     if (lse && tid == 0) lse[w] = (L > 0.0f) ? M + logf(L) : -INFINITY;
 }
 
+// The same merge for d = 128 with one warp per (b, q-head): lanes take the chunks for the maximum and the weight
+// sum (warp shuffles, no block barrier), then every lane sums four output features over all chunks (each chunk's
+// weight recomputed from its maximum, broadcast loads).  Eight rows per CTA of 256 threads.
+__global__ void __launch_bounds__(256) merge_warp_kernel(int BH, int n_chunks, const float* __restrict__ partial,
+                                                         float* __restrict__ out, float* __restrict__ lse) {
+    grid_dep_wait();   // the records come from the kernel before
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= BH) return;
+    constexpr int64_t rw = 128 + 2;
+    const float* P = partial + (int64_t)w * n_chunks * rw;
+    float M = -INFINITY;
+    for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, P[c * rw + 128]);
+    M = warp_max(M);
+    float L = 0.0f;
+    for (int c = lane; c < n_chunks; c += 32) {
+        const float mc = P[c * rw + 128];
+        L = fmaf(mc == -INFINITY ? 0.0f : __expf(mc - M), P[c * rw + 129], L);
+    }
+    L = warp_sum(L);
+    float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int c = 0; c < n_chunks; ++c) {
+        const float* pc = P + c * rw;
+        const float mc = pc[128];
+        const float wc = mc == -INFINITY ? 0.0f : __expf(mc - M);
+        const float2 v0 = *reinterpret_cast<const float2*>(pc + 4 * lane);       // rw even: 8-byte aligned
+        const float2 v1 = *reinterpret_cast<const float2*>(pc + 4 * lane + 2);
+        a[0] = fmaf(wc, v0.x, a[0]);
+        a[1] = fmaf(wc, v0.y, a[1]);
+        a[2] = fmaf(wc, v1.x, a[2]);
+        a[3] = fmaf(wc, v1.y, a[3]);
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    *reinterpret_cast<float4*>(out + (int64_t)w * 128 + 4 * lane) =
+        make_float4(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
+    if (lse && lane == 0) lse[w] = L > 0.0f ? M + logf(L) : -INFINITY;
+}
+
 cudaError_t launch_merge(int B, int H_q, int n_chunks, int d, const float* partial, float* out, float* lse,
                          cudaStream_t st) {
     const int BH = B * H_q;
     if (BH == 0) return cudaSuccess;
+    if (d == 128 && n_chunks > 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0)
+        return launch_pdl(merge_warp_kernel, dim3((unsigned)cdiv(BH, 8)), dim3(256), 0, st, BH, n_chunks, partial, out,
+                          lse);
     const size_t smem = sizeof(float) * (size_t)(n_chunks > 0 ? n_chunks : 1);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    merge_kernel<<<(unsigned)BH, kMergeThreads, smem, st>>>(n_chunks, d, partial, out, lse);
-    return cudaGetLastError();
+    return launch_pdl(merge_kernel, dim3((unsigned)BH), dim3(kMergeThreads), smem, st, n_chunks, d, partial, out, lse);
 }
 
 // ------------------------------------------------------------------------------------------------

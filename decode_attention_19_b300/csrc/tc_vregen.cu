@@ -1,5 +1,5 @@
-// tc_vregen.cu -- tensor-core (tcgen05) value regeneration for the selected tokens of bf16 caches (K3), with the
-// softmax partials of its chunks merged by the CTA that finishes a (sequence, kv-head) last.
+// tc_vregen.cu -- tensor-core (tcgen05) value regeneration for the selected tokens of bf16 caches (K3): one
+// split-softmax record per 128-token chunk, merged by the merge kernel launched after it.
 //
 // The method: each decode step rebuilds only a selected subset of KV pairs (LowRAM abstract); a selected
 // token's value is predicted from its pre-RoPE key by the head's MLP, plus the stored residual when the
@@ -25,7 +25,6 @@
 // per warpgroup (setmaxnreg): 56 for warps 0-7, 200 for the epilogue warps 8-15:
 //   warp 0      lane 0: TMA of F_h's k-chunks [m x 64] once per kv-head (into two staging buffers in TMEM
 //               mode, into the resident copy otherwise) or per stage when streamed;
-//               lane 1: merge tickets (the per-(b, h) chunk counter, one item behind the epilogue).
 //   warp 1      TMEM owner (two accumulators of m columns) and MMA issuer (one thread):
 //               D[m hidden x 128 tokens] = F_h . C_sel^T (M = 128 per 128 hidden units, N = 128, K = r), hidden
 //               units on TMEM lanes, tokens on columns; item j accumulates into buffer j % 2.  In TMEM mode it
@@ -42,8 +41,8 @@
 //               read); per thread one hidden unit and all 128 tokens: SiLU(D + b1) weighted by the softmax,
 //               summed; the TMEM buffer is released; w2 (rows held in registers per kv-head) on the hidden sums;
 //               the chunk's record.
-// The CTA finishing a (b, h)'s last chunk merges its chunks' records into out and lse (a counter per (b, h),
-// zeroed by the selection kernel; records read through L2).
+// The records are merged by a separate kernel (a dependent launch): merging in the CTA that finished a
+// (sequence, kv-head) last put a merge after the slowest CTA's last record and measured slower.
 //
 // Every pipeline wait is bounded by the call's wait limit (a parameter); on a timeout the kernel sets
 // LOWRAM_CHECK_TIMEOUT, lets the copies and MMAs it issued complete, frees TMEM and returns.  Every named
@@ -66,7 +65,6 @@ constexpr int kCBytes = kRows * 128;     // latent chunk [128 tokens x 64] bf16,
 constexpr int kGatRows = kRows / (kGat / 8);   // rows each gathering thread copies per stage
 constexpr int kMaxStages = 12;
 constexpr int kFStage = 2;               // TMEM mode: F_h staging buffers of 16 KB
-constexpr int kMaxMergeChunks = 64;      // chunks per (b, h) the fused merge takes (S <= 8192)
 constexpr size_t kSmemMax = 232448;
 
 struct VregenTcParams {
@@ -87,9 +85,6 @@ struct VregenTcParams {
     const int32_t* hit;       // [B, H_kv, S_eff] residual row of each selected token, or -1; null without residuals
     ResView res;
     float* partial;           // [B, H_q, n_chunks, d + 2]
-    int32_t* cnt;             // [B, H_kv] chunks finished per (b, h); zeroed by the selection kernel; null: no merge
-    float* out;               // [B, H_q, d]
-    float* lse;               // [B, H_q] or null
     uint32_t* check;
 };
 
@@ -98,15 +93,15 @@ __host__ __device__ constexpr int w2_ntiles(int g) { return (2 * g + 7) / 8; }
 constexpr int kWoStride = 132;           // floats per row of the second layer's output (conflict-free stores)
 
 // One epilogue team's scratch in 4-byte words, for g q-heads per kv-head: softmax weights [g][128], hidden sums
-// [g][m], the second layer's output [8 nt][132] and operand [8 nt][m + 8] bf16, merge weights [g][64] and (W, L)
-// [8][2], compacted hits (rows, slots), reductions [2][32] + counts [4]; a multiple of 4 words (16-byte aligned).
+// [g][m], the second layer's output [8 nt][132] and operand [8 nt][m + 8] bf16, compacted hits (rows, slots),
+// reductions [2][32] + counts [4]; a multiple of 4 words (16-byte aligned).
 __host__ __device__ constexpr int team_words(int m, int g) {
-    return (g * kRows + g * m + w2_ntiles(g) * 8 * kWoStride + w2_ntiles(g) * 4 * (m + 8) + g * kMaxMergeChunks + 16 +
-            2 * kRows + 64 + 4 + 3) & ~3;
+    return (g * kRows + g * m + w2_ntiles(g) * 8 * kWoStride + w2_ntiles(g) * 4 * (m + 8) + 2 * kRows + 64 + 4 + 3) &
+           ~3;
 }
-// Scratch beside the ring: two teams' scratch, then the barriers and the TMEM slot / flags.
+// Scratch beside the ring: two teams' scratch, then the barriers and the TMEM slot / abort flag.
 size_t scratch_bytes(int m, int g) {
-    return (size_t)8 * team_words(m, g) + 8 + 8 * (3 * kMaxStages + 2 * kFStage + 4 + 1 + 8) + 32;
+    return (size_t)8 * team_words(m, g) + 8 + 8 * (3 * kMaxStages + 2 * kFStage + 4 + 1) + 16;
 }
 
 struct VregenConfig {
@@ -176,12 +171,9 @@ __global__ void __launch_bounds__(kVThreads, 1)
     uint64_t* t_full = f_empty + kFStage;        // [2] accumulator ready
     uint64_t* t_empty = t_full + 2;              // [2] epilogue done reading the accumulator
     uint64_t* m_drain = t_empty + 2;
-    uint64_t* rec_done = m_drain + 1;            // [4] item j's record is written (slot j % 4, one arrival)
-    uint64_t* tick = rec_done + 4;               // [4] the helper lane took item j's merge ticket
-    uint32_t* tmem_slot = (uint32_t*)(tick + 4);
+    uint32_t* tmem_slot = (uint32_t*)(m_drain + 1);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-    volatile int* last_flag = (volatile int*)(tmem_slot + 2);   // [4] the ticket was the (b, h)'s last
-    if (layout_overflows(smem_raw, (const void*)(last_flag + 4), p.check)) return;
+    if (layout_overflows(smem_raw, (const void*)(abort_flag + 1), p.check)) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int it_begin = (int)((int64_t)blockIdx.x * p.n_items / gridDim.x);
@@ -215,11 +207,6 @@ __global__ void __launch_bounds__(kVThreads, 1)
             mbar_init(&t_empty[i], kTeam);
         }
         mbar_init(m_drain, 1);
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&rec_done[i], 1);
-            mbar_init(&tick[i], 1);
-            last_flag[i] = 0;
-        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -298,20 +285,6 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     else if (!fres)
                         for (uint32_t k = issued > (uint32_t)NS ? issued - NS : 0; k < issued; ++k)
                             mbar_wait_drain(&fullF[k % NS], (k / NS) & 1);
-                }
-            } else if (lane == 1 && p.cnt) {
-                // ------------------------------------------------------------------ merge tickets
-                // once an item's record is written (the epilogue's writes ordered before rec_done at CTA scope, then
-                // made visible device-wide by this lane's fence), count the chunk for its (b, h); the count that
-                // completes the (b, h) tells the epilogue to merge it.  The epilogue waits for the ticket one item
-                // later, so the atomic's round trip overlaps the next item.
-                for (int j = 0; j < n_local; ++j) {
-                    if (!mbar_wait_lim(&rec_done[j & 3], (j >> 2) & 1, abort_flag, p.wait_cycles)) break;
-                    int h, b, c;
-                    item_hbc(it_begin + j, h, b, c);
-                    __threadfence();
-                    last_flag[j & 3] = (atomicAdd(p.cnt + (int64_t)b * p.H_kv + h, 1) == p.n_chunks - 1) ? 1 : 0;
-                    mbar_arrive(&tick[j & 3]);
                 }
             }
         } else if (warp == 1) {
@@ -456,9 +429,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
         float* Z = Ps + G * kRows;                               // [G][M] hidden sums
         float* Wo = Z + G * M;                                   // [8 NT][132] second layer: rows n, features i
         __nv_bfloat16* Zs = reinterpret_cast<__nv_bfloat16*>(Wo + NT * 8 * kWoStride);   // [8 NT][M + 8] its operand
-        float* Wc = reinterpret_cast<float*>(Zs + NT * 8 * (M + 8));   // [G][n_chunks] merge weights
-        float* ML = Wc + G * kMaxMergeChunks;                    // [G][2] W and L of the merge (16 floats)
-        int* HitRow = (int*)(ML + 16);                           // compacted residual rows of the chunk's slots
+        int* HitRow = reinterpret_cast<int*>(Zs + NT * 8 * (M + 8));   // compacted residual rows of the chunk's slots
         int* HitSlot = HitRow + kRows;                           // ... and those slots, ascending
         float* redM = (float*)(HitSlot + kRows);                 // [4 slot quarters][8] partial max
         float* redL = redM + 32;                                 // [4][8] partial sums
@@ -505,73 +476,6 @@ __global__ void __launch_bounds__(kVThreads, 1)
 #pragma unroll
                 for (int jq = 0; jq < G; ++jq) sv[jq] = -INFINITY;
         };
-        // merge of (b, h) by the team that finished its last chunk: the records of its chunks, read through L2
-        auto merge = [&](int h, int b) {
-            const int64_t bh = (int64_t)b * p.H_kv + h;
-            __threadfence();
-            const float* P0 = p.partial + ((int64_t)b * p.H_q + h * G) * qstride;
-            if (et < G) {
-                const float* Pq = P0 + et * qstride;
-                float mx = -INFINITY;
-                for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
-                    float mc[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) mc[u] = c0 + u < p.n_chunks ? __ldcg(Pq + (c0 + u) * rw + 128) : -INFINITY;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) mx = fmaxf(mx, mc[u]);
-                }
-                float l = 0.0f;
-                for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
-                    float mc[8], lc[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const bool in = c0 + u < p.n_chunks;
-                        mc[u] = in ? __ldcg(Pq + (c0 + u) * rw + 128) : -INFINITY;
-                        lc[u] = in ? __ldcg(Pq + (c0 + u) * rw + 129) : 0.0f;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        if (c0 + u >= p.n_chunks) break;
-                        const float w = mc[u] == -INFINITY ? 0.0f : __expf(mc[u] - mx);
-                        Wc[et * kMaxMergeChunks + c0 + u] = w;
-                        l = fmaf(w, lc[u], l);
-                    }
-                }
-                ML[et * 2] = mx;
-                ML[et * 2 + 1] = l;
-            }
-            team_sync();
-            for (int jq = 0; jq < G; ++jq) {
-                const float* Pq = P0 + jq * qstride + i_out;
-                float a = 0.0f;
-                for (int c0 = 0; c0 < p.n_chunks; c0 += 8) {
-                    float v[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) v[u] = c0 + u < p.n_chunks ? __ldcg(Pq + (c0 + u) * rw) : 0.0f;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (c0 + u < p.n_chunks) a = fmaf(Wc[jq * kMaxMergeChunks + c0 + u], v[u], a);
-                }
-                const float L = ML[jq * 2 + 1];
-                p.out[((int64_t)b * p.H_q + h * G + jq) * 128 + i_out] = L > 0.0f ? a / L : 0.0f;
-            }
-            if (p.lse && et < G) {
-                const float L = ML[et * 2 + 1];
-                p.lse[(int64_t)b * p.H_q + h * G + et] = L > 0.0f ? ML[et * 2] + logf(L) : -INFINITY;
-            }
-            if (et == 0) p.cnt[bh] = 0;
-            team_sync();   // Wc and ML are free again
-        };
-        // the ticket of item jp (taken by the helper lane): merge its (b, h) when this CTA finished it last
-        auto settle = [&](int jp) {
-            const bool ok = mbar_wait_lim(&tick[jp & 3], (jp >> 2) & 1, abort_flag, p.wait_cycles);
-            if (ok && last_flag[jp & 3]) {
-                int h, b, c;
-                item_hbc(it_begin + jp, h, b, c);
-                merge(h, b);
-            }
-        };
-
         // The second layer on warp MMAs: warp q of the team makes output features [32 q, 32 q + 32) of every
         // q-head (two m16 tiles), W[i][n] = sum_k w2[i][k] Zs[n][k], from its w2 rows in m16n8k16 A fragments.
         // With M = 128 the fragments stay in registers while the items' kv-head (and, with a predictor per
@@ -829,18 +733,6 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 rec[i_out * qstride + 128] = chunk_max(i_out);
                 rec[i_out * qstride + 129] = chunk_sum(i_out);
             }
-            if (p.cnt) {
-                // the record is written: the helper lane takes this chunk's ticket while the team's next item
-                // starts; the ticket of the team's item before is settled here (merged if this CTA finished that
-                // (b, h)); tickets rotate over four slots, so a slot is reused only after its item was settled
-                team_sync();
-                if (et == 0) mbar_arrive(&rec_done[j & 3]);
-                if (j >= 2) settle(j - 2);
-            }
-        }
-        if (p.cnt) {
-            const int j_last = tm + ((n_local - 1 - tm) >> 1) * 2;   // the team's last item
-            if (tm < n_local) settle(j_last);
         }
     }
 
@@ -862,8 +754,6 @@ bool tc_vregen_supported(const lowram_decode_shape& s) {
 
 int tc_partial_width(const lowram_decode_shape& s) { return s.d + 2; }
 
-// The CTA finishing a (sequence, kv-head) merges its chunks when their weights fit the merge scratch.
-bool tc_fused_merge(const lowram_decode_shape&, int n_chunks) { return n_chunks <= kMaxMergeChunks; }
 
 cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     const auto& s = a.s;
@@ -898,9 +788,6 @@ cudaError_t launch_vregen_tc(const DecodeArgs& a, cudaStream_t st) {
     p.hit = a.hit;
     p.res = ResView{s.res_dtype, a.res_val, (const __half*)a.res_scale, s.d};
     p.partial = a.partial;
-    p.cnt = a.cnt;
-    p.out = a.out;
-    p.lse = a.lse;
     p.check = a.check;
     if (p.n_items == 0) return cudaSuccess;
     if (!a.fold || cfg.NS < 2) return cudaErrorInvalidValue;
