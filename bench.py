@@ -139,13 +139,13 @@ def gpu_backlog(ms=10.0):
 
 
 def launches_per_call(w, tc_path):
-    """Kernels one decode call launches: keys, selection, values (+ a separate merge unless the tensor-core
-    value pass merges as it finishes, which it does for predictor widths of 128 or 256), plus the two
-    kernels that split an int4 cache exactly into bf16 [hi | lo] and repeat the basis for the tensor cores."""
-    split = 2 if (tc_path and w.coef_fmt == "int4") else 0
+    """Kernels one decode call launches: keys, selection, values and the merge of the values' chunk records, plus,
+    for an int4 cache on the tensor cores, the one kernel that makes the fp16 copies of the coefficients and the
+    basis (the exact bf16 split behind LOWRAM_FLAG_INT4_EXACT_SPLIT takes two, and the bench does not set it)."""
+    copy = 1 if (tc_path and w.coef_fmt == "int4") else 0
     if w.S_eff == 0:
-        return 2 + split
-    return (3 if (tc_path and w.m in (128, 256)) else 4) + split
+        return 2 + copy
+    return 4 + copy
 
 
 def kernel_digest(paths):

@@ -262,17 +262,27 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(int BH, int n_chunks, c
         L = fmaf(mc == -INFINITY ? 0.0f : __expf(mc - M), P[c * rw + 129], L);
     }
     L = warp_sum(L);
+    // chunks in batches of 8: all of a batch's loads are issued before any is used
     float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int c = 0; c < n_chunks; ++c) {
-        const float* pc = P + c * rw;
-        const float mc = pc[128];
-        const float wc = mc == -INFINITY ? 0.0f : __expf(mc - M);
-        const float2 v0 = *reinterpret_cast<const float2*>(pc + 4 * lane);       // rw even: 8-byte aligned
-        const float2 v1 = *reinterpret_cast<const float2*>(pc + 4 * lane + 2);
-        a[0] = fmaf(wc, v0.x, a[0]);
-        a[1] = fmaf(wc, v0.y, a[1]);
-        a[2] = fmaf(wc, v1.x, a[2]);
-        a[3] = fmaf(wc, v1.y, a[3]);
+    for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+        float mc[8];
+        float2 v0[8], v1[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool in = c0 + u < n_chunks;
+            const float* pc = P + (in ? c0 + u : 0) * rw;
+            mc[u] = in ? pc[128] : -INFINITY;
+            v0[u] = *reinterpret_cast<const float2*>(pc + 4 * lane);   // rw even: 8-byte aligned
+            v1[u] = *reinterpret_cast<const float2*>(pc + 4 * lane + 2);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float wc = mc[u] == -INFINITY ? 0.0f : __expf(mc[u] - M);
+            a[0] = fmaf(wc, v0[u].x, a[0]);
+            a[1] = fmaf(wc, v0[u].y, a[1]);
+            a[2] = fmaf(wc, v1[u].x, a[2]);
+            a[3] = fmaf(wc, v1[u].y, a[3]);
+        }
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     *reinterpret_cast<float4*>(out + (int64_t)w * 128 + 4 * lane) =
