@@ -238,7 +238,7 @@ cudaError_t launch_evict_plan(int B, int T, int n_sink, int n_recent, int T_keep
     evict_scores_kernel<<<(unsigned)cdiv(n, 256), 256, 0, st>>>(mass, n, T, n_sink, n_recent, scores);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_select_topn(B, T, T_keep, scores, keep, st, nullptr, nullptr, nullptr, 0, check);
+    return launch_select_topn(B, T, T_keep, scores, keep, st, nullptr, nullptr, 0, check);
 }
 
 }  // namespace lowram

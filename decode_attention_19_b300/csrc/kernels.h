@@ -72,11 +72,11 @@ cudaError_t launch_rope_table(int d, double theta, int max_pos, float* cos_out, 
 // K1: selection keys of every token (CUDA-core path; any dtype)
 cudaError_t launch_score_simt(const DecodeArgs& a, cudaStream_t st);
 // K2: exact top-n per problem row (values [P][T] -> ascending indices [P][n]).  For the value pass it can also
-// zero zero_cnt[row] (merge counters) and write hit[row][j] = position of token out[row][j] in the row's
-// ascending residual list res_idx[row][0..n_res) or -1, checking the list (LOWRAM_CHECK_RES_INDEX into check).
+// write hit[row][j] = position of token out[row][j] in the row's ascending residual list res_idx[row][0..n_res)
+// or -1, checking the list (LOWRAM_CHECK_RES_INDEX into check).
 // With `fold`, spare CTAs of the same launch also compute the folded weights (they do not wait for the kernel before).
 cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, int32_t* out, cudaStream_t st,
-                               int32_t* zero_cnt = nullptr, int32_t* hit = nullptr, const int32_t* res_idx = nullptr,
+                               int32_t* hit = nullptr, const int32_t* res_idx = nullptr,
                                int n_res = 0, uint32_t* check = nullptr, const FoldArgs* fold = nullptr);
 size_t select_scratch_bytes(int P, int T, int n_keep);
 // K3: value regeneration + softmax partials for selected chunks of 32 (CUDA-core path)

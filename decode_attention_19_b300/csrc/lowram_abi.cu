@@ -304,7 +304,7 @@ static lowram_status decode_impl(const lowram_decode_shape* shape, const void* q
                         L.f16 ? s.basis_batch_stride : L.sx.basis_batch_stride, s.mlp_batch_stride, L.f16};
     if ((int64_t)s.B * L.S_eff > 0) {
         const Range stage("lowram selection");
-        e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs, nullptr, a.hit, res_idx, s.n_res, a.check,
+        e = launch_select_topn(s.B * s.H_kv, s.T, L.S_eff, a.key, a.sel, cs, a.hit, res_idx, s.n_res, a.check,
                                L.tc_vregen ? &fold : nullptr);
     }
     if (e != cudaSuccess) return cuda_fail(e, "select");

@@ -24,7 +24,6 @@ constexpr int kSelMaxStaged = 48 * 1024;   // row elements staged in shared memo
 // failure) and, when staged, copied into shared memory (free once the selection is written) for the
 // binary searches.
 struct SelectExtras {
-    int32_t* zero_cnt;        // [rows] set to 0, or null
     int32_t* hit;             // [rows][n_keep] residual row of each kept token, or null
     const int32_t* res_idx;   // [rows][n_res] ascending residual token indices
     int n_res;
@@ -179,7 +178,6 @@ __global__ void __launch_bounds__(kSelThreads) select_topn_kernel(int T, int n_k
     const float* v = values + (int64_t)row * T;
     int32_t* o = out + (int64_t)row * n_keep;
     grid_dep_wait();     // the keys come from the kernel before (launched with launch_pdl)
-    if (x.zero_cnt && tid == 0) x.zero_cnt[row] = 0;
     if (n_keep <= 0) return;
     if (n_keep >= T) {
         for (int t = tid; t < T; t += kSelThreads) o[t] = t;
@@ -398,7 +396,6 @@ __global__ void __launch_bounds__(kSelThreads) select_cl_kernel(int T, int n_kee
         __syncthreads();   // wsum_gt is free again (the passes may be skipped)
     }
     grid_dep_wait();     // the keys come from the kernel before (launched with launch_pdl)
-    if (x.zero_cnt && crank == 0 && tid == 0) x.zero_cnt[row] = 0;
     if (n_keep <= 0) return;   // uniform over the cluster: no CTA touched another's memory
     const int t0 = lo + tid * E;
     uint32_t k[E];
@@ -576,10 +573,10 @@ __global__ void __launch_bounds__(kSelThreads) select_cl_kernel(int T, int n_kee
 size_t select_scratch_bytes(int, int, int) { return 0; }
 
 cudaError_t launch_select_topn(int P, int T, int n_keep, const float* values, int32_t* out, cudaStream_t st,
-                               int32_t* zero_cnt, int32_t* hit, const int32_t* res_idx, int n_res, uint32_t* check,
+                               int32_t* hit, const int32_t* res_idx, int n_res, uint32_t* check,
                                const FoldArgs* fold) {
     if (P == 0) return cudaSuccess;
-    SelectExtras x{zero_cnt, (hit && n_res > 0) ? hit : nullptr, res_idx, n_res, check, P, FoldArgs{}};
+    SelectExtras x{(hit && n_res > 0) ? hit : nullptr, res_idx, n_res, check, P, FoldArgs{}};
     if (fold) x.fold = *fold;
     const int nf = fold_blocks(x.fold);
     const size_t fold_smem = nf ? fold_smem_bytes(x.fold.d) : 0;
