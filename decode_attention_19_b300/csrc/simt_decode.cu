@@ -243,9 +243,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(int n_chunks, int 
     if (lse && tid == 0) lse[w] = (L > 0.0f) ? M + logf(L) : -INFINITY;
 }
 
-// The same merge for d = 128 with one warp per (b, q-head): lanes take the chunks for the maximum and the weight
-// sum (warp shuffles, no block barrier), then every lane sums four output features over all chunks (each chunk's
-// weight recomputed from its maximum, broadcast loads).  Eight rows per CTA of 256 threads.
+// The same merge for d = 128 with one warp per (b, q-head) and no block barrier: chunks in batches of eight, every
+// load of a batch (each chunk's maximum and weight sum, broadcast, and the lane's four output features) issued
+// before any is used, and the batches folded into a running maximum with the usual rescale.  Eight rows per CTA of
+// 256 threads.
 __global__ void __launch_bounds__(256) merge_warp_kernel(int BH, int n_chunks, const float* __restrict__ partial,
                                                          float* __restrict__ out, float* __restrict__ lse) {
     grid_dep_wait();   // the records come from the kernel before
@@ -253,36 +254,38 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(int BH, int n_chunks, c
     if (w >= BH) return;
     constexpr int64_t rw = 128 + 2;
     const float* P = partial + (int64_t)w * n_chunks * rw;
-    float M = -INFINITY;
-    for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, P[c * rw + 128]);
-    M = warp_max(M);
-    float L = 0.0f;
-    for (int c = lane; c < n_chunks; c += 32) {
-        const float mc = P[c * rw + 128];
-        L = fmaf(mc == -INFINITY ? 0.0f : __expf(mc - M), P[c * rw + 129], L);
-    }
-    L = warp_sum(L);
-    // chunks in batches of 8: all of a batch's loads are issued before any is used
+    float M = -INFINITY, L = 0.0f;
     float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     for (int c0 = 0; c0 < n_chunks; c0 += 8) {
-        float mc[8];
+        float mc[8], lc[8];
         float2 v0[8], v1[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const bool in = c0 + u < n_chunks;
             const float* pc = P + (in ? c0 + u : 0) * rw;
             mc[u] = in ? pc[128] : -INFINITY;
+            lc[u] = in ? pc[129] : 0.0f;
             v0[u] = *reinterpret_cast<const float2*>(pc + 4 * lane);   // rw even: 8-byte aligned
             v1[u] = *reinterpret_cast<const float2*>(pc + 4 * lane + 2);
         }
+        float Mb = M;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) Mb = fmaxf(Mb, mc[u]);
+        if (Mb == -INFINITY) continue;   // nothing weighted yet
+        const float r = M == -INFINITY ? 0.0f : __expf(M - Mb);   // rescale what the batches before summed
+        L *= r;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[e] *= r;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const float wc = mc[u] == -INFINITY ? 0.0f : __expf(mc[u] - M);
+            const float wc = mc[u] == -INFINITY ? 0.0f : __expf(mc[u] - Mb);
+            L = fmaf(wc, lc[u], L);
             a[0] = fmaf(wc, v0[u].x, a[0]);
             a[1] = fmaf(wc, v0[u].y, a[1]);
             a[2] = fmaf(wc, v1[u].x, a[2]);
             a[3] = fmaf(wc, v1[u].y, a[3]);
         }
+        M = Mb;
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     *reinterpret_cast<float4*>(out + (int64_t)w * 128 + 4 * lane) =
