@@ -12,12 +12,15 @@
 // Outputs: proj = Q^T [r, D] float32 (a left inverse of the stacked bases) and the G layer blocks of Q as the
 // bases [H_kv*d, r] in the activation dtype: the inputs lowram_compress takes.
 //
-// Kernels: a key prep pass (dtype, inverse RoPE), a Gram kernel (64 x 64 output tiles of the upper triangle,
-// mirrored, split over tokens with atomics when the tiles alone do not fill the GPU), a row-major SGEMM, a
-// single-CTA fp64 Cholesky, a row-parallel triangular solve, and the output pass.  All CUDA cores: the fit runs once
-// per prompt and the Gram product needs fp32 accumulation of fp32 keys.
+// Kernels: a key prep pass (dtype, inverse RoPE); the Gram matrix and each step's product Z = (X^T X) Q on the
+// tensor cores in float32 accuracy (tc_fit.cu: an exact three-term bf16 split of the float32 operands, six bf16
+// products accumulated in float32); Z^T Z in fp64 on the CUDA cores (64 x 64 upper-triangle tiles, mirrored, split
+// over rows with atomics when the tiles alone do not fill the GPU); a blocked multi-CTA fp64 Cholesky; a
+// row-parallel triangular solve; and the output pass.
 #include "common.cuh"
 #include "kernels.h"
+
+#include <algorithm>
 
 namespace lowram {
 
@@ -111,45 +114,6 @@ __global__ void __launch_bounds__(kFThreads) gram_kernel(const float* __restrict
         }
 }
 
-// C[M, Nc] = A[M, K] B[K, Nc], row-major float32
-__global__ void __launch_bounds__(kFThreads) sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
-                                                          int M, int K, int Nc, float* __restrict__ C) {
-    const int m0 = blockIdx.y * kFT, c0 = blockIdx.x * kFT;
-    __shared__ float As[kFK][kFT + 4], Bs[kFK][kFT + 4];
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    float acc[4][4] = {};
-    for (int k0 = 0; k0 < K; k0 += kFK) {
-        for (int e = tid; e < kFK * kFT; e += kFThreads) {
-            const int r = e % kFK, m = e / kFK;      // A tile: consecutive threads along k within a row
-            As[r][m] = (m0 + m < M && k0 + r < K) ? A[(int64_t)(m0 + m) * K + k0 + r] : 0.0f;
-            const int kr = e / kFT, c = e % kFT;     // B tile: consecutive threads along the row
-            Bs[kr][c] = (k0 + kr < K && c0 + c < Nc) ? B[(int64_t)(k0 + kr) * Nc + c0 + c] : 0.0f;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < kFK; ++k) {
-            float a[4], b[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                a[u] = As[k][ty * 4 + u];
-                b[u] = Bs[k][tx * 4 + u];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(a[u], b[v], acc[u][v]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const int m = m0 + ty * 4 + u, c = c0 + tx * 4 + v;
-            if (m < M && c < Nc) C[(int64_t)m * Nc + c] = acc[u][v];
-        }
-}
-
 // Seeded standard normal start: splitmix64 of (seed, element) gives two uniforms, Box-Muller one normal.
 __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
     x += 0x9E3779B97F4A7C15ull;
@@ -167,51 +131,147 @@ __global__ void init_normal_kernel(float* Q, int64_t n, uint64_t seed) {
     Q[i] = sqrtf(-2.0f * logf(u1)) * cospif(2.0f * u2);
 }
 
-// One CTA: S [r, r] fp64 is overwritten with its Cholesky factor (S = L L^T, L lower), which is also written
-// as float32 to Lf [r, r] (lower triangle; the strict upper triangle is not read).  A pivot at or below 1e-10 of
-// the largest diagonal entry (rounding noise of float32 iterates: the keys have rank below r) sets
-// LOWRAM_CHECK_NOT_PD and stops; Lf is then incomplete and the fit's result is void.
-__global__ void __launch_bounds__(1024) chol_kernel(double* S, int r, float* Lf, uint32_t* check) {
-    __shared__ int bad;
-    __shared__ double floor_pivot;
-    const int tid = threadIdx.x, nt = blockDim.x;
-    if (tid == 0) {
-        bad = 0;
-        double mx = 0.0;
-        for (int k = 0; k < r; ++k) mx = fmax(mx, S[(int64_t)k * r + k]);
-        // pivot k ~ (lambda_k / lambda_1)^2 of the largest: below 1e-10 (an eigenvalue under 1e-5 of the largest,
-        // the level of float32 rounding in the Gram matrix) the iterate has lost rank
-        floor_pivot = 1e-10 * mx;
+// Blocked Cholesky of S [r, r] fp64 (S = L L^T, L lower, written over S's lower triangle), panel by panel
+// (kCb columns) over many CTAs: the panel's diagonal block is factored by one CTA, the rows below it are solved
+// against it (L21 = S21 L11^-T) a thread per row, and the trailing lower triangle takes the panel's product
+// (S22 -= L21 L21^T) in 16 x 16 tiles.  A pivot at or below 1e-10 of the largest diagonal entry of S (rounding
+// noise of float32 iterates: the keys have rank below r) sets LOWRAM_CHECK_NOT_PD; every later kernel of the
+// factorization then returns at once and the fit's result is void.  The float32 copy Lf [r, r] (lower
+// triangle; zeros above) is what the triangular solve reads.
+constexpr int kCb = 32;
+constexpr int kCRows = 16;   // rows a CTA solves
+constexpr int kCT = 16;      // trailing-update tile edge
+
+__device__ __forceinline__ bool not_pd(const uint32_t* check) {
+    return check && (*(volatile const uint32_t*)check & LOWRAM_CHECK_NOT_PD);
+}
+
+// pivot floor: 1e-10 of the largest diagonal entry of S (the pivots are ~ (lambda_k / lambda_1)^2 of it: below
+// 1e-10, an eigenvalue under 1e-5 of the largest, the level of float32 rounding in the Gram matrix, the iterate
+// has lost rank)
+__global__ void __launch_bounds__(256) chol_floor_kernel(const double* __restrict__ S, int r, double* floor_out) {
+    __shared__ double wm[8];
+    double mx = 0.0;
+    for (int k = threadIdx.x; k < r; k += 256) mx = fmax(mx, S[(int64_t)k * r + k]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < 8; ++w) mx = fmax(mx, wm[w]);
+        *floor_out = 1e-10 * fmax(mx, wm[0]);
+    }
+}
+
+// the diagonal block of panel k0 (kb x kb), one warp: lane i owns row i; right-looking, one pivot at a time
+__global__ void __launch_bounds__(32) chol_diag_kernel(double* S, int r, int k0, const double* floor_p,
+                                                       uint32_t* check) {
+    if (not_pd(check)) return;
+    __shared__ double Lb[kCb][kCb + 1];
+    const int kb = min(kCb, r - k0), lane = threadIdx.x;
+    for (int j = 0; j < kb; ++j)
+        if (lane < kb) Lb[lane][j] = S[(int64_t)(k0 + lane) * r + k0 + j];
+    __syncwarp();
+    const double fl = *floor_p;
+    for (int k = 0; k < kb; ++k) {
+        const double p = Lb[k][k];
+        if (!(p > fl)) {
+            if (lane == 0) flag(check, LOWRAM_CHECK_NOT_PD);
+            return;
+        }
+        const double lkk = sqrt(p);
+        __syncwarp();
+        if (lane == k) Lb[k][k] = lkk;
+        if (lane > k && lane < kb) Lb[lane][k] /= lkk;
+        __syncwarp();
+        if (lane > k && lane < kb) {
+            const double lik = Lb[lane][k];
+            for (int j = k + 1; j <= lane; ++j) Lb[lane][j] -= lik * Lb[j][k];
+        }
+        __syncwarp();
+    }
+    for (int j = 0; j < kb; ++j)
+        if (lane < kb && j <= lane) S[(int64_t)(k0 + lane) * r + k0 + j] = Lb[lane][j];
+}
+
+// rows i >= k0 + kb of panel k0: l_ij = (s_ij - sum_{t<j} l_it l_jt) / l_jj, a thread per row
+__global__ void __launch_bounds__(32) chol_rows_kernel(double* S, int r, int k0, const uint32_t* check) {
+    if (not_pd(check)) return;
+    __shared__ double Lb[kCb][kCb + 1];
+    const int kb = min(kCb, r - k0), k1 = k0 + kb, t = threadIdx.x;
+    for (int e = t; e < kb * kb; e += 32) {
+        const int i = e / kb, j = e - (e / kb) * kb;
+        Lb[i][j] = j <= i ? S[(int64_t)(k0 + i) * r + k0 + j] : 0.0;
     }
     __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
-    for (int k = 0; k < r; ++k) {
-        if (tid == 0) {
-            const double p = S[(int64_t)k * r + k];
-            if (!(p > floor_pivot)) bad = 1;
-            else S[(int64_t)k * r + k] = sqrt(p);
+    const int i = k1 + blockIdx.x * kCRows + t;
+    if (t >= kCRows || i >= r) return;
+    double* row = S + (int64_t)i * r + k0;
+    double l[kCb];
+#pragma unroll
+    for (int j = 0; j < kCb; ++j) {
+        if (j < kb) {
+            double v = row[j];
+            for (int q = 0; q < j; ++q) v -= l[q] * Lb[j][q];
+            l[j] = v / Lb[j][j];
         }
-        __syncthreads();
-        if (bad) break;
-        const double lkk = S[(int64_t)k * r + k];
-        for (int i = k + 1 + tid; i < r; i += nt) S[(int64_t)i * r + k] /= lkk;
-        __syncthreads();
-        // trailing update of the lower triangle: S[i][j] -= L[i][k] L[j][k], k < j <= i; a warp per row i, its
-        // lanes along j
-        for (int i = k + 1 + warp; i < r; i += nwarps) {
-            const double lik = S[(int64_t)i * r + k];
-            for (int j = k + 1 + lane; j <= i; j += 32) S[(int64_t)i * r + j] -= lik * S[(int64_t)j * r + k];
+    }
+#pragma unroll
+    for (int j = 0; j < kCb; ++j)
+        if (j < kb) row[j] = l[j];
+}
+
+// S[i][j] -= sum_{t < kb} L[i][k0 + t] L[j][k0 + t] for k0 + kb <= j <= i < r, a 16 x 16 tile per CTA
+__global__ void __launch_bounds__(kCT * kCT) chol_update_kernel(double* S, int r, int k0, const uint32_t* check) {
+    if (not_pd(check)) return;
+    __shared__ double Li[kCT][kCb + 1], Lj[kCT][kCb + 1];
+    const int kb = min(kCb, r - k0), k1 = k0 + kb;
+    const int nt = (int)cdiv(r - k1, kCT);
+    int lin = blockIdx.x, bi = 0;                    // lower-triangle tile (bj <= bi) from the linear index
+    while (lin > bi) {
+        lin -= bi + 1;
+        ++bi;
+    }
+    const int bj = lin;
+    if (bi >= nt) return;
+    const int i0 = k1 + bi * kCT, j0 = k1 + bj * kCT, tid = threadIdx.x;
+    for (int e = tid; e < kCT * kb; e += kCT * kCT) {
+        const int a = e / kb, q = e - (e / kb) * kb;
+        Li[a][q] = i0 + a < r ? S[(int64_t)(i0 + a) * r + k0 + q] : 0.0;
+        Lj[a][q] = j0 + a < r ? S[(int64_t)(j0 + a) * r + k0 + q] : 0.0;
+    }
+    __syncthreads();
+    const int a = tid / kCT, c = tid % kCT, i = i0 + a, j = j0 + c;
+    if (i >= r || j > i) return;
+    double acc = 0.0;
+    for (int q = 0; q < kb; ++q) acc += Li[a][q] * Lj[c][q];
+    S[(int64_t)i * r + j] -= acc;
+}
+
+__global__ void chol_out_kernel(const double* __restrict__ S, int r, float* __restrict__ Lf, const uint32_t* check) {
+    if (not_pd(check)) return;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= (int64_t)r * r) return;
+    const int i = (int)(e / r), j = (int)(e - (e / r) * r);
+    Lf[e] = j <= i ? (float)S[e] : 0.0f;
+}
+
+cudaError_t cholesky(double* S, int r, float* Lf, double* floor_p, uint32_t* check, cudaStream_t st) {
+    chol_floor_kernel<<<1, 256, 0, st>>>(S, r, floor_p);
+    cudaError_t e = cudaGetLastError();
+    for (int k0 = 0; k0 < r && e == cudaSuccess; k0 += kCb) {
+        const int kb = std::min(kCb, r - k0), n = r - k0 - kb;
+        chol_diag_kernel<<<1, 32, 0, st>>>(S, r, k0, floor_p, check);
+        if (n > 0) {
+            chol_rows_kernel<<<(unsigned)cdiv(n, kCRows), 32, 0, st>>>(S, r, k0, check);
+            const int nt = (int)cdiv(n, kCT);
+            chol_update_kernel<<<(unsigned)(nt * (nt + 1) / 2), kCT * kCT, 0, st>>>(S, r, k0, check);
         }
-        __syncthreads();
+        e = cudaGetLastError();
     }
-    if (bad) {
-        if (tid == 0) flag(check, LOWRAM_CHECK_NOT_PD);
-        return;
-    }
-    for (int64_t e = tid; e < (int64_t)r * r; e += nt) {
-        const int i = (int)(e / r), j = (int)(e - (int64_t)i * r);
-        Lf[e] = j <= i ? (float)S[e] : 0.0f;
-    }
+    if (e != cudaSuccess) return e;
+    chol_out_kernel<<<(unsigned)cdiv((int64_t)r * r, 256), 256, 0, st>>>(S, r, Lf, check);
+    return cudaGetLastError();
 }
 
 // Q = Z R^-1 with R = L^T: each row q of Q solves q L^T = z, i.e. q_j = (z_j - sum_{k<j} q_k L[j][k]) / L[j][j]
@@ -273,36 +333,70 @@ cudaError_t gram(const float* X, int64_t N, int D, TAcc* C, int sms, cudaStream_
     return cudaGetLastError();
 }
 
-cudaError_t sgemm(const float* A, const float* B, int M, int K, int Nc, float* C, cudaStream_t st) {
-    const dim3 grid((unsigned)cdiv(Nc, kFT), (unsigned)cdiv(M, kFT));
-    sgemm_kernel<<<grid, kFThreads, 0, st>>>(A, B, M, K, Nc, C);
-    return cudaGetLastError();
-}
-
 }  // namespace
 
-size_t fit_workspace_bytes(int64_t N, int D, int r) {
+// Workspace: X [N, D] float32; the three bf16 terms of X^T [Dp, Np], of the Gram matrix [Dp, Dp] and of Q^T
+// [Rp, Dp] (Np = N rounded up to 64, Dp = D to 256, Rp = r to 256: the tensor-core tiles); the Gram matrix [D, D],
+// Q and Z [D, r] float32; S [r, r] fp64, Lf [r, r] float32 and the pivot floor.
+namespace {
+struct FitLayout {
+    int64_t Np, Dp, Rp;
+    size_t x, xt, gm, gt, qt, q, z, s, lf, fl, total;
+};
+FitLayout fit_layout(int64_t N, int D, int r) {
     auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    return a(sizeof(float) * (size_t)N * D) + a(sizeof(float) * (size_t)D * D) + 2 * a(sizeof(float) * (size_t)D * r) +
-           a(sizeof(double) * (size_t)r * r) + a(sizeof(float) * (size_t)r * r);
+    FitLayout L;
+    L.Np = cdiv(N, 64) * 64;
+    L.Dp = cdiv(D, 256) * 256;
+    L.Rp = cdiv(r, 256) * 256;
+    size_t o = 0;
+    L.x = o;
+    o += a(sizeof(float) * (size_t)N * D);
+    L.xt = o;
+    o += 3 * a(2 * (size_t)L.Dp * L.Np);
+    L.gm = o;
+    o += a(sizeof(float) * (size_t)D * D);
+    L.gt = o;
+    o += 3 * a(2 * (size_t)L.Dp * L.Dp);
+    L.qt = o;
+    o += 3 * a(2 * (size_t)L.Rp * L.Dp);
+    L.q = o;
+    o += a(sizeof(float) * (size_t)D * r);
+    L.z = o;
+    o += a(sizeof(float) * (size_t)D * r);
+    L.s = o;
+    o += a(sizeof(double) * (size_t)r * r);
+    L.lf = o;
+    o += a(sizeof(float) * (size_t)r * r);
+    L.fl = o;
+    o += a(sizeof(double));
+    L.total = o;
+    return L;
 }
+}  // namespace
+
+size_t fit_workspace_bytes(int64_t N, int D, int r) { return fit_layout(N, D, r).total; }
 
 cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st) {
-    auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
     const int64_t N = (int64_t)f.B * f.T;
     const int D = f.G * f.H_kv * f.d, r = f.r;
+    const FitLayout L = fit_layout(N, D, r);
     char* w = (char*)f.scratch;
-    float* X = (float*)w;
-    w += a(sizeof(float) * (size_t)N * D);
-    float* Gm = (float*)w;
-    w += a(sizeof(float) * (size_t)D * D);
-    float* Q = (float*)w;
-    w += a(sizeof(float) * (size_t)D * r);
-    float* Z = (float*)w;
-    w += a(sizeof(float) * (size_t)D * r);
-    double* S = (double*)w;
-    w += a(sizeof(double) * (size_t)r * r);
-    float* Lf = (float*)w;
+    float* X = (float*)(w + L.x);
+    auto terms = [&](size_t off, int64_t rows, int64_t cols, void* (&t)[3]) {
+        const size_t step = ((2 * (size_t)rows * cols) + 255) & ~(size_t)255;
+        for (int i = 0; i < 3; ++i) t[i] = w + off + i * step;
+    };
+    void *Xt[3], *Gt[3], *Qt[3];
+    terms(L.xt, L.Dp, L.Np, Xt);
+    terms(L.gt, L.Dp, L.Dp, Gt);
+    terms(L.qt, L.Rp, L.Dp, Qt);
+    float* Gm = (float*)(w + L.gm);
+    float* Q = (float*)(w + L.q);
+    float* Z = (float*)(w + L.z);
+    double* S = (double*)(w + L.s);
+    float* Lf = (float*)(w + L.lf);
+    double* floor_p = (double*)(w + L.fl);
 
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -318,7 +412,12 @@ cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st) {
                                                                         f.rope_cos, f.rope_sin, f.max_pos,
                                                                         f.post_rope, f.check, X);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = gram<float>(X, N, D, Gm, sms, st)) != cudaSuccess) return e;
+    // Gram matrix X^T X on the tensor cores: the terms of X^T [Dp, Np] (reduction over tokens along the rows)
+    if ((e = launch_split3(X, (int)N, D, D, true, (int)L.Dp, (int)L.Np, Xt, st)) != cudaSuccess) return e;
+    if ((e = launch_split_gemm_tc(Xt, Xt, D, D, (int)L.Dp, (int)L.Dp, (int)L.Np, true, Gm, D, f.check, st)) !=
+        cudaSuccess)
+        return e;
+    if ((e = launch_split3(Gm, D, D, D, false, (int)L.Dp, (int)L.Dp, Gt, st)) != cudaSuccess) return e;
     init_normal_kernel<<<(unsigned)cdiv((int64_t)D * r, 256), 256, 0, st>>>(Q, (int64_t)D * r, f.seed);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // Cholesky QR of Z into Q: Z^T Z = L L^T (fp64), Q = Z L^-T by row-wise forward substitution
@@ -329,13 +428,16 @@ cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st) {
     auto chol_qr = [&](const float* Zin, float* Qout) -> cudaError_t {
         cudaError_t e2 = gram<double>(Zin, D, r, S, sms, st);
         if (e2 != cudaSuccess) return e2;
-        chol_kernel<<<1, 1024, 0, st>>>(S, r, Lf, f.check);
-        if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
+        if ((e2 = cholesky(S, r, Lf, floor_p, f.check, st)) != cudaSuccess) return e2;
         trsm_rows_kernel<<<(unsigned)cdiv(D, kTrsmWarps), kTrsmWarps * 32, trsm_smem, st>>>(Zin, Lf, D, r, Qout);
         return cudaGetLastError();
     };
     for (int it = 0; it < f.iters; ++it) {
-        if ((e = sgemm(Gm, Q, D, D, r, Z, st)) != cudaSuccess) return e;
+        // Z = G Q on the tensor cores: the terms of Q^T [Rp, Dp]
+        if ((e = launch_split3(Q, D, r, r, true, (int)L.Rp, (int)L.Dp, Qt, st)) != cudaSuccess) return e;
+        if ((e = launch_split_gemm_tc(Gt, Qt, D, r, (int)L.Dp, (int)L.Rp, (int)L.Dp, false, Z, r, f.check, st)) !=
+            cudaSuccess)
+            return e;
         if ((e = chol_qr(Z, Q)) != cudaSuccess) return e;
     }
     if ((e = cudaMemcpyAsync(Z, Q, sizeof(float) * (size_t)D * r, cudaMemcpyDeviceToDevice, st)) != cudaSuccess) return e;
