@@ -72,20 +72,21 @@ __global__ void __launch_bounds__(kFThreads) gram_kernel(const float* __restrict
     const int i0 = bi * kFT, j0 = bj * kFT;
     const int64_t per = (N + n_split - 1) / n_split;
     const int64_t n_begin = blockIdx.z * per, n_end = min(N, n_begin + per);
-    __shared__ float As[kFK][kFT + 4], Bs[kFK][kFT + 4];
+    // operands converted once, on their way into shared memory (an fp64 conversion costs as much as an fp64 FMA)
+    __shared__ TAcc As[kFK][kFT + 4], Bs[kFK][kFT + 4];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     TAcc acc[4][4] = {};
     for (int64_t n0 = n_begin; n0 < n_end; n0 += kFK) {
         for (int e = tid; e < kFK * kFT; e += kFThreads) {
             const int r = e / kFT, c = e % kFT;
             const int64_t n = n0 + r;
-            As[r][c] = (n < n_end && i0 + c < D) ? X[n * D + i0 + c] : 0.0f;
-            Bs[r][c] = (n < n_end && j0 + c < D) ? X[n * D + j0 + c] : 0.0f;
+            As[r][c] = (TAcc)((n < n_end && i0 + c < D) ? X[n * D + i0 + c] : 0.0f);
+            Bs[r][c] = (TAcc)((n < n_end && j0 + c < D) ? X[n * D + j0 + c] : 0.0f);
         }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < kFK; ++k) {
-            float a[4], b[4];
+            TAcc a[4], b[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 a[u] = As[k][ty * 4 + u];
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(kFThreads) gram_kernel(const float* __restrict
 #pragma unroll
             for (int u = 0; u < 4; ++u)
 #pragma unroll
-                for (int v = 0; v < 4; ++v) acc[u][v] += (TAcc)a[u] * (TAcc)b[v];
+                for (int v = 0; v < 4; ++v) acc[u][v] += a[u] * b[v];
         }
         __syncthreads();
     }
@@ -133,13 +134,12 @@ __global__ void init_normal_kernel(float* Q, int64_t n, uint64_t seed) {
 
 // Blocked Cholesky of S [r, r] fp64 (S = L L^T, L lower, written over S's lower triangle), panel by panel
 // (kCb columns) over many CTAs: the panel's diagonal block is factored by one CTA, the rows below it are solved
-// against it (L21 = S21 L11^-T) a thread per row, and the trailing lower triangle takes the panel's product
+// against it (L21 = S21 L11^-T) a warp per row, and the trailing lower triangle takes the panel's product
 // (S22 -= L21 L21^T) in 16 x 16 tiles.  A pivot at or below 1e-10 of the largest diagonal entry of S (rounding
 // noise of float32 iterates: the keys have rank below r) sets LOWRAM_CHECK_NOT_PD; every later kernel of the
 // factorization then returns at once and the fit's result is void.  The float32 copy Lf [r, r] (lower
 // triangle; zeros above) is what the triangular solve reads.
 constexpr int kCb = 32;
-constexpr int kCRows = 16;   // rows a CTA solves
 constexpr int kCT = 16;      // trailing-update tile edge
 
 __device__ __forceinline__ bool not_pd(const uint32_t* check) {
@@ -163,62 +163,70 @@ __global__ void __launch_bounds__(256) chol_floor_kernel(const double* __restric
     }
 }
 
-// the diagonal block of panel k0 (kb x kb), one warp: lane i owns row i; right-looking, one pivot at a time
-__global__ void __launch_bounds__(32) chol_diag_kernel(double* S, int r, int k0, const double* floor_p,
-                                                       uint32_t* check) {
+// the diagonal block of panel k0 (kb x kb): thread (i, j) = (warp, lane) holds element (i, j) of the lower
+// triangle in a register; per pivot k the pivot thread takes one reciprocal square root, the column threads scale
+// and publish column k, and every thread below and right of the pivot takes its one product
+__global__ void __launch_bounds__(kCb * kCb) chol_diag_kernel(double* S, int r, int k0, const double* floor_p,
+                                                              uint32_t* check) {
     if (not_pd(check)) return;
-    __shared__ double Lb[kCb][kCb + 1];
-    const int kb = min(kCb, r - k0), lane = threadIdx.x;
-    for (int j = 0; j < kb; ++j)
-        if (lane < kb) Lb[lane][j] = S[(int64_t)(k0 + lane) * r + k0 + j];
-    __syncwarp();
+    __shared__ double col[kCb];
+    __shared__ double s_rl;
+    __shared__ int s_bad;
+    const int kb = min(kCb, r - k0), i = threadIdx.x >> 5, j = threadIdx.x & 31;
+    const bool in = i < kb && j <= i;
+    double a = in ? S[(int64_t)(k0 + i) * r + k0 + j] : 0.0;
     const double fl = *floor_p;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
     for (int k = 0; k < kb; ++k) {
-        const double p = Lb[k][k];
-        if (!(p > fl)) {
-            if (lane == 0) flag(check, LOWRAM_CHECK_NOT_PD);
-            return;
+        if (i == k && j == k) {
+            if (!(a > fl)) {
+                s_bad = 1;
+            } else {
+                const double rl = rsqrt(a);   // 1 / l_kk
+                s_rl = rl;
+                a *= rl;                      // l_kk
+            }
         }
-        const double lkk = sqrt(p);
-        __syncwarp();
-        if (lane == k) Lb[k][k] = lkk;
-        if (lane > k && lane < kb) Lb[lane][k] /= lkk;
-        __syncwarp();
-        if (lane > k && lane < kb) {
-            const double lik = Lb[lane][k];
-            for (int j = k + 1; j <= lane; ++j) Lb[lane][j] -= lik * Lb[j][k];
+        __syncthreads();
+        if (s_bad) break;                     // the same answer in every thread
+        if (j == k && i > k && i < kb) {
+            a *= s_rl;                        // l_ik
+            col[i] = a;
         }
-        __syncwarp();
+        __syncthreads();
+        if (in && j > k) a -= col[i] * col[j];   // i >= j > k
     }
-    for (int j = 0; j < kb; ++j)
-        if (lane < kb && j <= lane) S[(int64_t)(k0 + lane) * r + k0 + j] = Lb[lane][j];
+    if (s_bad) {
+        if (threadIdx.x == 0) flag(check, LOWRAM_CHECK_NOT_PD);
+        return;
+    }
+    if (in) S[(int64_t)(k0 + i) * r + k0 + j] = a;
 }
 
-// rows i >= k0 + kb of panel k0: l_ij = (s_ij - sum_{t<j} l_it l_jt) / l_jj, a thread per row
-__global__ void __launch_bounds__(32) chol_rows_kernel(double* S, int r, int k0, const uint32_t* check) {
+// rows i >= k0 + kb of panel k0, a warp per row, lane t holding s_it: right-looking, so step j needs no reduction:
+// l_ij = s_ij / l_jj is final on lane j, and every lane t > j takes s_it -= l_ij l_tj
+constexpr int kCRowWarps = 4;
+__global__ void __launch_bounds__(kCRowWarps * 32) chol_rows_kernel(double* S, int r, int k0, const uint32_t* check) {
     if (not_pd(check)) return;
-    __shared__ double Lb[kCb][kCb + 1];
-    const int kb = min(kCb, r - k0), k1 = k0 + kb, t = threadIdx.x;
-    for (int e = t; e < kb * kb; e += 32) {
+    __shared__ double Lb[kCb][kCb + 1], rinv[kCb];
+    const int kb = min(kCb, r - k0), k1 = k0 + kb, tid = threadIdx.x;
+    for (int e = tid; e < kb * kb; e += kCRowWarps * 32) {
         const int i = e / kb, j = e - (e / kb) * kb;
         Lb[i][j] = j <= i ? S[(int64_t)(k0 + i) * r + k0 + j] : 0.0;
     }
+    if (tid < kb) rinv[tid] = 1.0 / S[(int64_t)(k0 + tid) * r + k0 + tid];   // one division per lane, in parallel
     __syncthreads();
-    const int i = k1 + blockIdx.x * kCRows + t;
-    if (t >= kCRows || i >= r) return;
+    const int lane = tid & 31, i = k1 + blockIdx.x * kCRowWarps + (tid >> 5);
+    if (i >= r) return;
     double* row = S + (int64_t)i * r + k0;
-    double l[kCb];
-#pragma unroll
-    for (int j = 0; j < kCb; ++j) {
-        if (j < kb) {
-            double v = row[j];
-            for (int q = 0; q < j; ++q) v -= l[q] * Lb[j][q];
-            l[j] = v / Lb[j][j];
-        }
+    double v = lane < kb ? row[lane] : 0.0;
+    for (int j = 0; j < kb; ++j) {
+        const double lj = __shfl_sync(0xffffffffu, v * rinv[j], j);
+        if (lane == j) v = lj;
+        else if (lane > j && lane < kb) v -= lj * Lb[lane][j];
     }
-#pragma unroll
-    for (int j = 0; j < kCb; ++j)
-        if (j < kb) row[j] = l[j];
+    if (lane < kb) row[lane] = v;
 }
 
 // S[i][j] -= sum_{t < kb} L[i][k0 + t] L[j][k0 + t] for k0 + kb <= j <= i < r, a 16 x 16 tile per CTA
@@ -261,9 +269,9 @@ cudaError_t cholesky(double* S, int r, float* Lf, double* floor_p, uint32_t* che
     cudaError_t e = cudaGetLastError();
     for (int k0 = 0; k0 < r && e == cudaSuccess; k0 += kCb) {
         const int kb = std::min(kCb, r - k0), n = r - k0 - kb;
-        chol_diag_kernel<<<1, 32, 0, st>>>(S, r, k0, floor_p, check);
+        chol_diag_kernel<<<1, kCb * kCb, 0, st>>>(S, r, k0, floor_p, check);
         if (n > 0) {
-            chol_rows_kernel<<<(unsigned)cdiv(n, kCRows), 32, 0, st>>>(S, r, k0, check);
+            chol_rows_kernel<<<(unsigned)cdiv(n, kCRowWarps), kCRowWarps * 32, 0, st>>>(S, r, k0, check);
             const int nt = (int)cdiv(n, kCT);
             chol_update_kernel<<<(unsigned)(nt * (nt + 1) / 2), kCT * kCT, 0, st>>>(S, r, k0, check);
         }
@@ -275,28 +283,75 @@ cudaError_t cholesky(double* S, int r, float* Lf, double* floor_p, uint32_t* che
 }
 
 // Q = Z R^-1 with R = L^T: each row q of Q solves q L^T = z, i.e. q_j = (z_j - sum_{k<j} q_k L[j][k]) / L[j][j]
-// (forward substitution; L's row j is contiguous).  A warp per row; the row's solution so far in shared memory.
+// (forward substitution; L's row j is contiguous, and zero above the diagonal).  A warp solves ROWS rows together,
+// so each row of L it reads from L2 serves all of them; the rows' solutions so far live in shared memory.  The
+// first 512 columns of L's next row are loaded into registers while the current row is applied (16 a lane), so
+// the steps do not wait on L2 one after another; columns past 512 (r > 512) are loaded in batches of 512.
 constexpr int kTrsmWarps = 8;
+constexpr int kTrsmPre = 16;   // L values a lane holds per batch: 512 columns a warp
+template <int ROWS>
 __global__ void __launch_bounds__(kTrsmWarps * 32) trsm_rows_kernel(const float* __restrict__ Z,
                                                                     const float* __restrict__ Lf, int D, int r,
                                                                     float* __restrict__ Q) {
-    extern __shared__ float xs[];   // [kTrsmWarps][r]
+    extern __shared__ float xs[];   // [kTrsmWarps][ROWS][r]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * kTrsmWarps + warp;
-    if (row >= D) return;
-    float* x = xs + warp * r;
-    const float* z = Z + (int64_t)row * r;
+    const int row0 = (blockIdx.x * kTrsmWarps + warp) * ROWS;
+    if (row0 >= D) return;
+    float* x = xs + (size_t)warp * ROWS * r;
+    for (int e = lane; e < ROWS * r; e += 32) x[e] = 0.0f;   // rows past D stay zero
+    __syncwarp();
+    auto load_batch = [&](const float* lrow, int kb, float (&v)[kTrsmPre]) {
+#pragma unroll
+        for (int u = 0; u < kTrsmPre; ++u) {
+            const int k = kb + u * 32 + lane;
+            v[u] = k < r ? lrow[k] : 0.0f;
+        }
+    };
+    float nxt[kTrsmPre];
+    load_batch(Lf, 0, nxt);
     for (int j = 0; j < r; ++j) {
         const float* lj = Lf + (int64_t)j * r;
-        float acc = 0.0f;
-        for (int k = lane; k < j; k += 32) acc = fmaf(x[k], lj[k], acc);
+        float cur[kTrsmPre];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        const float v = (z[j] - acc) / lj[j];
-        if (lane == 0) x[j] = v;
+        for (int u = 0; u < kTrsmPre; ++u) cur[u] = nxt[u];
+        if (j + 1 < r) load_batch(lj + r, 0, nxt);            // row j+1, in flight during this step
+        const float ljj = lj[j];
+        const float zq = lane < ROWS && row0 + lane < D ? Z[(int64_t)(row0 + lane) * r + j] : 0.0f;
+        float acc[ROWS];
+#pragma unroll
+        for (int q = 0; q < ROWS; ++q) acc[q] = 0.0f;
+#pragma unroll
+        for (int u = 0; u < kTrsmPre; ++u) {
+            if (u * 32 >= j) break;                            // uniform over the warp
+            const int k = u * 32 + lane;
+            if (k < j)
+#pragma unroll
+                for (int q = 0; q < ROWS; ++q) acc[q] = fmaf(x[q * r + k], cur[u], acc[q]);
+        }
+        for (int kb = kTrsmPre * 32; kb < j; kb += kTrsmPre * 32) {
+            float v[kTrsmPre];
+            load_batch(lj, kb, v);
+#pragma unroll
+            for (int u = 0; u < kTrsmPre; ++u) {
+                const int k = kb + u * 32 + lane;
+                if (k < j)
+#pragma unroll
+                    for (int q = 0; q < ROWS; ++q) acc[q] = fmaf(x[q * r + k], v[u], acc[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < ROWS; ++q)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+        float mine = acc[0];                       // lane q finishes row q
+#pragma unroll
+        for (int q = 1; q < ROWS; ++q)
+            if (lane == q) mine = acc[q];
+        if (lane < ROWS && row0 + lane < D) x[lane * r + j] = (zq - mine) / ljj;
         __syncwarp();
     }
-    for (int j = lane; j < r; j += 32) Q[(int64_t)row * r + j] = x[j];
+    for (int q = 0; q < ROWS && row0 + q < D; ++q)
+        for (int j = lane; j < r; j += 32) Q[(int64_t)(row0 + q) * r + j] = x[q * r + j];
 }
 
 // The G output bases, passed by value.
@@ -421,15 +476,20 @@ cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st) {
     init_normal_kernel<<<(unsigned)cdiv((int64_t)D * r, 256), 256, 0, st>>>(Q, (int64_t)D * r, f.seed);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // Cholesky QR of Z into Q: Z^T Z = L L^T (fp64), Q = Z L^-T by row-wise forward substitution
-    const size_t trsm_smem = sizeof(float) * (size_t)kTrsmWarps * r;
-    if ((e = cudaFuncSetAttribute(trsm_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)trsm_smem)) !=
-        cudaSuccess)
+    // four rows per warp while their solutions fit in shared memory, else one
+    const bool four = sizeof(float) * (size_t)kTrsmWarps * 4 * r <= 200 * 1024;
+    const int trsm_rows = four ? 4 : 1;
+    const size_t trsm_smem = sizeof(float) * (size_t)kTrsmWarps * trsm_rows * r;
+    if ((e = cudaFuncSetAttribute(four ? trsm_rows_kernel<4> : trsm_rows_kernel<1>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)trsm_smem)) != cudaSuccess)
         return e;
     auto chol_qr = [&](const float* Zin, float* Qout) -> cudaError_t {
         cudaError_t e2 = gram<double>(Zin, D, r, S, sms, st);
         if (e2 != cudaSuccess) return e2;
         if ((e2 = cholesky(S, r, Lf, floor_p, f.check, st)) != cudaSuccess) return e2;
-        trsm_rows_kernel<<<(unsigned)cdiv(D, kTrsmWarps), kTrsmWarps * 32, trsm_smem, st>>>(Zin, Lf, D, r, Qout);
+        const unsigned grid = (unsigned)cdiv(D, kTrsmWarps * trsm_rows);
+        if (four) trsm_rows_kernel<4><<<grid, kTrsmWarps * 32, trsm_smem, st>>>(Zin, Lf, D, r, Qout);
+        else trsm_rows_kernel<1><<<grid, kTrsmWarps * 32, trsm_smem, st>>>(Zin, Lf, D, r, Qout);
         return cudaGetLastError();
     };
     for (int it = 0; it < f.iters; ++it) {
