@@ -698,8 +698,10 @@ def fit_bench(w, dev, args, pk):
         "rebuild_rel_err_sampled": err,
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "traffic": None,
-                     "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock",
-                     "work": "Gram N*D^2 (symmetric) + per iteration 2*D^2*r + 4*D*r^2 + 2r^3/3"}}))
+                     "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock (a reference scale: the Gram "
+                                  "matrix and Z = G Q run on the tensor cores as six bf16 products each, Z^T Z and "
+                                  "the Cholesky in fp64 on the CUDA cores)",
+                     "work": "float32-equivalent: Gram N*D^2 (symmetric) + per iteration 2*D^2*r + 4*D*r^2 + 2r^3/3"}}))
 
 
 def fit_predictor_bench(w, dev, args, pk):
