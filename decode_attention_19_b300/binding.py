@@ -141,7 +141,7 @@ def _load():
             "lowram_evict_plan_workspace_size": [i32, i32, psz],
             "lowram_evict_plan": [i32] * 5 + [_vp, _vp, _vp, sz, _vp],
             "lowram_predictor_grad": [i32] * 6 + [_vp] * 11 + [_vp],
-            "lowram_fit_predictor_workspace_size": [i32, i32, i32, psz],
+            "lowram_fit_predictor_workspace_size": [i32] * 5 + [psz],
             "lowram_fit_predictor": [i32] * 6 + [_vp, _vp, i32, flt, flt, flt, flt] + [_vp] * 6 + [sz, _vp],
             "lowram_fit_basis_workspace_size": [ctypes.POINTER(lowram_compress_shape), psz],
             "lowram_fit_basis": [ctypes.POINTER(lowram_compress_shape), _vp, _vp, _vp, _vp, i32, ctypes.c_uint64, _vp,
@@ -602,7 +602,7 @@ def lowram_fit_predictor(keys: torch.Tensor, values: torch.Tensor, w1: torch.Ten
     _pred_params(H_kv, d, m, w1, b1, w2, b2)
     dev = _dev(keys, values, w1, b1, w2, b2, workspace)
     n = ctypes.c_size_t(0)
-    _check(_load().lowram_fit_predictor_workspace_size(H_kv, d, m, ctypes.byref(n)))
+    _check(_load().lowram_fit_predictor_workspace_size(B, T, H_kv, d, m, ctypes.byref(n)))
     ws = _workspace(n.value, workspace, dev)
     losses = torch.empty((int(steps), H_kv), dtype=torch.float32, device=dev) if want_losses else None
     with _on(dev):

@@ -468,11 +468,11 @@ cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st) {
                                                                         f.post_rope, f.check, X);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // Gram matrix X^T X on the tensor cores: the terms of X^T [Dp, Np] (reduction over tokens along the rows)
-    if ((e = launch_split3(X, (int)N, D, D, true, (int)L.Dp, (int)L.Np, Xt, st)) != cudaSuccess) return e;
+    if ((e = launch_split3(X, false, (int)N, D, D, true, (int)L.Dp, (int)L.Np, Xt, st)) != cudaSuccess) return e;
     if ((e = launch_split_gemm_tc(Xt, Xt, D, D, (int)L.Dp, (int)L.Dp, (int)L.Np, true, Gm, D, f.check, st)) !=
         cudaSuccess)
         return e;
-    if ((e = launch_split3(Gm, D, D, D, false, (int)L.Dp, (int)L.Dp, Gt, st)) != cudaSuccess) return e;
+    if ((e = launch_split3(Gm, false, D, D, D, false, (int)L.Dp, (int)L.Dp, Gt, st)) != cudaSuccess) return e;
     init_normal_kernel<<<(unsigned)cdiv((int64_t)D * r, 256), 256, 0, st>>>(Q, (int64_t)D * r, f.seed);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // Cholesky QR of Z into Q: Z^T Z = L L^T (fp64), Q = Z L^-T by row-wise forward substitution
@@ -494,7 +494,7 @@ cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st) {
     };
     for (int it = 0; it < f.iters; ++it) {
         // Z = G Q on the tensor cores: the terms of Q^T [Rp, Dp]
-        if ((e = launch_split3(Q, D, r, r, true, (int)L.Rp, (int)L.Dp, Qt, st)) != cudaSuccess) return e;
+        if ((e = launch_split3(Q, false, D, r, r, true, (int)L.Rp, (int)L.Dp, Qt, st)) != cudaSuccess) return e;
         if ((e = launch_split_gemm_tc(Gt, Qt, D, r, (int)L.Dp, (int)L.Rp, (int)L.Dp, false, Z, r, f.check, st)) !=
             cudaSuccess)
             return e;

@@ -158,12 +158,12 @@ struct FitArgs {
 size_t fit_workspace_bytes(int64_t N, int D, int r);
 cudaError_t launch_fit_basis(const FitArgs& f, cudaStream_t st);
 // tc_fit.cu: float32 products of the fit on the tensor cores through an exact three-term bf16 split.
-// launch_split3 writes the h, m, l terms of src [R, Cc] (row stride lds), or of its transpose, as [out_rows, out_cols]
-// bf16, zero past the source.  launch_split_gemm_tc sets C[M, N] (row stride ldc) = A B^T from the terms of A [Mp, Kp]
-// and B [Np, Kp] (Mp a multiple of 128, Np of 256, Kp of 64); sym: A = B and only the tiles meeting the upper
-// triangle run, each writing its upper entries and their mirrors.
-cudaError_t launch_split3(const float* src, int R, int Cc, int64_t lds, bool transpose, int out_rows, int out_cols,
-                          void* const out[3], cudaStream_t st);
+// launch_split3 writes the h, m, l terms of src [R, Cc] (float32, or bf16 when src_bf16; row stride lds), or of its
+// transpose, as [out_rows, out_cols] bf16, zero past the source.  launch_split_gemm_tc sets C[M, N] (row stride ldc)
+// = A B^T from the terms of A [Mp, Kp] and B [Np, Kp] (Mp and Np multiples of 128, Kp of 64); sym: A = B and only
+// the tiles meeting the upper triangle run, each writing its upper entries and their mirrors.
+cudaError_t launch_split3(const void* src, bool src_bf16, int R, int Cc, int64_t lds, bool transpose, int out_rows,
+                          int out_cols, void* const out[3], cudaStream_t st);
 cudaError_t launch_split_gemm_tc(const void* const a[3], const void* const b[3], int M, int N, int Mp, int Np, int Kp,
                                  bool sym, float* C, int ldc, uint32_t* check, cudaStream_t st);
 

@@ -477,12 +477,14 @@ lowram_status lowram_predictor_grad(int32_t B, int32_t T, int32_t H_kv, int32_t 
     return e == cudaSuccess ? LOWRAM_OK : cuda_fail(e, "predictor_grad");
 }
 
-lowram_status lowram_fit_predictor_workspace_size(int32_t H_kv, int32_t d, int32_t m, size_t* bytes) {
-    lowram_status st = check_predictor_shape(0, 0, H_kv, d, m, LOWRAM_F32);
+lowram_status lowram_fit_predictor_workspace_size(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m,
+                                                  size_t* bytes) {
+    lowram_status st = check_predictor_shape(B, T, H_kv, d, m, LOWRAM_F32);
     if (st != LOWRAM_OK) return st;
     if (!bytes) return fail(LOWRAM_ERR_INVALID_ARG, "bytes is NULL");
-    // gradient, first and second moments of every parameter, and a loss row
-    *bytes = kHeader + 3 * align256(sizeof(float) * predictor_params(H_kv, d, m)) + align256(sizeof(float) * H_kv);
+    // gradient, first and second moments of every parameter, a loss row, and the tensor-core products' scratch
+    *bytes = kHeader + 3 * align256(sizeof(float) * predictor_params(H_kv, d, m)) + align256(sizeof(float) * H_kv) +
+             align256(predictor_tc_scratch_bytes((int64_t)B * T, H_kv, d, m));
     return LOWRAM_OK;
 }
 
@@ -494,7 +496,7 @@ lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d
     lowram_status st = check_predictor_shape(B, T, H_kv, d, m, dtype);
     if (st != LOWRAM_OK) return st;
     size_t need = 0;
-    lowram_fit_predictor_workspace_size(H_kv, d, m, &need);
+    lowram_fit_predictor_workspace_size(B, T, H_kv, d, m, &need);
     if (!workspace || workspace_bytes < need || !aligned16(workspace))
         return fail(LOWRAM_ERR_WORKSPACE, "workspace %zu bytes, %zu needed", workspace ? workspace_bytes : 0, need);
     if (steps < 0) return fail(LOWRAM_ERR_INVALID_ARG, "steps=%d", steps);
@@ -512,6 +514,8 @@ lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d
     float* mom = (float*)(ws + seg);
     float* vel = (float*)(ws + 2 * seg);
     float* loss_tmp = (float*)(ws + 3 * seg);
+    void* tc_scratch = ws + 3 * seg + align256(sizeof(float) * H_kv);
+    uint32_t* check = (uint32_t*)workspace;   // the header's check word: LOWRAM_CHECK_TIMEOUT from the products
     // the four parameter tensors and their slices of the gradient / moment buffers
     const size_t n1 = (size_t)H_kv * m * d, nb1 = (size_t)H_kv * m, nb2 = (size_t)H_kv * d;
     float* params[4] = {w1, b1, w2, b2};
@@ -520,11 +524,17 @@ lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d
     off[0] = 0;
     for (int i = 1; i < 4; ++i) off[i] = off[i - 1] + count[i - 1];
     cudaError_t e = cudaMemsetAsync(mom, 0, 2 * seg, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(check, 0, sizeof(uint32_t), cs);
+    if (e == cudaSuccess && steps > 0) {
+        const PredictorFitArgs a0{B, T, H_kv, d, m, dtype == LOWRAM_BF16, keys, values, w1, b1, w2, b2, loss_tmp,
+                                  grad + off[0], grad + off[1], grad + off[2], grad + off[3]};
+        e = launch_predictor_prep_tc(a0, tc_scratch, cs);
+    }
     for (int s_ = 0; s_ < steps && e == cudaSuccess; ++s_) {
         PredictorFitArgs a{B, T, H_kv, d, m, dtype == LOWRAM_BF16, keys, values, w1, b1, w2, b2,
                            losses_out ? losses_out + (size_t)s_ * H_kv : loss_tmp, grad + off[0], grad + off[1],
                            grad + off[2], grad + off[3]};
-        e = launch_predictor_grad(a, cs);
+        e = launch_predictor_grad_tc(a, tc_scratch, check, cs);
         for (int i = 0; i < 4 && e == cudaSuccess; ++i)
             e = launch_adam(params[i], grad + off[i], mom + off[i], vel + off[i], (int64_t)count[i], lr, beta1, beta2,
                             eps, s_ + 1, cs);

@@ -10,12 +10,13 @@
 // bf16 MMAs with float32 accumulation.  So C = A B^T over float32 A [M, K] and B [N, K] is one tcgen05
 // accumulation chain over six (A term, B term) pairs times K / 64 reduction chunks.
 //
-// Operands are K-major bf16 terms, zero-padded (rows of A to a multiple of 128, rows of B to 256, K to 64): the
-// split kernel writes them, transposing when the float32 matrix holds the reduction along its rows (the keys
-// [tokens, D] for the Gram matrix, the iterate Q [D, r]).  One CTA of 128 threads per 128 x 256 output tile:
-// thread 0 TMA-loads a 16 KB A chunk and a 32 KB B chunk per stage into a 4-stage 128-byte-swizzled ring,
-// thread 32 issues four M=128, N=256, K=16 MMAs per chunk into a 256-column TMEM accumulator, and the four warps
-// then read their 32 TMEM lanes and add the tile into C (zeroed first) with float32 reductions, so a tile's
+// Operands are K-major bf16 terms, zero-padded (rows of A and of B to a multiple of 128, K to 64): the split
+// kernel writes them, transposing when the float32 matrix holds the reduction along its rows (the keys
+// [tokens, D] for the Gram matrix, the iterate Q [D, r]).  One CTA of 128 threads per 128 x BN output tile (BN = 256,
+// or 128 when B's padded rows are not a multiple of 256): thread 0 TMA-loads a 16 KB A chunk and a BN x 128 B
+// B chunk per stage into a 4-stage 128-byte-swizzled ring, thread 32 issues four M=128, N=BN, K=16 MMAs per chunk
+// into a BN-column TMEM accumulator, and the four warps then read their 32 TMEM lanes and add the tile into C
+// (zeroed first) with float32 reductions, so a tile's
 // reduction may be split over several CTAs (gridDim.z) when the tiles alone do not fill the GPU.  For a symmetric
 // product (the Gram matrix, A = B) tiles wholly below the diagonal are skipped and every other tile adds its
 // entries on or above the diagonal and their mirrors.  Every wait is bounded: on a timeout the CTA sets
@@ -28,21 +29,21 @@ namespace lowram {
 namespace {
 
 constexpr int kGM = 128;                  // output rows per tile (TMEM lanes)
-constexpr int kGN = 256;                  // output columns per tile (TMEM columns)
 constexpr int kGK = 64;                   // reduction elements per chunk: one 128-byte swizzled row
 constexpr int kGStages = 4;
 constexpr int kGThreads = 128;
 constexpr int kGPairs = 6;
 constexpr uint32_t kGABytes = kGM * kGK * 2;    // 16 KB
-constexpr uint32_t kGBBytes = kGN * kGK * 2;    // 32 KB
-constexpr int kGSmem = 1024 /* alignment */ + kGStages * (kGABytes + kGBBytes) + 256;
+// BN = output columns per tile (TMEM columns): 256, or 128 when B's rows are not a multiple of 256
+__host__ __device__ constexpr uint32_t g_bbytes(int BN) { return (uint32_t)BN * kGK * 2; }
+__host__ __device__ constexpr int g_smem(int BN) { return 1024 /* alignment */ + kGStages * (int)(kGABytes + g_bbytes(BN)) + 256; }
 // the six products, largest first: pair p multiplies A term (kPairA >> 4p) & 15 by B term (kPairB >> 4p) & 15
 // (0 = h, 1 = m, 2 = l): hh, hm, mh, hl, lh, mm
 constexpr uint32_t kPairA = 0x120100u, kPairB = 0x102010u;
 
 struct SplitMaps {
     CUtensorMap a[3];   // A's terms [Mp, Kp], box 64 x 128
-    CUtensorMap b[3];   // B's terms [Np, Kp], box 64 x 256
+    CUtensorMap b[3];   // B's terms [Np, Kp], box 64 x BN
 };
 
 struct SplitGemmParams {
@@ -55,11 +56,13 @@ struct SplitGemmParams {
     uint32_t* check;
 };
 
+template <int BN>
 __global__ void __launch_bounds__(kGThreads, 1)
     split_gemm_tc_kernel(const __grid_constant__ SplitMaps maps, SplitGemmParams p) {
     using namespace tc;
-    const int row0 = blockIdx.y * kGM, col0 = blockIdx.x * kGN;
-    if (p.sym && col0 + kGN <= row0) return;          // below the diagonal: the mirror of a computed tile
+    constexpr uint32_t kGBBytes = g_bbytes(BN);
+    const int row0 = blockIdx.y * kGM, col0 = blockIdx.x * BN;
+    if (p.sym && col0 + BN <= row0) return;           // below the diagonal: the mirror of a computed tile
     const int total = kGPairs * p.KC;
     const int per = (total + p.n_split - 1) / p.n_split;
     const int c_begin = blockIdx.z * per, n_chunks = min(total, c_begin + per) - c_begin;
@@ -67,7 +70,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* As = smem;                                // [stage][128 rows x 128 B]
-    uint8_t* Bs = As + kGStages * kGABytes;            // [stage][256 rows x 128 B]
+    uint8_t* Bs = As + kGStages * kGABytes;            // [stage][BN rows x 128 B]
     uint64_t* full = (uint64_t*)(Bs + kGStages * kGBBytes);
     uint64_t* empty = full + kGStages;
     uint64_t* done = empty + kGStages;
@@ -94,7 +97,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, kGN);
+        tmem_alloc(tmem_slot, BN);
         tmem_relinquish();
     }
     fence_before();
@@ -121,8 +124,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         *issued_s = i;
     } else if (tid == 32) {
-        // MMAs: D [128 x 256] (+)= A chunk [128 x 64] B chunk [256 x 64]^T, four K=16 steps per chunk
-        const uint32_t idesc = idesc_bf16(kGM, kGN);
+        // MMAs: D [128 x BN] (+)= A chunk [128 x 64] B chunk [BN x 64]^T, four K=16 steps per chunk
+        const uint32_t idesc = idesc_bf16(kGM, BN);
         int i = 0;
         for (; i < n_chunks; ++i) {
             const int s = i % kGStages;
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int i = row0 + warp * 32 + lane;
         const uint32_t tw = tmem + ((uint32_t)(warp * 32) << 16);
         float* Ci = p.C + (int64_t)i * p.ldc;
-        for (int cb = 0; cb < kGN && col0 + cb < p.N; cb += 64) {
+        for (int cb = 0; cb < BN && col0 + cb < p.N; cb += 64) {
             float x[32], y[32];
             tmem_ld_2x32(tw + (uint32_t)cb, tw + (uint32_t)cb + 32u, x, y);
             if (i < p.M) {
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     __syncthreads();
     if (warp == 0) {
         fence_after();
-        tmem_dealloc(tmem, kGN);
+        tmem_dealloc(tmem, BN);
     }
 }
 
@@ -191,7 +194,8 @@ __device__ __forceinline__ void split3(float x, __nv_bfloat16& h, __nv_bfloat16&
 // out_t[orow][ocol] for t = h, m, l (each [out_rows, out_cols] bf16): the terms of src[orow][ocol], or of
 // src[ocol][orow] when transposing; zero outside src [R, Cc] (row stride lds).  32 x 32 tiles through shared
 // memory, so both the reads and the writes are coalesced.
-__global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ src, int R, int Cc, int64_t lds,
+template <typename TS>
+__global__ void __launch_bounds__(256) split3_kernel(const TS* __restrict__ src, int R, int Cc, int64_t lds,
                                                      int transpose, int out_rows, int out_cols,
                                                      __nv_bfloat16* __restrict__ oh, __nv_bfloat16* __restrict__ om,
                                                      __nv_bfloat16* __restrict__ ol) {
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ s
     const int64_t sr0 = transpose ? ocol0 : orow0, sc0 = transpose ? orow0 : ocol0;
     for (int k = ty; k < 32; k += 8) {
         const int64_t sr = sr0 + k, sc = sc0 + tx;
-        tile[k][tx] = (sr < R && sc < Cc) ? src[sr * lds + sc] : 0.0f;
+        tile[k][tx] = (sr < R && sc < Cc) ? ld(src, sr * lds + sc) : 0.0f;
     }
     __syncthreads();
     for (int k = ty; k < 32; k += 8) {
@@ -220,31 +224,37 @@ __global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ s
 
 }  // namespace
 
-cudaError_t launch_split3(const float* src, int R, int Cc, int64_t lds, bool transpose, int out_rows, int out_cols,
-                          void* const out[3], cudaStream_t st) {
+cudaError_t launch_split3(const void* src, bool src_bf16, int R, int Cc, int64_t lds, bool transpose, int out_rows,
+                          int out_cols, void* const out[3], cudaStream_t st) {
     if ((int64_t)out_rows * out_cols == 0) return cudaSuccess;
     const dim3 grid((unsigned)cdiv(out_cols, 32), (unsigned)cdiv(out_rows, 32));
-    split3_kernel<<<grid, 256, 0, st>>>(src, R, Cc, lds, transpose ? 1 : 0, out_rows, out_cols,
-                                        (__nv_bfloat16*)out[0], (__nv_bfloat16*)out[1], (__nv_bfloat16*)out[2]);
+    __nv_bfloat16 *h = (__nv_bfloat16*)out[0], *m = (__nv_bfloat16*)out[1], *l = (__nv_bfloat16*)out[2];
+    if (src_bf16)
+        split3_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)src, R, Cc, lds, transpose ? 1 : 0,
+                                                           out_rows, out_cols, h, m, l);
+    else
+        split3_kernel<float><<<grid, 256, 0, st>>>((const float*)src, R, Cc, lds, transpose ? 1 : 0, out_rows,
+                                                   out_cols, h, m, l);
     return cudaGetLastError();
 }
 
 cudaError_t launch_split_gemm_tc(const void* const a[3], const void* const b[3], int M, int N, int Mp, int Np, int Kp,
                                  bool sym, float* C, int ldc, uint32_t* check, cudaStream_t st) {
     if (M <= 0 || N <= 0) return cudaSuccess;
-    if (Mp % kGM || Np % kGN || Kp % kGK || Mp < M || Np < N || Kp <= 0) return cudaErrorInvalidValue;
+    if (Mp % kGM || Np % 128 || Kp % kGK || Mp < M || Np < N || Kp <= 0) return cudaErrorInvalidValue;
+    const int BN = Np % 256 == 0 ? 256 : 128;
     cudaError_t e = cudaMemsetAsync(C, 0, sizeof(float) * (size_t)M * ldc, st);
     if (e != cudaSuccess) return e;
     SplitMaps maps;
     const uint64_t dA[2] = {(uint64_t)Kp, (uint64_t)Mp}, dB[2] = {(uint64_t)Kp, (uint64_t)Np};
-    const uint32_t bA[2] = {(uint32_t)kGK, (uint32_t)kGM}, bB[2] = {(uint32_t)kGK, (uint32_t)kGN};
+    const uint32_t bA[2] = {(uint32_t)kGK, (uint32_t)kGM}, bB[2] = {(uint32_t)kGK, (uint32_t)BN};
     for (int t = 0; t < 3; ++t)
         if (!tc::make_map(&maps.a[t], a[t], 2, dA, bA) || !tc::make_map(&maps.b[t], b[t], 2, dB, bB))
             return cudaErrorInvalidValue;
-    const int tm = Mp / kGM, tn = Np / kGN;
+    const int tm = Mp / kGM, tn = Np / BN;
     int tiles = 0;
     for (int bm = 0; bm < tm; ++bm)
-        for (int bn = 0; bn < tn; ++bn) tiles += (!sym || bn * kGN + kGN > bm * kGM) ? 1 : 0;
+        for (int bn = 0; bn < tn; ++bn) tiles += (!sym || bn * BN + BN > bm * kGM) ? 1 : 0;
     SplitGemmParams p;
     p.M = M;
     p.N = N;
@@ -258,10 +268,15 @@ cudaError_t launch_split_gemm_tc(const void* const a[3], const void* const b[3],
     int n_split = 1;
     while ((int64_t)tiles * n_split * 2 <= sms && total / (n_split * 2) >= 4) n_split *= 2;
     p.n_split = n_split;
-    e = cudaFuncSetAttribute(split_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
-    if (e != cudaSuccess) return e;
-    split_gemm_tc_kernel<<<dim3((unsigned)tn, (unsigned)tm, (unsigned)n_split), kGThreads, kGSmem, st>>>(maps, p);
-    return cudaGetLastError();
+    const dim3 grid((unsigned)tn, (unsigned)tm, (unsigned)n_split);
+    if (BN == 256) {
+        e = cudaFuncSetAttribute(split_gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem(256));
+        if (e == cudaSuccess) split_gemm_tc_kernel<256><<<grid, kGThreads, g_smem(256), st>>>(maps, p);
+    } else {
+        e = cudaFuncSetAttribute(split_gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem(128));
+        if (e == cudaSuccess) split_gemm_tc_kernel<128><<<grid, kGThreads, g_smem(128), st>>>(maps, p);
+    }
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace lowram

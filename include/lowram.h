@@ -319,23 +319,28 @@ LOWRAM_API lowram_status lowram_evict_plan(int32_t B, int32_t T, int32_t n_sink,
  * Parameters are float32 master copies: w1 [H_kv, m, d], b1 [H_kv, m], w2 [H_kv, d, m],
  * b2 [H_kv, d] (decode takes w1, w2 in the activation dtype: round them after the fit).
  * keys, values [B, T, H_kv, d] in dtype (LOWRAM_F32 or LOWRAM_BF16); d is 64 or 128, m a multiple
- * of 32 up to 256.  CUDA cores, float32.
+ * of 32 up to 256.  Float32 accuracy throughout.
  * ------------------------------------------------------------------------------------------- */
 
 /* Loss [H_kv] and gradient of every head's predictor at the given parameters (outputs shaped like the
- * parameters; overwritten). */
+ * parameters; overwritten).  One fused CUDA-core kernel, no workspace. */
 LOWRAM_API lowram_status lowram_predictor_grad(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m, int32_t dtype,
                                                const void* keys, const void* values, const float* w1, const float* b1,
                                                const float* w2, const float* b2, float* loss_out, float* g_w1,
                                                float* g_b1, float* g_w2, float* g_b2, void* stream);
 
-/* Workspace bytes lowram_fit_predictor needs (the gradient and Adam's two moments of every parameter). */
-LOWRAM_API lowram_status lowram_fit_predictor_workspace_size(int32_t H_kv, int32_t d, int32_t m, size_t* bytes);
+/* Workspace bytes lowram_fit_predictor needs for B*T prompt tokens: the gradient and Adam's two moments of every
+ * parameter, and the scratch of the tensor-core products (the keys' bf16 terms in two layouts, about 12*B*T*H_kv*d
+ * bytes, plus per-head activations and their terms, about 40*B*T*max(d, m) bytes). */
+LOWRAM_API lowram_status lowram_fit_predictor_workspace_size(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m,
+                                                             size_t* bytes);
 
 /*
  * lowram_fit_predictor -- `steps` Adam steps (Kingma and Ba, bias-corrected; moments start at zero)
  * from the parameters given, updated in place.  losses_out [steps, H_kv] float32 (the loss before each
- * step) or NULL.  Errors: LOWRAM_ERR_INVALID_ARG (shape, steps < 0, lr <= 0, beta outside [0, 1),
+ * step) or NULL.  The five products of each step's forward and backward pass run on the tensor cores
+ * with float32 operands split exactly into three bf16 terms (six bf16 products, float32 accumulation);
+ * a pipeline timeout sets LOWRAM_CHECK_TIMEOUT in the workspace's check word (lowram_get_error).  Errors: LOWRAM_ERR_INVALID_ARG (shape, steps < 0, lr <= 0, beta outside [0, 1),
  * eps <= 0, NULL pointers), LOWRAM_ERR_UNSUPPORTED (d, m), LOWRAM_ERR_ALIGNMENT, LOWRAM_ERR_WORKSPACE.
  */
 LOWRAM_API lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m, int32_t dtype,
@@ -347,7 +352,8 @@ LOWRAM_API lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv
 /* ---------------------------------------------------------------------------------------------
  * Fitted basis: the group's shared low-rank key basis from the prompt's keys (before compress).
  * ------------------------------------------------------------------------------------------- */
-/* Workspace bytes lowram_fit_basis needs (a multiple of 256; about 4*B*T*D + 4*D*D bytes, D = G*H_kv*d).
+/* Workspace bytes lowram_fit_basis needs (a multiple of 256; about 10*B*T*D + 10*D*D bytes, D = G*H_kv*d: the
+ * float32 keys and their bf16 terms, the Gram matrix and its terms).
  * Uses shape fields B, T, G, H_kv, d, r, act_dtype, keys_post_rope and max_pos. */
 LOWRAM_API lowram_status lowram_fit_basis_workspace_size(const lowram_compress_shape* shape, size_t* bytes);
 

@@ -130,10 +130,13 @@ def test_tail_merge_and_fit_entry_points_check_arguments_on_the_host():
     assert lib.lowram_fit_basis(ctypes.byref(good), None, None, None, None, 8, 0, None, None, None, 0,
                                 None) == WORKSPACE
     # predictor fit: hidden width, head dim, Adam hyper-parameters, workspace
-    assert lib.lowram_fit_predictor_workspace_size(8, 128, 300, ctypes.byref(n)) == UNSUPPORTED
-    assert lib.lowram_fit_predictor_workspace_size(8, 96, 128, ctypes.byref(n)) == UNSUPPORTED
-    assert lib.lowram_fit_predictor_workspace_size(8, 128, 128, ctypes.byref(n)) == 0
-    assert n.value >= 3 * 4 * 8 * (2 * 128 * 128 + 256)
+    assert lib.lowram_fit_predictor_workspace_size(1, 10, 8, 128, 300, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.lowram_fit_predictor_workspace_size(1, 10, 8, 96, 128, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.lowram_fit_predictor_workspace_size(1, 10, 8, 128, 128, ctypes.byref(n)) == 0
+    assert n.value >= 3 * 4 * 8 * (2 * 128 * 128 + 256)      # gradient and the two moments
+    n_big = ctypes.c_size_t(0)
+    assert lib.lowram_fit_predictor_workspace_size(8, 8192, 8, 128, 128, ctypes.byref(n_big)) == 0
+    assert n_big.value >= 12 * 8 * 8192 * 8 * 128              # the keys' bf16 terms in two layouts
     ws = ctypes.create_string_buffer(n.value + 256)
     wsp = ctypes.c_void_p((ctypes.addressof(ws) + 255) & ~255)
     assert lib.lowram_fit_predictor(1, 10, 8, 128, 128, 1, None, None, 5, 0.0, 0.9, 0.999, 1e-8, None, None, None,
@@ -181,7 +184,7 @@ def test_eviction_entry_points_and_batch_limit_check_arguments_on_the_host():
     assert lib.lowram_dense_workspace_size(65535, 100, 32, 8, 128, ctypes.byref(n)) == 0
     # and on the token rows: B*T below 2^31
     assert lib.lowram_attention_mass_workspace_size(2, 1 << 30, 1, 8, 8, 64, 1, ctypes.byref(n)) == UNSUPPORTED
-    assert lib.lowram_fit_predictor_workspace_size(8, 128, 128, ctypes.byref(n)) == 0
+    assert lib.lowram_fit_predictor_workspace_size(2, 1 << 30, 8, 128, 128, ctypes.byref(n)) == UNSUPPORTED
     assert lib.lowram_predictor_grad(2, 1 << 30, 8, 128, 128, 1, None, None, None, None, None, None, None, None, None,
                                      None, None, None) == UNSUPPORTED
 
