@@ -15,9 +15,9 @@
 // [tokens, D] for the Gram matrix, the iterate Q [D, r]).  One CTA of 128 threads per 128 x BN output tile (BN = 256,
 // or 128 when B's padded rows are not a multiple of 256): thread 0 TMA-loads a 16 KB A chunk and a BN x 128 B
 // B chunk per stage into a 4-stage 128-byte-swizzled ring, thread 32 issues four M=128, N=BN, K=16 MMAs per chunk
-// into a BN-column TMEM accumulator, and the four warps then read their 32 TMEM lanes and add the tile into C
-// (zeroed first) with float32 reductions, so a tile's
-// reduction may be split over several CTAs (gridDim.z) when the tiles alone do not fill the GPU.  For a symmetric
+// into a BN-column TMEM accumulator, and the four warps then read their 32 TMEM lanes and store the tile into C; when
+// the tiles alone do not fill the GPU a tile's reduction is split over several CTAs (gridDim.z), which add their
+// parts into C (zeroed first) with float32 reductions.  For a symmetric
 // product (the Gram matrix, A = B) tiles wholly below the diagonal are skipped and every other tile adds its
 // entries on or above the diagonal and their mirrors.  Every wait is bounded: on a timeout the CTA sets
 // LOWRAM_CHECK_TIMEOUT, waits for the copies and MMAs it issued, frees TMEM and returns.
@@ -51,7 +51,8 @@ struct SplitGemmParams {
     int KC;             // reduction chunks of 64 per product
     int ldc;
     int sym;
-    int n_split;        // reduction ranges per tile (gridDim.z)
+    int n_split;        // reduction ranges per tile (gridDim.z): 1 stores the tile, more add it with reductions
+    int vec4;           // ldc and C allow float4 accesses
     float* C;
     uint32_t* check;
 };
@@ -156,21 +157,41 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
     } else {
         fence_after();
-        // thread = output row (TMEM lane warp*32 + lane), 64 columns per pass
+        // thread = output row (TMEM lane warp*32 + lane), 64 columns per pass; a tile that owns its outputs
+        // (n_split == 1) stores them, else it adds them (float4 where the row allows)
         const int i = row0 + warp * 32 + lane;
         const uint32_t tw = tmem + ((uint32_t)(warp * 32) << 16);
         float* Ci = p.C + (int64_t)i * p.ldc;
+        const bool own = p.n_split == 1;
         for (int cb = 0; cb < BN && col0 + cb < p.N; cb += 64) {
             float x[32], y[32];
             tmem_ld_2x32(tw + (uint32_t)cb, tw + (uint32_t)cb + 32u, x, y);
             if (i < p.M) {
 #pragma unroll
-                for (int u = 0; u < 64; ++u) {
+                for (int u = 0; u < 64; u += 4) {
                     const int j = col0 + cb + u;
-                    const float v = u < 32 ? x[u] : y[u - 32];
-                    if (j < p.N && (!p.sym || j >= i)) {
-                        atomicAdd(Ci + j, v);
-                        if (p.sym && j > i) atomicAdd(p.C + (int64_t)j * p.ldc + i, v);
+                    float v[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[q] = u + q < 32 ? x[u + q] : y[u + q - 32];
+                    if (!p.sym && p.vec4 && j + 3 < p.N) {
+                        const float4 v4 = make_float4(v[0], v[1], v[2], v[3]);
+                        if (own) *reinterpret_cast<float4*>(Ci + j) = v4;
+                        else atomicAdd(reinterpret_cast<float4*>(Ci + j), v4);
+                        continue;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int jq = j + q;
+                        if (jq < p.N && (!p.sym || jq >= i)) {
+                            float* mirror = p.C + (int64_t)jq * p.ldc + i;
+                            if (own) {
+                                Ci[jq] = v[q];
+                                if (p.sym && jq > i) *mirror = v[q];
+                            } else {
+                                atomicAdd(Ci + jq, v[q]);
+                                if (p.sym && jq > i) atomicAdd(mirror, v[q]);
+                            }
+                        }
                     }
                 }
             }
@@ -243,8 +264,7 @@ cudaError_t launch_split_gemm_tc(const void* const a[3], const void* const b[3],
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (Mp % kGM || Np % 128 || Kp % kGK || Mp < M || Np < N || Kp <= 0) return cudaErrorInvalidValue;
     const int BN = Np % 256 == 0 ? 256 : 128;
-    cudaError_t e = cudaMemsetAsync(C, 0, sizeof(float) * (size_t)M * ldc, st);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     SplitMaps maps;
     const uint64_t dA[2] = {(uint64_t)Kp, (uint64_t)Mp}, dB[2] = {(uint64_t)Kp, (uint64_t)Np};
     const uint32_t bA[2] = {(uint32_t)kGK, (uint32_t)kGM}, bB[2] = {(uint32_t)kGK, (uint32_t)BN};
@@ -268,6 +288,8 @@ cudaError_t launch_split_gemm_tc(const void* const a[3], const void* const b[3],
     int n_split = 1;
     while ((int64_t)tiles * n_split * 2 <= sms && total / (n_split * 2) >= 4) n_split *= 2;
     p.n_split = n_split;
+    p.vec4 = (ldc % 4 == 0 && ((uintptr_t)C & 15u) == 0) ? 1 : 0;
+    if (n_split > 1 && (e = cudaMemsetAsync(C, 0, sizeof(float) * (size_t)M * ldc, st)) != cudaSuccess) return e;
     const dim3 grid((unsigned)tn, (unsigned)tm, (unsigned)n_split);
     if (BN == 256) {
         e = cudaFuncSetAttribute(split_gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem(256));

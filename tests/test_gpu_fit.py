@@ -53,8 +53,9 @@ def check_fit(proj, bases, keys, r, G, H_kv, d, dtype, **kw):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("B,T,G,H_kv,d,r", [(2, 300, 2, 2, 64, 64), (1, 777, 4, 1, 128, 96), (3, 100, 1, 8, 64, 256),
-                                             (1, 1500, 2, 4, 128, 640)])
+                                             (1, 1500, 2, 4, 128, 640), (1, 600, 3, 6, 128, 64)])
 def test_fit_basis_matches_oracle(dtype, B, T, G, H_kv, d, r):
+    # D = 2304 (the last case): 90 Gram tiles, enough that each owns its outputs (stored, not added), as at full size
     import decode_attention_19_b300 as L
     keys = low_rank_keys(B, T, G, H_kv, d, r, 0.05, 1, dtype)
     proj, bases, ws = L.lowram_fit_basis(keys.cuda(), r, iters=8, seed=3)
