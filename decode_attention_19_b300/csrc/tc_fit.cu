@@ -213,33 +213,59 @@ __device__ __forceinline__ void split3(float x, __nv_bfloat16& h, __nv_bfloat16&
 }
 
 // out_t[orow][ocol] for t = h, m, l (each [out_rows, out_cols] bf16): the terms of src[orow][ocol], or of
-// src[ocol][orow] when transposing; zero outside src [R, Cc] (row stride lds).  32 x 32 tiles through shared
-// memory, so both the reads and the writes are coalesced.
+// src[ocol][orow] when transposing; zero outside src [R, Cc] (row stride lds).  A CTA of 32 x 8 threads takes a
+// 32 x 64 output tile through shared memory (held as t[column][row], so both layouts read the source along its
+// rows), and each thread writes two adjacent columns as bf16 pairs.
 template <typename TS>
 __global__ void __launch_bounds__(256) split3_kernel(const TS* __restrict__ src, int R, int Cc, int64_t lds,
                                                      int transpose, int out_rows, int out_cols,
                                                      __nv_bfloat16* __restrict__ oh, __nv_bfloat16* __restrict__ om,
                                                      __nv_bfloat16* __restrict__ ol) {
-    __shared__ float tile[32][33];
+    __shared__ float t[64][33];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
-    const int64_t ocol0 = (int64_t)blockIdx.x * 32, orow0 = (int64_t)blockIdx.y * 32;
-    // source tile: rows sr0.., columns sc0.. (read along the source's rows)
-    const int64_t sr0 = transpose ? ocol0 : orow0, sc0 = transpose ? orow0 : ocol0;
-    for (int k = ty; k < 32; k += 8) {
-        const int64_t sr = sr0 + k, sc = sc0 + tx;
-        tile[k][tx] = (sr < R && sc < Cc) ? ld(src, sr * lds + sc) : 0.0f;
+    const int64_t ocol0 = (int64_t)blockIdx.x * 64, orow0 = (int64_t)blockIdx.y * 32;
+    if (transpose) {
+        // source rows ocol0 .. +63, columns orow0 .. +31
+        for (int k = ty; k < 64; k += 8) {
+            const int64_t sr = ocol0 + k, sc = orow0 + tx;
+            t[k][tx] = (sr < R && sc < Cc) ? ld(src, sr * lds + sc) : 0.0f;
+        }
+    } else {
+        // source rows orow0 .. +31, columns ocol0 .. +63
+        for (int k = ty; k < 32; k += 8) {
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                const int c = tx + 32 * hlf;
+                const int64_t sr = orow0 + k, sc = ocol0 + c;
+                t[c][k] = (sr < R && sc < Cc) ? ld(src, sr * lds + sc) : 0.0f;
+            }
+        }
     }
     __syncthreads();
+    const int c0 = 2 * tx;
+    const int64_t ocol = ocol0 + c0;
     for (int k = ty; k < 32; k += 8) {
-        const int64_t orow = orow0 + k, ocol = ocol0 + tx;
+        const int64_t orow = orow0 + k;
         if (orow >= out_rows || ocol >= out_cols) continue;
-        const float x = transpose ? tile[tx][k] : tile[k][tx];
-        __nv_bfloat16 h, m, l;
-        split3(x, h, m, l);
+        __nv_bfloat16 h0, m0, l0, h1, m1, l1;
+        split3(t[c0][k], h0, m0, l0);
         const int64_t o = orow * out_cols + ocol;
-        oh[o] = h;
-        om[o] = m;
-        ol[o] = l;
+        if (ocol + 1 < out_cols && (o & 1) == 0) {
+            split3(t[c0 + 1][k], h1, m1, l1);
+            *reinterpret_cast<__nv_bfloat162*>(oh + o) = __halves2bfloat162(h0, h1);
+            *reinterpret_cast<__nv_bfloat162*>(om + o) = __halves2bfloat162(m0, m1);
+            *reinterpret_cast<__nv_bfloat162*>(ol + o) = __halves2bfloat162(l0, l1);
+        } else {
+            oh[o] = h0;
+            om[o] = m0;
+            ol[o] = l0;
+            if (ocol + 1 < out_cols) {
+                split3(t[c0 + 1][k], h1, m1, l1);
+                oh[o + 1] = h1;
+                om[o + 1] = m1;
+                ol[o + 1] = l1;
+            }
+        }
     }
 }
 
@@ -248,7 +274,7 @@ __global__ void __launch_bounds__(256) split3_kernel(const TS* __restrict__ src,
 cudaError_t launch_split3(const void* src, bool src_bf16, int R, int Cc, int64_t lds, bool transpose, int out_rows,
                           int out_cols, void* const out[3], cudaStream_t st) {
     if ((int64_t)out_rows * out_cols == 0) return cudaSuccess;
-    const dim3 grid((unsigned)cdiv(out_cols, 32), (unsigned)cdiv(out_rows, 32));
+    const dim3 grid((unsigned)cdiv(out_cols, 64), (unsigned)cdiv(out_rows, 32));
     __nv_bfloat16 *h = (__nv_bfloat16*)out[0], *m = (__nv_bfloat16*)out[1], *l = (__nv_bfloat16*)out[2];
     if (src_bf16)
         split3_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)src, R, Cc, lds, transpose ? 1 : 0,
