@@ -734,8 +734,9 @@ def fit_predictor_bench(w, dev, args, pk):
         "loss_first_last": [float(ls[0].mean()), float(ls[-1].mean())],
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "traffic": None,
-                     "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock",
-                     "work": "10 * B*T * d * m * H_kv per step"}}))
+                     "peak_kind": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOP x max SM clock (a reference scale: the five "
+                                  "products run on the tensor cores as six bf16 products each)",
+                     "work": "float32-equivalent: 10 * B*T * d * m * H_kv per step"}}))
 
 
 def evict_bench(w, dev, args, pk):
