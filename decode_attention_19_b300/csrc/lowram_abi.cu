@@ -481,6 +481,9 @@ lowram_status lowram_fit_predictor_workspace_size(int32_t B, int32_t T, int32_t 
                                                   size_t* bytes) {
     lowram_status st = check_predictor_shape(B, T, H_kv, d, m, LOWRAM_F32);
     if (st != LOWRAM_OK) return st;
+    if ((int64_t)B * T > predictor_tc_max_tokens())
+        return fail(LOWRAM_ERR_UNSUPPORTED, "B*T=%lld prompt tokens (at most %lld for the fit)", (long long)B * T,
+                    (long long)predictor_tc_max_tokens());
     if (!bytes) return fail(LOWRAM_ERR_INVALID_ARG, "bytes is NULL");
     // gradient, first and second moments of every parameter, a loss row, and the tensor-core products' scratch
     *bytes = kHeader + 3 * align256(sizeof(float) * predictor_params(H_kv, d, m)) + align256(sizeof(float) * H_kv) +
@@ -496,7 +499,7 @@ lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d
     lowram_status st = check_predictor_shape(B, T, H_kv, d, m, dtype);
     if (st != LOWRAM_OK) return st;
     size_t need = 0;
-    lowram_fit_predictor_workspace_size(B, T, H_kv, d, m, &need);
+    if ((st = lowram_fit_predictor_workspace_size(B, T, H_kv, d, m, &need)) != LOWRAM_OK) return st;
     if (!workspace || workspace_bytes < need || !aligned16(workspace))
         return fail(LOWRAM_ERR_WORKSPACE, "workspace %zu bytes, %zu needed", workspace ? workspace_bytes : 0, need);
     if (steps < 0) return fail(LOWRAM_ERR_INVALID_ARG, "steps=%d", steps);

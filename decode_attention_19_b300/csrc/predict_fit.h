@@ -22,6 +22,7 @@ cudaError_t launch_predictor_grad(const PredictorFitArgs& a, cudaStream_t st);
 // predictor_tc_scratch_bytes; launch_predictor_prep_tc writes the keys' terms into it once per fit (the keys do not
 // change between steps).  A pipeline timeout sets LOWRAM_CHECK_TIMEOUT in *check.
 size_t predictor_tc_scratch_bytes(int64_t N, int H_kv, int d, int m);
+int64_t predictor_tc_max_tokens();   // B*T above it: LOWRAM_ERR_UNSUPPORTED
 cudaError_t launch_predictor_prep_tc(const PredictorFitArgs& a, void* scratch, cudaStream_t st);
 cudaError_t launch_predictor_grad_tc(const PredictorFitArgs& a, void* scratch, uint32_t* check, cudaStream_t st);
 cudaError_t launch_adam(float* p, const float* g, float* mom, float* vel, int64_t n, float lr, float beta1, float beta2,

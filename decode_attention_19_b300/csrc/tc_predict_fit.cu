@@ -154,6 +154,9 @@ __global__ void pf_scale_kernel(float* __restrict__ g, int64_t n, float c) {
 
 size_t predictor_tc_scratch_bytes(int64_t N, int H_kv, int d, int m) { return pf_tc_layout(N, H_kv, d, m).total; }
 
+// The token-major split passes put 32 output rows (tokens) per grid row, and a grid has at most 65535 rows.
+int64_t predictor_tc_max_tokens() { return 65535LL * 32; }
+
 cudaError_t launch_predictor_prep_tc(const PredictorFitArgs& a, void* scratch, cudaStream_t st) {
     const int64_t N = (int64_t)a.B * a.T;
     if (N == 0) return cudaSuccess;

@@ -339,9 +339,12 @@ LOWRAM_API lowram_status lowram_fit_predictor_workspace_size(int32_t B, int32_t 
  * lowram_fit_predictor -- `steps` Adam steps (Kingma and Ba, bias-corrected; moments start at zero)
  * from the parameters given, updated in place.  losses_out [steps, H_kv] float32 (the loss before each
  * step) or NULL.  The five products of each step's forward and backward pass run on the tensor cores
- * with float32 operands split exactly into three bf16 terms (six bf16 products, float32 accumulation);
- * a pipeline timeout sets LOWRAM_CHECK_TIMEOUT in the workspace's check word (lowram_get_error).  Errors: LOWRAM_ERR_INVALID_ARG (shape, steps < 0, lr <= 0, beta outside [0, 1),
- * eps <= 0, NULL pointers), LOWRAM_ERR_UNSUPPORTED (d, m), LOWRAM_ERR_ALIGNMENT, LOWRAM_ERR_WORKSPACE.
+ * with the float32 operands split exactly into three bf16 terms (six bf16 products, float32
+ * accumulation); a pipeline timeout sets LOWRAM_CHECK_TIMEOUT in the workspace's check word
+ * (lowram_get_error).  B*T is at most 2,097,120 prompt tokens, here and in
+ * lowram_fit_predictor_workspace_size.  Errors: LOWRAM_ERR_INVALID_ARG (shape, steps < 0, lr <= 0,
+ * beta outside [0, 1), eps <= 0, NULL pointers), LOWRAM_ERR_UNSUPPORTED (d, m, B*T),
+ * LOWRAM_ERR_ALIGNMENT, LOWRAM_ERR_WORKSPACE.
  */
 LOWRAM_API lowram_status lowram_fit_predictor(int32_t B, int32_t T, int32_t H_kv, int32_t d, int32_t m, int32_t dtype,
                                               const void* keys, const void* values, int32_t steps, float lr,

@@ -185,6 +185,9 @@ def test_eviction_entry_points_and_batch_limit_check_arguments_on_the_host():
     # and on the token rows: B*T below 2^31
     assert lib.lowram_attention_mass_workspace_size(2, 1 << 30, 1, 8, 8, 64, 1, ctypes.byref(n)) == UNSUPPORTED
     assert lib.lowram_fit_predictor_workspace_size(2, 1 << 30, 8, 128, 128, ctypes.byref(n)) == UNSUPPORTED
+    # the predictor fit's own limit: 65535 * 32 prompt tokens (the split passes' grid rows)
+    assert lib.lowram_fit_predictor_workspace_size(1, 65535 * 32, 8, 128, 128, ctypes.byref(n)) == 0
+    assert lib.lowram_fit_predictor_workspace_size(1, 65535 * 32 + 1, 8, 128, 128, ctypes.byref(n)) == UNSUPPORTED
     assert lib.lowram_predictor_grad(2, 1 << 30, 8, 128, 128, 1, None, None, None, None, None, None, None, None, None,
                                      None, None, None) == UNSUPPORTED
 
